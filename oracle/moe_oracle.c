@@ -1,0 +1,432 @@
+/*
+ * CPU oracle for the single-GPU MoE layer forward: test infrastructure only.
+ *
+ * Plain, slow, obviously correct C, fp64 unless a step fixes another precision. It shares
+ * no code with the CUDA library (no header, helper or table); only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg call it. Each function names the passage of
+ * the method it follows. The pages ("Scalable Training of Mixture-of-Experts Models with
+ * Megatron Core" summary, the Megatron-Core distributed-training skill card, the Piper
+ * summary and the Hybrid-EP article) state WHAT the layer does but print no formula; where
+ * they are silent the plainest reading is taken and named at the function.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared (no fast-math: the
+ * routing scores below must be computed with exactly the IEEE operations written).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Deterministic fp32 exp: Cody-Waite argument reduction (W. J. Cody and W. Waite,       */
+/* "Software Manual for the Elementary Functions", 1980) with a two-constant split of    */
+/* ln 2, a degree-7 Taylor polynomial of e^r on |r| <= ln2/2 evaluated by Horner with     */
+/* fused multiply-adds, and an exact power-of-two scaling in two steps.                   */
+/* Every operation is a correctly rounded IEEE fp32 operation, so any machine that        */
+/* performs the same sequence gets the same bits. Used only where an fp32 value decides  */
+/* an integer (the sigmoid group scores of group-limited routing).                        */
+/* ------------------------------------------------------------------------------------ */
+static float pow2i(int n) { /* 2^n for n in [-126, 127], exact */
+  union { uint32_t u; float f; } v;
+  v.u = (uint32_t)(n + 127) << 23;
+  return v.f;
+}
+
+float oc_det_expf(float a) {
+  if (a != a) return a;
+  if (a > 88.72283935546875f) return INFINITY;
+  if (a < -103.972084045410156f) return 0.0f;
+  const float log2e = 1.44269502162933349609375f;      /* fp32(1/ln 2) */
+  const float ln2_hi = 0.693145751953125f;              /* 0x3F317200: 16 significant bits */
+  const float ln2_lo = 1.428606765330187045e-06f;       /* 0x35BFBE8E: fp32(ln2 - ln2_hi) */
+  float t = a * log2e;
+  float n = rintf(t);
+  float r = fmaf(-n, ln2_hi, a);
+  r = fmaf(-n, ln2_lo, r);
+  /* e^r = sum r^i / i!, i = 0..7 */
+  float p = 1.98412698412698412698e-04f;                /* 1/7! */
+  p = fmaf(p, r, 1.38888888888888888889e-03f);          /* 1/6! */
+  p = fmaf(p, r, 8.33333333333333333333e-03f);          /* 1/5! */
+  p = fmaf(p, r, 4.16666666666666666667e-02f);          /* 1/4! */
+  p = fmaf(p, r, 1.66666666666666666667e-01f);          /* 1/3! */
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int ni = (int)n;
+  int n1 = ni >> 1; /* floor(n/2); n1, n - n1 in [-75, 64] */
+  int n2 = ni - n1;
+  return (p * pow2i(n1)) * pow2i(n2);
+}
+
+/* s = 1 / (1 + e^-l), fp32, with the deterministic exp above. */
+float oc_det_sigmoidf(float l) { return 1.0f / (1.0f + oc_det_expf(-l)); }
+
+void oc_det_expf_array(const float* a, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oc_det_expf(a[i]);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S0: router logits. l[t,e] = sum_h x[t,h] * Wr[e,h] (+ b[e]) accumulated in fp64 from   */
+/* the stored values, rounded once to fp32. The router "scores each token against the    */
+/* experts" (P1 "O essencial"; BASELINE router weights ~N(0,0.02)). b is the optional     */
+/* per-expert additive bias of the imbalanced workload.                                   */
+/* ------------------------------------------------------------------------------------ */
+void oc_router_logits(const float* x, const float* wr, const float* bias, int T, int H, int E,
+                      float* logits) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += (double)x[(int64_t)t * H + h] * (double)wr[(int64_t)e * H + h];
+      if (bias) s += (double)bias[e];
+      logits[(int64_t)t * E + e] = (float)s;
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S1: top-k routing with optional group-limited selection.                               */
+/* Key = fp32 logit, descending; equal keys go to the lower expert index (softmax and     */
+/* sigmoid are strictly increasing, so this is the ranking by score). Group-limited       */
+/* selection (DeepSeek-V3 shape: 256 experts, top-8; Hybrid-EP article results) keeps    */
+/* the topk_groups groups of contiguous experts with the largest group score, ties to the */
+/* lower group; group score = sum of the two largest fp32 sigmoid scores in the group     */
+/* (group_score 0) or the largest (group_score 1), scores from oc_det_sigmoidf.           */
+/* Weights (fp64): softmax over all experts, or over the selected ones when renorm;       */
+/* sigmoid s_j, divided by the selected sum when renorm; then times routed_scale.         */
+/* Returns 0, or -1 if a logit is not finite.                                             */
+/* ------------------------------------------------------------------------------------ */
+typedef struct { float key; int idx; } oc_kv;
+
+static int kv_desc(const void* a, const void* b) {
+  const oc_kv* p = (const oc_kv*)a;
+  const oc_kv* q = (const oc_kv*)b;
+  if (p->key > q->key) return -1;
+  if (p->key < q->key) return 1;
+  return (p->idx < q->idx) ? -1 : (p->idx > q->idx);
+}
+
+static int route_one(const float* l, int E, int k, int score_fn, int renorm, int n_groups,
+                     int topk_groups, int group_score, double routed_scale, int32_t* idx_out,
+                     double* w_out, float* group_scores_out) {
+  for (int e = 0; e < E; ++e)
+    if (!isfinite(l[e])) return -1;
+  oc_kv* kv = (oc_kv*)malloc(sizeof(oc_kv) * (size_t)E);
+  char* allowed = (char*)malloc((size_t)E);
+  for (int e = 0; e < E; ++e) allowed[e] = 1;
+  if (n_groups > 1 && topk_groups < n_groups) {
+    int gs = E / n_groups;
+    oc_kv* gk = (oc_kv*)malloc(sizeof(oc_kv) * (size_t)n_groups);
+    float* s = (float*)malloc(sizeof(float) * (size_t)gs);
+    for (int g = 0; g < n_groups; ++g) {
+      for (int i = 0; i < gs; ++i) s[i] = oc_det_sigmoidf(l[g * gs + i]);
+      float m1 = -INFINITY, m2 = -INFINITY; /* two largest scores */
+      for (int i = 0; i < gs; ++i) {
+        if (s[i] > m1) { m2 = m1; m1 = s[i]; }
+        else if (s[i] > m2) m2 = s[i];
+      }
+      float sc = (group_score == 0 && gs >= 2) ? (m1 + m2) : m1;
+      gk[g].key = sc;
+      gk[g].idx = g;
+      if (group_scores_out) group_scores_out[g] = sc;
+    }
+    qsort(gk, (size_t)n_groups, sizeof(oc_kv), kv_desc);
+    for (int e = 0; e < E; ++e) allowed[e] = 0;
+    for (int r = 0; r < topk_groups; ++r)
+      for (int i = 0; i < gs; ++i) allowed[gk[r].idx * gs + i] = 1;
+    free(s);
+    free(gk);
+  }
+  int n = 0;
+  for (int e = 0; e < E; ++e)
+    if (allowed[e]) { kv[n].key = l[e]; kv[n].idx = e; ++n; }
+  qsort(kv, (size_t)n, sizeof(oc_kv), kv_desc);
+  for (int j = 0; j < k; ++j) idx_out[j] = kv[j].idx;
+
+  if (score_fn == 0) {
+    double m = -INFINITY;
+    for (int e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+    double denom = 0.0;
+    if (renorm) for (int j = 0; j < k; ++j) denom += exp((double)l[idx_out[j]] - m);
+    else for (int e = 0; e < E; ++e) denom += exp((double)l[e] - m);
+    for (int j = 0; j < k; ++j) w_out[j] = routed_scale * exp((double)l[idx_out[j]] - m) / denom;
+  } else {
+    double sum = 0.0, sj[1024];
+    for (int j = 0; j < k; ++j) { sj[j] = 1.0 / (1.0 + exp(-(double)l[idx_out[j]])); sum += sj[j]; }
+    for (int j = 0; j < k; ++j) w_out[j] = routed_scale * (renorm ? sj[j] / sum : sj[j]);
+  }
+  free(allowed);
+  free(kv);
+  return 0;
+}
+
+int oc_route(const float* logits, int T, int E, int k, int score_fn, int renorm, int n_groups,
+             int topk_groups, int group_score, double routed_scale, int32_t* topk_idx,
+             double* topk_w) {
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int t = 0; t < T; ++t)
+    if (route_one(logits + (int64_t)t * E, E, k, score_fn, renorm, n_groups, topk_groups,
+                  group_score, routed_scale, topk_idx + (int64_t)t * k, topk_w + (int64_t)t * k,
+                  NULL))
+      bad = 1;
+  return bad ? -1 : 0;
+}
+
+/* Group scores of one token (for tests of the group step). */
+int oc_group_scores(const float* l, int E, int n_groups, int group_score, float* out) {
+  int gs = E / n_groups;
+  float* s = (float*)malloc(sizeof(float) * (size_t)gs);
+  for (int g = 0; g < n_groups; ++g) {
+    for (int i = 0; i < gs; ++i) s[i] = oc_det_sigmoidf(l[g * gs + i]);
+    float m1 = -INFINITY, m2 = -INFINITY;
+    for (int i = 0; i < gs; ++i) {
+      if (s[i] > m1) { m2 = m1; m1 = s[i]; }
+      else if (s[i] > m2) m2 = s[i];
+    }
+    out[g] = (group_score == 0 && gs >= 2) ? (m1 + m2) : m1;
+  }
+  free(s);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S2: per-expert counts, offsets and the permutation. counts[e] = #{(t,j): idx=e};        */
+/* offsets = exclusive prefix sum (offsets[E] = T*k); within expert e the rows hold the    */
+/* tokens that chose e in ascending token id ("the routing map" of the Hybrid-EP article;  */
+/* the stable order is the reading taken). row_token[r] = t, tok_row[t*k+j] = r.           */
+/* Returns 0, or -1 if an expert id is outside [0, E).                                    */
+/* ------------------------------------------------------------------------------------ */
+int oc_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+               int32_t* row_token, int32_t* tok_row) {
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t i = 0; i < (int64_t)T * k; ++i) {
+    int e = topk_idx[i];
+    if (e < 0 || e >= E) return -1;
+    counts[e]++;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* fill = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      int e = topk_idx[(int64_t)t * k + j];
+      int r = offsets[e] + fill[e]++;
+      row_token[r] = t;
+      tok_row[(int64_t)t * k + j] = r;
+    }
+  free(fill);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S3: dispatch, xd[r] = x[row_token[r]] (the dispatch operator "directs the tokens to    */
+/* the corresponding experts", Hybrid-EP article). Bit copy.                              */
+/* ------------------------------------------------------------------------------------ */
+void oc_dispatch(const float* x, int H, const int32_t* row_token, int64_t nrows, float* xd) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < nrows; ++r)
+    memcpy(xd + r * H, x + (int64_t)row_token[r] * H, sizeof(float) * (size_t)H);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* FP8 e4m3 (OCP 8-bit floating point specification, E4M3 "fn" variant): 1 sign bit,     */
+/* 4 exponent bits (bias 7), 3 mantissa bits, no infinities, max finite 448, one NaN      */
+/* pattern per sign (S.1111.111). Encoding rounds to nearest, ties to even, and          */
+/* saturates finite values beyond 448 to +-448 ("satfinite").                             */
+/* ------------------------------------------------------------------------------------ */
+double oc_e4m3_decode(uint8_t c) {
+  int s = c >> 7, ex = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (ex == 15 && m == 7) return NAN;
+  if (ex == 0) v = ldexp((double)m, -9);           /* subnormal: m * 2^-6 / 8 */
+  else v = ldexp(8.0 + m, ex - 7 - 3);              /* (1 + m/8) * 2^(ex-7) */
+  return s ? -v : v;
+}
+
+uint8_t oc_e4m3_encode(float f) {
+  if (f != f) return 0x7F;
+  int s = signbit(f) ? 1 : 0;
+  double a = fabs((double)f);
+  uint8_t code;
+  if (a >= 448.0) code = 0x7E;                       /* satfinite */
+  else if (a < ldexp(1.0, -6)) {                     /* subnormal range: step 2^-9 */
+    double m = rint(a * 512.0);                      /* exact scaling, RNE */
+    if (m >= 8.0) code = (uint8_t)(1 << 3);          /* rounds up to min normal 2^-6 */
+    else code = (uint8_t)m;
+  } else {
+    int ex;
+    frexp(a, &ex);                                   /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                                  /* a in [2^e, 2^(e+1)) */
+    double m = rint(ldexp(a, 3 - e));                /* in [8, 16], RNE */
+    if (m >= 16.0) { m = 8.0; e += 1; }
+    if (e > 8 || (e == 8 && m > 14.0)) code = 0x7E; /* above 448: saturate */
+    else code = (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+  }
+  return (uint8_t)(code | (s << 7));
+}
+
+void oc_e4m3_encode_array(const float* f, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oc_e4m3_encode(f[i]);
+}
+
+/* Block quantisation with fp32 scales (the FP8-dispatch variant: tokens in 1x128 blocks,  */
+/* weights in 128x128 blocks; the pages name FP8 dispatch and FP8/FP4 training, BASELINE   */
+/* fixes the block shapes). Per block: amax = max |v| (exact); if amax == 0 the scale is 1 */
+/* and every code is 0; else scale = amax / 448 and q = e4m3(v * (448 / amax)), each       */
+/* division and the product one correctly rounded fp32 operation. The value the block      */
+/* stands for is decode(q) * scale. scale is [rows/br][cols/bc] row-major.                 */
+void oc_quant_blocks(const float* v, int64_t rows, int64_t cols, int br, int bc, uint8_t* q,
+                     float* scale) {
+  int64_t nbr = (rows + br - 1) / br, nbc = (cols + bc - 1) / bc;
+#pragma omp parallel for schedule(static)
+  for (int64_t bi = 0; bi < nbr * nbc; ++bi) {
+    int64_t r0 = (bi / nbc) * br, c0 = (bi % nbc) * bc;
+    int64_t r1 = r0 + br < rows ? r0 + br : rows, c1 = c0 + bc < cols ? c0 + bc : cols;
+    float amax = 0.0f;
+    for (int64_t r = r0; r < r1; ++r)
+      for (int64_t c = c0; c < c1; ++c) {
+        float a = fabsf(v[r * cols + c]);
+        if (a > amax) amax = a;
+      }
+    if (amax == 0.0f) {
+      scale[bi] = 1.0f;
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t c = c0; c < c1; ++c) q[r * cols + c] = 0;
+    } else {
+      volatile float sc = amax / 448.0f; /* volatile: keep each fp32 rounding */
+      volatile float rs = 448.0f / amax;
+      scale[bi] = sc;
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t c = c0; c < c1; ++c) {
+          volatile float p = v[r * cols + c] * rs;
+          q[r * cols + c] = oc_e4m3_encode(p);
+        }
+    }
+  }
+}
+
+/* decode(q) * scale in fp64 (the exact value of a quantised block). */
+void oc_dequant_blocks(const uint8_t* q, const float* scale, int64_t rows, int64_t cols, int br,
+                       int bc, double* out) {
+  int64_t nbc = (cols + bc - 1) / bc;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c)
+      out[r * cols + c] = oc_e4m3_decode(q[r * cols + c]) * (double)scale[(r / br) * nbc + c / bc];
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S4 + S5: one expert's SwiGLU MLP on a set of rows, fp64 ("the experts' GEMMs" of the    */
+/* grouped GEMM; SwiGLU from the workload definition):                                    */
+/*   g = a . Wg^T,  u = a . Wu^T,  h = g / (1 + e^-g) * u,  y = h . Wd^T.                 */
+/* a is [n, H], Wg/Wu [F, H], Wd [H, F] (all fp64 values). If quant_h, h is rounded to     */
+/* fp32 and requantised in 1x128 blocks as the FP8-dispatch variant does before the down   */
+/* projection, and y uses the dequantised h.                                              */
+/* ------------------------------------------------------------------------------------ */
+void oc_expert_mlp(const double* a, int64_t n, int H, int F, const double* wg, const double* wu,
+                   const double* wd, int quant_h, double* y) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)F);
+    const double* ar = a + r * H;
+    for (int f = 0; f < F; ++f) {
+      double g = 0.0, u = 0.0;
+      const double* wgf = wg + (int64_t)f * H;
+      const double* wuf = wu + (int64_t)f * H;
+      for (int i = 0; i < H; ++i) { g += ar[i] * wgf[i]; u += ar[i] * wuf[i]; }
+      h[f] = g / (1.0 + exp(-g)) * u;
+    }
+    if (quant_h) {
+      float* h32 = (float*)malloc(sizeof(float) * (size_t)F);
+      uint8_t* q = (uint8_t*)malloc((size_t)F);
+      float* sc = (float*)malloc(sizeof(float) * (size_t)((F + 127) / 128));
+      for (int f = 0; f < F; ++f) h32[f] = (float)h[f];
+      oc_quant_blocks(h32, 1, F, 1, 128, q, sc);
+      for (int f = 0; f < F; ++f) h[f] = oc_e4m3_decode(q[f]) * (double)sc[f / 128];
+      free(h32); free(q); free(sc);
+    }
+    for (int o = 0; o < H; ++o) {
+      double s = 0.0;
+      const double* wdo = wd + (int64_t)o * F;
+      for (int f = 0; f < F; ++f) s += h[f] * wdo[f];
+      y[r * H + o] = s;
+    }
+    free(h);
+  }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* S7: combine. y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ ys[t], the shared expert's row) */
+/* in fp64, w already holding the routed scale: the combine operator "sends the tokens     */
+/* back" with high-precision accumulation (Hybrid-EP article); dropless, every token gets  */
+/* all k rows (Megatron-Core summary, dropless MoE). ys may be NULL.                       */
+/* ------------------------------------------------------------------------------------ */
+void oc_combine(const double* yd, const int32_t* tok_row, const double* w, const double* ys,
+                int T, int k, int H, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int o = 0; o < H; ++o) {
+      double s = 0.0;
+      for (int j = 0; j < k; ++j)
+        s += w[(int64_t)t * k + j] * yd[(int64_t)tok_row[(int64_t)t * k + j] * H + o];
+      if (ys) s += ys[(int64_t)t * H + o];
+      y[(int64_t)t * H + o] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Second, independent oracle: the dense per-token loop. For each token, re-derive the    */
+/* top-k from its fp32 logits and run the chosen experts directly, with no counts, no     */
+/* permutation and no dispatch buffer. Weights in fp64 (Wg/Wu [E,F,H], Wd [E,H,F]).        */
+/* Shared expert optional (wsg/wsu [Fs,H], wsd [H,Fs], may be NULL).                       */
+/* ------------------------------------------------------------------------------------ */
+int oc_dense_forward(const double* x, const float* logits, int T, int H, int E, int k, int F,
+                     int score_fn, int renorm, int n_groups, int topk_groups, int group_score,
+                     double rho, const double* wg, const double* wu, const double* wd,
+                     int Fs, const double* wsg, const double* wsu, const double* wsd,
+                     double* y) {
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int t = 0; t < T; ++t) {
+    int32_t idx[1024];
+    double w[1024];
+    if (route_one(logits + (int64_t)t * E, E, k, score_fn, renorm, n_groups, topk_groups,
+                  group_score, rho, idx, w, NULL)) { bad = 1; continue; }
+    const double* xt = x + (int64_t)t * H;
+    double* yt = y + (int64_t)t * H;
+    for (int o = 0; o < H; ++o) yt[o] = 0.0;
+    int nexp = k + (wsg ? 1 : 0);
+    for (int j = 0; j < nexp; ++j) {
+      int shared = (j == k);
+      int FF = shared ? Fs : F;
+      const double* G = shared ? wsg : wg + (int64_t)idx[j] * F * H;
+      const double* U = shared ? wsu : wu + (int64_t)idx[j] * F * H;
+      const double* D = shared ? wsd : wd + (int64_t)idx[j] * H * F;
+      double c = shared ? 1.0 : w[j];
+      double* h = (double*)malloc(sizeof(double) * (size_t)FF);
+      for (int f = 0; f < FF; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < H; ++i) { g += xt[i] * G[(int64_t)f * H + i]; u += xt[i] * U[(int64_t)f * H + i]; }
+        h[f] = g / (1.0 + exp(-g)) * u;
+      }
+      for (int o = 0; o < H; ++o) {
+        double s = 0.0;
+        for (int f = 0; f < FF; ++f) s += h[f] * D[(int64_t)o * FF + f];
+        yt[o] += c * s;
+      }
+      free(h);
+    }
+  }
+  return bad ? -1 : 0;
+}

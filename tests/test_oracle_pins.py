@@ -1,0 +1,425 @@
+"""Pins of the CPU oracle to things other than itself (no GPU).
+
+Each test checks one oracle function against what the mathematics or a library routine
+fixes: brute force on tiny inputs, closed forms, special cases that reduce to a textbook
+routine, invariants, and the fixed points of the e4m3 format. A plausible mistake in the
+oracle (a dropped term, a wrong sign or index, a transposed operand, a wrong tie-break)
+fails at least one of them.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def cfg(E, k, score_fn=0, renorm=0, n_groups=1, topk_groups=1, group_score=0, rho=1.0, **kw):
+    d = dict(T=0, H=0, E=E, k=k, F=0, n_shared=0, F_shared=0, score_fn=score_fn, renorm=renorm,
+             n_groups=n_groups, topk_groups=topk_groups, group_score=group_score,
+             routed_scale=rho, act_dtype=0, xfer_dtype=0)
+    d.update(kw)
+    return d
+
+
+# ------------------------------------------------------------------ input generator
+def test_splitmix64_published_sequence():
+    # splitmix64 from state 0 (Steele, Lea, Flood 2014; Vigna's reference code): the first
+    # two outputs are 0xE220A8397B1DCDAF and 0x6E789E6AA1B965F4.
+    with np.errstate(over="ignore"):
+        z = synth._mix64(np.array([synth.GOLDEN, synth.GOLDEN * np.uint64(2)], dtype=np.uint64))
+    assert int(z[0]) == 0xE220A8397B1DCDAF
+    assert int(z[1]) == 0x6E789E6AA1B965F4
+
+
+def test_generator_moments_and_counter_access():
+    a = synth.normal(3, synth.X, (512, 256), 1.0, "f32")
+    assert abs(a.mean()) < 0.01 and abs(a.std() - 1.0) < 0.01
+    r = synth.rows(3, synth.X, [7, 300], 256, 1.0, "f32")
+    assert np.array_equal(r, a[[7, 300]])
+    b = synth.normal(3, synth.X, (512, 256), 0.02, "bf16")
+    assert np.array_equal(b, synth.round_bf16(b))
+    assert np.array_equal(torch.from_numpy(b).to(torch.bfloat16).float().numpy(), b)
+
+
+def test_bf16_rounding_matches_torch():
+    v = synth.normal(1, 99, (4096,), 3.0, "f32")
+    ours = synth.round_bf16(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_zipf_bias_recipe():
+    b = synth.zipf_bias(0, 128)
+    r = np.rint(np.exp(-b.astype(np.float64) / 1.2)).astype(int)
+    assert sorted(r.tolist()) == list(range(1, 129))
+    assert b.max() == 0.0 and abs(b.min() + 1.2 * math.log(128)) < 1e-5
+
+
+# ------------------------------------------------------------------ deterministic exp
+def test_det_expf_accuracy_against_fp64():
+    a = np.concatenate([np.linspace(-103.0, 88.7, 200001, dtype=np.float32),
+                        synth.normal(5, 98, (100000,), 4.0, "f32")])
+    ours = oracle.det_expf(a).astype(np.float64)
+    ref = np.exp(a.astype(np.float64))
+    normal = ref > 1.2e-38
+    ulp = np.spacing(ref[normal].astype(np.float32)).astype(np.float64)
+    err = np.abs(ours[normal] - ref[normal]) / ulp
+    assert err.max() <= 2.0, err.max()
+    tiny = ~normal
+    assert np.all(np.abs(ours[tiny] - ref[tiny]) <= 2.0 ** -149 * 2)
+
+
+def test_det_expf_special_values():
+    v = oracle.det_expf(np.array([0.0, -0.0, 89.0, -104.0, np.inf, -np.inf], np.float32))
+    assert v[0] == 1.0 and v[1] == 1.0 and np.isinf(v[2]) and v[3] == 0.0
+    assert np.isinf(v[4]) and v[5] == 0.0
+    assert oracle.det_sigmoidf(0.0) == 0.5
+
+
+def test_det_sigmoid_close_to_fp64():
+    l = synth.normal(2, 97, (20000,), 3.0, "f32")
+    ours = np.array([oracle.det_sigmoidf(float(x)) for x in l[:2000]])
+    ref = 1.0 / (1.0 + np.exp(-l[:2000].astype(np.float64)))
+    assert np.max(np.abs(ours - ref) / ref) < 4 * 2.0 ** -24
+
+
+# ------------------------------------------------------------------ e4m3 codec
+def test_e4m3_decode_all_codes_match_torch():
+    ours = oracle.e4m3_decode_all()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_spec_points_golden():
+    vals = oracle.e4m3_decode_all()
+    with open(os.path.join(GOLDEN, "e4m3_ocp_points.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            code, v = line.split()
+            c = int(code, 16)
+            if v == "nan":
+                assert np.isnan(vals[c])
+            else:
+                assert vals[c] == float(v) and math.copysign(1, vals[c]) == math.copysign(1, float(v))
+                assert oracle.e4m3_encode(np.float32(float(v)))[0] == c
+
+
+def test_e4m3_encode_roundtrip_midpoints_and_saturation():
+    vals = oracle.e4m3_decode_all()
+    fin = [c for c in range(256) if not np.isnan(vals[c])]
+    # every finite code round-trips
+    assert all(oracle.e4m3_encode(np.float32(vals[c]))[0] == c for c in fin)
+    # midpoints between neighbours go to the even (lower mantissa bit 0) code
+    pos = sorted((vals[c], c) for c in range(128) if not np.isnan(vals[c]))
+    for (v0, c0), (v1, c1) in zip(pos, pos[1:]):
+        mid = np.float32((v0 + v1) / 2)
+        assert float(mid) == (v0 + v1) / 2  # representable in fp32
+        got = oracle.e4m3_encode(mid)[0]
+        assert got == (c0 if c0 % 2 == 0 else c1), (v0, v1)
+        # just off the midpoint goes to the nearer one
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(0)))[0] == c0
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(1e9)))[0] == c1
+    # satfinite
+    big = np.array([448.0, 460.0, 464.0, 1e6, np.inf, -1e30], np.float32)
+    assert list(oracle.e4m3_encode(big)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_e4m3_encode_in_range_matches_torch_cast():
+    v = synth.normal(4, 96, (200000,), 60.0, "f32")
+    v = v[np.abs(v) < 448]
+    ours = oracle.e4m3_encode(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------------ block quantisation
+def test_quant_blocks_rule_and_error_bound():
+    v = synth.normal(6, 95, (64, 384), 1.0, "bf16")
+    v[3, 128:256] = 0.0  # an all-zero block
+    q, s = oracle.quant_blocks(v, 1, 128)
+    assert s.shape == (64, 3)
+    assert s[3, 1] == 1.0 and not q[3, 128:256].any()
+    amax = np.abs(v.reshape(64, 3, 128)).max(-1)
+    nz = amax > 0
+    assert np.array_equal(s[nz], (amax[nz] / np.float32(448.0)).astype(np.float32))
+    # the largest element of each block lands on +-448 exactly
+    arg = np.abs(v.reshape(64, 3, 128)).argmax(-1)
+    codes = np.take_along_axis(q.reshape(64, 3, 128), arg[..., None], -1)[..., 0]
+    assert np.all((codes[nz] & 0x7F) == 0x7E)
+    dq = oracle.dequant_blocks(q, s, 1, 128)
+    # e4m3 has 3 mantissa bits: relative error <= 2^-4 for normals, abs <= 2^-10*scale below
+    sc = np.repeat(s, 128, axis=1).astype(np.float64)
+    bound = np.maximum(np.abs(v) * 2.0 ** -4, sc * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(np.abs(dq - v) <= bound)
+    # q matches the rule written with numpy + torch's cast
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rs = (np.float32(448.0) / np.repeat(amax.astype(np.float32), 128, 1)).astype(np.float32)
+        prod = (v * rs).astype(np.float32)
+    ref = torch.from_numpy(np.clip(prod, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    m = np.repeat(nz, 128, axis=1)
+    assert np.array_equal(q[m], ref[m])
+
+
+def test_quant_blocks_128x128():
+    w = synth.normal(7, 94, (256, 384), 0.02, "bf16")
+    q, s = oracle.quant_blocks(w, 128, 128)
+    assert s.shape == (2, 3)
+    for bi in range(2):
+        for bj in range(3):
+            blk = w[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            assert s[bi, bj] == np.float32(np.abs(blk).max()) / np.float32(448)
+    dq = oracle.dequant_blocks(q, s, 128, 128)
+    assert oracle.rel_l2(dq, w) < 0.05
+
+
+# ------------------------------------------------------------------ router logits
+def test_router_logits_fp64_then_round():
+    x = synth.normal(0, 1, (64, 96), 1.0, "bf16")
+    wr = synth.normal(0, 2, (16, 96), 0.02, "bf16")
+    b = synth.zipf_bias(0, 16)
+    l = oracle.router_logits(x, wr, b)
+    exact = x.astype(np.float64) @ wr.astype(np.float64).T + b.astype(np.float64)
+    assert np.max(np.abs(l - exact.astype(np.float32))) <= np.max(np.spacing(np.abs(l))) + 0
+    assert np.mean(l == exact.astype(np.float32)) > 0.99
+
+
+# ------------------------------------------------------------------ routing
+def brute_topk(row, k, allowed=None):
+    items = [(-float(row[e]), e) for e in range(len(row)) if allowed is None or allowed[e]]
+    items.sort()
+    return [e for _, e in items[:k]]
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (8, 2), (8, 8), (16, 3), (16, 16), (12, 5)])
+def test_topk_brute_force_with_ties(E, k):
+    for seed, levels in [(0, 0), (1, 3), (2, 6)]:
+        l = synth.synthetic_logits(seed, 200, E, 1.0, tie_levels=levels)
+        l[0, :] = 0.0
+        l[1, :] = -0.0
+        l[2, ::2] = 0.0
+        l[2, 1::2] = -0.0
+        idx, w = oracle.route(l, cfg(E, k))
+        for t in range(l.shape[0]):
+            assert list(idx[t]) == brute_topk(l[t], k), (t, l[t])
+
+
+def test_softmax_weights_closed_forms():
+    l = synth.synthetic_logits(3, 100, 8)
+    # k = E: every expert selected; weights = full softmax (no renorm) in selection order
+    idx, w = oracle.route(l, cfg(8, 8))
+    p = np.exp(l.astype(np.float64) - l.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    assert np.allclose(w, np.take_along_axis(p, idx, 1), rtol=1e-14, atol=0)
+    # renormalised top-2 sums to 1 and equals softmax over the two logits
+    idx, w = oracle.route(l, cfg(8, 2, renorm=1, rho=1.0))
+    assert np.allclose(w.sum(1), 1.0, rtol=1e-14)
+    l2 = np.take_along_axis(l.astype(np.float64), idx, 1)
+    ref = 1.0 / (1.0 + np.exp(l2[:, 1] - l2[:, 0]))
+    assert np.allclose(w[:, 0], ref, rtol=1e-13)
+    # no renorm: weights are the softmax probabilities of the chosen experts
+    idx, w = oracle.route(l, cfg(8, 2, renorm=0, rho=2.5))
+    assert np.allclose(w, 2.5 * np.take_along_axis(p, idx, 1), rtol=1e-13)
+
+
+def test_sigmoid_weights_closed_form():
+    l = synth.synthetic_logits(4, 100, 16)
+    idx, w = oracle.route(l, cfg(16, 4, score_fn=1, renorm=1))
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(l.astype(np.float64), idx, 1)))
+    assert np.allclose(w, s / s.sum(1, keepdims=True), rtol=1e-13)
+    idx, w = oracle.route(l, cfg(16, 4, score_fn=1, renorm=0, rho=0.5))
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(l.astype(np.float64), idx, 1)))
+    assert np.allclose(w, 0.5 * s, rtol=1e-13)
+
+
+def test_group_limited_special_cases_reduce_to_plain_topk():
+    l = synth.synthetic_logits(5, 300, 32, tie_levels=8)
+    plain, _ = oracle.route(l, cfg(32, 4, score_fn=1))
+    g1, _ = oracle.route(l, cfg(32, 4, score_fn=1, n_groups=1, topk_groups=1))
+    gG, _ = oracle.route(l, cfg(32, 4, score_fn=1, n_groups=4, topk_groups=4))
+    assert np.array_equal(plain, g1) and np.array_equal(plain, gG)
+
+
+@pytest.mark.parametrize("group_score", [0, 1])
+def test_group_limited_brute_force(group_score):
+    E, G, g, k = 16, 4, 2, 3
+    l = synth.synthetic_logits(6, 400, E, 2.0, tie_levels=12)
+    idx, _ = oracle.route(l, cfg(E, k, score_fn=1, n_groups=G, topk_groups=g, group_score=group_score))
+    gs = E // G
+    for t in range(l.shape[0]):
+        s = [oracle.det_sigmoidf(float(v)) for v in l[t]]
+        # group score written from the definition with Python's sort
+        scores = []
+        for q in range(G):
+            top = sorted(s[q * gs:(q + 1) * gs], reverse=True)
+            scores.append(np.float32(np.float32(top[0]) + np.float32(top[1])) if group_score == 0 else np.float32(top[0]))
+        assert np.array_equal(oracle.group_scores(l[t], G, group_score), np.array(scores, np.float32))
+        # enumerate all subsets of g groups; the kept set is the lexicographically first
+        # subset among those whose sorted score vector is largest
+        best = max(itertools.combinations(range(G), g),
+                   key=lambda c: (sorted([scores[q] for q in c], reverse=True), [-q for q in c]))
+        allowed = [(e // gs) in best for e in range(E)]
+        assert list(idx[t]) == brute_topk(l[t], k, allowed), t
+
+
+def test_group_score_uses_sigmoid_not_logit():
+    # two groups: A has one huge and one tiny logit, B two moderate ones; the sum of
+    # sigmoids prefers B although A's top logit is far larger
+    l = np.array([[8.0, -8.0, 1.0, 1.0]], np.float32)
+    idx, _ = oracle.route(l, cfg(4, 1, score_fn=1, n_groups=2, topk_groups=1))
+    assert idx[0, 0] == 2
+    idx, _ = oracle.route(l, cfg(4, 1, score_fn=1, n_groups=2, topk_groups=1, group_score=1))
+    assert idx[0, 0] == 0
+
+
+def test_route_rejects_non_finite():
+    l = np.zeros((2, 8), np.float32)
+    l[1, 3] = np.nan
+    with pytest.raises(ValueError):
+        oracle.route(l, cfg(8, 2))
+
+
+# ------------------------------------------------------------------ counts / permutation
+@pytest.mark.parametrize("E,k,T", [(8, 2, 256), (128, 8, 1000), (16, 16, 33), (4, 1, 1)])
+def test_permutation_invariants(E, k, T):
+    l = synth.synthetic_logits(7, T, E, 1.0)
+    l[:, : min(E, 3)] += 3.0  # hot experts
+    idx, _ = oracle.route(l, cfg(E, k))
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert counts.sum() == T * k and offsets[0] == 0 and offsets[E] == T * k
+    assert np.array_equal(np.diff(offsets), counts)
+    assert np.array_equal(np.sort(tok_row.ravel()), np.arange(T * k))
+    for e in range(E):
+        seg = row_token[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)
+        assert np.array_equal(seg, np.nonzero((idx == e).any(1))[0])
+    for t in range(T):
+        for j in range(k):
+            r = tok_row[t, j]
+            assert row_token[r] == t and offsets[idx[t, j]] <= r < offsets[idx[t, j] + 1]
+
+
+def test_permute_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[0, 8]], np.int32), 8)
+
+
+# ------------------------------------------------------------------ dispatch + combine
+@pytest.mark.parametrize("k", [2, 8])
+def test_dispatch_combine_identity_experts_give_kx(k):
+    T, H, E = 300, 64, 16
+    x = synth.normal(8, 1, (T, H), 1.0, "bf16")
+    idx, _ = oracle.route(synth.synthetic_logits(8, T, E), cfg(E, k))
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    xd = oracle.dispatch(x, row_token)
+    assert np.array_equal(xd, x[row_token])
+    y = oracle.combine(xd, tok_row, np.ones((T, k)))
+    assert np.array_equal(y, k * x.astype(np.float64))
+
+
+def test_combine_definition_with_shared_rows():
+    T, H, k = 50, 32, 3
+    yd = synth.normal(9, 12, (T * k, H), 1.0, "f32").astype(np.float64)
+    ys = synth.normal(9, 13, (T, H), 1.0, "f32").astype(np.float64)
+    perm = np.argsort(synth.bits_at(9, 14, np.arange(T * k, dtype=np.uint64)), kind="stable")
+    tok_row = perm.reshape(T, k).astype(np.int32)
+    w = synth.uniform_at(9, 15, np.arange(T * k)).reshape(T, k)
+    y = oracle.combine(yd, tok_row, w, ys)
+    ref = np.einsum("tj,tjh->th", w, yd[tok_row]) + ys
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------------------ expert MLP
+def test_expert_mlp_matches_torch_swiglu():
+    n, H, F = 37, 64, 96
+    a = synth.normal(10, 1, (n, H), 1.0, "f32").astype(np.float64)
+    wg = synth.normal(10, 3, (F, H), 0.1, "f32").astype(np.float64)
+    wu = synth.normal(10, 4, (F, H), 0.1, "f32").astype(np.float64)
+    wd = synth.normal(10, 5, (H, F), 0.1, "f32").astype(np.float64)
+    y = oracle.expert_mlp(a, wg, wu, wd)
+    A, G, U, D = (torch.from_numpy(v) for v in (a, wg, wu, wd))
+    ref = (torch.nn.functional.silu(A @ G.T) * (A @ U.T)) @ D.T
+    assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_expert_mlp_quantised_h():
+    n, H, F = 9, 128, 256
+    a = synth.normal(11, 1, (n, H), 1.0, "f32").astype(np.float64)
+    wg = synth.normal(11, 3, (F, H), 0.1, "f32").astype(np.float64)
+    wu = synth.normal(11, 4, (F, H), 0.1, "f32").astype(np.float64)
+    wd = synth.normal(11, 5, (H, F), 0.1, "f32").astype(np.float64)
+    A, G, U = (torch.from_numpy(v) for v in (a, wg, wu))
+    h = (torch.nn.functional.silu(A @ G.T) * (A @ U.T)).numpy().astype(np.float32)
+    q, s = oracle.quant_blocks(h, 1, 128)
+    ref = oracle.dequant_blocks(q, s, 1, 128) @ wd.T
+    y = oracle.expert_mlp(a, wg, wu, wd, quant_h=True)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+    assert oracle.rel_l2(y, oracle.expert_mlp(a, wg, wu, wd)) < 0.05
+
+
+# ------------------------------------------------------------------ whole layer
+def small(name, **kw):
+    return synth.scaled(synth.WORKLOADS[name], **kw)
+
+
+SMALL = {
+    "tiny": small("tiny_fp32", T=64),
+    "mixtral": small("mixtral_bf16", T=96, H=128, F=256),
+    "dsv3": small("dsv3_bf16", T=64, H=128, E=32, F=128, F_shared=128),
+    "imbalanced": small("imbalanced_bf16", T=128, H=128, E=16, F=128),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_permuted_oracle_equals_dense_loop(name):
+    w = SMALL[name]
+    inp = synth.host_inputs(w, seed=1)
+    a = oracle.forward(w, inp)
+    b = oracle.dense_forward(w, inp)
+    assert oracle.rel_l2(a["y"], b) < 1e-12
+
+
+def test_identical_experts_with_renorm_equal_dense_mlp():
+    w = small("mixtral_bf16", T=40, H=64, E=8, F=96, renorm=1)
+    inp = synth.host_inputs(w, seed=2)
+    for key in ("w_gate", "w_up", "w_down"):
+        inp[key] = np.repeat(inp[key][:1], w["E"], axis=0)
+    y = oracle.forward(w, inp)["y"]
+    X = torch.from_numpy(inp["x"].astype(np.float64))
+    G, U, D = (torch.from_numpy(inp[k][0].astype(np.float64)) for k in ("w_gate", "w_up", "w_down"))
+    ref = ((torch.nn.functional.silu(X @ G.T) * (X @ U.T)) @ D.T).numpy()
+    assert oracle.rel_l2(y, ref) < 1e-12
+
+
+def test_single_expert_layer_is_dense_mlp_with_shared():
+    w = small("dsv3_bf16", T=16, H=64, E=1, k=1, F=64, F_shared=32, n_groups=1, topk_groups=1)
+    inp = synth.host_inputs(w, seed=3)
+    y = oracle.forward(w, inp)["y"]
+    X = torch.from_numpy(inp["x"].astype(np.float64))
+
+    def mlp(g, u, d):
+        g, u, d = (torch.from_numpy(v.astype(np.float64)) for v in (g, u, d))
+        return (torch.nn.functional.silu(X @ g.T) * (X @ u.T)) @ d.T
+
+    ref = mlp(inp["w_gate"][0], inp["w_up"][0], inp["w_down"][0]) + mlp(inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+    assert oracle.rel_l2(y, ref.numpy()) < 1e-12
+
+
+def test_fp8_layer_close_to_unquantised():
+    w = small("dsv3_fp8", T=32, H=256, E=16, F=128, F_shared=128, n_groups=4, topk_groups=2)
+    inp = synth.host_inputs(w, seed=4)
+    q = oracle.forward(w, inp)
+    ref = oracle.forward(dict(w, xfer_dtype=synth.BF16), inp)
+    assert np.array_equal(q["topk_idx"], ref["topk_idx"])
+    # three e4m3 rounding points (x, weights, h), each up to 2^-4 relative
+    assert 1e-3 < oracle.rel_l2(q["y"], ref["y"]) < 0.1
