@@ -1,0 +1,425 @@
+"""Benchmark of the MoE layer forward on GB300 (one JSON line on rank 0).
+
+A step is one moe_forward over one batch of T synthetic tokens (router logits, top-k,
+counts/offsets/permutation, dispatch, the grouped SwiGLU expert GEMMs, combine), with the
+inputs and weights resident in HBM. L2 is flushed (a 512 MB write) before every timed step
+and each step is timed with CUDA events on the launching stream. Per-stage times come from
+a second loop over the staged entry points, timed the same way.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+Multi-GPU: independent token-sharded replicas (no collective in the data path; the path has
+no exchange step on one node), launched with torch.distributed.run; value = tokens of all
+ranks / max-over-ranks time. --impl reference times the CPU oracle on a bounded token
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "mixtral_bf16"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def describe(w):
+    return (f"{w['name']} (T={w['T']}, H={w['H']}, E={w['E']}, k={w['k']}, F={w['F']}"
+            + (f", shared F={w['F_shared']}" if w["n_shared"] else "")
+            + (f", groups {w['topk_groups']}/{w['n_groups']}" if w["n_groups"] > 1 else "")
+            + (", e4m3 transfer" if w["xfer_dtype"] == synth.E4M3 else "") + ")")
+
+
+def algorithmic(w):
+    """Algorithmic bytes / flops per forward (each tensor read or written once)."""
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    R = T * k
+    a = 4 if w["act_dtype"] == synth.F32 else 2
+    x8 = w["xfer_dtype"] == synth.E4M3
+    xs = 1 if x8 else a
+    shared = T if w["n_shared"] else 0
+    d = {}
+    d["gemm_flops"] = synth.gemm_flops(w)
+    d["router_flops"] = 2.0 * T * H * E
+    d["dispatch_bytes"] = T * H * a + (R + (shared if x8 else 0)) * H * xs + R * 4 \
+        + ((R + shared) * (H // 128) * 4 if x8 else 0)
+    d["combine_bytes"] = (R + shared) * H * a + T * H * a + R * 8
+    d["weight_bytes"] = (E * 3 * F * H + (3 * w["F_shared"] * H if w["n_shared"] else 0)) * xs
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_gpu(args, w):
+    import torch
+    import token_routing_expert_router_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    moe.build()
+    peaks, peak_kind = load_peaks()
+
+    # ---- inputs: this rank's token shard (seed = rank) and the replicated weights (seed 0)
+    dt = torch.bfloat16 if w["act_dtype"] == synth.BF16 else torch.float32
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    s = w["w_std"]
+
+    def gen(shape, tid, std, seed=0, dtype=dt):
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        return synth.device_normal(t, seed, tid, std)
+
+    x = gen((T, H), synth.X, 1.0, seed=rank)
+    wts = {"w_router": gen((E, H), synth.W_ROUTER, s), "w_gate": gen((E, F, H), synth.W_GATE, s),
+           "w_up": gen((E, F, H), synth.W_UP, s), "w_down": gen((E, H, F), synth.W_DOWN, s),
+           "router_bias": torch.from_numpy(synth.zipf_bias(0, E)).to(dev) if w["zipf"] else None}
+    if w["n_shared"]:
+        wts["ws_gate"] = gen((F, H), synth.WS_GATE, s)
+        wts["ws_up"] = gen((F, H), synth.WS_UP, s)
+        wts["ws_down"] = gen((H, F), synth.WS_DOWN, s)
+    if w["xfer_dtype"] == synth.E4M3:
+        pairs = [("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")]
+        if w["n_shared"]:
+            pairs += [("ws_gate", "ss_gate"), ("ws_up", "ss_up"), ("ws_down", "ss_down")]
+        for wn, sn in pairs:
+            src = wts[wn].reshape(-1, wts[wn].shape[-1])
+            q = torch.empty(src.shape, dtype=torch.uint8, device=dev)
+            sc = torch.empty((src.shape[0] // 128, src.shape[1] // 128), dtype=torch.float32, device=dev)
+            moe.moe_quantize_e4m3(src, 128, 128, q, sc)
+            wts[wn] = q.reshape(wts[wn].shape)
+            wts[sn] = sc
+    cfg = moe.MoEConfig.make(**{kk: w[kk] for kk in (
+        "T", "H", "E", "k", "F", "n_shared", "F_shared", "score_fn", "renorm", "n_groups",
+        "topk_groups", "group_score", "routed_scale", "act_dtype", "xfer_dtype")})
+    ws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device=dev)
+    moe.moe_workspace_init(ws)
+    y = torch.empty((T, H), dtype=dt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- whole-layer steps
+    for _ in range(args.warmup):
+        moe.moe_forward(cfg, x, wts, y, ws)
+    st = moe.moe_read_status(ws)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))  # evict the previous step's lines from L2
+            ev[i][0].record(stream)
+            moe.moe_forward(cfg, x, wts, y, ws)
+            ev[i][1].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    assert moe.moe_read_status(ws) == moe.MOE_OK
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # ---- per-stage times through the staged entry points (same kernels)
+    R = T * k
+    rows = R + (T if w["n_shared"] else 0)
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    xdt = torch.uint8 if fp8 else dt
+    b = {"logits": torch.empty((T, E), dtype=torch.float32, device=dev),
+         "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+         "w": torch.empty((T, k), dtype=torch.float32, device=dev),
+         "counts": torch.empty(E, dtype=torch.int32, device=dev),
+         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "row_token": torch.empty(R, dtype=torch.int32, device=dev),
+         "tok_row": torch.empty((T, k), dtype=torch.int32, device=dev),
+         "xd": torch.empty((rows, H), dtype=xdt, device=dev),
+         "xd_scale": torch.empty((H // 128, rows), dtype=torch.float32, device=dev) if fp8 else None,
+         "h": torch.empty((rows, F), dtype=xdt, device=dev),
+         "h_scale": torch.empty((F // 128, rows), dtype=torch.float32, device=dev) if fp8 else None,
+         "yd": torch.empty((rows, H), dtype=dt, device=dev)}
+    stages = {
+        "router_logits": lambda: moe.moe_router_logits(cfg, x, wts["w_router"], wts["router_bias"], b["logits"], ws),
+        "route": lambda: moe.moe_route(cfg, b["logits"], b["idx"], b["w"], b["counts"], b["offsets"],
+                                       b["row_token"], b["tok_row"], ws),
+        "dispatch": lambda: moe.moe_dispatch(cfg, x, b["tok_row"], b["xd"], b["xd_scale"]),
+        "grouped_mlp": lambda: moe.moe_grouped_mlp(cfg, b["xd"], b["xd_scale"], x, b["offsets"], wts, b["h"],
+                                                   b["h_scale"], b["yd"], ws),
+        "combine": lambda: moe.moe_combine(cfg, b["yd"], b["tok_row"], b["w"], y),
+    }
+    for _ in range(2):
+        for f in stages.values():
+            f()
+    reps = max(3, min(args.steps, 10))
+    times = {n: [] for n in stages}
+    for _ in range(reps):
+        for n, f in stages.items():
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            times[n].append((e0, e1))
+    torch.cuda.synchronize()
+    stage_ms = {n: statistics.median(a.elapsed_time(bb) for a, bb in v) for n, v in times.items()}
+    alg = algorithmic(w)
+
+    # ---- end to end: pinned host x in, host y out, through the public call
+    xh = torch.empty((T, H), dtype=dt, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.empty((T, H), dtype=dt, pin_memory=True)
+    xdev = torch.empty_like(x)
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        xdev.copy_(xh, non_blocking=True)
+        moe.moe_forward(cfg, xdev, wts, y, ws)
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return None
+    gemm_ms = stage_ms["grouped_mlp"]
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    if fp8:
+        tensor_peak *= 2.0  # nominal fp8:bf16 dense ratio of the part
+    achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+    counts = b["counts"].cpu().numpy()
+    line = {
+        "metric": "MoE-layer fwd tokens/s",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3+bf16" if fp8 else ("bf16" if w["act_dtype"] == synth.BF16 else "f32"),
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset or trained weights)",
+        "config": {"workload": describe(w), "tokens_per_gpu": T, "parallelism": f"replicas x{world} (token-sharded)",
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "weights_bytes": alg["weight_bytes"]},
+        "stages_ms": {n: round(v, 4) for n, v in stage_ms.items()},
+        "dispatch_gbs": round(alg["dispatch_bytes"] / (stage_ms["dispatch"] / 1e3) / 1e9, 1),
+        "combine_gbs": round(alg["combine_bytes"] / (stage_ms["combine"] / 1e3) / 1e9, 1),
+        "grouped_gemm_tflops": round(achieved, 1),
+        "grouped_gemm_frac_of_peak": round(achieved / tensor_peak, 3),
+        "roofline": {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
+                     "bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
+                     "peak_kind": f"{peak_kind} bf16 sustained" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
+                     "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 3), "traffic": None},
+        "hbm_roofline": {"dispatch_frac": round(alg["dispatch_bytes"] / (stage_ms["dispatch"] / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
+                         "combine_frac": round(alg["combine_bytes"] / (stage_ms["combine"] / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
+                         "peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
+        "expert_rows": {"min": int(counts.min()), "max": int(counts.max()), "empty": int((counts == 0).sum())},
+        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(y.numel() * y.element_size())},
+        "gpu_launches": args.steps * launches_per_forward(w),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def launches_per_forward(w):
+    # router logits, top-k, 3 scan passes, dispatch, 2 grouped GEMMs, combine
+    return 9
+
+
+def cpu_baseline(w, n_tokens, seed=0):
+    """The oracle as it stands, on n_tokens tokens of the workload (fp64, OpenMP)."""
+    import oracle
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    dt = synth.act_name(w)
+    toks = np.arange(n_tokens)
+    x = synth.rows(seed, synth.X, toks, H, 1.0, dt)
+    wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], dt)
+    bias = synth.zipf_bias(0, E) if w["zipf"] else None
+    t_or = 0.0
+    t0 = time.perf_counter()
+    logits = oracle.router_logits(x, wr, bias)
+    sub = dict(w, T=n_tokens)
+    idx, wt = oracle.route(logits, sub)
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    if fp8:
+        q, sc = oracle.quant_blocks(x, 1, 128)
+        a = oracle.dequant_blocks(q, sc, 1, 128)
+    else:
+        a = x.astype(np.float64)
+    xd = a[row_token]
+    t_or += time.perf_counter() - t0
+    yd = np.zeros((n_tokens * k, H))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 == r0:
+            continue
+        g, u, d = synth.expert_weights(w, 0, e)  # drawing the weights is not timed
+        t0 = time.perf_counter()
+        if fp8:
+            g, u, d = (oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
+        yd[r0:r1] = oracle.expert_mlp(xd[r0:r1], g, u, d, quant_h=fp8)
+        t_or += time.perf_counter() - t0
+    ys = None
+    if w["n_shared"]:
+        Fs = w["F_shared"]
+        g = synth.normal(0, synth.WS_GATE, (Fs, H), w["w_std"], dt)
+        u = synth.normal(0, synth.WS_UP, (Fs, H), w["w_std"], dt)
+        d = synth.normal(0, synth.WS_DOWN, (H, Fs), w["w_std"], dt)
+        t0 = time.perf_counter()
+        if fp8:
+            g, u, d = (oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
+        ys = oracle.expert_mlp(a, g, u, d, quant_h=fp8)
+        t_or += time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.combine(yd, tok_row, wt, ys)
+    t_or += time.perf_counter() - t0
+    return {"value": round(n_tokens / t_or, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n_tokens} tokens of the workload (router, top-k, permutation, every chosen expert's "
+                      f"fp64 SwiGLU MLP, combine); OpenMP over rows; weight drawing not timed; "
+                      f"{t_or:.1f} s of oracle time"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; its build happens on import
+    vals = []
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        cb = cpu_baseline(w, args.cpu_tokens, seed=i)
+        vals.append(cb)
+    t_all = time.perf_counter() - t_all
+    value = statistics.median(v["value"] for v in vals)
+    cb = dict(vals[0])
+    cb["value"] = value
+    return {"impl": "reference", "metric": "MoE-layer fwd tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t_all / args.steps, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(w)}, "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_gpu(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) single-GPU Mixture-of-Experts layer forward.
+ *
+ * The layer, as the method states it: a router scores every token against the experts
+ * and activates k of them ("Scalable Training of Mixture-of-Experts Models with Megatron
+ * Core" summary, "O essencial"); dispatch directs each token to its experts and combine
+ * sends the results back, accumulating in high precision (Hybrid-EP article, dispatch and
+ * combine operators); the experts' GEMMs run together as one grouped GEMM (Megatron-Core
+ * summary, section 2.4 "Grouped GEMM"); routing is dropless, and kernels read the dynamic
+ * per-expert shapes from device memory so that no host synchronisation is needed
+ * (section 2.4, "Kernels Iniciados pelo Dispositivo"; Hybrid-EP article, pre-sized
+ * buffers). On one GPU, dispatch and combine are on-device permutations.
+ *
+ *   moe_router_logits   S0  logits[t,e] = sum_h x[t,h] * Wr[e,h] (+ bias[e])
+ *   moe_route           S1  top-k (optionally group-limited) + weights, then S2
+ *   moe_route_from_map  S2  counts, offsets and the permutation from a given map (replay)
+ *   moe_dispatch        S3  xd[r] = x[row_token[r]] (FP8: quantised once per token)
+ *   moe_grouped_mlp     S4-S6  per expert: h = silu(xd Wg^T) * (xd Wu^T); yd = h Wd^T
+ *   moe_combine         S7  y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ shared row)
+ *   moe_forward         S0-S7 in one stream-ordered call
+ *
+ * Conventions shared by every call:
+ *  - Every data pointer is DEVICE memory owned by the caller; the library allocates
+ *    nothing and frees nothing. Pointers must be 16-byte aligned.
+ *  - Every matrix is row-major and dense (leading dimension = its column count).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL means the legacy default
+ *    stream) and never synchronise the host, except moe_read_status.
+ *  - The return code covers host-side validation and launch errors only. Faults found on
+ *    the device (an expert id out of range in a replayed map, a non-finite router score,
+ *    a bounded wait that expired) are written to a status word in the workspace; read it
+ *    with moe_read_status.
+ *  - Re-entrant as long as two calls in flight at once do not share a workspace.
+ *
+ * Shapes: T tokens, H hidden, E routed experts, k experts per token, F expert FFN width.
+ * R = T*k routed rows; with a shared expert the dispatch/expert buffers hold R + T rows,
+ * the shared expert's row for token t being row R + t.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, inconsistent sizes */
+  MOE_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. H % 64 != 0 on bf16) */
+  MOE_ERR_CUDA = 3,             /* a CUDA launch or driver call failed */
+  MOE_ERR_DEVICE_BAD_INPUT = 4, /* device status: id out of range or non-finite score */
+  MOE_ERR_TIMEOUT = 5           /* device status: a bounded wait in a kernel expired */
+} moe_status_t;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1, MOE_DTYPE_E4M3 = 2 };
+enum { MOE_GROUP_SCORE_TOP2_SUM = 0, MOE_GROUP_SCORE_MAX = 1 };
+
+/* Layer configuration: plain values, no pointers. */
+typedef struct {
+  int32_t T, H, E, k, F;
+  int32_t n_shared;    /* 0 or 1 shared expert, applied to every token with weight 1 */
+  int32_t F_shared;    /* its FFN width; must equal F when n_shared = 1 */
+  int32_t score_fn;    /* MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID */
+  int32_t renorm;      /* 1: weights normalised over the k selected experts */
+  int32_t n_groups;    /* G: experts split into G contiguous groups (1 = no grouping) */
+  int32_t topk_groups; /* g: groups kept before the top-k (g = G: no limit); sigmoid only */
+  int32_t group_score; /* MOE_GROUP_SCORE_*: sum of the two largest scores, or the max */
+  float routed_scale;  /* every routed weight is multiplied by this (1.0) */
+  int32_t act_dtype;   /* MOE_DTYPE_F32 or MOE_DTYPE_BF16: x, router and (unless E4M3) expert weights, y */
+  int32_t xfer_dtype;  /* = act_dtype, or MOE_DTYPE_E4M3 (bf16 act only): dispatched rows and expert GEMMs in e4m3 */
+} moe_config_t;
+
+/* Layer weights (device pointers). act = act_dtype; q = e4m3 when xfer_dtype is E4M3,
+ * else act. E4M3 weights carry fp32 scales per 128x128 block (value = code * scale). */
+typedef struct {
+  const void* w_router;     /* [E, H] act */
+  const float* router_bias; /* [E] fp32 added to every logit, or NULL */
+  const void* w_gate;       /* [E, F, H] q */
+  const void* w_up;         /* [E, F, H] q */
+  const void* w_down;       /* [E, H, F] q */
+  const float* s_gate;      /* E4M3 only: [E, F/128, H/128] */
+  const float* s_up;        /* E4M3 only: [E, F/128, H/128] */
+  const float* s_down;      /* E4M3 only: [E, H/128, F/128] */
+  const void* ws_gate;      /* shared expert [F, H] q, or NULL when n_shared = 0 */
+  const void* ws_up;        /* [F, H] q */
+  const void* ws_down;      /* [H, F] q */
+  const float* ss_gate;     /* E4M3 only: [F/128, H/128] */
+  const float* ss_up;       /* E4M3 only: [F/128, H/128] */
+  const float* ss_down;     /* E4M3 only: [H/128, F/128] */
+} moe_weights_t;
+
+/* Bytes of device workspace needed by every call below except moe_forward (the status
+ * word plus the routing scan's per-block counts). Zero it once with moe_workspace_init. */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Bytes of device workspace for moe_forward: the part above followed by every
+ * intermediate of the layer (logits, routing map, permutation, dispatched rows, h, yd). */
+moe_status_t moe_forward_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Clears the status word of a workspace (stream-ordered). Call once after allocating. */
+moe_status_t moe_workspace_init(void* ws, moe_stream_t stream);
+
+/* S0 — router logits (Megatron-Core summary, "O essencial": the router scores each token
+ * against every expert). x [T,H] act, w_router [E,H] act, router_bias [E] fp32 or NULL ->
+ * logits [T,E] fp32, accumulated in fp32. */
+moe_status_t moe_router_logits(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias, float* logits, void* ws,
+                               moe_stream_t stream);
+
+/* S1 + S2 — routing. From fp32 scores `logits` [T,E]: per token the k experts with the
+ * largest logit (ties to the lower expert index), after keeping only the topk_groups best
+ * groups when n_groups > 1 (group score from sigmoid scores computed with a fixed,
+ * machine-independent fp32 exp). Outputs:
+ *   topk_idx [T,k] int32, in descending key order;
+ *   topk_w   [T,k] fp32: softmax (over all experts, or the k selected when renorm) or
+ *            sigmoid (divided by the selected sum when renorm), times routed_scale;
+ *   counts [E], offsets [E+1] int32 (offsets[E] = T*k);
+ *   row_token [T*k]: the token in each dispatched row, rows of expert e being
+ *            [offsets[e], offsets[e+1]) in ascending token id;
+ *   tok_row [T,k]: the row holding token t's j-th choice.
+ * Bit-exact and deterministic (no atomics whose order shows in the result).
+ * A non-finite logit sets MOE_ERR_DEVICE_BAD_INPUT in the status word. */
+moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* topk_idx,
+                       float* topk_w, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                       int32_t* tok_row, void* ws, moe_stream_t stream);
+
+/* S2 only, from a given routing map (router replay, Megatron-Core summary section 2.5).
+ * An id outside [0,E) sets MOE_ERR_DEVICE_BAD_INPUT; that entry is then counted for
+ * expert 0 so that every output stays in bounds. */
+moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx,
+                                int32_t* counts, int32_t* offsets, int32_t* row_token,
+                                int32_t* tok_row, void* ws, moe_stream_t stream);
+
+/* S3 — dispatch (Hybrid-EP article, dispatch operator): xd[tok_row[t,j]] = x[t], reading
+ * each token once. act xfer: xd [R(+T), H] act, bit copy; xd_scale unused (NULL).
+ * E4M3 xfer: each token is quantised once in 1x128 blocks (scale = amax/448, codes =
+ * e4m3_rn_satfinite(v * (448/amax)); an all-zero block has scale 1) and written to its k
+ * rows (and row R+t with a shared expert); xd [R(+T), H] e4m3, xd_scale [H/128, R(+T)]
+ * fp32 (block-major: scale of row r, block b at b*(R(+T)) + r). */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* tok_row,
+                          void* xd, float* xd_scale, moe_stream_t stream);
+
+/* S4 + S5 + S6 — the experts as one grouped GEMM (Megatron-Core summary section 2.4).
+ * For expert e, rows r in [offsets[e], offsets[e+1]) of xd:
+ *     h[r]  = silu(xd[r] . Wg[e]^T) * (xd[r] . Wu[e]^T),  silu(z) = z / (1 + e^-z)
+ *     yd[r] = h[r] . Wd[e]^T
+ * and, with a shared expert, the same for rows R + t with A = x[t] (act xfer) or the
+ * dispatched row R + t (E4M3 xfer) and weights ws_*. The per-expert row counts are read
+ * on the device; empty experts cost nothing. h [R(+T), F] act, or e4m3 with h_scale
+ * [F/128, R(+T)] requantised in 1x128 blocks (E4M3 xfer); yd [R(+T), H] act.
+ * `x` may be NULL unless act xfer with a shared expert. */
+moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const float* xd_scale,
+                             const void* x, const int32_t* offsets, const moe_weights_t* w,
+                             void* h, float* h_scale, void* yd, void* ws, moe_stream_t stream);
+
+/* S7 — combine (Hybrid-EP article, combine operator with high-precision accumulation):
+ * y[t] = sum_{j<k} topk_w[t,j] * yd[tok_row[t,j]]  (+ yd[R + t] with a shared expert),
+ * accumulated in fp32 in that fixed order, written once in act dtype. */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* tok_row,
+                         const float* topk_w, void* y, moe_stream_t stream);
+
+/* S0..S7 — the whole layer forward, stream-ordered with no host synchronisation, so the
+ * call can be captured in a CUDA graph. ws: moe_forward_workspace_size bytes. The optional
+ * outputs (NULL to skip) receive copies of the routing map and counts. */
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                         void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
+                         int32_t* counts_out, moe_stream_t stream);
+
+/* Offline weight preparation for the E4M3 variant: quantise a bf16 [rows, cols] matrix in
+ * br x bc blocks with the rule of moe_dispatch; q [rows, cols] e4m3, scale
+ * [ceil(rows/br), ceil(cols/bc)] fp32 row-major. br, bc in {1, 128}. */
+moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols, int32_t br,
+                               int32_t bc, uint8_t* q, float* scale, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the device status word of `ws` in *device_status
+ * (MOE_OK or a moe_status_t code) and clears it. The only call that blocks the host. */
+moe_status_t moe_read_status(void* ws, moe_stream_t stream, int32_t* device_status);
+
+/* Static string naming a status code. */
+const char* moe_status_string(moe_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -82,9 +82,36 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(f32_to_bf16_bits(a))
 
 
-def normal_at(seed: int, tid: int, idx: np.ndarray, std: float = 1.0, dtype: str = "f32") -> np.ndarray:
-    """Values of elements ``idx`` (flat, row-major) of tensor ``tid``; fp32 array holding
-    exact fp32 (or exact bf16) values."""
+_HOST = None
+
+
+def _host_lib():
+    """The C host generator (synth/gen_host.c), compiled on first use."""
+    global _HOST
+    if _HOST is None:
+        import ctypes
+        import os
+        import subprocess
+        here = os.path.dirname(os.path.abspath(__file__))
+        src = os.path.join(here, "gen_host.c")
+        out = os.path.join(here, "_build", "libsynth_host.so")
+        os.makedirs(os.path.dirname(out), exist_ok=True)
+        if not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+            tmp = out + f".{os.getpid()}.tmp"
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+                                   "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+            os.replace(tmp, out)
+        L = ctypes.CDLL(out)
+        P = ctypes.c_void_p
+        L.synth_normal_host.argtypes = [P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_uint32, ctypes.c_uint32, ctypes.c_double]
+        L.synth_normal_host.restype = None
+        _HOST = L
+    return _HOST
+
+
+def normal_at_numpy(seed: int, tid: int, idx: np.ndarray, std: float = 1.0, dtype: str = "f32") -> np.ndarray:
+    """The recipe written out in numpy (slow; the definition the C generator is pinned to)."""
     idx = np.asarray(idx, dtype=np.uint64).ravel()
     out = np.empty(idx.size, dtype=np.float32)
     for s in range(0, idx.size, _CHUNK):
@@ -94,10 +121,26 @@ def normal_at(seed: int, tid: int, idx: np.ndarray, std: float = 1.0, dtype: str
     return out
 
 
+def normal_at(seed: int, tid: int, idx: np.ndarray, std: float = 1.0, dtype: str = "f32") -> np.ndarray:
+    """Values of elements ``idx`` (flat, row-major) of tensor ``tid``; fp32 array holding
+    exact fp32 (or exact bf16) values."""
+    import ctypes
+    idx = np.ascontiguousarray(np.asarray(idx).ravel(), dtype=np.int64)
+    out = np.empty(idx.size, dtype=np.float32)
+    _host_lib().synth_normal_host(out.ctypes.data_as(ctypes.c_void_p), idx.size,
+                                  idx.ctypes.data_as(ctypes.c_void_p), 0, int(dtype == "bf16"),
+                                  seed & 0xFFFFFFFF, tid & 0xFFFFFFFF, float(std))
+    return out
+
+
 def normal(seed: int, tid: int, shape, std: float = 1.0, dtype: str = "f32", offset: int = 0) -> np.ndarray:
     """Whole tensor of ``shape`` (flat index = row-major position + ``offset``)."""
+    import ctypes
     n = int(np.prod(shape))
-    return normal_at(seed, tid, np.arange(offset, offset + n, dtype=np.uint64), std, dtype).reshape(shape)
+    out = np.empty(n, dtype=np.float32)
+    _host_lib().synth_normal_host(out.ctypes.data_as(ctypes.c_void_p), n, None, offset,
+                                  int(dtype == "bf16"), seed & 0xFFFFFFFF, tid & 0xFFFFFFFF, float(std))
+    return out.reshape(shape)
 
 
 def rows(seed: int, tid: int, row_ids, ncols: int, std: float = 1.0, dtype: str = "f32", base: int = 0) -> np.ndarray:
@@ -216,3 +259,44 @@ def gemm_flops(w: dict) -> float:
 def describe(w: dict) -> str:
     return ", ".join(f"{k}={w[k]}" for k in ("T", "H", "E", "k", "F", "n_shared", "score_fn",
                                               "renorm", "n_groups", "topk_groups"))
+
+
+# ----------------------------------------------------------------------------------------
+# Device twin (synth/gen.cu) for tensors too large to draw on the host.
+# ----------------------------------------------------------------------------------------
+_DEV = None
+
+
+def build_device(force: bool = False) -> str:
+    import os
+    import subprocess
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "gen.cu")
+    out = os.path.join(here, "_build", "libsynth.so")
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".{os.getpid()}.tmp"
+        subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                               "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-o", tmp, src])
+        os.replace(tmp, out)
+    return out
+
+
+def device_normal(t, seed: int, tid: int, std: float = 1.0, offset: int = 0):
+    """Fill CUDA tensor ``t`` (float32 or bfloat16, contiguous) with the generator's values
+    for flat indices offset .. offset + t.numel() - 1."""
+    global _DEV
+    import ctypes
+    import torch
+    if _DEV is None:
+        L = ctypes.CDLL(build_device())
+        L.synth_normal.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32,
+                                   ctypes.c_uint32, ctypes.c_double, ctypes.c_int64, ctypes.c_void_p]
+        L.synth_normal.restype = ctypes.c_int
+        _DEV = L
+    assert t.is_cuda and t.is_contiguous() and t.dtype in (torch.float32, torch.bfloat16)
+    rc = _DEV.synth_normal(t.data_ptr(), t.numel(), int(t.dtype == torch.bfloat16), seed, tid,
+                           float(std), offset, torch.cuda.current_stream().cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_normal failed: CUDA error {rc}")
+    return t

@@ -1,0 +1,183 @@
+"""Helpers shared by the GPU tests: build device inputs from the seeded generator, allocate
+the layer's buffers, and run the library through its Python binding. Oracle inputs always
+come from the host generator (never from a GPU result)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+import token_routing_expert_router_gb300 as moe
+
+
+def cfg_of(w: dict) -> moe.MoEConfig:
+    return moe.MoEConfig.make(**{k: w[k] for k in (
+        "T", "H", "E", "k", "F", "n_shared", "F_shared", "score_fn", "renorm", "n_groups",
+        "topk_groups", "group_score", "routed_scale", "act_dtype", "xfer_dtype")})
+
+
+def tdtype(w: dict):
+    return torch.bfloat16 if w["act_dtype"] == synth.BF16 else torch.float32
+
+
+def up(a: np.ndarray, dtype=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)  # fp32 -> bf16 is exact for bf16-valued arrays
+    return t.cuda()
+
+
+def quantize_dev(src: torch.Tensor, br: int, bc: int):
+    rows, cols = src.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    s = torch.empty(((rows + br - 1) // br, (cols + bc - 1) // bc), dtype=torch.float32, device="cuda")
+    moe.moe_quantize_e4m3(src, br, bc, q, s)
+    return q, s
+
+
+def _attach_fp8(w: dict, d: dict) -> dict:
+    """Replace expert weights by their e4m3 128x128-block quantisation (on the GPU)."""
+    if w["xfer_dtype"] != synth.E4M3:
+        return d
+    names = [("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")]
+    if w["n_shared"]:
+        names += [("ws_gate", "ss_gate"), ("ws_up", "ss_up"), ("ws_down", "ss_down")]
+    for wn, sn in names:
+        src = d[wn]
+        q, s = quantize_dev(src.reshape(-1, src.shape[-1]), 128, 128)
+        d[wn + "_bf16"] = src
+        d[wn] = q.reshape(src.shape)
+        d[sn] = s
+    return d
+
+
+def device_weights_from_host(w: dict, inp: dict) -> dict:
+    dt = tdtype(w)
+    d = {"x": up(inp["x"], dt), "w_router": up(inp["w_router"], dt),
+         "router_bias": None if inp.get("router_bias") is None else up(inp["router_bias"])}
+    for key in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"):
+        if key in inp:
+            d[key] = up(inp[key], dt)
+    return _attach_fp8(w, d)
+
+
+def device_weights_generated(w: dict, seed: int = 0) -> dict:
+    """The same tensors as synth.host_inputs, drawn by the device twin of the generator."""
+    dt = tdtype(w)
+    T, H, E, F = w["T"], w["H"], w["E"], w["F"]
+    s = w["w_std"]
+
+    def gen(shape, tid, std):
+        t = torch.empty(shape, dtype=dt, device="cuda")
+        return synth.device_normal(t, seed, tid, std)
+
+    d = {"x": gen((T, H), synth.X, 1.0), "w_router": gen((E, H), synth.W_ROUTER, s),
+         "w_gate": gen((E, F, H), synth.W_GATE, s), "w_up": gen((E, F, H), synth.W_UP, s),
+         "w_down": gen((E, H, F), synth.W_DOWN, s)}
+    d["router_bias"] = up(synth.zipf_bias(seed, E)) if w["zipf"] else None
+    if w["n_shared"]:
+        Fs = w["F_shared"]
+        d["ws_gate"] = gen((Fs, H), synth.WS_GATE, s)
+        d["ws_up"] = gen((Fs, H), synth.WS_UP, s)
+        d["ws_down"] = gen((H, Fs), synth.WS_DOWN, s)
+    return _attach_fp8(w, d)
+
+
+def weights_arg(d: dict) -> dict:
+    return {k: d.get(k) for k in ("w_router", "router_bias", "w_gate", "w_up", "w_down", "s_gate",
+                                  "s_up", "s_down", "ws_gate", "ws_up", "ws_down", "ss_gate",
+                                  "ss_up", "ss_down")}
+
+
+def alloc(w: dict) -> dict:
+    """Buffers of the staged calls."""
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    R = T * k
+    rows = R + (T if w["n_shared"] else 0)
+    dt = tdtype(w)
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    xdt = torch.uint8 if fp8 else dt
+    cfg = cfg_of(w)
+    b = {
+        "cfg": cfg,
+        "ws": torch.zeros(max(moe.moe_workspace_size(cfg), 256) // 4 + 64, dtype=torch.int32, device="cuda"),
+        "logits": torch.empty((T, E), dtype=torch.float32, device="cuda"),
+        "topk_idx": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+        "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+        "counts": torch.empty(E, dtype=torch.int32, device="cuda"),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+        "row_token": torch.empty(R, dtype=torch.int32, device="cuda"),
+        "tok_row": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+        "xd": torch.empty((rows, H), dtype=xdt, device="cuda"),
+        "xd_scale": torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None,
+        "h": torch.empty((rows, F), dtype=xdt, device="cuda"),
+        "h_scale": torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None,
+        "yd": torch.empty((rows, H), dtype=dt, device="cuda"),
+        "y": torch.empty((T, H), dtype=dt, device="cuda"),
+    }
+    moe.moe_workspace_init(b["ws"])
+    return b
+
+
+def run_staged(w: dict, d: dict, b: dict, logits: torch.Tensor | None = None):
+    """S0..S7 through the staged entry points. With ``logits`` given, S0 is skipped and the
+    routing uses those scores."""
+    cfg = b["cfg"]
+    if logits is None:
+        moe.moe_router_logits(cfg, d["x"], d["w_router"], d["router_bias"], b["logits"], b["ws"])
+        logits = b["logits"]
+    moe.moe_route(cfg, logits, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"],
+                  b["row_token"], b["tok_row"], b["ws"])
+    moe.moe_dispatch(cfg, d["x"], b["tok_row"], b["xd"], b["xd_scale"])
+    moe.moe_grouped_mlp(cfg, b["xd"], b["xd_scale"], d["x"], b["offsets"], weights_arg(d),
+                        b["h"], b["h_scale"], b["yd"], b["ws"])
+    moe.moe_combine(cfg, b["yd"], b["tok_row"], b["topk_w"], b["y"])
+    return b
+
+
+def run_forward(w: dict, d: dict):
+    cfg = cfg_of(w)
+    ws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(ws)
+    T, k, E = w["T"], w["k"], w["E"]
+    y = torch.empty((T, w["H"]), dtype=tdtype(w), device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+    moe.moe_forward(cfg, d["x"], weights_arg(d), y, ws, idx, wt, cnt)
+    return y, idx, wt, cnt, ws
+
+
+def np_of(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def routing_ambiguity(w: dict, l_oracle: np.ndarray, delta: float) -> np.ndarray:
+    """Tokens whose top-k selection is not decided by fp32 logits known only to within
+    ``delta`` (the measured |GPU - oracle| logit difference bound): the k-th and (k+1)-th
+    allowed keys are within 2*delta, or (group-limited) the topk_groups-th and next group
+    scores are within delta/2 (sigmoid slope <= 1/4, two scores per group) + 1e-6."""
+    import oracle
+    T, E, k = l_oracle.shape[0], w["E"], w["k"]
+    amb = np.zeros(T, dtype=bool)
+    grouped = w["n_groups"] > 1 and w["topk_groups"] < w["n_groups"]
+    gs = E // w["n_groups"]
+    for t in range(T):
+        row = l_oracle[t]
+        allowed = np.ones(E, dtype=bool)
+        if grouped:
+            sc = oracle.group_scores(row, w["n_groups"], w["group_score"]).astype(np.float64)
+            order = np.argsort(-sc, kind="stable")
+            g = w["topk_groups"]
+            if sc[order[g - 1]] - sc[order[g]] <= delta / 2 + 1e-6:
+                amb[t] = True
+                continue
+            allowed[:] = False
+            for q in order[:g]:
+                allowed[q * gs:(q + 1) * gs] = True
+        keys = np.sort(row[allowed].astype(np.float64))[::-1]
+        if len(keys) > k and keys[k - 1] - keys[k] <= 2 * delta:
+            amb[t] = True
+    return amb

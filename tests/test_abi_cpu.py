@@ -1,0 +1,86 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every entry
+point that include/moe.h declares, and rejects invalid arguments on the host before any
+CUDA call."""
+import os
+import re
+
+import pytest
+
+import token_routing_expert_router_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status_t|const char\*)\s+(moe_\w+)\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe.build()
+    return moe.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("moe_route", "moe_route_from_map", "moe_dispatch", "moe_grouped_mlp", "moe_combine",
+              "moe_forward", "moe_router_logits", "moe_read_status", "moe_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared():
+        assert hasattr(L, n), n
+    assert sorted(moe.exported_symbols()) == declared()
+
+
+def test_no_symbol_outside_header(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", moe._build.LIB], capture_output=True, text=True).stdout
+    exported = sorted({m for m in re.findall(r"\bT (moe_\w+)", out)})
+    assert exported == declared()
+
+
+def cfg(**kw):
+    d = dict(T=64, H=128, E=8, k=2, F=256, act_dtype=moe.BF16)
+    d.update(kw)
+    return moe.MoEConfig.make(**d)
+
+
+def test_workspace_sizes(L):
+    c = cfg()
+    assert moe.moe_workspace_size(c) >= 256
+    assert moe.moe_forward_workspace_size(c) > moe.moe_workspace_size(c)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9), moe.MOE_ERR_INVALID_ARG),
+    (dict(E=6, n_groups=4, topk_groups=2, score_fn=moe.SIGMOID), moe.MOE_ERR_INVALID_ARG),
+    (dict(n_groups=4, topk_groups=5), moe.MOE_ERR_INVALID_ARG),
+    (dict(n_groups=4, topk_groups=2), moe.MOE_ERR_UNSUPPORTED),  # group limit needs sigmoid
+    (dict(E=8, k=4, n_groups=4, topk_groups=1, score_fn=moe.SIGMOID), moe.MOE_ERR_INVALID_ARG),
+    (dict(xfer_dtype=moe.E4M3, act_dtype=moe.F32), moe.MOE_ERR_UNSUPPORTED),
+    (dict(xfer_dtype=moe.E4M3, H=200), moe.MOE_ERR_UNSUPPORTED),
+    (dict(n_shared=1, F_shared=128), moe.MOE_ERR_UNSUPPORTED),
+    (dict(H=100), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=33, E=64), moe.MOE_ERR_UNSUPPORTED),
+])
+def test_invalid_configs_rejected_on_host(L, kw, code):
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_workspace_size(cfg(**kw))
+    assert ei.value.code == code
+
+
+def test_null_and_misaligned_pointers_rejected_on_host(L):
+    import ctypes
+    c = cfg()
+    P = ctypes.c_void_p
+    assert L.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch(ctypes.byref(c), P(4096 + 8), P(4096), P(4096), None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(c), P(4096), P(4096), None, P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(None, None, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_read_status(None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_status_string(moe.MOE_ERR_TIMEOUT).startswith("device")

@@ -1,0 +1,96 @@
+"""S4-S6 (the grouped expert MLP) and S0 (router logits) on the GPU against the oracle, on
+sizes the oracle finishes in seconds that still span several tiles, ragged segment tails,
+empty and hot experts, and the shared expert."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import token_routing_expert_router_gb300 as moe
+from moe_case import alloc, np_of, tdtype, up, weights_arg, device_weights_from_host
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+CASES = [
+    synth.scaled(W["tiny_fp32"], name="tiny_fp32"),
+    synth.scaled(W["mixtral_bf16"], T=600, H=512, F=384, name="mixtral_small"),
+    synth.scaled(W["dsv3_bf16"], T=260, H=512, E=32, F=256, F_shared=256, name="dsv3_small"),
+    synth.scaled(W["imbalanced_bf16"], T=700, H=256, E=32, k=4, F=384, name="imbalanced_small"),
+    synth.scaled(W["dsv3_fp8"], T=300, H=512, E=16, F=256, F_shared=256, n_groups=4,
+                 topk_groups=2, name="fp8_small"),
+]
+
+
+def tol(w):
+    return {synth.F32: 1e-5, synth.BF16: 1e-2}[w["act_dtype"]] if w["xfer_dtype"] != synth.E4M3 else 3e-2
+
+
+def logits_for(w, seed):
+    l = synth.synthetic_logits(seed, w["T"], w["E"])
+    if w["zipf"]:
+        l = (l + 4.0 * synth.zipf_bias(seed, w["E"])).astype(np.float32)  # hot + empty experts
+    return l
+
+
+def routing(w, seed):
+    idx, wt = oracle.route(logits_for(w, seed), w)
+    return idx, wt, oracle.permute(idx, w["E"])
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c["name"] for c in CASES])
+def test_grouped_mlp_against_oracle(w):
+    seed = 4
+    inp = synth.host_inputs(w, seed=seed)
+    idx, wt, (counts, offsets, row_token, tok_row) = routing(w, seed)
+    if w["zipf"]:
+        assert (counts == 0).any() and counts.max() > 3 * counts.mean()
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    T, H, k = w["T"], w["H"], w["k"]
+    R = T * k
+    if fp8:
+        q, s = oracle.quant_blocks(inp["x"], 1, 128)
+        rows = np.concatenate([row_token, np.arange(T)]) if w["n_shared"] else row_token
+        b["xd"].copy_(up(q[rows]))
+        b["xd_scale"].copy_(up(np.ascontiguousarray(s[rows].T)))
+    else:
+        xd = oracle.dispatch(inp["x"], row_token)
+        b["xd"][:R].copy_(up(xd, tdtype(w)))
+    moe.moe_grouped_mlp(b["cfg"], b["xd"], b["xd_scale"], d["x"], up(offsets), weights_arg(d),
+                        b["h"], b["h_scale"], b["yd"], b["ws"])
+    ref = oracle.forward(w, inp, logits=logits_for(w, seed))
+    assert np.array_equal(ref["offsets"], offsets)
+    got = np_of(b["yd"]).astype(np.float64)
+    assert oracle.rel_l2(got[:R], ref["yd"]) < tol(w)
+    for e in range(w["E"]):  # every expert segment on its own (ragged tails included)
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            assert oracle.rel_l2(got[r0:r1], ref["yd"][r0:r1]) < tol(w), e
+    if w["n_shared"]:
+        assert oracle.rel_l2(got[R:], ref["ys"]) < tol(w)
+    assert moe.moe_read_status(b["ws"]) == moe.MOE_OK
+
+
+@pytest.mark.parametrize("w", CASES[:4], ids=[c["name"] for c in CASES[:4]])
+def test_router_logits_against_oracle(w):
+    inp = synth.host_inputs(w, seed=6, with_weights=False)
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    moe.moe_router_logits(b["cfg"], d["x"], d["w_router"], d["router_bias"], b["logits"], b["ws"])
+    ref = oracle.router_logits(inp["x"], inp["w_router"], inp["router_bias"])
+    assert oracle.rel_l2(np_of(b["logits"]), ref) < (1e-5 if w["act_dtype"] == synth.F32 else 1e-4)
+
+
+@pytest.mark.parametrize("name,T,H,E", [("dsv3_router", 1000, 7168, 256), ("imb_router", 2000, 2048, 128),
+                                        ("mixtral_router", 700, 4096, 8)])
+def test_router_logits_real_widths(name, T, H, E):
+    w = synth.workload(name, T, H, E, 2, 128)
+    inp = synth.host_inputs(w, seed=7, with_weights=False)
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    moe.moe_router_logits(b["cfg"], d["x"], d["w_router"], None, b["logits"], b["ws"])
+    ref = oracle.router_logits(inp["x"], inp["w_router"], None)
+    assert oracle.rel_l2(np_of(b["logits"]), ref) < 1e-4

@@ -1,0 +1,359 @@
+// The C ABI (include/moe.h): host-side validation, workspace layout and the stream-ordered
+// sequence of kernels. Nothing here synchronises the host except moe_read_status, and
+// nothing allocates device memory: every buffer is the caller's.
+#include <string.h>
+
+#include "moe_internal.cuh"
+#include "gemm_tc.cuh"
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+
+moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->H <= 0 || c->E < 1 || c->k < 1 || c->F <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->k > 32 || c->E > 512) return MOE_ERR_UNSUPPORTED;
+  if (c->n_groups < 1 || c->E % c->n_groups != 0) return MOE_ERR_INVALID_ARG;
+  if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->group_score != MOE_GROUP_SCORE_TOP2_SUM && c->group_score != MOE_GROUP_SCORE_MAX) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 1 && c->topk_groups < c->n_groups) {
+    if (c->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)c->topk_groups * (c->E / c->n_groups) < c->k) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->act_dtype != MOE_DTYPE_F32 && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->xfer_dtype != c->act_dtype && c->xfer_dtype != MOE_DTYPE_E4M3) return MOE_ERR_INVALID_ARG;
+  if (c->xfer_dtype == MOE_DTYPE_E4M3 && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_UNSUPPORTED;
+  if (c->n_shared && c->F_shared != c->F) return MOE_ERR_UNSUPPORTED;
+  // rows move as 8-element (16-byte bf16) steps in dispatch and combine
+  if (c->H % 8 || c->F % 8) return MOE_ERR_UNSUPPORTED;
+  if (c->xfer_dtype == MOE_DTYPE_E4M3 && (c->H % 128 || c->F % 128)) return MOE_ERR_UNSUPPORTED;
+  if (total_rows(*c) >= (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// T = 0: nothing routed; counts and offsets (if given) become zero.
+moe_status_t empty_routing(const moe_config_t& c, int32_t* counts, int32_t* offsets, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (counts && aligned16(counts)) e = cudaMemsetAsync(counts, 0, (size_t)c.E * 4, s);
+  if (e == cudaSuccess && offsets && aligned16(offsets)) e = cudaMemsetAsync(offsets, 0, (size_t)(c.E + 1) * 4, s);
+  return cuda_status(e);
+}
+
+DeviceStatus* status_of(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); }
+int32_t* blockcnt_of(void* ws) { return reinterpret_cast<int32_t*>((char*)ws + kWsHead); }
+
+size_t route_ws_bytes(const moe_config_t& c) {
+  return kWsHead + align_up((size_t)scan_blocks(c) * c.E * sizeof(int32_t), 256);
+}
+
+size_t act_size(const moe_config_t& c) { return c.act_dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+size_t xfer_size(const moe_config_t& c) {
+  return c.xfer_dtype == MOE_DTYPE_E4M3 ? 1 : act_size(c);
+}
+
+// moe_forward's workspace: the routing part, then every intermediate.
+struct FwdLayout {
+  size_t logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, xd, xd_scale, h, h_scale,
+      yd, total;
+};
+
+FwdLayout fwd_layout(const moe_config_t& c) {
+  FwdLayout L;
+  size_t o = route_ws_bytes(c);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const int64_t Tk = (int64_t)c.T * c.k, rows = total_rows(c);
+  const bool fp8 = c.xfer_dtype == MOE_DTYPE_E4M3;
+  L.logits = take((size_t)c.T * c.E * 4);
+  L.topk_idx = take((size_t)Tk * 4);
+  L.topk_w = take((size_t)Tk * 4);
+  L.counts = take((size_t)c.E * 4);
+  L.offsets = take((size_t)(c.E + 1) * 4);
+  L.row_token = take((size_t)Tk * 4);
+  L.tok_row = take((size_t)Tk * 4);
+  L.xd = take((size_t)rows * c.H * xfer_size(c));
+  L.xd_scale = take(fp8 ? (size_t)rows * (c.H / 128) * 4 : 0);
+  L.h = take((size_t)rows * c.F * xfer_size(c));
+  L.h_scale = take(fp8 ? (size_t)rows * (c.F / 128) * 4 : 0);
+  L.yd = take((size_t)rows * c.H * act_size(c));
+  L.total = o;
+  return L;
+}
+
+moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* w, bool need_router) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (need_router && !ptr_ok(w->w_router)) return MOE_ERR_INVALID_ARG;
+  if (w->router_bias && !aligned16(w->router_bias)) return MOE_ERR_INVALID_ARG;
+  if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up) || !ptr_ok(w->w_down)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = c.xfer_dtype == MOE_DTYPE_E4M3;
+  if (fp8 && (!ptr_ok(w->s_gate) || !ptr_ok(w->s_up) || !ptr_ok(w->s_down))) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared) {
+    if (!ptr_ok(w->ws_gate) || !ptr_ok(w->ws_up) || !ptr_ok(w->ws_down)) return MOE_ERR_INVALID_ARG;
+    if (fp8 && (!ptr_ok(w->ss_gate) || !ptr_ok(w->ss_up) || !ptr_ok(w->ss_down))) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+cudaError_t router_logits(const moe_config_t& c, const void* x, const void* w_router,
+                          const float* bias, float* logits, DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  if (c.act_dtype == MOE_DTYPE_BF16 && tc::router_supported(c))
+    return tc::launch_router(c, x, w_router, bias, logits, st, s);
+  SimtGemmArgs a{};
+  a.mode = 0;
+  a.act_bf16 = c.act_dtype == MOE_DTYPE_BF16;
+  a.M_static = c.T;
+  a.A = x;
+  a.B0 = w_router;
+  a.bias = bias;
+  a.C = logits;
+  a.N = c.E;
+  a.K = c.H;
+  return launch_simt_gemm(a, s);
+}
+
+cudaError_t grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
+                        const void* x, const int32_t* offsets, const moe_weights_t& w, void* h,
+                        float* h_scale, void* yd, DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  if (tc::mlp_supported(c))
+    return tc::launch_grouped_mlp(c, xd, xd_scale, x, offsets, w, h, h_scale, yd, st, s);
+  // exact-fp32 FFMA path (fp32 layers, and bf16 shapes the tensor-core tiles do not take)
+  const int64_t R = routed_rows(c);
+  SimtGemmArgs a{};
+  a.act_bf16 = c.act_dtype == MOE_DTYPE_BF16;
+  a.M_static = -1;
+  a.offsets = offsets;
+  a.G = c.E;
+  a.extra_group = c.n_shared ? 1 : 0;
+  a.routed_rows = R;
+  a.T_extra = c.T;
+  // gate/up: h = silu(xd Wg^T) * (xd Wu^T)
+  a.mode = 1;
+  a.A = xd;
+  a.A_extra = x;
+  a.B0 = w.w_gate;
+  a.B1 = w.w_up;
+  a.B0_extra = w.ws_gate;
+  a.B1_extra = w.ws_up;
+  a.C = h;
+  a.N = c.F;
+  a.K = c.H;
+  cudaError_t e = launch_simt_gemm(a, s);
+  if (e != cudaSuccess) return e;
+  // down: yd = h Wd^T
+  a.mode = 2;
+  a.A = h;
+  a.A_extra = (const char*)h + (size_t)R * c.F * act_size(c);
+  a.B0 = w.w_down;
+  a.B1 = nullptr;
+  a.B0_extra = w.ws_down;
+  a.B1_extra = nullptr;
+  a.C = yd;
+  a.N = c.H;
+  a.K = c.F;
+  return launch_simt_gemm(a, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = route_ws_bytes(*cfg);
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = fwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* ws, moe_stream_t stream) {
+  if (!ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), (cudaStream_t)stream));
+}
+
+moe_status_t moe_router_logits(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* router_bias, float* logits, void* ws,
+                               moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(w_router) || !ptr_ok(logits) || !ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(router_logits(*cfg, x, w_router, router_bias, logits, status_of(ws),
+                                   (cudaStream_t)stream));
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* topk_idx,
+                       float* topk_w, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                       int32_t* tok_row, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return empty_routing(*cfg, counts, offsets, (cudaStream_t)stream);
+  if (!ptr_ok(logits) || !ptr_ok(topk_idx) || !ptr_ok(topk_w) || !ptr_ok(counts) ||
+      !ptr_ok(offsets) || !ptr_ok(row_token) || !ptr_ok(tok_row) || !ptr_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_route_topk(*cfg, logits, topk_idx, topk_w, status_of(ws), s);
+  if (e == cudaSuccess)
+    e = launch_route_scan(*cfg, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
+                          status_of(ws), s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx,
+                                int32_t* counts, int32_t* offsets, int32_t* row_token,
+                                int32_t* tok_row, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return empty_routing(*cfg, counts, offsets, (cudaStream_t)stream);
+  if (!ptr_ok(topk_idx) || !ptr_ok(counts) || !ptr_ok(offsets) || !ptr_ok(row_token) ||
+      !ptr_ok(tok_row) || !ptr_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route_scan(*cfg, topk_idx, counts, offsets, row_token, tok_row,
+                                       blockcnt_of(ws), status_of(ws), (cudaStream_t)stream));
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* tok_row,
+                          void* xd, float* xd_scale, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(tok_row) || !ptr_ok(xd)) return MOE_ERR_INVALID_ARG;
+  if (cfg->xfer_dtype == MOE_DTYPE_E4M3 && !ptr_ok(xd_scale)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch(*cfg, x, tok_row, xd, xd_scale, (cudaStream_t)stream));
+}
+
+moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const float* xd_scale,
+                             const void* x, const int32_t* offsets, const moe_weights_t* w,
+                             void* h, float* h_scale, void* yd, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  v = check_weights(*cfg, w, false);
+  if (v != MOE_OK) return v;
+  const bool fp8 = cfg->xfer_dtype == MOE_DTYPE_E4M3;
+  if (!ptr_ok(xd) || !ptr_ok(offsets) || !ptr_ok(h) || !ptr_ok(yd) || !ptr_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!ptr_ok(xd_scale) || !ptr_ok(h_scale))) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared && !fp8 && !ptr_ok(x)) return MOE_ERR_INVALID_ARG;
+  if (fp8 && !tc::mlp_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(grouped_mlp(*cfg, xd, xd_scale, x, offsets, *w, h, h_scale, yd,
+                                 status_of(ws), (cudaStream_t)stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* tok_row,
+                         const float* topk_w, void* y, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(yd) || !ptr_ok(tok_row) || !ptr_ok(topk_w) || !ptr_ok(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*cfg, yd, tok_row, topk_w, y, (cudaStream_t)stream));
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                         void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
+                         int32_t* counts_out, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  v = check_weights(*cfg, w, true);
+  if (v != MOE_OK) return v;
+  if (!ptr_ok(x) || !ptr_ok(y) || !ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  if ((topk_idx_out && !aligned16(topk_idx_out)) || (topk_w_out && !aligned16(topk_w_out)) ||
+      (counts_out && !aligned16(counts_out)))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  if (c.xfer_dtype == MOE_DTYPE_E4M3 && !tc::mlp_supported(c)) return MOE_ERR_UNSUPPORTED;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  const FwdLayout L = fwd_layout(c);
+  char* base = (char*)ws;
+  float* logits = (float*)(base + L.logits);
+  int32_t* topk_idx = (int32_t*)(base + L.topk_idx);
+  float* topk_w = (float*)(base + L.topk_w);
+  int32_t* counts = (int32_t*)(base + L.counts);
+  int32_t* offsets = (int32_t*)(base + L.offsets);
+  int32_t* row_token = (int32_t*)(base + L.row_token);
+  int32_t* tok_row = (int32_t*)(base + L.tok_row);
+  void* xd = base + L.xd;
+  float* xd_scale = c.xfer_dtype == MOE_DTYPE_E4M3 ? (float*)(base + L.xd_scale) : nullptr;
+  void* h = base + L.h;
+  float* h_scale = c.xfer_dtype == MOE_DTYPE_E4M3 ? (float*)(base + L.h_scale) : nullptr;
+  void* yd = base + L.yd;
+
+  cudaError_t e = router_logits(c, x, w->w_router, w->router_bias, logits, status_of(ws), s);
+  if (e == cudaSuccess) e = launch_route_topk(c, logits, topk_idx, topk_w, status_of(ws), s);
+  if (e == cudaSuccess)
+    e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
+                          status_of(ws), s);
+  if (e == cudaSuccess) e = launch_dispatch(c, x, tok_row, xd, xd_scale, s);
+  if (e == cudaSuccess)
+    e = grouped_mlp(c, xd, xd_scale, x, offsets, *w, h, h_scale, yd, status_of(ws), s);
+  if (e == cudaSuccess) e = launch_combine(c, yd, tok_row, topk_w, y, s);
+  const size_t Tk = (size_t)c.T * c.k;
+  if (e == cudaSuccess && topk_idx_out)
+    e = cudaMemcpyAsync(topk_idx_out, topk_idx, Tk * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && topk_w_out)
+    e = cudaMemcpyAsync(topk_w_out, topk_w, Tk * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && counts_out)
+    e = cudaMemcpyAsync(counts_out, counts, (size_t)c.E * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols, int32_t br,
+                               int32_t bc, uint8_t* q, float* scale, moe_stream_t stream) {
+  if (!ptr_ok(src_bf16) || !ptr_ok(q) || !ptr_ok(scale) || rows < 0 || cols < 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((br != 1 && br != 128) || (bc != 1 && bc != 128)) return MOE_ERR_UNSUPPORTED;
+  if (ceil_div(rows, br) * ceil_div(cols, bc) > (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_quantize_e4m3(src_bf16, rows, cols, br, bc, q, scale, (cudaStream_t)stream));
+}
+
+moe_status_t moe_read_status(void* ws, moe_stream_t stream, int32_t* device_status) {
+  if (!ptr_ok(ws) || !device_status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus h{};
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(h), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *device_status = h.code;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_BAD_INPUT: return "device: bad input (expert id out of range, repeated id or non-finite score)";
+    case MOE_ERR_TIMEOUT: return "device: bounded wait expired";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

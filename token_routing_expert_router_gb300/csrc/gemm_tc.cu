@@ -1,0 +1,481 @@
+// The grouped expert GEMMs and the router GEMM on the 5th-generation tensor cores.
+//
+// "Grouped GEMM" runs all experts' GEMMs in one kernel to fill the tensor cores, and the
+// kernels read the dynamic per-expert shapes from device memory instead of synchronising
+// with the host ("Scalable Training of Mixture-of-Experts Models with Megatron Core"
+// summary, section 2.4). Here that is one persistent kernel per GEMM:
+//   * warp 0: TMA producer (128-byte-swizzled K-major tiles into a ring of smem stages);
+//   * warp 1: TMEM owner and the single thread issuing tcgen05.mma (M = 128, N = BN);
+//   * warps 2-5: epilogue, one TMEM lane (= one output row) per thread, two TMEM
+//     accumulators so a tile's epilogue overlaps the next tile's main loop.
+// Tiles are ordered group-major, then N tile, then M tile (fastest), so CTAs running at the
+// same time share each weight tile through L2 and empty groups produce no tiles; a hot
+// group's many M tiles spread over every SM. Ragged segment tails are handled by loading
+// the full 128-row box (rows past the segment belong to the next group or are zero-filled
+// past the end of the tensor) and storing only the segment's rows.
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
+#include "tc_common.cuh"
+
+namespace moe {
+namespace tc {
+namespace {
+
+constexpr int BM = 128;            // rows per tile (TMEM lanes)
+constexpr int BK = 64;             // bf16 K per stage: one 128-byte swizzle row
+constexpr int kThreads = 192;      // 6 warps
+constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group + 1
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+
+enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2 };
+
+struct TcParams {
+  const int32_t* offsets;   // [G+1] routed segment starts (device); may be null when G = 0
+  int G;                    // routed groups
+  int has_extra;            // one more group of T_extra rows (shared expert, or the router's
+  int T_extra;              //   single problem), A from tmA2 at row a2_row_base
+  int a2_row_base;
+  int64_t out_extra_base;   // output row of the extra group's row 0
+  int K;                    // reduction length, multiple of BK
+  int n_tiles;              // N tiles per group
+  int b_group_rows;         // rows of B per routed group
+  int ldc;                  // output row length in elements
+  void* out;
+  const float* bias;        // EPI_STORE_F32_BIAS: [N] or null
+  DeviceStatus* status;
+  uint64_t timeout_ns;
+};
+
+template <int BN>
+struct Smem {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = BM * BK * 2;          // 16 KB
+  static constexpr int kBBytes = BN * BK * 2;          // 32 KB (BN 256) / 16 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;             // two accumulators
+  static constexpr size_t kBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + 256 /*barriers*/ +
+                                   2 * kMaxGroups * sizeof(int32_t);
+};
+
+// Tile -> (group, m tile, n tile) from the block's copy of the m-tile prefix.
+struct TileCoord {
+  int g, mb, nb, rows;  // rows: valid rows of this tile (<= BM)
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
+                                                 const int32_t* seg_rows) {
+  // largest g with n_tiles * mt_prefix[g] <= tile
+  int lo = 0, hi = ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileCoord c;
+  c.g = lo;
+  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
+  const int local = tile - n_tiles * mt_prefix[lo];
+  c.nb = local / mt;
+  c.mb = local - c.nb * mt;
+  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  return c;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmB1x,
+                        const TcParams p) {
+  using S = Smem<BN>;
+  constexpr int STAGES = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * S::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* mt_prefix = reinterpret_cast<int32_t*>(bars + 32);  // [ngroups + 1]
+  int32_t* seg_rows = mt_prefix + kMaxGroups;                 // [ngroups]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = p.G + p.has_extra;
+
+  // ---- per-block setup: barriers, TMEM, and the m-tile prefix over the groups
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (EPI == EPI_SWIGLU_BF16) tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (warp == 2) {
+    // rows per group and an exclusive prefix of ceil(rows / BM), 32 groups per step
+    int carry = 0;
+    for (int g0 = 0; g0 < ngroups; g0 += 32) {
+      const int g = g0 + lane;
+      int rows = 0;
+      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
+      else if (g < ngroups) rows = p.T_extra;
+      const int mt = (rows + BM - 1) / BM;
+      int inc = mt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      if (g < ngroups) {
+        seg_rows[g] = rows;
+        mt_prefix[g] = carry + inc - mt;
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) mt_prefix[ngroups] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.n_tiles * mt_prefix[ngroups];
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ======================= TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+        const bool extra = c.g >= p.G;
+        const CUtensorMap* ta = extra ? &tmA2 : &tmA;
+        const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
+        const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
+        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * BM;
+        const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;
+        const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+          uint8_t* a_dst = sA + stage * S::kABytes;
+          uint8_t* b_dst = sB + stage * S::kBBytes;
+          tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+          if (EPI == EPI_SWIGLU_BF16) {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
+            tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows
+          } else {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // tail: every stage's last fill has been consumed (so no TMA write or MMA commit
+      // is still in flight when the block exits); after an abort, only wait for the loads
+      const int used = issued < STAGES ? (int)issued : STAGES;
+      for (int i = 0; i < used; ++i) {
+        // slot (stage - 1 - i) mod STAGES holds fill number issued - 1 - i
+        const int s = (stage - 1 - i + 2 * STAGES) % STAGES;
+        const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
+        if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
+        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_make(1u /*bf16*/, BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_addr(sA + stage * S::kABytes);
+          const uint32_t b_addr = smem_addr(sB + stage * S::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {  // K = 16 per instruction: +32 bytes in the row
+            mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc,
+                     (kb | k) != 0);
+          }
+          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      mma_commit(drain);  // completes when every MMA above has
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    }
+  } else {
+    // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+      bool ok = mbar_wait(&tfull[acc], acc_phase, abort, p.timeout_ns, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool extra = c.g >= p.G;
+      const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * BM + row_in_tile;
+      const bool live = row_in_tile < c.rows;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (EPI == EPI_SWIGLU_BF16) {
+        // cols [0, BN/2) gate, [BN/2, BN) up -> BN/2 columns of h
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * (BN / 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(t_row + c0, g);
+          tmem_ld32(t_row + BN / 2 + c0, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+            const float h1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          }
+        }
+      } else if (EPI == EPI_STORE_BF16) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_row + c0, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      } else {
+        float* out = reinterpret_cast<float*>(p.out) + out_row * p.ldc + c.nb * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_row + c0, v);
+          tmem_ld_wait();
+          if (live) {
+            float4* dst = reinterpret_cast<float4*>(out + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 f = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+              if (p.bias) {
+                const int n = c.nb * BN + c0 + 4 * q;
+                f.x += p.bias[n]; f.y += p.bias[n + 1]; f.z += p.bias[n + 2]; f.w += p.bias[n + 3];
+              }
+              dst[q] = f;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major [rows, cols] matrix, box of box_rows x box_cols, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows, uint64_t cols,
+               uint32_t box_rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, box_rows, BK);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int BN, int EPI>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
+                   const CUtensorMap& b0x, const CUtensorMap& b1x, const TcParams& p, int64_t max_tiles,
+                   cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  auto kern = tc_gemm_bf16_kernel<BN, EPI>;
+  const size_t smem = Smem<BN>::kBytes;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+  kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool router_supported(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && (c.E == 128 || c.E == 256) && c.H % BK == 0;
+}
+
+bool mlp_supported(const moe_config_t& c) {
+  if (c.act_dtype != MOE_DTYPE_BF16 || c.xfer_dtype != MOE_DTYPE_BF16) return false;
+  return c.H % 128 == 0 && c.F % 128 == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router, const float* bias,
+                          float* logits, DeviceStatus* st, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_bf16(&ta, x, c.T, c.H, BM) || !make_bf16(&tb, w_router, c.E, c.H, c.E)) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.G = 0;
+  p.has_extra = 1;
+  p.T_extra = c.T;
+  p.a2_row_base = 0;
+  p.out_extra_base = 0;
+  p.K = c.H;
+  p.n_tiles = 1;
+  p.b_group_rows = 0;
+  p.ldc = c.E;
+  p.out = logits;
+  p.bias = bias;
+  p.timeout_ns = kTimeoutNs;
+  p.status = st;
+  const int64_t tiles = ceil_div(c.T, BM);
+  if (c.E == 256) return launch<256, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
+  return launch<128, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
+}
+
+cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float*, const void* x,
+                               const int32_t* offsets, const moe_weights_t& w, void* h, float*, void* yd,
+                               DeviceStatus* st, cudaStream_t s) {
+  const int64_t R = routed_rows(c), rows = total_rows(c);
+  const bool shared = c.n_shared != 0;
+  // ---- GEMM1: h = silu(A Wg^T) * (A Wu^T), tiles of 128 h columns (256 B rows)
+  CUtensorMap a1, a1x, bg, bu, bgx, bux;
+  bool ok = make_bf16(&a1, xd, rows, c.H, BM) && make_bf16(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
+            make_bf16(&bu, w.w_up, (uint64_t)c.E * c.F, c.H, 128);
+  if (shared) {
+    ok = ok && make_bf16(&a1x, x, c.T, c.H, BM) && make_bf16(&bgx, w.ws_gate, c.F, c.H, 128) &&
+         make_bf16(&bux, w.ws_up, c.F, c.H, 128);
+  } else {
+    a1x = a1; bgx = bg; bux = bu;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.offsets = offsets;
+  p.G = c.E;
+  p.has_extra = shared ? 1 : 0;
+  p.T_extra = c.T;
+  p.a2_row_base = 0;
+  p.out_extra_base = R;
+  p.K = c.H;
+  p.n_tiles = c.F / 128;
+  p.b_group_rows = c.F;
+  p.ldc = c.F;
+  p.out = h;
+  p.status = st;
+  p.timeout_ns = kTimeoutNs;
+  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  cudaError_t e = launch<256, EPI_SWIGLU_BF16>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  if (e != cudaSuccess) return e;
+  // ---- GEMM2: yd = h Wd^T (the shared expert's h rows follow the routed ones)
+  const int bn2 = c.H % 256 == 0 ? 256 : 128;
+  CUtensorMap a2, bd, bdx;
+  ok = make_bf16(&a2, h, rows, c.F, BM) && make_bf16(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, bn2);
+  if (shared) ok = ok && make_bf16(&bdx, w.ws_down, c.H, c.F, bn2);
+  else bdx = bd;
+  if (!ok) return cudaErrorInvalidValue;
+  p.a2_row_base = (int)R;
+  p.K = c.F;
+  p.n_tiles = c.H / bn2;
+  p.b_group_rows = c.H;
+  p.ldc = c.H;
+  p.out = yd;
+  if (bn2 == 256) return launch<256, EPI_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  return launch<128, EPI_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+}
+
+}  // namespace tc
+}  // namespace moe

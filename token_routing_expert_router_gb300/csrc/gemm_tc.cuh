@@ -1,0 +1,22 @@
+// Tensor-core (tcgen05 / TMEM / TMA) paths of the router logits and the grouped expert MLP.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace tc {
+
+// Shapes the tcgen05 kernels take (bf16 activations; E4M3 transfer when configured).
+bool router_supported(const moe_config_t& c);
+bool mlp_supported(const moe_config_t& c);
+
+cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router,
+                          const float* bias, float* logits, DeviceStatus* st, cudaStream_t s);
+
+cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
+                               const void* x, const int32_t* offsets, const moe_weights_t& w,
+                               void* h, float* h_scale, void* yd, DeviceStatus* st,
+                               cudaStream_t s);
+
+}  // namespace tc
+}  // namespace moe

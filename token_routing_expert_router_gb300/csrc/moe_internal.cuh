@@ -1,0 +1,76 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Workspace layout. The head (256 B) holds the device status word; the routing scan's
+// per-block expert counts follow. moe_forward's intermediates come after that.
+// ---------------------------------------------------------------------------------------
+constexpr size_t kWsHead = 256;
+constexpr int kScanChunk = 128;  // tokens per block of the counting pass
+
+struct DeviceStatus {
+  int32_t code;    // first error wins (atomicCAS from 0)
+  int32_t detail;  // e.g. the offending token
+};
+
+__device__ __forceinline__ void set_status(DeviceStatus* st, int32_t code, int32_t detail) {
+  if (atomicCAS(&st->code, 0, code) == 0) st->detail = detail;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int64_t routed_rows(const moe_config_t& c) { return (int64_t)c.T * c.k; }
+inline int64_t total_rows(const moe_config_t& c) { return (int64_t)c.T * c.k + (c.n_shared ? c.T : 0); }
+inline int scan_blocks(const moe_config_t& c) { return (int)ceil_div(c.T, kScanChunk); }
+
+// ---------------------------------------------------------------------------------------
+// Kernel launchers (one translation unit each; all stream-ordered, no host sync).
+// ---------------------------------------------------------------------------------------
+cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_t* topk_idx,
+                              float* topk_w, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
+                              int32_t* offsets, int32_t* row_token, int32_t* tok_row,
+                              int32_t* blockcnt, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_dispatch(const moe_config_t& c, const void* x, const int32_t* tok_row,
+                            void* xd, float* xd_scale, cudaStream_t s);
+cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t* tok_row,
+                           const float* topk_w, void* y, cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const void* src, int64_t rows, int64_t cols, int br, int bc,
+                                 uint8_t* q, float* scale, cudaStream_t s);
+
+// SIMT grouped GEMM (fp32 FFMA): C = A . B^T per group, with optional SwiGLU pair.
+// Groups: routed experts g < E over rows [offsets[g], offsets[g+1]) of A, plus an optional
+// extra group (shared expert) over rows [0, T) of A2 written at output row R + t.
+struct SimtGemmArgs {
+  int mode;             // 0: C fp32 (+ bias over columns), 1: SwiGLU -> act, 2: store act
+  int act_bf16;         // element type of A, B and the act output: 1 bf16, 0 fp32
+  int M_static;         // rows of a single-group problem (router: T); -1 for grouped
+  const int32_t* offsets;  // [G+1] device (grouped)
+  int G;                // routed groups
+  int extra_group;      // 1: shared expert group present
+  int64_t routed_rows;  // R = T*k: rows of A covered by the G groups; the extra group's
+                        // output rows start at R
+  const void* A;        // [rows, K]
+  const void* A_extra;  // [T, K] shared-expert A (may equal A + R*K)
+  int T_extra;          // rows of the extra group
+  const void* B0;       // [G, N, K] (mode 1: gate), or [N, K] single
+  const void* B1;       // mode 1: up [G, N, K]
+  const void* B0_extra; // shared expert weights [N, K]
+  const void* B1_extra;
+  const float* bias;    // mode 0: [N] or NULL
+  void* C;              // [rows, N]
+  int N, K;
+};
+cudaError_t launch_simt_gemm(const SimtGemmArgs& a, cudaStream_t s);
+
+}  // namespace moe

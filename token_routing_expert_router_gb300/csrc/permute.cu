@@ -1,0 +1,227 @@
+// S3 dispatch and S7 combine: the on-device form of the dispatch and combine operators
+// (Hybrid-EP article: dispatch sends each token only where the routing map says; combine
+// brings the expert outputs back with high-precision accumulation). Both walk tokens, so
+// x is read once on the way out and y written once on the way back; rows move as 16-byte
+// vectors. Also the block quantiser of the FP8-dispatch variant.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxVec = 8;  // 16-byte vectors held per thread per pass
+
+// xd[tok_row[t, j]] = x[t] for j < k. One block per token; nvec = 16-byte vectors per row.
+__global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x, int nvec,
+                                                            int k, const int32_t* __restrict__ tok_row,
+                                                            uint4* __restrict__ xd) {
+  __shared__ int32_t rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
+  __syncthreads();
+  const uint4* src = x + (int64_t)t * nvec;
+  for (int base = 0; base < nvec; base += kThreads * kMaxVec) {
+    uint4 v[kMaxVec];
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i) {
+      const int idx = base + i * kThreads + threadIdx.x;
+      if (idx < nvec) v[i] = __ldg(src + idx);
+    }
+    for (int j = 0; j < k; ++j) {
+      uint4* dst = xd + (int64_t)rows[j] * nvec;
+#pragma unroll
+      for (int i = 0; i < kMaxVec; ++i) {
+        const int idx = base + i * kThreads + threadIdx.x;
+        if (idx < nvec) dst[idx] = v[i];
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// e4m3 (round to nearest even, finite values beyond 448 saturate) of four floats, packed
+// little-endian (first value in the lowest byte).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// FP8 dispatch: each token quantised once in 1x128 blocks (one warp per block, four values
+// per lane), written to its k rows and, with a shared expert, to row R + t.
+__global__ void __launch_bounds__(256) dispatch_e4m3_kernel(
+    const uint2* __restrict__ x, int H, int k, int64_t R, int64_t rows_total, int shared,
+    const int32_t* __restrict__ tok_row, uint8_t* __restrict__ xd, float* __restrict__ xd_scale) {
+  __shared__ int32_t rows[33];
+  const int t = blockIdx.x;
+  const int nrows = k + shared;
+  if (threadIdx.x < k) rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
+  if (threadIdx.x == 0 && shared) rows[k] = (int32_t)(R + t);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int nb = H / 128;
+  for (int b = warp; b < nb; b += nwarps) {
+    const uint2 u = __ldg(x + ((int64_t)t * H + b * 128) / 4 + lane);
+    const float v0 = bf16_lo(u.x), v1 = bf16_hi(u.x), v2 = bf16_lo(u.y), v3 = bf16_hi(u.y);
+    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float scale = 1.0f;
+    uint32_t q = 0;
+    if (amax > 0.0f) {
+      scale = __fdiv_rn(amax, 448.0f);
+      const float rs = __fdiv_rn(448.0f, amax);
+      q = e4m3x4(__fmul_rn(v0, rs), __fmul_rn(v1, rs), __fmul_rn(v2, rs), __fmul_rn(v3, rs));
+    }
+    for (int j = 0; j < nrows; ++j) {
+      const int64_t r = rows[j];
+      reinterpret_cast<uint32_t*>(xd + r * H + b * 128)[lane] = q;
+      if (lane == 0) xd_scale[(int64_t)b * rows_total + r] = scale;
+    }
+  }
+}
+
+// y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ yd[R+t]), fp32 in fixed j order, one rounding
+// to the output type. One block per token, 8 elements per thread per step.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const void* __restrict__ yd_, int H, int k,
+                                                           const int32_t* __restrict__ tok_row,
+                                                           const float* __restrict__ topk_w,
+                                                           int shared, int64_t R, void* __restrict__ y_) {
+  __shared__ int32_t rows[32];
+  __shared__ float wts[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int n8 = H / 8;
+  for (int c = threadIdx.x; c < n8; c += kThreads) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k + shared; j0 += 8) {
+      float v[8][8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        if (j < k + shared) {
+          const int64_t r = (j < k) ? rows[j] : R + t;
+          if (BF16) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(yd_) + (r * H) / 8 + c);
+            v[jj][0] = bf16_lo(u.x); v[jj][1] = bf16_hi(u.x);
+            v[jj][2] = bf16_lo(u.y); v[jj][3] = bf16_hi(u.y);
+            v[jj][4] = bf16_lo(u.z); v[jj][5] = bf16_hi(u.z);
+            v[jj][6] = bf16_lo(u.w); v[jj][7] = bf16_hi(u.w);
+          } else {
+            const float4* p = reinterpret_cast<const float4*>(yd_) + (r * H) / 4 + 2 * c;
+            const float4 a = __ldg(p), b = __ldg(p + 1);
+            v[jj][0] = a.x; v[jj][1] = a.y; v[jj][2] = a.z; v[jj][3] = a.w;
+            v[jj][4] = b.x; v[jj][5] = b.y; v[jj][6] = b.z; v[jj][7] = b.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        if (j < k) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(wts[j], v[jj][i], acc[i]);
+        } else if (j < k + shared) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], v[jj][i]);
+        }
+      }
+    }
+    if (BF16) {
+      uint4 o;
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&p0);
+      o.y = *reinterpret_cast<uint32_t*>(&p1);
+      o.z = *reinterpret_cast<uint32_t*>(&p2);
+      o.w = *reinterpret_cast<uint32_t*>(&p3);
+      reinterpret_cast<uint4*>(y_)[((int64_t)t * H) / 8 + c] = o;
+    } else {
+      float4* p = reinterpret_cast<float4*>(y_) + ((int64_t)t * H) / 4 + 2 * c;
+      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
+// Block quantisation of a bf16 matrix (br x bc blocks) with the dispatch rule.
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                                       int64_t cols, int br, int bc, uint8_t* __restrict__ q,
+                                                       float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int64_t nbc = ceil_div(cols, bc);
+  const int64_t r0 = (blockIdx.x / nbc) * br, c0 = (blockIdx.x % nbc) * bc;
+  const int64_t r1 = min(r0 + br, rows), c1 = min(c0 + bc, cols);
+  const int64_t w = c1 - c0, n = (r1 - r0) * w;
+  float amax = 0.0f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t r = r0 + i / w, c = c0 + i % w;
+    amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[r * cols + c] << 16)));
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.0f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+  const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const float rs = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 0.0f;
+  if (threadIdx.x == 0) scale[blockIdx.x] = sc;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t r = r0 + i / w, c = c0 + i % w;
+    const float v = __uint_as_float((uint32_t)src[r * cols + c] << 16);
+    const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fmul_rn(v, rs), __NV_SATFINITE, __NV_E4M3);
+    q[r * cols + c] = amax > 0.0f ? (uint8_t)code : (uint8_t)0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_config_t& c, const void* x, const int32_t* tok_row,
+                            void* xd, float* xd_scale, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  if (c.xfer_dtype == MOE_DTYPE_E4M3) {
+    dispatch_e4m3_kernel<<<c.T, 256, 0, s>>>(reinterpret_cast<const uint2*>(x), c.H, c.k,
+                                             routed_rows(c), total_rows(c), c.n_shared ? 1 : 0,
+                                             tok_row, reinterpret_cast<uint8_t*>(xd), xd_scale);
+  } else {
+    const int esize = c.act_dtype == MOE_DTYPE_BF16 ? 2 : 4;
+    const int nvec = c.H * esize / 16;
+    dispatch_kernel<<<c.T, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), nvec, c.k, tok_row,
+                                              reinterpret_cast<uint4*>(xd));
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t* tok_row,
+                           const float* topk_w, void* y, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int shared = c.n_shared ? 1 : 0;
+  if (c.act_dtype == MOE_DTYPE_BF16)
+    combine_kernel<true><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, shared, routed_rows(c), y);
+  else
+    combine_kernel<false><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, shared, routed_rows(c), y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e4m3(const void* src, int64_t rows, int64_t cols, int br, int bc,
+                                 uint8_t* q, float* scale, cudaStream_t s) {
+  const int64_t nblk = ceil_div(rows, br) * ceil_div(cols, bc);
+  if (nblk == 0) return cudaSuccess;
+  quantize_kernel<<<(unsigned)nblk, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(src), rows, cols,
+                                                 br, bc, q, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,350 @@
+// S1 (score + top-k, group-limited selection, weights) and S2 (per-expert counts, offsets
+// and the stable permutation) of the MoE layer forward.
+//
+// The router activates k experts per token ("Scalable Training of Mixture-of-Experts Models
+// with Megatron Core" summary, "O essencial"); the dispatch follows "the routing map"
+// (Hybrid-EP article); the per-expert shapes stay in device memory so no host sync is
+// needed (Megatron-Core summary, section 2.4, device-initiated kernels).
+#include <float.h>
+#include <limits.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Deterministic fp32 exp: Cody-Waite reduction by ln 2 split into a 16-bit head and a
+// tail, a degree-7 Taylor polynomial of e^r (|r| <= ln2/2) by Horner with fused
+// multiply-adds, and a two-step power-of-two scaling. Written with explicit round-to-
+// nearest intrinsics so that no contraction or fast path changes a bit: any IEEE machine
+// running the same operations gets the same result, which is what lets group-limited
+// routing decide the same groups everywhere. Constants are the fp32 bit patterns of
+// 1/ln2, ln2 (head, tail) and 1/i!.
+__device__ __forceinline__ float det_exp(float a) {
+  if (a != a) return a;
+  if (a > __int_as_float(0x42b17218)) return __int_as_float(0x7f800000);  // > 88.7228...
+  if (a < __int_as_float(0xc2cff1b5)) return 0.0f;                        // < -103.972...
+  const float n = rintf(__fmul_rn(a, __int_as_float(0x3fb8aa3b)));
+  float r = __fmaf_rn(-n, __int_as_float(0x3f317200), a);
+  r = __fmaf_rn(-n, __int_as_float(0x35bfbe8e), r);
+  float p = __int_as_float(0x39500d01);             // 1/7!
+  p = __fmaf_rn(p, r, __int_as_float(0x3ab60b61));  // 1/6!
+  p = __fmaf_rn(p, r, __int_as_float(0x3c088889));  // 1/5!
+  p = __fmaf_rn(p, r, __int_as_float(0x3d2aaaab));  // 1/4!
+  p = __fmaf_rn(p, r, __int_as_float(0x3e2aaaab));  // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int ni = (int)n;
+  const int n1 = ni >> 1, n2 = ni - n1;
+  return __fmul_rn(__fmul_rn(p, __int_as_float((n1 + 127) << 23)), __int_as_float((n2 + 127) << 23));
+}
+
+__device__ __forceinline__ float det_sigmoid(float l) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, det_exp(-l)));
+}
+
+// (key, idx) order: larger key first, equal keys to the lower index.
+__device__ __forceinline__ bool better(float k1, int i1, float k2, int i2) {
+  return k1 > k2 || (k1 == k2 && i1 < i2);
+}
+
+__device__ __forceinline__ void warp_argmax(float& key, int& idx) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float ok = __shfl_xor_sync(kFull, key, off);
+    const int oi = __shfl_xor_sync(kFull, idx, off);
+    if (better(ok, oi, key, idx)) { key = ok; idx = oi; }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
+  return v;
+}
+
+// One warp per token. Lane l holds experts l, l+32, l+64, ... (NSLOT slots).
+template <int NSLOT>
+__global__ void __launch_bounds__(256) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G,
+    int g_keep, int group_score, float rho, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, DeviceStatus* st) {
+  extern __shared__ float s_score[];  // [warps][E] sigmoid scores (group-limited only)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  const float* row = logits + (int64_t)t * E;
+
+  float v[NSLOT];
+  uint32_t ok = 0;
+  bool bad = false;
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) {
+    const int e = s * 32 + lane;
+    v[s] = -FLT_MAX;
+    if (e < E) {
+      float x = row[e];
+      if (!isfinite(x)) { bad = true; x = -FLT_MAX; }
+      v[s] = x;
+      ok |= 1u << s;
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0) set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t);
+
+  uint32_t allowed = ok;
+  if (G > 1 && g_keep < G) {
+    float* sc = s_score + (size_t)warp * E;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s)
+      if (ok >> s & 1) sc[s * 32 + lane] = det_sigmoid(v[s]);
+    __syncwarp();
+    const int gs = E / G;
+    float gkey = -INFINITY;
+    int gidx = INT_MAX;
+    if (lane < G) {
+      float m1 = -INFINITY, m2 = -INFINITY;  // the two largest scores of the group
+      for (int i = 0; i < gs; ++i) {
+        const float x = sc[lane * gs + i];
+        if (x > m1) { m2 = m1; m1 = x; }
+        else if (x > m2) m2 = x;
+      }
+      gkey = (group_score == MOE_GROUP_SCORE_TOP2_SUM && gs >= 2) ? __fadd_rn(m1, m2) : m1;
+      gidx = lane;
+    }
+    uint32_t keep = 0;
+    for (int r = 0; r < g_keep; ++r) {
+      float bk = gkey;
+      int bi = gidx;
+      warp_argmax(bk, bi);
+      keep |= 1u << bi;
+      if (lane == bi) { gkey = -INFINITY; gidx = INT_MAX; }
+    }
+    allowed = 0;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      const int e = s * 32 + lane;
+      if ((ok >> s & 1) && (keep >> (e / gs) & 1)) allowed |= 1u << s;
+    }
+  }
+
+  int my_idx = 0;
+  float my_key = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    float bk = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      const int e = s * 32 + lane;
+      if ((allowed >> s & 1) && better(v[s], e, bk, bi)) { bk = v[s]; bi = e; }
+    }
+    warp_argmax(bk, bi);
+    if (lane == j) { my_idx = bi; my_key = bk; }
+    if ((bi & 31) == lane) allowed &= ~(1u << (bi >> 5));
+  }
+
+  float w;
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s)
+      if (ok >> s & 1) m = fmaxf(m, v[s]);
+    m = warp_max(m);
+    const float ej = (lane < k) ? expf(my_key - m) : 0.0f;
+    float part = 0.0f;
+    if (renorm) {
+      part = ej;
+    } else {
+#pragma unroll
+      for (int s = 0; s < NSLOT; ++s)
+        if (ok >> s & 1) part += expf(v[s] - m);
+    }
+    w = ej / warp_sum(part);
+  } else {
+    const float sj = (lane < k) ? det_sigmoid(my_key) : 0.0f;
+    const float denom = renorm ? warp_sum(sj) : 1.0f;
+    w = sj / denom;
+  }
+  if (lane < k) {
+    topk_idx[(int64_t)t * k + lane] = my_idx;
+    topk_w[(int64_t)t * k + lane] = w * rho;
+  }
+}
+
+// S2 pass 1: per block of kScanChunk tokens, the count of entries per expert.
+// Out-of-range ids are reported and counted for expert 0 (keeps every later index in
+// bounds; the map is then garbage and the status word says so).
+__global__ void __launch_bounds__(kScanChunk) scan_count_kernel(
+    const int32_t* __restrict__ topk_idx, int T, int k, int E, int32_t* __restrict__ blockcnt,
+    DeviceStatus* st) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kScanChunk + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      int e = topk_idx[(int64_t)t * k + j];
+      if (e < 0 || e >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); e = 0; }
+      atomicAdd(&hist[e], 1);  // a count: the order of the adds does not show
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// S2 pass 2 (one block): counts, offsets (exclusive scan over experts) and, in place of
+// each block's count, the first row that block's entries of expert e take.
+__global__ void __launch_bounds__(1024) scan_offsets_kernel(int E, int NB, int32_t* __restrict__ blockcnt,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    int32_t tot = 0;
+    if (e < E)
+      for (int b = 0; b < NB; ++b) tot += blockcnt[(int64_t)b * E + e];
+    int32_t inc = tot;  // inclusive warp scan
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(kFull, inc, off);
+      if (lane >= off) inc += o;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x >> 5;
+      int32_t wv = lane < nw ? warp_tot[lane] : 0;
+      int32_t wi = wv;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(kFull, wi, off);
+        if (lane >= off) wi += o;
+      }
+      if (lane < nw) warp_tot[lane] = wi - wv;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int32_t excl = carry + warp_tot[warp] + inc - tot;
+    if (e < E) {
+      counts[e] = tot;
+      offsets[e] = excl;
+      int32_t run = excl;
+      for (int b = 0; b < NB; ++b) {
+        const int32_t c = blockcnt[(int64_t)b * E + e];
+        blockcnt[(int64_t)b * E + e] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[E] = carry;
+}
+
+// S2 pass 3: one warp per block of kScanChunk tokens walks them in ascending order, 32 at
+// a time. For each expert e, bit l of mask[e] says that lane l's token chose e; the rank of
+// that token among the 32 is the number of lower set bits, which keeps rows of an expert
+// in ascending token order with no atomics whose order could show.
+__global__ void __launch_bounds__(32) scan_assign_kernel(
+    const int32_t* __restrict__ topk_idx, int T, int k, int E, const int32_t* __restrict__ base,
+    int32_t* __restrict__ row_token, int32_t* __restrict__ tok_row, DeviceStatus* st) {
+  extern __shared__ int32_t smem[];
+  int32_t* counter = smem;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(smem + E);
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) {
+    counter[e] = base[(int64_t)blockIdx.x * E + e];
+    mask[e] = 0;
+  }
+  __syncwarp();
+  const uint32_t below = (1u << lane) - 1u;
+  for (int sub = 0; sub < kScanChunk; sub += 32) {
+    const int t = blockIdx.x * kScanChunk + sub + lane;
+    const bool valid = t < T;
+    const int32_t* ids = topk_idx + (int64_t)t * k;
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int e = ids[j];
+        if (e < 0 || e >= E) e = 0;
+        const uint32_t old = atomicOr(&mask[e], 1u << lane);
+        if (old >> lane & 1) set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t);  // repeated id
+      }
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int e = ids[j];
+        if (e < 0 || e >= E) e = 0;
+        const int32_t r = counter[e] + __popc(mask[e] & below);
+        row_token[r] = t;
+        tok_row[(int64_t)t * k + j] = r;
+      }
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int e = ids[j];
+        if (e < 0 || e >= E) e = 0;
+        const uint32_t m = mask[e];
+        if (m && 31 - __clz(m) == lane) {  // the highest lane closes expert e's batch
+          counter[e] += __popc(m);
+          mask[e] = 0;
+        }
+      }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_t* topk_idx,
+                              float* topk_w, DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int warps = 8;
+  const dim3 grid((unsigned)ceil_div(c.T, warps)), block(warps * 32);
+  const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
+  const size_t smem = grouped ? (size_t)warps * c.E * sizeof(float) : 0;
+  const int nslot = (int)ceil_div(c.E, 32);
+#define MOE_ROUTE_CASE(NS)                                                                  \
+  if (nslot <= NS) {                                                                        \
+    route_topk_kernel<NS><<<grid, block, smem, s>>>(logits, c.T, c.E, c.k, c.score_fn,      \
+                                                    c.renorm, c.n_groups, c.topk_groups,    \
+                                                    c.group_score, c.routed_scale, topk_idx, \
+                                                    topk_w, st);                            \
+    return cudaGetLastError();                                                              \
+  }
+  MOE_ROUTE_CASE(1)
+  MOE_ROUTE_CASE(2)
+  MOE_ROUTE_CASE(4)
+  MOE_ROUTE_CASE(8)
+  MOE_ROUTE_CASE(16)
+#undef MOE_ROUTE_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
+                              int32_t* offsets, int32_t* row_token, int32_t* tok_row,
+                              int32_t* blockcnt, DeviceStatus* st, cudaStream_t s) {
+  const int NB = scan_blocks(c);
+  if (NB > 0) {
+    scan_count_kernel<<<NB, kScanChunk, c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, blockcnt, st);
+  }
+  scan_offsets_kernel<<<1, 1024, 0, s>>>(c.E, NB, blockcnt, counts, offsets);
+  if (NB > 0) {
+    scan_assign_kernel<<<NB, 32, 2 * c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, blockcnt,
+                                                                 row_token, tok_row, st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe
