@@ -178,11 +178,18 @@ def run_gpu(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- whole-layer steps
+    # ---- whole-layer steps (moe_forward issues no host sync, so one step is a CUDA graph)
     for _ in range(args.warmup):
         moe.moe_forward(cfg, x, wts, y, ws)
     st = moe.moe_read_status(ws)
     assert st == moe.MOE_OK, moe.moe_status_string(st)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            moe.moe_forward(cfg, x, wts, y, ws)
+        graph.replay()
+    step = graph.replay if graph is not None else (lambda: moe.moe_forward(cfg, x, wts, y, ws))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     with ClockSampler(torch.cuda.current_device()) as clocks:
@@ -190,7 +197,7 @@ def run_gpu(args, w):
         for i in range(args.steps):
             flush.fill_(float(i))  # evict the previous step's lines from L2
             ev[i][0].record(stream)
-            moe.moe_forward(cfg, x, wts, y, ws)
+            step()
             ev[i][1].record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
@@ -292,6 +299,7 @@ def run_gpu(args, w):
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset or trained weights)",
         "config": {"workload": describe(w), "tokens_per_gpu": T, "parallelism": f"replicas x{world} (token-sharded)",
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "launch": "CUDA graph replay of moe_forward" if graph is not None else "moe_forward calls",
                    "weights_bytes": alg["weight_bytes"]},
         "stages_ms": {n: round(v, 4) for n, v in stage_ms.items()},
         "dispatch_gbs": round(alg["dispatch_bytes"] / (stage_ms["dispatch"] / 1e3) / 1e9, 1),
@@ -406,12 +414,13 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct moe_forward calls")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

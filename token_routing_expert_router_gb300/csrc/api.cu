@@ -112,6 +112,7 @@ cudaError_t router_logits(const moe_config_t& c, const void* x, const void* w_ro
   if (c.T == 0) return cudaSuccess;
   if (c.act_dtype == MOE_DTYPE_BF16 && tc::router_supported(c))
     return tc::launch_router(c, x, w_router, bias, logits, st, s);
+  if (router_small_supported(c)) return launch_router_small(c, x, w_router, bias, logits, s);
   SimtGemmArgs a{};
   a.mode = 0;
   a.act_bf16 = c.act_dtype == MOE_DTYPE_BF16;

@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -360,9 +362,13 @@ bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 bool make_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, box_rows, BK);
 }
+
+}  // namespace
 
 int num_sms() {
   static int n = 0;
@@ -374,6 +380,8 @@ int num_sms() {
   }
   return n;
 }
+
+namespace {
 
 template <int BN, int EPI>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
@@ -400,14 +408,17 @@ bool router_supported(const moe_config_t& c) {
 }
 
 bool mlp_supported(const moe_config_t& c) {
+  if (encode_fn() == nullptr) return false;
+  if (c.xfer_dtype == MOE_DTYPE_E4M3) return fp8_supported(c);
   if (c.act_dtype != MOE_DTYPE_BF16 || c.xfer_dtype != MOE_DTYPE_BF16) return false;
-  return c.H % 128 == 0 && c.F % 128 == 0 && encode_fn() != nullptr;
+  return c.H % 128 == 0 && c.F % 128 == 0;
 }
 
 cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router, const float* bias,
                           float* logits, DeviceStatus* st, cudaStream_t s) {
+  // 128-wide N tiles: E / 128 tiles per 128 tokens, so small T still spreads over the SMs
   CUtensorMap ta, tb;
-  if (!make_bf16(&ta, x, c.T, c.H, BM) || !make_bf16(&tb, w_router, c.E, c.H, c.E)) return cudaErrorInvalidValue;
+  if (!make_bf16(&ta, x, c.T, c.H, BM) || !make_bf16(&tb, w_router, c.E, c.H, 128)) return cudaErrorInvalidValue;
   TcParams p{};
   p.G = 0;
   p.has_extra = 1;
@@ -415,21 +426,22 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
   p.a2_row_base = 0;
   p.out_extra_base = 0;
   p.K = c.H;
-  p.n_tiles = 1;
+  p.n_tiles = c.E / 128;
   p.b_group_rows = 0;
   p.ldc = c.E;
   p.out = logits;
   p.bias = bias;
   p.timeout_ns = kTimeoutNs;
   p.status = st;
-  const int64_t tiles = ceil_div(c.T, BM);
-  if (c.E == 256) return launch<256, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
+  const int64_t tiles = ceil_div(c.T, BM) * p.n_tiles;
   return launch<128, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
 }
 
-cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float*, const void* x,
-                               const int32_t* offsets, const moe_weights_t& w, void* h, float*, void* yd,
+cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale, const void* x,
+                               const int32_t* offsets, const moe_weights_t& w, void* h, float* h_scale, void* yd,
                                DeviceStatus* st, cudaStream_t s) {
+  if (c.xfer_dtype == MOE_DTYPE_E4M3)
+    return launch_grouped_mlp_fp8(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
   // ---- GEMM1: h = silu(A Wg^T) * (A Wu^T), tiles of 128 h columns (256 B rows)

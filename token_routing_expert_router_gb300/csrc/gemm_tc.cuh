@@ -18,5 +18,11 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
                                cudaStream_t s);
 
+// FP8 (e4m3, fp32 block scales) variant of the grouped MLP.
+bool fp8_supported(const moe_config_t& c);
+cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const float* xd_scale,
+                                   const int32_t* offsets, const moe_weights_t& w, void* h,
+                                   float* h_scale, void* yd, DeviceStatus* st, cudaStream_t s);
+
 }  // namespace tc
 }  // namespace moe

@@ -155,6 +155,85 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const void* __restric
   }
 }
 
+// Same sum with the row count NR = k (+1 shared) known at compile time: every row's
+// 16-byte vector of a chunk is loaded before any of them is summed, so one memory round
+// trip covers all NR rows. The shared row enters with weight 1 (fma(1, v, acc) == acc + v).
+template <int NR, bool BF16>
+__global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __restrict__ yd_, int H, int k,
+                                                              const int32_t* __restrict__ tok_row,
+                                                              const float* __restrict__ topk_w, int64_t R,
+                                                              void* __restrict__ y_) {
+  __shared__ int64_t rows[NR];
+  __shared__ float wts[NR];
+  const int t = blockIdx.x;
+  if (threadIdx.x < NR) {
+    const int j = threadIdx.x;
+    rows[j] = j < k ? (int64_t)tok_row[(int64_t)t * k + j] : R + t;
+    wts[j] = j < k ? topk_w[(int64_t)t * k + j] : 1.0f;
+  }
+  __syncthreads();
+  const int n8 = H / 8;
+  for (int c = threadIdx.x; c < n8; c += kThreads) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    if (BF16) {
+      uint4 raw[NR];
+#pragma unroll
+      for (int j = 0; j < NR; ++j) raw[j] = __ldg(reinterpret_cast<const uint4*>(yd_) + rows[j] * (H / 8) + c);
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        const float wj = wts[j];
+        const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = __fmaf_rn(wj, bf16_lo(u[q]), acc[2 * q]);
+          acc[2 * q + 1] = __fmaf_rn(wj, bf16_hi(u[q]), acc[2 * q + 1]);
+        }
+      }
+      uint4 o;
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&p0);
+      o.y = *reinterpret_cast<uint32_t*>(&p1);
+      o.z = *reinterpret_cast<uint32_t*>(&p2);
+      o.w = *reinterpret_cast<uint32_t*>(&p3);
+      reinterpret_cast<uint4*>(y_)[(int64_t)t * n8 + c] = o;
+    } else {
+      float4 raw[NR][2];
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        const float4* p = reinterpret_cast<const float4*>(yd_) + rows[j] * (H / 4) + 2 * c;
+        raw[j][0] = __ldg(p);
+        raw[j][1] = __ldg(p + 1);
+      }
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        const float wj = wts[j];
+        acc[0] = __fmaf_rn(wj, raw[j][0].x, acc[0]); acc[1] = __fmaf_rn(wj, raw[j][0].y, acc[1]);
+        acc[2] = __fmaf_rn(wj, raw[j][0].z, acc[2]); acc[3] = __fmaf_rn(wj, raw[j][0].w, acc[3]);
+        acc[4] = __fmaf_rn(wj, raw[j][1].x, acc[4]); acc[5] = __fmaf_rn(wj, raw[j][1].y, acc[5]);
+        acc[6] = __fmaf_rn(wj, raw[j][1].z, acc[6]); acc[7] = __fmaf_rn(wj, raw[j][1].w, acc[7]);
+      }
+      float4* p = reinterpret_cast<float4*>(y_) + ((int64_t)t * H) / 4 + 2 * c;
+      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
+template <int NR>
+cudaError_t launch_combine_nr(const moe_config_t& c, const void* yd, const int32_t* tok_row,
+                              const float* topk_w, void* y, cudaStream_t s) {
+  if (c.act_dtype == MOE_DTYPE_BF16)
+    combine_nr_kernel<NR, true><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, routed_rows(c), y);
+  else
+    combine_nr_kernel<NR, false><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, routed_rows(c), y);
+  return cudaGetLastError();
+}
+
 // Block quantisation of a bf16 matrix (br x bc blocks) with the dispatch rule.
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ src, int64_t rows,
                                                        int64_t cols, int br, int bc, uint8_t* __restrict__ q,
@@ -208,6 +287,18 @@ cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t*
                            const float* topk_w, void* y, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int shared = c.n_shared ? 1 : 0;
+  switch (c.k + shared) {
+    case 1: return launch_combine_nr<1>(c, yd, tok_row, topk_w, y, s);
+    case 2: return launch_combine_nr<2>(c, yd, tok_row, topk_w, y, s);
+    case 3: return launch_combine_nr<3>(c, yd, tok_row, topk_w, y, s);
+    case 4: return launch_combine_nr<4>(c, yd, tok_row, topk_w, y, s);
+    case 5: return launch_combine_nr<5>(c, yd, tok_row, topk_w, y, s);
+    case 6: return launch_combine_nr<6>(c, yd, tok_row, topk_w, y, s);
+    case 7: return launch_combine_nr<7>(c, yd, tok_row, topk_w, y, s);
+    case 8: return launch_combine_nr<8>(c, yd, tok_row, topk_w, y, s);
+    case 9: return launch_combine_nr<9>(c, yd, tok_row, topk_w, y, s);
+    default: break;  // larger k: the generic loop below
+  }
   if (c.act_dtype == MOE_DTYPE_BF16)
     combine_kernel<true><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, shared, routed_rows(c), y);
   else

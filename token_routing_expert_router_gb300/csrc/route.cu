@@ -8,6 +8,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -305,7 +307,87 @@ __global__ void __launch_bounds__(32) scan_assign_kernel(
   }
 }
 
+// S0 for small expert counts (E <= EP <= 32): one warp per token, lanes stride over the
+// token's 16-byte chunks, each lane keeps E partial dot products in registers (the router
+// weight, E x H, stays in L1/L2), then a warp reduction per expert. fp32 accumulation.
+template <int EP, bool BF16>
+__global__ void __launch_bounds__(256) router_small_kernel(const void* __restrict__ x_, const void* __restrict__ w_,
+                                                           const float* __restrict__ bias, int T, int H, int E,
+                                                           float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  constexpr int EPC = BF16 ? 8 : 4;  // elements per 16-byte chunk
+  const int nchunk = H / EPC;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    float acc[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[e] = 0.0f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x_) + (int64_t)t * nchunk;
+    for (int c = lane; c < nchunk; c += 32) {
+      const uint4 xv = __ldg(xr + c);
+      float xf[EPC];
+      if (BF16) {
+        const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) { xf[2 * q] = __uint_as_float(u[q] << 16); xf[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
+      } else {
+        xf[0] = __uint_as_float(xv.x); xf[1] = __uint_as_float(xv.y);
+        xf[2] = __uint_as_float(xv.z); xf[3] = __uint_as_float(xv.w);
+      }
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if (e < E) {
+          const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_) + (int64_t)e * nchunk + c);
+          if (BF16) {
+            const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[e] = __fmaf_rn(xf[2 * q], __uint_as_float(u[q] << 16), acc[e]);
+              acc[e] = __fmaf_rn(xf[2 * q + 1], __uint_as_float(u[q] & 0xffff0000u), acc[e]);
+            }
+          } else {
+            acc[e] = __fmaf_rn(xf[0], __uint_as_float(wv.x), acc[e]);
+            acc[e] = __fmaf_rn(xf[1], __uint_as_float(wv.y), acc[e]);
+            acc[e] = __fmaf_rn(xf[2], __uint_as_float(wv.z), acc[e]);
+            acc[e] = __fmaf_rn(xf[3], __uint_as_float(wv.w), acc[e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      float v = acc[e];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      if (lane == e && e < E) logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
+    }
+  }
+}
+
 }  // namespace
+
+bool router_small_supported(const moe_config_t& c) { return c.E <= 32; }
+
+cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void* w, const float* bias,
+                                float* logits, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = std::min<int64_t>(ceil_div(c.T, 8), (int64_t)sms * 8);
+  const bool bf = c.act_dtype == MOE_DTYPE_BF16;
+#define MOE_RS(EP)                                                                                            \
+  if (c.E <= EP) {                                                                                          \
+    if (bf) router_small_kernel<EP, true><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits);  \
+    else router_small_kernel<EP, false><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits); \
+    return cudaGetLastError();                                                                              \
+  }
+  MOE_RS(8)
+  MOE_RS(16)
+  MOE_RS(32)
+#undef MOE_RS
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_t* topk_idx,
                               float* topk_w, DeviceStatus* st, cudaStream_t s) {
