@@ -177,6 +177,27 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
 moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols, int32_t br,
                                int32_t bc, uint8_t* q, float* scale, moe_stream_t stream);
 
+/* moe_route for callers that cannot allocate device memory. The paper has no counterpart:
+ * this is a library convenience. It computes exactly what moe_route computes (same kernels,
+ * same bits) but takes no workspace: the routing scan's scratch lives in a fixed array
+ * inside the library (1 MiB of device memory per GPU that loads the library, held until
+ * the process exits), so callers that are handed only their inputs and outputs, or that
+ * must not allocate while a CUDA graph is being captured, can still route.
+ *  - Limit: ceil(T / 128) * E <= 262144 (e.g. T = 131072 tokens with E = 256); larger
+ *    problems return MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on each device looks up the array's device address (no allocation);
+ *    make that first call before any stream capture.
+ *  - Every call on a device shares the one array: calls whose kernels overlap on the GPU
+ *    (two streams, two host threads) race, and the caller must serialise them.
+ *  - device_status: optional caller-owned device int32[2] (code, detail) that receives
+ *    device-detected faults (non-finite scores) like the workspace's status word; zero it
+ *    before the call. With NULL those faults are not reported (outputs stay in bounds).
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
+moe_status_t moe_route_static_scratch(const moe_config_t* cfg, const float* logits,
+                                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                      int32_t* offsets, int32_t* row_token, int32_t* tok_row,
+                                      int32_t* device_status, moe_stream_t stream);
+
 /* Synchronises `stream`, returns the device status word of `ws` in *device_status
  * (MOE_OK or a moe_status_t code) and clears it. The only call that blocks the host. */
 moe_status_t moe_read_status(void* ws, moe_stream_t stream, int32_t* device_status);

@@ -95,6 +95,7 @@ def lib():
             "moe_forward": [cfg, P, wts, P, P, P, P, P, P],
             "moe_quantize_e4m3": [P, c_int64, c_int64, c_int32, c_int32, P, P, P],
             "moe_read_status": [P, P, POINTER(c_int32)],
+            "moe_route_static_scratch": [cfg, P, P, P, P, P, P, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -110,7 +111,7 @@ def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
             "moe_router_logits", "moe_route", "moe_route_from_map", "moe_dispatch",
             "moe_grouped_mlp", "moe_combine", "moe_forward", "moe_quantize_e4m3",
-            "moe_read_status", "moe_status_string"]
+            "moe_read_status", "moe_status_string", "moe_route_static_scratch"]
 
 
 def _ptr(t):
@@ -204,6 +205,18 @@ def moe_quantize_e4m3(src, br: int, bc: int, q, scale, stream=None):
     rows, cols = src.shape
     _check(lib().moe_quantize_e4m3(_ptr(src), rows, cols, br, bc, _ptr(q), _ptr(scale),
                                    _stream(stream)), "moe_quantize_e4m3")
+
+
+def moe_route_static_scratch(cfg, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row,
+                             device_status=None, stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device memory: the
+    scan's scratch is a fixed 1 MiB array inside the library, shared by every call on a
+    device (overlapping calls race; the first call on a device must precede any capture).
+    ``device_status``: optional int32 CUDA tensor of 2 elements for device-side faults."""
+    _check(lib().moe_route_static_scratch(byref(cfg), _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+                                          _ptr(counts), _ptr(offsets), _ptr(row_token),
+                                          _ptr(tok_row), _ptr(device_status), _stream(stream)),
+           "moe_route_static_scratch")
 
 
 def moe_read_status(ws, stream=None) -> int:
