@@ -43,6 +43,32 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def rank_env():
+    """(world, rank, local_rank) from the torch.distributed.run environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_seed(rank: int) -> int:
+    """Each replica draws its own token shard; the weights use seed 0 on every rank."""
+    return rank
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest value over all ranks (the job's time is its slowest replica's)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def describe(w):
     return (f"{w['name']} (T={w['T']}, H={w['H']}, E={w['E']}, k={w['k']}, F={w['F']}"
             + (f", shared F={w['F_shared']}" if w["n_shared"] else "")
@@ -121,9 +147,7 @@ def run_gpu(args, w):
     import torch
     import token_routing_expert_router_gb300 as moe
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -144,7 +168,7 @@ def run_gpu(args, w):
         t = torch.empty(shape, dtype=dtype, device=dev)
         return synth.device_normal(t, seed, tid, std)
 
-    x = gen((T, H), synth.X, 1.0, seed=rank)
+    x = gen((T, H), synth.X, 1.0, seed=shard_seed(rank))
     wts = {"w_router": gen((E, H), synth.W_ROUTER, s), "w_gate": gen((E, F, H), synth.W_GATE, s),
            "w_up": gen((E, F, H), synth.W_UP, s), "w_down": gen((E, H, F), synth.W_DOWN, s),
            "router_bias": torch.from_numpy(synth.zipf_bias(0, E)).to(dev) if w["zipf"] else None}
@@ -202,14 +226,10 @@ def run_gpu(args, w):
         barrier()
         t_wall = time.perf_counter() - t_wall
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     assert moe.moe_read_status(ws) == moe.MOE_OK
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
 
     # ---- per-stage times through the staged entry points (same kernels)
     R = T * k
@@ -269,11 +289,7 @@ def run_gpu(args, w):
         yh.copy_(y, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -314,7 +330,7 @@ def run_gpu(args, w):
                          "combine_frac": round(alg["combine_bytes"] / (stage_ms["combine"] / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
                          "peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
         "expert_rows": {"min": int(counts.min()), "max": int(counts.max()), "empty": int((counts == 0).sum())},
-        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, T, 1, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
         "gpu_launches": args.steps * launches_per_forward(w),
@@ -389,9 +405,9 @@ def cpu_baseline(w, n_tokens, seed=0):
 
 
 def run_reference(args, w):
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = rank_env()
     if rank != 0:
-        return None
+        return None  # the oracle runs once, on rank 0; the other ranks exit without work
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; its build happens on import
     vals = []

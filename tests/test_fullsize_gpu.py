@@ -1,0 +1,228 @@
+"""Parity at the workloads' full sizes, in the launch configuration the benchmark times
+(moe_forward captured once in a CUDA graph and replayed), on outputs the oracle computes
+one by one: sampled router-logit rows, sampled dispatched rows, sampled rows of sampled
+experts' MLP outputs, sampled combined tokens, and the whole-layer output of sampled
+tokens. Large weights are drawn on the GPU by the device twin of the generator; every
+oracle input is redrawn on the host from the same counters (never read back from a GPU
+result)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import token_routing_expert_router_gb300 as moe
+from moe_case import cfg_of, device_weights_generated, np_of, routing_ambiguity, up, weights_arg
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["mixtral_bf16", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8"]
+SAMPLE_TOKENS = {"mixtral_bf16": 6, "dsv3_bf16": 4, "imbalanced_bf16": 8, "dsv3_fp8": 3}
+
+
+class Layer:
+    """One full-size layer on the GPU: generated weights, one forward by graph replay."""
+
+    def __init__(self, name):
+        w = synth.WORKLOADS[name]
+        self.w = w
+        self.d = device_weights_generated(w, seed=0)
+        for key in list(self.d):
+            if key.endswith("_bf16"):
+                del self.d[key]  # keep only what the layer reads
+        cfg = cfg_of(w)
+        self.cfg = cfg
+        T, k, E, H = w["T"], w["k"], w["E"], w["H"]
+        ws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+        moe.moe_workspace_init(ws)
+        dt = torch.bfloat16 if w["act_dtype"] == synth.BF16 else torch.float32
+        self.y = torch.empty((T, H), dtype=dt, device="cuda")
+        self.idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        self.wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        self.cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+        args = (cfg, self.d["x"], weights_arg(self.d), self.y, ws, self.idx, self.wt, self.cnt)
+        moe.moe_forward(*args)  # warm-up outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            moe.moe_forward(*args)
+        self.y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_read_status(ws) == moe.MOE_OK
+        self.logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_router_logits(cfg, self.d["x"], self.d["w_router"], self.d["router_bias"],
+                              self.logits, ws)
+        torch.cuda.synchronize()
+        self.ws = ws
+
+
+_CACHE = {}
+
+
+def layer(name):
+    if name not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        _CACHE[name] = Layer(name)
+    return _CACHE[name]
+
+
+def sample_tokens(w, n, seed=5):
+    T = w["T"]
+    rng = synth.bits_at(seed, 90, np.arange(n, dtype=np.uint64)) % np.uint64(T)
+    return np.unique(np.concatenate([[0, T - 1], rng.astype(np.int64)]))
+
+
+def host_expert(w, e, fp8):
+    g, u, d = synth.expert_weights(w, 0, e)
+    if fp8:
+        return tuple(oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
+    return g.astype(np.float64), u.astype(np.float64), d.astype(np.float64)
+
+
+def host_shared(w, fp8):
+    H, Fs, s, dt = w["H"], w["F_shared"], w["w_std"], synth.act_name(w)
+    mats = (synth.normal(0, synth.WS_GATE, (Fs, H), s, dt), synth.normal(0, synth.WS_UP, (Fs, H), s, dt),
+            synth.normal(0, synth.WS_DOWN, (H, Fs), s, dt))
+    if fp8:
+        return tuple(oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in mats)
+    return tuple(m.astype(np.float64) for m in mats)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_fullsize_generator_twin_and_router_logits(name):
+    L = layer(name)
+    w = L.w
+    toks = sample_tokens(w, 16)
+    xs = synth.rows(0, synth.X, toks, w["H"], 1.0, synth.act_name(w))
+    assert np.array_equal(np_of(L.d["x"][torch.from_numpy(toks).cuda()]), xs)  # device twin == host
+    wr = synth.normal(0, synth.W_ROUTER, (w["E"], w["H"]), w["w_std"], synth.act_name(w))
+    bias = synth.zipf_bias(0, w["E"]) if w["zipf"] else None
+    ref = oracle.router_logits(xs, wr, bias)
+    got = np_of(L.logits[torch.from_numpy(toks).cuda()])
+    assert oracle.rel_l2(got, ref) < 1e-4
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_fullsize_layer_sampled_tokens(name):
+    L = layer(name)
+    w = L.w
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    toks = sample_tokens(w, SAMPLE_TOKENS[name])
+    counts = np_of(L.cnt)
+    assert counts.sum() == T * k
+    xs = synth.rows(0, synth.X, toks, H, 1.0, synth.act_name(w))
+    wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], synth.act_name(w))
+    bias = synth.zipf_bias(0, E) if w["zipf"] else None
+    l_ref = oracle.router_logits(xs, wr, bias)
+    idx_ref, wt_ref = oracle.route(l_ref, dict(w, T=len(toks)))
+    l_gpu = np_of(L.logits[torch.from_numpy(toks).cuda()])
+    delta = float(np.abs(l_gpu.astype(np.float64) - l_ref).max())
+    amb = routing_ambiguity(w, l_ref, delta)
+    idx_gpu = np_of(L.idx)[toks]
+    same = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
+    assert np.all(same | amb)
+    if fp8:
+        q, s = oracle.quant_blocks(xs, 1, 128)
+        a = oracle.dequant_blocks(q, s, 1, 128)
+    else:
+        a = xs.astype(np.float64)
+    y_ref = np.zeros((len(toks), H))
+    for e in sorted(set(idx_ref[same].ravel().tolist())):
+        mats = host_expert(w, e, fp8)
+        for i in np.nonzero(same)[0]:
+            for j in range(k):
+                if idx_ref[i, j] == e:
+                    y_ref[i] += wt_ref[i, j] * oracle.expert_mlp(a[i:i + 1], *mats, quant_h=fp8)[0]
+    if w["n_shared"]:
+        y_ref += oracle.expert_mlp(a, *host_shared(w, fp8), quant_h=fp8)
+    got = np_of(L.y)[toks].astype(np.float64)
+    tol = 3e-2 if fp8 else 1e-2
+    err = oracle.rel_l2(got[same], y_ref[same])
+    assert err < tol, err
+
+
+@pytest.mark.parametrize("name", ["dsv3_bf16", "dsv3_fp8"])
+def test_fullsize_dispatch_and_expert_rows(name):
+    """Dispatch of the full batch with the oracle's own routing of generator scores, then the
+    grouped MLP on it; sampled rows of three experts and of the shared expert."""
+    L = layer(name)
+    w = L.w
+    fp8 = w["xfer_dtype"] == synth.E4M3
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    R = T * k
+    rows = R + T
+    l = synth.synthetic_logits(7, T, E)
+    idx, wt = oracle.route(l, w)
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    xdt = torch.uint8 if fp8 else torch.bfloat16
+    xd = torch.empty((rows, H), dtype=xdt, device="cuda")
+    xs = torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
+    moe.moe_dispatch(L.cfg, L.d["x"], up(tok_row), xd, xs)
+    h = torch.empty((rows, F), dtype=xdt, device="cuda")
+    hs = torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
+    yd = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_mlp(L.cfg, xd, xs, L.d["x"], up(offsets), weights_arg(L.d), h, hs, yd, L.ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(L.ws) == moe.MOE_OK
+    # sampled dispatched rows are bit-exact copies (or quantisations) of host-drawn tokens
+    pick = np.unique(np.concatenate([[0, R - 1], (synth.bits_at(8, 91, np.arange(24, dtype=np.uint64)) % np.uint64(R)).astype(np.int64)]))
+    xt = synth.rows(0, synth.X, row_token[pick], H, 1.0, "bf16")
+    if fp8:
+        q, s = oracle.quant_blocks(xt, 1, 128)
+        assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), q)
+        assert np.array_equal(np_of(xs[:, torch.from_numpy(pick).cuda()]).T, s)
+        a_rows = oracle.dequant_blocks(q, s, 1, 128)
+    else:
+        assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), xt)
+    # sampled rows of three experts (first, largest, last non-empty) and of the shared expert
+    nz = np.nonzero(counts)[0]
+    experts = sorted({int(nz[0]), int(np.argmax(counts)), int(nz[-1])})
+    got_all = []
+    ref_all = []
+    for e in experts:
+        r0, r1 = offsets[e], offsets[e + 1]
+        rr = np.unique(np.array([r0, (r0 + r1) // 2, r1 - 1]))
+        xa = synth.rows(0, synth.X, row_token[rr], H, 1.0, "bf16")
+        if fp8:
+            qa, sa = oracle.quant_blocks(xa, 1, 128)
+            xa = oracle.dequant_blocks(qa, sa, 1, 128)
+        ref_all.append(oracle.expert_mlp(xa, *host_expert(w, e, fp8), quant_h=fp8))
+        got_all.append(np_of(yd[torch.from_numpy(rr).cuda()]))
+    ts = np.array([0, T // 2, T - 1])
+    xa = synth.rows(0, synth.X, ts, H, 1.0, "bf16")
+    if fp8:
+        qa, sa = oracle.quant_blocks(xa, 1, 128)
+        xa = oracle.dequant_blocks(qa, sa, 1, 128)
+    ref_all.append(oracle.expert_mlp(xa, *host_shared(w, fp8), quant_h=fp8))
+    got_all.append(np_of(yd[torch.from_numpy(R + ts).cuda()]))
+    got = np.concatenate(got_all).astype(np.float64)
+    ref = np.concatenate(ref_all)
+    assert oracle.rel_l2(got, ref) < (3e-2 if fp8 else 1e-2)
+
+
+@pytest.mark.parametrize("name", ["dsv3_bf16", "imbalanced_bf16"])
+def test_fullsize_combine_sampled(name):
+    L = layer(name)
+    w = L.w
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    R = T * k
+    rows = R + (T if w["n_shared"] else 0)
+    idx, _ = oracle.route(synth.synthetic_logits(9, T, E), w)
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    yd = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda")
+    synth.device_normal(yd, 9, synth.YD, 1.0)
+    wts = synth.uniform_at(9, synth.TOPK_W, np.arange(T * k)).reshape(T, k).astype(np.float32)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(L.cfg, yd, up(tok_row), up(wts), y)
+    toks = sample_tokens(w, 12, seed=9)
+    ref = np.zeros((len(toks), H))
+    for i, t in enumerate(toks):
+        r = tok_row[t]
+        ydr = synth.rows(9, synth.YD, r, H, 1.0, "bf16").astype(np.float64)
+        ref[i] = wts[t].astype(np.float64) @ ydr
+        if w["n_shared"]:
+            ref[i] += synth.rows(9, synth.YD, [R + t], H, 1.0, "bf16")[0]
+    got = np_of(y[torch.from_numpy(toks).cuda()]).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
