@@ -27,6 +27,7 @@ constexpr int BK = 64;             // bf16 K per stage: one 128-byte swizzle row
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group + 1
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+constexpr int kPrefetch = 8;  // K blocks between an L2 prefetch and its load
 
 enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2 };
 
@@ -174,12 +175,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * BM;
         const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;
         const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        const int next = tile + gridDim.x;
+        const bool has_next = next < total_tiles;
+        const CUtensorMap *na = ta, *nb0 = tb0, *nb1 = tb1;
+        int na_row = a_row, nb_row = b_row;
+        if (has_next) {
+          const TileCoord n = decode_tile(next, mt_prefix, ngroups, p.n_tiles, seg_rows);
+          const bool nx = n.g >= p.G;
+          na = nx ? &tmA2 : &tmA;
+          nb0 = nx ? &tmB0x : &tmB0;
+          nb1 = nx ? &tmB1x : &tmB1;
+          na_row = (nx ? p.a2_row_base : p.offsets[n.g]) + n.mb * BM;
+          nb_row = (nx ? 0 : n.g * p.b_group_rows) + n.nb * b_tile_rows;
+        }
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
           uint8_t* a_dst = sA + stage * S::kABytes;
           uint8_t* b_dst = sB + stage * S::kBBytes;
           tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+          if (kb + kPrefetch < kblocks) {  // warm L2 for a later stage of this tile
+            const int kp = (kb + kPrefetch) * BK;
+            tma_prefetch_l2_2d(ta, kp, a_row);
+            tma_prefetch_l2_2d(tb0, kp, b_row);
+            if (EPI == EPI_SWIGLU_BF16) tma_prefetch_l2_2d(tb1, kp, b_row);
+          } else if (has_next) {  // ... or for the first stages of this block's next tile
+            const int kp = (kb + kPrefetch - kblocks) * BK;
+            tma_prefetch_l2_2d(na, kp, na_row);
+            tma_prefetch_l2_2d(nb0, kp, nb_row);
+            if (EPI == EPI_SWIGLU_BF16) tma_prefetch_l2_2d(nb1, kp, nb_row);
+          }
           if (EPI == EPI_SWIGLU_BF16) {
             tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
             tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows

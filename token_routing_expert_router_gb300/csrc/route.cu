@@ -307,10 +307,11 @@ __global__ void __launch_bounds__(32) scan_assign_kernel(
   }
 }
 
-// S0 for small expert counts (E <= EP <= 32): one warp per token, lanes stride over the
-// token's 16-byte chunks, each lane keeps E partial dot products in registers (the router
-// weight, E x H, stays in L1/L2), then a warp reduction per expert. fp32 accumulation.
-template <int EP, bool BF16>
+// S0 for small expert counts (E <= EP <= 32): one warp per TPW tokens. Lanes stride over
+// 16-byte chunks; each chunk of the router weight (E x 16 B, from L1/L2) is loaded once and
+// applied to all TPW tokens, whose E partial dot products each lane keeps in registers,
+// then a warp reduction per (token, expert). fp32 accumulation.
+template <int EP, int TPW, bool BF16>
 __global__ void __launch_bounds__(256) router_small_kernel(const void* __restrict__ x_, const void* __restrict__ w_,
                                                            const float* __restrict__ bias, int T, int H, int E,
                                                            float* __restrict__ logits) {
@@ -318,49 +319,56 @@ __global__ void __launch_bounds__(256) router_small_kernel(const void* __restric
   const int warps = (gridDim.x * blockDim.x) >> 5;
   constexpr int EPC = BF16 ? 8 : 4;  // elements per 16-byte chunk
   const int nchunk = H / EPC;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    float acc[EP];
+  for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * TPW; t0 < T; t0 += warps * TPW) {
+    float acc[TPW][EP];
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = 0.0f;
-    const uint4* xr = reinterpret_cast<const uint4*>(x_) + (int64_t)t * nchunk;
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[i][e] = 0.0f;
     for (int c = lane; c < nchunk; c += 32) {
-      const uint4 xv = __ldg(xr + c);
-      float xf[EPC];
-      if (BF16) {
-        const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+      float xf[TPW][EPC];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) { xf[2 * q] = __uint_as_float(u[q] << 16); xf[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
-      } else {
-        xf[0] = __uint_as_float(xv.x); xf[1] = __uint_as_float(xv.y);
-        xf[2] = __uint_as_float(xv.z); xf[3] = __uint_as_float(xv.w);
+      for (int i = 0; i < TPW; ++i) {
+        const int t = min(t0 + i, T - 1);  // a short last group repeats a row; not stored
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x_) + (int64_t)t * nchunk + c);
+        if (BF16) {
+          const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) { xf[i][2 * q] = __uint_as_float(u[q] << 16); xf[i][2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
+        } else {
+          xf[i][0] = __uint_as_float(xv.x); xf[i][1] = __uint_as_float(xv.y);
+          xf[i][2] = __uint_as_float(xv.z); xf[i][3] = __uint_as_float(xv.w);
+        }
       }
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
         if (e < E) {
           const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_) + (int64_t)e * nchunk + c);
+          float wf[EPC];
           if (BF16) {
             const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[e] = __fmaf_rn(xf[2 * q], __uint_as_float(u[q] << 16), acc[e]);
-              acc[e] = __fmaf_rn(xf[2 * q + 1], __uint_as_float(u[q] & 0xffff0000u), acc[e]);
-            }
+            for (int q = 0; q < 4; ++q) { wf[2 * q] = __uint_as_float(u[q] << 16); wf[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
           } else {
-            acc[e] = __fmaf_rn(xf[0], __uint_as_float(wv.x), acc[e]);
-            acc[e] = __fmaf_rn(xf[1], __uint_as_float(wv.y), acc[e]);
-            acc[e] = __fmaf_rn(xf[2], __uint_as_float(wv.z), acc[e]);
-            acc[e] = __fmaf_rn(xf[3], __uint_as_float(wv.w), acc[e]);
+            wf[0] = __uint_as_float(wv.x); wf[1] = __uint_as_float(wv.y);
+            wf[2] = __uint_as_float(wv.z); wf[3] = __uint_as_float(wv.w);
           }
+#pragma unroll
+          for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) acc[i][e] = __fmaf_rn(xf[i][q], wf[q], acc[i][e]);
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < EP; ++e) {
-      float v = acc[e];
+    for (int i = 0; i < TPW; ++i)
 #pragma unroll
-      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-      if (lane == e && e < E) logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
-    }
+      for (int e = 0; e < EP; ++e) {
+        float v = acc[i][e];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+        if (lane == e && e < E && t0 + i < T) logits[(int64_t)(t0 + i) * E + e] = bias ? v + bias[e] : v;
+      }
   }
 }
 
@@ -374,17 +382,18 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t blocks = std::min<int64_t>(ceil_div(c.T, 8), (int64_t)sms * 8);
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
-#define MOE_RS(EP)                                                                                            \
-  if (c.E <= EP) {                                                                                          \
-    if (bf) router_small_kernel<EP, true><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits);  \
-    else router_small_kernel<EP, false><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits); \
-    return cudaGetLastError();                                                                              \
+  // TPW tokens per warp (fewer for wider E: TPW * EP accumulators per lane), 8 warps a block
+#define MOE_RS(EP, TPW)                                                                                   \
+  if (c.E <= EP) {                                                                                      \
+    const int64_t blocks = std::min<int64_t>(ceil_div(c.T, 8 * TPW), (int64_t)sms * 8);                \
+    if (bf) router_small_kernel<EP, TPW, true><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits); \
+    else router_small_kernel<EP, TPW, false><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits);   \
+    return cudaGetLastError();                                                                          \
   }
-  MOE_RS(8)
-  MOE_RS(16)
-  MOE_RS(32)
+  MOE_RS(8, 4)
+  MOE_RS(16, 2)
+  MOE_RS(32, 1)
 #undef MOE_RS
   return cudaErrorInvalidValue;
 }
