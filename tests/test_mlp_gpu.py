@@ -20,6 +20,11 @@ CASES = [
     synth.scaled(W["imbalanced_bf16"], T=700, H=256, E=32, k=4, F=384, name="imbalanced_small"),
     synth.scaled(W["dsv3_fp8"], T=300, H=512, E=16, F=256, F_shared=256, n_groups=4,
                  topk_groups=2, name="fp8_small"),
+    # >= 512 rows per expert on average: the 256-row CTA-pair tiles of the bf16 GEMMs
+    synth.scaled(W["mixtral_bf16"], T=1100, H=512, E=4, F=384, name="pair_mixtral"),
+    synth.scaled(W["imbalanced_bf16"], T=2100, H=256, E=8, k=2, F=256, name="pair_imbalanced"),
+    synth.scaled(W["dsv3_bf16"], T=1200, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
+                 topk_groups=1, name="pair_shared"),
 ]
 
 

@@ -35,7 +35,6 @@ constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 514;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int kPrefetch = 8;  // K blocks between an L2 prefetch and its load
 constexpr int kABytes = BM * BK, kBBytes = BN * BK, kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 512;  // two 256-column partial accumulators
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * BM * sizeof(float) +
@@ -182,36 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * BM;
         const int b_tile_rows = EPI == FP8_SWIGLU_Q8 ? BN / 2 : BN;
         const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-        const int next = tile + gridDim.x;
-        const bool has_next = next < total_tiles;
-        const CUtensorMap *na = ta, *nb0 = tb0, *nb1 = tb1;
-        int na_row = a_row, nb_row = b_row;
-        if (has_next) {
-          const TileCoord n = decode_tile(next, mt_prefix, ngroups, p.n_tiles, seg_rows);
-          const bool nx = n.g >= p.G;
-          na = nx ? &tmA2 : &tmA;
-          nb0 = nx ? &tmB0x : &tmB0;
-          nb1 = nx ? &tmB1x : &tmB1;
-          na_row = (nx ? p.a2_row_base : p.offsets[n.g]) + n.mb * BM;
-          nb_row = (nx ? 0 : n.g * p.b_group_rows) + n.nb * b_tile_rows;
-        }
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
           tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
-          if (kb + kPrefetch < kblocks) {  // warm L2 for a later stage of this tile
-            const int kp = (kb + kPrefetch) * BK;
-            tma_prefetch_l2_2d(ta, kp, a_row);
-            tma_prefetch_l2_2d(tb0, kp, b_row);
-            if (EPI == FP8_SWIGLU_Q8) tma_prefetch_l2_2d(tb1, kp, b_row);
-          } else if (has_next) {  // ... or for the first stages of this block's next tile
-            const int kp = (kb + kPrefetch - kblocks) * BK;
-            tma_prefetch_l2_2d(na, kp, na_row);
-            tma_prefetch_l2_2d(nb0, kp, nb_row);
-            if (EPI == FP8_SWIGLU_Q8) tma_prefetch_l2_2d(nb1, kp, nb_row);
-          }
           if (EPI == FP8_SWIGLU_Q8) {
             tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
             tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);

@@ -27,7 +27,6 @@ constexpr int BK = 64;             // bf16 K per stage: one 128-byte swizzle row
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group + 1
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
-constexpr int kPrefetch = 8;  // K blocks between an L2 prefetch and its load
 
 enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2 };
 
@@ -48,24 +47,27 @@ struct TcParams {
   uint64_t timeout_ns;
 };
 
-template <int BN>
+// Shared memory of one CTA. CG = 2 (a CTA pair) halves the B rows each CTA holds, so a
+// stage is 32 KB instead of 48 KB and six stages fit instead of four.
+template <int BN, int CG>
 struct Smem {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kABytes = BM * BK * 2;          // 16 KB
-  static constexpr int kBBytes = BN * BK * 2;          // 32 KB (BN 256) / 16 KB
+  static constexpr int kABytes = BM * BK * 2;                // 16 KB
+  static constexpr int kBBytes = (BN / CG) * BK * 2;         // this CTA's B rows
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;             // two accumulators
+  static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
+  static constexpr int kTmemCols = 2 * BN;                   // two accumulators
   static constexpr size_t kBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + 256 /*barriers*/ +
                                    2 * kMaxGroups * sizeof(int32_t);
 };
 
-// Tile -> (group, m tile, n tile) from the block's copy of the m-tile prefix.
+// Tile -> (group, m tile, n tile) from the block's copy of the m-tile prefix; tm = rows of
+// an m tile (128, or 256 for a CTA pair).
 struct TileCoord {
-  int g, mb, nb, rows;  // rows: valid rows of this tile (<= BM)
+  int g, mb, nb, rows;  // rows: valid rows of this tile (<= tm)
 };
 
 __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows) {
+                                                 const int32_t* seg_rows, int tm) {
   // largest g with n_tiles * mt_prefix[g] <= tile
   int lo = 0, hi = ngroups - 1;
   while (lo < hi) {
@@ -79,18 +81,25 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_pre
   const int local = tile - n_tiles * mt_prefix[lo];
   c.nb = local / mt;
   c.mb = local - c.nb * mt;
-  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
   return c;
 }
 
-template <int BN, int EPI>
+// CG = 1: one CTA per 128-row tile (tcgen05.mma.cta_group::1, M = 128).
+// CG = 2: a cluster of two CTAs per 256-row tile (cta_group::2, M = 256): each CTA loads its
+// 128 A rows and half of the tile's B rows (SwiGLU: CTA 0 the gate rows, CTA 1 the up rows);
+// the leader (rank 0) waits for both halves on its own barrier, issues the MMAs, and its
+// commits arrive on both CTAs' barriers; each CTA's epilogue drains its own TMEM rows and
+// the second CTA's epilogue reports to the leader's barrier.
+template <int BN, int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmB1x,
                         const TcParams p) {
-  using S = Smem<BN>;
+  using S = Smem<BN, CG>;
   constexpr int STAGES = S::kStages;
+  constexpr int TM = BM * CG;  // rows of an m tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -108,6 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
 
   // ---- per-block setup: barriers, TMEM, and the m-tile prefix over the groups
   if (threadIdx.x == 0) {
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 128 * CG);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -128,16 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
     if (EPI == EPI_SWIGLU_BF16) tma_prefetch_desc(&tmB1);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, S::kTmemCols);
   if (warp == 2) {
-    // rows per group and an exclusive prefix of ceil(rows / BM), 32 groups per step
+    // rows per group and an exclusive prefix of ceil(rows / TM), 32 groups per step
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
       const int g = g0 + lane;
       int rows = 0;
       if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
       else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + BM - 1) / BM;
+      const int mt = (rows + TM - 1) / TM;
       int inc = mt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -154,88 +166,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.n_tiles * mt_prefix[ngroups];
   const int kblocks = p.K / BK;
 
   if (warp == 0) {
-    // ======================= TMA producer
+    // ======================= TMA producer (every CTA loads its own halves)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
         const bool extra = c.g >= p.G;
         const CUtensorMap* ta = extra ? &tmA2 : &tmA;
         const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
         const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
-        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * BM;
-        const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;
-        const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-        const int next = tile + gridDim.x;
-        const bool has_next = next < total_tiles;
-        const CUtensorMap *na = ta, *nb0 = tb0, *nb1 = tb1;
-        int na_row = a_row, nb_row = b_row;
-        if (has_next) {
-          const TileCoord n = decode_tile(next, mt_prefix, ngroups, p.n_tiles, seg_rows);
-          const bool nx = n.g >= p.G;
-          na = nx ? &tmA2 : &tmA;
-          nb0 = nx ? &tmB0x : &tmB0;
-          nb1 = nx ? &tmB1x : &tmB1;
-          na_row = (nx ? p.a2_row_base : p.offsets[n.g]) + n.mb * BM;
-          nb_row = (nx ? 0 : n.g * p.b_group_rows) + n.nb * b_tile_rows;
-        }
+        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
+        const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;  // rows of B per N tile
+        int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        if (CG == 2 && EPI != EPI_SWIGLU_BF16) b_row += (int)rank * (BN / 2);
+        const CUtensorMap* tb_mine = (CG == 2 && EPI == EPI_SWIGLU_BF16 && rank == 1) ? tb1 : tb0;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
           uint8_t* a_dst = sA + stage * S::kABytes;
           uint8_t* b_dst = sB + stage * S::kBBytes;
-          tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
-          if (kb + kPrefetch < kblocks) {  // warm L2 for a later stage of this tile
-            const int kp = (kb + kPrefetch) * BK;
-            tma_prefetch_l2_2d(ta, kp, a_row);
-            tma_prefetch_l2_2d(tb0, kp, b_row);
-            if (EPI == EPI_SWIGLU_BF16) tma_prefetch_l2_2d(tb1, kp, b_row);
-          } else if (has_next) {  // ... or for the first stages of this block's next tile
-            const int kp = (kb + kPrefetch - kblocks) * BK;
-            tma_prefetch_l2_2d(na, kp, na_row);
-            tma_prefetch_l2_2d(nb0, kp, nb_row);
-            if (EPI == EPI_SWIGLU_BF16) tma_prefetch_l2_2d(nb1, kp, nb_row);
-          }
-          if (EPI == EPI_SWIGLU_BF16) {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
-            tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+            tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+            if (EPI == EPI_SWIGLU_BF16) {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
+              tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows
+            } else {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            }
           } else {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            // both CTAs' loads complete on the leader's barrier, which expects both
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
+            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+            tma_load_2d_pair(ta, a_dst, bar, kb * BK, a_row);
+            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
       // tail: every stage's last fill has been consumed (so no TMA write or MMA commit
-      // is still in flight when the block exits); after an abort, only wait for the loads
+      // is still in flight when the block exits); after an abort, only the own loads
       const int used = issued < STAGES ? (int)issued : STAGES;
       for (int i = 0; i < used; ++i) {
         // slot (stage - 1 - i) mod STAGES holds fill number issued - 1 - i
         const int s = (stage - 1 - i + 2 * STAGES) % STAGES;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_make(1u /*bf16*/, BM, BN);
+    // ======================= MMA issuer (the leader of a pair issues for both CTAs)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_make(1u /*bf16*/, TM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -246,33 +245,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_addr(sB + stage * S::kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {  // K = 16 per instruction: +32 bytes in the row
-            mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc,
-                     (kb | k) != 0);
+            if constexpr (CG == 1)
+              mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+            else
+              mma_bf16_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc,
+                            (kb | k) != 0);
           }
-          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          // frees the stage (in both CTAs) once these MMAs have read it
+          if constexpr (CG == 1) mma_commit(&empty[stage]);
+          else mma_commit_pair(&empty[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        if constexpr (CG == 1) mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        else mma_commit_pair(&tfull[acc], 0x3);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      mma_commit(drain);  // completes when every MMA above has
+      if constexpr (CG == 1) mma_commit(drain);  // completes when every MMA above has
+      else mma_commit_pair(drain, 0x3);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    } else if (lane == 0 && CG == 2) {
+      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
   } else {
     // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
     const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
+    const int row_in_tile = (int)rank * BM + quarter * 32 + lane;
+    const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_addr(&tempty[0]), 0) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+    for (int tile = unit; tile < total_tiles; tile += nunits) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
       bool ok = mbar_wait(&tfull[acc], acc_phase, abort, p.timeout_ns, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const bool extra = c.g >= p.G;
-      const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * BM + row_in_tile;
+      const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
       const bool live = row_in_tile < c.rows;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (EPI == EPI_SWIGLU_BF16) {
@@ -343,17 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if (CG == 2 && !leader) mbar_arrive_cluster(tempty_leader + acc * 8);
+      else mbar_arrive(&tempty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    tmem_dealloc_cg<CG>(tmem_base, S::kTmemCols);
   }
 }
 
@@ -408,21 +420,46 @@ int num_sms() {
 
 namespace {
 
-template <int BN, int EPI>
+template <int BN, int EPI, int CG = 1>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
                    const CUtensorMap& b0x, const CUtensorMap& b1x, const TcParams& p, int64_t max_tiles,
                    cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_bf16_kernel<BN, EPI>;
-  const size_t smem = Smem<BN>::kBytes;
+  auto kern = tc_gemm_bf16_kernel<BN, EPI, CG>;
+  const size_t smem = Smem<BN, CG>::kBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-  kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
+  if constexpr (CG == 1) {
+    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+    kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must be resident all at once: no more pairs than fit together
+    static int max_pairs = 0;
+    if (!max_pairs) {
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
+      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+    }
+    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
+    cfg.gridDim = dim3(2 * pairs);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, a2, b0, b1, b0x, b1x, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -494,14 +531,20 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.out = h;
   p.status = st;
   p.timeout_ns = kTimeoutNs;
-  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
-  cudaError_t e = launch<256, EPI_SWIGLU_BF16>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  // CTA pairs (256-row tiles) when experts average at least 512 rows; with fewer rows the
+  // second 128 rows of a pair tile would mostly be padding.
+  const bool pair = (int64_t)c.T * c.k >= 512LL * c.E && c.H % 256 == 0;
+  const int tm = pair ? 2 * BM : BM;
+  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
+  cudaError_t e = pair ? launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+                       : launch<256, EPI_SWIGLU_BF16, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = h Wd^T (the shared expert's h rows follow the routed ones)
   const int bn2 = c.H % 256 == 0 ? 256 : 128;
+  const uint32_t box2 = pair ? bn2 / 2 : bn2;  // a pair's CTAs each load half of the N tile
   CUtensorMap a2, bd, bdx;
-  ok = make_bf16(&a2, h, rows, c.F, BM) && make_bf16(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, bn2);
-  if (shared) ok = ok && make_bf16(&bdx, w.ws_down, c.H, c.F, bn2);
+  ok = make_bf16(&a2, h, rows, c.F, BM) && make_bf16(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, box2);
+  if (shared) ok = ok && make_bf16(&bdx, w.ws_down, c.H, c.F, box2);
   else bdx = bd;
   if (!ok) return cudaErrorInvalidValue;
   p.a2_row_base = (int)R;
@@ -510,8 +553,9 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.b_group_rows = c.H;
   p.ldc = c.H;
   p.out = yd;
-  if (bn2 == 256) return launch<256, EPI_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
-  return launch<128, EPI_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  if (pair) return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  if (bn2 == 256) return launch<256, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  return launch<128, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc

@@ -307,68 +307,78 @@ __global__ void __launch_bounds__(32) scan_assign_kernel(
   }
 }
 
-// S0 for small expert counts (E <= EP <= 32): one warp per TPW tokens. Lanes stride over
-// 16-byte chunks; each chunk of the router weight (E x 16 B, from L1/L2) is loaded once and
-// applied to all TPW tokens, whose E partial dot products each lane keeps in registers,
-// then a warp reduction per (token, expert). fp32 accumulation.
-template <int EP, int TPW, bool BF16>
+// S0 for small expert counts (E <= EP <= 32): one 256-thread block per TB tokens; the
+// threads split the hidden dimension (16-byte chunks c = tid, tid + 256, ...), each keeping
+// TB x E partial dot products, then a warp reduction and a cross-warp sum through smem.
+// Splitting H over the block keeps many independent loads in flight per SM, which is what
+// this memory-bound pass needs. fp32 accumulation.
+template <int EP, int TB, bool BF16>
 __global__ void __launch_bounds__(256) router_small_kernel(const void* __restrict__ x_, const void* __restrict__ w_,
                                                            const float* __restrict__ bias, int T, int H, int E,
                                                            float* __restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
+  __shared__ float part[8][TB][EP];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int EPC = BF16 ? 8 : 4;  // elements per 16-byte chunk
   const int nchunk = H / EPC;
-  for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * TPW; t0 < T; t0 += warps * TPW) {
-    float acc[TPW][EP];
+  const int t0 = blockIdx.x * TB;
+  float acc[TB][EP];
 #pragma unroll
-    for (int i = 0; i < TPW; ++i)
+  for (int i = 0; i < TB; ++i)
 #pragma unroll
-      for (int e = 0; e < EP; ++e) acc[i][e] = 0.0f;
-    for (int c = lane; c < nchunk; c += 32) {
-      float xf[TPW][EPC];
+    for (int e = 0; e < EP; ++e) acc[i][e] = 0.0f;
+  for (int c = threadIdx.x; c < nchunk; c += 256) {
+    float xf[TB][EPC];
 #pragma unroll
-      for (int i = 0; i < TPW; ++i) {
-        const int t = min(t0 + i, T - 1);  // a short last group repeats a row; not stored
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x_) + (int64_t)t * nchunk + c);
-        if (BF16) {
-          const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
+    for (int i = 0; i < TB; ++i) {
+      const int t = min(t0 + i, T - 1);  // a short last block repeats a row; not stored
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x_) + (int64_t)t * nchunk + c);
+      if (BF16) {
+        const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) { xf[i][2 * q] = __uint_as_float(u[q] << 16); xf[i][2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
-        } else {
-          xf[i][0] = __uint_as_float(xv.x); xf[i][1] = __uint_as_float(xv.y);
-          xf[i][2] = __uint_as_float(xv.z); xf[i][3] = __uint_as_float(xv.w);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (e < E) {
-          const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_) + (int64_t)e * nchunk + c);
-          float wf[EPC];
-          if (BF16) {
-            const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) { wf[2 * q] = __uint_as_float(u[q] << 16); wf[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
-          } else {
-            wf[0] = __uint_as_float(wv.x); wf[1] = __uint_as_float(wv.y);
-            wf[2] = __uint_as_float(wv.z); wf[3] = __uint_as_float(wv.w);
-          }
-#pragma unroll
-          for (int i = 0; i < TPW; ++i)
-#pragma unroll
-            for (int q = 0; q < EPC; ++q) acc[i][e] = __fmaf_rn(xf[i][q], wf[q], acc[i][e]);
-        }
+        for (int q = 0; q < 4; ++q) { xf[i][2 * q] = __uint_as_float(u[q] << 16); xf[i][2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
+      } else {
+        xf[i][0] = __uint_as_float(xv.x); xf[i][1] = __uint_as_float(xv.y);
+        xf[i][2] = __uint_as_float(xv.z); xf[i][3] = __uint_as_float(xv.w);
       }
     }
 #pragma unroll
-    for (int i = 0; i < TPW; ++i)
+    for (int e = 0; e < EP; ++e) {
+      if (e < E) {
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_) + (int64_t)e * nchunk + c);
+        float wf[EPC];
+        if (BF16) {
+          const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        float v = acc[i][e];
+          for (int q = 0; q < 4; ++q) { wf[2 * q] = __uint_as_float(u[q] << 16); wf[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u); }
+        } else {
+          wf[0] = __uint_as_float(wv.x); wf[1] = __uint_as_float(wv.y);
+          wf[2] = __uint_as_float(wv.z); wf[3] = __uint_as_float(wv.w);
+        }
 #pragma unroll
-        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-        if (lane == e && e < E && t0 + i < T) logits[(int64_t)(t0 + i) * E + e] = bias ? v + bias[e] : v;
+        for (int i = 0; i < TB; ++i)
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) acc[i][e] = __fmaf_rn(xf[i][q], wf[q], acc[i][e]);
       }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < TB; ++i)
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      float v = acc[i][e];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      if (lane == 0) part[warp][i][e] = v;
+    }
+  __syncthreads();
+  if (threadIdx.x < TB * EP) {
+    const int i = threadIdx.x / EP, e = threadIdx.x % EP;
+    if (e < E && t0 + i < T) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += part[w][i][e];
+      logits[(int64_t)(t0 + i) * E + e] = bias ? v + bias[e] : v;
+    }
   }
 }
 
@@ -383,15 +393,15 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
-  // TPW tokens per warp (fewer for wider E: TPW * EP accumulators per lane), 8 warps a block
-#define MOE_RS(EP, TPW)                                                                                   \
-  if (c.E <= EP) {                                                                                      \
-    const int64_t blocks = std::min<int64_t>(ceil_div(c.T, 8 * TPW), (int64_t)sms * 8);                \
-    if (bf) router_small_kernel<EP, TPW, true><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits); \
-    else router_small_kernel<EP, TPW, false><<<(unsigned)blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits);   \
-    return cudaGetLastError();                                                                          \
+  (void)sms;
+#define MOE_RS(EP, TB)                                                                                \
+  if (c.E <= EP) {                                                                                  \
+    const unsigned blocks = (unsigned)ceil_div(c.T, TB);                                            \
+    if (bf) router_small_kernel<EP, TB, true><<<blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits); \
+    else router_small_kernel<EP, TB, false><<<blocks, 256, 0, s>>>(x, w, bias, c.T, c.H, c.E, logits);   \
+    return cudaGetLastError();                                                                      \
   }
-  MOE_RS(8, 4)
+  MOE_RS(8, 2)
   MOE_RS(16, 2)
   MOE_RS(32, 1)
 #undef MOE_RS
