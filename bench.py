@@ -437,10 +437,15 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct moe_forward calls")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = synth.WORKLOADS[args.workload]
+    if args.tokens or args.experts:
+        w = synth.scaled(w, T=args.tokens or w["T"], E=args.experts or w["E"],
+                         name=f"{w['name']}_T{args.tokens or w['T']}_E{args.experts or w['E']}")
     line = run_reference(args, w) if args.impl == "reference" else run_gpu(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -136,6 +136,17 @@ moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx
                                 int32_t* counts, int32_t* offsets, int32_t* row_token,
                                 int32_t* tok_row, void* ws, moe_stream_t stream);
 
+/* Auxiliary load-balancing loss of the routing (Megatron-Core skill card, Fluxo 2:
+ * load-balancing type "aux_loss" with --moe-aux-loss-coeff, 0.01 there; the pages give no
+ * formula, so the switch-style form is taken):
+ *   loss = alpha * E / (T*k) * sum_e counts[e] * Pbar_e,
+ * Pbar_e = the mean over tokens of expert e's probability: the softmax of the token's logits
+ * over all experts, or its sigmoid scores divided by their sum (score_fn). logits [T,E]
+ * fp32, counts [E] from moe_route; *loss is one device float. Uses the workspace's scan
+ * scratch (stream-ordered after moe_route on the same workspace is fine). Deterministic. */
+moe_status_t moe_aux_loss(const moe_config_t* cfg, const float* logits, const int32_t* counts,
+                          float alpha, float* loss, void* ws, moe_stream_t stream);
+
 /* S3 — dispatch (Hybrid-EP article, dispatch operator): xd[tok_row[t,j]] = x[t], reading
  * each token once. act xfer: xd [R(+T), H] act, bit copy; xd_scale unused (NULL).
  * E4M3 xfer: each token is quantised once in 1x128 blocks (scale = amax/448, codes =
@@ -197,6 +208,13 @@ moe_status_t moe_route_static_scratch(const moe_config_t* cfg, const float* logi
                                       int32_t* topk_idx, float* topk_w, int32_t* counts,
                                       int32_t* offsets, int32_t* row_token, int32_t* tok_row,
                                       int32_t* device_status, moe_stream_t stream);
+
+/* Diagnostic: runs the bounded wait that guards every wait inside the library's tensor-core
+ * kernels on a barrier nothing arrives on. With a working limit it records MOE_ERR_TIMEOUT
+ * in device_status (caller-owned device int32[2], zeroed by the caller) after about
+ * timeout_ns (0 < timeout_ns <= 10 s) and returns, and the context stays usable. */
+moe_status_t moe_selftest_bounded_wait(int64_t timeout_ns, int32_t* device_status,
+                                       moe_stream_t stream);
 
 /* Synchronises `stream`, returns the device status word of `ws` in *device_status
  * (MOE_OK or a moe_status_t code) and clears it. The only call that blocks the host. */

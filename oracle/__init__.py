@@ -70,6 +70,7 @@ def _L():
             "oc_dequant_blocks": (None, [P, P, i64, i64, i32, i32, P]),
             "oc_expert_mlp": (None, [P, i64, i32, i32, P, P, P, i32, P]),
             "oc_combine": (None, [P, P, P, P, i32, i32, i32, P]),
+            "oc_aux_loss": (f64, [P, P, i32, i32, i32, i32, f64, P]),
             "oc_dense_forward": (i32, [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f64, P, P, P, i32, P, P, P, P]),
         }
@@ -215,6 +216,16 @@ def combine(yd, tok_row, topk_w, ys=None) -> np.ndarray:
     y = np.empty((T, H), dtype=np.float64)
     _L().oc_combine(_p(yd), _p(tr), _p(w), _p(ys), T, k, H, _p(y))
     return y
+
+
+def aux_loss(logits, counts, k: int, score_fn: int, alpha: float = 0.01):
+    """(loss, Pbar[E]) of the switch-style load-balancing loss (fp64)."""
+    l = _c(logits, np.float32)
+    c = _c(counts, np.int32)
+    T, E = l.shape
+    pbar = np.empty(E, dtype=np.float64)
+    loss = _L().oc_aux_loss(_p(l), _p(c), T, E, k, score_fn, float(alpha), _p(pbar))
+    return float(loss), pbar
 
 
 # ---------------------------------------------------------------- whole layer

@@ -430,3 +430,39 @@ int oc_dense_forward(const double* x, const float* logits, int T, int H, int E, 
   }
   return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Auxiliary load-balancing loss (Megatron-Core skill card, Fluxo 2: the "aux_loss" load */
+/* balancing type with --moe-aux-loss-coeff 0.01; the pages give no formula). Reading:    */
+/* the switch-style loss  L = alpha * E / (T*k) * sum_e c_e * Pbar_e,  c_e the routed      */
+/* count of expert e and Pbar_e the mean over tokens of the token's probability for e:    */
+/* the softmax over all experts (score_fn 0) or the sigmoid scores divided by their sum    */
+/* over all experts (score_fn 1). fp64.                                                   */
+/* ------------------------------------------------------------------------------------ */
+double oc_aux_loss(const float* logits, const int32_t* counts, int T, int E, int k, int score_fn,
+                   double alpha, double* pbar_out) {
+  double* pbar = (double*)calloc((size_t)E, sizeof(double));
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    double sum = 0.0;
+    if (score_fn == 0) {
+      double m = -INFINITY;
+      for (int e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+      for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - m); sum += p[e]; }
+    } else {
+      for (int e = 0; e < E; ++e) { p[e] = 1.0 / (1.0 + exp(-(double)l[e])); sum += p[e]; }
+    }
+    for (int e = 0; e < E; ++e) pbar[e] += p[e] / sum;
+  }
+  double loss = 0.0;
+  for (int e = 0; e < E; ++e) {
+    pbar[e] /= (double)T;
+    if (pbar_out) pbar_out[e] = pbar[e];
+    loss += (double)counts[e] * pbar[e];
+  }
+  loss *= alpha * (double)E / ((double)T * (double)k);
+  free(p);
+  free(pbar);
+  return loss;
+}

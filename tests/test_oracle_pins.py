@@ -423,3 +423,38 @@ def test_fp8_layer_close_to_unquantised():
     assert np.array_equal(q["topk_idx"], ref["topk_idx"])
     # three e4m3 rounding points (x, weights, h), each up to 2^-4 relative
     assert 1e-3 < oracle.rel_l2(q["y"], ref["y"]) < 0.1
+
+
+# ------------------------------------------------------------------ aux load-balancing loss
+def test_aux_loss_closed_forms():
+    T, E, k = 64, 8, 2
+    c8 = cfg(E, k)
+    # uniform probabilities: Pbar = 1/E, loss = alpha whatever the counts
+    l = np.zeros((T, E), np.float32)
+    idx, _ = oracle.route(l, c8)
+    counts = oracle.permute(idx, E)[0]
+    loss, pbar = oracle.aux_loss(l, counts, k, 0, 0.01)
+    assert np.allclose(pbar, 1.0 / E, rtol=1e-15) and loss == pytest.approx(0.01, rel=1e-14)
+    # all tokens on experts 0 and 1 with equal, dominant logits: Pbar_0 = Pbar_1 -> 1/2,
+    # loss -> alpha * E / k
+    l = np.zeros((T, E), np.float32)
+    l[:, :2] = 40.0
+    idx, _ = oracle.route(l, c8)
+    counts = oracle.permute(idx, E)[0]
+    loss, _ = oracle.aux_loss(l, counts, k, 0, 0.01)
+    assert loss == pytest.approx(0.01 * E / k, rel=1e-12)
+
+
+def test_aux_loss_matches_numpy_definition():
+    T, E, k = 200, 16, 3
+    l = synth.synthetic_logits(12, T, E, 2.0)
+    for score_fn in (0, 1):
+        idx, _ = oracle.route(l, cfg(E, k, score_fn=score_fn))
+        counts = oracle.permute(idx, E)[0]
+        loss, pbar = oracle.aux_loss(l, counts, k, score_fn, 0.01)
+        L = l.astype(np.float64)
+        p = np.exp(L - L.max(1, keepdims=True)) if score_fn == 0 else 1.0 / (1.0 + np.exp(-L))
+        p /= p.sum(1, keepdims=True)
+        ref_pbar = p.mean(0)
+        assert np.allclose(pbar, ref_pbar, rtol=1e-12)
+        assert loss == pytest.approx(0.01 * E / (T * k) * float(np.dot(np.bincount(idx.ravel(), minlength=E), ref_pbar)), rel=1e-12)

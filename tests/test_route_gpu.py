@@ -142,3 +142,20 @@ def test_zero_tokens():
     e = torch.empty(0, device="cuda")
     moe.moe_route(cfg, e, e, e, counts, offsets, e, e, ws)
     assert int(counts.abs().sum()) == 0 and int(offsets.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[3], CASES[4], CASES[10]],
+                         ids=["tiny", "dsv3", "imbalanced", "dsv3_fp8_tokens", "e33_ragged"])
+def test_aux_loss_against_oracle(w):
+    l = logits_of(w, seed=4)
+    idx, _ = oracle.route(l, w)
+    counts = oracle.permute(idx, w["E"])[0]
+    ref, _ = oracle.aux_loss(l, counts, w["k"], w["score_fn"], 0.01)
+    b = alloc(w)
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_aux_loss(b["cfg"], up(l), up(counts), 0.01, loss, b["ws"])
+    got = float(loss.item())
+    assert got == pytest.approx(ref, rel=2e-5)
+    loss2 = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_aux_loss(b["cfg"], up(l), up(counts), 0.01, loss2, b["ws"])
+    assert torch.equal(loss, loss2)  # deterministic

@@ -89,6 +89,7 @@ def lib():
             "moe_router_logits": [cfg, P, P, P, P, P, P],
             "moe_route": [cfg, P, P, P, P, P, P, P, P, P],
             "moe_route_from_map": [cfg, P, P, P, P, P, P, P],
+            "moe_aux_loss": [cfg, P, P, ctypes.c_float, P, P, P],
             "moe_dispatch": [cfg, P, P, P, P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
@@ -96,6 +97,7 @@ def lib():
             "moe_quantize_e4m3": [P, c_int64, c_int64, c_int32, c_int32, P, P, P],
             "moe_read_status": [P, P, POINTER(c_int32)],
             "moe_route_static_scratch": [cfg, P, P, P, P, P, P, P, P, P],
+            "moe_selftest_bounded_wait": [c_int64, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -109,9 +111,10 @@ def lib():
 
 def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
-            "moe_router_logits", "moe_route", "moe_route_from_map", "moe_dispatch",
+            "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
             "moe_grouped_mlp", "moe_combine", "moe_forward", "moe_quantize_e4m3",
-            "moe_read_status", "moe_status_string", "moe_route_static_scratch"]
+            "moe_read_status", "moe_status_string", "moe_route_static_scratch",
+            "moe_selftest_bounded_wait"]
 
 
 def _ptr(t):
@@ -177,6 +180,11 @@ def moe_route_from_map(cfg, topk_idx, counts, offsets, row_token, tok_row, ws, s
            "moe_route_from_map")
 
 
+def moe_aux_loss(cfg, logits, counts, alpha: float, loss, ws, stream=None):
+    _check(lib().moe_aux_loss(byref(cfg), _ptr(logits), _ptr(counts), float(alpha), _ptr(loss), _ptr(ws),
+                              _stream(stream)), "moe_aux_loss")
+
+
 def moe_dispatch(cfg, x, tok_row, xd, xd_scale=None, stream=None):
     _check(lib().moe_dispatch(byref(cfg), _ptr(x), _ptr(tok_row), _ptr(xd), _ptr(xd_scale),
                               _stream(stream)), "moe_dispatch")
@@ -217,6 +225,11 @@ def moe_route_static_scratch(cfg, logits, topk_idx, topk_w, counts, offsets, row
                                           _ptr(counts), _ptr(offsets), _ptr(row_token),
                                           _ptr(tok_row), _ptr(device_status), _stream(stream)),
            "moe_route_static_scratch")
+
+
+def moe_selftest_bounded_wait(timeout_ns: int, device_status, stream=None):
+    _check(lib().moe_selftest_bounded_wait(int(timeout_ns), _ptr(device_status), _stream(stream)),
+           "moe_selftest_bounded_wait")
 
 
 def moe_read_status(ws, stream=None) -> int:

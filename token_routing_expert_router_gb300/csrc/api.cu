@@ -236,6 +236,15 @@ moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx
                                        blockcnt_of(ws), status_of(ws), (cudaStream_t)stream));
 }
 
+moe_status_t moe_aux_loss(const moe_config_t* cfg, const float* logits, const int32_t* counts,
+                          float alpha, float* loss, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!ptr_ok(counts) || !loss || !ptr_ok(ws) || (cfg->T > 0 && !ptr_ok(logits))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_aux_loss(*cfg, logits, counts, alpha, loss, reinterpret_cast<float*>(blockcnt_of(ws)),
+                                     (cudaStream_t)stream));
+}
+
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* tok_row,
                           void* xd, float* xd_scale, moe_stream_t stream) {
   moe_status_t v = validate(cfg);

@@ -41,6 +41,8 @@ cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_
 bool router_small_supported(const moe_config_t& c);
 cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void* w, const float* bias,
                                 float* logits, cudaStream_t s);
+cudaError_t launch_aux_loss(const moe_config_t& c, const float* logits, const int32_t* counts, float alpha,
+                            float* loss, float* part, cudaStream_t s);
 cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
                               int32_t* offsets, int32_t* row_token, int32_t* tok_row,
                               int32_t* blockcnt, DeviceStatus* st, cudaStream_t s);

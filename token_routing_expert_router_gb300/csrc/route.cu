@@ -382,7 +382,89 @@ __global__ void __launch_bounds__(256) router_small_kernel(const void* __restric
   }
 }
 
+// Auxiliary load-balancing loss, pass 1: per block of 128 tokens (8 warps x 16 tokens), the
+// sum over its tokens of each expert's probability (softmax over all experts, or sigmoid
+// scores divided by their sum). Every sum runs in a fixed order: no float atomics.
+template <int NSLOT>
+__global__ void __launch_bounds__(256) aux_pbar_kernel(const float* __restrict__ logits, int T, int E,
+                                                       int score_fn, float* __restrict__ part) {
+  __shared__ float wsum[8][NSLOT * 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[NSLOT];
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) acc[s] = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    const int t = blockIdx.x * 128 + warp * 16 + i;
+    if (t >= T) break;
+    const float* row = logits + (int64_t)t * E;
+    float v[NSLOT];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      const int e = s * 32 + lane;
+      v[s] = e < E ? row[e] : -FLT_MAX;
+      if (e < E) m = fmaxf(m, v[s]);
+    }
+    m = warp_max(m);
+    float sum = 0.0f;
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      const int e = s * 32 + lane;
+      v[s] = e < E ? (score_fn == MOE_SCORE_SOFTMAX ? expf(v[s] - m) : det_sigmoid(v[s])) : 0.0f;
+      sum += v[s];
+    }
+    sum = warp_sum(sum);
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) acc[s] += v[s] / sum;
+  }
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) wsum[warp][s * 32 + lane] = acc[s];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += wsum[w][e];
+    part[(int64_t)blockIdx.x * E + e] = v;
+  }
+}
+
+// Pass 2 (one block): Pbar_e = sum over blocks / T, then
+// loss = alpha * E / (T * k) * sum_e counts[e] * Pbar_e, reduced as a fixed tree.
+__global__ void __launch_bounds__(1024) aux_loss_kernel(const float* __restrict__ part, int NB, int E,
+                                                        const int32_t* __restrict__ counts, int T, int k,
+                                                        float alpha, float* __restrict__ loss) {
+  __shared__ float red[32];
+  float v = 0.0f;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float pb = 0.0f;
+    for (int b = 0; b < NB; ++b) pb += part[(int64_t)b * E + e];
+    v += (float)counts[e] * (pb / (float)T);
+  }
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) *loss = alpha * (float)E / ((float)T * (float)k) * v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_aux_loss(const moe_config_t& c, const float* logits, const int32_t* counts, float alpha,
+                            float* loss, float* part, cudaStream_t s) {
+  const int NB = scan_blocks(c);
+  const int nslot = (int)ceil_div(c.E, 32);
+  if (NB > 0) {
+#define MOE_AUX(NS) \
+  if (nslot <= NS) aux_pbar_kernel<NS><<<NB, 256, 0, s>>>(logits, c.T, c.E, c.score_fn, part); else
+    MOE_AUX(1) MOE_AUX(2) MOE_AUX(4) MOE_AUX(8) MOE_AUX(16) return cudaErrorInvalidValue;
+#undef MOE_AUX
+  }
+  aux_loss_kernel<<<1, 1024, 0, s>>>(part, NB, c.E, counts, c.T > 0 ? c.T : 1, c.k, alpha, loss);
+  return cudaGetLastError();
+}
 
 bool router_small_supported(const moe_config_t& c) { return c.E <= 32; }
 
