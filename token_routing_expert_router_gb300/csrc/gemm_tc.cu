@@ -229,12 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= MMA issuer (the leader of a pair issues for both CTAs)
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_make(1u /*bf16*/, TM, BN);
+      // a single-CTA tile with at most 64 valid rows (a segment's tail) runs as M = 64: half
+      // the MMA work; its rows land in the first 16 lanes of each TMEM lane quarter
+      constexpr uint32_t idesc64 = idesc_make(1u, 64, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
+        const uint32_t id = (CG == 1 && c.rows <= 64) ? idesc64 : idesc;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {  // K = 16 per instruction: +32 bytes in the row
             if constexpr (CG == 1)
-              mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+              mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), id, (kb | k) != 0);
             else
               mma_bf16_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc,
                             (kb | k) != 0);
@@ -271,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
     const int quarter = warp & 3;
-    const int row_in_tile = (int)rank * BM + quarter * 32 + lane;
     const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_addr(&tempty[0]), 0) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -282,8 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool extra = c.g >= p.G;
+      const bool m64 = CG == 1 && c.rows <= 64;  // M = 64 tile: 16 rows per lane quarter
+      const int row_in_tile = m64 ? quarter * 16 + lane : (int)rank * BM + quarter * 32 + lane;
       const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
-      const bool live = row_in_tile < c.rows;
+      const bool live = (!m64 || lane < 16) && row_in_tile < c.rows;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (EPI == EPI_SWIGLU_BF16) {
         // cols [0, BN/2) gate, [BN/2, BN) up -> BN/2 columns of h
