@@ -257,6 +257,9 @@ def run_gpu(args, w):
                                                    b["h_scale"], b["yd"], ws),
         "combine": lambda: moe.moe_combine(cfg, b["yd"], b["tok_row"], b["w"], y),
     }
+    if w["act_dtype"] == synth.BF16 and not fp8:  # the fused-permutation alternative
+        stages["grouped_mlp_gather"] = lambda: moe.moe_grouped_mlp_gather(cfg, x, b["row_token"], b["offsets"],
+                                                                          wts, b["h"], b["yd"], ws)
     for _ in range(2):
         for f in stages.values():
             f()

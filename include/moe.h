@@ -169,6 +169,19 @@ moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const floa
                              const void* x, const int32_t* offsets, const moe_weights_t* w,
                              void* h, float* h_scale, void* yd, void* ws, moe_stream_t stream);
 
+/* S3 + S4 + S5 fused — the grouped expert MLP with the dispatch folded into GEMM1's operand
+ * loads: the memory-efficient permutation of the Megatron-Core summary (section 2.2: the
+ * computation is reorganised so that no redundant intermediate tensor is materialised).
+ * Routed A rows are gathered from x by token (row r reads x[row_token[r]]) four rows per
+ * TMA instruction, so no dispatched copy xd exists; the shared expert reads x directly.
+ * Same outputs as moe_dispatch + moe_grouped_mlp (bit-identical). bf16 layers on the
+ * tensor-core path only (else MOE_ERR_UNSUPPORTED). x [T,H], row_token [T*k], offsets
+ * [E+1], h [R(+T), F], yd [R(+T), H]. moe_forward keeps the separate dispatch: the four-row
+ * gathers are slower on GB300 than the dispatch pass they replace. */
+moe_status_t moe_grouped_mlp_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
+                                    const int32_t* offsets, const moe_weights_t* w, void* h,
+                                    void* yd, void* ws, moe_stream_t stream);
+
 /* S7 — combine (Hybrid-EP article, combine operator with high-precision accumulation):
  * y[t] = sum_{j<k} topk_w[t,j] * yd[tok_row[t,j]]  (+ yd[R + t] with a shared expert),
  * accumulated in fp32 in that fixed order, written once in act dtype. */

@@ -99,3 +99,26 @@ def test_router_logits_real_widths(name, T, H, E):
     moe.moe_router_logits(b["cfg"], d["x"], d["w_router"], None, b["logits"], b["ws"])
     ref = oracle.router_logits(inp["x"], inp["w_router"], None)
     assert oracle.rel_l2(np_of(b["logits"]), ref) < 1e-4
+
+
+BF16_CASES = [c for c in CASES if c["act_dtype"] == synth.BF16 and c["xfer_dtype"] == synth.BF16]
+
+
+@pytest.mark.parametrize("w", BF16_CASES, ids=[c["name"] for c in BF16_CASES])
+def test_gathered_rows_equal_dispatched_rows(w):
+    """The fused permutation: GEMM1 gathering its rows from x by token gives bit-identical h
+    and yd to dispatch + grouped MLP on the dispatched copy."""
+    seed = 5
+    inp = synth.host_inputs(w, seed=seed)
+    idx, wt, (counts, offsets, row_token, tok_row) = routing(w, seed)
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    moe.moe_dispatch(b["cfg"], d["x"], up(tok_row), b["xd"], None)
+    moe.moe_grouped_mlp(b["cfg"], b["xd"], None, d["x"], up(offsets), weights_arg(d), b["h"], None,
+                        b["yd"], b["ws"])
+    h2, yd2 = torch.empty_like(b["h"]), torch.empty_like(b["yd"])
+    moe.moe_grouped_mlp_gather(b["cfg"], d["x"], up(row_token), up(offsets), weights_arg(d), h2, yd2,
+                               b["ws"])
+    assert torch.equal(h2, b["h"])
+    assert torch.equal(yd2, b["yd"])
+    assert moe.moe_read_status(b["ws"]) == moe.MOE_OK

@@ -92,6 +92,7 @@ def lib():
             "moe_aux_loss": [cfg, P, P, ctypes.c_float, P, P, P],
             "moe_dispatch": [cfg, P, P, P, P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
+            "moe_grouped_mlp_gather": [cfg, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
             "moe_forward": [cfg, P, wts, P, P, P, P, P, P],
             "moe_quantize_e4m3": [P, c_int64, c_int64, c_int32, c_int32, P, P, P],
@@ -112,7 +113,7 @@ def lib():
 def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
             "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
-            "moe_grouped_mlp", "moe_combine", "moe_forward", "moe_quantize_e4m3",
+            "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_quantize_e4m3",
             "moe_read_status", "moe_status_string", "moe_route_static_scratch",
             "moe_selftest_bounded_wait"]
 
@@ -195,6 +196,13 @@ def moe_grouped_mlp(cfg, xd, xd_scale, x, offsets, weights: dict, h, h_scale, yd
     _check(lib().moe_grouped_mlp(byref(cfg), _ptr(xd), _ptr(xd_scale), _ptr(x), _ptr(offsets),
                                  byref(w), _ptr(h), _ptr(h_scale), _ptr(yd), _ptr(ws),
                                  _stream(stream)), "moe_grouped_mlp")
+
+
+def moe_grouped_mlp_gather(cfg, x, row_token, offsets, weights: dict, h, yd, ws, stream=None):
+    w = MoEWeights.from_tensors(weights)
+    _check(lib().moe_grouped_mlp_gather(byref(cfg), _ptr(x), _ptr(row_token), _ptr(offsets), byref(w),
+                                        _ptr(h), _ptr(yd), _ptr(ws), _stream(stream)),
+           "moe_grouped_mlp_gather")
 
 
 def moe_combine(cfg, yd, tok_row, topk_w, y, stream=None):

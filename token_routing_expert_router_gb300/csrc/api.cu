@@ -61,6 +61,13 @@ size_t xfer_size(const moe_config_t& c) {
   return c.xfer_dtype == MOE_DTYPE_E4M3 ? 1 : act_size(c);
 }
 
+// Layers the gathered-row GEMM1 (moe_grouped_mlp_gather) takes: bf16 on the tensor cores.
+// moe_forward does not use it: on GB300 the 32 four-row TMA gathers per K block cost more
+// than the separate dispatch pass they save (measured by bench.py as grouped_mlp_gather).
+bool fused_gather(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && c.xfer_dtype == MOE_DTYPE_BF16 && tc::mlp_supported(c);
+}
+
 // moe_forward's workspace: the routing part, then every intermediate.
 struct FwdLayout {
   size_t logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, xd, xd_scale, h, h_scale,
@@ -271,6 +278,21 @@ moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const floa
   if (fp8 && !tc::mlp_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
   return cuda_status(grouped_mlp(*cfg, xd, xd_scale, x, offsets, *w, h, h_scale, yd,
                                  status_of(ws), (cudaStream_t)stream));
+}
+
+moe_status_t moe_grouped_mlp_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
+                                    const int32_t* offsets, const moe_weights_t* w, void* h, void* yd,
+                                    void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->T == 0) return MOE_OK;
+  v = check_weights(*cfg, w, false);
+  if (v != MOE_OK) return v;
+  if (!ptr_ok(x) || !ptr_ok(row_token) || !ptr_ok(offsets) || !ptr_ok(h) || !ptr_ok(yd) || !ptr_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (!fused_gather(*cfg)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(tc::launch_grouped_mlp(*cfg, nullptr, nullptr, x, offsets, *w, h, nullptr, yd, status_of(ws),
+                                            (cudaStream_t)stream, row_token));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* tok_row,

@@ -43,6 +43,8 @@ struct TcParams {
   int ldc;                  // output row length in elements
   void* out;
   const float* bias;        // EPI_STORE_F32_BIAS: [N] or null
+  const int32_t* row_token; // non-null: routed A rows are gathered, row r = token row_token[r]
+                            //   of tmA (a one-row-box map of x); else tmA holds the rows
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
@@ -173,47 +175,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kblocks = p.K / BK;
 
   if (warp == 0) {
-    // ======================= TMA producer (every CTA loads its own halves)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
-        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
-        const bool extra = c.g >= p.G;
-        const CUtensorMap* ta = extra ? &tmA2 : &tmA;
-        const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
-        const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
-        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
-        const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;  // rows of B per N tile
-        int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-        if (CG == 2 && EPI != EPI_SWIGLU_BF16) b_row += (int)rank * (BN / 2);
-        const CUtensorMap* tb_mine = (CG == 2 && EPI == EPI_SWIGLU_BF16 && rank == 1) ? tb1 : tb0;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
-          uint8_t* a_dst = sA + stage * S::kABytes;
-          uint8_t* b_dst = sB + stage * S::kBBytes;
-          if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+    // ======================= TMA producer (every CTA loads its own halves). Lane 0 issues
+    // the box loads; with gathered A rows every lane gathers four of the 128 rows.
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
+      const bool extra = c.g >= p.G;
+      const bool gather = p.row_token != nullptr && !extra;
+      const CUtensorMap* ta = extra ? &tmA2 : &tmA;
+      const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
+      const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
+      const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
+      const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;  // rows of B per N tile
+      int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+      if (CG == 2 && EPI != EPI_SWIGLU_BF16) b_row += (int)rank * (BN / 2);
+      const CUtensorMap* tb_mine = (CG == 2 && EPI == EPI_SWIGLU_BF16 && rank == 1) ? tb1 : tb0;
+      int tok[4] = {0, 0, 0, 0};
+      if (gather) {  // tokens of this lane's rows; rows past the segment repeat its last row
+        const int seg_end = p.offsets[c.g + 1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tok[i] = p.row_token[min(a_row + 4 * lane + i, seg_end - 1)];
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status));
+        if (!ok) break;
+        uint8_t* a_dst = sA + stage * S::kABytes;
+        uint8_t* b_dst = sB + stage * S::kBBytes;
+        if constexpr (CG == 1) {
+          if (lane == 0) mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+          if (gather) {
+            tma_gather4(ta, a_dst + lane * 4 * BK * 2, &full[stage], kb * BK, tok[0], tok[1], tok[2], tok[3]);
+          } else if (lane == 0) {
             tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+          }
+          if (lane == 0) {
             if (EPI == EPI_SWIGLU_BF16) {
               tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
               tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows
             } else {
               tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
             }
-          } else {
-            // both CTAs' loads complete on the leader's barrier, which expects both
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
-            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
-            tma_load_2d_pair(ta, a_dst, bar, kb * BK, a_row);
-            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row);
           }
-          ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        } else {
+          // both CTAs' loads complete on the leader's barrier, which expects both
+          if (lane == 0 && leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
+          const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+          if (gather) {
+            tma_gather4_pair(ta, a_dst + lane * 4 * BK * 2, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
+          } else if (lane == 0) {
+            tma_load_2d_pair(ta, a_dst, bar, kb * BK, a_row);
+          }
+          if (lane == 0) tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row);
         }
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
+    }
+    if (lane == 0) {
       // tail: every stage's last fill has been consumed (so no TMA write or MMA commit
       // is still in flight when the block exits); after an abort, only the own loads
       const int used = issued < STAGES ? (int)issued : STAGES;
@@ -507,14 +528,16 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
 
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale, const void* x,
                                const int32_t* offsets, const moe_weights_t& w, void* h, float* h_scale, void* yd,
-                               DeviceStatus* st, cudaStream_t s) {
+                               DeviceStatus* st, cudaStream_t s, const int32_t* row_token) {
   if (c.xfer_dtype == MOE_DTYPE_E4M3)
     return launch_grouped_mlp_fp8(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
-  // ---- GEMM1: h = silu(A Wg^T) * (A Wu^T), tiles of 128 h columns (256 B rows)
+  // ---- GEMM1: h = silu(A Wg^T) * (A Wu^T), tiles of 128 h columns (256 B rows). A is the
+  // dispatched rows xd, or (row_token given) the token rows of x gathered four at a time.
   CUtensorMap a1, a1x, bg, bu, bgx, bux;
-  bool ok = make_bf16(&a1, xd, rows, c.H, BM) && make_bf16(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
+  bool ok = (row_token ? make_bf16(&a1, x, c.T, c.H, 1) : make_bf16(&a1, xd, rows, c.H, BM)) &&
+            make_bf16(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
             make_bf16(&bu, w.w_up, (uint64_t)c.E * c.F, c.H, 128);
   if (shared) {
     ok = ok && make_bf16(&a1x, x, c.T, c.H, BM) && make_bf16(&bgx, w.ws_gate, c.F, c.H, 128) &&
@@ -535,6 +558,7 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.b_group_rows = c.F;
   p.ldc = c.F;
   p.out = h;
+  p.row_token = row_token;
   p.status = st;
   p.timeout_ns = kTimeoutNs;
   // CTA pairs (256-row tiles) when experts average at least 512 rows; with fewer rows the
@@ -554,6 +578,7 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   else bdx = bd;
   if (!ok) return cudaErrorInvalidValue;
   p.a2_row_base = (int)R;
+  p.row_token = nullptr;
   p.K = c.F;
   p.n_tiles = c.H / bn2;
   p.b_group_rows = c.H;

@@ -13,10 +13,12 @@ bool mlp_supported(const moe_config_t& c);
 cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router,
                           const float* bias, float* logits, DeviceStatus* st, cudaStream_t s);
 
+// row_token non-null (bf16 only): GEMM1 gathers its routed A rows from x by token instead
+// of reading dispatched rows from xd (xd unused).
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
                                const void* x, const int32_t* offsets, const moe_weights_t& w,
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
-                               cudaStream_t s);
+                               cudaStream_t s, const int32_t* row_token = nullptr);
 
 // FP8 (e4m3, fp32 block scales) variant of the grouped MLP.
 bool fp8_supported(const moe_config_t& c);

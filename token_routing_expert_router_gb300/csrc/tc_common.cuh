@@ -137,6 +137,27 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* m, void* dst
       : "memory");
 }
 
+// Row gather: four rows y0..y3 of a tensor whose map has a one-row box, columns [x, x + box
+// width), written as four consecutive 128-byte rows at `dst` (the map's swizzle applies).
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* m, void* dst, uint64_t* bar, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
+// Pair form of the row gather (the mbarrier may be in the other CTA of the pair).
+__device__ __forceinline__ void tma_gather4_pair(const CUtensorMap* m, void* dst, uint32_t bar_cluster, int32_t x,
+                                                 int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation by one warp of the CTA (CG = 1) or by one warp of each CTA of the pair
 // (CG = 2); the address lands in shared memory.
