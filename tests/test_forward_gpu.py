@@ -27,6 +27,8 @@ CASES = [
     synth.scaled(W["imbalanced_bf16"], T=2100, H=256, E=8, k=2, F=256, name="pair_imbalanced"),
     synth.scaled(W["dsv3_bf16"], T=1200, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
                  topk_groups=1, name="pair_shared"),
+    synth.scaled(W["dsv3_fp8"], T=1100, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
+                 topk_groups=1, name="pair_fp8"),
 ]
 
 

@@ -30,15 +30,23 @@ int num_sms();
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;  // BK in elements = bytes (e4m3)
-constexpr int kStages = 4;
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 514;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int kABytes = BM * BK, kBBytes = BN * BK, kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = BM * BK;
 constexpr int kTmemCols = 512;  // two 256-column partial accumulators
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * BM * sizeof(float) +
-                              2 * kMaxGroups * sizeof(int32_t);
+
+// Shared memory of one CTA: CG = 2 (a CTA pair) holds half of the tile's B rows, so a stage
+// is 32 KB and six stages fit instead of four.
+template <int CG>
+struct F8Smem {
+  static constexpr int kBBytes = BN * BK / CG;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
+  static constexpr size_t kBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * BM * sizeof(float) +
+                                   2 * kMaxGroups * sizeof(int32_t);
+};
 
 enum { FP8_SWIGLU_Q8 = 0, FP8_STORE_BF16 = 1 };
 
@@ -68,7 +76,7 @@ struct TileCoord {
 };
 
 __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows) {
+                                                 const int32_t* seg_rows, int tm) {
   int lo = 0, hi = ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -81,8 +89,16 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_pre
   const int local = tile - n_tiles * mt_prefix[lo];
   c.nb = local / mt;
   c.mb = local - c.nb * mt;
-  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
   return c;
+}
+
+// TMEM column of the q-th 16-column chunk a thread of column-half `half` promotes.
+// GEMM1: q 0-3 gate cols [half*64, +64), q 4-7 up cols [128 + half*64, +64);
+// GEMM2: cols [half*128 + 16q, +16).
+template <int EPI>
+__device__ __forceinline__ uint32_t col_of_t(int q, int half) {
+  return EPI == 0 ? (q < 4 ? half * 64 + 16 * q : 128 + half * 64 + 16 * (q - 4)) : half * 128 + 16 * q;
 }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
@@ -93,12 +109,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-template <int EPI>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmB1x,
                        const Fp8Params p) {
+  using S = F8Smem<CG>;
+  constexpr int kStages = S::kStages, kBBytes = S::kBBytes, kStageBytes = S::kStageBytes;
+  constexpr int TM = BM * CG;  // rows of an m tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -117,6 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
+  auto col_of = [](int q, int half) { return col_of_t<EPI>(q, half); };
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -125,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&pfull[a], 1);
-      mbar_init(&pempty[a], kEpiThreads);
+      mbar_init(&pempty[a], kEpiThreads * CG);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -135,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
   if (warp == 2) {
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
@@ -143,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rows = 0;
       if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
       else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + BM - 1) / BM;
+      const int mt = (rows + TM - 1) / TM;
       int inc = mt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -160,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.n_tiles * mt_prefix[ngroups];
@@ -172,26 +196,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
         const bool extra = c.g >= p.G;
         const CUtensorMap* ta = extra ? &tmA2 : &tmA;
         const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
         const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
-        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * BM;
+        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
         const int b_tile_rows = EPI == FP8_SWIGLU_Q8 ? BN / 2 : BN;
-        const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        if (CG == 2 && EPI != FP8_SWIGLU_Q8) b_row += (int)rank * (BN / 2);
+        const CUtensorMap* tb_mine = (CG == 2 && EPI == FP8_SWIGLU_Q8 && rank == 1) ? tb1 : tb0;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
-          tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
-          if (EPI == FP8_SWIGLU_Q8) {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-            tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+            if (EPI == FP8_SWIGLU_Q8) {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+              tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
+            } else {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            }
           } else {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            // both CTAs' loads complete on the leader's barrier, which expects both
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+            tma_load_2d_pair(ta, a_dst, bar, kb * BK, a_row);
+            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -202,19 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (stage - 1 - i + 2 * kStages) % kStages;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer: one partial accumulator per K block
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_make(0u /*e4m3*/, BM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_make(0u /*e4m3*/, TM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int pb = 0;
       uint32_t pphase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&pempty[pb], pphase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           if (!mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status)) { ok = false; break; }
@@ -223,15 +257,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
           const uint32_t d_tmem = tmem_base + pb * BN;
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction: +32 bytes
-            mma_f8(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
-          mma_commit(&empty[stage]);
-          mma_commit(&pfull[pb]);
+          for (int k = 0; k < BK / 32; ++k) {  // K = 32 e4m3 per instruction: +32 bytes
+            if constexpr (CG == 1)
+              mma_f8(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
+            else
+              mma_f8_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
+          }
+          if constexpr (CG == 1) {
+            mma_commit(&empty[stage]);
+            mma_commit(&pfull[pb]);
+          } else {  // both CTAs' stage and partial barriers
+            mma_commit_pair(&empty[stage], 0x3);
+            mma_commit_pair(&pfull[pb], 0x3);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
           if (++pb == 2) { pb = 0; pphase ^= 1; }
         }
       }
-      mma_commit(drain);
+      if constexpr (CG == 1) mma_commit(drain);
+      else mma_commit_pair(drain, 0x3);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    } else if (lane == 0 && CG == 2) {
+      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -244,10 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pphase = 0;
     int tile_parity = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, tile_parity ^= 1) {
-      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+    const uint32_t pempty_leader = CG == 2 ? mapa_shared(smem_addr(&pempty[0]), 0) : 0;
+    for (int tile = unit; tile < total_tiles; tile += nunits, tile_parity ^= 1) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
       const bool extra = c.g >= p.G;
-      const int64_t a_row = (extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g]) + c.mb * BM + r;
+      const int row_in_tile = (int)rank * BM + r;
+      const int64_t a_row = (extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
       const int64_t a_row_c = a_row < p.rows_total ? a_row : p.rows_total - 1;  // dead rows: any scale
       const float* sb0 = (extra ? p.b0x_scale : p.b0_scale + (int64_t)c.g * p.nblk_b * kblocks);
       const float* sb1 = (extra ? p.b1x_scale : p.b1_scale + (int64_t)c.g * p.nblk_b * kblocks);
@@ -280,28 +329,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           const uint32_t t = tmem_base + ((uint32_t)(quarter * 32) << 16) + pb * BN;
+          // software-pipelined: the load of chunk q + 1 is in flight while chunk q's FMAs run
+          uint32_t v[2][16];
+          tmem_ld16(t + col_of(0, half), v[0]);
+          tmem_ld_wait();
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            // GEMM1: q 0-3 gate cols [half*64, +64), q 4-7 up cols [128 + half*64, +64)
-            // GEMM2: cols [half*128 + 16q, +16)
-            const uint32_t col = EPI == FP8_SWIGLU_Q8 ? (q < 4 ? half * 64 + 16 * q : 128 + half * 64 + 16 * (q - 4))
-                                                      : half * 128 + 16 * q;
-            uint32_t v[16];
-            tmem_ld16(t + col, v);
-            tmem_ld_wait();
-            if (q == 7) {
-              tc_fence_before();
-              mbar_arrive(&pempty[pb]);
-            }
+            if (q < 7) tmem_ld16(t + col_of(q + 1, half), v[(q + 1) & 1]);
             const float f = (q < 4) ? fa : fb;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[16 * q + i] = __fmaf_rn(__uint_as_float(v[i]), f, acc[16 * q + i]);
+            for (int i = 0; i < 16; ++i)
+              acc[16 * q + i] = __fmaf_rn(__uint_as_float(v[q & 1][i]), f, acc[16 * q + i]);
+            tmem_ld_wait();
+            if (q == 6) {  // every chunk of this buffer has been read: hand it back to the MMA
+              tc_fence_before();
+              if (CG == 2 && !leader) mbar_arrive_cluster(pempty_leader + pb * 8);
+              else mbar_arrive(&pempty[pb]);
+            }
           }
         }
         if (++pb == 2) { pb = 0; pphase ^= 1; }
       }
-      const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * BM + r;
-      const bool live = ok && r < c.rows;
+      const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
+      const bool live = ok && row_in_tile < c.rows;
       if (EPI == FP8_SWIGLU_Q8) {
         // h = silu(g) * u for this thread's 64 columns; 1x128 requantisation across both halves
         float amax = 0.0f;
@@ -353,10 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_cg<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -364,20 +415,46 @@ bool make_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, box_rows, BK);
 }
 
-template <int EPI>
+template <int EPI, int CG>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
                    const CUtensorMap& b0x, const CUtensorMap& b1x, const Fp8Params& p, int64_t max_tiles,
                    cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_fp8_kernel<EPI>;
-  static bool attr_set = false;
+  auto kern = tc_gemm_fp8_kernel<EPI, CG>;
+  const size_t smem = F8Smem<CG>::kBytes;
+  static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, a2, b0, b1, b0x, b1x, p);
+  if constexpr (CG == 1) {
+    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+    kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must be resident all at once: no more pairs than fit together
+    static int max_pairs = 0;
+    if (!max_pairs) {
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
+      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+    }
+    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
+    cfg.gridDim = dim3(2 * pairs);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, a2, b0, b1, b0x, b1x, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -421,13 +498,20 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.out_scale = h_scale;
   p.status = st;
   p.timeout_ns = kTimeoutNs;
-  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
-  cudaError_t e = launch<FP8_SWIGLU_Q8>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  // Single-CTA tiles. The CTA-pair form (CG = 2) computes the same results but measured
+  // twice as slow on GB300 for this kernel (76 pairs resident, each at half the rate), so
+  // the dispatcher does not select it.
+  const bool pair = false;
+  const int tm = pair ? 2 * BM : BM;
+  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
+  cudaError_t e = pair ? launch<FP8_SWIGLU_Q8, 2>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+                       : launch<FP8_SWIGLU_Q8, 1>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = (h * h_scale) (Wd * s_down)^T, bf16 out
+  const uint32_t box2 = pair ? BN / 2 : BN;  // a pair's CTAs each load half of the N tile
   CUtensorMap a2, bd, bdx;
-  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, BN);
-  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, BN);
+  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, box2);
+  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, box2);
   else bdx = bd;
   if (!ok) return cudaErrorInvalidValue;
   p.K = c.F;
@@ -442,7 +526,8 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.ldc = c.H;
   p.out = yd;
   p.out_scale = nullptr;
-  return launch<FP8_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  return pair ? launch<FP8_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s)
+              : launch<FP8_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc
