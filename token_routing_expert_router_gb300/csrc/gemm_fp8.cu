@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&pfull[a], 1);
-      mbar_init(&pempty[a], kEpiThreads * CG);
+      mbar_init(&pempty[a], (kEpiThreads / 32) * CG);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -343,8 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (q == 6) {  // every chunk of this buffer has been read: hand it back to the MMA
               tc_fence_before();
-              if (CG == 2 && !leader) mbar_arrive_cluster(pempty_leader + pb * 8);
-              else mbar_arrive(&pempty[pb]);
+              __syncwarp();    // all lanes' loads are complete: one arrival per warp
+              if (lane == 0) {
+                if (CG == 2 && !leader) mbar_arrive_cluster(pempty_leader + pb * 8);
+                else mbar_arrive(&pempty[pb]);
+              }
             }
           }
         }
@@ -499,8 +502,9 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.status = st;
   p.timeout_ns = kTimeoutNs;
   // Single-CTA tiles. The CTA-pair form (CG = 2) computes the same results but measured
-  // twice as slow on GB300 for this kernel (76 pairs resident, each at half the rate), so
-  // the dispatcher does not select it.
+  // twice as slow on GB300 (76 pairs resident, each at half the rate): this kernel hands a
+  // partial accumulator between the MMA and the epilogue every K block, and in a pair that
+  // handshake crosses SMs with only two partial buffers to hide it. Not selected.
   const bool pair = false;
   const int tm = pair ? 2 * BM : BM;
   const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
