@@ -14,10 +14,12 @@ plus the independent dense per-token loop that skips the permutation altogether.
 Readings where the pages are silent (each one is a config field, so the oracle and the
 library expose the same choices): the stable ascending-token order inside each expert,
 the lowest-index tie-break, the group score (sum of the two largest sigmoid scores), the
-softmax and sigmoid weight formulas, the routed scale, and the FP8 block-scale rule
-(scale = amax / 448, non-power-of-two fp32). Parity of these readings against the pages
-is unpinned (the pages print no formula or worked example); the tests pin the code to
-brute force, closed forms, library routines and invariants instead.
+softmax and sigmoid weight formulas, the routed scale, the FP8 block-scale rule
+(scale = amax / 448, non-power-of-two fp32) and, for the MXFP8 variant, the OCP MX v1.0
+conversion (1x32 blocks, UE8M0 scale 2^(floor(log2 amax) - 8), saturating e4m3). Parity
+of these readings against the pages is unpinned (the pages print no formula or worked
+example); the tests pin the code to brute force, closed forms, library routines and
+invariants instead.
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ _SRC = os.path.join(_HERE, "moe_oracle.c")
 _SO = os.path.join(_HERE, "_build", "libmoe_oracle.so")
 _lib = None
 
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, MXE4M3 = 0, 1, 2, 3
 SOFTMAX, SIGMOID = 0, 1
 
 
@@ -68,6 +70,8 @@ def _L():
             "oc_e4m3_encode_array": (None, [P, P, i64]),
             "oc_quant_blocks": (None, [P, i64, i64, i32, i32, P, P]),
             "oc_dequant_blocks": (None, [P, P, i64, i64, i32, i32, P]),
+            "oc_mx_quant": (None, [P, i64, i64, P, P]),
+            "oc_mx_dequant": (None, [P, P, i64, i64, P]),
             "oc_expert_mlp": (None, [P, i64, i32, i32, P, P, P, i32, P]),
             "oc_combine": (None, [P, P, P, P, i32, i32, i32, P]),
             "oc_aux_loss": (f64, [P, P, i32, i32, i32, i32, f64, P]),
@@ -194,8 +198,31 @@ def dequant_blocks(q, scale, br: int, bc: int) -> np.ndarray:
     return out
 
 
-def expert_mlp(a, wg, wu, wd, quant_h: bool = False) -> np.ndarray:
-    """One expert's SwiGLU MLP on rows a [n,H] (fp64 values) -> [n,H] fp64."""
+def mx_quant(v):
+    """MX (OCP MXFP8 E4M3) quantisation along rows: e4m3 codes [rows, cols] and UE8M0
+    scale codes [rows, cols/32] (value = decode(q) * 2^(code - 127))."""
+    v = _c(v, np.float32)
+    rows, cols = v.shape
+    if cols % 32:
+        raise ValueError("MX blocks need cols % 32 == 0")
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty((rows, cols // 32), dtype=np.uint8)
+    _L().oc_mx_quant(_p(v), rows, cols, _p(q), _p(sc))
+    return q, sc
+
+
+def mx_dequant(q, sc) -> np.ndarray:
+    q = _c(q, np.uint8)
+    sc = _c(sc, np.uint8)
+    rows, cols = q.shape
+    out = np.empty((rows, cols), dtype=np.float64)
+    _L().oc_mx_dequant(_p(q), _p(sc), rows, cols, _p(out))
+    return out
+
+
+def expert_mlp(a, wg, wu, wd, quant_h=0) -> np.ndarray:
+    """One expert's SwiGLU MLP on rows a [n,H] (fp64 values) -> [n,H] fp64. quant_h: 0 none,
+    1 (or True) 1x128 fp32-scale requantisation of h, 2 MX (1x32 UE8M0) requantisation."""
     a = _c(a, np.float64)
     wg, wu, wd = _c(wg, np.float64), _c(wu, np.float64), _c(wd, np.float64)
     n, H = a.shape
@@ -229,11 +256,14 @@ def aux_loss(logits, counts, k: int, score_fn: int, alpha: float = 0.01):
 
 
 # ---------------------------------------------------------------- whole layer
-def _expert_values(cfg: dict, W: np.ndarray, blocks: bool):
-    """The values an expert weight stands for: the stored values, or for the FP8 variant
-    decode(q) * scale of its 128x128-block quantisation (done here, by the oracle)."""
+def _expert_values(cfg: dict, W: np.ndarray, blocks):
+    """The values an expert weight stands for: the stored values; for the FP8 variant
+    decode(q) * scale of its 128x128-block quantisation; for the MXFP8 variant its 1x32 MX
+    quantisation along the reduction dimension (each done here, by the oracle)."""
     if not blocks:
         return W.astype(np.float64)
+    if blocks == MXE4M3:
+        return mx_dequant(*mx_quant(W))
     q, s = quant_blocks(W, 128, 128)
     return dequant_blocks(q, s, 128, 128)
 
@@ -244,14 +274,20 @@ def forward(cfg: dict, inp: dict, logits=None) -> dict:
     w_down [E,H,F] and, with a shared expert, ws_gate/ws_up [Fs,H], ws_down [H,Fs].
     Returns every intermediate (fp64 where the layer computes in floating point)."""
     T, H, E, k, F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
-    fp8 = cfg["xfer_dtype"] == E4M3
+    xfer = cfg["xfer_dtype"]
+    fp8 = xfer if xfer in (E4M3, MXE4M3) else 0  # which quantisation, 0 = none
+    quant_h = {0: 0, E4M3: 1, MXE4M3: 2}[fp8]
     out = {}
     out["logits"] = router_logits(inp["x"], inp["w_router"], inp.get("router_bias")) if logits is None else logits
     idx, w = route(out["logits"], cfg)
     counts, offsets, row_token, tok_row = permute(idx, E)
     out.update(topk_idx=idx, topk_w=w, counts=counts, offsets=offsets, row_token=row_token,
                tok_row=tok_row)
-    if fp8:
+    if fp8 == MXE4M3:
+        qx, sx = mx_quant(inp["x"])
+        out["x_q"], out["x_scale"] = qx, sx
+        a_tok = mx_dequant(qx, sx)
+    elif fp8:
         qx, sx = quant_blocks(inp["x"], 1, 128)
         out["x_q"], out["x_scale"] = qx, sx
         a_tok = dequant_blocks(qx, sx, 1, 128)
@@ -264,13 +300,13 @@ def forward(cfg: dict, inp: dict, logits=None) -> dict:
         if r1 > r0:
             yd[r0:r1] = expert_mlp(xd[r0:r1], _expert_values(cfg, inp["w_gate"][e], fp8),
                                    _expert_values(cfg, inp["w_up"][e], fp8),
-                                   _expert_values(cfg, inp["w_down"][e], fp8), quant_h=fp8)
+                                   _expert_values(cfg, inp["w_down"][e], fp8), quant_h=quant_h)
     out["yd"] = yd
     ys = None
     if cfg["n_shared"]:
         ys = expert_mlp(a_tok, _expert_values(cfg, inp["ws_gate"], fp8),
                         _expert_values(cfg, inp["ws_up"], fp8),
-                        _expert_values(cfg, inp["ws_down"], fp8), quant_h=fp8)
+                        _expert_values(cfg, inp["ws_down"], fp8), quant_h=quant_h)
     out["ys"] = ys
     out["y"] = combine(yd, tok_row, w, ys)
     return out
@@ -279,7 +315,7 @@ def forward(cfg: dict, inp: dict, logits=None) -> dict:
 def dense_forward(cfg: dict, inp: dict, logits=None) -> np.ndarray:
     """The independent dense per-token loop (no counts, no permutation, no dispatch)."""
     T, H, E, k, F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
-    fp8 = cfg["xfer_dtype"] == E4M3
+    fp8 = cfg["xfer_dtype"] in (E4M3, MXE4M3)
     if logits is None:
         logits = router_logits(inp["x"], inp["w_router"], inp.get("router_bias"))
     l = _c(logits, np.float32)

@@ -326,13 +326,58 @@ void oc_dequant_blocks(const uint8_t* q, const float* scale, int64_t rows, int64
       out[r * cols + c] = oc_e4m3_decode(q[r * cols + c]) * (double)scale[(r / br) * nbc + c / bc];
 }
 
+/* MX block quantisation (the MXFP8 format the Megatron-Core summary and the Hybrid-EP    */
+/* article name for Blackwell; defined by the OCP Microscaling Formats (MX) specification */
+/* v1.0, conversion of a block to MXFP8 E4M3). Every 32 consecutive values of a row share */
+/* one power-of-two scale X = 2^s, stored as the UE8M0 code s + 127:                       */
+/*   s = floor(log2(amax)) - 8   (8 = exponent of the largest e4m3 normal, 448 = 1.75*2^8) */
+/* clamped to [-127, 127]; an all-zero block takes s = -127. Each element is              */
+/* e4m3(v * 2^-s), a correctly rounded fp32 scaling by a power of two, encoded with RNE    */
+/* and saturation to +-448, so the largest element of a block may saturate, as the         */
+/* specification's conversion allows. cols is a multiple of 32; sc is [rows][cols/32].     */
+void oc_mx_quant(const float* v, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sc) {
+  int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t bi = 0; bi < rows * nb; ++bi) {
+    const int64_t off = (bi / nb) * cols + (bi % nb) * 32;
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      float a = fabsf(v[off + i]);
+      if (a > amax) amax = a;
+    }
+    int s = -127;
+    if (amax > 0.0f) {
+      int ex;
+      frexpf(amax, &ex); /* amax = m * 2^ex, m in [0.5, 1): floor(log2(amax)) = ex - 1 */
+      s = ex - 1 - 8;
+      if (s < -127) s = -127;
+      if (s > 127) s = 127;
+    }
+    sc[bi] = (uint8_t)(s + 127);
+    for (int i = 0; i < 32; ++i) {
+      volatile float p = ldexpf(v[off + i], -s);
+      q[off + i] = oc_e4m3_encode(p);
+    }
+  }
+}
+
+/* decode(q) * 2^(code - 127) in fp64 (the exact value of an MX block). */
+void oc_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t cols, double* out) {
+  int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c)
+      out[r * cols + c] = ldexp(oc_e4m3_decode(q[r * cols + c]), (int)sc[r * nb + c / 32] - 127);
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* S4 + S5: one expert's SwiGLU MLP on a set of rows, fp64 ("the experts' GEMMs" of the    */
 /* grouped GEMM; SwiGLU from the workload definition):                                    */
 /*   g = a . Wg^T,  u = a . Wu^T,  h = g / (1 + e^-g) * u,  y = h . Wd^T.                 */
-/* a is [n, H], Wg/Wu [F, H], Wd [H, F] (all fp64 values). If quant_h, h is rounded to     */
+/* a is [n, H], Wg/Wu [F, H], Wd [H, F] (all fp64 values). quant_h 1: h is rounded to     */
 /* fp32 and requantised in 1x128 blocks as the FP8-dispatch variant does before the down   */
-/* projection, and y uses the dequantised h.                                              */
+/* projection; quant_h 2: the same in 1x32 MX blocks (MXFP8 variant). y then uses the      */
+/* dequantised h.                                                                         */
 /* ------------------------------------------------------------------------------------ */
 void oc_expert_mlp(const double* a, int64_t n, int H, int F, const double* wg, const double* wu,
                    const double* wd, int quant_h, double* y) {
@@ -347,13 +392,21 @@ void oc_expert_mlp(const double* a, int64_t n, int H, int F, const double* wg, c
       for (int i = 0; i < H; ++i) { g += ar[i] * wgf[i]; u += ar[i] * wuf[i]; }
       h[f] = g / (1.0 + exp(-g)) * u;
     }
-    if (quant_h) {
+    if (quant_h == 1) {
       float* h32 = (float*)malloc(sizeof(float) * (size_t)F);
       uint8_t* q = (uint8_t*)malloc((size_t)F);
       float* sc = (float*)malloc(sizeof(float) * (size_t)((F + 127) / 128));
       for (int f = 0; f < F; ++f) h32[f] = (float)h[f];
       oc_quant_blocks(h32, 1, F, 1, 128, q, sc);
       for (int f = 0; f < F; ++f) h[f] = oc_e4m3_decode(q[f]) * (double)sc[f / 128];
+      free(h32); free(q); free(sc);
+    } else if (quant_h == 2) {
+      float* h32 = (float*)malloc(sizeof(float) * (size_t)F);
+      uint8_t* q = (uint8_t*)malloc((size_t)F);
+      uint8_t* sc = (uint8_t*)malloc((size_t)(F / 32));
+      for (int f = 0; f < F; ++f) h32[f] = (float)h[f];
+      oc_mx_quant(h32, 1, F, q, sc);
+      oc_mx_dequant(q, sc, 1, F, h);
       free(h32); free(q); free(sc);
     }
     for (int o = 0; o < H; ++o) {

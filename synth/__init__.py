@@ -172,7 +172,7 @@ def zipf_bias(seed: int, E: int, alpha: float = 1.2) -> np.ndarray:
 # k experts per token, F expert FFN width, optional shared expert of width F_shared,
 # score function, renormalisation, G groups with g kept (group-limited routing).
 # ----------------------------------------------------------------------------------------
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, MXE4M3 = 0, 1, 2, 3
 SOFTMAX, SIGMOID = 0, 1
 
 
@@ -193,6 +193,8 @@ WORKLOADS = {
     "imbalanced_bf16": workload("imbalanced_bf16", 16384, 2048, 128, 8, 768, zipf=True),
     "dsv3_fp8": workload("dsv3_fp8", 32768, 7168, 256, 8, 2048, n_shared=1, F_shared=2048,
                          score_fn=SIGMOID, renorm=1, n_groups=8, topk_groups=4, xfer=E4M3),
+    "dsv3_mxfp8": workload("dsv3_mxfp8", 32768, 7168, 256, 8, 2048, n_shared=1, F_shared=2048,
+                           score_fn=SIGMOID, renorm=1, n_groups=8, topk_groups=4, xfer=MXE4M3),
 }
 
 

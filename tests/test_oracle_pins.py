@@ -182,6 +182,79 @@ def test_quant_blocks_128x128():
     assert oracle.rel_l2(dq, w) < 0.05
 
 
+# ------------------------------------------------------------------ MX (MXFP8) quantisation
+def test_mx_quant_worked_points():
+    """Hand-derived points of the OCP MX v1.0 conversion to MXFP8 E4M3 (1x32 blocks)."""
+    v = np.zeros((4, 32), dtype=np.float32)
+    # amax 1.0: s = floor(log2 1) - 8 = -8 (code 119); 1.0 * 2^8 = 256 = 2^8 -> e4m3 0x78;
+    # 0.3 * 2^8 = 76.8 = 9.6 * 2^3 -> mantissa rounds to 10 -> 80 = 1.25 * 2^6 -> 0x6A,
+    # standing for 80 / 256 = 0.3125; -0.5 * 2^8 = -128 -> 0xF0
+    v[0, 0], v[0, 5], v[0, 31] = 1.0, 0.3, -0.5
+    # amax 1.9: s = -8; 1.9 * 256 = 486.4 > 448 saturates to 0x7E (stands for 1.75)
+    v[1, 7], v[1, 8] = 1.9, np.float32(2.0 ** -9)
+    # all-zero block: s = -127 (code 0), every element 0
+    # amax 3 * 2^-140 (an fp32 subnormal): floor(log2) = -139, s = -147 clamps to -127;
+    # 3 * 2^-140 * 2^127 = 3 * 2^-13 is below half the smallest e4m3 subnormal (2^-9) -> 0
+    v[3, 2] = np.float32(3.0) * np.float32(2.0 ** -70) * np.float32(2.0 ** -70)
+    q, sc = oracle.mx_quant(v)
+    assert list(sc[:, 0]) == [119, 119, 0, 0]
+    assert (q[0, 0], q[0, 5], q[0, 31]) == (0x78, 0x6A, 0xF0)
+    assert q[1, 7] == 0x7E
+    # 2^-9 * 2^8 = 0.5 = 2^-1 -> exponent field 6, mantissa 0 -> 0x30
+    assert q[1, 8] == 0x30
+    assert not q[2].any() and not q[3].any()
+    dq = oracle.mx_dequant(q, sc)
+    assert dq[0, 5] == 0.3125 and dq[1, 7] == 1.75 and dq[0, 31] == -0.5
+
+
+def test_mx_quant_scale_invariant_and_error_bound():
+    v = synth.normal(12, 93, (48, 256), 1.0, "bf16")
+    v[5, 64:96] = 0.0
+    v[9, 0:32] *= np.float32(2.0 ** 40)   # scale codes far from the centre of the range
+    v[10, 32:64] *= np.float32(2.0 ** -40)
+    q, sc = oracle.mx_quant(v)
+    assert sc.shape == (48, 8) and sc.dtype == np.uint8
+    blk = np.abs(v.reshape(48, 8, 32)).astype(np.float64)
+    amax = blk.max(-1)
+    s = sc.astype(np.int64) - 127
+    nz = amax > 0
+    # the defining property of s = floor(log2(amax)) - 8: amax * 2^-s in [256, 512)
+    scaled = amax[nz] * np.exp2(-s[nz].astype(np.float64))
+    assert np.all((scaled >= 256) & (scaled < 512))
+    assert np.all(sc[~nz] == 0)
+    dq = oracle.mx_dequant(q, sc)
+    X = np.repeat(np.exp2(s.astype(np.float64)), 32, axis=1)
+    a = np.abs(v).astype(np.float64)
+    sat = a / X > 448
+    # unsaturated: 3 mantissa bits -> relative error <= 2^-4, absolute <= 2^-10 * X below
+    # the smallest normal; saturated elements (in (448, 512) * X) stand for 448 * X
+    bound = np.maximum(a * 2.0 ** -4, X * 2.0 ** -10) * (1 + 1e-9)
+    assert np.all(np.abs(dq - v)[~sat] <= bound[~sat])
+    assert np.array_equal(np.abs(dq[sat]), 448 * X[sat])
+    # in-range codes agree with torch's float8_e4m3fn cast of v * 2^-s (a library routine)
+    prod = (v.astype(np.float64) / X).astype(np.float32)
+    ref = torch.from_numpy(np.clip(prod, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q[~sat], ref[~sat])
+
+
+def test_mx_quant_lossless_on_representable_blocks():
+    """A block whose values are e4m3 values times one power of two, with its largest
+    magnitude in [256, 448] * 2^j, is reproduced exactly: the scale comes out as 2^j."""
+    vals = oracle.e4m3_decode_all()
+    codes = np.arange(256)
+    fin = codes[np.isfinite(vals)]
+    rng = np.random.default_rng(5)
+    rows = []
+    for j in (-20, -8, 0, 3, 30):
+        c = rng.choice(fin, size=32)
+        c[rng.integers(32)] = rng.choice([0x78, 0x7A, 0x7E, 0xFE])  # 256, 320, 448, -448
+        rows.append(vals[c] * 2.0 ** j)
+    v = np.array(rows, dtype=np.float32)
+    q, sc = oracle.mx_quant(v)
+    assert list(sc[:, 0].astype(int) - 127) == [-20, -8, 0, 3, 30]
+    assert np.array_equal(oracle.mx_dequant(q, sc), v.astype(np.float64))
+
+
 # ------------------------------------------------------------------ router logits
 def test_router_logits_fp64_then_round():
     x = synth.normal(0, 1, (64, 96), 1.0, "bf16")
@@ -367,6 +440,20 @@ def test_expert_mlp_quantised_h():
     assert oracle.rel_l2(y, oracle.expert_mlp(a, wg, wu, wd)) < 0.05
 
 
+def test_expert_mlp_mx_quantised_h():
+    n, H, F = 9, 128, 256
+    a = synth.normal(11, 1, (n, H), 1.0, "f32").astype(np.float64)
+    wg = synth.normal(11, 3, (F, H), 0.1, "f32").astype(np.float64)
+    wu = synth.normal(11, 4, (F, H), 0.1, "f32").astype(np.float64)
+    wd = synth.normal(11, 5, (H, F), 0.1, "f32").astype(np.float64)
+    A, G, U = (torch.from_numpy(v) for v in (a, wg, wu))
+    h = (torch.nn.functional.silu(A @ G.T) * (A @ U.T)).numpy().astype(np.float32)
+    ref = oracle.mx_dequant(*oracle.mx_quant(h)) @ wd.T
+    y = oracle.expert_mlp(a, wg, wu, wd, quant_h=2)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+    assert oracle.rel_l2(y, oracle.expert_mlp(a, wg, wu, wd)) < 0.05
+
+
 # ------------------------------------------------------------------ whole layer
 def small(name, **kw):
     return synth.scaled(synth.WORKLOADS[name], **kw)
@@ -423,6 +510,37 @@ def test_fp8_layer_close_to_unquantised():
     assert np.array_equal(q["topk_idx"], ref["topk_idx"])
     # three e4m3 rounding points (x, weights, h), each up to 2^-4 relative
     assert 1e-3 < oracle.rel_l2(q["y"], ref["y"]) < 0.1
+
+
+def test_mxfp8_layer_close_to_unquantised():
+    w = small("dsv3_mxfp8", T=32, H=256, E=16, F=128, F_shared=128, n_groups=4, topk_groups=2)
+    inp = synth.host_inputs(w, seed=4)
+    q = oracle.forward(w, inp)
+    ref = oracle.forward(dict(w, xfer_dtype=synth.BF16), inp)
+    assert np.array_equal(q["topk_idx"], ref["topk_idx"])
+    assert q["x_scale"].shape == (32, 256 // 32)
+    # three e4m3 rounding points (x, weights, h) with power-of-two block scales
+    assert 1e-3 < oracle.rel_l2(q["y"], ref["y"]) < 0.1
+
+
+def test_mxfp8_layer_with_representable_inputs_is_exact_before_h():
+    """With x and every weight already MX-representable, the MXFP8 layer differs from the
+    unquantised one only through the requantisation of h (checked step by step)."""
+    w = small("dsv3_mxfp8", T=16, H=128, E=4, k=2, F=64, n_shared=0, F_shared=0, n_groups=1,
+              topk_groups=1)
+    inp = synth.host_inputs(w, seed=6)
+    for key in ("x", "w_gate", "w_up", "w_down"):
+        a = inp[key]
+        flat = a.reshape(-1, a.shape[-1])
+        inp[key] = oracle.mx_dequant(*oracle.mx_quant(flat)).astype(np.float32).reshape(a.shape)
+    q = oracle.forward(w, inp)
+    assert np.array_equal(oracle.mx_dequant(q["x_q"], q["x_scale"]), inp["x"].astype(np.float64))
+    y = np.zeros_like(q["yd"])
+    for e in range(w["E"]):
+        r0, r1 = q["offsets"][e], q["offsets"][e + 1]
+        a = inp["x"][q["row_token"][r0:r1]].astype(np.float64)
+        y[r0:r1] = oracle.expert_mlp(a, inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], quant_h=2)
+    assert np.array_equal(y, q["yd"])
 
 
 # ------------------------------------------------------------------ aux load-balancing loss
