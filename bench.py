@@ -73,7 +73,13 @@ def describe(w):
     return (f"{w['name']} (T={w['T']}, H={w['H']}, E={w['E']}, k={w['k']}, F={w['F']}"
             + (f", shared F={w['F_shared']}" if w["n_shared"] else "")
             + (f", groups {w['topk_groups']}/{w['n_groups']}" if w["n_groups"] > 1 else "")
-            + (", e4m3 transfer" if w["xfer_dtype"] == synth.E4M3 else "") + ")")
+            + (", e4m3 transfer (1x128 / 128x128 fp32 scales)" if w["xfer_dtype"] == synth.E4M3 else "")
+            + (", MXFP8 transfer (e4m3, 1x32 UE8M0 scales)" if w["xfer_dtype"] == synth.MXE4M3 else "") + ")")
+
+
+def quant_kind(w):
+    """0 unquantised, 1 FP8 with fp32 block scales, 2 MXFP8."""
+    return {synth.E4M3: 1, synth.MXE4M3: 2}.get(w["xfer_dtype"], 0)
 
 
 def algorithmic(w):
@@ -81,14 +87,17 @@ def algorithmic(w):
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
     R = T * k
     a = 4 if w["act_dtype"] == synth.F32 else 2
-    x8 = w["xfer_dtype"] == synth.E4M3
+    qk = quant_kind(w)
+    x8 = qk != 0
     xs = 1 if x8 else a
     shared = T if w["n_shared"] else 0
     d = {}
     d["gemm_flops"] = synth.gemm_flops(w)
     d["router_flops"] = 2.0 * T * H * E
+    # x read once, the k (+1 shared) rows written, tok_row read, and the scales written:
+    # fp32 per 1x128 block, or one UE8M0 byte per 1x32 block (plus the expert ids read)
     d["dispatch_bytes"] = T * H * a + (R + (shared if x8 else 0)) * H * xs + R * 4 \
-        + ((R + shared) * (H // 128) * 4 if x8 else 0)
+        + ((R + shared) * (H // 128) * 4 if qk == 1 else 0) + ((R + shared) * (H // 32) + R * 4 if qk == 2 else 0)
     d["combine_bytes"] = (R + shared) * H * a + T * H * a + R * 8
     d["weight_bytes"] = (E * 3 * F * H + (3 * w["F_shared"] * H if w["n_shared"] else 0)) * xs
     return d
@@ -176,17 +185,22 @@ def run_gpu(args, w):
         wts["ws_gate"] = gen((F, H), synth.WS_GATE, s)
         wts["ws_up"] = gen((F, H), synth.WS_UP, s)
         wts["ws_down"] = gen((H, F), synth.WS_DOWN, s)
-    if w["xfer_dtype"] == synth.E4M3:
+    if quant_kind(w):
         pairs = [("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")]
         if w["n_shared"]:
             pairs += [("ws_gate", "ss_gate"), ("ws_up", "ss_up"), ("ws_down", "ss_down")]
         for wn, sn in pairs:
             src = wts[wn].reshape(-1, wts[wn].shape[-1])
             q = torch.empty(src.shape, dtype=torch.uint8, device=dev)
-            sc = torch.empty((src.shape[0] // 128, src.shape[1] // 128), dtype=torch.float32, device=dev)
-            moe.moe_quantize_e4m3(src, 128, 128, q, sc)
+            if quant_kind(w) == 2:
+                sc = torch.empty((src.shape[0] // 128) * (src.shape[1] // 128) * 512, dtype=torch.uint8, device=dev)
+                moe.moe_quantize_mx(src, q, sc)
+            else:
+                sc = torch.empty((src.shape[0] // 128, src.shape[1] // 128), dtype=torch.float32, device=dev)
+                moe.moe_quantize_e4m3(src, 128, 128, q, sc)
             wts[wn] = q.reshape(wts[wn].shape)
             wts[sn] = sc
+            del src
     cfg = moe.MoEConfig.make(**{kk: w[kk] for kk in (
         "T", "H", "E", "k", "F", "n_shared", "F_shared", "score_fn", "renorm", "n_groups",
         "topk_groups", "group_score", "routed_scale", "act_dtype", "xfer_dtype")})
@@ -234,8 +248,15 @@ def run_gpu(args, w):
     # ---- per-stage times through the staged entry points (same kernels)
     R = T * k
     rows = R + (T if w["n_shared"] else 0)
-    fp8 = w["xfer_dtype"] == synth.E4M3
+    qk = quant_kind(w)
+    fp8 = qk != 0
     xdt = torch.uint8 if fp8 else dt
+
+    def act_scales(K):
+        if qk == 2:
+            return torch.empty(moe.moe_mx_scale_bytes(cfg, K), dtype=torch.uint8, device=dev)
+        return torch.empty((K // 128, rows), dtype=torch.float32, device=dev) if qk == 1 else None
+
     b = {"logits": torch.empty((T, E), dtype=torch.float32, device=dev),
          "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
          "w": torch.empty((T, k), dtype=torch.float32, device=dev),
@@ -244,15 +265,17 @@ def run_gpu(args, w):
          "row_token": torch.empty(R, dtype=torch.int32, device=dev),
          "tok_row": torch.empty((T, k), dtype=torch.int32, device=dev),
          "xd": torch.empty((rows, H), dtype=xdt, device=dev),
-         "xd_scale": torch.empty((H // 128, rows), dtype=torch.float32, device=dev) if fp8 else None,
+         "xd_scale": act_scales(H),
          "h": torch.empty((rows, F), dtype=xdt, device=dev),
-         "h_scale": torch.empty((F // 128, rows), dtype=torch.float32, device=dev) if fp8 else None,
+         "h_scale": act_scales(F),
          "yd": torch.empty((rows, H), dtype=dt, device=dev)}
     stages = {
         "router_logits": lambda: moe.moe_router_logits(cfg, x, wts["w_router"], wts["router_bias"], b["logits"], ws),
         "route": lambda: moe.moe_route(cfg, b["logits"], b["idx"], b["w"], b["counts"], b["offsets"],
                                        b["row_token"], b["tok_row"], ws),
-        "dispatch": lambda: moe.moe_dispatch(cfg, x, b["tok_row"], b["xd"], b["xd_scale"]),
+        "dispatch": (lambda: moe.moe_dispatch_mx(cfg, x, b["idx"], b["tok_row"], b["offsets"], b["xd"],
+                                                 b["xd_scale"])) if qk == 2 else
+                    (lambda: moe.moe_dispatch(cfg, x, b["tok_row"], b["xd"], b["xd_scale"])),
         "grouped_mlp": lambda: moe.moe_grouped_mlp(cfg, b["xd"], b["xd_scale"], x, b["offsets"], wts, b["h"],
                                                    b["h_scale"], b["yd"], ws),
         "combine": lambda: moe.moe_combine(cfg, b["yd"], b["tok_row"], b["w"], y),
@@ -314,7 +337,7 @@ def run_gpu(args, w):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3+bf16" if fp8 else ("bf16" if w["act_dtype"] == synth.BF16 else "f32"),
+        "dtype": {1: "e4m3+bf16", 2: "mxfp8(e4m3,ue8m0)+bf16"}.get(qk, "bf16" if w["act_dtype"] == synth.BF16 else "f32"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset or trained weights)",
         "config": {"workload": describe(w), "tokens_per_gpu": T, "parallelism": f"replicas x{world} (token-sharded)",
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
@@ -356,9 +379,14 @@ def cpu_baseline(w, n_tokens, seed=0):
     """The oracle as it stands, on n_tokens tokens of the workload (fp64, OpenMP)."""
     import oracle
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
-    fp8 = w["xfer_dtype"] == synth.E4M3
+    qk = quant_kind(w)
     dt = synth.act_name(w)
     toks = np.arange(n_tokens)
+
+    def qw(m):  # the oracle's own quantisation of a weight matrix
+        if qk == 1:
+            return oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128)
+        return oracle.mx_dequant(*oracle.mx_quant(m)) if qk == 2 else m
     x = synth.rows(seed, synth.X, toks, H, 1.0, dt)
     wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], dt)
     bias = synth.zipf_bias(0, E) if w["zipf"] else None
@@ -368,9 +396,11 @@ def cpu_baseline(w, n_tokens, seed=0):
     sub = dict(w, T=n_tokens)
     idx, wt = oracle.route(logits, sub)
     counts, offsets, row_token, tok_row = oracle.permute(idx, E)
-    if fp8:
+    if qk == 1:
         q, sc = oracle.quant_blocks(x, 1, 128)
         a = oracle.dequant_blocks(q, sc, 1, 128)
+    elif qk == 2:
+        a = oracle.mx_dequant(*oracle.mx_quant(x))
     else:
         a = x.astype(np.float64)
     xd = a[row_token]
@@ -382,9 +412,8 @@ def cpu_baseline(w, n_tokens, seed=0):
             continue
         g, u, d = synth.expert_weights(w, 0, e)  # drawing the weights is not timed
         t0 = time.perf_counter()
-        if fp8:
-            g, u, d = (oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
-        yd[r0:r1] = oracle.expert_mlp(xd[r0:r1], g, u, d, quant_h=fp8)
+        g, u, d = qw(g), qw(u), qw(d)
+        yd[r0:r1] = oracle.expert_mlp(xd[r0:r1], g, u, d, quant_h=qk)
         t_or += time.perf_counter() - t0
     ys = None
     if w["n_shared"]:
@@ -393,9 +422,8 @@ def cpu_baseline(w, n_tokens, seed=0):
         u = synth.normal(0, synth.WS_UP, (Fs, H), w["w_std"], dt)
         d = synth.normal(0, synth.WS_DOWN, (H, Fs), w["w_std"], dt)
         t0 = time.perf_counter()
-        if fp8:
-            g, u, d = (oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
-        ys = oracle.expert_mlp(a, g, u, d, quant_h=fp8)
+        g, u, d = qw(g), qw(u), qw(d)
+        ys = oracle.expert_mlp(a, g, u, d, quant_h=qk)
         t_or += time.perf_counter() - t0
     t0 = time.perf_counter()
     oracle.combine(yd, tok_row, wt, ys)

@@ -15,6 +15,7 @@
  *   moe_route           S1  top-k (optionally group-limited) + weights, then S2
  *   moe_route_from_map  S2  counts, offsets and the permutation from a given map (replay)
  *   moe_dispatch        S3  xd[r] = x[row_token[r]] (FP8: quantised once per token)
+ *   moe_dispatch_mx     S3  the same for the MXFP8 variant (1x32 blocks, UE8M0 scales)
  *   moe_grouped_mlp     S4-S6  per expert: h = silu(xd Wg^T) * (xd Wu^T); yd = h Wd^T
  *   moe_combine         S7  y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ shared row)
  *   moe_forward         S0-S7 in one stream-ordered call
@@ -57,7 +58,10 @@ typedef enum {
 } moe_status_t;
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
-enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1, MOE_DTYPE_E4M3 = 2 };
+/* MOE_DTYPE_E4M3: e4m3 with fp32 scales per 1x128 (activations) / 128x128 (weights) block.
+ * MOE_DTYPE_MXE4M3: MXFP8 (OCP Microscaling v1.0): e4m3 with one power-of-two UE8M0 scale
+ * per 1x32 block of every row, stored in scale atoms (below). */
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1, MOE_DTYPE_E4M3 = 2, MOE_DTYPE_MXE4M3 = 3 };
 enum { MOE_GROUP_SCORE_TOP2_SUM = 0, MOE_GROUP_SCORE_MAX = 1 };
 
 /* Layer configuration: plain values, no pointers. */
@@ -72,27 +76,44 @@ typedef struct {
   int32_t group_score; /* MOE_GROUP_SCORE_*: sum of the two largest scores, or the max */
   float routed_scale;  /* every routed weight is multiplied by this (1.0) */
   int32_t act_dtype;   /* MOE_DTYPE_F32 or MOE_DTYPE_BF16: x, router and (unless E4M3) expert weights, y */
-  int32_t xfer_dtype;  /* = act_dtype, or MOE_DTYPE_E4M3 (bf16 act only): dispatched rows and expert GEMMs in e4m3 */
+  int32_t xfer_dtype;  /* = act_dtype, or MOE_DTYPE_E4M3 / MOE_DTYPE_MXE4M3 (bf16 act only): dispatched rows and expert GEMMs in e4m3 */
 } moe_config_t;
 
-/* Layer weights (device pointers). act = act_dtype; q = e4m3 when xfer_dtype is E4M3,
- * else act. E4M3 weights carry fp32 scales per 128x128 block (value = code * scale). */
+/* Layer weights (device pointers). act = act_dtype; q = e4m3 when xfer_dtype is E4M3 or
+ * MXE4M3, else act. E4M3 weights carry fp32 scales per 128x128 block (value = code *
+ * scale, [rows/128, cols/128] row-major); MXE4M3 weights carry the UE8M0 scale atoms of
+ * their rows (moe_quantize_mx: tile a = rows [128a, 128a + 128)). The s_* / ss_* fields are
+ * NULL for unquantised layers. */
 typedef struct {
   const void* w_router;     /* [E, H] act */
   const float* router_bias; /* [E] fp32 added to every logit, or NULL */
   const void* w_gate;       /* [E, F, H] q */
   const void* w_up;         /* [E, F, H] q */
   const void* w_down;       /* [E, H, F] q */
-  const float* s_gate;      /* E4M3 only: [E, F/128, H/128] */
-  const float* s_up;        /* E4M3 only: [E, F/128, H/128] */
-  const float* s_down;      /* E4M3 only: [E, H/128, F/128] */
+  const void* s_gate;       /* E4M3: fp32 [E, F/128, H/128]; MXE4M3: atoms of [E*F, H] */
+  const void* s_up;         /* E4M3: fp32 [E, F/128, H/128]; MXE4M3: atoms of [E*F, H] */
+  const void* s_down;       /* E4M3: fp32 [E, H/128, F/128]; MXE4M3: atoms of [E*H, F] */
   const void* ws_gate;      /* shared expert [F, H] q, or NULL when n_shared = 0 */
   const void* ws_up;        /* [F, H] q */
   const void* ws_down;      /* [H, F] q */
-  const float* ss_gate;     /* E4M3 only: [F/128, H/128] */
-  const float* ss_up;       /* E4M3 only: [F/128, H/128] */
-  const float* ss_down;     /* E4M3 only: [H/128, F/128] */
+  const void* ss_gate;      /* E4M3: fp32 [F/128, H/128]; MXE4M3: atoms of [F, H] */
+  const void* ss_up;        /* E4M3: fp32 [F/128, H/128]; MXE4M3: atoms of [F, H] */
+  const void* ss_down;      /* E4M3: fp32 [H/128, F/128]; MXE4M3: atoms of [H, F] */
 } moe_weights_t;
+
+/* MX scale atoms. The UE8M0 codes (code = s + 127 for the block scale 2^s) of an e4m3
+ * matrix with K columns (K a multiple of 128) are stored in 512-byte atoms, each covering
+ * 128 rows ("tile" a) and one 128-column K stage ks (four 1x32 blocks kb = 0..3): atom
+ * (a, ks) begins at byte (a * (K/128) + ks) * 512, and the code of the tile's row i and
+ * block kb is at byte (i % 32) * 16 + (i / 32) * 4 + kb of the atom. This is the order in
+ * which the block-scaled tensor-core MMA reads scale factors, so one copy per atom feeds it.
+ *  - Weights: tile a holds rows [128a, 128a + 128).
+ *  - Grouped activations (dispatched rows, h): the rows of expert e (e = E: the shared
+ *    expert, whose offset is offsets[E] = T*k) start a fresh tile at
+ *    base(e) = ceil((offsets[e] + 127 * e) / 128), and row r of expert e is row
+ *    (r - offsets[e]) % 128 of tile base(e) + (r - offsets[e]) / 128. The buffer size
+ *    comes from moe_mx_scale_bytes. Tile rows past an expert's last row are never written
+ *    and never read into a result. */
 
 /* Bytes of device workspace needed by every call below except moe_forward (the status
  * word plus the routing scan's per-block counts). Zero it once with moe_workspace_init. */
@@ -156,18 +177,38 @@ moe_status_t moe_aux_loss(const moe_config_t* cfg, const float* logits, const in
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* tok_row,
                           void* xd, float* xd_scale, moe_stream_t stream);
 
+/* S3 for the MXFP8 variant (xfer_dtype = MOE_DTYPE_MXE4M3; moe_dispatch returns
+ * MOE_ERR_UNSUPPORTED for it). Each token is quantised once in 1x32 blocks (OCP MX v1.0:
+ * s = floor(log2(amax)) - 8 clamped to [-127, 127], s = -127 for an all-zero block; codes
+ * e4m3_rn_satfinite(v * 2^-s)) and written to its k rows xd[tok_row[t,j]] and, with a
+ * shared expert, to row R + t; the UE8M0 codes go to the rows' places in the scale atoms
+ * xd_sf (layout above: needs the expert of each row, hence topk_idx [T,k] and offsets
+ * [E+1] from moe_route). xd [R(+T), H] e4m3; xd_sf moe_mx_scale_bytes(cfg, H, ...) bytes.
+ * H % 128 == 0. A routed row whose expert id is outside [0, E) gets no scales. */
+moe_status_t moe_dispatch_mx(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                             const int32_t* tok_row, const int32_t* offsets, void* xd, void* xd_sf,
+                             moe_stream_t stream);
+
+/* Bytes of an MX scale-atom buffer for the grouped activations of `cfg` with K columns
+ * (K = H for moe_dispatch_mx's xd_sf, K = F for moe_grouped_mlp's h_scale). K % 128 == 0. */
+moe_status_t moe_mx_scale_bytes(const moe_config_t* cfg, int32_t K, size_t* bytes);
+
 /* S4 + S5 + S6 — the experts as one grouped GEMM (Megatron-Core summary section 2.4).
  * For expert e, rows r in [offsets[e], offsets[e+1]) of xd:
  *     h[r]  = silu(xd[r] . Wg[e]^T) * (xd[r] . Wu[e]^T),  silu(z) = z / (1 + e^-z)
  *     yd[r] = h[r] . Wd[e]^T
  * and, with a shared expert, the same for rows R + t with A = x[t] (act xfer) or the
- * dispatched row R + t (E4M3 xfer) and weights ws_*. The per-expert row counts are read
- * on the device; empty experts cost nothing. h [R(+T), F] act, or e4m3 with h_scale
- * [F/128, R(+T)] requantised in 1x128 blocks (E4M3 xfer); yd [R(+T), H] act.
- * `x` may be NULL unless act xfer with a shared expert. */
-moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const float* xd_scale,
+ * dispatched row R + t (E4M3 / MXE4M3 xfer) and weights ws_*. The per-expert row counts
+ * are read on the device; empty experts cost nothing. h [R(+T), F] act, or e4m3 (E4M3 /
+ * MXE4M3 xfer) requantised from fp32 before the down projection: in 1x128 blocks with
+ * h_scale fp32 [F/128, R(+T)] (E4M3), or in 1x32 MX blocks with h_scale the scale atoms
+ * of h (MXE4M3, moe_mx_scale_bytes(cfg, F, ...) bytes); yd [R(+T), H] act. xd_scale: the
+ * dispatched rows' scales (fp32 [H/128, R(+T)] for E4M3, atoms for MXE4M3), NULL otherwise.
+ * MXE4M3 runs the block-scaled tensor-core MMA (the hardware applies the scales) and needs
+ * H % 256 == 0, F % 128 == 0. `x` may be NULL unless act xfer with a shared expert. */
+moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const void* xd_scale,
                              const void* x, const int32_t* offsets, const moe_weights_t* w,
-                             void* h, float* h_scale, void* yd, void* ws, moe_stream_t stream);
+                             void* h, void* h_scale, void* yd, void* ws, moe_stream_t stream);
 
 /* S3 + S4 + S5 fused — the grouped expert MLP with the dispatch folded into GEMM1's operand
  * loads: the memory-efficient permutation of the Megatron-Core summary (section 2.2: the
@@ -200,6 +241,14 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
  * [ceil(rows/br), ceil(cols/bc)] fp32 row-major. br, bc in {1, 128}. */
 moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols, int32_t br,
                                int32_t bc, uint8_t* q, float* scale, moe_stream_t stream);
+
+/* Offline weight preparation for the MXFP8 variant: quantise a bf16 [rows, cols] matrix
+ * along its rows in 1x32 blocks with the rule of moe_dispatch_mx; q [rows, cols] e4m3, sf
+ * the scale atoms with tile a = rows [128a, 128a + 128): (rows/128) * (cols/128) * 512
+ * bytes. rows % 128 == 0 and cols % 128 == 0 (else MOE_ERR_UNSUPPORTED). For the expert
+ * weights pass [E*F, H] (gate, up) and [E*H, F] (down). */
+moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q,
+                             uint8_t* sf, moe_stream_t stream);
 
 /* moe_route for callers that cannot allocate device memory. The paper has no counterpart:
  * this is a library convenience. It computes exactly what moe_route computes (same kernels,

@@ -35,20 +35,71 @@ def quantize_dev(src: torch.Tensor, br: int, bc: int):
     return q, s
 
 
+def quantize_mx_dev(src: torch.Tensor):
+    """MX quantisation on the GPU: e4m3 codes and the scale atoms of the rows."""
+    rows, cols = src.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((rows // 128) * (cols // 128) * 512, dtype=torch.uint8, device="cuda")
+    moe.moe_quantize_mx(src, q, sf)
+    return q, sf
+
+
+def is_quant(w: dict) -> bool:
+    return w["xfer_dtype"] in (synth.E4M3, synth.MXE4M3)
+
+
 def _attach_fp8(w: dict, d: dict) -> dict:
-    """Replace expert weights by their e4m3 128x128-block quantisation (on the GPU)."""
-    if w["xfer_dtype"] != synth.E4M3:
+    """Replace expert weights by their e4m3 quantisation (on the GPU): 128x128 blocks with
+    fp32 scales, or 1x32 MX blocks with scale atoms."""
+    if not is_quant(w):
         return d
     names = [("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")]
     if w["n_shared"]:
         names += [("ws_gate", "ss_gate"), ("ws_up", "ss_up"), ("ws_down", "ss_down")]
     for wn, sn in names:
         src = d[wn]
-        q, s = quantize_dev(src.reshape(-1, src.shape[-1]), 128, 128)
+        if w["xfer_dtype"] == synth.MXE4M3:
+            q, s = quantize_mx_dev(src.reshape(-1, src.shape[-1]))
+        else:
+            q, s = quantize_dev(src.reshape(-1, src.shape[-1]), 128, 128)
         d[wn + "_bf16"] = src
         d[wn] = q.reshape(src.shape)
         d[sn] = s
     return d
+
+
+# ---------------------------------------------------------------- MX scale-atom layout
+# The byte of (row, 1x32 block) in a scale-atom buffer, as the C header documents it:
+# atom (a, ks) at (a * K/128 + ks) * 512, row i of the atom's 128 and block kb of the
+# stage's four at (i % 32) * 16 + (i // 32) * 4 + kb.
+def mx_atom_offsets(atom_row: np.ndarray, row_in_tile: np.ndarray, K: int) -> np.ndarray:
+    b = np.arange(K // 32)
+    ks, kb = b // 4, b % 4
+    a = atom_row.astype(np.int64)[:, None]
+    i = row_in_tile.astype(np.int64)[:, None]
+    return ((a * (K // 128) + ks[None, :]) << 9) + (i % 32) * 16 + (i // 32) * 4 + kb[None, :]
+
+
+def mx_weight_rows(rows: int):
+    r = np.arange(rows)
+    return r // 128, r % 128
+
+
+def mx_grouped_rows(offsets: np.ndarray, T: int, k: int, E: int, shared: bool):
+    """(atom row, row in tile) of every dispatched row: expert e's rows start a fresh tile
+    at ceil((offsets[e] + 127 e) / 128); the shared expert is e = E with offset T*k."""
+    R = T * k
+    r = np.arange(R, dtype=np.int64)
+    off = offsets.astype(np.int64)
+    g = np.searchsorted(off, r, side="right") - 1
+    gofs = off[g]
+    if shared:
+        g = np.concatenate([g, np.full(T, E)])
+        gofs = np.concatenate([gofs, np.full(T, R)])
+        r = np.concatenate([r, R + np.arange(T)])
+    base = (gofs + 127 * g + 127) // 128
+    local = r - gofs
+    return base + local // 128, local % 128
 
 
 def device_weights_from_host(w: dict, inp: dict) -> dict:
@@ -96,8 +147,13 @@ def alloc(w: dict) -> dict:
     rows = R + (T if w["n_shared"] else 0)
     dt = tdtype(w)
     fp8 = w["xfer_dtype"] == synth.E4M3
-    xdt = torch.uint8 if fp8 else dt
+    mx = w["xfer_dtype"] == synth.MXE4M3
+    xdt = torch.uint8 if (fp8 or mx) else dt
     cfg = cfg_of(w)
+
+    def mx_sf(K):  # filled with 0xFF (NaN scales): a read of an unwritten slot shows
+        return torch.full((moe.moe_mx_scale_bytes(cfg, K),), 0xFF, dtype=torch.uint8, device="cuda")
+
     b = {
         "cfg": cfg,
         "ws": torch.zeros(max(moe.moe_workspace_size(cfg), 256) // 4 + 64, dtype=torch.int32, device="cuda"),
@@ -109,9 +165,11 @@ def alloc(w: dict) -> dict:
         "row_token": torch.empty(R, dtype=torch.int32, device="cuda"),
         "tok_row": torch.empty((T, k), dtype=torch.int32, device="cuda"),
         "xd": torch.empty((rows, H), dtype=xdt, device="cuda"),
-        "xd_scale": torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None,
+        "xd_scale": torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else (
+            mx_sf(H) if mx else None),
         "h": torch.empty((rows, F), dtype=xdt, device="cuda"),
-        "h_scale": torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None,
+        "h_scale": torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else (
+            mx_sf(F) if mx else None),
         "yd": torch.empty((rows, H), dtype=dt, device="cuda"),
         "y": torch.empty((T, H), dtype=dt, device="cuda"),
     }
@@ -128,7 +186,10 @@ def run_staged(w: dict, d: dict, b: dict, logits: torch.Tensor | None = None):
         logits = b["logits"]
     moe.moe_route(cfg, logits, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"],
                   b["row_token"], b["tok_row"], b["ws"])
-    moe.moe_dispatch(cfg, d["x"], b["tok_row"], b["xd"], b["xd_scale"])
+    if w["xfer_dtype"] == synth.MXE4M3:
+        moe.moe_dispatch_mx(cfg, d["x"], b["topk_idx"], b["tok_row"], b["offsets"], b["xd"], b["xd_scale"])
+    else:
+        moe.moe_dispatch(cfg, d["x"], b["tok_row"], b["xd"], b["xd_scale"])
     moe.moe_grouped_mlp(cfg, b["xd"], b["xd_scale"], d["x"], b["offsets"], weights_arg(d),
                         b["h"], b["h_scale"], b["yd"], b["ws"])
     moe.moe_combine(cfg, b["yd"], b["tok_row"], b["topk_w"], b["y"])

@@ -29,11 +29,14 @@ CASES = [
                  topk_groups=1, name="pair_shared"),
     synth.scaled(W["dsv3_fp8"], T=1100, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
                  topk_groups=1, name="pair_fp8"),
+    synth.scaled(W["dsv3_mxfp8"], T=256, H=512, E=32, F=256, F_shared=256, name="mxfp8_small"),
+    synth.scaled(W["dsv3_mxfp8"], T=900, H=1024, E=8, k=2, F=384, F_shared=384, n_groups=2,
+                 topk_groups=1, name="mxfp8_deep_k"),
 ]
 
 
 def tol(w):
-    if w["xfer_dtype"] == synth.E4M3:
+    if w["xfer_dtype"] in (synth.E4M3, synth.MXE4M3):
         return 3e-2
     return 1e-5 if w["act_dtype"] == synth.F32 else 1e-2
 

@@ -12,12 +12,35 @@ import torch
 import oracle
 import synth
 import token_routing_expert_router_gb300 as moe
-from moe_case import cfg_of, device_weights_generated, np_of, routing_ambiguity, up, weights_arg
+from moe_case import (cfg_of, device_weights_generated, mx_atom_offsets, mx_grouped_rows, np_of, routing_ambiguity,
+                      up, weights_arg)
 
 pytestmark = pytest.mark.gpu
 
-NAMES = ["mixtral_bf16", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8"]
-SAMPLE_TOKENS = {"mixtral_bf16": 6, "dsv3_bf16": 4, "imbalanced_bf16": 8, "dsv3_fp8": 3}
+NAMES = ["mixtral_bf16", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8", "dsv3_mxfp8"]
+SAMPLE_TOKENS = {"mixtral_bf16": 6, "dsv3_bf16": 4, "imbalanced_bf16": 8, "dsv3_fp8": 3, "dsv3_mxfp8": 3}
+
+
+def qmode(w):
+    """0 unquantised, 1 FP8 with fp32 block scales, 2 MXFP8 (the oracle's quant_h codes)."""
+    return {synth.E4M3: 1, synth.MXE4M3: 2}.get(w["xfer_dtype"], 0)
+
+
+def quant_act(a, mode):
+    """The values the dispatched rows stand for, quantised by the oracle."""
+    if mode == 1:
+        return oracle.dequant_blocks(*oracle.quant_blocks(a, 1, 128), 1, 128)
+    if mode == 2:
+        return oracle.mx_dequant(*oracle.mx_quant(a))
+    return a.astype(np.float64)
+
+
+def quant_weight(m, mode):
+    if mode == 1:
+        return oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128)
+    if mode == 2:
+        return oracle.mx_dequant(*oracle.mx_quant(m))
+    return m.astype(np.float64)
 
 
 class Layer:
@@ -73,20 +96,15 @@ def sample_tokens(w, n, seed=5):
     return np.unique(np.concatenate([[0, T - 1], rng.astype(np.int64)]))
 
 
-def host_expert(w, e, fp8):
-    g, u, d = synth.expert_weights(w, 0, e)
-    if fp8:
-        return tuple(oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in (g, u, d))
-    return g.astype(np.float64), u.astype(np.float64), d.astype(np.float64)
+def host_expert(w, e, mode):
+    return tuple(quant_weight(m, mode) for m in synth.expert_weights(w, 0, e))
 
 
-def host_shared(w, fp8):
+def host_shared(w, mode):
     H, Fs, s, dt = w["H"], w["F_shared"], w["w_std"], synth.act_name(w)
     mats = (synth.normal(0, synth.WS_GATE, (Fs, H), s, dt), synth.normal(0, synth.WS_UP, (Fs, H), s, dt),
             synth.normal(0, synth.WS_DOWN, (H, Fs), s, dt))
-    if fp8:
-        return tuple(oracle.dequant_blocks(*oracle.quant_blocks(m, 128, 128), 128, 128) for m in mats)
-    return tuple(m.astype(np.float64) for m in mats)
+    return tuple(quant_weight(m, mode) for m in mats)
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -107,7 +125,7 @@ def test_fullsize_generator_twin_and_router_logits(name):
 def test_fullsize_layer_sampled_tokens(name):
     L = layer(name)
     w = L.w
-    fp8 = w["xfer_dtype"] == synth.E4M3
+    mode = qmode(w)
     T, H, E, k = w["T"], w["H"], w["E"], w["k"]
     toks = sample_tokens(w, SAMPLE_TOKENS[name])
     counts = np_of(L.cnt)
@@ -123,45 +141,47 @@ def test_fullsize_layer_sampled_tokens(name):
     idx_gpu = np_of(L.idx)[toks]
     same = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
     assert np.all(same | amb)
-    if fp8:
-        q, s = oracle.quant_blocks(xs, 1, 128)
-        a = oracle.dequant_blocks(q, s, 1, 128)
-    else:
-        a = xs.astype(np.float64)
+    a = quant_act(xs, mode)
     y_ref = np.zeros((len(toks), H))
     for e in sorted(set(idx_ref[same].ravel().tolist())):
-        mats = host_expert(w, e, fp8)
+        mats = host_expert(w, e, mode)
         for i in np.nonzero(same)[0]:
             for j in range(k):
                 if idx_ref[i, j] == e:
-                    y_ref[i] += wt_ref[i, j] * oracle.expert_mlp(a[i:i + 1], *mats, quant_h=fp8)[0]
+                    y_ref[i] += wt_ref[i, j] * oracle.expert_mlp(a[i:i + 1], *mats, quant_h=mode)[0]
     if w["n_shared"]:
-        y_ref += oracle.expert_mlp(a, *host_shared(w, fp8), quant_h=fp8)
+        y_ref += oracle.expert_mlp(a, *host_shared(w, mode), quant_h=mode)
     got = np_of(L.y)[toks].astype(np.float64)
-    tol = 3e-2 if fp8 else 1e-2
+    tol = 3e-2 if mode else 1e-2
     err = oracle.rel_l2(got[same], y_ref[same])
     assert err < tol, err
 
 
-@pytest.mark.parametrize("name", ["dsv3_bf16", "dsv3_fp8"])
+@pytest.mark.parametrize("name", ["dsv3_bf16", "dsv3_fp8", "dsv3_mxfp8"])
 def test_fullsize_dispatch_and_expert_rows(name):
     """Dispatch of the full batch with the oracle's own routing of generator scores, then the
     grouped MLP on it; sampled rows of three experts and of the shared expert."""
     L = layer(name)
     w = L.w
-    fp8 = w["xfer_dtype"] == synth.E4M3
+    mode = qmode(w)
+    fp8, mx = mode == 1, mode == 2
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
     R = T * k
     rows = R + T
     l = synth.synthetic_logits(7, T, E)
     idx, wt = oracle.route(l, w)
     counts, offsets, row_token, tok_row = oracle.permute(idx, E)
-    xdt = torch.uint8 if fp8 else torch.bfloat16
+    xdt = torch.uint8 if mode else torch.bfloat16
     xd = torch.empty((rows, H), dtype=xdt, device="cuda")
-    xs = torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
-    moe.moe_dispatch(L.cfg, L.d["x"], up(tok_row), xd, xs)
+    if mx:
+        xs = torch.empty(moe.moe_mx_scale_bytes(L.cfg, H), dtype=torch.uint8, device="cuda")
+        hs = torch.empty(moe.moe_mx_scale_bytes(L.cfg, F), dtype=torch.uint8, device="cuda")
+        moe.moe_dispatch_mx(L.cfg, L.d["x"], up(idx), up(tok_row), up(offsets), xd, xs)
+    else:
+        xs = torch.empty((H // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
+        hs = torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
+        moe.moe_dispatch(L.cfg, L.d["x"], up(tok_row), xd, xs)
     h = torch.empty((rows, F), dtype=xdt, device="cuda")
-    hs = torch.empty((F // 128, rows), dtype=torch.float32, device="cuda") if fp8 else None
     yd = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda")
     moe.moe_grouped_mlp(L.cfg, xd, xs, L.d["x"], up(offsets), weights_arg(L.d), h, hs, yd, L.ws)
     torch.cuda.synchronize()
@@ -173,7 +193,12 @@ def test_fullsize_dispatch_and_expert_rows(name):
         q, s = oracle.quant_blocks(xt, 1, 128)
         assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), q)
         assert np.array_equal(np_of(xs[:, torch.from_numpy(pick).cuda()]).T, s)
-        a_rows = oracle.dequant_blocks(q, s, 1, 128)
+    elif mx:
+        q, s = oracle.mx_quant(xt)
+        assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), q)
+        arow, irow = mx_grouped_rows(offsets, T, k, E, True)
+        pos = mx_atom_offsets(arow[pick], irow[pick], H)
+        assert np.array_equal(np_of(xs[torch.from_numpy(pos.ravel()).cuda()]).reshape(pos.shape), s)
     else:
         assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), xt)
     # sampled rows of three experts (first, largest, last non-empty) and of the shared expert
@@ -184,22 +209,16 @@ def test_fullsize_dispatch_and_expert_rows(name):
     for e in experts:
         r0, r1 = offsets[e], offsets[e + 1]
         rr = np.unique(np.array([r0, (r0 + r1) // 2, r1 - 1]))
-        xa = synth.rows(0, synth.X, row_token[rr], H, 1.0, "bf16")
-        if fp8:
-            qa, sa = oracle.quant_blocks(xa, 1, 128)
-            xa = oracle.dequant_blocks(qa, sa, 1, 128)
-        ref_all.append(oracle.expert_mlp(xa, *host_expert(w, e, fp8), quant_h=fp8))
+        xa = quant_act(synth.rows(0, synth.X, row_token[rr], H, 1.0, "bf16"), mode)
+        ref_all.append(oracle.expert_mlp(xa, *host_expert(w, e, mode), quant_h=mode))
         got_all.append(np_of(yd[torch.from_numpy(rr).cuda()]))
     ts = np.array([0, T // 2, T - 1])
-    xa = synth.rows(0, synth.X, ts, H, 1.0, "bf16")
-    if fp8:
-        qa, sa = oracle.quant_blocks(xa, 1, 128)
-        xa = oracle.dequant_blocks(qa, sa, 1, 128)
-    ref_all.append(oracle.expert_mlp(xa, *host_shared(w, fp8), quant_h=fp8))
+    xa = quant_act(synth.rows(0, synth.X, ts, H, 1.0, "bf16"), mode)
+    ref_all.append(oracle.expert_mlp(xa, *host_shared(w, mode), quant_h=mode))
     got_all.append(np_of(yd[torch.from_numpy(R + ts).cuda()]))
     got = np.concatenate(got_all).astype(np.float64)
     ref = np.concatenate(ref_all)
-    assert oracle.rel_l2(got, ref) < (3e-2 if fp8 else 1e-2)
+    assert oracle.rel_l2(got, ref) < (3e-2 if mode else 1e-2)
 
 
 @pytest.mark.parametrize("name", ["dsv3_bf16", "imbalanced_bf16"])

@@ -13,7 +13,7 @@ from ctypes import c_float, c_int32, c_int64, c_size_t, c_void_p, POINTER, byref
 
 from ._build import build as _build_lib, LIB as _LIB_PATH
 
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, MXE4M3 = 0, 1, 2, 3
 SOFTMAX, SIGMOID = 0, 1
 GROUP_TOP2_SUM, GROUP_MAX = 0, 1
 
@@ -91,6 +91,9 @@ def lib():
             "moe_route_from_map": [cfg, P, P, P, P, P, P, P],
             "moe_aux_loss": [cfg, P, P, ctypes.c_float, P, P, P],
             "moe_dispatch": [cfg, P, P, P, P, P],
+            "moe_dispatch_mx": [cfg, P, P, P, P, P, P, P],
+            "moe_mx_scale_bytes": [cfg, c_int32, POINTER(c_size_t)],
+            "moe_quantize_mx": [P, c_int64, c_int64, P, P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
             "moe_grouped_mlp_gather": [cfg, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
@@ -114,6 +117,7 @@ def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
             "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
             "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_quantize_e4m3",
+            "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
             "moe_read_status", "moe_status_string", "moe_route_static_scratch",
             "moe_selftest_bounded_wait"]
 
@@ -191,6 +195,17 @@ def moe_dispatch(cfg, x, tok_row, xd, xd_scale=None, stream=None):
                               _stream(stream)), "moe_dispatch")
 
 
+def moe_dispatch_mx(cfg, x, topk_idx, tok_row, offsets, xd, xd_sf, stream=None):
+    _check(lib().moe_dispatch_mx(byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(tok_row), _ptr(offsets), _ptr(xd),
+                                 _ptr(xd_sf), _stream(stream)), "moe_dispatch_mx")
+
+
+def moe_mx_scale_bytes(cfg: MoEConfig, K: int) -> int:
+    n = c_size_t()
+    _check(lib().moe_mx_scale_bytes(byref(cfg), int(K), byref(n)), "moe_mx_scale_bytes")
+    return n.value
+
+
 def moe_grouped_mlp(cfg, xd, xd_scale, x, offsets, weights: dict, h, h_scale, yd, ws, stream=None):
     w = MoEWeights.from_tensors(weights)
     _check(lib().moe_grouped_mlp(byref(cfg), _ptr(xd), _ptr(xd_scale), _ptr(x), _ptr(offsets),
@@ -221,6 +236,11 @@ def moe_quantize_e4m3(src, br: int, bc: int, q, scale, stream=None):
     rows, cols = src.shape
     _check(lib().moe_quantize_e4m3(_ptr(src), rows, cols, br, bc, _ptr(q), _ptr(scale),
                                    _stream(stream)), "moe_quantize_e4m3")
+
+
+def moe_quantize_mx(src, q, sf, stream=None):
+    rows, cols = src.shape
+    _check(lib().moe_quantize_mx(_ptr(src), rows, cols, _ptr(q), _ptr(sf), _stream(stream)), "moe_quantize_mx")
 
 
 def moe_route_static_scratch(cfg, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row,

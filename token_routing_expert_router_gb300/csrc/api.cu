@@ -5,6 +5,7 @@
 
 #include "moe_internal.cuh"
 #include "gemm_tc.cuh"
+#include "mx_common.cuh"
 
 using namespace moe;
 
@@ -28,13 +29,14 @@ moe_status_t validate(const moe_config_t* c) {
     if ((int64_t)c->topk_groups * (c->E / c->n_groups) < c->k) return MOE_ERR_INVALID_ARG;
   }
   if (c->act_dtype != MOE_DTYPE_F32 && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->xfer_dtype != c->act_dtype && c->xfer_dtype != MOE_DTYPE_E4M3) return MOE_ERR_INVALID_ARG;
-  if (c->xfer_dtype == MOE_DTYPE_E4M3 && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool quant = c->xfer_dtype == MOE_DTYPE_E4M3 || c->xfer_dtype == MOE_DTYPE_MXE4M3;
+  if (c->xfer_dtype != c->act_dtype && !quant) return MOE_ERR_INVALID_ARG;
+  if (quant && c->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_UNSUPPORTED;
   if (c->n_shared && c->F_shared != c->F) return MOE_ERR_UNSUPPORTED;
   // rows move as 8-element (16-byte bf16) steps in dispatch and combine
   if (c->H % 8 || c->F % 8) return MOE_ERR_UNSUPPORTED;
-  if (c->xfer_dtype == MOE_DTYPE_E4M3 && (c->H % 128 || c->F % 128)) return MOE_ERR_UNSUPPORTED;
+  if (quant && (c->H % 128 || c->F % 128)) return MOE_ERR_UNSUPPORTED;
   if (total_rows(*c) >= (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -57,8 +59,15 @@ size_t route_ws_bytes(const moe_config_t& c) {
 }
 
 size_t act_size(const moe_config_t& c) { return c.act_dtype == MOE_DTYPE_BF16 ? 2 : 4; }
-size_t xfer_size(const moe_config_t& c) {
-  return c.xfer_dtype == MOE_DTYPE_E4M3 ? 1 : act_size(c);
+bool is_mx(const moe_config_t& c) { return c.xfer_dtype == MOE_DTYPE_MXE4M3; }
+bool is_quant(const moe_config_t& c) { return c.xfer_dtype == MOE_DTYPE_E4M3 || is_mx(c); }
+size_t xfer_size(const moe_config_t& c) { return is_quant(c) ? 1 : act_size(c); }
+
+// Bytes of the scales of the grouped activations with K columns.
+size_t act_scale_bytes(const moe_config_t& c, int K) {
+  if (c.xfer_dtype == MOE_DTYPE_E4M3) return (size_t)total_rows(c) * (K / 128) * 4;
+  if (is_mx(c)) return (size_t)mx_act_atom_rows(c) * (K / 128) * 512;
+  return 0;
 }
 
 // Layers the gathered-row GEMM1 (moe_grouped_mlp_gather) takes: bf16 on the tensor cores.
@@ -83,7 +92,6 @@ FwdLayout fwd_layout(const moe_config_t& c) {
     return at;
   };
   const int64_t Tk = (int64_t)c.T * c.k, rows = total_rows(c);
-  const bool fp8 = c.xfer_dtype == MOE_DTYPE_E4M3;
   L.logits = take((size_t)c.T * c.E * 4);
   L.topk_idx = take((size_t)Tk * 4);
   L.topk_w = take((size_t)Tk * 4);
@@ -92,9 +100,9 @@ FwdLayout fwd_layout(const moe_config_t& c) {
   L.row_token = take((size_t)Tk * 4);
   L.tok_row = take((size_t)Tk * 4);
   L.xd = take((size_t)rows * c.H * xfer_size(c));
-  L.xd_scale = take(fp8 ? (size_t)rows * (c.H / 128) * 4 : 0);
+  L.xd_scale = take(act_scale_bytes(c, c.H));
   L.h = take((size_t)rows * c.F * xfer_size(c));
-  L.h_scale = take(fp8 ? (size_t)rows * (c.F / 128) * 4 : 0);
+  L.h_scale = take(act_scale_bytes(c, c.F));
   L.yd = take((size_t)rows * c.H * act_size(c));
   L.total = o;
   return L;
@@ -105,7 +113,7 @@ moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* w, bool n
   if (need_router && !ptr_ok(w->w_router)) return MOE_ERR_INVALID_ARG;
   if (w->router_bias && !aligned16(w->router_bias)) return MOE_ERR_INVALID_ARG;
   if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up) || !ptr_ok(w->w_down)) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = c.xfer_dtype == MOE_DTYPE_E4M3;
+  const bool fp8 = is_quant(c);
   if (fp8 && (!ptr_ok(w->s_gate) || !ptr_ok(w->s_up) || !ptr_ok(w->s_down))) return MOE_ERR_INVALID_ARG;
   if (c.n_shared) {
     if (!ptr_ok(w->ws_gate) || !ptr_ok(w->ws_up) || !ptr_ok(w->ws_down)) return MOE_ERR_INVALID_ARG;
@@ -133,12 +141,14 @@ cudaError_t router_logits(const moe_config_t& c, const void* x, const void* w_ro
   return launch_simt_gemm(a, s);
 }
 
-cudaError_t grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
+cudaError_t grouped_mlp(const moe_config_t& c, const void* xd, const void* xd_scale,
                         const void* x, const int32_t* offsets, const moe_weights_t& w, void* h,
-                        float* h_scale, void* yd, DeviceStatus* st, cudaStream_t s) {
+                        void* h_scale, void* yd, DeviceStatus* st, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
+  if (is_mx(c)) return tc::launch_grouped_mlp_mx(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
   if (tc::mlp_supported(c))
-    return tc::launch_grouped_mlp(c, xd, xd_scale, x, offsets, w, h, h_scale, yd, st, s);
+    return tc::launch_grouped_mlp(c, xd, static_cast<const float*>(xd_scale), x, offsets, w, h,
+                                  static_cast<float*>(h_scale), yd, st, s);
   // exact-fp32 FFMA path (fp32 layers, and bf16 shapes the tensor-core tiles do not take)
   const int64_t R = routed_rows(c);
   SimtGemmArgs a{};
@@ -258,19 +268,41 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (v != MOE_OK) return v;
   if (cfg->T == 0) return MOE_OK;
   if (!ptr_ok(x) || !ptr_ok(tok_row) || !ptr_ok(xd)) return MOE_ERR_INVALID_ARG;
+  if (is_mx(*cfg)) return MOE_ERR_UNSUPPORTED;  // moe_dispatch_mx
   if (cfg->xfer_dtype == MOE_DTYPE_E4M3 && !ptr_ok(xd_scale)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_dispatch(*cfg, x, tok_row, xd, xd_scale, (cudaStream_t)stream));
 }
 
-moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const float* xd_scale,
+moe_status_t moe_dispatch_mx(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                             const int32_t* tok_row, const int32_t* offsets, void* xd, void* xd_sf,
+                             moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!is_mx(*cfg)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(topk_idx) || !ptr_ok(tok_row) || !ptr_ok(offsets) || !ptr_ok(xd) || !ptr_ok(xd_sf))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch_mx(*cfg, x, topk_idx, tok_row, offsets, xd, xd_sf, (cudaStream_t)stream));
+}
+
+moe_status_t moe_mx_scale_bytes(const moe_config_t* cfg, int32_t K, size_t* bytes) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!bytes || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 128) return MOE_ERR_UNSUPPORTED;
+  *bytes = (size_t)mx_act_atom_rows(*cfg) * (K / 128) * 512;
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const void* xd_scale,
                              const void* x, const int32_t* offsets, const moe_weights_t* w,
-                             void* h, float* h_scale, void* yd, void* ws, moe_stream_t stream) {
+                             void* h, void* h_scale, void* yd, void* ws, moe_stream_t stream) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (cfg->T == 0) return MOE_OK;
   v = check_weights(*cfg, w, false);
   if (v != MOE_OK) return v;
-  const bool fp8 = cfg->xfer_dtype == MOE_DTYPE_E4M3;
+  const bool fp8 = is_quant(*cfg);
   if (!ptr_ok(xd) || !ptr_ok(offsets) || !ptr_ok(h) || !ptr_ok(yd) || !ptr_ok(ws))
     return MOE_ERR_INVALID_ARG;
   if (fp8 && (!ptr_ok(xd_scale) || !ptr_ok(h_scale))) return MOE_ERR_INVALID_ARG;
@@ -317,7 +349,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
       (counts_out && !aligned16(counts_out)))
     return MOE_ERR_INVALID_ARG;
   const moe_config_t& c = *cfg;
-  if (c.xfer_dtype == MOE_DTYPE_E4M3 && !tc::mlp_supported(c)) return MOE_ERR_UNSUPPORTED;
+  if (is_quant(c) && !tc::mlp_supported(c)) return MOE_ERR_UNSUPPORTED;
   if (c.T == 0) return MOE_OK;
   cudaStream_t s = (cudaStream_t)stream;
   const FwdLayout L = fwd_layout(c);
@@ -330,9 +362,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
   int32_t* row_token = (int32_t*)(base + L.row_token);
   int32_t* tok_row = (int32_t*)(base + L.tok_row);
   void* xd = base + L.xd;
-  float* xd_scale = c.xfer_dtype == MOE_DTYPE_E4M3 ? (float*)(base + L.xd_scale) : nullptr;
+  void* xd_scale = is_quant(c) ? (void*)(base + L.xd_scale) : nullptr;
   void* h = base + L.h;
-  float* h_scale = c.xfer_dtype == MOE_DTYPE_E4M3 ? (float*)(base + L.h_scale) : nullptr;
+  void* h_scale = is_quant(c) ? (void*)(base + L.h_scale) : nullptr;
   void* yd = base + L.yd;
 
   cudaError_t e = router_logits(c, x, w->w_router, w->router_bias, logits, status_of(ws), s);
@@ -340,7 +372,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
   if (e == cudaSuccess)
     e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
                           status_of(ws), s);
-  if (e == cudaSuccess) e = launch_dispatch(c, x, tok_row, xd, xd_scale, s);
+  if (e == cudaSuccess)
+    e = is_mx(c) ? launch_dispatch_mx(c, x, topk_idx, tok_row, offsets, xd, xd_scale, s)
+                 : launch_dispatch(c, x, tok_row, xd, static_cast<float*>(xd_scale), s);
   if (e == cudaSuccess)
     e = grouped_mlp(c, xd, xd_scale, x, offsets, *w, h, h_scale, yd, status_of(ws), s);
   if (e == cudaSuccess) e = launch_combine(c, yd, tok_row, topk_w, y, s);
@@ -361,6 +395,14 @@ moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols,
   if ((br != 1 && br != 128) || (bc != 1 && bc != 128)) return MOE_ERR_UNSUPPORTED;
   if (ceil_div(rows, br) * ceil_div(cols, bc) > (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_quantize_e4m3(src_bf16, rows, cols, br, bc, q, scale, (cudaStream_t)stream));
+}
+
+moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                             moe_stream_t stream) {
+  if (!ptr_ok(src_bf16) || !ptr_ok(q) || !ptr_ok(sf) || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED;
+  if (rows * (cols / 32) / 256 >= (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_quantize_mx(src_bf16, rows, cols, q, sf, (cudaStream_t)stream));
 }
 
 moe_status_t moe_read_status(void* ws, moe_stream_t stream, int32_t* device_status) {

@@ -491,10 +491,10 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.b_group_rows = c.F;
   p.rows_total = rows;
   p.a_scale = xd_scale;
-  p.b0_scale = w.s_gate;
-  p.b1_scale = w.s_up;
-  p.b0x_scale = shared ? w.ss_gate : w.s_gate;
-  p.b1x_scale = shared ? w.ss_up : w.s_up;
+  p.b0_scale = static_cast<const float*>(w.s_gate);
+  p.b1_scale = static_cast<const float*>(w.s_up);
+  p.b0x_scale = static_cast<const float*>(shared ? w.ss_gate : w.s_gate);
+  p.b1x_scale = static_cast<const float*>(shared ? w.ss_up : w.s_up);
   p.nblk_b = c.F / 128;
   p.ldc = c.F;
   p.out = h;
@@ -522,9 +522,9 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.n_tiles = c.H / BN;
   p.b_group_rows = c.H;
   p.a_scale = h_scale;
-  p.b0_scale = w.s_down;
-  p.b1_scale = w.s_down;
-  p.b0x_scale = shared ? w.ss_down : w.s_down;
+  p.b0_scale = static_cast<const float*>(w.s_down);
+  p.b1_scale = p.b0_scale;
+  p.b0x_scale = static_cast<const float*>(shared ? w.ss_down : w.s_down);
   p.b1x_scale = p.b0x_scale;
   p.nblk_b = c.H / 128;
   p.ldc = c.H;

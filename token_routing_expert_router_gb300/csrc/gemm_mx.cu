@@ -1,0 +1,477 @@
+// MXFP8 grouped expert GEMMs on the block-scaled tcgen05 tensor-core MMA.
+//
+// The MXFP8 variant ("Scalable Training of Mixture-of-Experts Models with Megatron Core"
+// summary, reduced precision on Blackwell; the Hybrid-EP article's MXFP8 results) carries
+// one power-of-two UE8M0 scale per 1x32 block of every operand row (OCP MX v1.0). Such
+// scales are applied by the tensor core itself: tcgen05.mma.kind::mxf8f6f4.block_scale
+// multiplies each 32-wide K slice of A and B by their scale factors, which it reads from
+// tensor memory, so the whole K loop accumulates in one TMEM accumulator with no software
+// promotion.
+//
+// Tile 128 x 256, K stages of 128 (four MMAs of K = 32, scale-factor id = the slice).
+// Block: warp 0 TMA producer, warp 1 MMA issuer (TMEM owner), warps 2-9 epilogue (two
+// warps per TMEM lane quarter, each owning half of the tile's columns).
+//   Per stage the producer loads the A and B tiles (TMA, 128-byte swizzle) and the stage's
+//   scale atoms (one 512-byte atom per 128 rows, plain bulk copies); the MMA issuer moves
+//   the atoms into tensor memory with tcgen05.cp 32x128b.warpx4 (the copy and the MMAs
+//   that read it come from one thread, so they execute in order) and issues the MMAs.
+//   TMEM: accumulator in columns [0, 256); stage s's scale factors in [256 + 16s, +12).
+//   The accumulator is single-buffered: the epilogue loads its 128 x 256 values into
+//   registers and hands the accumulator back before it computes and stores, so the next
+//   tile's MMAs wait only for the loads.
+//   GEMM1 (gate/up): columns [0,128) gate and [128,256) up of one 128-wide F block; a
+//     thread owns 64 gate + 64 up columns of one row, computes h = silu(g) * u and
+//     requantises its two 1x32 blocks of h (the scale is thread-local), writing h's codes
+//     and its UE8M0 codes into h's scale atoms.
+//   GEMM2 (down): 256 output columns, bf16.
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
+#include "mx_common.cuh"
+#include "tc_common.cuh"
+
+namespace moe {
+namespace tc {
+
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows, uint64_t cols,
+               uint32_t box_rows, uint32_t box_cols);
+int num_sms();
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;  // BK in elements = bytes (e4m3)
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK;
+constexpr int kBBytes = BN * BK;
+constexpr int kAtomBytes = 512;
+constexpr int kSfBytes = 3 * kAtomBytes;  // A atom, then B atoms for columns [0,128), [128,256)
+constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+constexpr int kMaxGroups = 514;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256, kSfColsPerStage = 16;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t);
+
+enum { MX_SWIGLU_Q8 = 0, MX_STORE_BF16 = 1 };
+
+struct MxParams {
+  const int32_t* offsets;
+  int G, has_extra, T_extra, a2_row_base;  // the extra (shared) group's A rows start at a2_row_base = T*k
+  int64_t out_extra_base;
+  int K;             // multiple of 128
+  int n_tiles;       // N tiles per group (GEMM1: F/128; GEMM2: N/256)
+  int b_group_rows;  // rows of B per routed group (GEMM1: F; GEMM2: N)
+  const uint8_t* a_sf;    // A's scale atoms, grouped rows (K columns)
+  const uint8_t* b0_sf;   // routed weights' atoms: GEMM1 gate [G*F/128][K/128]; GEMM2 down [G*N/128][K/128]
+  const uint8_t* b1_sf;   // GEMM1 up
+  const uint8_t* b0x_sf;  // the shared expert's
+  const uint8_t* b1x_sf;
+  int ldc;                // output row length (elements)
+  void* out;              // GEMM1: h e4m3 [rows, F]; GEMM2: yd bf16 [rows, N]
+  uint8_t* out_sf;        // GEMM1: h's scale atoms (F columns)
+  DeviceStatus* status;
+  uint64_t timeout_ns;
+};
+
+struct TileCoord {
+  int g, mb, nb, rows;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
+                                                 const int32_t* seg_rows) {
+  int lo = 0, hi = ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileCoord c;
+  c.g = lo;
+  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
+  const int local = tile - n_tiles * mt_prefix[lo];
+  c.nb = local / mt;
+  c.mb = local - c.nb * mt;
+  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  return c;
+}
+
+// Non-tensor bulk copy global -> shared completing `bytes` on the mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Shared-memory descriptor of a scale atom for tcgen05.cp: no swizzle, 8-row core matrices
+// of 16-byte rows stored contiguously (stride 128 bytes between 8-row groups).
+__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(512u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// 32 lanes x 128 bits of shared memory to TMEM, repeated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4: e4m3 x e4m3, fp32 accumulate, K-major A and B,
+// UE8M0 scales (bit 23), B scale-factor id at bits 4-5, A scale-factor id at bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0x,
+                      const __grid_constant__ CUtensorMap tmB1x, const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint8_t* sSF = sB + kStages * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* mt_prefix = reinterpret_cast<int32_t*>(bars + 32);
+  int32_t* seg_rows = mt_prefix + kMaxGroups;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = p.G + p.has_extra;
+  const int kblocks = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);  // one arrival per epilogue warp
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 2) {
+    int carry = 0;
+    for (int g0 = 0; g0 < ngroups; g0 += 32) {
+      const int g = g0 + lane;
+      int rows = 0;
+      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
+      else if (g < ngroups) rows = p.T_extra;
+      const int mt = (rows + BM - 1) / BM;
+      int inc = mt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      if (g < ngroups) {
+        seg_rows[g] = rows;
+        mt_prefix[g] = carry + inc - mt;
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) mt_prefix[ngroups] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = p.n_tiles * mt_prefix[ngroups];
+
+  if (warp == 0) {
+    // ======================= TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+        const bool extra = c.g >= p.G;
+        const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
+        const int a_row = (int)gofs + c.mb * BM;
+        const int64_t a_atom = mx_group_atom_base(gofs, c.g) + c.mb;
+        const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
+        const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
+        const uint8_t* sf0 = extra ? p.b0x_sf : p.b0_sf;
+        const uint8_t* sf1 = extra ? p.b1x_sf : p.b1_sf;
+        const int b_tile_rows = EPI == MX_SWIGLU_Q8 ? BN / 2 : BN;
+        const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
+        const int64_t b_atom = b_row / 128;  // b_row is a multiple of 128
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          uint8_t* sf_dst = sSF + stage * kSfBytes;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row);
+          bulk_load(sf_dst, p.a_sf + ((a_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
+          if (EPI == MX_SWIGLU_Q8) {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
+            bulk_load(sf_dst + kAtomBytes, sf0 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
+            bulk_load(sf_dst + 2 * kAtomBytes, sf1 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
+          } else {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            bulk_load(sf_dst + kAtomBytes, sf0 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
+            bulk_load(sf_dst + 2 * kAtomBytes, sf0 + (((b_atom + 1) * kblocks + kb) << 9), kAtomBytes,
+                      &full[stage]);
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      // wind down: every issued load has landed and been consumed before the block exits
+      const int used = issued < kStages ? (int)issued : kStages;
+      for (int i = 0; i < used; ++i) {
+        const int s = (stage - 1 - i + 2 * kStages) % kStages;
+        const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
+        if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
+        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        // the epilogue has taken the previous tile's accumulator out of TMEM
+        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
+        acc_phase ^= 1;
+        tc_fence_after();
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_addr(sA + stage * kABytes);
+          const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
+          const uint32_t sf_addr = smem_addr(sSF + stage * kSfBytes);
+          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + 4;
+          tmem_cp_atom(sfa_t, desc_atom(sf_addr));
+          tmem_cp_atom(sfb_t, desc_atom(sf_addr + kAtomBytes));
+          tmem_cp_atom(sfb_t + 4, desc_atom(sf_addr + 2 * kAtomBytes));
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction: +32 bytes, scale id k
+            mma_mx(tmem_base, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32),
+                   idesc_mx(BM, BN, (uint32_t)k), sfa_t, sfb_t, (kb | k) != 0);
+          mma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit(acc_full);
+      }
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    }
+  } else {
+    // ======================= epilogue: warps 2..9
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;  // which 128 of the tile's 256 columns this warp owns
+    const int r = quarter * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+      const bool extra = c.g >= p.G;
+      ok = mbar_wait(acc_full, acc_phase, abort, p.timeout_ns, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      acc_phase ^= 1;
+      tc_fence_after();
+      const uint32_t t = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      uint32_t v[128];
+      if (EPI == MX_SWIGLU_Q8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tmem_ld16(t + half * 64 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * q]));
+          tmem_ld16(t + 128 + half * 64 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&v[64 + 16 * q]));
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tmem_ld16(t + half * 128 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * q]));
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();  // every lane's loads are complete: one arrival per warp
+      if (lane == 0) mbar_arrive(acc_empty);
+
+      const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
+      const int64_t out_row = (extra ? p.out_extra_base : gofs) + c.mb * BM + r;
+      if (r < c.rows) {
+        if (EPI == MX_SWIGLU_Q8) {
+          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + out_row * p.ldc + c.nb * 128 + half * 64;
+          uint32_t codes = 0;
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            float h[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(v[32 * blk + i]);
+              h[i] = g / (1.0f + __expf(-g)) * __uint_as_float(v[64 + 32 * blk + i]);
+              amax = fmaxf(amax, fabsf(h[i]));
+            }
+            const int s = mx_scale_exp(amax);
+            const float inv = mx_inv_scale(s);
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w[i] = e4m3x4(__fmul_rn(h[4 * i], inv), __fmul_rn(h[4 * i + 1], inv), __fmul_rn(h[4 * i + 2], inv),
+                            __fmul_rn(h[4 * i + 3], inv));
+            reinterpret_cast<uint4*>(out + 32 * blk)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(out + 32 * blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            codes |= (uint32_t)(s + 127) << (8 * blk);
+          }
+          // blocks 2*half and 2*half + 1 of the h stage nb, in the tile's atom row
+          const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb;
+          *reinterpret_cast<uint16_t*>(p.out_sf + mx_atom_byte(atom, c.nb, p.ldc / 128, r) + 2 * half) =
+              (uint16_t)codes;
+        } else {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * BN + half * 128;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 b2 =
+                  __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * j]), __uint_as_float(v[8 * q + 2 * j + 1]));
+              w4[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            reinterpret_cast<uint4*>(out)[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+bool make_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, box_rows, BK);
+}
+
+template <int EPI>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0x,
+                   const CUtensorMap& b1x, const MxParams& p, int64_t max_tiles, cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  auto kern = tc_gemm_mx_kernel<EPI>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, b0x, b1x, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mx_supported(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && c.xfer_dtype == MOE_DTYPE_MXE4M3 && c.H % 256 == 0 && c.F % 128 == 0 &&
+         c.E + 1 <= kMaxGroups;
+}
+
+cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const void* xd_sf, const int32_t* offsets,
+                                  const moe_weights_t& w, void* h, void* h_sf, void* yd, DeviceStatus* st,
+                                  cudaStream_t s) {
+  const int64_t R = routed_rows(c), rows = total_rows(c);
+  const bool shared = c.n_shared != 0;
+  // ---- GEMM1: h = mx(silu(A Wg^T) * (A Wu^T)); the shared expert's A = dispatched rows R..
+  CUtensorMap a1, bg, bu, bgx, bux;
+  bool ok = make_u8(&a1, xd, rows, c.H, BM) && make_u8(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
+            make_u8(&bu, w.w_up, (uint64_t)c.E * c.F, c.H, 128);
+  if (shared) ok = ok && make_u8(&bgx, w.ws_gate, c.F, c.H, 128) && make_u8(&bux, w.ws_up, c.F, c.H, 128);
+  else { bgx = bg; bux = bu; }
+  if (!ok) return cudaErrorInvalidValue;
+  MxParams p{};
+  p.offsets = offsets;
+  p.G = c.E;
+  p.has_extra = shared ? 1 : 0;
+  p.T_extra = c.T;
+  p.a2_row_base = (int)R;
+  p.out_extra_base = R;
+  p.K = c.H;
+  p.n_tiles = c.F / 128;
+  p.b_group_rows = c.F;
+  p.a_sf = static_cast<const uint8_t*>(xd_sf);
+  p.b0_sf = static_cast<const uint8_t*>(w.s_gate);
+  p.b1_sf = static_cast<const uint8_t*>(w.s_up);
+  p.b0x_sf = static_cast<const uint8_t*>(shared ? w.ss_gate : w.s_gate);
+  p.b1x_sf = static_cast<const uint8_t*>(shared ? w.ss_up : w.s_up);
+  p.ldc = c.F;
+  p.out = h;
+  p.out_sf = static_cast<uint8_t*>(h_sf);
+  p.status = st;
+  p.timeout_ns = kTimeoutNs;
+  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  cudaError_t e = launch<MX_SWIGLU_Q8>(a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  if (e != cudaSuccess) return e;
+  // ---- GEMM2: yd = h Wd^T with both operands' MX scales, bf16 out
+  CUtensorMap a2, bd, bdx;
+  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, BN);
+  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, BN);
+  else bdx = bd;
+  if (!ok) return cudaErrorInvalidValue;
+  p.K = c.F;
+  p.n_tiles = c.H / BN;
+  p.b_group_rows = c.H;
+  p.a_sf = static_cast<const uint8_t*>(h_sf);
+  p.b0_sf = static_cast<const uint8_t*>(w.s_down);
+  p.b1_sf = p.b0_sf;
+  p.b0x_sf = static_cast<const uint8_t*>(shared ? w.ss_down : w.s_down);
+  p.b1x_sf = p.b0x_sf;
+  p.ldc = c.H;
+  p.out = yd;
+  p.out_sf = nullptr;
+  return launch<MX_STORE_BF16>(a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+}
+
+}  // namespace tc
+}  // namespace moe

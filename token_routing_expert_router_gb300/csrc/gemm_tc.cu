@@ -499,6 +499,7 @@ bool router_supported(const moe_config_t& c) {
 bool mlp_supported(const moe_config_t& c) {
   if (encode_fn() == nullptr) return false;
   if (c.xfer_dtype == MOE_DTYPE_E4M3) return fp8_supported(c);
+  if (c.xfer_dtype == MOE_DTYPE_MXE4M3) return mx_supported(c);
   if (c.act_dtype != MOE_DTYPE_BF16 || c.xfer_dtype != MOE_DTYPE_BF16) return false;
   return c.H % 128 == 0 && c.F % 128 == 0;
 }

@@ -6,7 +6,7 @@
 namespace moe {
 namespace tc {
 
-// Shapes the tcgen05 kernels take (bf16 activations; E4M3 transfer when configured).
+// Shapes the tcgen05 kernels take (bf16 activations; E4M3 / MXE4M3 transfer when configured).
 bool router_supported(const moe_config_t& c);
 bool mlp_supported(const moe_config_t& c);
 
@@ -19,6 +19,12 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                const void* x, const int32_t* offsets, const moe_weights_t& w,
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
                                cudaStream_t s, const int32_t* row_token = nullptr);
+
+// MXFP8 (e4m3, UE8M0 scale atoms) variant on the block-scaled MMA.
+bool mx_supported(const moe_config_t& c);
+cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const void* xd_sf,
+                                  const int32_t* offsets, const moe_weights_t& w, void* h, void* h_sf,
+                                  void* yd, DeviceStatus* st, cudaStream_t s);
 
 // FP8 (e4m3, fp32 block scales) variant of the grouped MLP.
 bool fp8_supported(const moe_config_t& c);

@@ -52,6 +52,12 @@ cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t*
                            const float* topk_w, void* y, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* src, int64_t rows, int64_t cols, int br, int bc,
                                  uint8_t* q, float* scale, cudaStream_t s);
+// MXFP8 variant (scale atoms as described in mx_common.cuh).
+cudaError_t launch_dispatch_mx(const moe_config_t& c, const void* x, const int32_t* topk_idx,
+                               const int32_t* tok_row, const int32_t* offsets, void* xd, void* xd_sf,
+                               cudaStream_t s);
+cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                               cudaStream_t s);
 
 // SIMT grouped GEMM (fp32 FFMA): C = A . B^T per group, with optional SwiGLU pair.
 // Groups: routed experts g < E over rows [offsets[g], offsets[g+1]) of A, plus an optional

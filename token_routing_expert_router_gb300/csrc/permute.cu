@@ -2,8 +2,9 @@
 // (Hybrid-EP article: dispatch sends each token only where the routing map says; combine
 // brings the expert outputs back with high-precision accumulation). Both walk tokens, so
 // x is read once on the way out and y written once on the way back; rows move as 16-byte
-// vectors. Also the block quantiser of the FP8-dispatch variant.
+// vectors. Also the block quantisers of the FP8 and MXFP8 dispatch variants.
 #include "moe_internal.cuh"
+#include "mx_common.cuh"
 
 namespace moe {
 namespace {
@@ -81,6 +82,112 @@ __global__ void __launch_bounds__(256) dispatch_e4m3_kernel(
       if (lane == 0) xd_scale[(int64_t)b * rows_total + r] = scale;
     }
   }
+}
+
+// 32 bf16 values from 64 bytes (four 16-byte vectors).
+__device__ __forceinline__ void load_bf16x32(const uint4* __restrict__ p, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = __ldg(p + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = bf16_lo(w[j]);
+      v[8 * i + 2 * j + 1] = bf16_hi(w[j]);
+    }
+  }
+}
+
+// One 1x32 MX block: returns the UE8M0 code and writes the 32 e4m3 codes to q (two 16-byte
+// vectors).
+__device__ __forceinline__ uint32_t mx_quant_block(const float (&v)[32], uint4 (&q)[2]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_scale_exp(amax);
+  const float inv = mx_inv_scale(s);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = e4m3x4(__fmul_rn(v[4 * i], inv), __fmul_rn(v[4 * i + 1], inv), __fmul_rn(v[4 * i + 2], inv),
+                  __fmul_rn(v[4 * i + 3], inv));
+  q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return (uint32_t)(s + 127);
+}
+
+// MXFP8 dispatch: each token quantised once in 1x32 blocks (one block per thread), the
+// codes written to its k rows and, with a shared expert, to row R + t; the UE8M0 codes go
+// to each row's place in the scale atoms (one 32-bit word per row and 128-column stage).
+// A routed row whose expert id is out of range gets its payload but no scales.
+__global__ void __launch_bounds__(256) dispatch_mx_kernel(
+    const uint4* __restrict__ x, int H, int k, int E, int64_t R, int shared, const int32_t* __restrict__ topk_idx,
+    const int32_t* __restrict__ tok_row, const int32_t* __restrict__ offsets, uint8_t* __restrict__ xd,
+    uint8_t* __restrict__ xd_sf) {
+  extern __shared__ uint32_t codes[];  // [H / 128] words: the token's H / 32 UE8M0 codes
+  __shared__ int64_t rows[33];
+  __shared__ int64_t atom_row[33];
+  __shared__ int32_t atom_i[33];
+  const int t = blockIdx.x;
+  const int nrows = k + shared;
+  if (threadIdx.x < nrows) {
+    const int j = threadIdx.x;
+    int64_t r, gofs;
+    int g;
+    if (j < k) {
+      r = tok_row[(int64_t)t * k + j];
+      g = topk_idx[(int64_t)t * k + j];
+      gofs = (g >= 0 && g < E) ? offsets[g] : -1;
+    } else {
+      r = R + t;
+      g = E;
+      gofs = R;
+    }
+    rows[j] = r;
+    atom_row[j] = gofs < 0 ? -1 : mx_group_atom_base(gofs, g) + (r - gofs) / 128;
+    atom_i[j] = gofs < 0 ? 0 : (int)((r - gofs) % 128);
+  }
+  __syncthreads();
+  const int nb = H / 32;
+  uint8_t* code_bytes = reinterpret_cast<uint8_t*>(codes);
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    float v[32];
+    load_bf16x32(x + ((int64_t)t * H + b * 32) / 8, v);
+    uint4 q[2];
+    code_bytes[b] = (uint8_t)mx_quant_block(v, q);
+    for (int j = 0; j < nrows; ++j) {
+      uint4* dst = reinterpret_cast<uint4*>(xd + rows[j] * H + b * 32);
+      dst[0] = q[0];
+      dst[1] = q[1];
+    }
+  }
+  __syncthreads();
+  const int ks_total = H / 128;
+  for (int i = threadIdx.x; i < nrows * ks_total; i += blockDim.x) {
+    const int j = i / ks_total, ks = i - j * ks_total;
+    if (atom_row[j] >= 0)
+      *reinterpret_cast<uint32_t*>(xd_sf + mx_atom_byte(atom_row[j], ks, ks_total, atom_i[j])) = codes[ks];
+  }
+}
+
+// MX quantisation of a bf16 [rows, cols] matrix along its rows (offline weight preparation):
+// one 1x32 block per thread; rows and cols are multiples of 128; codes to q, UE8M0 scales
+// to atoms of 128 rows (tile a = rows [128a, 128a + 128)).
+__global__ void __launch_bounds__(256) quantize_mx_kernel(const uint4* __restrict__ src, int64_t rows,
+                                                          int64_t cols, uint8_t* __restrict__ q,
+                                                          uint8_t* __restrict__ sf) {
+  const int64_t nb = cols / 32;
+  const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= rows * nb) return;
+  const int64_t r = blk / nb, b = blk - r * nb;
+  float v[32];
+  load_bf16x32(src + (r * cols + b * 32) / 8, v);
+  uint4 qq[2];
+  const uint32_t code = mx_quant_block(v, qq);
+  uint4* dst = reinterpret_cast<uint4*>(q + r * cols + b * 32);
+  dst[0] = qq[0];
+  dst[1] = qq[1];
+  sf[mx_atom_byte(r / 128, (int)(b / 4), (int)(cols / 128), (int)(r % 128)) + (b & 3)] = (uint8_t)code;
 }
 
 // y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ yd[R+t]), fp32 in fixed j order, one rounding
@@ -303,6 +410,26 @@ cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t*
     combine_kernel<true><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, shared, routed_rows(c), y);
   else
     combine_kernel<false><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, topk_w, shared, routed_rows(c), y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_mx(const moe_config_t& c, const void* x, const int32_t* topk_idx,
+                               const int32_t* tok_row, const int32_t* offsets, void* xd, void* xd_sf,
+                               cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const size_t smem = align_up((size_t)c.H / 32, 16);
+  dispatch_mx_kernel<<<c.T, 256, smem, s>>>(reinterpret_cast<const uint4*>(x), c.H, c.k, c.E, routed_rows(c),
+                                            c.n_shared ? 1 : 0, topk_idx, tok_row, offsets,
+                                            reinterpret_cast<uint8_t*>(xd), reinterpret_cast<uint8_t*>(xd_sf));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                               cudaStream_t s) {
+  const int64_t nblk = rows * (cols / 32);
+  if (nblk == 0) return cudaSuccess;
+  quantize_mx_kernel<<<(unsigned)ceil_div(nblk, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), rows, cols,
+                                                                    q, sf);
   return cudaGetLastError();
 }
 
