@@ -23,7 +23,9 @@
 //     thread owns 64 gate + 64 up columns of one row, computes h = silu(g) * u and
 //     requantises its two 1x32 blocks of h (the scale is thread-local), writing h's codes
 //     and its UE8M0 codes into h's scale atoms.
-//   GEMM2 (down): 256 output columns, bf16.
+//   GEMM2 (down): 256 output columns, bf16, stored through a per-warp shared-memory
+//     staging buffer (the row-per-thread TMEM layout would otherwise make every store
+//     instruction touch 32 rows).
 #include <cudaTypedefs.h>
 
 #include "gemm_tc.cuh"
@@ -52,7 +54,9 @@ constexpr int kMaxGroups = 514;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256, kSfColsPerStage = 16;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t);
+constexpr int kEpiStageBytes = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (GEMM2 stores)
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) +
+                              kEpiWarps * kEpiStageBytes;
 
 enum { MX_SWIGLU_Q8 = 0, MX_STORE_BF16 = 1 };
 
@@ -144,6 +148,28 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// A warp's 32 rows x 64 bytes, staged in shared memory so that the global stores are
+// coalesced: each thread puts its own row's four 16-byte pieces in (stage_piece), then
+// each store instruction of flush_rows_64B writes 8 rows x 64 contiguous bytes. Piece c of row r sits at r * 64 +
+// 16 * (c ^ ((r >> 1) & 3)), which keeps both the row-wise writes and the column-wise
+// reads free of bank conflicts. Row r goes to base + r * stride; rows r >= live (past the
+// end of an expert's segment) are skipped.
+__device__ __forceinline__ void stage_piece(uint8_t* stage, int lane, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(stage + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) = v;
+}
+
+__device__ __forceinline__ void flush_rows_64B(uint8_t* stage, int lane, uint8_t* base, int64_t stride, int live) {
+  __syncwarp();
+  const int c = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = 8 * j + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + row * 64 + 16 * (c ^ ((row >> 1) & 3)));
+    if (row < live) *reinterpret_cast<uint4*>(base + row * stride + 16 * c) = v;
+  }
+  __syncwarp();
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -164,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* mt_prefix = reinterpret_cast<int32_t*>(bars + 32);
   int32_t* seg_rows = mt_prefix + kMaxGroups;
+  uint8_t* sEpi = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups);  // [kEpiWarps][32 rows][64 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
@@ -306,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = ew >> 2;  // which 128 of the tile's 256 columns this warp owns
     const int r = quarter * 32 + lane;
+    uint8_t* stage = sEpi + ew * kEpiStageBytes;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
@@ -334,10 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(acc_empty);
 
       const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
-      const int64_t out_row = (extra ? p.out_extra_base : gofs) + c.mb * BM + r;
-      if (r < c.rows) {
-        if (EPI == MX_SWIGLU_Q8) {
-          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + out_row * p.ldc + c.nb * 128 + half * 64;
+      const int64_t row0 = (extra ? p.out_extra_base : gofs) + c.mb * BM + quarter * 32;  // the warp's first row
+      const int live_rows = c.rows - quarter * 32;  // rows of this warp inside the segment
+      if (EPI == MX_SWIGLU_Q8) {
+        // 64 bytes of h codes per thread per tile: direct 16-byte stores
+        if (r < c.rows) {
+          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (row0 + lane) * p.ldc + c.nb * 128 + half * 64;
           uint32_t codes = 0;
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
@@ -364,19 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb;
           *reinterpret_cast<uint16_t*>(p.out_sf + mx_atom_byte(atom, c.nb, p.ldc / 128, r) + 2 * half) =
               (uint16_t)codes;
-        } else {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * BN + half * 128;
+        }
+      } else {
+        // 256 bytes of bf16 per thread per tile: staged through shared memory, 32 columns
+        // at a time, so that the stores are coalesced
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (row0 * p.ldc + c.nb * BN + half * 128) * 2;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 4; ++q) {  // 32 columns (64 bytes of bf16) per pass
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t w4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * j]), __uint_as_float(v[8 * q + 2 * j + 1]));
+              const int i = 32 * q + 8 * c4 + 2 * j;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
               w4[j] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            reinterpret_cast<uint4*>(out)[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            stage_piece(stage, lane, c4, make_uint4(w4[0], w4[1], w4[2], w4[3]));
           }
+          flush_rows_64B(stage, lane, out + 64 * q, (int64_t)p.ldc * 2, live_rows);
         }
       }
     }
