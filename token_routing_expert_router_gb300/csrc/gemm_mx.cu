@@ -148,28 +148,6 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// A warp's 32 rows x 64 bytes, staged in shared memory so that the global stores are
-// coalesced: each thread puts its own row's four 16-byte pieces in (stage_piece), then
-// each store instruction of flush_rows_64B writes 8 rows x 64 contiguous bytes. Piece c of row r sits at r * 64 +
-// 16 * (c ^ ((r >> 1) & 3)), which keeps both the row-wise writes and the column-wise
-// reads free of bank conflicts. Row r goes to base + r * stride; rows r >= live (past the
-// end of an expert's segment) are skipped.
-__device__ __forceinline__ void stage_piece(uint8_t* stage, int lane, int c, uint4 v) {
-  *reinterpret_cast<uint4*>(stage + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) = v;
-}
-
-__device__ __forceinline__ void flush_rows_64B(uint8_t* stage, int lane, uint8_t* base, int64_t stride, int live) {
-  __syncwarp();
-  const int c = lane & 3;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int row = 8 * j + (lane >> 2);
-    const uint4 v = *reinterpret_cast<const uint4*>(stage + row * 64 + 16 * (c ^ ((row >> 1) & 3)));
-    if (row < live) *reinterpret_cast<uint4*>(base + row * stride + 16 * c) = v;
-  }
-  __syncwarp();
-}
-
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,

@@ -59,7 +59,7 @@ struct Smem {
   static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;                   // two accumulators
   static constexpr size_t kBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + 256 /*barriers*/ +
-                                   2 * kMaxGroups * sizeof(int32_t);
+                                   2 * kMaxGroups * sizeof(int32_t) + 4 * 2048 /*epilogue store staging*/;
 };
 
 // Tile -> (group, m tile, n tile) from the block's copy of the m-tile prefix; tm = rows of
@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
     const int quarter = warp & 3;
+    // 32 rows x 64 bytes per warp: bf16 rows leave through shared memory, coalesced
+    uint8_t* stage = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups) + (warp - 2) * 2048;
     const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_addr(&tempty[0]), 0) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -311,10 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_in_tile = m64 ? quarter * 16 + lane : (int)rank * BM + quarter * 32 + lane;
       const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
       const bool live = (!m64 || lane < 16) && row_in_tile < c.rows;
+      // rows of this warp inside the segment (lane l holds warp row l; an M = 64 tile
+      // gives a warp 16 rows)
+      const int warp_live = min(c.rows - (row_in_tile - lane), m64 ? 16 : 32);
+      const int64_t warp_row0 = out_row - lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (EPI == EPI_SWIGLU_BF16) {
         // cols [0, BN/2) gate, [BN/2, BN) up -> BN/2 columns of h
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * (BN / 2);
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * (BN / 2)) * 2;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN / 2; c0 += 32) {
           uint32_t g[32], u[32];
@@ -330,15 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
             packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            stage_piece(stage, lane, v, make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+          flush_rows_64B(stage, lane, out + 2 * c0, (int64_t)p.ldc * 2, warp_live);
         }
       } else if (EPI == EPI_STORE_BF16) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * BN;
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
@@ -350,12 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-          }
+          for (int q = 0; q < 4; ++q)
+            stage_piece(stage, lane, q, make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]));
+          flush_rows_64B(stage, lane, out + 2 * c0, (int64_t)p.ldc * 2, warp_live);
         }
       } else {
         float* out = reinterpret_cast<float*>(p.out) + out_row * p.ldc + c.nb * BN;
