@@ -45,7 +45,7 @@ struct F8Smem {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
   static constexpr size_t kBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * BM * sizeof(float) +
-                                   2 * kMaxGroups * sizeof(int32_t);
+                                   2 * kMaxGroups * sizeof(int32_t) + (kEpiThreads / 32) * 2048 /*store staging*/;
 };
 
 enum { FP8_SWIGLU_Q8 = 0, FP8_STORE_BF16 = 1 };
@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* amax_buf = reinterpret_cast<float*>(bars + 32);  // [2][BM]
   int32_t* mt_prefix = reinterpret_cast<int32_t*>(amax_buf + 2 * BM);
   int32_t* seg_rows = mt_prefix + kMaxGroups;
+  uint8_t* sEpi = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups);  // [8 warps][32 rows][64 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
@@ -387,18 +388,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (half == 0) p.out_scale[(int64_t)c.nb * p.rows_total + out_row] = scale;
         }
       } else {
-        if (live) {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + out_row * p.ldc + c.nb * BN + half * 128;
+        // bf16 rows leave through a per-warp shared-memory staging buffer, 32 columns at a
+        // time, so that each store instruction writes 8 rows x 64 contiguous bytes
+        uint8_t* stage = sEpi + ew * 2048;
+        const int warp_live = ok ? c.rows - (row_in_tile - lane) : 0;
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + ((out_row - lane) * p.ldc + c.nb * BN + half * 128) * 2;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t w4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * q + 2 * j], acc[8 * q + 2 * j + 1]);
+              const int i = 32 * q + 8 * c4 + 2 * j;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i], acc[i + 1]);
               w4[j] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            reinterpret_cast<uint4*>(out)[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            stage_piece(stage, lane, c4, make_uint4(w4[0], w4[1], w4[2], w4[3]));
           }
+          flush_rows_64B(stage, lane, out + 64 * q, (int64_t)p.ldc * 2, warp_live);
         }
       }
     }
