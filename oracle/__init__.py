@@ -75,6 +75,9 @@ def _L():
             "oc_expert_mlp": (None, [P, i64, i32, i32, P, P, P, i32, P]),
             "oc_combine": (None, [P, P, P, P, i32, i32, i32, P]),
             "oc_aux_loss": (f64, [P, P, i32, i32, i32, i32, f64, P]),
+            "oc_combine_backward": (None, [P, P, P, P, i32, i32, i32, i32, P, P]),
+            "oc_expert_mlp_backward": (None, [P, i64, i32, i32, P, P, P, P, P, P, P, P]),
+            "oc_dispatch_backward": (None, [P, P, i32, i32, i32, i32, P]),
             "oc_dense_forward": (i32, [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f64, P, P, P, i32, P, P, P, P]),
         }
@@ -140,6 +143,9 @@ def route(logits, cfg: dict):
     l = _c(logits, np.float32)
     T, E = l.shape
     k = cfg["k"]
+    G, g = cfg["n_groups"], cfg["topk_groups"]
+    if k > E or E % G or not 1 <= g <= G or (G > 1 and g < G and g * (E // G) < k):
+        raise ValueError("oracle route: k larger than the experts the groups allow")
     idx = np.empty((T, k), dtype=np.int32)
     w = np.empty((T, k), dtype=np.float64)
     rc = _L().oc_route(_p(l), T, E, k, cfg["score_fn"], cfg["renorm"], cfg["n_groups"],
@@ -337,6 +343,81 @@ def dense_forward(cfg: dict, inp: dict, logits=None) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle dense loop: non-finite logit")
     return y
+
+
+# ---------------------------------------------------------------- backward (training step)
+def combine_backward(dy, yd, tok_row, topk_w, shared: bool):
+    """(dyd [R(+T), H], dtopk_w [T, k]) from dy [T, H] and the forward's yd (fp64)."""
+    dy = _c(dy, np.float64)
+    yd = _c(yd, np.float64)
+    tr = _c(tok_row, np.int32)
+    w = _c(topk_w, np.float64)
+    T, k = tr.shape
+    H = dy.shape[1]
+    dyd = np.zeros((T * k + (T if shared else 0), H), dtype=np.float64)
+    dw = np.empty((T, k), dtype=np.float64)
+    _L().oc_combine_backward(_p(dy), _p(yd), _p(tr), _p(w), T, k, H, int(shared), _p(dyd), _p(dw))
+    return dyd, dw
+
+
+def expert_mlp_backward(a, wg, wu, wd, dyd):
+    """(dxd [n,H], dWg [F,H], dWu [F,H], dWd [H,F]) of one expert's SwiGLU MLP (fp64,
+    activations recomputed from a)."""
+    a = _c(a, np.float64)
+    wg, wu, wd = _c(wg, np.float64), _c(wu, np.float64), _c(wd, np.float64)
+    dyd = _c(dyd, np.float64)
+    n, H = a.shape
+    F = wg.shape[0]
+    dxd = np.zeros((n, H), dtype=np.float64)
+    dwg = np.zeros((F, H), dtype=np.float64)
+    dwu = np.zeros((F, H), dtype=np.float64)
+    dwd = np.zeros((H, F), dtype=np.float64)
+    if n:
+        _L().oc_expert_mlp_backward(_p(a), n, H, F, _p(wg), _p(wu), _p(wd), _p(dyd), _p(dxd), _p(dwg), _p(dwu),
+                                    _p(dwd))
+    return dxd, dwg, dwu, dwd
+
+
+def dispatch_backward(dxd, tok_row, shared: bool) -> np.ndarray:
+    dxd = _c(dxd, np.float64)
+    tr = _c(tok_row, np.int32)
+    T, k = tr.shape
+    H = dxd.shape[1]
+    dx = np.empty((T, H), dtype=np.float64)
+    _L().oc_dispatch_backward(_p(dxd), _p(tr), T, k, H, int(shared), _p(dx))
+    return dx
+
+
+def backward(cfg: dict, inp: dict, fwd: dict, dy) -> dict:
+    """The layer's backward with the routing of ``fwd`` (an oracle.forward result) held fixed:
+    combine backward -> each expert's MLP backward -> dispatch backward. Unquantised layers.
+    Returns dyd, dtopk_w, dxd, dx (the gradient reaching x through the experts), the
+    expert weight gradients dw_gate/dw_up [E,F,H], dw_down [E,H,F] and, with a shared
+    expert, dws_gate/dws_up [F,H], dws_down [H,F]."""
+    if cfg["xfer_dtype"] in (E4M3, MXE4M3):
+        raise NotImplementedError("the backward covers the unquantised layers")
+    T, H, E, k, F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
+    shared = bool(cfg["n_shared"])
+    R = T * k
+    yd = fwd["yd"] if not shared else np.concatenate([fwd["yd"], fwd["ys"]])
+    dyd, dw = combine_backward(dy, yd, fwd["tok_row"], fwd["topk_w"], shared)
+    x = inp["x"].astype(np.float64)
+    xd = x[fwd["row_token"]]
+    offsets = fwd["offsets"]
+    dxd = np.zeros((R + (T if shared else 0), H))
+    out = {"dyd": dyd, "dtopk_w": dw,
+           "dw_gate": np.zeros((E, F, H)), "dw_up": np.zeros((E, F, H)), "dw_down": np.zeros((E, H, F))}
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            dxd[r0:r1], out["dw_gate"][e], out["dw_up"][e], out["dw_down"][e] = expert_mlp_backward(
+                xd[r0:r1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], dyd[r0:r1])
+    if shared:
+        dxd[R:], out["dws_gate"], out["dws_up"], out["dws_down"] = expert_mlp_backward(
+            x, inp["ws_gate"], inp["ws_up"], inp["ws_down"], dyd[R:])
+    out["dxd"] = dxd
+    out["dx"] = dispatch_backward(dxd, fwd["tok_row"], shared)
+    return out
 
 
 def rel_l2(a, b) -> float:

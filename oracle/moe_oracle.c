@@ -439,6 +439,111 @@ void oc_combine(const double* yd, const int32_t* tok_row, const double* w, const
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Backward of the layer for a training step (the pages' grouped GEMM and permutation    */
+/* serve the backward as well as the forward: Megatron-Core summary, section 2.4 grouped  */
+/* GEMM and the memory-efficient permutation; section 2.2 recomputation of activations).  */
+/* With the routing fixed (its map and weights are inputs here), y depends on x through   */
+/* dispatch, the experts and combine; the functions below are the chain rule of those     */
+/* steps, in fp64, in the reverse order.                                                 */
+/* ------------------------------------------------------------------------------------ */
+
+/* Combine backward. From y[t] = sum_j w[t,j] * yd[r_tj] (+ yd[R+t]):                    */
+/*   dyd[r_tj] = w[t,j] * dy[t],  dyd[R+t] = dy[t]  (shared),                            */
+/*   dw[t,j]  = sum_o dy[t,o] * yd[r_tj, o].                                              */
+void oc_combine_backward(const double* dy, const double* yd, const int32_t* tok_row, const double* w,
+                         int T, int k, int H, int shared, double* dyd, double* dw) {
+  const int64_t R = (int64_t)T * k;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double* g = dy + (int64_t)t * H;
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = tok_row[(int64_t)t * k + j];
+      const double wj = w[(int64_t)t * k + j];
+      double s = 0.0;
+      for (int o = 0; o < H; ++o) {
+        dyd[r * H + o] = wj * g[o];
+        s += g[o] * yd[r * H + o];
+      }
+      dw[(int64_t)t * k + j] = s;
+    }
+    if (shared)
+      for (int o = 0; o < H; ++o) dyd[(R + t) * H + o] = g[o];
+  }
+}
+
+/* One expert's SwiGLU MLP backward on rows a [n,H] with output gradient dyd [n,H]. The  */
+/* activations are recomputed from a (g = a Wg^T, u = a Wu^T, s = 1/(1+e^-g),            */
+/* h = g s u), not stored:                                                              */
+/*   dh  = dyd . Wd                 (dgrad of the down projection)                       */
+/*   dg  = dh * u * s * (1 + g (1 - s)),  du = dh * g * s   (SwiGLU backward)            */
+/*   dxd = dg . Wg + du . Wu        (dgrad of gate/up)                                   */
+/*   dWd = dyd^T . h,  dWg = dg^T . a,  dWu = du^T . a   (wgrad, summed over the rows)   */
+/* Outputs: dxd [n,H], dwg/dwu [F,H], dwd [H,F].                                         */
+void oc_expert_mlp_backward(const double* a, int64_t n, int H, int F, const double* wg, const double* wu,
+                            const double* wd, const double* dyd, double* dxd, double* dwg, double* dwu,
+                            double* dwd) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)(n * F > 0 ? n * F : 1));
+  double* dg = (double*)malloc(sizeof(double) * (size_t)(n * F > 0 ? n * F : 1));
+  double* du = (double*)malloc(sizeof(double) * (size_t)(n * F > 0 ? n * F : 1));
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const double* ar = a + r * H;
+    const double* gy = dyd + r * H;
+    for (int f = 0; f < F; ++f) {
+      double g = 0.0, u = 0.0, dh = 0.0;
+      for (int i = 0; i < H; ++i) {
+        g += ar[i] * wg[(int64_t)f * H + i];
+        u += ar[i] * wu[(int64_t)f * H + i];
+      }
+      for (int o = 0; o < H; ++o) dh += gy[o] * wd[(int64_t)o * F + f];
+      const double s = 1.0 / (1.0 + exp(-g));
+      h[r * F + f] = g * s * u;
+      dg[r * F + f] = dh * u * s * (1.0 + g * (1.0 - s));
+      du[r * F + f] = dh * g * s;
+    }
+    for (int i = 0; i < H; ++i) {
+      double x = 0.0;
+      for (int f = 0; f < F; ++f) x += dg[r * F + f] * wg[(int64_t)f * H + i] + du[r * F + f] * wu[(int64_t)f * H + i];
+      dxd[r * H + i] = x;
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int o = 0; o < H; ++o)
+    for (int f = 0; f < F; ++f) {
+      double x = 0.0;
+      for (int64_t r = 0; r < n; ++r) x += dyd[r * H + o] * h[r * F + f];
+      dwd[(int64_t)o * F + f] = x;
+    }
+#pragma omp parallel for schedule(static)
+  for (int f = 0; f < F; ++f)
+    for (int i = 0; i < H; ++i) {
+      double xg = 0.0, xu = 0.0;
+      for (int64_t r = 0; r < n; ++r) {
+        xg += dg[r * F + f] * a[r * H + i];
+        xu += du[r * F + f] * a[r * H + i];
+      }
+      dwg[(int64_t)f * H + i] = xg;
+      dwu[(int64_t)f * H + i] = xu;
+    }
+  free(h); free(dg); free(du);
+}
+
+/* Dispatch backward: dx[t] = sum_j dxd[r_tj] (+ dxd[R+t]): every copy of a token sends   */
+/* its gradient back to the token.                                                       */
+void oc_dispatch_backward(const double* dxd, const int32_t* tok_row, int T, int k, int H, int shared,
+                          double* dx) {
+  const int64_t R = (int64_t)T * k;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int i = 0; i < H; ++i) {
+      double s = 0.0;
+      for (int j = 0; j < k; ++j) s += dxd[(int64_t)tok_row[(int64_t)t * k + j] * H + i];
+      if (shared) s += dxd[(R + t) * H + i];
+      dx[(int64_t)t * H + i] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Second, independent oracle: the dense per-token loop. For each token, re-derive the    */
 /* top-k from its fp32 logits and run the chosen experts directly, with no counts, no     */
 /* permutation and no dispatch buffer. Weights in fp64 (Wg/Wu [E,F,H], Wd [E,H,F]).        */

@@ -543,6 +543,74 @@ def test_mxfp8_layer_with_representable_inputs_is_exact_before_h():
     assert np.array_equal(y, q["yd"])
 
 
+# ------------------------------------------------------------------ backward
+def test_expert_mlp_backward_matches_torch_autograd():
+    n, H, F = 13, 48, 40
+    a = synth.normal(20, 1, (n, H), 1.0, "f32").astype(np.float64)
+    wg = synth.normal(20, 3, (F, H), 0.2, "f32").astype(np.float64)
+    wu = synth.normal(20, 4, (F, H), 0.2, "f32").astype(np.float64)
+    wd = synth.normal(20, 5, (H, F), 0.2, "f32").astype(np.float64)
+    dyd = synth.normal(20, 6, (n, H), 1.0, "f32").astype(np.float64)
+    dxd, dwg, dwu, dwd = oracle.expert_mlp_backward(a, wg, wu, wd, dyd)
+    A, G, U, D = (torch.tensor(v, requires_grad=True) for v in (a, wg, wu, wd))
+    y = (torch.nn.functional.silu(A @ G.T) * (A @ U.T)) @ D.T
+    y.backward(torch.from_numpy(dyd))
+    for ours, ref in ((dxd, A), (dwg, G), (dwu, U), (dwd, D)):
+        assert np.allclose(ours, ref.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_combine_and_dispatch_backward_are_adjoints():
+    """<combine(yd), dy> = <yd, combine_bwd(dy)>, <dispatch(x), z> = <x, dispatch_bwd(z)>,
+    and the weight gradient is <dy[t], yd[r_tj]>: the backward steps are the transposes of
+    the forward permutations."""
+    T, k, E, H = 40, 3, 6, 24
+    idx, w = oracle.route(synth.synthetic_logits(21, T, E), cfg(E, k, renorm=1))
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    R = T * k
+    for shared in (False, True):
+        rows = R + (T if shared else 0)
+        yd = synth.normal(21, 7, (rows, H), 1.0, "f32").astype(np.float64)
+        dy = synth.normal(21, 8, (T, H), 1.0, "f32").astype(np.float64)
+        y = oracle.combine(yd[:R], tok_row, w, yd[R:] if shared else None)
+        dyd, dw = oracle.combine_backward(dy, yd, tok_row, w, shared)
+        assert np.isclose(np.sum(y * dy), np.sum(yd * dyd), rtol=1e-12)
+        assert np.allclose(dw, np.einsum("th,tjh->tj", dy, yd[tok_row]), rtol=1e-12)
+        x = synth.normal(21, 9, (T, H), 1.0, "f32").astype(np.float64)
+        z = synth.normal(21, 10, (rows, H), 1.0, "f32").astype(np.float64)
+        xd = x[row_token] if not shared else np.concatenate([x[row_token], x])
+        dx = oracle.dispatch_backward(z, tok_row, shared)
+        assert np.isclose(np.sum(xd * z), np.sum(x * dx), rtol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "dsv3"])
+def test_layer_backward_matches_finite_differences(name):
+    """L = <dy, y>; with the routing held fixed, the central difference of L along a random
+    direction of x or of each weight equals <grad, direction> (error O(eps^2))."""
+    w = {"mixtral": small("mixtral_bf16", T=10, H=32, E=4, F=24, renorm=1),
+         "dsv3": small("dsv3_bf16", T=8, H=32, E=8, k=2, F=16, F_shared=16, n_groups=2, topk_groups=1)}[name]
+    inp = {kk: (v.astype(np.float64) if isinstance(v, np.ndarray) else v)
+           for kk, v in synth.host_inputs(w, seed=22).items()}
+    logits = synth.synthetic_logits(22, w["T"], w["E"])
+    fwd = oracle.forward(w, inp, logits=logits)
+    dy = synth.normal(22, 11, (w["T"], w["H"]), 1.0, "f32").astype(np.float64)
+    g = oracle.backward(w, inp, fwd, dy)
+    pairs = [("x", "dx"), ("w_gate", "dw_gate"), ("w_up", "dw_up"), ("w_down", "dw_down")]
+    if w["n_shared"]:
+        pairs += [("ws_gate", "dws_gate"), ("ws_up", "dws_up"), ("ws_down", "dws_down")]
+    for tid, (key, gkey) in enumerate(pairs):
+        v = synth.normal(23, 40 + tid, inp[key].shape, 1.0, "f32").astype(np.float64)
+        eps = 1e-5 * np.abs(inp[key]).max()
+
+        def L(delta):
+            p = dict(inp)
+            p[key] = inp[key] + delta * v
+            return float(np.sum(oracle.forward(w, p, logits=logits)["y"] * dy))
+
+        fd = (L(eps) - L(-eps)) / (2 * eps)
+        an = float(np.sum(g[gkey] * v))
+        assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3), (key, fd, an)
+
+
 # ------------------------------------------------------------------ aux load-balancing loss
 def test_aux_loss_closed_forms():
     T, E, k = 64, 8, 2
