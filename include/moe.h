@@ -19,6 +19,8 @@
  *   moe_grouped_mlp     S4-S6  per expert: h = silu(xd Wg^T) * (xd Wu^T); yd = h Wd^T
  *   moe_combine         S7  y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ shared row)
  *   moe_forward         S0-S7 in one stream-ordered call
+ *   moe_backward        the training step's backward of S3-S7 (bf16 layers): combine,
+ *                       the experts' grouped dgrad/wgrad with recomputed SwiGLU, dispatch
  *
  * Conventions shared by every call:
  *  - Every data pointer is DEVICE memory owned by the caller; the library allocates
@@ -100,6 +102,17 @@ typedef struct {
   const void* ss_up;        /* E4M3: fp32 [F/128, H/128]; MXE4M3: atoms of [F, H] */
   const void* ss_down;      /* E4M3: fp32 [H/128, F/128]; MXE4M3: atoms of [H, F] */
 } moe_weights_t;
+
+/* Weight gradients written by the backward (device fp32, caller-owned; overwritten, not
+ * accumulated). */
+typedef struct {
+  float* dw_gate;  /* [E, F, H] */
+  float* dw_up;    /* [E, F, H] */
+  float* dw_down;  /* [E, H, F] */
+  float* dws_gate; /* shared expert [F, H], or NULL when n_shared = 0 */
+  float* dws_up;   /* [F, H] */
+  float* dws_down; /* [H, F] */
+} moe_weight_grads_t;
 
 /* MX scale atoms. The UE8M0 codes (code = s + 127 for the block scale 2^s) of an e4m3
  * matrix with K columns (K a multiple of 128) are stored in 512-byte atoms, each covering
@@ -235,6 +248,56 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                          void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
                          int32_t* counts_out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Backward (a training step; bf16 layers on the tensor-core path, H % 256 == 0 and
+ * F % 256 == 0, else MOE_ERR_UNSUPPORTED). The routing (map, weights, permutation) is that
+ * of the forward and is held fixed: these calls return the gradient of the layer output with
+ * respect to x through the experts, to the routing weights and to the expert weights. The
+ * router's own backward (to its logits and weight) is not part of them. The experts' grouped
+ * GEMMs serve the backward as in the forward (Megatron-Core summary, section 2.4), and the
+ * SwiGLU activation is recomputed from the dispatched rows instead of being kept from the
+ * forward (section 2.2, recomputation).
+ * --------------------------------------------------------------------------------------- */
+
+/* Bytes of workspace for moe_grouped_mlp_backward and moe_backward: the status head, then
+ * dyd and dxd [R(+T), H], g/u and their gradients [R(+T), 2F], and h [R(+T), F], all bf16.
+ * Zero it once with moe_workspace_init (its status word). */
+moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Combine backward: from the output gradient dy [T,H] and the forward's yd [R(+T), H],
+ *   dyd[tok_row[t,j]] = topk_w[t,j] * dy[t],  dyd[R + t] = dy[t] (shared expert),
+ *   dtopk_w[t,j] = sum_o dy[t,o] * yd[tok_row[t,j], o]   (fp32, the routing-weight gradient).
+ * dyd [R(+T), H] bf16. */
+moe_status_t moe_combine_backward(const moe_config_t* cfg, const void* dy, const void* yd,
+                                  const int32_t* tok_row, const float* topk_w, void* dyd,
+                                  float* dtopk_w, moe_stream_t stream);
+
+/* The experts' backward as grouped GEMMs on the tensor cores, per expert e over its rows
+ * (and the shared expert over rows R + t with input x[t]): g, u = xd Wg^T, xd Wu^T are
+ * recomputed; dh = dyd Wd; dg = dh u s (1 + g (1 - s)), du = dh g s with s = sigmoid(g);
+ * dxd = dg Wg + du Wu; dWd[e] = dyd^T h with h = g s u; dWg[e] = dg^T xd; dWu[e] = du^T xd
+ * (sums over the expert's rows; an expert without rows gets zero gradients). xd [R, H] are
+ * the forward's dispatched rows, x [T, H] the tokens (read for the shared expert), dyd from
+ * moe_combine_backward; dxd [R(+T), H] bf16; grads fp32. ws: moe_backward_workspace_size. */
+moe_status_t moe_grouped_mlp_backward(const moe_config_t* cfg, const void* xd, const void* x,
+                                      const int32_t* offsets, const moe_weights_t* w, const void* dyd,
+                                      void* dxd, const moe_weight_grads_t* grads, void* ws,
+                                      moe_stream_t stream);
+
+/* Dispatch backward: dx[t] = sum_j dxd[tok_row[t,j]] (+ dxd[R + t]), fp32 in that order,
+ * written once in bf16 (the combine kernel with unit weights). */
+moe_status_t moe_dispatch_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row,
+                                   void* dx, moe_stream_t stream);
+
+/* The three calls above in one stream-ordered call after moe_forward: the routing, the
+ * dispatched rows and yd are read from that call's workspace fwd_ws (so it must not have
+ * been reused in between), x and w are the forward's inputs, dy [T,H] bf16. Writes
+ * dx [T,H] bf16, dtopk_w [T,k] fp32 and the weight gradients. bwd_ws:
+ * moe_backward_workspace_size bytes. */
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                          const void* dy, const void* fwd_ws, void* dx, float* dtopk_w,
+                          const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream);
 
 /* Offline weight preparation for the E4M3 variant: quantise a bf16 [rows, cols] matrix in
  * br x bc blocks with the rule of moe_dispatch; q [rows, cols] e4m3, scale

@@ -1,0 +1,157 @@
+"""The backward (training step) on the GPU against the oracle's chain rule: combine
+backward (row gradients and routing-weight gradients), the experts' grouped dgrad/wgrad
+with the SwiGLU activation recomputed, and dispatch backward, on bf16 layers that span
+several tiles, ragged segments, K tails of the weight-gradient reductions, empty and hot
+experts, the shared expert and the CTA-pair form of the recomputed gate/up GEMM. The
+routing is the oracle's (uploaded); the GPU runs its own forward on it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import token_routing_expert_router_gb300 as moe
+from moe_case import alloc, cfg_of, device_weights_from_host, np_of, up, weights_arg
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+CASES = [
+    synth.scaled(W["mixtral_bf16"], T=600, H=512, E=4, F=512, name="mixtral_small"),
+    synth.scaled(W["dsv3_bf16"], T=260, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="dsv3_small"),
+    synth.scaled(W["imbalanced_bf16"], T=700, H=256, E=32, k=4, F=256, name="imbalanced_small"),
+    # >= 512 rows per expert: the recomputed gate/up GEMM runs as CTA pairs
+    synth.scaled(W["dsv3_bf16"], T=1200, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2, topk_groups=1,
+                 name="pair_shared"),
+]
+TOL = 1e-2  # bf16 layers
+
+
+def logits_for(w, seed):
+    l = synth.synthetic_logits(seed, w["T"], w["E"])
+    if w["zipf"]:
+        l = (l + 4.0 * synth.zipf_bias(seed, w["E"])).astype(np.float32)
+    return l
+
+
+def grads_alloc(w):
+    E, H, F = w["E"], w["H"], w["F"]
+    g = {"dw_gate": torch.empty((E, F, H), dtype=torch.float32, device="cuda"),
+         "dw_up": torch.empty((E, F, H), dtype=torch.float32, device="cuda"),
+         "dw_down": torch.empty((E, H, F), dtype=torch.float32, device="cuda")}
+    if w["n_shared"]:
+        g["dws_gate"] = torch.empty((F, H), dtype=torch.float32, device="cuda")
+        g["dws_up"] = torch.empty((F, H), dtype=torch.float32, device="cuda")
+        g["dws_down"] = torch.empty((H, F), dtype=torch.float32, device="cuda")
+    return g
+
+
+def run_staged_backward(w, d, b, dy):
+    """GPU forward on the routing already in b, then the three staged backward calls."""
+    cfg = b["cfg"]
+    T, H, k = w["T"], w["H"], w["k"]
+    rows = T * k + (T if w["n_shared"] else 0)
+    moe.moe_dispatch(cfg, d["x"], b["tok_row"], b["xd"], None)
+    moe.moe_grouped_mlp(cfg, b["xd"], None, d["x"], b["offsets"], weights_arg(d), b["h"], None, b["yd"], b["ws"])
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(bws)
+    out = {"dyd": torch.empty((rows, H), dtype=torch.bfloat16, device="cuda"),
+           "dtopk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+           "dxd": torch.empty((rows, H), dtype=torch.bfloat16, device="cuda"),
+           "dx": torch.empty((T, H), dtype=torch.bfloat16, device="cuda")}
+    g = grads_alloc(w)
+    moe.moe_combine_backward(cfg, dy, b["yd"], b["tok_row"], b["topk_w"], out["dyd"], out["dtopk_w"])
+    moe.moe_grouped_mlp_backward(cfg, b["xd"], d["x"], b["offsets"], weights_arg(d), out["dyd"], out["dxd"], g, bws)
+    moe.moe_dispatch_backward(cfg, out["dxd"], b["tok_row"], out["dx"])
+    out.update(g)
+    assert moe.moe_read_status(bws) == moe.MOE_OK
+    return out
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c["name"] for c in CASES])
+def test_backward_against_oracle(w):
+    seed = 31
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    R = T * k
+    inp = synth.host_inputs(w, seed=seed)
+    logits = logits_for(w, seed)
+    ref_fwd = oracle.forward(w, inp, logits=logits)
+    dy_h = synth.normal(seed, 50, (T, H), 1.0, "bf16")
+    ref = oracle.backward(w, inp, ref_fwd, dy_h.astype(np.float64))
+    counts = ref_fwd["counts"]
+    if w["zipf"]:
+        assert (counts == 0).any()
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    b["topk_w"].copy_(up(ref_fwd["topk_w"].astype(np.float32)))
+    b["offsets"].copy_(up(ref_fwd["offsets"]))
+    b["tok_row"].copy_(up(ref_fwd["tok_row"]))
+    got = run_staged_backward(w, d, b, up(dy_h, torch.bfloat16))
+    g = {key: np_of(v).astype(np.float64) for key, v in got.items()}
+    assert oracle.rel_l2(g["dyd"], ref["dyd"]) < TOL
+    assert oracle.rel_l2(g["dtopk_w"], ref["dtopk_w"]) < TOL
+    assert oracle.rel_l2(g["dxd"], ref["dxd"]) < TOL
+    assert oracle.rel_l2(g["dx"], ref["dx"]) < TOL
+    off = ref_fwd["offsets"]
+    for e in range(E):  # each expert's rows and weight gradients on their own
+        if counts[e] == 0:
+            for key in ("dw_gate", "dw_up", "dw_down"):
+                assert not g[key][e].any(), (key, e)
+            continue
+        assert oracle.rel_l2(g["dxd"][off[e]:off[e + 1]], ref["dxd"][off[e]:off[e + 1]]) < TOL, e
+        for key in ("dw_gate", "dw_up", "dw_down"):
+            assert oracle.rel_l2(g[key][e], ref[key][e]) < TOL, (key, e)
+    if w["n_shared"]:
+        for key in ("dws_gate", "dws_up", "dws_down"):
+            assert oracle.rel_l2(g[key], ref[key]) < TOL, key
+        assert oracle.rel_l2(g["dxd"][R:], ref["dxd"][R:]) < TOL
+
+
+@pytest.mark.parametrize("w", [CASES[1], CASES[3]], ids=["dsv3_small", "pair_shared"])
+def test_backward_after_forward_equals_staged(w):
+    """moe_backward reads the routing, xd and yd from moe_forward's workspace and runs the
+    same kernels as the staged calls: identical bits."""
+    seed = 32
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    inp = synth.host_inputs(w, seed=seed)
+    d = device_weights_from_host(w, inp)
+    cfg = cfg_of(w)
+    fws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(fws)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_forward(cfg, d["x"], weights_arg(d), y, fws, idx, wt)
+    dy = up(synth.normal(seed, 50, (T, H), 1.0, "bf16"), torch.bfloat16)
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(bws)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dtw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    g1 = grads_alloc(w)
+    moe.moe_backward(cfg, d["x"], weights_arg(d), dy, fws, dx, dtw, g1, bws)
+    assert moe.moe_read_status(bws) == moe.MOE_OK
+    # staged, on the same routing (the permutation rebuilt from the forward's map)
+    b = alloc(w)
+    moe.moe_route_from_map(b["cfg"], idx, b["counts"], b["offsets"], b["row_token"], b["tok_row"], b["ws"])
+    b["topk_w"].copy_(wt)
+    got = run_staged_backward(w, d, b, dy)
+    assert torch.equal(got["dx"], dx)
+    assert torch.equal(got["dtopk_w"], dtw)
+    for key in g1:
+        assert torch.equal(got[key], g1[key]), key
+
+
+def test_backward_no_tokens_gives_zero_weight_gradients():
+    w = synth.scaled(CASES[1], T=0)
+    cfg = cfg_of(w)
+    inp = synth.host_inputs(synth.scaled(CASES[1], T=4), seed=33)
+    d = device_weights_from_host(synth.scaled(CASES[1], T=4), inp)
+    g = grads_alloc(w)
+    for v in g.values():
+        v.fill_(7.0)
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_backward(cfg, None, weights_arg(d), None, None, None, None, g, bws)
+    torch.cuda.synchronize()
+    for key, v in g.items():
+        assert not v.any(), key

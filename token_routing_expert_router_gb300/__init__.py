@@ -63,6 +63,17 @@ class MoEWeights(ctypes.Structure):
         return w
 
 
+class MoEWeightGrads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw_up", "dw_down", "dws_gate", "dws_up", "dws_down")]
+
+    @classmethod
+    def from_tensors(cls, d: dict) -> "MoEWeightGrads":
+        g = cls()
+        for name, _ in cls._fields_:
+            setattr(g, name, _ptr(d.get(name)))
+        return g
+
+
 _lib = None
 
 
@@ -94,6 +105,11 @@ def lib():
             "moe_dispatch_mx": [cfg, P, P, P, P, P, P, P],
             "moe_mx_scale_bytes": [cfg, c_int32, POINTER(c_size_t)],
             "moe_quantize_mx": [P, c_int64, c_int64, P, P, P],
+            "moe_backward_workspace_size": [cfg, POINTER(c_size_t)],
+            "moe_combine_backward": [cfg, P, P, P, P, P, P, P],
+            "moe_grouped_mlp_backward": [cfg, P, P, P, wts, P, P, POINTER(MoEWeightGrads), P, P],
+            "moe_dispatch_backward": [cfg, P, P, P, P],
+            "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
             "moe_grouped_mlp_gather": [cfg, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
@@ -118,6 +134,8 @@ def exported_symbols() -> list:
             "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
             "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_quantize_e4m3",
             "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
+            "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_mlp_backward",
+            "moe_dispatch_backward", "moe_backward",
             "moe_read_status", "moe_status_string", "moe_route_static_scratch",
             "moe_selftest_bounded_wait"]
 
@@ -236,6 +254,36 @@ def moe_quantize_e4m3(src, br: int, bc: int, q, scale, stream=None):
     rows, cols = src.shape
     _check(lib().moe_quantize_e4m3(_ptr(src), rows, cols, br, bc, _ptr(q), _ptr(scale),
                                    _stream(stream)), "moe_quantize_e4m3")
+
+
+def moe_backward_workspace_size(cfg: MoEConfig) -> int:
+    n = c_size_t()
+    _check(lib().moe_backward_workspace_size(byref(cfg), byref(n)), "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_combine_backward(cfg, dy, yd, tok_row, topk_w, dyd, dtopk_w, stream=None):
+    _check(lib().moe_combine_backward(byref(cfg), _ptr(dy), _ptr(yd), _ptr(tok_row), _ptr(topk_w), _ptr(dyd),
+                                      _ptr(dtopk_w), _stream(stream)), "moe_combine_backward")
+
+
+def moe_grouped_mlp_backward(cfg, xd, x, offsets, weights: dict, dyd, dxd, grads: dict, ws, stream=None):
+    w = MoEWeights.from_tensors(weights)
+    g = MoEWeightGrads.from_tensors(grads)
+    _check(lib().moe_grouped_mlp_backward(byref(cfg), _ptr(xd), _ptr(x), _ptr(offsets), byref(w), _ptr(dyd),
+                                          _ptr(dxd), byref(g), _ptr(ws), _stream(stream)), "moe_grouped_mlp_backward")
+
+
+def moe_dispatch_backward(cfg, dxd, tok_row, dx, stream=None):
+    _check(lib().moe_dispatch_backward(byref(cfg), _ptr(dxd), _ptr(tok_row), _ptr(dx), _stream(stream)),
+           "moe_dispatch_backward")
+
+
+def moe_backward(cfg, x, weights: dict, dy, fwd_ws, dx, dtopk_w, grads: dict, bwd_ws, stream=None):
+    w = MoEWeights.from_tensors(weights)
+    g = MoEWeightGrads.from_tensors(grads)
+    _check(lib().moe_backward(byref(cfg), _ptr(x), byref(w), _ptr(dy), _ptr(fwd_ws), _ptr(dx), _ptr(dtopk_w),
+                              byref(g), _ptr(bwd_ws), _stream(stream)), "moe_backward")
 
 
 def moe_quantize_mx(src, q, sf, stream=None):

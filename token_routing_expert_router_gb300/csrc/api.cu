@@ -108,6 +108,35 @@ FwdLayout fwd_layout(const moe_config_t& c) {
   return L;
 }
 
+// Backward workspace: status head, then dyd, dxd [rows, H], gu, dgu [rows, 2F], h [rows, F].
+struct BwdLayout {
+  size_t dyd, dxd, gu, dgu, h, total;
+};
+
+BwdLayout bwd_layout(const moe_config_t& c) {
+  BwdLayout L;
+  size_t o = kWsHead;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t rows = (size_t)total_rows(c);
+  L.dyd = take(rows * c.H * 2);
+  L.dxd = take(rows * c.H * 2);
+  L.gu = take(rows * 2 * c.F * 2);
+  L.dgu = take(rows * 2 * c.F * 2);
+  L.h = take(rows * c.F * 2);
+  L.total = o;
+  return L;
+}
+
+bool grads_ok(const moe_config_t& c, const moe_weight_grads_t* g) {
+  if (!g || !ptr_ok(g->dw_gate) || !ptr_ok(g->dw_up) || !ptr_ok(g->dw_down)) return false;
+  if (c.n_shared && (!ptr_ok(g->dws_gate) || !ptr_ok(g->dws_up) || !ptr_ok(g->dws_down))) return false;
+  return true;
+}
+
 moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* w, bool need_router) {
   if (!w) return MOE_ERR_INVALID_ARG;
   if (need_router && !ptr_ok(w->w_router)) return MOE_ERR_INVALID_ARG;
@@ -395,6 +424,94 @@ moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols,
   if ((br != 1 && br != 128) || (bc != 1 && bc != 128)) return MOE_ERR_UNSUPPORTED;
   if (ceil_div(rows, br) * ceil_div(cols, bc) > (int64_t)INT32_MAX) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_quantize_e4m3(src_bf16, rows, cols, br, bc, q, scale, (cudaStream_t)stream));
+}
+
+moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (!tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  *bytes = bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_combine_backward(const moe_config_t* cfg, const void* dy, const void* yd, const int32_t* tok_row,
+                                  const float* topk_w, void* dyd, float* dtopk_w, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(dy) || !ptr_ok(yd) || !ptr_ok(tok_row) || !ptr_ok(topk_w) || !ptr_ok(dyd) || !ptr_ok(dtopk_w))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_backward(*cfg, dy, yd, tok_row, topk_w, dyd, dtopk_w, (cudaStream_t)stream));
+}
+
+moe_status_t moe_grouped_mlp_backward(const moe_config_t* cfg, const void* xd, const void* x, const int32_t* offsets,
+                                      const moe_weights_t* w, const void* dyd, void* dxd,
+                                      const moe_weight_grads_t* grads, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  v = check_weights(*cfg, w, false);
+  if (v != MOE_OK) return v;
+  if (!grads_ok(*cfg, grads)) return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c.T > 0 && (!ptr_ok(xd) || !ptr_ok(offsets) || !ptr_ok(dyd) || !ptr_ok(dxd) || !ptr_ok(ws) ||
+                  (c.n_shared && !ptr_ok(x))))
+    return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) {  // no rows: every weight gradient is zero
+    cudaError_t e = cudaMemsetAsync(grads->dw_gate, 0, (size_t)c.E * c.F * c.H * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(grads->dw_up, 0, (size_t)c.E * c.F * c.H * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(grads->dw_down, 0, (size_t)c.E * c.F * c.H * 4, s);
+    if (e == cudaSuccess && c.n_shared) e = cudaMemsetAsync(grads->dws_gate, 0, (size_t)c.F * c.H * 4, s);
+    if (e == cudaSuccess && c.n_shared) e = cudaMemsetAsync(grads->dws_up, 0, (size_t)c.F * c.H * 4, s);
+    if (e == cudaSuccess && c.n_shared) e = cudaMemsetAsync(grads->dws_down, 0, (size_t)c.F * c.H * 4, s);
+    return cuda_status(e);
+  }
+  const BwdLayout L = bwd_layout(c);
+  char* base = (char*)ws;
+  return cuda_status(tc::launch_grouped_mlp_backward(c, xd, x, offsets, *w, dyd, base + L.gu, base + L.dgu,
+                                                     base + L.h, dxd, *grads, status_of(ws), s));
+}
+
+moe_status_t moe_dispatch_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row, void* dx,
+                                   moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->act_dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(dxd) || !ptr_ok(tok_row) || !ptr_ok(dx)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*cfg, dxd, tok_row, nullptr, dx, (cudaStream_t)stream));
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                          const void* fwd_ws, void* dx, float* dtopk_w, const moe_weight_grads_t* grads, void* bwd_ws,
+                          moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return moe_grouped_mlp_backward(cfg, nullptr, nullptr, nullptr, w, nullptr, nullptr, grads,
+                                                   bwd_ws, stream);
+  v = check_weights(*cfg, w, false);
+  if (v != MOE_OK) return v;
+  if (!ptr_ok(x) || !ptr_ok(dy) || !ptr_ok(fwd_ws) || !ptr_ok(dx) || !ptr_ok(dtopk_w) || !ptr_ok(bwd_ws) ||
+      !grads_ok(*cfg, grads))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  cudaStream_t s = (cudaStream_t)stream;
+  const FwdLayout F = fwd_layout(c);
+  const BwdLayout B = bwd_layout(c);
+  const char* fb = (const char*)fwd_ws;
+  char* bb = (char*)bwd_ws;
+  const int32_t* tok_row = (const int32_t*)(fb + F.tok_row);
+  cudaError_t e = launch_combine_backward(c, dy, fb + F.yd, tok_row, (const float*)(fb + F.topk_w), bb + B.dyd,
+                                          dtopk_w, s);
+  if (e == cudaSuccess)
+    e = tc::launch_grouped_mlp_backward(c, fb + F.xd, x, (const int32_t*)(fb + F.offsets), *w, bb + B.dyd,
+                                        bb + B.gu, bb + B.dgu, bb + B.h, bb + B.dxd, *grads, status_of(bwd_ws), s);
+  if (e == cudaSuccess) e = launch_combine(c, bb + B.dxd, tok_row, nullptr, dx, s);
+  return cuda_status(e);
 }
 
 moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,

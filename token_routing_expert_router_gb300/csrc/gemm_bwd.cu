@@ -1,0 +1,583 @@
+// Backward of the grouped expert MLP (bf16 layers) on the tcgen05 tensor cores.
+//
+// The backward of the experts' grouped GEMM ("Scalable Training of Mixture-of-Experts
+// Models with Megatron Core" summary, section 2.4 grouped GEMM, which serves the training
+// step in both directions; section 2.2 recomputation instead of stored activations) is
+// four grouped GEMMs over the same expert segments as the forward:
+//   DGRAD_DOWN  dh  = dyd . Wd            K = H, B = Wd read MN-major (its rows are the K
+//               index), fused epilogue: g and u (recomputed by the forward GEMM1 kernel
+//               into gu) give h = silu(g) u and the SwiGLU backward dg, du -> dgu, h
+//   DGRAD_GU    dxd = dg . Wg + du . Wu   K = 2F (dgu's interleaved gate/up blocks), B =
+//               Wg or Wu per K block, read MN-major
+//   WGRAD_DOWN  dWd[e] = dyd_e^T . h_e    K = the expert's token rows, both operands
+//               MN-major (an activation's rows are the K index)
+//   WGRAD_GU    dWg[e], dWu[e] = dgu_e^T . xd_e
+// An MN-major operand is loaded by TMA as boxes of 64 MN elements (128 bytes, 128-byte
+// swizzle) x 64 K rows; its shared-memory descriptor has LBO = the byte distance between
+// the 64-element MN blocks (8 KB here), SBO = 1024 B between 8-row K groups, and each MMA
+// of K = 16 advances the start by 16 rows (2 KB). Instruction-descriptor bits 15 / 16 mark
+// A / B as MN-major.
+// Wgrad reduces over an expert's rows: the last K stage of a segment holds rows of the next
+// expert past the segment's end, so the MMA warp zeroes those rows of B in shared memory
+// (whole 128-byte lines, which the swizzle keeps intact) before the MMAs; an expert without
+// rows gets an all-zero gradient from the epilogue without touching the tensor core.
+//
+// Block (as the forward bf16 kernel): warp 0 TMA producer, warp 1 MMA issuer (TMEM owner),
+// warps 2-5 epilogue (one output row per thread, two TMEM accumulators of 256 columns).
+// Tile 128 x 256, K stages of 64 (128 bytes), 4 stages of 48 KB.
+#include <cudaTypedefs.h>
+
+#include "gemm_tc.cuh"
+#include "tc_common.cuh"
+
+namespace moe {
+namespace tc {
+
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows, uint64_t cols,
+               uint32_t box_rows, uint32_t box_cols);
+int num_sms();
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;  // BK in bf16 elements (128 bytes)
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB: four MN boxes of 8 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kMaxGroups = 514;
+constexpr int kTmemCols = 2 * BN;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + 4 * 2048;
+
+enum Mode { DGRAD_DOWN = 0, DGRAD_GU = 1, WGRAD_DOWN = 2, WGRAD_GU = 3 };
+
+struct BwdParams {
+  const int32_t* offsets;
+  int G, has_extra, T_extra, a2_row_base;  // the shared expert's rows: [a2_row_base, + T_extra)
+  int K;             // dgrad: the contraction length (H or 2F)
+  int n_tiles;       // 256-wide N tiles (dgrad: N/256; wgrad: N_out/256)
+  int m_tiles_out;   // wgrad: M_out/128
+  int b_group_rows;  // dgrad: rows of B per routed group in its map (H for Wd, F for Wg/Wu)
+  int F;
+  int ldc;                    // dgrad output row length (elements)
+  __nv_bfloat16* out;         // DGRAD_DOWN: dgu [rows, 2F]; DGRAD_GU: dxd [rows, H]
+  __nv_bfloat16* h_out;       // DGRAD_DOWN: h [rows, F]
+  const __nv_bfloat16* gu;    // DGRAD_DOWN: g and u [rows, 2F], interleaved in 128-column blocks
+  float* w0;                  // WGRAD_DOWN: dWd [G, M_out, N_out]; WGRAD_GU: dWg [G, F, H]
+  float* w1;                  // WGRAD_GU: dWu [G, F, H]
+  float* w0x;                 // the shared expert's (same layouts without the G dimension)
+  float* w1x;
+  int M_out, N_out;
+  int extra_b_row0;           // wgrad: the shared expert's first row in its B map (tmB0x)
+  DeviceStatus* status;
+  uint64_t timeout_ns;
+};
+
+struct TileCoord {
+  int g, mb, nb, rows;  // dgrad: m tile mb of group g (rows valid); wgrad: out tile (mb, nb), rows = K rows
+};
+
+__device__ __forceinline__ TileCoord decode_dgrad(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
+                                                  const int32_t* seg_rows) {
+  int lo = 0, hi = ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileCoord c;
+  c.g = lo;
+  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
+  const int local = tile - n_tiles * mt_prefix[lo];
+  c.nb = local / mt;
+  c.mb = local - c.nb * mt;
+  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  return c;
+}
+
+__device__ __forceinline__ TileCoord decode_wgrad(int tile, int m_tiles, int n_tiles, const int32_t* seg_rows) {
+  const int per = m_tiles * n_tiles;
+  TileCoord c;
+  c.g = tile / per;
+  const int local = tile - c.g * per;
+  c.mb = local / n_tiles;
+  c.nb = local - c.mb * n_tiles;
+  c.rows = seg_rows[c.g];
+  return c;
+}
+
+// Shared-memory descriptor of an MN-major operand stored as MN blocks of 64 elements x
+// the stage's K rows (128-byte swizzle): LBO = distance between the MN blocks, SBO =
+// 1024 B between groups of 8 K rows.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bwd(bool a_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0x,
+                       const __grid_constant__ CUtensorMap tmB1x, const BwdParams p) {
+  constexpr bool kWgrad = MODE == WGRAD_DOWN || MODE == WGRAD_GU;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* mt_prefix = reinterpret_cast<int32_t*>(bars + 32);
+  int32_t* seg_rows = mt_prefix + kMaxGroups;
+  uint8_t* sEpi = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups);  // [4 warps][32 rows][64 B]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = p.G + p.has_extra;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 2) {
+    int carry = 0;
+    for (int g0 = 0; g0 < ngroups; g0 += 32) {
+      const int g = g0 + lane;
+      int rows = 0;
+      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
+      else if (g < ngroups) rows = p.T_extra;
+      const int mt = (rows + BM - 1) / BM;
+      int inc = mt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      if (g < ngroups) {
+        seg_rows[g] = rows;
+        mt_prefix[g] = carry + inc - mt;
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) mt_prefix[ngroups] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = kWgrad ? ngroups * p.m_tiles_out * p.n_tiles : p.n_tiles * mt_prefix[ngroups];
+  auto decode = [&](int tile) {
+    return kWgrad ? decode_wgrad(tile, p.m_tiles_out, p.n_tiles, seg_rows)
+                  : decode_dgrad(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+  };
+  auto kblocks_of = [&](const TileCoord& c) { return kWgrad ? (c.rows + BK - 1) / BK : p.K / BK; };
+  auto group_row0 = [&](int g) { return g >= p.G ? p.a2_row_base : p.offsets[g]; };
+
+  if (warp == 0) {
+    // ======================= TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const TileCoord c = decode(tile);
+        const bool extra = c.g >= p.G;
+        const int row0 = group_row0(c.g);
+        const int kbs = kblocks_of(c);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          if constexpr (kWgrad) {
+            // A: activation [rows, M_out] MN-major (2 boxes); B: activation [rows, N_out] (4 boxes)
+            const int y = row0 + kb * BK;
+            tma_load_2d(&tmA, a_dst, &full[stage], c.mb * BM, y);
+            tma_load_2d(&tmA, a_dst + 8192, &full[stage], c.mb * BM + 64, y);
+            const CUtensorMap* tb = extra ? &tmB0x : &tmB0;
+            const int yb = extra ? p.extra_b_row0 + kb * BK : y;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], c.nb * BN + 64 * j, yb);
+          } else {
+            // A: [rows, K] K-major, 128 rows; B: weight rows = the K index, MN-major (4 boxes)
+            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, row0 + c.mb * BM);
+            const CUtensorMap* tb;
+            int brow;
+            if (MODE == DGRAD_DOWN) {
+              tb = extra ? &tmB0x : &tmB0;
+              brow = kb * BK;
+            } else {  // K = 2F: 128-column blocks alternate gate / up
+              const bool up = (kb >> 1) & 1;
+              tb = extra ? (up ? &tmB1x : &tmB0x) : (up ? &tmB1 : &tmB0);
+              brow = (kb >> 2) * 128 + (kb & 1) * 64;
+            }
+            brow += extra ? 0 : c.g * p.b_group_rows;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], c.nb * BN + 64 * j, brow);
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      const int used = issued < kStages ? (int)issued : kStages;
+      for (int i = 0; i < used; ++i) {
+        const int s = (stage - 1 - i + 2 * kStages) % kStages;
+        const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
+        if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
+        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (lane 0), with the warp zeroing wgrad tails
+    constexpr uint32_t idesc = idesc_bwd(kWgrad);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const TileCoord c = decode(tile);
+      const int kbs = kblocks_of(c);
+      if (kbs == 0) continue;  // an expert without rows: the epilogue writes zeros
+      ok = mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < kbs; ++kb) {
+        ok = mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint8_t* b_st = sB + stage * kBBytes;
+        if (kWgrad) {
+          const int valid = c.rows - kb * BK;
+          if (valid < BK) {  // rows past the segment's end contribute nothing
+            const int lines = BK - valid;
+            for (int i = lane; i < 4 * lines * 8; i += 32) {
+              const int box = i / (lines * 8), rem = i - box * lines * 8;
+              const int line = valid + rem / 8, chunk = rem & 7;
+              *reinterpret_cast<uint4*>(b_st + box * 8192 + line * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_addr = smem_addr(sA + stage * kABytes);
+          const uint32_t b_addr = smem_addr(b_st);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = kWgrad ? desc_mn_sw128(a_addr + k * 2048, 8192) : desc_k_sw128(a_addr + k * 32);
+            mma_bf16(d_tmem, ad, desc_mn_sw128(b_addr + k * 2048, 8192), idesc, (kb | k) != 0);
+          }
+          mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (ok && lane == 0) mma_commit(&tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if (lane == 0) {
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    uint8_t* stage = sEpi + (warp - 2) * 2048;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord c = decode(tile);
+      const bool extra = c.g >= p.G;
+      const bool empty_tile = kblocks_of(c) == 0;
+      if (!empty_tile) {
+        bool ok = mbar_wait(&tfull[acc], acc_phase, abort, p.timeout_ns, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if constexpr (kWgrad) {
+        // fp32 gradient rows: row r of the 128-row output tile, 256 columns
+        float* wbase;
+        int64_t ldo;
+        if (MODE == WGRAD_DOWN) {
+          ldo = p.N_out;
+          wbase = (extra ? p.w0x : p.w0 + (int64_t)c.g * p.M_out * p.N_out) + (int64_t)c.mb * BM * ldo;
+        } else {  // dgu's 128-row blocks alternate dWg / dWu rows of one F block
+          ldo = p.N_out;
+          const bool up = c.mb & 1;
+          float* w = up ? (extra ? p.w1x : p.w1 + (int64_t)c.g * p.F * p.N_out)
+                        : (extra ? p.w0x : p.w0 + (int64_t)c.g * p.F * p.N_out);
+          wbase = w + (int64_t)(c.mb >> 1) * BM * ldo;
+        }
+        uint8_t* out = reinterpret_cast<uint8_t*>(wbase + (int64_t)quarter * 32 * ldo + c.nb * BN);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          if (!empty_tile) {
+            tmem_ld32(t_row + c0, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {  // 16 fp32 = 64 bytes per pass
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              stage_piece(stage, lane, q, make_uint4(v[16 * h2 + 4 * q], v[16 * h2 + 4 * q + 1], v[16 * h2 + 4 * q + 2],
+                                                     v[16 * h2 + 4 * q + 3]));
+            flush_rows_64B(stage, lane, out + 4 * (c0 + 16 * h2), ldo * 4, 32);
+          }
+        }
+      } else {
+        const int row0 = group_row0(c.g);
+        const int64_t warp_row0 = (int64_t)row0 + c.mb * BM + quarter * 32;
+        const int warp_live = c.rows - quarter * 32;
+        const bool live = r < c.rows;
+        if (MODE == DGRAD_GU) {
+          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(t_row + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              stage_piece(stage, lane, q,
+                          make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
+            flush_rows_64B(stage, lane, out + 2 * c0, (int64_t)p.ldc * 2, warp_live);
+          }
+        } else {  // DGRAD_DOWN: dh -> SwiGLU backward with g, u from gu; writes dg, du and h
+          const int64_t row = warp_row0 + lane;
+          const int ld_gu = 2 * p.F;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            const int f0 = c.nb * BN + c0;     // first F column of the chunk
+            const int blk = f0 >> 7, cb = f0 & 127;
+            uint32_t dh[32];
+            tmem_ld32(t_row + c0, dh);
+            uint4 graw[4], uraw[4];
+            if (live) {
+              const uint4* gp = reinterpret_cast<const uint4*>(p.gu + row * ld_gu + blk * 256 + cb);
+              const uint4* up = reinterpret_cast<const uint4*>(p.gu + row * ld_gu + blk * 256 + 128 + cb);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                graw[q] = __ldg(gp + q);
+                uraw[q] = __ldg(up + q);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) graw[q] = uraw[q] = make_uint4(0, 0, 0, 0);
+            }
+            tmem_ld_wait();
+            uint32_t pdg[16], pdu[16], ph[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t gw[4] = {graw[q].x, graw[q].y, graw[q].z, graw[q].w};
+              const uint32_t uw[4] = {uraw[q].x, uraw[q].y, uraw[q].z, uraw[q].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float dgv[2], duv[2], hv[2];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                  const float g = __uint_as_float(s2 ? (gw[e] & 0xffff0000u) : (gw[e] << 16));
+                  const float u = __uint_as_float(s2 ? (uw[e] & 0xffff0000u) : (uw[e] << 16));
+                  const float d = __uint_as_float(dh[8 * q + 2 * e + s2]);
+                  const float sg = 1.0f / (1.0f + __expf(-g));
+                  const float silu = g * sg;
+                  hv[s2] = silu * u;
+                  dgv[s2] = d * u * sg * (1.0f + g * (1.0f - sg));
+                  duv[s2] = d * silu;
+                }
+                pdg[4 * q + e] = pack_bf16(dgv[0], dgv[1]);
+                pdu[4 * q + e] = pack_bf16(duv[0], duv[1]);
+                ph[4 * q + e] = pack_bf16(hv[0], hv[1]);
+              }
+            }
+            uint8_t* dgu_rows = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * ld_gu + blk * 256 + cb) * 2;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              stage_piece(stage, lane, q, make_uint4(pdg[4 * q], pdg[4 * q + 1], pdg[4 * q + 2], pdg[4 * q + 3]));
+            flush_rows_64B(stage, lane, dgu_rows, (int64_t)ld_gu * 2, warp_live);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              stage_piece(stage, lane, q, make_uint4(pdu[4 * q], pdu[4 * q + 1], pdu[4 * q + 2], pdu[4 * q + 3]));
+            flush_rows_64B(stage, lane, dgu_rows + 256, (int64_t)ld_gu * 2, warp_live);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              stage_piece(stage, lane, q, make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]));
+            flush_rows_64B(stage, lane, reinterpret_cast<uint8_t*>(p.h_out) + (warp_row0 * p.F + f0) * 2,
+                           (int64_t)p.F * 2, warp_live);
+          }
+        }
+      }
+      if (!empty_tile) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+bool make_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, box_rows, 64);
+}
+
+template <int MODE>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0x,
+                   const CUtensorMap& b1x, const BwdParams& p, int64_t max_tiles, cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  auto kern = tc_gemm_bwd_kernel<MODE>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, b0x, b1x, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mlp_backward_supported(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && c.xfer_dtype == MOE_DTYPE_BF16 && c.H % 256 == 0 && c.F % 256 == 0 &&
+         c.E + 1 <= kMaxGroups;
+}
+
+cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, const void* x,
+                                        const int32_t* offsets, const moe_weights_t& w, const void* dyd, void* gu,
+                                        void* dgu, void* h, void* dxd, const moe_weight_grads_t& gr,
+                                        DeviceStatus* st, cudaStream_t s) {
+  const int64_t R = routed_rows(c), rows = total_rows(c);
+  const bool shared = c.n_shared != 0;
+  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  // ---- recompute g and u (the forward GEMM1 without its activation)
+  cudaError_t e = launch_gate_up_preact(c, xd, x, offsets, w, gu, st, s);
+  if (e != cudaSuccess) return e;
+  BwdParams p{};
+  p.offsets = offsets;
+  p.G = c.E;
+  p.has_extra = shared ? 1 : 0;
+  p.T_extra = c.T;
+  p.a2_row_base = (int)R;
+  p.F = c.F;
+  p.status = st;
+  p.timeout_ns = kTimeoutNs;
+  // ---- dh = dyd Wd, then dg, du, h (B = Wd [E*H rows, F cols] read MN-major)
+  CUtensorMap a, b0, b1, b0x, b1x;
+  bool ok = make_bf16_box(&a, dyd, rows, c.H, BM) && make_bf16_box(&b0, w.w_down, (uint64_t)c.E * c.H, c.F, 64);
+  if (shared) ok = ok && make_bf16_box(&b0x, w.ws_down, c.H, c.F, 64);
+  else b0x = b0;
+  if (!ok) return cudaErrorInvalidValue;
+  p.K = c.H;
+  p.n_tiles = c.F / BN;
+  p.b_group_rows = c.H;
+  p.ldc = 2 * c.F;
+  p.out = static_cast<__nv_bfloat16*>(dgu);
+  p.h_out = static_cast<__nv_bfloat16*>(h);
+  p.gu = static_cast<const __nv_bfloat16*>(gu);
+  e = launch<DGRAD_DOWN>(a, b0, b0, b0x, b0x, p, mt_bound * p.n_tiles, s);
+  if (e != cudaSuccess) return e;
+  // ---- dxd = dg Wg + du Wu (K = 2F in dgu's interleaved order; B = Wg or Wu rows)
+  ok = make_bf16_box(&a, dgu, rows, 2 * (uint64_t)c.F, BM) && make_bf16_box(&b0, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
+       make_bf16_box(&b1, w.w_up, (uint64_t)c.E * c.F, c.H, 64);
+  if (shared) ok = ok && make_bf16_box(&b0x, w.ws_gate, c.F, c.H, 64) && make_bf16_box(&b1x, w.ws_up, c.F, c.H, 64);
+  else { b0x = b0; b1x = b1; }
+  if (!ok) return cudaErrorInvalidValue;
+  p.K = 2 * c.F;
+  p.n_tiles = c.H / BN;
+  p.b_group_rows = c.F;
+  p.ldc = c.H;
+  p.out = static_cast<__nv_bfloat16*>(dxd);
+  e = launch<DGRAD_GU>(a, b0, b1, b0x, b1x, p, mt_bound * p.n_tiles, s);
+  if (e != cudaSuccess) return e;
+  // ---- dWd[e] = dyd_e^T h_e (M_out = H, N_out = F; both operands MN-major)
+  const int ngroups = c.E + (shared ? 1 : 0);
+  ok = make_bf16_box(&a, dyd, rows, c.H, 64) && make_bf16_box(&b0, h, rows, c.F, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  p.extra_b_row0 = (int)R;  // h holds the shared expert's rows after the routed ones
+  p.M_out = c.H;
+  p.N_out = c.F;
+  p.m_tiles_out = c.H / BM;
+  p.n_tiles = c.F / BN;
+  p.w0 = gr.dw_down;
+  p.w0x = gr.dws_down;
+  p.w1 = p.w1x = nullptr;
+  e = launch<WGRAD_DOWN>(a, b0, b0, b0, b0, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
+  if (e != cudaSuccess) return e;
+  // ---- dWg[e], dWu[e] = dgu_e^T xd_e (M_out = 2F interleaved, N_out = H)
+  ok = make_bf16_box(&a, dgu, rows, 2 * (uint64_t)c.F, 64) && make_bf16_box(&b0, xd, rows, c.H, 64);
+  if (shared) ok = ok && make_bf16_box(&b0x, x, c.T, c.H, 64);  // the shared expert's input is x
+  else b0x = b0;
+  if (!ok) return cudaErrorInvalidValue;
+  p.extra_b_row0 = 0;
+  p.M_out = 2 * c.F;
+  p.N_out = c.H;
+  p.m_tiles_out = 2 * c.F / BM;
+  p.n_tiles = c.H / BN;
+  p.w0 = gr.dw_gate;
+  p.w1 = gr.dw_up;
+  p.w0x = gr.dws_gate;
+  p.w1x = gr.dws_up;
+  return launch<WGRAD_GU>(a, b0, b0, b0x, b0x, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
+}
+
+}  // namespace tc
+}  // namespace moe

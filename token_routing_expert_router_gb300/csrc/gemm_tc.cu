@@ -28,7 +28,9 @@ constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group + 1
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
-enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2 };
+// EPI_STORE_GU: the gate/up GEMM (B = gate and up rows, as for SwiGLU) storing g and u
+// themselves, for the backward's recomputation of the activation.
+enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2, EPI_STORE_GU = 3 };
 
 struct TcParams {
   const int32_t* offsets;   // [G+1] routed segment starts (device); may be null when G = 0
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (EPI == EPI_SWIGLU_BF16) tma_prefetch_desc(&tmB1);
+    if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU) tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, S::kTmemCols);
   if (warp == 2) {
@@ -189,10 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
       const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
       const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
-      const int b_tile_rows = EPI == EPI_SWIGLU_BF16 ? BN / 2 : BN;  // rows of B per N tile
+      constexpr bool kGatedB = EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU;  // B = gate + up rows
+      const int b_tile_rows = kGatedB ? BN / 2 : BN;  // rows of B per N tile
       int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-      if (CG == 2 && EPI != EPI_SWIGLU_BF16) b_row += (int)rank * (BN / 2);
-      const CUtensorMap* tb_mine = (CG == 2 && EPI == EPI_SWIGLU_BF16 && rank == 1) ? tb1 : tb0;
+      if (CG == 2 && !kGatedB) b_row += (int)rank * (BN / 2);
+      const CUtensorMap* tb_mine = (CG == 2 && kGatedB && rank == 1) ? tb1 : tb0;
       int tok[4] = {0, 0, 0, 0};
       if (gather) {  // tokens of this lane's rows; rows past the segment repeat its last row
         const int seg_end = p.offsets[c.g + 1];
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
           }
           if (lane == 0) {
-            if (EPI == EPI_SWIGLU_BF16) {
+            if (kGatedB) {
               tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);                    // gate rows
               tma_load_2d(tb1, b_dst + (BN / 2) * BK * 2, &full[stage], kb * BK, b_row);  // up rows
             } else {
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage_piece(stage, lane, v, make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
           flush_rows_64B(stage, lane, out + 2 * c0, (int64_t)p.ldc * 2, warp_live);
         }
-      } else if (EPI == EPI_STORE_BF16) {
+      } else if (EPI == EPI_STORE_BF16 || EPI == EPI_STORE_GU) {
         uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -590,6 +593,42 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   if (pair) return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
   if (bn2 == 256) return launch<256, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
   return launch<128, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+}
+
+cudaError_t launch_gate_up_preact(const moe_config_t& c, const void* xd, const void* x, const int32_t* offsets,
+                                  const moe_weights_t& w, void* gu, DeviceStatus* st, cudaStream_t s) {
+  const int64_t R = routed_rows(c), rows = total_rows(c);
+  const bool shared = c.n_shared != 0;
+  // the operands, tiles and CTA-pair choice of the forward's GEMM1 (the shared expert's A = x)
+  CUtensorMap a1, a1x, bg, bu, bgx, bux;
+  bool ok = make_bf16(&a1, xd, rows, c.H, BM) && make_bf16(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
+            make_bf16(&bu, w.w_up, (uint64_t)c.E * c.F, c.H, 128);
+  if (shared) {
+    ok = ok && make_bf16(&a1x, x, c.T, c.H, BM) && make_bf16(&bgx, w.ws_gate, c.F, c.H, 128) &&
+         make_bf16(&bux, w.ws_up, c.F, c.H, 128);
+  } else {
+    a1x = a1; bgx = bg; bux = bu;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.offsets = offsets;
+  p.G = c.E;
+  p.has_extra = shared ? 1 : 0;
+  p.T_extra = c.T;
+  p.a2_row_base = 0;
+  p.out_extra_base = R;
+  p.K = c.H;
+  p.n_tiles = c.F / 128;
+  p.b_group_rows = c.F;
+  p.ldc = 2 * c.F;
+  p.out = gu;
+  p.status = st;
+  p.timeout_ns = kTimeoutNs;
+  const bool pair = (int64_t)c.T * c.k >= 512LL * c.E && c.H % 256 == 0;
+  const int tm = pair ? 2 * BM : BM;
+  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
+  return pair ? launch<256, EPI_STORE_GU, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+              : launch<256, EPI_STORE_GU, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc

@@ -20,6 +20,17 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
                                cudaStream_t s, const int32_t* row_token = nullptr);
 
+// Backward of the grouped expert MLP (bf16). gu [R(+T), 2F] (g and u in 128-column blocks,
+// as the gate/up GEMM's tiles hold them), dgu the same layout, h [R(+T), F]: workspace.
+// launch_gate_up_preact is the forward's gate/up GEMM storing g and u (no activation).
+bool mlp_backward_supported(const moe_config_t& c);
+cudaError_t launch_gate_up_preact(const moe_config_t& c, const void* xd, const void* x, const int32_t* offsets,
+                                  const moe_weights_t& w, void* gu, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, const void* x,
+                                        const int32_t* offsets, const moe_weights_t& w, const void* dyd, void* gu,
+                                        void* dgu, void* h, void* dxd, const moe_weight_grads_t& gr,
+                                        DeviceStatus* st, cudaStream_t s);
+
 // MXFP8 (e4m3, UE8M0 scale atoms) variant on the block-scaled MMA.
 bool mx_supported(const moe_config_t& c);
 cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const void* xd_sf,

@@ -52,6 +52,10 @@ cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t*
                            const float* topk_w, void* y, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* src, int64_t rows, int64_t cols, int br, int bc,
                                  uint8_t* q, float* scale, cudaStream_t s);
+// Backward of combine (bf16 layers): dyd = w * dy (+ shared rows = dy), dtopk_w = <dy, yd>.
+// Dispatch backward is launch_combine with topk_w = nullptr (unit weights).
+cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy, const void* yd, const int32_t* tok_row,
+                                    const float* topk_w, void* dyd, float* dtopk_w, cudaStream_t s);
 // MXFP8 variant (scale atoms as described in mx_common.cuh).
 cudaError_t launch_dispatch_mx(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                                const int32_t* tok_row, const int32_t* offsets, void* xd, void* xd_sf,

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const void* __restric
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
-    wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = topk_w ? topk_w[(int64_t)t * k + threadIdx.x] : 1.0f;
   }
   __syncthreads();
   const int n8 = H / 8;
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __rest
   if (threadIdx.x < NR) {
     const int j = threadIdx.x;
     rows[j] = j < k ? (int64_t)tok_row[(int64_t)t * k + j] : R + t;
-    wts[j] = j < k ? topk_w[(int64_t)t * k + j] : 1.0f;
+    wts[j] = (j < k && topk_w) ? topk_w[(int64_t)t * k + j] : 1.0f;
   }
   __syncthreads();
   const int n8 = H / 8;
@@ -328,6 +328,60 @@ __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __rest
       p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
+  }
+}
+
+// Combine backward, one block per token: dy[t] is read once per row it feeds;
+// dyd[tok_row[t,j]] = bf16(w[t,j] * dy[t]), dyd[R+t] = dy[t] (shared expert), and
+// dtopk_w[t,j] = sum_o dy[t,o] * yd[tok_row[t,j], o] in fp32 (block reduction).
+__global__ void __launch_bounds__(kThreads) combine_backward_kernel(
+    const uint4* __restrict__ dy, const uint4* __restrict__ yd, int H, int k, const int32_t* __restrict__ tok_row,
+    const float* __restrict__ topk_w, int shared, int64_t R, uint4* __restrict__ dyd, float* __restrict__ dtopk_w) {
+  __shared__ int64_t rows[32];
+  __shared__ float wts[32];
+  __shared__ float red[32][kThreads / 32];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
+    wts[threadIdx.x] = topk_w[(int64_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int n8 = H / 8;
+  const uint4* g = dy + (int64_t)t * n8;
+  for (int j = 0; j < k; ++j) {
+    const float wj = wts[j];
+    const uint4* src = yd + rows[j] * n8;
+    uint4* dst = dyd + rows[j] * n8;
+    float dot = 0.0f;
+    for (int c = threadIdx.x; c < n8; c += kThreads) {
+      const uint4 a = __ldg(g + c), b = __ldg(src + c);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a0 = bf16_lo(av[q]), a1 = bf16_hi(av[q]);
+        dot = __fmaf_rn(a0, bf16_lo(bv[q]), dot);
+        dot = __fmaf_rn(a1, bf16_hi(bv[q]), dot);
+        const __nv_bfloat162 p = __floats2bfloat162_rn(wj * a0, wj * a1);
+        o[q] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) red[j][warp] = dot;
+  }
+  if (shared) {
+    uint4* dst = dyd + (R + t) * n8;
+    for (int c = threadIdx.x; c < n8; c += kThreads) dst[c] = __ldg(g + c);
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) s += red[threadIdx.x][w];
+    dtopk_w[(int64_t)t * k + threadIdx.x] = s;
   }
 }
 
@@ -430,6 +484,15 @@ cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint
   if (nblk == 0) return cudaSuccess;
   quantize_mx_kernel<<<(unsigned)ceil_div(nblk, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), rows, cols,
                                                                     q, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy, const void* yd, const int32_t* tok_row,
+                                    const float* topk_w, void* dyd, float* dtopk_w, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  combine_backward_kernel<<<c.T, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(dy), reinterpret_cast<const uint4*>(yd),
+                                                   c.H, c.k, tok_row, topk_w, c.n_shared ? 1 : 0, routed_rows(c),
+                                                   reinterpret_cast<uint4*>(dyd), dtopk_w);
   return cudaGetLastError();
 }
 
