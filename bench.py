@@ -317,6 +317,11 @@ def run_gpu(args, w):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
 
+    # ---- backward (training step) of the same layer: bf16 layers
+    bwd = None
+    if not args.no_backward and w["act_dtype"] == synth.BF16 and not fp8:
+        bwd = time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt)
+
     if rank != 0:
         dist.destroy_process_group()
         return None
@@ -360,6 +365,7 @@ def run_gpu(args, w):
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
         "gpu_launches": args.steps * launches_per_forward(w),
+        **({"backward": bwd} if bwd is not None else {}),
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
@@ -368,6 +374,63 @@ def run_gpu(args, w):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
+    """moe_backward after the forward whose workspace is ws, and its three staged calls
+    (combine backward, grouped MLP backward, dispatch backward), L2 flushed before each."""
+    import torch
+    import token_routing_expert_router_gb300 as moe
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    rows = T * k + (T if w["n_shared"] else 0)
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device=dev)
+    moe.moe_workspace_init(bws)
+    dy = gen((T, H), synth.DY, 1.0)
+    dx = torch.empty((T, H), dtype=dt, device=dev)
+    dtw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    grads = {"dw_gate": torch.empty((E, F, H), dtype=torch.float32, device=dev),
+             "dw_up": torch.empty((E, F, H), dtype=torch.float32, device=dev),
+             "dw_down": torch.empty((E, H, F), dtype=torch.float32, device=dev)}
+    if w["n_shared"]:
+        Fs = w["F_shared"]
+        grads.update(dws_gate=torch.empty((Fs, H), dtype=torch.float32, device=dev),
+                     dws_up=torch.empty((Fs, H), dtype=torch.float32, device=dev),
+                     dws_down=torch.empty((H, Fs), dtype=torch.float32, device=dev))
+    dyd = torch.empty((rows, H), dtype=dt, device=dev)
+    dxd = torch.empty((rows, H), dtype=dt, device=dev)
+    moe.moe_forward(cfg, x, wts, torch.empty((T, H), dtype=dt, device=dev), ws)
+    stages = {
+        "backward": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
+        "combine_backward": lambda: moe.moe_combine_backward(cfg, dy, b["yd"], b["tok_row"], b["w"], dyd, dtw),
+        "grouped_mlp_backward": lambda: moe.moe_grouped_mlp_backward(cfg, b["xd"], x, b["offsets"], wts, dyd, dxd,
+                                                                     grads, bws),
+        "dispatch_backward": lambda: moe.moe_dispatch_backward(cfg, dxd, b["tok_row"], dx),
+    }
+    for f in stages.values():
+        f()
+    reps = max(3, min(args.steps, 5))
+    times = {n: [] for n in stages}
+    for _ in range(reps):
+        for n, f in stages.items():
+            flush.fill_(2.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            times[n].append((e0, e1))
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(bws) == moe.MOE_OK
+    ms = {n: statistics.median(a.elapsed_time(bb) for a, bb in v) for n, v in times.items()}
+    flops = 2.0 * synth.gemm_flops(w)  # dgrad + wgrad, each the forward GEMMs' flops
+    recompute = synth.gemm_flops(w) * 2.0 / 3.0  # the gate/up GEMM run again
+    peak = load_peaks()[0].get("bf16_tflops_sustained", load_peaks()[0]["bf16_tflops"])
+    tf = flops / (ms["grouped_mlp_backward"] / 1e3) / 1e12
+    return {"metric": "MoE-layer bwd tokens/s", "value": round(T / (ms["backward"] / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms["backward"], 4), "stages_ms": {n: round(v, 4) for n, v in ms.items() if n != "backward"},
+            "grouped_gemm_tflops": round(tf, 1), "grouped_gemm_frac_of_peak": round(tf / peak, 3),
+            "algorithmic_flops": flops, "recompute_flops": recompute,
+            "note": "dgrad + wgrad flops over the grouped MLP backward time (the gate/up recompute is extra work "
+                    "in that time); weight gradients fp32; L2 flushed before each call"}
 
 
 def launches_per_forward(w):
@@ -468,6 +531,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct moe_forward calls")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (bf16 layers)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     args = ap.parse_args()

@@ -35,6 +35,7 @@ TWO_PI = 6.283185307179586  # fp64 nearest to 2*pi; the device twin uses the sam
 # Tensor ids: one independent stream per named tensor.
 X, W_ROUTER, W_GATE, W_UP, W_DOWN, WS_GATE, WS_UP, WS_DOWN = 1, 2, 3, 4, 5, 6, 7, 8
 LOGITS, ZIPF, TOPK_W, YD, ROUTER_BIAS = 9, 10, 11, 12, 13
+DY = 14  # output gradient of the backward
 
 _CHUNK = 1 << 22
 
