@@ -108,7 +108,8 @@ FwdLayout fwd_layout(const moe_config_t& c) {
   return L;
 }
 
-// Backward workspace: status head, then dyd, dxd [rows, H], gu, dgu [rows, 2F], h [rows, F].
+// Backward workspace: status head, then dyd, dxd [rows, H], gu [rows, 2F], dgu [prows, 2F],
+// h [prows, F] (prows: every expert's rows padded to a multiple of 64).
 struct BwdLayout {
   size_t dyd, dxd, gu, dgu, h, total;
 };
@@ -122,11 +123,12 @@ BwdLayout bwd_layout(const moe_config_t& c) {
     return at;
   };
   const size_t rows = (size_t)total_rows(c);
+  const size_t prows = (size_t)tc::backward_padded_rows(c);  // dgu and h: 64-row padded segments
   L.dyd = take(rows * c.H * 2);
   L.dxd = take(rows * c.H * 2);
   L.gu = take(rows * 2 * c.F * 2);
-  L.dgu = take(rows * 2 * c.F * 2);
-  L.h = take(rows * c.F * 2);
+  L.dgu = take(prows * 2 * c.F * 2);
+  L.h = take(prows * c.F * 2);
   L.total = o;
   return L;
 }

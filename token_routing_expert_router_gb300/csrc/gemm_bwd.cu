@@ -17,13 +17,21 @@
 // the 64-element MN blocks (8 KB here), SBO = 1024 B between 8-row K groups, and each MMA
 // of K = 16 advances the start by 16 rows (2 KB). Instruction-descriptor bits 15 / 16 mark
 // A / B as MN-major.
-// Wgrad reduces over an expert's rows: the last K stage of a segment holds rows of the next
-// expert past the segment's end, so the MMA warp zeroes those rows of B in shared memory
-// (whole 128-byte lines, which the swizzle keeps intact) before the MMAs; an expert without
-// rows gets an all-zero gradient from the epilogue without touching the tensor core.
+// Wgrad reduces over an expert's rows in K stages of 64, and the last stage of a segment
+// reaches past its end. dgu and h, which the backward writes itself, are therefore laid out
+// with every expert's rows padded to a multiple of 64 by zero rows: expert g (the shared
+// expert is g = E at offset T*k) starts at padded row P(g) = 64 * ceil((offsets[g] + 63 g) /
+// 64), which needs no prefix sum and never overlaps the next expert. Each wgrad pairs one
+// padded operand (dgu, or h) with an unpadded one (xd, or dyd): past the segment's end the
+// padded operand's rows are zero, so the other's rows (the next expert's, or the TMA's
+// zero fill past the end of the map) add nothing. An expert without rows gets an all-zero
+// gradient from the epilogue without touching the tensor core.
 //
-// Block (as the forward bf16 kernel): warp 0 TMA producer, warp 1 MMA issuer (TMEM owner),
-// warps 2-5 epilogue (one output row per thread, two TMEM accumulators of 256 columns).
+// Block: warp 0 TMA producer, warp 1 MMA issuer (TMEM owner), warps 2-9 epilogue (one
+// output row per thread, two warps per TMEM lane quarter each owning 128 of the tile's 256
+// columns; two TMEM accumulators of 256 columns). Weight-gradient tiles are short (K = one
+// expert's rows) and write 128 KB of fp32 each, so the epilogue must keep pace with a few
+// microseconds of MMAs: eight warps, and TMEM loads issued one chunk ahead.
 // Tile 128 x 256, K stages of 64 (128 bytes), 4 stages of 48 KB.
 #include <cudaTypedefs.h>
 
@@ -40,7 +48,8 @@ int num_sms();
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;  // BK in bf16 elements (128 bytes)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB: four MN boxes of 8 KB
@@ -48,7 +57,8 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kMaxGroups = 514;
 constexpr int kTmemCols = 2 * BN;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + 4 * 2048;
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + kEpiWarps * 2048;
 
 enum Mode { DGRAD_DOWN = 0, DGRAD_GU = 1, WGRAD_DOWN = 2, WGRAD_GU = 3 };
 
@@ -77,6 +87,11 @@ struct BwdParams {
 struct TileCoord {
   int g, mb, nb, rows;  // dgrad: m tile mb of group g (rows valid); wgrad: out tile (mb, nb), rows = K rows
 };
+
+// First padded row of group g (offset = its first row in the unpadded buffers).
+__host__ __device__ __forceinline__ int64_t padded_row0(int64_t offset, int g) {
+  return (offset + 63 * (int64_t)g + 63) / 64 * 64;
+}
 
 __device__ __forceinline__ TileCoord decode_dgrad(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
                                                   const int32_t* seg_rows) {
@@ -149,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* mt_prefix = reinterpret_cast<int32_t*>(bars + 32);
   int32_t* seg_rows = mt_prefix + kMaxGroups;
-  uint8_t* sEpi = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups);  // [4 warps][32 rows][64 B]
+  uint8_t* sEpi = reinterpret_cast<uint8_t*>(seg_rows + kMaxGroups);  // [8 warps][32 rows][64 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -224,17 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_dst = sB + stage * kBBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           if constexpr (kWgrad) {
-            // A: activation [rows, M_out] MN-major (2 boxes); B: activation [rows, N_out] (4 boxes)
-            const int y = row0 + kb * BK;
+            // A: activation [rows, M_out] MN-major (2 boxes); B: activation [rows, N_out] (4
+            // boxes). WGRAD_GU: A = dgu (padded rows), B = xd or x; WGRAD_DOWN: A = dyd, B = h
+            // (padded rows).
+            const int y_pad = (int)padded_row0(row0, c.g) + kb * BK;
+            const int y = (MODE == WGRAD_GU ? y_pad : row0 + kb * BK);
             tma_load_2d(&tmA, a_dst, &full[stage], c.mb * BM, y);
             tma_load_2d(&tmA, a_dst + 8192, &full[stage], c.mb * BM + 64, y);
             const CUtensorMap* tb = extra ? &tmB0x : &tmB0;
-            const int yb = extra ? p.extra_b_row0 + kb * BK : y;
+            const int yb = MODE == WGRAD_DOWN ? y_pad : (extra ? p.extra_b_row0 + kb * BK : row0 + kb * BK);
 #pragma unroll
             for (int j = 0; j < 4; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], c.nb * BN + 64 * j, yb);
           } else {
-            // A: [rows, K] K-major, 128 rows; B: weight rows = the K index, MN-major (4 boxes)
-            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, row0 + c.mb * BM);
+            // A: [rows, K] K-major, 128 rows (dgu: padded rows); B: weight rows = the K index,
+            // MN-major (4 boxes)
+            const int a_row0 = MODE == DGRAD_GU ? (int)padded_row0(row0, c.g) : row0;
+            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row0 + c.mb * BM);
             const CUtensorMap* tb;
             int brow;
             if (MODE == DGRAD_DOWN) {
@@ -262,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer (lane 0), with the warp zeroing wgrad tails
+    // ======================= MMA issuer (lane 0 of the warp)
     constexpr uint32_t idesc = idesc_bwd(kWgrad);
     int stage = 0;
     uint32_t phase = 0;
@@ -283,19 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         uint8_t* b_st = sB + stage * kBBytes;
-        if (kWgrad) {
-          const int valid = c.rows - kb * BK;
-          if (valid < BK) {  // rows past the segment's end contribute nothing
-            const int lines = BK - valid;
-            for (int i = lane; i < 4 * lines * 8; i += 32) {
-              const int box = i / (lines * 8), rem = i - box * lines * 8;
-              const int line = valid + rem / 8, chunk = rem & 7;
-              *reinterpret_cast<uint4*>(b_st + box * 8192 + line * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          }
-          __syncwarp();
-        }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t a_addr = smem_addr(sA + stage * kABytes);
@@ -320,8 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= epilogue (warps 2..5; TMEM lane quarter = warp % 4)
+    // ======================= epilogue (warps 2..9; TMEM lane quarter = warp % 4)
     const int quarter = warp & 3;
+    const int cbase = ((warp - 2) >> 2) * (BN / 2);  // this warp's 128 of the tile's 256 columns
     const int r = quarter * 32 + lane;
     uint8_t* stage = sEpi + (warp - 2) * 2048;
     int acc = 0;
@@ -351,13 +359,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : (extra ? p.w0x : p.w0 + (int64_t)c.g * p.F * p.N_out);
           wbase = w + (int64_t)(c.mb >> 1) * BM * ldo;
         }
-        uint8_t* out = reinterpret_cast<uint8_t*>(wbase + (int64_t)quarter * 32 * ldo + c.nb * BN);
+        uint8_t* out = reinterpret_cast<uint8_t*>(wbase + (int64_t)quarter * 32 * ldo + c.nb * BN + cbase);
+        uint32_t nxt[32];
+        if (!empty_tile) tmem_ld32(t_row + cbase, nxt);
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
           uint32_t v[32];
           if (!empty_tile) {
-            tmem_ld32(t_row + c0, v);
             tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = nxt[i];
+            if (c0 + 32 < BN / 2) tmem_ld32(t_row + cbase + c0 + 32, nxt);  // next chunk in flight
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
@@ -377,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int warp_live = c.rows - quarter * 32;
         const bool live = r < c.rows;
         if (MODE == DGRAD_GU) {
-          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
+          uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN + cbase) * 2;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = 0; c0 < BN / 2; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(t_row + c0, v);
+            tmem_ld32(t_row + cbase + c0, v);
             tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -395,8 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {  // DGRAD_DOWN: dh -> SwiGLU backward with g, u from gu; writes dg, du and h
           const int64_t row = warp_row0 + lane;
           const int ld_gu = 2 * p.F;
+          // dgu and h rows are padded: this warp's rows start at prow0, and the rows past the
+          // segment up to its multiple of 64 are written as zeros (g = u = 0 there)
+          const int64_t prow0 = padded_row0(row0, c.g) + c.mb * BM + quarter * 32;
+          const int seg = c.g < p.G ? p.offsets[c.g + 1] - p.offsets[c.g] : p.T_extra;
+          const int pad_live = min((seg + 63) / 64 * 64 - c.mb * BM, BM) - quarter * 32;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = cbase; c0 < cbase + BN / 2; c0 += 32) {
             const int f0 = c.nb * BN + c0;     // first F column of the chunk
             const int blk = f0 >> 7, cb = f0 & 127;
             uint32_t dh[32];
@@ -439,20 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ph[4 * q + e] = pack_bf16(hv[0], hv[1]);
               }
             }
-            uint8_t* dgu_rows = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * ld_gu + blk * 256 + cb) * 2;
+            uint8_t* dgu_rows = reinterpret_cast<uint8_t*>(p.out) + (prow0 * ld_gu + blk * 256 + cb) * 2;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               stage_piece(stage, lane, q, make_uint4(pdg[4 * q], pdg[4 * q + 1], pdg[4 * q + 2], pdg[4 * q + 3]));
-            flush_rows_64B(stage, lane, dgu_rows, (int64_t)ld_gu * 2, warp_live);
+            flush_rows_64B(stage, lane, dgu_rows, (int64_t)ld_gu * 2, pad_live);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               stage_piece(stage, lane, q, make_uint4(pdu[4 * q], pdu[4 * q + 1], pdu[4 * q + 2], pdu[4 * q + 3]));
-            flush_rows_64B(stage, lane, dgu_rows + 256, (int64_t)ld_gu * 2, warp_live);
+            flush_rows_64B(stage, lane, dgu_rows + 256, (int64_t)ld_gu * 2, pad_live);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               stage_piece(stage, lane, q, make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]));
-            flush_rows_64B(stage, lane, reinterpret_cast<uint8_t*>(p.h_out) + (warp_row0 * p.F + f0) * 2,
-                           (int64_t)p.F * 2, warp_live);
+            flush_rows_64B(stage, lane, reinterpret_cast<uint8_t*>(p.h_out) + (prow0 * p.F + f0) * 2,
+                           (int64_t)p.F * 2, pad_live);
           }
         }
       }
@@ -496,6 +513,10 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 
 }  // namespace
 
+int64_t backward_padded_rows(const moe_config_t& c) {
+  return total_rows(c) + 63 * ((int64_t)c.E + 1) + 64;
+}
+
 bool mlp_backward_supported(const moe_config_t& c) {
   return c.act_dtype == MOE_DTYPE_BF16 && c.xfer_dtype == MOE_DTYPE_BF16 && c.H % 256 == 0 && c.F % 256 == 0 &&
          c.E + 1 <= kMaxGroups;
@@ -507,6 +528,7 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
                                         DeviceStatus* st, cudaStream_t s) {
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
+  const int64_t prows = backward_padded_rows(c);  // rows of the padded dgu and h
   const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
   // ---- recompute g and u (the forward GEMM1 without its activation)
   cudaError_t e = launch_gate_up_preact(c, xd, x, offsets, w, gu, st, s);
@@ -536,7 +558,7 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   e = launch<DGRAD_DOWN>(a, b0, b0, b0x, b0x, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- dxd = dg Wg + du Wu (K = 2F in dgu's interleaved order; B = Wg or Wu rows)
-  ok = make_bf16_box(&a, dgu, rows, 2 * (uint64_t)c.F, BM) && make_bf16_box(&b0, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
+  ok = make_bf16_box(&a, dgu, prows, 2 * (uint64_t)c.F, BM) && make_bf16_box(&b0, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
        make_bf16_box(&b1, w.w_up, (uint64_t)c.E * c.F, c.H, 64);
   if (shared) ok = ok && make_bf16_box(&b0x, w.ws_gate, c.F, c.H, 64) && make_bf16_box(&b1x, w.ws_up, c.F, c.H, 64);
   else { b0x = b0; b1x = b1; }
@@ -550,9 +572,9 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   if (e != cudaSuccess) return e;
   // ---- dWd[e] = dyd_e^T h_e (M_out = H, N_out = F; both operands MN-major)
   const int ngroups = c.E + (shared ? 1 : 0);
-  ok = make_bf16_box(&a, dyd, rows, c.H, 64) && make_bf16_box(&b0, h, rows, c.F, 64);
+  ok = make_bf16_box(&a, dyd, rows, c.H, 64) && make_bf16_box(&b0, h, prows, c.F, 64);
   if (!ok) return cudaErrorInvalidValue;
-  p.extra_b_row0 = (int)R;  // h holds the shared expert's rows after the routed ones
+  p.extra_b_row0 = 0;  // unused: h's rows are addressed by their padded position
   p.M_out = c.H;
   p.N_out = c.F;
   p.m_tiles_out = c.H / BM;
@@ -563,7 +585,9 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   e = launch<WGRAD_DOWN>(a, b0, b0, b0, b0, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- dWg[e], dWu[e] = dgu_e^T xd_e (M_out = 2F interleaved, N_out = H)
-  ok = make_bf16_box(&a, dgu, rows, 2 * (uint64_t)c.F, 64) && make_bf16_box(&b0, xd, rows, c.H, 64);
+  // xd's map ends at the last routed row: the TMA fills zeros past it, never reading rows
+  // the dispatch did not write
+  ok = make_bf16_box(&a, dgu, prows, 2 * (uint64_t)c.F, 64) && make_bf16_box(&b0, xd, R, c.H, 64);
   if (shared) ok = ok && make_bf16_box(&b0x, x, c.T, c.H, 64);  // the shared expert's input is x
   else b0x = b0;
   if (!ok) return cudaErrorInvalidValue;

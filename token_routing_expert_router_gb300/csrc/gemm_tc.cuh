@@ -21,9 +21,12 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                cudaStream_t s, const int32_t* row_token = nullptr);
 
 // Backward of the grouped expert MLP (bf16). gu [R(+T), 2F] (g and u in 128-column blocks,
-// as the gate/up GEMM's tiles hold them), dgu the same layout, h [R(+T), F]: workspace.
+// as the gate/up GEMM's tiles hold them); dgu the same columns and h [., F] with each
+// expert's rows padded to a multiple of 64 (backward_padded_rows rows): workspace.
 // launch_gate_up_preact is the forward's gate/up GEMM storing g and u (no activation).
 bool mlp_backward_supported(const moe_config_t& c);
+// Rows of the padded dgu and h buffers (every expert's rows padded to a multiple of 64).
+int64_t backward_padded_rows(const moe_config_t& c);
 cudaError_t launch_gate_up_preact(const moe_config_t& c, const void* xd, const void* x, const int32_t* offsets,
                                   const moe_weights_t& w, void* gu, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, const void* x,
