@@ -30,9 +30,10 @@
 // Block: warp 0 TMA producer, warp 1 MMA issuer (TMEM owner), warps 2-9 epilogue (one
 // output row per thread, two warps per TMEM lane quarter each owning 128 of the tile's 256
 // columns; two TMEM accumulators of 256 columns). Weight-gradient tiles are short (K = one
-// expert's rows) and write 128 KB of fp32 each, so the epilogue must keep pace with a few
-// microseconds of MMAs: eight warps, and TMEM loads issued one chunk ahead.
-// Tile 128 x 256, K stages of 64 (128 bytes), 4 stages of 48 KB.
+// expert's rows) and write 128 KB of fp32 per CTA each, so the epilogue must keep pace with
+// a few microseconds of MMAs: eight warps, and TMEM loads issued one chunk ahead.
+// Tiles of 128 x 256 (one CTA) or 256 x 256 (a CTA pair, M = 256 pair MMAs, each CTA
+// holding half of B: 6 stages of 32 KB instead of 4 of 48 KB), K stages of 64 (128 bytes).
 #include <cudaTypedefs.h>
 
 #include "gemm_tc.cuh"
@@ -50,15 +51,21 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;  // BK in bf16 elements (128 bytes)
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB: four MN boxes of 8 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = BM * BK * 2;  // 16 KB: this CTA's 128 rows of A
 constexpr int kMaxGroups = 514;
 constexpr int kTmemCols = 2 * BN;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + kEpiWarps * 2048;
+
+// Shared memory of one CTA. A CTA pair (CG = 2) holds half of B's 256 columns per CTA, so a
+// stage is 32 KB and six stages fit instead of four.
+template <int CG>
+struct BwdSmem {
+  static constexpr int kBBytes = (BN / CG) * BK * 2;  // (BN / CG) / 64 MN boxes of 8 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = CG == 2 ? 6 : 4;
+  static constexpr size_t kBytes =
+      1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + kEpiWarps * 2048;
+};
 
 enum Mode { DGRAD_DOWN = 0, DGRAD_GU = 1, WGRAD_DOWN = 2, WGRAD_GU = 3 };
 
@@ -67,19 +74,19 @@ struct BwdParams {
   int G, has_extra, T_extra, a2_row_base;  // the shared expert's rows: [a2_row_base, + T_extra)
   int K;             // dgrad: the contraction length (H or 2F)
   int n_tiles;       // 256-wide N tiles (dgrad: N/256; wgrad: N_out/256)
-  int m_tiles_out;   // wgrad: M_out/128
+  int m_tiles_out;   // wgrad: M_out / (128 * CG)
   int b_group_rows;  // dgrad: rows of B per routed group in its map (H for Wd, F for Wg/Wu)
   int F;
   int ldc;                    // dgrad output row length (elements)
-  __nv_bfloat16* out;         // DGRAD_DOWN: dgu [rows, 2F]; DGRAD_GU: dxd [rows, H]
-  __nv_bfloat16* h_out;       // DGRAD_DOWN: h [rows, F]
+  __nv_bfloat16* out;         // DGRAD_DOWN: dgu [prows, 2F]; DGRAD_GU: dxd [rows, H]
+  __nv_bfloat16* h_out;       // DGRAD_DOWN: h [prows, F]
   const __nv_bfloat16* gu;    // DGRAD_DOWN: g and u [rows, 2F], interleaved in 128-column blocks
   float* w0;                  // WGRAD_DOWN: dWd [G, M_out, N_out]; WGRAD_GU: dWg [G, F, H]
   float* w1;                  // WGRAD_GU: dWu [G, F, H]
   float* w0x;                 // the shared expert's (same layouts without the G dimension)
   float* w1x;
   int M_out, N_out;
-  int extra_b_row0;           // wgrad: the shared expert's first row in its B map (tmB0x)
+  int extra_b_row0;           // WGRAD_GU: the shared expert's first row in its B map (x)
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
@@ -94,7 +101,7 @@ __host__ __device__ __forceinline__ int64_t padded_row0(int64_t offset, int g) {
 }
 
 __device__ __forceinline__ TileCoord decode_dgrad(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                  const int32_t* seg_rows) {
+                                                  const int32_t* seg_rows, int tm) {
   int lo = 0, hi = ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -107,7 +114,7 @@ __device__ __forceinline__ TileCoord decode_dgrad(int tile, const int32_t* mt_pr
   const int local = tile - n_tiles * mt_prefix[lo];
   c.nb = local / mt;
   c.mb = local - c.nb * mt;
-  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
   return c;
 }
 
@@ -134,9 +141,9 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t mn_bl
   return d;
 }
 
-__host__ __device__ constexpr uint32_t idesc_bwd(bool a_mn) {
+__host__ __device__ constexpr uint32_t idesc_bwd(bool a_mn, int M) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
-         ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -144,11 +151,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-template <int MODE>
+// CG = 2: a CTA pair works one 256-row tile (dgrad: 256 rows of an expert segment; wgrad:
+// 256 rows of the weight gradient); each CTA loads its own 128 rows of A and 128 of B's 256
+// columns, the leader issues the pair MMAs (M = 256) and its commits reach both CTAs, and
+// each CTA's epilogue drains its own TMEM rows.
+template <int MODE, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0x,
                        const __grid_constant__ CUtensorMap tmB1x, const BwdParams p) {
+  using S = BwdSmem<CG>;
+  constexpr int kStages = S::kStages, kBBytes = S::kBBytes, kStageBytes = S::kStageBytes;
+  constexpr int TM = BM * CG;               // rows of a tile
+  constexpr int kBoxes = (BN / CG) / 64;    // MN boxes of B per CTA
   constexpr bool kWgrad = MODE == WGRAD_DOWN || MODE == WGRAD_GU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -168,6 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -176,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], kEpiWarps * CG);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -186,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
   if (warp == 2) {
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rows = 0;
       if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
       else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + BM - 1) / BM;
+      const int mt = (rows + TM - 1) / TM;
       int inc = mt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -211,63 +229,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = kWgrad ? ngroups * p.m_tiles_out * p.n_tiles : p.n_tiles * mt_prefix[ngroups];
   auto decode = [&](int tile) {
     return kWgrad ? decode_wgrad(tile, p.m_tiles_out, p.n_tiles, seg_rows)
-                  : decode_dgrad(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+                  : decode_dgrad(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
   };
   auto kblocks_of = [&](const TileCoord& c) { return kWgrad ? (c.rows + BK - 1) / BK : p.K / BK; };
   auto group_row0 = [&](int g) { return g >= p.G ? p.a2_row_base : p.offsets[g]; };
 
   if (warp == 0) {
-    // ======================= TMA producer
+    // ======================= TMA producer (each CTA loads its own rows of A and half of B)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
         const TileCoord c = decode(tile);
         const bool extra = c.g >= p.G;
         const int row0 = group_row0(c.g);
         const int kbs = kblocks_of(c);
+        const int bx0 = c.nb * BN + (int)rank * (BN / CG);  // this CTA's first B column
         for (int kb = 0; kb < kbs; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          const CUtensorMap* ta = &tmA;
+          const CUtensorMap* tb;
+          int ax, ay, by;
+          bool a_two_boxes;
           if constexpr (kWgrad) {
-            // A: activation [rows, M_out] MN-major (2 boxes); B: activation [rows, N_out] (4
-            // boxes). WGRAD_GU: A = dgu (padded rows), B = xd or x; WGRAD_DOWN: A = dyd, B = h
-            // (padded rows).
+            // A: activation [rows, M_out] MN-major; B: activation [rows, N_out] MN-major.
+            // WGRAD_GU: A = dgu (padded rows), B = xd or x; WGRAD_DOWN: A = dyd, B = h (padded)
             const int y_pad = (int)padded_row0(row0, c.g) + kb * BK;
-            const int y = (MODE == WGRAD_GU ? y_pad : row0 + kb * BK);
-            tma_load_2d(&tmA, a_dst, &full[stage], c.mb * BM, y);
-            tma_load_2d(&tmA, a_dst + 8192, &full[stage], c.mb * BM + 64, y);
-            const CUtensorMap* tb = extra ? &tmB0x : &tmB0;
-            const int yb = MODE == WGRAD_DOWN ? y_pad : (extra ? p.extra_b_row0 + kb * BK : row0 + kb * BK);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], c.nb * BN + 64 * j, yb);
+            ax = c.mb * TM + (int)rank * BM;
+            ay = MODE == WGRAD_GU ? y_pad : row0 + kb * BK;
+            a_two_boxes = true;
+            tb = extra ? &tmB0x : &tmB0;
+            by = MODE == WGRAD_DOWN ? y_pad : (extra ? p.extra_b_row0 + kb * BK : row0 + kb * BK);
           } else {
-            // A: [rows, K] K-major, 128 rows (dgu: padded rows); B: weight rows = the K index,
-            // MN-major (4 boxes)
+            // A: [rows, K] K-major, this CTA's 128 rows (dgu: padded rows); B: weight rows =
+            // the K index, MN-major
             const int a_row0 = MODE == DGRAD_GU ? (int)padded_row0(row0, c.g) : row0;
-            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row0 + c.mb * BM);
-            const CUtensorMap* tb;
-            int brow;
+            ax = kb * BK;
+            ay = a_row0 + c.mb * TM + (int)rank * BM;
+            a_two_boxes = false;
             if (MODE == DGRAD_DOWN) {
               tb = extra ? &tmB0x : &tmB0;
-              brow = kb * BK;
+              by = kb * BK;
             } else {  // K = 2F: 128-column blocks alternate gate / up
               const bool up = (kb >> 1) & 1;
               tb = extra ? (up ? &tmB1x : &tmB0x) : (up ? &tmB1 : &tmB0);
-              brow = (kb >> 2) * 128 + (kb & 1) * 64;
+              by = (kb >> 2) * 128 + (kb & 1) * 64;
             }
-            brow += extra ? 0 : c.g * p.b_group_rows;
+            by += extra ? 0 : c.g * p.b_group_rows;
+          }
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(ta, a_dst, &full[stage], ax, ay);
+            if (a_two_boxes) tma_load_2d(ta, a_dst + 8192, &full[stage], ax + 64, ay);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], c.nb * BN + 64 * j, brow);
+            for (int j = 0; j < kBoxes; ++j) tma_load_2d(tb, b_dst + 8192 * j, &full[stage], bx0 + 64 * j, by);
+          } else {
+            // both CTAs' loads complete on the leader's barrier, which expects both
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+            tma_load_2d_pair(ta, a_dst, bar, ax, ay);
+            if (a_two_boxes) tma_load_2d_pair(ta, a_dst + 8192, bar, ax + 64, ay);
+#pragma unroll
+            for (int j = 0; j < kBoxes; ++j) tma_load_2d_pair(tb, b_dst + 8192 * j, bar, bx0 + 64 * j, by);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -278,63 +311,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (stage - 1 - i + 2 * kStages) % kStages;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer (lane 0 of the warp)
-    constexpr uint32_t idesc = idesc_bwd(kWgrad);
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      const TileCoord c = decode(tile);
-      const int kbs = kblocks_of(c);
-      if (kbs == 0) continue;  // an expert without rows: the epilogue writes zeros
-      ok = mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < kbs; ++kb) {
-        ok = mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        uint8_t* b_st = sB + stage * kBBytes;
-        if (lane == 0) {
+    // ======================= MMA issuer (the leader of a pair issues for both CTAs)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bwd(kWgrad, TM);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+        const TileCoord c = decode(tile);
+        const int kbs = kblocks_of(c);
+        if (kbs == 0) continue;  // an expert without rows: the epilogues write zeros
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_addr(sA + stage * kABytes);
-          const uint32_t b_addr = smem_addr(b_st);
+          const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = kWgrad ? desc_mn_sw128(a_addr + k * 2048, 8192) : desc_k_sw128(a_addr + k * 32);
-            mma_bf16(d_tmem, ad, desc_mn_sw128(b_addr + k * 2048, 8192), idesc, (kb | k) != 0);
+            const uint64_t bd = desc_mn_sw128(b_addr + k * 2048, 8192);
+            if constexpr (CG == 1) mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            else mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
-          mma_commit(&empty[stage]);
+          if constexpr (CG == 1) mma_commit(&empty[stage]);
+          else mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (!ok) break;
+        if constexpr (CG == 1) mma_commit(&tfull[acc]);
+        else mma_commit_pair(&tfull[acc], 0x3);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      if (ok && lane == 0) mma_commit(&tfull[acc]);
-      __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-    }
-    if (lane == 0) {
-      mma_commit(drain);
+      if constexpr (CG == 1) mma_commit(drain);
+      else mma_commit_pair(drain, 0x3);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    } else if (lane == 0 && CG == 2) {
+      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
-    __syncwarp();
   } else {
     // ======================= epilogue (warps 2..9; TMEM lane quarter = warp % 4)
     const int quarter = warp & 3;
     const int cbase = ((warp - 2) >> 2) * (BN / 2);  // this warp's 128 of the tile's 256 columns
-    const int r = quarter * 32 + lane;
+    const int wrow = (int)rank * BM + quarter * 32;   // the warp's first row in the tile
+    const int r = wrow + lane;
     uint8_t* stage = sEpi + (warp - 2) * 2048;
+    const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_addr(&tempty[0]), 0) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit; tile < total_tiles; tile += nunits) {
       const TileCoord c = decode(tile);
       const bool extra = c.g >= p.G;
       const bool empty_tile = kblocks_of(c) == 0;
@@ -346,20 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if constexpr (kWgrad) {
-        // fp32 gradient rows: row r of the 128-row output tile, 256 columns
+        // fp32 gradient rows: row r of the output tile, 256 columns
+        const int64_t ldo = p.N_out;
         float* wbase;
-        int64_t ldo;
         if (MODE == WGRAD_DOWN) {
-          ldo = p.N_out;
-          wbase = (extra ? p.w0x : p.w0 + (int64_t)c.g * p.M_out * p.N_out) + (int64_t)c.mb * BM * ldo;
+          wbase = (extra ? p.w0x : p.w0 + (int64_t)c.g * p.M_out * p.N_out) + ((int64_t)c.mb * TM + wrow) * ldo;
         } else {  // dgu's 128-row blocks alternate dWg / dWu rows of one F block
-          ldo = p.N_out;
-          const bool up = c.mb & 1;
+          const int blk = c.mb * CG + (int)rank;
+          const bool up = blk & 1;
           float* w = up ? (extra ? p.w1x : p.w1 + (int64_t)c.g * p.F * p.N_out)
                         : (extra ? p.w0x : p.w0 + (int64_t)c.g * p.F * p.N_out);
-          wbase = w + (int64_t)(c.mb >> 1) * BM * ldo;
+          wbase = w + ((int64_t)(blk >> 1) * BM + quarter * 32) * ldo;
         }
-        uint8_t* out = reinterpret_cast<uint8_t*>(wbase + (int64_t)quarter * 32 * ldo + c.nb * BN + cbase);
+        uint8_t* out = reinterpret_cast<uint8_t*>(wbase + c.nb * BN + cbase);
         uint32_t nxt[32];
         if (!empty_tile) tmem_ld32(t_row + cbase, nxt);
 #pragma unroll 1
@@ -385,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int row0 = group_row0(c.g);
-        const int64_t warp_row0 = (int64_t)row0 + c.mb * BM + quarter * 32;
-        const int warp_live = c.rows - quarter * 32;
+        const int64_t warp_row0 = (int64_t)row0 + c.mb * TM + wrow;
+        const int warp_live = c.rows - wrow;
         const bool live = r < c.rows;
         if (MODE == DGRAD_GU) {
           uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN + cbase) * 2;
@@ -409,9 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ld_gu = 2 * p.F;
           // dgu and h rows are padded: this warp's rows start at prow0, and the rows past the
           // segment up to its multiple of 64 are written as zeros (g = u = 0 there)
-          const int64_t prow0 = padded_row0(row0, c.g) + c.mb * BM + quarter * 32;
+          const int64_t prow0 = padded_row0(row0, c.g) + c.mb * TM + wrow;
           const int seg = c.g < p.G ? p.offsets[c.g + 1] - p.offsets[c.g] : p.T_extra;
-          const int pad_live = min((seg + 63) / 64 * 64 - c.mb * BM, BM) - quarter * 32;
+          const int pad_live = min((seg + 63) / 64 * 64 - c.mb * TM, TM) - wrow;
 #pragma unroll 1
           for (int c0 = cbase; c0 < cbase + BN / 2; c0 += 32) {
             const int f0 = c.nb * BN + c0;     // first F column of the chunk
@@ -476,7 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!empty_tile) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+          if (CG == 2 && !leader) mbar_arrive_cluster(tempty_leader + acc * 8);
+          else mbar_arrive(&tempty[acc]);
+        }
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
     }
@@ -484,10 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_cg<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -495,19 +532,45 @@ bool make_bf16_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, box_rows, 64);
 }
 
-template <int MODE>
+template <int MODE, int CG>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0x,
                    const CUtensorMap& b1x, const BwdParams& p, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_bwd_kernel<MODE>;
+  auto kern = tc_gemm_bwd_kernel<MODE, CG>;
+  const size_t smem = BwdSmem<CG>::kBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, b0x, b1x, p);
+  if constexpr (CG == 1) {
+    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+    kern<<<grid, kThreads, smem, s>>>(a, b0, b1, b0x, b1x, p);
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must be resident all at once: no more pairs than fit together
+    static int max_pairs = 0;
+    if (!max_pairs) {
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
+      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+    }
+    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
+    cfg.gridDim = dim3(2 * pairs);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, b0x, b1x, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -529,7 +592,11 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
   const int64_t prows = backward_padded_rows(c);  // rows of the padded dgu and h
-  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  // dgrad tiles are expert segments: CTA pairs (256-row tiles) when experts average at least
+  // 512 rows, as in the forward; wgrad tiles are weight-gradient rows and always pairs
+  const bool pair = (int64_t)c.T * c.k >= 512LL * c.E;
+  const int tm = pair ? 2 * BM : BM;
+  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
   // ---- recompute g and u (the forward GEMM1 without its activation)
   cudaError_t e = launch_gate_up_preact(c, xd, x, offsets, w, gu, st, s);
   if (e != cudaSuccess) return e;
@@ -555,7 +622,8 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   p.out = static_cast<__nv_bfloat16*>(dgu);
   p.h_out = static_cast<__nv_bfloat16*>(h);
   p.gu = static_cast<const __nv_bfloat16*>(gu);
-  e = launch<DGRAD_DOWN>(a, b0, b0, b0x, b0x, p, mt_bound * p.n_tiles, s);
+  e = pair ? launch<DGRAD_DOWN, 2>(a, b0, b0, b0x, b0x, p, mt_bound * p.n_tiles, s)
+           : launch<DGRAD_DOWN, 1>(a, b0, b0, b0x, b0x, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- dxd = dg Wg + du Wu (K = 2F in dgu's interleaved order; B = Wg or Wu rows)
   ok = make_bf16_box(&a, dgu, prows, 2 * (uint64_t)c.F, BM) && make_bf16_box(&b0, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
@@ -568,7 +636,8 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   p.b_group_rows = c.F;
   p.ldc = c.H;
   p.out = static_cast<__nv_bfloat16*>(dxd);
-  e = launch<DGRAD_GU>(a, b0, b1, b0x, b1x, p, mt_bound * p.n_tiles, s);
+  e = pair ? launch<DGRAD_GU, 2>(a, b0, b1, b0x, b1x, p, mt_bound * p.n_tiles, s)
+           : launch<DGRAD_GU, 1>(a, b0, b1, b0x, b1x, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- dWd[e] = dyd_e^T h_e (M_out = H, N_out = F; both operands MN-major)
   const int ngroups = c.E + (shared ? 1 : 0);
@@ -577,12 +646,12 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   p.extra_b_row0 = 0;  // unused: h's rows are addressed by their padded position
   p.M_out = c.H;
   p.N_out = c.F;
-  p.m_tiles_out = c.H / BM;
+  p.m_tiles_out = c.H / (2 * BM);
   p.n_tiles = c.F / BN;
   p.w0 = gr.dw_down;
   p.w0x = gr.dws_down;
   p.w1 = p.w1x = nullptr;
-  e = launch<WGRAD_DOWN>(a, b0, b0, b0, b0, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
+  e = launch<WGRAD_DOWN, 2>(a, b0, b0, b0, b0, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- dWg[e], dWu[e] = dgu_e^T xd_e (M_out = 2F interleaved, N_out = H)
   // xd's map ends at the last routed row: the TMA fills zeros past it, never reading rows
@@ -594,13 +663,13 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   p.extra_b_row0 = 0;
   p.M_out = 2 * c.F;
   p.N_out = c.H;
-  p.m_tiles_out = 2 * c.F / BM;
+  p.m_tiles_out = 2 * c.F / (2 * BM);
   p.n_tiles = c.H / BN;
   p.w0 = gr.dw_gate;
   p.w1 = gr.dw_up;
   p.w0x = gr.dws_gate;
   p.w1x = gr.dws_up;
-  return launch<WGRAD_GU>(a, b0, b0, b0x, b0x, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
+  return launch<WGRAD_GU, 2>(a, b0, b0, b0x, b0x, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
 }
 
 }  // namespace tc
