@@ -32,6 +32,8 @@ CASES = [
     synth.scaled(W["dsv3_mxfp8"], T=256, H=512, E=32, F=256, F_shared=256, name="mxfp8_small"),
     synth.scaled(W["dsv3_mxfp8"], T=900, H=1024, E=8, k=2, F=384, F_shared=384, n_groups=2,
                  topk_groups=1, name="mxfp8_deep_k"),
+    synth.scaled(W["dsv3_mxfp8"], T=1300, H=768, E=4, k=2, F=640, F_shared=640, n_groups=2,
+                 topk_groups=1, name="mxfp8_pair"),
 ]
 
 

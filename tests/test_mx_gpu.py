@@ -26,6 +26,8 @@ CASES = [
     # hot and empty experts (Zipf-biased logits), no shared expert
     synth.scaled(MX, T=600, H=256, E=32, k=4, F=128, n_shared=0, F_shared=0, n_groups=1, topk_groups=1,
                  score_fn=synth.SOFTMAX, renorm=0, zipf=True, name="mx_imbalanced"),
+    # >= 512 rows per expert on average: 256-row CTA-pair tiles, ragged pair tails, shared expert
+    synth.scaled(MX, T=1100, H=512, E=4, k=2, F=384, F_shared=384, n_groups=2, topk_groups=1, name="mx_pair"),
 ]
 
 

@@ -8,13 +8,20 @@
 // tensor memory, so the whole K loop accumulates in one TMEM accumulator with no software
 // promotion.
 //
-// Tile 128 x 256, K stages of 128 (four MMAs of K = 32, scale-factor id = the slice).
+// Tile 128 x 256 (one CTA) or 256 x 256 (a CTA pair), K stages of 128 (four MMAs of K = 32,
+// scale-factor id = the slice).
 // Block: warp 0 TMA producer, warp 1 MMA issuer (TMEM owner), warps 2-9 epilogue (two
 // warps per TMEM lane quarter, each owning half of the tile's columns).
 //   Per stage the producer loads the A and B tiles (TMA, 128-byte swizzle) and the stage's
-//   scale atoms (one 512-byte atom per 128 rows, plain bulk copies); the MMA issuer moves
-//   the atoms into tensor memory with tcgen05.cp 32x128b.warpx4 (the copy and the MMAs
-//   that read it come from one thread, so they execute in order) and issues the MMAs.
+//   scale atoms (one 512-byte atom per 128 rows, TMA boxes of a linear [atoms, 128 x u32]
+//   view); the MMA issuer moves the atoms into tensor memory with tcgen05.cp 32x128b.warpx4
+//   (the copy and the MMAs that read it come from one thread, so they execute in order)
+//   and issues the MMAs.
+//   CTA pair (CG = 2; built, not selected: see launch_grouped_mlp_mx): M = 256 pair MMAs; each CTA loads its
+//   own 128 rows of A with their scale atom, its half of B (GEMM1: CTA 0 the gate rows, CTA 1
+//   the up rows) and both B atoms, because each CTA's tensor core reads the scales of all
+//   256 B columns from its own TMEM; the leader's tcgen05.cp.cta_group::2 copies in both
+//   CTAs, each from its own shared memory. Stages are 33.5 KB, six in flight.
 //   TMEM: accumulator in columns [0, 256); stage s's scale factors in [256 + 16s, +12).
 //   The accumulator is single-buffered: the epilogue loads its 128 x 256 values into
 //   registers and hands the accumulator back before it computes and stores, so the next
@@ -37,6 +44,8 @@ namespace tc {
 
 bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows, uint64_t cols,
                uint32_t box_rows, uint32_t box_cols);
+bool make_tmap_linear(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows,
+                      uint64_t cols, uint32_t box_rows, uint32_t box_cols);
 int num_sms();
 
 namespace {
@@ -44,19 +53,23 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 128;  // BK in elements = bytes (e4m3)
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
-constexpr int kStages = 4;
 constexpr int kABytes = BM * BK;
-constexpr int kBBytes = BN * BK;
 constexpr int kAtomBytes = 512;
 constexpr int kSfBytes = 3 * kAtomBytes;  // A atom, then B atoms for columns [0,128), [128,256)
-constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
 constexpr int kMaxGroups = 514;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kSfCol0 = 256, kSfColsPerStage = 16;
+constexpr uint32_t kSfCol0 = 256, kSfColsPerStage = 16;  // up to 6 stages: columns 256..351
 constexpr int kEpiStageBytes = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (GEMM2 stores)
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) +
-                              kEpiWarps * kEpiStageBytes;
+
+template <int CG>
+struct MxSmem {
+  static constexpr int kBBytes = (BN / CG) * BK;  // this CTA's B rows
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+  static constexpr int kStages = CG == 2 ? 6 : 4;
+  static constexpr size_t kBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) +
+                                   kEpiWarps * kEpiStageBytes;
+};
 
 enum { MX_SWIGLU_Q8 = 0, MX_STORE_BF16 = 1 };
 
@@ -84,7 +97,7 @@ struct TileCoord {
 };
 
 __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows) {
+                                                 const int32_t* seg_rows, int tm) {
   int lo = 0, hi = ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -97,17 +110,8 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_pre
   const int local = tile - n_tiles * mt_prefix[lo];
   c.nb = local / mt;
   c.mb = local - c.nb * mt;
-  c.rows = min(BM, seg_rows[lo] - c.mb * BM);
+  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
   return c;
-}
-
-// Non-tensor bulk copy global -> shared completing `bytes` on the mbarrier (16-byte
-// aligned addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
 }
 
 // Shared-memory descriptor of a scale atom for tcgen05.cp: no swizzle, 8-row core matrices
@@ -120,9 +124,14 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
   return d;
 }
 
-// 32 lanes x 128 bits of shared memory to TMEM, repeated into all four lane quarters.
+// 32 lanes x 128 bits of shared memory to TMEM, repeated into all four lane quarters (the
+// pair form copies in both CTAs of the pair, each from its own shared memory).
+template <int CG>
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // Instruction descriptor of kind::mxf8f6f4: e4m3 x e4m3, fp32 accumulate, K-major A and B,
@@ -131,15 +140,25 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
   return (sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 
+template <int CG>
 __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -148,11 +167,17 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-template <int EPI>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0x,
-                      const __grid_constant__ CUtensorMap tmB1x, const MxParams p) {
+                      const __grid_constant__ CUtensorMap tmB1x, const __grid_constant__ CUtensorMap tmSA,
+                      const __grid_constant__ CUtensorMap tmSB0, const __grid_constant__ CUtensorMap tmSB1,
+                      const __grid_constant__ CUtensorMap tmSB0x, const __grid_constant__ CUtensorMap tmSB1x,
+                      const MxParams p) {
+  using S = MxSmem<CG>;
+  constexpr int kStages = S::kStages, kBBytes = S::kBBytes, kStageBytes = S::kStageBytes;
+  constexpr int TM = BM * CG;  // rows of an m tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -173,6 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
   const int kblocks = p.K / BK;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -180,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kEpiWarps);  // one arrival per epilogue warp
+    mbar_init(acc_empty, kEpiWarps * CG);  // one arrival per epilogue warp of the pair
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -188,8 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmSA);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
   if (warp == 2) {
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
@@ -197,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rows = 0;
       if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
       else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + BM - 1) / BM;
+      const int mt = (rows + TM - 1) / TM;
       int inc = mt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -214,48 +243,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.n_tiles * mt_prefix[ngroups];
 
   if (warp == 0) {
-    // ======================= TMA producer
+    // ======================= TMA producer (each CTA loads its own A rows, half of B, scales)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+        const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
         const bool extra = c.g >= p.G;
         const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
-        const int a_row = (int)gofs + c.mb * BM;
-        const int64_t a_atom = mx_group_atom_base(gofs, c.g) + c.mb;
+        const int a_row = (int)gofs + c.mb * TM + (int)rank * BM;
+        const int a_atom = (int)(mx_group_atom_base(gofs, c.g) + c.mb * CG + rank);
         const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
         const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
-        const uint8_t* sf0 = extra ? p.b0x_sf : p.b0_sf;
-        const uint8_t* sf1 = extra ? p.b1x_sf : p.b1_sf;
+        const CUtensorMap* ts0 = extra ? &tmSB0x : &tmSB0;
+        const CUtensorMap* ts1 = extra ? &tmSB1x : &tmSB1;
         const int b_tile_rows = EPI == MX_SWIGLU_Q8 ? BN / 2 : BN;
         const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-        const int64_t b_atom = b_row / 128;  // b_row is a multiple of 128
+        const int b_atom = b_row / 128;  // b_row is a multiple of 128
+        // this CTA's B rows: GEMM1 the gate (rank 0) or up (rank 1) rows of the F block;
+        // GEMM2 rows [rank * 128, +128) of the N tile
+        const CUtensorMap* tb_mine = (CG == 2 && EPI == MX_SWIGLU_Q8 && rank == 1) ? tb1 : tb0;
+        const int b_row_mine = b_row + ((CG == 2 && EPI != MX_SWIGLU_Q8) ? (int)rank * (BN / 2) : 0);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
           uint8_t* sf_dst = sSF + stage * kSfBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row);
-          bulk_load(sf_dst, p.a_sf + ((a_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
-          if (EPI == MX_SWIGLU_Q8) {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-            tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
-            bulk_load(sf_dst + kAtomBytes, sf0 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
-            bulk_load(sf_dst + 2 * kAtomBytes, sf1 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
+          const int sa_y = a_atom * kblocks + kb;
+          const int sb0_y = (EPI == MX_SWIGLU_Q8 ? b_atom : b_atom) * kblocks + kb;
+          const int sb1_y = (EPI == MX_SWIGLU_Q8 ? b_atom : b_atom + 1) * kblocks + kb;
+          const CUtensorMap* tsb1 = EPI == MX_SWIGLU_Q8 ? ts1 : ts0;
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row);
+            if (EPI == MX_SWIGLU_Q8) {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+              tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
+            } else {
+              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            }
+            tma_load_2d(&tmSA, sf_dst, &full[stage], 0, sa_y);
+            tma_load_2d(ts0, sf_dst + kAtomBytes, &full[stage], 0, sb0_y);
+            tma_load_2d(tsb1, sf_dst + 2 * kAtomBytes, &full[stage], 0, sb1_y);
           } else {
-            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-            bulk_load(sf_dst + kAtomBytes, sf0 + ((b_atom * kblocks + kb) << 9), kAtomBytes, &full[stage]);
-            bulk_load(sf_dst + 2 * kAtomBytes, sf0 + (((b_atom + 1) * kblocks + kb) << 9), kAtomBytes,
-                      &full[stage]);
+            // both CTAs' loads complete on the leader's barrier, which expects both
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+            tma_load_2d_pair(&tmA, a_dst, bar, kb * BK, a_row);
+            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row_mine);
+            tma_load_2d_pair(&tmSA, sf_dst, bar, 0, sa_y);
+            tma_load_2d_pair(ts0, sf_dst + kAtomBytes, bar, 0, sb0_y);
+            tma_load_2d_pair(tsb1, sf_dst + 2 * kAtomBytes, bar, 0, sb1_y);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -267,17 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (stage - 1 - i + 2 * kStages) % kStages;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer
-    if (lane == 0) {
+    // ======================= MMA issuer (the leader of a pair issues for both CTAs)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
         // the epilogue has taken the previous tile's accumulator out of TMEM
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
         acc_phase ^= 1;
@@ -290,19 +336,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf_addr = smem_addr(sSF + stage * kSfBytes);
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_atom(sfa_t, desc_atom(sf_addr));
-          tmem_cp_atom(sfb_t, desc_atom(sf_addr + kAtomBytes));
-          tmem_cp_atom(sfb_t + 4, desc_atom(sf_addr + 2 * kAtomBytes));
+          tmem_cp_atom<CG>(sfa_t, desc_atom(sf_addr));
+          tmem_cp_atom<CG>(sfb_t, desc_atom(sf_addr + kAtomBytes));
+          tmem_cp_atom<CG>(sfb_t + 4, desc_atom(sf_addr + 2 * kAtomBytes));
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction: +32 bytes, scale id k
-            mma_mx(tmem_base, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32),
-                   idesc_mx(BM, BN, (uint32_t)k), sfa_t, sfb_t, (kb | k) != 0);
-          mma_commit(&empty[stage]);
+            mma_mx<CG>(tmem_base, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32),
+                       idesc_mx(TM, BN, (uint32_t)k), sfa_t, sfb_t, (kb | k) != 0);
+          if constexpr (CG == 1) mma_commit(&empty[stage]);
+          else mma_commit_pair(&empty[stage], 0x3);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        if (ok) mma_commit(acc_full);
+        if (ok) {
+          if constexpr (CG == 1) mma_commit(acc_full);
+          else mma_commit_pair(acc_full, 0x3);
+        }
       }
-      mma_commit(drain);
+      if constexpr (CG == 1) mma_commit(drain);
+      else mma_commit_pair(drain, 0x3);
+      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
+    } else if (lane == 0 && CG == 2) {
+      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -310,12 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int half = ew >> 2;  // which 128 of the tile's 256 columns this warp owns
-    const int r = quarter * 32 + lane;
+    const int r = quarter * 32 + lane;          // TMEM lane = this CTA's row
+    const int row_in_tile = (int)rank * BM + r;  // row of the (pair) tile
     uint8_t* stage = sEpi + ew * kEpiStageBytes;
+    const uint32_t acc_empty_leader = CG == 2 ? mapa_shared(smem_addr(acc_empty), 0) : 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows);
+    for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
+      const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
       const bool extra = c.g >= p.G;
       ok = mbar_wait(acc_full, acc_phase, abort, p.timeout_ns, p.status);
       ok = __all_sync(0xffffffffu, ok);
@@ -337,14 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();  // every lane's loads are complete: one arrival per warp
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) {
+        if (CG == 2 && !leader) mbar_arrive_cluster(acc_empty_leader);
+        else mbar_arrive(acc_empty);
+      }
 
       const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
-      const int64_t row0 = (extra ? p.out_extra_base : gofs) + c.mb * BM + quarter * 32;  // the warp's first row
-      const int live_rows = c.rows - quarter * 32;  // rows of this warp inside the segment
+      const int64_t row0 = (extra ? p.out_extra_base : gofs) + c.mb * TM + (int)rank * BM + quarter * 32;
+      const int live_rows = c.rows - ((int)rank * BM + quarter * 32);  // rows of this warp inside the segment
       if (EPI == MX_SWIGLU_Q8) {
         // 64 bytes of h codes per thread per tile: direct 16-byte stores
-        if (r < c.rows) {
+        if (row_in_tile < c.rows) {
           uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (row0 + lane) * p.ldc + c.nb * 128 + half * 64;
           uint32_t codes = 0;
 #pragma unroll
@@ -368,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(out + 32 * blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
             codes |= (uint32_t)(s + 127) << (8 * blk);
           }
-          // blocks 2*half and 2*half + 1 of the h stage nb, in the tile's atom row
-          const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb;
+          // blocks 2*half and 2*half + 1 of the h stage nb, in this CTA's atom row
+          const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb * CG + rank;
           *reinterpret_cast<uint16_t*>(p.out_sf + mx_atom_byte(atom, c.nb, p.ldc / 128, r) + 2 * half) =
               (uint16_t)codes;
         }
@@ -398,10 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_cg<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -409,19 +469,54 @@ bool make_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, box_rows, BK);
 }
 
-template <int EPI>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0x,
-                   const CUtensorMap& b1x, const MxParams& p, int64_t max_tiles, cudaStream_t s) {
+// Scale atoms as rows of 128 uint32 (one 512-byte box per atom, no swizzle).
+bool make_atoms(CUtensorMap* m, const void* base, uint64_t atoms) {
+  return make_tmap_linear(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, atoms, 128, 1, 128);
+}
+
+struct MxMaps {
+  CUtensorMap a, b0, b1, b0x, b1x, sa, sb0, sb1, sb0x, sb1x;
+};
+
+template <int EPI, int CG>
+cudaError_t launch(const MxMaps& m, const MxParams& p, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_mx_kernel<EPI>;
+  auto kern = tc_gemm_mx_kernel<EPI, CG>;
+  const size_t smem = MxSmem<CG>::kBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, b0x, b1x, p);
+  if constexpr (CG == 1) {
+    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+    kern<<<grid, kThreads, smem, s>>>(m.a, m.b0, m.b1, m.b0x, m.b1x, m.sa, m.sb0, m.sb1, m.sb0x, m.sb1x, p);
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must be resident all at once: no more pairs than fit together
+    static int max_pairs = 0;
+    if (!max_pairs) {
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
+      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+    }
+    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
+    cfg.gridDim = dim3(2 * pairs);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, m.a, m.b0, m.b1, m.b0x, m.b1x, m.sa, m.sb0, m.sb1, m.sb0x,
+                                       m.sb1x, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -437,12 +532,27 @@ cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const v
                                   cudaStream_t s) {
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
+  // Single-CTA tiles. The CTA-pair form (CG = 2) computes the same results (it passes the
+  // same tests when selected) but measured slower on GB300: 10.67 against 9.76 ms for the
+  // DeepSeek-V3-shaped MXFP8 layer. Its accumulator stays single-buffered (two 256-column
+  // accumulators and the scale factors do not fit in 512 TMEM columns), so every tile
+  // boundary waits for both CTAs' epilogues across the pair, and 256-row tiles double the
+  // padding of ragged segment tails. Not selected.
+  const bool pair = false;
+  const int tm = pair ? 2 * BM : BM;
+  const int64_t atoms_act = mx_act_atom_rows(c);
   // ---- GEMM1: h = mx(silu(A Wg^T) * (A Wu^T)); the shared expert's A = dispatched rows R..
-  CUtensorMap a1, bg, bu, bgx, bux;
-  bool ok = make_u8(&a1, xd, rows, c.H, BM) && make_u8(&bg, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
-            make_u8(&bu, w.w_up, (uint64_t)c.E * c.F, c.H, 128);
-  if (shared) ok = ok && make_u8(&bgx, w.ws_gate, c.F, c.H, 128) && make_u8(&bux, w.ws_up, c.F, c.H, 128);
-  else { bgx = bg; bux = bu; }
+  MxMaps m{};
+  bool ok = make_u8(&m.a, xd, rows, c.H, BM) && make_u8(&m.b0, w.w_gate, (uint64_t)c.E * c.F, c.H, 128) &&
+            make_u8(&m.b1, w.w_up, (uint64_t)c.E * c.F, c.H, 128) &&
+            make_atoms(&m.sa, xd_sf, (uint64_t)atoms_act * (c.H / 128)) &&
+            make_atoms(&m.sb0, w.s_gate, (uint64_t)c.E * c.F / 128 * (c.H / 128)) &&
+            make_atoms(&m.sb1, w.s_up, (uint64_t)c.E * c.F / 128 * (c.H / 128));
+  if (shared)
+    ok = ok && make_u8(&m.b0x, w.ws_gate, c.F, c.H, 128) && make_u8(&m.b1x, w.ws_up, c.F, c.H, 128) &&
+         make_atoms(&m.sb0x, w.ss_gate, (uint64_t)c.F / 128 * (c.H / 128)) &&
+         make_atoms(&m.sb1x, w.ss_up, (uint64_t)c.F / 128 * (c.H / 128));
+  else { m.b0x = m.b0; m.b1x = m.b1; m.sb0x = m.sb0; m.sb1x = m.sb1; }
   if (!ok) return cudaErrorInvalidValue;
   MxParams p{};
   p.offsets = offsets;
@@ -454,37 +564,35 @@ cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const v
   p.K = c.H;
   p.n_tiles = c.F / 128;
   p.b_group_rows = c.F;
-  p.a_sf = static_cast<const uint8_t*>(xd_sf);
-  p.b0_sf = static_cast<const uint8_t*>(w.s_gate);
-  p.b1_sf = static_cast<const uint8_t*>(w.s_up);
-  p.b0x_sf = static_cast<const uint8_t*>(shared ? w.ss_gate : w.s_gate);
-  p.b1x_sf = static_cast<const uint8_t*>(shared ? w.ss_up : w.s_up);
   p.ldc = c.F;
   p.out = h;
   p.out_sf = static_cast<uint8_t*>(h_sf);
   p.status = st;
   p.timeout_ns = kTimeoutNs;
-  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
-  cudaError_t e = launch<MX_SWIGLU_Q8>(a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
+  cudaError_t e = pair ? launch<MX_SWIGLU_Q8, 2>(m, p, mt_bound * p.n_tiles, s)
+                       : launch<MX_SWIGLU_Q8, 1>(m, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = h Wd^T with both operands' MX scales, bf16 out
-  CUtensorMap a2, bd, bdx;
-  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, BN);
-  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, BN);
-  else bdx = bd;
+  const uint32_t box2 = pair ? BN / 2 : BN;  // a pair's CTAs each load half of the N tile
+  MxMaps m2{};
+  ok = make_u8(&m2.a, h, rows, c.F, BM) && make_u8(&m2.b0, w.w_down, (uint64_t)c.E * c.H, c.F, box2) &&
+       make_atoms(&m2.sa, h_sf, (uint64_t)atoms_act * (c.F / 128)) &&
+       make_atoms(&m2.sb0, w.s_down, (uint64_t)c.E * c.H / 128 * (c.F / 128));
+  if (shared)
+    ok = ok && make_u8(&m2.b0x, w.ws_down, c.H, c.F, box2) &&
+         make_atoms(&m2.sb0x, w.ss_down, (uint64_t)c.H / 128 * (c.F / 128));
+  else { m2.b0x = m2.b0; m2.sb0x = m2.sb0; }
   if (!ok) return cudaErrorInvalidValue;
+  m2.b1 = m2.b0; m2.b1x = m2.b0x; m2.sb1 = m2.sb0; m2.sb1x = m2.sb0x;
   p.K = c.F;
   p.n_tiles = c.H / BN;
   p.b_group_rows = c.H;
-  p.a_sf = static_cast<const uint8_t*>(h_sf);
-  p.b0_sf = static_cast<const uint8_t*>(w.s_down);
-  p.b1_sf = p.b0_sf;
-  p.b0x_sf = static_cast<const uint8_t*>(shared ? w.ss_down : w.s_down);
-  p.b1x_sf = p.b0x_sf;
   p.ldc = c.H;
   p.out = yd;
   p.out_sf = nullptr;
-  return launch<MX_STORE_BF16>(a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  return pair ? launch<MX_STORE_BF16, 2>(m2, p, mt_bound * p.n_tiles, s)
+              : launch<MX_STORE_BF16, 1>(m2, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc

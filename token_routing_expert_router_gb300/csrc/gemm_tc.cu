@@ -431,6 +431,21 @@ bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [rows, cols] matrix copied box by box without swizzle (the shared-memory copy
+// keeps the global byte order), e.g. the 512-byte MX scale atoms as rows of 128 uint32.
+bool make_tmap_linear(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t rows,
+                      uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 bool make_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
