@@ -281,8 +281,10 @@ def run_gpu(args, w):
         "combine": lambda: moe.moe_combine(cfg, b["yd"], b["tok_row"], b["w"], y),
     }
     if w["act_dtype"] == synth.BF16 and not fp8:  # the fused-permutation alternative
+        # rows gathered by token in GEMM1, routing weights applied in GEMM2's epilogue
         stages["grouped_mlp_gather"] = lambda: moe.moe_grouped_mlp_gather(cfg, x, b["row_token"], b["offsets"],
-                                                                          wts, b["h"], b["yd"], ws)
+                                                                          wts, b["h"], b["yd"], ws,
+                                                                          tok_row=b["tok_row"], topk_w=b["w"])
     for _ in range(2):
         for f in stages.values():
             f()

@@ -231,14 +231,21 @@ moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const void
  * Same outputs as moe_dispatch + moe_grouped_mlp (bit-identical). bf16 layers on the
  * tensor-core path only (else MOE_ERR_UNSUPPORTED). x [T,H], row_token [T*k], offsets
  * [E+1], h [R(+T), F], yd [R(+T), H]. moe_forward keeps the separate dispatch: the four-row
- * gathers are slower on GB300 than the dispatch pass they replace. */
+ * gathers are slower on GB300 than the dispatch pass they replace.
+ * The other half of the fused permutation is optional: with tok_row [T,k] and topk_w [T,k]
+ * (both given, or both NULL; else MOE_ERR_INVALID_ARG) the down projection's epilogue
+ * scales each routed row by its routing weight before rounding,
+ *     yd[r] = bf16(topk_w[t,j] * (h[r] . Wd[e]^T)),  t = row_token[r], tok_row[t,j] = r,
+ * (shared-expert rows unweighted), and moe_combine with topk_w = NULL finishes the layer. */
 moe_status_t moe_grouped_mlp_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
-                                    const int32_t* offsets, const moe_weights_t* w, void* h,
-                                    void* yd, void* ws, moe_stream_t stream);
+                                    const int32_t* offsets, const int32_t* tok_row, const float* topk_w,
+                                    const moe_weights_t* w, void* h, void* yd, void* ws,
+                                    moe_stream_t stream);
 
 /* S7 — combine (Hybrid-EP article, combine operator with high-precision accumulation):
  * y[t] = sum_{j<k} topk_w[t,j] * yd[tok_row[t,j]]  (+ yd[R + t] with a shared expert),
- * accumulated in fp32 in that fixed order, written once in act dtype. */
+ * accumulated in fp32 in that fixed order, written once in act dtype. topk_w = NULL means
+ * unit weights: the plain sum, for rows already weighted by moe_grouped_mlp_gather. */
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* tok_row,
                          const float* topk_w, void* y, moe_stream_t stream);
 

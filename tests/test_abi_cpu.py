@@ -80,7 +80,11 @@ def test_null_and_misaligned_pointers_rejected_on_host(L):
     P = ctypes.c_void_p
     assert L.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_dispatch(ctypes.byref(c), P(4096 + 8), P(4096), P(4096), None, None) == moe.MOE_ERR_INVALID_ARG
-    assert L.moe_combine(ctypes.byref(c), P(4096), P(4096), None, P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(c), P(4096), None, P(4096), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(c), P(4096), P(4096), P(4096 + 4), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    # the routing-weight epilogue takes tok_row and topk_w together or not at all
+    assert L.moe_grouped_mlp_gather(ctypes.byref(c), P(4096), P(4096), P(4096), P(4096), None, None, P(4096),
+                                    P(4096), P(4096), None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_forward(None, None, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_read_status(None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_status_string(moe.MOE_ERR_TIMEOUT).startswith("device")

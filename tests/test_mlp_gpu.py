@@ -124,3 +124,38 @@ def test_gathered_rows_equal_dispatched_rows(w):
     assert torch.equal(h2, b["h"])
     assert torch.equal(yd2, b["yd"])
     assert moe.moe_read_status(b["ws"]) == moe.MOE_OK
+
+
+@pytest.mark.parametrize("w", BF16_CASES, ids=[c["name"] for c in BF16_CASES])
+def test_routing_weight_in_down_projection_epilogue(w):
+    """The other half of the fused permutation: GEMM2's epilogue scales each routed row by
+    its routing weight before rounding, so that the combine is a plain sum. Each weighted
+    routed row is within two bf16 roundings of the weight times the unweighted row, shared
+    rows are untouched, and the unit-weight combine gives the layer output of the oracle."""
+    seed = 6
+    T, H, k = w["T"], w["H"], w["k"]
+    R = T * k
+    inp = synth.host_inputs(w, seed=seed)
+    logits = logits_for(w, seed)
+    idx, wt, (counts, offsets, row_token, tok_row) = routing(w, seed)
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    h1, yd1 = torch.empty_like(b["h"]), torch.empty_like(b["yd"])
+    moe.moe_grouped_mlp_gather(b["cfg"], d["x"], up(row_token), up(offsets), weights_arg(d), h1, yd1, b["ws"])
+    wt32 = wt.astype(np.float32)
+    h2, yd2 = torch.empty_like(b["h"]), torch.empty_like(b["yd"])
+    moe.moe_grouped_mlp_gather(b["cfg"], d["x"], up(row_token), up(offsets), weights_arg(d), h2, yd2, b["ws"],
+                               tok_row=up(tok_row), topk_w=up(wt32))
+    assert torch.equal(h2, h1)
+    w_row = np.empty(R, dtype=np.float32)
+    w_row[tok_row.ravel()] = wt32.ravel()
+    u = np_of(yd1).astype(np.float64)
+    g = np_of(yd2).astype(np.float64)
+    expect = w_row[:, None].astype(np.float64) * u[:R]
+    assert np.all(np.abs(g[:R] - expect) <= 2.0 ** -7 * 1.01 * np.abs(expect) + 1e-30)
+    assert np.array_equal(g[R:], u[R:])
+    y = torch.empty((T, H), dtype=tdtype(w), device="cuda")
+    moe.moe_combine(b["cfg"], yd2, up(tok_row), None, y)
+    ref = oracle.forward(w, inp, logits=logits)
+    assert oracle.rel_l2(np_of(y).astype(np.float64), ref["y"]) < tol(w)
+    assert moe.moe_read_status(b["ws"]) == moe.MOE_OK

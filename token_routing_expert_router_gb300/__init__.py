@@ -111,7 +111,7 @@ def lib():
             "moe_dispatch_backward": [cfg, P, P, P, P],
             "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
-            "moe_grouped_mlp_gather": [cfg, P, P, P, wts, P, P, P, P],
+            "moe_grouped_mlp_gather": [cfg, P, P, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
             "moe_forward": [cfg, P, wts, P, P, P, P, P, P],
             "moe_quantize_e4m3": [P, c_int64, c_int64, c_int32, c_int32, P, P, P],
@@ -231,10 +231,12 @@ def moe_grouped_mlp(cfg, xd, xd_scale, x, offsets, weights: dict, h, h_scale, yd
                                  _stream(stream)), "moe_grouped_mlp")
 
 
-def moe_grouped_mlp_gather(cfg, x, row_token, offsets, weights: dict, h, yd, ws, stream=None):
+def moe_grouped_mlp_gather(cfg, x, row_token, offsets, weights: dict, h, yd, ws, stream=None,
+                           tok_row=None, topk_w=None):
+    """tok_row and topk_w (both or neither): the routing weights applied in GEMM2's epilogue."""
     w = MoEWeights.from_tensors(weights)
-    _check(lib().moe_grouped_mlp_gather(byref(cfg), _ptr(x), _ptr(row_token), _ptr(offsets), byref(w),
-                                        _ptr(h), _ptr(yd), _ptr(ws), _stream(stream)),
+    _check(lib().moe_grouped_mlp_gather(byref(cfg), _ptr(x), _ptr(row_token), _ptr(offsets), _ptr(tok_row),
+                                        _ptr(topk_w), byref(w), _ptr(h), _ptr(yd), _ptr(ws), _stream(stream)),
            "moe_grouped_mlp_gather")
 
 

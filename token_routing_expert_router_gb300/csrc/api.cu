@@ -344,10 +344,11 @@ moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const void
 }
 
 moe_status_t moe_grouped_mlp_gather(const moe_config_t* cfg, const void* x, const int32_t* row_token,
-                                    const int32_t* offsets, const moe_weights_t* w, void* h, void* yd,
-                                    void* ws, moe_stream_t stream) {
+                                    const int32_t* offsets, const int32_t* tok_row, const float* topk_w,
+                                    const moe_weights_t* w, void* h, void* yd, void* ws, moe_stream_t stream) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
+  if ((tok_row == nullptr) != (topk_w == nullptr)) return MOE_ERR_INVALID_ARG;  // both or neither
   if (cfg->T == 0) return MOE_OK;
   v = check_weights(*cfg, w, false);
   if (v != MOE_OK) return v;
@@ -355,7 +356,7 @@ moe_status_t moe_grouped_mlp_gather(const moe_config_t* cfg, const void* x, cons
     return MOE_ERR_INVALID_ARG;
   if (!fused_gather(*cfg)) return MOE_ERR_UNSUPPORTED;
   return cuda_status(tc::launch_grouped_mlp(*cfg, nullptr, nullptr, x, offsets, *w, h, nullptr, yd, status_of(ws),
-                                            (cudaStream_t)stream, row_token));
+                                            (cudaStream_t)stream, row_token, tok_row, topk_w));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t* tok_row,
@@ -363,7 +364,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (cfg->T == 0) return MOE_OK;
-  if (!ptr_ok(yd) || !ptr_ok(tok_row) || !ptr_ok(topk_w) || !ptr_ok(y)) return MOE_ERR_INVALID_ARG;
+  // topk_w NULL: unit weights (rows already weighted by moe_grouped_mlp_gather)
+  if (!ptr_ok(yd) || !ptr_ok(tok_row) || (topk_w != nullptr && !ptr_ok(topk_w)) || !ptr_ok(y))
+    return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_combine(*cfg, yd, tok_row, topk_w, y, (cudaStream_t)stream));
 }
 

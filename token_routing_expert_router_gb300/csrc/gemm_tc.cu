@@ -47,6 +47,13 @@ struct TcParams {
   const float* bias;        // EPI_STORE_F32_BIAS: [N] or null
   const int32_t* row_token; // non-null: routed A rows are gathered, row r = token row_token[r]
                             //   of tmA (a one-row-box map of x); else tmA holds the rows
+  // EPI_STORE_BF16 with w_topk non-null: routed row r is scaled by its routing weight
+  // w_topk[t * w_k + j] before rounding, t = w_row_token[r] and j the slot with
+  // w_tok_row[t * w_k + j] == r (the routing weight applied in the down projection's epilogue)
+  const int32_t* w_row_token;
+  const int32_t* w_tok_row;
+  const float* w_topk;
+  int w_k;
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
@@ -346,6 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (EPI == EPI_STORE_BF16 || EPI == EPI_STORE_GU) {
         uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
+        float rw = 1.0f;  // this lane's row weight (1 unless the routing weight is applied here)
+        if (EPI == EPI_STORE_BF16 && p.w_topk != nullptr && !extra && live) {
+          const int t = p.w_row_token[out_row];
+          for (int j = 0; j < p.w_k; ++j)
+            if (p.w_tok_row[(int64_t)t * p.w_k + j] == out_row) rw = p.w_topk[(int64_t)t * p.w_k + j];
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
@@ -354,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            const __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(rw * __uint_as_float(v[2 * i]), rw * __uint_as_float(v[2 * i + 1]));
             packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
 #pragma unroll
@@ -549,7 +563,8 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
 
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale, const void* x,
                                const int32_t* offsets, const moe_weights_t& w, void* h, float* h_scale, void* yd,
-                               DeviceStatus* st, cudaStream_t s, const int32_t* row_token) {
+                               DeviceStatus* st, cudaStream_t s, const int32_t* row_token, const int32_t* tok_row,
+                               const float* topk_w) {
   if (c.xfer_dtype == MOE_DTYPE_E4M3)
     return launch_grouped_mlp_fp8(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
   const int64_t R = routed_rows(c), rows = total_rows(c);
@@ -600,6 +615,12 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   if (!ok) return cudaErrorInvalidValue;
   p.a2_row_base = (int)R;
   p.row_token = nullptr;
+  if (topk_w != nullptr) {  // routing weights in GEMM2's epilogue (row_token and tok_row given)
+    p.w_row_token = row_token;
+    p.w_tok_row = tok_row;
+    p.w_topk = topk_w;
+    p.w_k = c.k;
+  }
   p.K = c.F;
   p.n_tiles = c.H / bn2;
   p.b_group_rows = c.H;

@@ -14,11 +14,13 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
                           const float* bias, float* logits, DeviceStatus* st, cudaStream_t s);
 
 // row_token non-null (bf16 only): GEMM1 gathers its routed A rows from x by token instead
-// of reading dispatched rows from xd (xd unused).
+// of reading dispatched rows from xd (xd unused). topk_w non-null (with row_token and
+// tok_row): GEMM2 scales each routed row of yd by its routing weight before rounding.
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
                                const void* x, const int32_t* offsets, const moe_weights_t& w,
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
-                               cudaStream_t s, const int32_t* row_token = nullptr);
+                               cudaStream_t s, const int32_t* row_token = nullptr,
+                               const int32_t* tok_row = nullptr, const float* topk_w = nullptr);
 
 // Backward of the grouped expert MLP (bf16). gu [R(+T), 2F] (g and u in 128-column blocks,
 // as the gate/up GEMM's tiles hold them); dgu the same columns and h [., F] with each
