@@ -339,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q < 7) tmem_ld16(t + col_of(q + 1, half), v[(q + 1) & 1]);
             const float f = (q < 4) ? fa : fb;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              acc[16 * q + i] = __fmaf_rn(__uint_as_float(v[q & 1][i]), f, acc[16 * q + i]);
+            for (int i = 0; i < 16; i += 2)
+              fma2(acc[16 * q + i], acc[16 * q + i + 1], __uint_as_float(v[q & 1][i]),
+                   __uint_as_float(v[q & 1][i + 1]), f);
             tmem_ld_wait();
             if (q == 6) {  // every chunk of this buffer has been read: hand it back to the MMA
               tc_fence_before();

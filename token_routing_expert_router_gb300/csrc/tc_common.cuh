@@ -291,6 +291,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// (a0, a1) += (x0, x1) * f as one packed two-lane fp32 FMA (fma.rn.f32x2): each lane is
+// rounded on its own, so the result is bit-identical to two fmaf calls at half the issue cost.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float f) {
+  asm("{\n\t.reg .b64 a, x, s;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 s, {%4, %4};\n\t"
+      "fma.rn.f32x2 a, x, s, a;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(f));
+}
+
 // A warp's 32 rows x 64 bytes, staged in shared memory so that the global stores are
 // coalesced: each thread puts its own row's four 16-byte pieces in (stage_piece), then
 // each store instruction of flush_rows_64B writes 8 rows x 64 contiguous bytes. Piece c of
