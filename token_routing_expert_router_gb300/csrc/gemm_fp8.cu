@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_before();
               __syncwarp();    // all lanes' loads are complete: one arrival per warp
               if (lane == 0) {
-                if (CG == 2 && !leader) mbar_arrive_cluster(pempty_leader + pb * 8);
-                else mbar_arrive(&pempty[pb]);
+                if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(pempty_leader + pb * 8);
+                else mbar_arrive_relaxed(&pempty[pb]);
               }
             }
           }

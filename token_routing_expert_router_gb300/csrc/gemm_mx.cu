@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();  // every lane's loads are complete: one arrival per warp
       if (lane == 0) {
-        if (CG == 2 && !leader) mbar_arrive_cluster(acc_empty_leader);
-        else mbar_arrive(acc_empty);
+        if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(acc_empty_leader);
+        else mbar_arrive_relaxed(acc_empty);
       }
 
       const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];

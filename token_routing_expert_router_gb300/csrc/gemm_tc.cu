@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      if (CG == 2 && !leader) mbar_arrive_cluster(tempty_leader + acc * 8);
-      else mbar_arrive(&tempty[acc]);
+      if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+      else mbar_arrive_relaxed(&tempty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
