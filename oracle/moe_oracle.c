@@ -78,9 +78,10 @@ void oc_det_expf_array(const float* a, float* out, int64_t n) {
 
 /* ------------------------------------------------------------------------------------ */
 /* S0: router logits. l[t,e] = sum_h x[t,h] * Wr[e,h] (+ b[e]) accumulated in fp64 from   */
-/* the stored values, rounded once to fp32. The router "scores each token against the    */
-/* experts" (P1 "O essencial"; BASELINE router weights ~N(0,0.02)). b is the optional     */
-/* per-expert additive bias of the imbalanced workload.                                   */
+/* the stored values, rounded once to fp32: the router gives every token one score per   */
+/* expert (Megatron-Core summary, section "O essencial"); the synthetic router weights    */
+/* are drawn N(0, 0.02^2). b is the optional per-expert additive bias of the imbalanced   */
+/* workload.                                                                              */
 /* ------------------------------------------------------------------------------------ */
 void oc_router_logits(const float* x, const float* wr, const float* bias, int T, int H, int E,
                       float* logits) {
@@ -203,8 +204,9 @@ int oc_group_scores(const float* l, int E, int n_groups, int group_score, float*
 /* ------------------------------------------------------------------------------------ */
 /* S2: per-expert counts, offsets and the permutation. counts[e] = #{(t,j): idx=e};        */
 /* offsets = exclusive prefix sum (offsets[E] = T*k); within expert e the rows hold the    */
-/* tokens that chose e in ascending token id ("the routing map" of the Hybrid-EP article;  */
-/* the stable order is the reading taken). row_token[r] = t, tok_row[t*k+j] = r.           */
+/* tokens that chose e in ascending token id (the routing map of the Hybrid-EP article,  */
+/* whose order the pages leave open; the stable order is the reading taken).              */
+/* row_token[r] = t, tok_row[t*k+j] = r.                                                  */
 /* Returns 0, or -1 if an expert id is outside [0, E).                                    */
 /* ------------------------------------------------------------------------------------ */
 int oc_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
@@ -230,8 +232,8 @@ int oc_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, in
 }
 
 /* ------------------------------------------------------------------------------------ */
-/* S3: dispatch, xd[r] = x[row_token[r]] (the dispatch operator "directs the tokens to    */
-/* the corresponding experts", Hybrid-EP article). Bit copy.                              */
+/* S3: dispatch, xd[r] = x[row_token[r]] (the Hybrid-EP article's dispatch operator, which */
+/* moves each token to the experts it was routed to). Bit copy.                           */
 /* ------------------------------------------------------------------------------------ */
 void oc_dispatch(const float* x, int H, const int32_t* row_token, int64_t nrows, float* xd) {
 #pragma omp parallel for schedule(static)
@@ -281,9 +283,10 @@ void oc_e4m3_encode_array(const float* f, uint8_t* out, int64_t n) {
 }
 
 /* Block quantisation with fp32 scales (the FP8-dispatch variant: tokens in 1x128 blocks,  */
-/* weights in 128x128 blocks; the pages name FP8 dispatch and FP8/FP4 training, BASELINE   */
-/* fixes the block shapes). Per block: amax = max |v| (exact); if amax == 0 the scale is 1 */
-/* and every code is 0; else scale = amax / 448 and q = e4m3(v * (448 / amax)), each       */
+/* weights in 128x128 blocks; the pages name FP8 dispatch and FP8/FP4 training but no     */
+/* block shape, and these are the reading taken). Per block: amax = max |v| (exact); if    */
+/* amax == 0 the scale is 1 and every code is 0; else scale = amax / 448 and              */
+/* q = e4m3(v * (448 / amax)), each                                                       */
 /* division and the product one correctly rounded fp32 operation. The value the block      */
 /* stands for is decode(q) * scale. scale is [rows/br][cols/bc] row-major.                 */
 void oc_quant_blocks(const float* v, int64_t rows, int64_t cols, int br, int bc, uint8_t* q,
@@ -371,8 +374,9 @@ void oc_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t co
 }
 
 /* ------------------------------------------------------------------------------------ */
-/* S4 + S5: one expert's SwiGLU MLP on a set of rows, fp64 ("the experts' GEMMs" of the    */
-/* grouped GEMM; SwiGLU from the workload definition):                                    */
+/* S4 + S5: one expert's SwiGLU MLP on a set of rows, fp64 (one expert's share of the     */
+/* grouped GEMM of the Megatron-Core summary, section 2.4; SwiGLU from the workload       */
+/* definition):                                                                           */
 /*   g = a . Wg^T,  u = a . Wu^T,  h = g / (1 + e^-g) * u,  y = h . Wd^T.                 */
 /* a is [n, H], Wg/Wu [F, H], Wd [H, F] (all fp64 values). quant_h 1: h is rounded to     */
 /* fp32 and requantised in 1x128 blocks as the FP8-dispatch variant does before the down   */
@@ -421,9 +425,10 @@ void oc_expert_mlp(const double* a, int64_t n, int H, int F, const double* wg, c
 
 /* ------------------------------------------------------------------------------------ */
 /* S7: combine. y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ ys[t], the shared expert's row) */
-/* in fp64, w already holding the routed scale: the combine operator "sends the tokens     */
-/* back" with high-precision accumulation (Hybrid-EP article); dropless, every token gets  */
-/* all k rows (Megatron-Core summary, dropless MoE). ys may be NULL.                       */
+/* in fp64, w already holding the routed scale: the Hybrid-EP article's combine operator */
+/* returns the expert outputs to token order and accumulates them in high precision;     */
+/* dropless, every token gets all k rows (Megatron-Core summary, dropless MoE). ys may    */
+/* be NULL.                                                                               */
 /* ------------------------------------------------------------------------------------ */
 void oc_combine(const double* yd, const int32_t* tok_row, const double* w, const double* ys,
                 int T, int k, int H, double* y) {

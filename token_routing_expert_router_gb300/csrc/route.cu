@@ -2,7 +2,7 @@
 // and the stable permutation) of the MoE layer forward.
 //
 // The router activates k experts per token ("Scalable Training of Mixture-of-Experts Models
-// with Megatron Core" summary, "O essencial"); the dispatch follows "the routing map"
+// with Megatron Core" summary, "O essencial"); the dispatch follows the routing map
 // (Hybrid-EP article); the per-expert shapes stay in device memory so no host sync is
 // needed (Megatron-Core summary, section 2.4, device-initiated kernels).
 #include <float.h>
