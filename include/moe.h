@@ -19,6 +19,7 @@
  *   moe_grouped_mlp     S4-S6  per expert: h = silu(xd Wg^T) * (xd Wu^T); yd = h Wd^T
  *   moe_combine         S7  y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ shared row)
  *   moe_forward         S0-S7 in one stream-ordered call
+ *   moe_forward_host    the same with the tokens and the output in host memory
  *   moe_backward        the training step's backward of S3-S7 (bf16 layers): combine,
  *                       the experts' grouped dgrad/wgrad with recomputed SwiGLU, dispatch
  *
@@ -255,6 +256,17 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                          void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
                          int32_t* counts_out, moe_stream_t stream);
+
+/* S0..S7 with the tokens and the output in host memory: x_host [T,H] is copied to x_dev,
+ * moe_forward runs on it into y_dev, and y_dev is copied back to y_host, all three steps
+ * stream-ordered on `stream`, so a caller can run the copies of one call under the kernels
+ * of another issued on a second stream (with its own ws, x_dev and y_dev). x_host and y_host
+ * are host memory; page-locked memory keeps the copies asynchronous (with pageable memory
+ * the results are the same but the copies block the calling thread). x_dev, y_dev: device
+ * buffers of T*H act-dtype elements, 16-byte aligned; ws as for moe_forward. The library
+ * allocates nothing. Bit-identical to the copies around moe_forward. */
+moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host, const moe_weights_t* w,
+                              void* y_host, void* x_dev, void* y_dev, void* ws, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Backward (a training step; bf16 layers on the tensor-core path, H % 256 == 0 and

@@ -82,6 +82,11 @@ def test_null_and_misaligned_pointers_rejected_on_host(L):
     assert L.moe_dispatch(ctypes.byref(c), P(4096 + 8), P(4096), P(4096), None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(c), P(4096), None, P(4096), P(4096), None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(c), P(4096), P(4096), P(4096 + 4), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    # host-buffer forward: host pointers must be given, device staging 16-byte aligned
+    assert L.moe_forward_host(ctypes.byref(c), None, None, P(4096), P(4096), P(4096), P(4096),
+                              None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_host(ctypes.byref(c), P(4096), None, P(4096), P(4096 + 8), P(4096), P(4096),
+                              None) == moe.MOE_ERR_INVALID_ARG
     # the routing-weight epilogue takes tok_row and topk_w together or not at all
     assert L.moe_grouped_mlp_gather(ctypes.byref(c), P(4096), P(4096), P(4096), P(4096), None, None, P(4096),
                                     P(4096), P(4096), None) == moe.MOE_ERR_INVALID_ARG

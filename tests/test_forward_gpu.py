@@ -108,3 +108,30 @@ def test_forward_graph_capture():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(y, y_ref)
+
+
+@pytest.mark.parametrize("w", [CASES[1], CASES[4], CASES[9]], ids=["mixtral_small", "fp8_small", "mxfp8_small"])
+def test_forward_host_equals_forward(w):
+    """moe_forward_host (host tokens in, host output back) gives the bits of moe_forward, also
+    with two calls in flight on two streams, each with its own workspace and staging."""
+    inp = synth.host_inputs(w, seed=14)
+    d = device_weights_from_host(w, inp)
+    y_ref, *_ = run_forward(w, d)
+    from moe_case import weights_arg
+    cfg = cfg_of(w)
+    T, H = w["T"], w["H"]
+    xh = d["x"].cpu().pin_memory()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for s in streams:
+        ws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+        moe.moe_workspace_init(ws)
+        yh = torch.full((T, H), 7, dtype=y_ref.dtype).pin_memory()
+        outs.append((ws, torch.empty_like(d["x"]), torch.empty_like(y_ref), yh, s))
+    torch.cuda.synchronize()
+    for ws, xdev, ydev, yh, s in outs:
+        moe.moe_forward_host(cfg, xh, weights_arg(d), yh, xdev, ydev, ws, stream=s)
+    torch.cuda.synchronize()
+    for ws, xdev, ydev, yh, s in outs:
+        assert torch.equal(yh, y_ref.cpu())
+        assert moe.moe_read_status(ws) == moe.MOE_OK

@@ -114,6 +114,7 @@ def lib():
             "moe_grouped_mlp_gather": [cfg, P, P, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
             "moe_forward": [cfg, P, wts, P, P, P, P, P, P],
+            "moe_forward_host": [cfg, P, wts, P, P, P, P, P],
             "moe_quantize_e4m3": [P, c_int64, c_int64, c_int32, c_int32, P, P, P],
             "moe_read_status": [P, P, POINTER(c_int32)],
             "moe_route_static_scratch": [cfg, P, P, P, P, P, P, P, P, P],
@@ -132,7 +133,8 @@ def lib():
 def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
             "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
-            "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_quantize_e4m3",
+            "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_forward_host",
+            "moe_quantize_e4m3",
             "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
             "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_mlp_backward",
             "moe_dispatch_backward", "moe_backward",
@@ -147,6 +149,14 @@ def _ptr(t):
         return t
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return t.data_ptr()
@@ -250,6 +260,14 @@ def moe_forward(cfg, x, weights: dict, y, ws, topk_idx_out=None, topk_w_out=None
     w = MoEWeights.from_tensors(weights)
     _check(lib().moe_forward(byref(cfg), _ptr(x), byref(w), _ptr(y), _ptr(ws), _ptr(topk_idx_out),
                              _ptr(topk_w_out), _ptr(counts_out), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(cfg, x_host, weights: dict, y_host, x_dev, y_dev, ws, stream=None):
+    """The layer on host tokens: x_host -> x_dev, moe_forward, y_dev -> y_host, stream-ordered
+    (pin the host tensors to keep the copies asynchronous)."""
+    w = MoEWeights.from_tensors(weights)
+    _check(lib().moe_forward_host(byref(cfg), _host_ptr(x_host), byref(w), _host_ptr(y_host), _ptr(x_dev),
+                                  _ptr(y_dev), _ptr(ws), _stream(stream)), "moe_forward_host")
 
 
 def moe_quantize_e4m3(src, br: int, bc: int, q, scale, stream=None):

@@ -422,6 +422,21 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
   return cuda_status(e);
 }
 
+moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host, const moe_weights_t* w,
+                              void* y_host, void* x_dev, void* y_dev, void* ws, moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (x_host == nullptr || y_host == nullptr || !ptr_ok(x_dev) || !ptr_ok(y_dev)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  const size_t bytes = (size_t)cfg->T * cfg->H * act_size(*cfg);
+  cudaStream_t s = (cudaStream_t)stream;
+  v = cuda_status(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s));
+  if (v != MOE_OK) return v;
+  v = moe_forward(cfg, x_dev, w, y_dev, ws, nullptr, nullptr, nullptr, stream);
+  if (v != MOE_OK) return v;
+  return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, s));
+}
+
 moe_status_t moe_quantize_e4m3(const void* src_bf16, int64_t rows, int64_t cols, int32_t br,
                                int32_t bc, uint8_t* q, float* scale, moe_stream_t stream) {
   if (!ptr_ok(src_bf16) || !ptr_ok(q) || !ptr_ok(scale) || rows < 0 || cols < 0)
