@@ -51,36 +51,66 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 }
 
 // FP8 dispatch: each token quantised once in 1x128 blocks (one warp per block, four values
-// per lane), written to its k rows and, with a shared expert, to row R + t.
-__global__ void __launch_bounds__(256) dispatch_e4m3_kernel(
+// per lane), written to its k rows and, with a shared expert, to row R + t. A pass covers
+// 8 warps x kFp8Blocks blocks: each warp issues the loads of its kFp8Blocks blocks before
+// quantising any, so several 256-byte loads per warp are in flight; the pass's scales go
+// through shared memory and leave with all threads storing, one row's scales per group of
+// lanes, instead of one lane per warp issuing a store per block and row.
+constexpr int kFp8Blocks = 8;
+constexpr int kFp8Warps = 8;
+__global__ void __launch_bounds__(32 * kFp8Warps) dispatch_e4m3_kernel(
     const uint2* __restrict__ x, int H, int k, int64_t R, int64_t rows_total, int shared,
     const int32_t* __restrict__ tok_row, uint8_t* __restrict__ xd, float* __restrict__ xd_scale) {
+  constexpr int kPass = kFp8Warps * kFp8Blocks;  // blocks per pass
   __shared__ int32_t rows[33];
+  __shared__ float sc_s[kPass];
   const int t = blockIdx.x;
   const int nrows = k + shared;
   if (threadIdx.x < k) rows[threadIdx.x] = tok_row[(int64_t)t * k + threadIdx.x];
   if (threadIdx.x == 0 && shared) rows[k] = (int32_t)(R + t);
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = H / 128;
-  for (int b = warp; b < nb; b += nwarps) {
-    const uint2 u = __ldg(x + ((int64_t)t * H + b * 128) / 4 + lane);
-    const float v0 = bf16_lo(u.x), v1 = bf16_hi(u.x), v2 = bf16_lo(u.y), v3 = bf16_hi(u.y);
-    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  for (int p0 = 0; p0 < nb; p0 += kPass) {  // block-uniform trip count
+    uint2 u[kFp8Blocks];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    float scale = 1.0f;
-    uint32_t q = 0;
-    if (amax > 0.0f) {
-      scale = __fdiv_rn(amax, 448.0f);
-      const float rs = __fdiv_rn(448.0f, amax);
-      q = e4m3x4(__fmul_rn(v0, rs), __fmul_rn(v1, rs), __fmul_rn(v2, rs), __fmul_rn(v3, rs));
+    for (int i = 0; i < kFp8Blocks; ++i) {
+      const int b = p0 + i * kFp8Warps + warp;
+      if (b < nb) u[i] = __ldg(x + ((int64_t)t * H + b * 128) / 4 + lane);
+    }
+    uint32_t q[kFp8Blocks];
+#pragma unroll
+    for (int i = 0; i < kFp8Blocks; ++i) {
+      q[i] = 0;
+      const int b = p0 + i * kFp8Warps + warp;
+      if (b >= nb) continue;  // warp-uniform
+      const float v0 = bf16_lo(u[i].x), v1 = bf16_hi(u[i].x), v2 = bf16_lo(u[i].y), v3 = bf16_hi(u[i].y);
+      float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      float scale = 1.0f;
+      if (amax > 0.0f) {
+        scale = __fdiv_rn(amax, 448.0f);
+        const float rs = __fdiv_rn(448.0f, amax);
+        q[i] = e4m3x4(__fmul_rn(v0, rs), __fmul_rn(v1, rs), __fmul_rn(v2, rs), __fmul_rn(v3, rs));
+      }
+      if (lane == 0) sc_s[b - p0] = scale;
     }
     for (int j = 0; j < nrows; ++j) {
       const int64_t r = rows[j];
-      reinterpret_cast<uint32_t*>(xd + r * H + b * 128)[lane] = q;
-      if (lane == 0) xd_scale[(int64_t)b * rows_total + r] = scale;
+#pragma unroll
+      for (int i = 0; i < kFp8Blocks; ++i) {
+        const int b = p0 + i * kFp8Warps + warp;
+        if (b < nb) reinterpret_cast<uint32_t*>(xd + r * H + b * 128)[lane] = q[i];
+      }
     }
+    __syncthreads();
+    const int npass = min(kPass, nb - p0);
+    for (int i = threadIdx.x; i < nrows * npass; i += blockDim.x) {
+      const int j = i / npass, bb = i - j * npass;
+      xd_scale[(int64_t)(p0 + bb) * rows_total + rows[j]] = sc_s[bb];
+    }
+    __syncthreads();  // sc_s is rewritten by the next pass
   }
 }
 
@@ -150,15 +180,38 @@ __global__ void __launch_bounds__(256) dispatch_mx_kernel(
   __syncthreads();
   const int nb = H / 32;
   uint8_t* code_bytes = reinterpret_cast<uint8_t*>(codes);
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    float v[32];
-    load_bf16x32(x + ((int64_t)t * H + b * 32) / 8, v);
-    uint4 q[2];
-    code_bytes[b] = (uint8_t)mx_quant_block(v, q);
-    for (int j = 0; j < nrows; ++j) {
-      uint4* dst = reinterpret_cast<uint4*>(xd + rows[j] * H + b * 32);
-      dst[0] = q[0];
-      dst[1] = q[1];
+  const int lane = threadIdx.x & 31;
+  // Every warp quantises 32 consecutive blocks (H % 128 == 0 keeps a warp's blocks all
+  // inside the row or all past it); the two 16-byte halves of the blocks are then traded
+  // between lanes so that each store instruction writes 512 contiguous bytes.
+  for (int b = threadIdx.x; b - lane < nb; b += blockDim.x) {
+    const bool live = b < nb;
+    uint4 q[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (live) {
+      float v[32];
+      load_bf16x32(x + ((int64_t)t * H + b * 32) / 8, v);
+      code_bytes[b] = (uint8_t)mx_quant_block(v, q);
+    }
+    // store s (0, 1) of this warp covers its blocks 16 s .. 16 s + 15: lane l writes half
+    // l % 2 of block 16 s + l / 2, which lane 16 s + l / 2 holds
+    uint4 o[2];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const int src = 16 * st + (lane >> 1);
+      const uint4 h0 = make_uint4(__shfl_sync(0xffffffffu, q[0].x, src), __shfl_sync(0xffffffffu, q[0].y, src),
+                                  __shfl_sync(0xffffffffu, q[0].z, src), __shfl_sync(0xffffffffu, q[0].w, src));
+      const uint4 h1 = make_uint4(__shfl_sync(0xffffffffu, q[1].x, src), __shfl_sync(0xffffffffu, q[1].y, src),
+                                  __shfl_sync(0xffffffffu, q[1].z, src), __shfl_sync(0xffffffffu, q[1].w, src));
+      o[st] = (lane & 1) ? h1 : h0;
+    }
+    const int wb0 = b - lane;  // the warp's first block
+    if (wb0 < nb) {
+      for (int j = 0; j < nrows; ++j) {
+        uint4* dst = reinterpret_cast<uint4*>(xd + rows[j] * H + wb0 * 32);
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          if (wb0 + 16 * st + (lane >> 1) < nb) dst[32 * st + lane] = o[st];
+      }
     }
   }
   __syncthreads();
@@ -264,12 +317,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const void* __restric
 
 // Same sum with the row count NR = k (+1 shared) known at compile time: every row's
 // 16-byte vector of a chunk is loaded before any of them is summed, so one memory round
-// trip covers all NR rows. The shared row enters with weight 1 (fma(1, v, acc) == acc + v).
+// trip covers all NR rows. With few rows, each thread takes U chunks per pass and issues
+// all NR * U loads first, so about eight 16-byte loads are in flight per thread whatever k
+// is. The shared row enters with weight 1 (fma(1, v, acc) == acc + v).
 template <int NR, bool BF16>
 __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __restrict__ yd_, int H, int k,
                                                               const int32_t* __restrict__ tok_row,
                                                               const float* __restrict__ topk_w, int64_t R,
                                                               void* __restrict__ y_) {
+  constexpr int U = NR >= 8 ? 1 : 8 / NR;
   __shared__ int64_t rows[NR];
   __shared__ float wts[NR];
   const int t = blockIdx.x;
@@ -280,53 +336,78 @@ __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __rest
   }
   __syncthreads();
   const int n8 = H / 8;
-  for (int c = threadIdx.x; c < n8; c += kThreads) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int base = threadIdx.x; base < n8; base += kThreads * U) {
     if (BF16) {
-      uint4 raw[NR];
+      uint4 raw[U][NR];
 #pragma unroll
-      for (int j = 0; j < NR; ++j) raw[j] = __ldg(reinterpret_cast<const uint4*>(yd_) + rows[j] * (H / 8) + c);
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * kThreads;
+        if (c < n8) {
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        const float wj = wts[j];
-        const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = __fmaf_rn(wj, bf16_lo(u[q]), acc[2 * q]);
-          acc[2 * q + 1] = __fmaf_rn(wj, bf16_hi(u[q]), acc[2 * q + 1]);
+          for (int j = 0; j < NR; ++j) raw[u][j] = __ldg(reinterpret_cast<const uint4*>(yd_) + rows[j] * n8 + c);
         }
       }
-      uint4 o;
-      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-      o.x = *reinterpret_cast<uint32_t*>(&p0);
-      o.y = *reinterpret_cast<uint32_t*>(&p1);
-      o.z = *reinterpret_cast<uint32_t*>(&p2);
-      o.w = *reinterpret_cast<uint32_t*>(&p3);
-      reinterpret_cast<uint4*>(y_)[(int64_t)t * n8 + c] = o;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * kThreads;
+        if (c >= n8) continue;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const float wj = wts[j];
+          const uint32_t w4[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = __fmaf_rn(wj, bf16_lo(w4[q]), acc[2 * q]);
+            acc[2 * q + 1] = __fmaf_rn(wj, bf16_hi(w4[q]), acc[2 * q + 1]);
+          }
+        }
+        uint4 o;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+        o.x = *reinterpret_cast<uint32_t*>(&p0);
+        o.y = *reinterpret_cast<uint32_t*>(&p1);
+        o.z = *reinterpret_cast<uint32_t*>(&p2);
+        o.w = *reinterpret_cast<uint32_t*>(&p3);
+        reinterpret_cast<uint4*>(y_)[(int64_t)t * n8 + c] = o;
+      }
     } else {
-      float4 raw[NR][2];
+      float4 raw[U][NR][2];
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        const float4* p = reinterpret_cast<const float4*>(yd_) + rows[j] * (H / 4) + 2 * c;
-        raw[j][0] = __ldg(p);
-        raw[j][1] = __ldg(p + 1);
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * kThreads;
+        if (c < n8) {
+#pragma unroll
+          for (int j = 0; j < NR; ++j) {
+            const float4* p = reinterpret_cast<const float4*>(yd_) + rows[j] * (H / 4) + 2 * c;
+            raw[u][j][0] = __ldg(p);
+            raw[u][j][1] = __ldg(p + 1);
+          }
+        }
       }
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        const float wj = wts[j];
-        acc[0] = __fmaf_rn(wj, raw[j][0].x, acc[0]); acc[1] = __fmaf_rn(wj, raw[j][0].y, acc[1]);
-        acc[2] = __fmaf_rn(wj, raw[j][0].z, acc[2]); acc[3] = __fmaf_rn(wj, raw[j][0].w, acc[3]);
-        acc[4] = __fmaf_rn(wj, raw[j][1].x, acc[4]); acc[5] = __fmaf_rn(wj, raw[j][1].y, acc[5]);
-        acc[6] = __fmaf_rn(wj, raw[j][1].z, acc[6]); acc[7] = __fmaf_rn(wj, raw[j][1].w, acc[7]);
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * kThreads;
+        if (c >= n8) continue;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const float wj = wts[j];
+          acc[0] = __fmaf_rn(wj, raw[u][j][0].x, acc[0]); acc[1] = __fmaf_rn(wj, raw[u][j][0].y, acc[1]);
+          acc[2] = __fmaf_rn(wj, raw[u][j][0].z, acc[2]); acc[3] = __fmaf_rn(wj, raw[u][j][0].w, acc[3]);
+          acc[4] = __fmaf_rn(wj, raw[u][j][1].x, acc[4]); acc[5] = __fmaf_rn(wj, raw[u][j][1].y, acc[5]);
+          acc[6] = __fmaf_rn(wj, raw[u][j][1].z, acc[6]); acc[7] = __fmaf_rn(wj, raw[u][j][1].w, acc[7]);
+        }
+        float4* p = reinterpret_cast<float4*>(y_) + ((int64_t)t * H) / 4 + 2 * c;
+        p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
       }
-      float4* p = reinterpret_cast<float4*>(y_) + ((int64_t)t * H) / 4 + 2 * c;
-      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -432,7 +513,7 @@ cudaError_t launch_dispatch(const moe_config_t& c, const void* x, const int32_t*
                             void* xd, float* xd_scale, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   if (c.xfer_dtype == MOE_DTYPE_E4M3) {
-    dispatch_e4m3_kernel<<<c.T, 256, 0, s>>>(reinterpret_cast<const uint2*>(x), c.H, c.k,
+    dispatch_e4m3_kernel<<<c.T, 32 * kFp8Warps, 0, s>>>(reinterpret_cast<const uint2*>(x), c.H, c.k,
                                              routed_rows(c), total_rows(c), c.n_shared ? 1 : 0,
                                              tok_row, reinterpret_cast<uint8_t*>(xd), xd_scale);
   } else {
