@@ -24,6 +24,9 @@ CASES = [
     # >= 512 rows per expert: the recomputed gate/up GEMM runs as CTA pairs
     synth.scaled(W["dsv3_bf16"], T=1200, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2, topk_groups=1,
                  name="pair_shared"),
+    # 192..511 rows per expert: the recomputed gate/up GEMM on two or three m tiles per expert
+    synth.scaled(W["dsv3_bf16"], T=520, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="mid_shared"),
 ]
 TOL = 1e-2  # bf16 layers
 
@@ -108,7 +111,7 @@ def test_backward_against_oracle(w):
         assert oracle.rel_l2(g["dxd"][R:], ref["dxd"][R:]) < TOL
 
 
-@pytest.mark.parametrize("w", [CASES[1], CASES[3]], ids=["dsv3_small", "pair_shared"])
+@pytest.mark.parametrize("w", [CASES[1], CASES[3], CASES[4]], ids=["dsv3_small", "pair_shared", "mid_shared"])
 def test_backward_after_forward_equals_staged(w):
     """moe_backward reads the routing, xd and yd from moe_forward's workspace and runs the
     same kernels as the staged calls: identical bits."""

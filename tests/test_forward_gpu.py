@@ -29,6 +29,9 @@ CASES = [
                  topk_groups=1, name="pair_shared"),
     synth.scaled(W["dsv3_fp8"], T=1100, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
                  topk_groups=1, name="pair_fp8"),
+    # single-CTA tiles with two or three m tiles per expert (192..511 rows per expert)
+    synth.scaled(W["dsv3_bf16"], T=520, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="mid_dsv3"),
     synth.scaled(W["dsv3_mxfp8"], T=256, H=512, E=32, F=256, F_shared=256, name="mxfp8_small"),
     synth.scaled(W["dsv3_mxfp8"], T=900, H=1024, E=8, k=2, F=384, F_shared=384, n_groups=2,
                  topk_groups=1, name="mxfp8_deep_k"),
@@ -110,7 +113,8 @@ def test_forward_graph_capture():
     assert torch.equal(y, y_ref)
 
 
-@pytest.mark.parametrize("w", [CASES[1], CASES[4], CASES[9]], ids=["mixtral_small", "fp8_small", "mxfp8_small"])
+@pytest.mark.parametrize("w", [c for c in CASES if c["name"] in ("mixtral_small", "fp8_small", "mxfp8_small")],
+                         ids=["mixtral_small", "fp8_small", "mxfp8_small"])
 def test_forward_host_equals_forward(w):
     """moe_forward_host (host tokens in, host output back) gives the bits of moe_forward, also
     with two calls in flight on two streams, each with its own workspace and staging."""

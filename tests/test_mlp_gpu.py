@@ -27,6 +27,12 @@ CASES = [
                  topk_groups=1, name="pair_shared"),
     synth.scaled(W["dsv3_fp8"], T=1100, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2,
                  topk_groups=1, name="pair_fp8"),
+    # 192..511 rows per expert on average: single-CTA tiles, two or three m tiles per expert
+    # (full 128-row tiles, M = 64 tails), hot and empty experts
+    synth.scaled(W["dsv3_bf16"], T=520, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="mid_dsv3"),
+    synth.scaled(W["mixtral_bf16"], T=1060, H=512, E=8, F=384, name="mid_mixtral"),
+    synth.scaled(W["imbalanced_bf16"], T=800, H=256, E=16, k=4, F=256, name="mid_imbalanced"),
 ]
 
 
