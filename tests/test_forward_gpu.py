@@ -37,6 +37,15 @@ CASES = [
                  topk_groups=1, name="mxfp8_deep_k"),
     synth.scaled(W["dsv3_mxfp8"], T=1300, H=768, E=4, k=2, F=640, F_shared=640, n_groups=2,
                  topk_groups=1, name="mxfp8_pair"),
+    # degenerate layers: one token (a one-row tile per chosen expert), every expert chosen
+    # by every token with H = 384 (down-projection tiles of 128 columns, 6 K blocks), and
+    # the FP8 variants on one and three tokens
+    synth.scaled(W["mixtral_bf16"], T=1, H=512, E=8, F=256, name="one_token"),
+    synth.scaled(W["mixtral_bf16"], T=100, H=384, E=4, k=4, F=128, name="k_eq_e_h384"),
+    synth.scaled(W["dsv3_fp8"], T=1, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="fp8_one_token"),
+    synth.scaled(W["dsv3_mxfp8"], T=3, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
+                 name="mxfp8_three_tokens"),
 ]
 
 
