@@ -37,13 +37,11 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kABytes = BM * BK;
 constexpr int kTmemCols = 512;  // two 256-column partial accumulators
 
-// Shared memory of one CTA: CG = 2 (a CTA pair) holds half of the tile's B rows, so a stage
-// is 32 KB and six stages fit instead of four.
-template <int CG>
+// Shared memory of one CTA: four 48 KB stages (A 16 KB + B 32 KB).
 struct F8Smem {
-  static constexpr int kBBytes = BN * BK / CG;
+  static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
+  static constexpr int kStages = 4;
   static constexpr size_t kBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * BM * sizeof(float) +
                                    2 * kMaxGroups * sizeof(int32_t) + (kEpiThreads / 32) * 2048 /*store staging*/;
 };
@@ -109,15 +107,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-template <int EPI, int CG>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmB1x,
                        const Fp8Params p) {
-  using S = F8Smem<CG>;
+  using S = F8Smem;
   constexpr int kStages = S::kStages, kBBytes = S::kBBytes, kStageBytes = S::kStageBytes;
-  constexpr int TM = BM * CG;  // rows of an m tile
+  constexpr int TM = BM;  // rows of an m tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -138,9 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
   auto col_of = [](int q, int half) { return col_of_t<EPI>(q, half); };
-  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
-  const bool leader = rank == 0;
-  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
+  const int unit = blockIdx.x, nunits = gridDim.x;  // persistent tile walkers
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -149,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&pfull[a], 1);
-      mbar_init(&pempty[a], (kEpiThreads / 32) * CG);  // one arrival per epilogue warp
+      mbar_init(&pempty[a], kEpiThreads / 32);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -159,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
   }
-  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_cg<1>(tmem_slot, kTmemCols);
   if (warp == 2) {
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
@@ -184,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.n_tiles * mt_prefix[ngroups];
@@ -203,30 +198,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* ta = extra ? &tmA2 : &tmA;
         const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
         const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
-        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
+        const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM;
         const int b_tile_rows = EPI == FP8_SWIGLU_Q8 ? BN / 2 : BN;
-        int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
-        if (CG == 2 && EPI != FP8_SWIGLU_Q8) b_row += (int)rank * (BN / 2);
-        const CUtensorMap* tb_mine = (CG == 2 && EPI == FP8_SWIGLU_Q8 && rank == 1) ? tb1 : tb0;
+        const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
-          if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
-            if (EPI == FP8_SWIGLU_Q8) {
-              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-              tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
-            } else {
-              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-            }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+          if (EPI == FP8_SWIGLU_Q8) {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
           } else {
-            // both CTAs' loads complete on the leader's barrier, which expects both
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
-            tma_load_2d_pair(ta, a_dst, bar, kb * BK, a_row);
-            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row);
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -237,12 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (stage - 1 - i + 2 * kStages) % kStages;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer: one partial accumulator per K block
-    if (lane == 0 && leader) {
+    if (lane == 0) {
       constexpr uint32_t idesc = idesc_make(0u /*e4m3*/, TM, BN);
       int stage = 0;
       uint32_t phase = 0;
@@ -258,28 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
           const uint32_t d_tmem = tmem_base + pb * BN;
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {  // K = 32 e4m3 per instruction: +32 bytes
-            if constexpr (CG == 1)
-              mma_f8(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
-            else
-              mma_f8_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
-          }
-          if constexpr (CG == 1) {
-            mma_commit(&empty[stage]);
-            mma_commit(&pfull[pb]);
-          } else {  // both CTAs' stage and partial barriers
-            mma_commit_pair(&empty[stage], 0x3);
-            mma_commit_pair(&pfull[pb], 0x3);
-          }
+          for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction: +32 bytes
+            mma_f8(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc, k != 0);
+          mma_commit(&empty[stage]);
+          mma_commit(&pfull[pb]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
           if (++pb == 2) { pb = 0; pphase ^= 1; }
         }
       }
-      if constexpr (CG == 1) mma_commit(drain);
-      else mma_commit_pair(drain, 0x3);
-      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
-    } else if (lane == 0 && CG == 2) {
-      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
+      mma_commit(drain);
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -292,11 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pphase = 0;
     int tile_parity = 0;
     bool ok = true;
-    const uint32_t pempty_leader = CG == 2 ? mapa_shared(smem_addr(&pempty[0]), 0) : 0;
     for (int tile = unit; tile < total_tiles; tile += nunits, tile_parity ^= 1) {
       const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
       const bool extra = c.g >= p.G;
-      const int row_in_tile = (int)rank * BM + r;
+      const int row_in_tile = r;
       const int64_t a_row = (extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
       const int64_t a_row_c = a_row < p.rows_total ? a_row : p.rows_total - 1;  // dead rows: any scale
       const float* sb0 = (extra ? p.b0x_scale : p.b0_scale + (int64_t)c.g * p.nblk_b * kblocks);
@@ -346,10 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 6) {  // every chunk of this buffer has been read: hand it back to the MMA
               tc_fence_before();
               __syncwarp();    // all lanes' loads are complete: one arrival per warp
-              if (lane == 0) {
-                if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(pempty_leader + pb * 8);
-                else mbar_arrive_relaxed(&pempty[pb]);
-              }
+              if (lane == 0) mbar_arrive_relaxed(&pempty[pb]);
             }
           }
         }
@@ -415,11 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc_cg<CG>(tmem_base, kTmemCols);
+    tmem_dealloc_cg<1>(tmem_base, kTmemCols);
   }
 }
 
@@ -427,46 +394,21 @@ bool make_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, box_rows, BK);
 }
 
-template <int EPI, int CG>
+template <int EPI>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
                    const CUtensorMap& b0x, const CUtensorMap& b1x, const Fp8Params& p, int64_t max_tiles,
                    cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_fp8_kernel<EPI, CG>;
-  const size_t smem = F8Smem<CG>::kBytes;
+  auto kern = tc_gemm_fp8_kernel<EPI>;
+  const size_t smem = F8Smem::kBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if constexpr (CG == 1) {
-    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-    kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
-  } else {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2 * (num_sms() / 2));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // a persistent grid must be resident all at once: no more pairs than fit together
-    static int max_pairs = 0;
-    if (!max_pairs) {
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
-      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-    }
-    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
-    cfg.gridDim = dim3(2 * pairs);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, a2, b0, b1, b0x, b1x, p);
-    if (e != cudaSuccess) return e;
-  }
+  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+  kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
   return cudaGetLastError();
 }
 
@@ -510,21 +452,16 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.out_scale = h_scale;
   p.status = st;
   p.timeout_ns = kTimeoutNs;
-  // Single-CTA tiles. The CTA-pair form (CG = 2) computes the same results but measured
-  // twice as slow on GB300 (76 pairs resident, each at half the rate): this kernel hands a
-  // partial accumulator between the MMA and the epilogue every K block, and in a pair that
-  // handshake crosses SMs with only two partial buffers to hide it. Not selected.
-  const bool pair = false;
-  const int tm = pair ? 2 * BM : BM;
-  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
-  cudaError_t e = pair ? launch<FP8_SWIGLU_Q8, 2>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
-                       : launch<FP8_SWIGLU_Q8, 1>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  // Single-CTA tiles: a CTA-pair form of this kernel computed the same results but ran at
+  // half the rate, because the partial accumulator it hands from the MMA to the epilogue
+  // every K block then crosses SMs with only two partial buffers to hide the handshake.
+  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  cudaError_t e = launch<FP8_SWIGLU_Q8>(a1, a1, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = (h * h_scale) (Wd * s_down)^T, bf16 out
-  const uint32_t box2 = pair ? BN / 2 : BN;  // a pair's CTAs each load half of the N tile
   CUtensorMap a2, bd, bdx;
-  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, box2);
-  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, box2);
+  ok = make_u8(&a2, h, rows, c.F, BM) && make_u8(&bd, w.w_down, (uint64_t)c.E * c.H, c.F, BN);
+  if (shared) ok = ok && make_u8(&bdx, w.ws_down, c.H, c.F, BN);
   else bdx = bd;
   if (!ok) return cudaErrorInvalidValue;
   p.K = c.F;
@@ -539,8 +476,7 @@ cudaError_t launch_grouped_mlp_fp8(const moe_config_t& c, const void* xd, const 
   p.ldc = c.H;
   p.out = yd;
   p.out_scale = nullptr;
-  return pair ? launch<FP8_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s)
-              : launch<FP8_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
+  return launch<FP8_STORE_BF16>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc

@@ -8,8 +8,8 @@
 // tensor memory, so the whole K loop accumulates in one TMEM accumulator with no software
 // promotion.
 //
-// Tile 128 x 256 (one CTA) or 256 x 256 (a CTA pair), K stages of 128 (four MMAs of K = 32,
-// scale-factor id = the slice).
+// Tile 128 x 256 (one CTA), K stages of 128 (four MMAs of K = 32, scale-factor id = the
+// slice).
 // Block: warp 0 TMA producer, warp 1 MMA issuer (TMEM owner), warps 2-9 epilogue (two
 // warps per TMEM lane quarter, each owning half of the tile's columns).
 //   Per stage the producer loads the A and B tiles (TMA, 128-byte swizzle) and the stage's
@@ -17,11 +17,6 @@
 //   view); the MMA issuer moves the atoms into tensor memory with tcgen05.cp 32x128b.warpx4
 //   (the copy and the MMAs that read it come from one thread, so they execute in order)
 //   and issues the MMAs.
-//   CTA pair (CG = 2; built, not selected: see launch_grouped_mlp_mx): M = 256 pair MMAs; each CTA loads its
-//   own 128 rows of A with their scale atom, its half of B (GEMM1: CTA 0 the gate rows, CTA 1
-//   the up rows) and both B atoms, because each CTA's tensor core reads the scales of all
-//   256 B columns from its own TMEM; the leader's tcgen05.cp.cta_group::2 copies in both
-//   CTAs, each from its own shared memory. Stages are 33.5 KB, six in flight.
 //   TMEM: accumulator in columns [0, 256); stage s's scale factors in [256 + 16s, +12).
 //   The accumulator is single-buffered: the epilogue loads its 128 x 256 values into
 //   registers and hands the accumulator back before it computes and stores, so the next
@@ -62,11 +57,10 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256, kSfColsPerStage = 16;  // up to 6 stages: columns 256..351
 constexpr int kEpiStageBytes = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes (GEMM2 stores)
 
-template <int CG>
 struct MxSmem {
-  static constexpr int kBBytes = (BN / CG) * BK;  // this CTA's B rows
+  static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
-  static constexpr int kStages = CG == 2 ? 6 : 4;
+  static constexpr int kStages = 4;
   static constexpr size_t kBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) +
                                    kEpiWarps * kEpiStageBytes;
 };
@@ -124,14 +118,9 @@ __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
   return d;
 }
 
-// 32 lanes x 128 bits of shared memory to TMEM, repeated into all four lane quarters (the
-// pair form copies in both CTAs of the pair, each from its own shared memory).
-template <int CG>
+// 32 lanes x 128 bits of shared memory to TMEM, repeated into all four lane quarters.
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t desc) {
-  if constexpr (CG == 1)
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-  else
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // Instruction descriptor of kind::mxf8f6f4: e4m3 x e4m3, fp32 accumulate, K-major A and B,
@@ -140,25 +129,15 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
   return (sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 
-template <int CG>
 __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  if constexpr (CG == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -167,7 +146,7 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-template <int EPI, int CG>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0x,
@@ -175,9 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmSB0, const __grid_constant__ CUtensorMap tmSB1,
                       const __grid_constant__ CUtensorMap tmSB0x, const __grid_constant__ CUtensorMap tmSB1x,
                       const MxParams p) {
-  using S = MxSmem<CG>;
+  using S = MxSmem;
   constexpr int kStages = S::kStages, kBBytes = S::kBBytes, kStageBytes = S::kStageBytes;
-  constexpr int TM = BM * CG;  // rows of an m tile
+  constexpr int TM = BM;  // rows of an m tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -198,9 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.G + p.has_extra;
   const int kblocks = p.K / BK;
-  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;
-  const bool leader = rank == 0;
-  const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
+  const int unit = blockIdx.x, nunits = gridDim.x;  // persistent tile walkers
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -208,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kEpiWarps * CG);  // one arrival per epilogue warp of the pair
+    mbar_init(acc_empty, kEpiWarps);  // one arrival per epilogue warp
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -218,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmSA);
   }
-  if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_cg<1>(tmem_slot, kTmemCols);
   if (warp == 2) {
     int carry = 0;
     for (int g0 = 0; g0 < ngroups; g0 += 32) {
@@ -243,13 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = p.n_tiles * mt_prefix[ngroups];
 
   if (warp == 0) {
-    // ======================= TMA producer (each CTA loads its own A rows, half of B, scales)
+    // ======================= TMA producer (A rows, B rows and the stage's scale atoms)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -259,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
         const bool extra = c.g >= p.G;
         const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
-        const int a_row = (int)gofs + c.mb * TM + (int)rank * BM;
-        const int a_atom = (int)(mx_group_atom_base(gofs, c.g) + c.mb * CG + rank);
+        const int a_row = (int)gofs + c.mb * TM;
+        const int a_atom = (int)(mx_group_atom_base(gofs, c.g) + c.mb);
         const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
         const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
         const CUtensorMap* ts0 = extra ? &tmSB0x : &tmSB0;
@@ -268,10 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b_tile_rows = EPI == MX_SWIGLU_Q8 ? BN / 2 : BN;
         const int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
         const int b_atom = b_row / 128;  // b_row is a multiple of 128
-        // this CTA's B rows: GEMM1 the gate (rank 0) or up (rank 1) rows of the F block;
-        // GEMM2 rows [rank * 128, +128) of the N tile
-        const CUtensorMap* tb_mine = (CG == 2 && EPI == MX_SWIGLU_Q8 && rank == 1) ? tb1 : tb0;
-        const int b_row_mine = b_row + ((CG == 2 && EPI != MX_SWIGLU_Q8) ? (int)rank * (BN / 2) : 0);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status)) { ok = false; break; }
           uint8_t* a_dst = sA + stage * kABytes;
@@ -281,28 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sb0_y = (EPI == MX_SWIGLU_Q8 ? b_atom : b_atom) * kblocks + kb;
           const int sb1_y = (EPI == MX_SWIGLU_Q8 ? b_atom : b_atom + 1) * kblocks + kb;
           const CUtensorMap* tsb1 = EPI == MX_SWIGLU_Q8 ? ts1 : ts0;
-          if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row);
-            if (EPI == MX_SWIGLU_Q8) {
-              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-              tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
-            } else {
-              tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
-            }
-            tma_load_2d(&tmSA, sf_dst, &full[stage], 0, sa_y);
-            tma_load_2d(ts0, sf_dst + kAtomBytes, &full[stage], 0, sb0_y);
-            tma_load_2d(tsb1, sf_dst + 2 * kAtomBytes, &full[stage], 0, sb1_y);
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(&tmA, a_dst, &full[stage], kb * BK, a_row);
+          if (EPI == MX_SWIGLU_Q8) {
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
+            tma_load_2d(tb1, b_dst + (BN / 2) * BK, &full[stage], kb * BK, b_row);
           } else {
-            // both CTAs' loads complete on the leader's barrier, which expects both
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
-            tma_load_2d_pair(&tmA, a_dst, bar, kb * BK, a_row);
-            tma_load_2d_pair(tb_mine, b_dst, bar, kb * BK, b_row_mine);
-            tma_load_2d_pair(&tmSA, sf_dst, bar, 0, sa_y);
-            tma_load_2d_pair(ts0, sf_dst + kAtomBytes, bar, 0, sb0_y);
-            tma_load_2d_pair(tsb1, sf_dst + 2 * kAtomBytes, bar, 0, sb1_y);
+            tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
           }
+          tma_load_2d(&tmSA, sf_dst, &full[stage], 0, sa_y);
+          tma_load_2d(ts0, sf_dst + kAtomBytes, &full[stage], 0, sb0_y);
+          tma_load_2d(tsb1, sf_dst + 2 * kAtomBytes, &full[stage], 0, sb1_y);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -313,12 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (stage - 1 - i + 2 * kStages) % kStages;
         const uint32_t ph = (stage - 1 - i < 0) ? (phase ^ 1) : phase;
         if (ok) ok = mbar_wait(&empty[s], ph, abort, p.timeout_ns, p.status);
-        if (!ok && (CG == 1 || leader)) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
+        if (!ok) mbar_wait_drain(&full[s], ph, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer (the leader of a pair issues for both CTAs)
-    if (lane == 0 && leader) {
+    // ======================= MMA issuer
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -336,27 +297,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf_addr = smem_addr(sSF + stage * kSfBytes);
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_atom<CG>(sfa_t, desc_atom(sf_addr));
-          tmem_cp_atom<CG>(sfb_t, desc_atom(sf_addr + kAtomBytes));
-          tmem_cp_atom<CG>(sfb_t + 4, desc_atom(sf_addr + 2 * kAtomBytes));
+          tmem_cp_atom(sfa_t, desc_atom(sf_addr));
+          tmem_cp_atom(sfb_t, desc_atom(sf_addr + kAtomBytes));
+          tmem_cp_atom(sfb_t + 4, desc_atom(sf_addr + 2 * kAtomBytes));
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction: +32 bytes, scale id k
-            mma_mx<CG>(tmem_base, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32),
-                       idesc_mx(TM, BN, (uint32_t)k), sfa_t, sfb_t, (kb | k) != 0);
-          if constexpr (CG == 1) mma_commit(&empty[stage]);
-          else mma_commit_pair(&empty[stage], 0x3);
+            mma_mx(tmem_base, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32),
+                   idesc_mx(TM, BN, (uint32_t)k), sfa_t, sfb_t, (kb | k) != 0);
+          mma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        if (ok) {
-          if constexpr (CG == 1) mma_commit(acc_full);
-          else mma_commit_pair(acc_full, 0x3);
-        }
+        if (ok) mma_commit(acc_full);
       }
-      if constexpr (CG == 1) mma_commit(drain);
-      else mma_commit_pair(drain, 0x3);
-      mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
-    } else if (lane == 0 && CG == 2) {
-      // the pair's MMAs write this CTA's TMEM and read its shared memory: stay until done
+      mma_commit(drain);
       mbar_wait_drain(drain, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -364,10 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int half = ew >> 2;  // which 128 of the tile's 256 columns this warp owns
-    const int r = quarter * 32 + lane;          // TMEM lane = this CTA's row
-    const int row_in_tile = (int)rank * BM + r;  // row of the (pair) tile
+    const int r = quarter * 32 + lane;  // TMEM lane = row of the tile
     uint8_t* stage = sEpi + ew * kEpiStageBytes;
-    const uint32_t acc_empty_leader = CG == 2 ? mapa_shared(smem_addr(acc_empty), 0) : 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
@@ -393,17 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();  // every lane's loads are complete: one arrival per warp
-      if (lane == 0) {
-        if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(acc_empty_leader);
-        else mbar_arrive_relaxed(acc_empty);
-      }
+      if (lane == 0) mbar_arrive_relaxed(acc_empty);
 
       const int64_t gofs = extra ? (int64_t)p.a2_row_base : (int64_t)p.offsets[c.g];
-      const int64_t row0 = (extra ? p.out_extra_base : gofs) + c.mb * TM + (int)rank * BM + quarter * 32;
-      const int live_rows = c.rows - ((int)rank * BM + quarter * 32);  // rows of this warp inside the segment
+      const int64_t row0 = (extra ? p.out_extra_base : gofs) + c.mb * TM + quarter * 32;
+      const int live_rows = c.rows - quarter * 32;  // rows of this warp inside the segment
       if (EPI == MX_SWIGLU_Q8) {
         // 64 bytes of h codes per thread per tile: direct 16-byte stores
-        if (row_in_tile < c.rows) {
+        if (r < c.rows) {
           uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (row0 + lane) * p.ldc + c.nb * 128 + half * 64;
           uint32_t codes = 0;
 #pragma unroll
@@ -427,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(out + 32 * blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
             codes |= (uint32_t)(s + 127) << (8 * blk);
           }
-          // blocks 2*half and 2*half + 1 of the h stage nb, in this CTA's atom row
-          const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb * CG + rank;
+          // blocks 2*half and 2*half + 1 of the h stage nb, in the tile's atom row
+          const int64_t atom = mx_group_atom_base(gofs, c.g) + c.mb;
           *reinterpret_cast<uint16_t*>(p.out_sf + mx_atom_byte(atom, c.nb, p.ldc / 128, r) + 2 * half) =
               (uint16_t)codes;
         }
@@ -457,11 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the pair still uses it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc_cg<CG>(tmem_base, kTmemCols);
+    tmem_dealloc_cg<1>(tmem_base, kTmemCols);
   }
 }
 
@@ -478,45 +425,19 @@ struct MxMaps {
   CUtensorMap a, b0, b1, b0x, b1x, sa, sb0, sb1, sb0x, sb1x;
 };
 
-template <int EPI, int CG>
+template <int EPI>
 cudaError_t launch(const MxMaps& m, const MxParams& p, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
-  auto kern = tc_gemm_mx_kernel<EPI, CG>;
-  const size_t smem = MxSmem<CG>::kBytes;
+  auto kern = tc_gemm_mx_kernel<EPI>;
+  const size_t smem = MxSmem::kBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if constexpr (CG == 1) {
-    const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-    kern<<<grid, kThreads, smem, s>>>(m.a, m.b0, m.b1, m.b0x, m.b1x, m.sa, m.sb0, m.sb1, m.sb0x, m.sb1x, p);
-  } else {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2 * (num_sms() / 2));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // a persistent grid must be resident all at once: no more pairs than fit together
-    static int max_pairs = 0;
-    if (!max_pairs) {
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg);
-      if (e != cudaSuccess || max_pairs <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-    }
-    const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
-    cfg.gridDim = dim3(2 * pairs);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, m.a, m.b0, m.b1, m.b0x, m.b1x, m.sa, m.sb0, m.sb1, m.sb0x,
-                                       m.sb1x, p);
-    if (e != cudaSuccess) return e;
-  }
+  const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
+  kern<<<grid, kThreads, smem, s>>>(m.a, m.b0, m.b1, m.b0x, m.b1x, m.sa, m.sb0, m.sb1, m.sb0x, m.sb1x, p);
   return cudaGetLastError();
 }
 
@@ -532,14 +453,11 @@ cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const v
                                   cudaStream_t s) {
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
-  // Single-CTA tiles. The CTA-pair form (CG = 2) computes the same results (it passes the
-  // same tests when selected) but measured slower on GB300: 10.67 against 9.76 ms for the
-  // DeepSeek-V3-shaped MXFP8 layer. Its accumulator stays single-buffered (two 256-column
-  // accumulators and the scale factors do not fit in 512 TMEM columns), so every tile
-  // boundary waits for both CTAs' epilogues across the pair, and 256-row tiles double the
-  // padding of ragged segment tails. Not selected.
-  const bool pair = false;
-  const int tm = pair ? 2 * BM : BM;
+  // Single-CTA tiles: a CTA-pair form of this kernel computed the same results but ran
+  // slower (10.67 against 9.76 ms on the DeepSeek-V3-shaped MXFP8 layer): its accumulator
+  // has to stay single-buffered (two 256-column accumulators and the scale factors exceed
+  // 512 TMEM columns), so every tile boundary waits for both CTAs' epilogues, and 256-row
+  // tiles double the padding of ragged segment tails.
   const int64_t atoms_act = mx_act_atom_rows(c);
   // ---- GEMM1: h = mx(silu(A Wg^T) * (A Wu^T)); the shared expert's A = dispatched rows R..
   MxMaps m{};
@@ -569,18 +487,16 @@ cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const v
   p.out_sf = static_cast<uint8_t*>(h_sf);
   p.status = st;
   p.timeout_ns = kTimeoutNs;
-  const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
-  cudaError_t e = pair ? launch<MX_SWIGLU_Q8, 2>(m, p, mt_bound * p.n_tiles, s)
-                       : launch<MX_SWIGLU_Q8, 1>(m, p, mt_bound * p.n_tiles, s);
+  const int64_t mt_bound = ceil_div(R, BM) + c.E + (shared ? ceil_div(c.T, BM) : 0);
+  cudaError_t e = launch<MX_SWIGLU_Q8>(m, p, mt_bound * p.n_tiles, s);
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = h Wd^T with both operands' MX scales, bf16 out
-  const uint32_t box2 = pair ? BN / 2 : BN;  // a pair's CTAs each load half of the N tile
   MxMaps m2{};
-  ok = make_u8(&m2.a, h, rows, c.F, BM) && make_u8(&m2.b0, w.w_down, (uint64_t)c.E * c.H, c.F, box2) &&
+  ok = make_u8(&m2.a, h, rows, c.F, BM) && make_u8(&m2.b0, w.w_down, (uint64_t)c.E * c.H, c.F, BN) &&
        make_atoms(&m2.sa, h_sf, (uint64_t)atoms_act * (c.F / 128)) &&
        make_atoms(&m2.sb0, w.s_down, (uint64_t)c.E * c.H / 128 * (c.F / 128));
   if (shared)
-    ok = ok && make_u8(&m2.b0x, w.ws_down, c.H, c.F, box2) &&
+    ok = ok && make_u8(&m2.b0x, w.ws_down, c.H, c.F, BN) &&
          make_atoms(&m2.sb0x, w.ss_down, (uint64_t)c.H / 128 * (c.F / 128));
   else { m2.b0x = m2.b0; m2.sb0x = m2.sb0; }
   if (!ok) return cudaErrorInvalidValue;
@@ -591,8 +507,7 @@ cudaError_t launch_grouped_mlp_mx(const moe_config_t& c, const void* xd, const v
   p.ldc = c.H;
   p.out = yd;
   p.out_sf = nullptr;
-  return pair ? launch<MX_STORE_BF16, 2>(m2, p, mt_bound * p.n_tiles, s)
-              : launch<MX_STORE_BF16, 1>(m2, p, mt_bound * p.n_tiles, s);
+  return launch<MX_STORE_BF16>(m2, p, mt_bound * p.n_tiles, s);
 }
 
 }  // namespace tc
