@@ -91,33 +91,13 @@ struct BwdParams {
   uint64_t timeout_ns;
 };
 
-struct TileCoord {
-  int g, mb, nb, rows;  // dgrad: m tile mb of group g (rows valid); wgrad: out tile (mb, nb), rows = K rows
-};
-
 // First padded row of group g (offset = its first row in the unpadded buffers).
 __host__ __device__ __forceinline__ int64_t padded_row0(int64_t offset, int g) {
   return (offset + 63 * (int64_t)g + 63) / 64 * 64;
 }
 
-__device__ __forceinline__ TileCoord decode_dgrad(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                  const int32_t* seg_rows, int tm) {
-  int lo = 0, hi = ngroups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileCoord c;
-  c.g = lo;
-  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
-  const int local = tile - n_tiles * mt_prefix[lo];
-  c.nb = local / mt;
-  c.mb = local - c.nb * mt;
-  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
-  return c;
-}
-
+// Weight-gradient tiles: per group, m_tiles x n_tiles output tiles (mb, nb) of the gradient;
+// rows = the group's token rows, the tile's reduction length.
 __device__ __forceinline__ TileCoord decode_wgrad(int tile, int m_tiles, int n_tiles, const int32_t* seg_rows) {
   const int per = m_tiles * n_tiles;
   TileCoord c;
@@ -205,28 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
   }
   if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, kTmemCols);
-  if (warp == 2) {
-    int carry = 0;
-    for (int g0 = 0; g0 < ngroups; g0 += 32) {
-      const int g = g0 + lane;
-      int rows = 0;
-      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
-      else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + TM - 1) / TM;
-      int inc = mt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      if (g < ngroups) {
-        seg_rows[g] = rows;
-        mt_prefix[g] = carry + inc - mt;
-      }
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) mt_prefix[ngroups] = carry;
-  }
+  if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
   tc_fence_before();
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use
@@ -235,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = kWgrad ? ngroups * p.m_tiles_out * p.n_tiles : p.n_tiles * mt_prefix[ngroups];
   auto decode = [&](int tile) {
     return kWgrad ? decode_wgrad(tile, p.m_tiles_out, p.n_tiles, seg_rows)
-                  : decode_dgrad(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
+                  : decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
   };
   auto kblocks_of = [&](const TileCoord& c) { return kWgrad ? (c.rows + BK - 1) / BK : p.K / BK; };
   auto group_row0 = [&](int g) { return g >= p.G ? p.a2_row_base : p.offsets[g]; };

@@ -69,28 +69,6 @@ struct Fp8Params {
   uint64_t timeout_ns;
 };
 
-struct TileCoord {
-  int g, mb, nb, rows;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows, int tm) {
-  int lo = 0, hi = ngroups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileCoord c;
-  c.g = lo;
-  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
-  const int local = tile - n_tiles * mt_prefix[lo];
-  c.nb = local / mt;
-  c.mb = local - c.nb * mt;
-  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
-  return c;
-}
-
 // TMEM column of the q-th 16-column chunk a thread of column-half `half` promotes.
 // GEMM1: q 0-3 gate cols [half*64, +64), q 4-7 up cols [128 + half*64, +64);
 // GEMM2: cols [half*128 + 16q, +16).
@@ -156,28 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
   }
   if (warp == 1) tmem_alloc_cg<1>(tmem_slot, kTmemCols);
-  if (warp == 2) {
-    int carry = 0;
-    for (int g0 = 0; g0 < ngroups; g0 += 32) {
-      const int g = g0 + lane;
-      int rows = 0;
-      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
-      else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + TM - 1) / TM;
-      int inc = mt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      if (g < ngroups) {
-        seg_rows[g] = rows;
-        mt_prefix[g] = carry + inc - mt;
-      }
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) mt_prefix[ngroups] = carry;
-  }
+  if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -86,28 +86,6 @@ struct MxParams {
   uint64_t timeout_ns;
 };
 
-struct TileCoord {
-  int g, mb, nb, rows;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows, int tm) {
-  int lo = 0, hi = ngroups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileCoord c;
-  c.g = lo;
-  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
-  const int local = tile - n_tiles * mt_prefix[lo];
-  c.nb = local / mt;
-  c.mb = local - c.nb * mt;
-  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
-  return c;
-}
-
 // Shared-memory descriptor of a scale atom for tcgen05.cp: no swizzle, 8-row core matrices
 // of 16-byte rows stored contiguously (stride 128 bytes between 8-row groups).
 __device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
@@ -196,28 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmSA);
   }
   if (warp == 1) tmem_alloc_cg<1>(tmem_slot, kTmemCols);
-  if (warp == 2) {
-    int carry = 0;
-    for (int g0 = 0; g0 < ngroups; g0 += 32) {
-      const int g = g0 + lane;
-      int rows = 0;
-      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
-      else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + TM - 1) / TM;
-      int inc = mt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      if (g < ngroups) {
-        seg_rows[g] = rows;
-        mt_prefix[g] = carry + inc - mt;
-      }
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) mt_prefix[ngroups] = carry;
-  }
+  if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -71,31 +71,6 @@ struct Smem {
                                    2 * kMaxGroups * sizeof(int32_t) + 4 * 2048 /*epilogue store staging*/;
 };
 
-// Tile -> (group, m tile, n tile) from the block's copy of the m-tile prefix; tm = rows of
-// an m tile (128, or 256 for a CTA pair).
-struct TileCoord {
-  int g, mb, nb, rows;  // rows: valid rows of this tile (<= tm)
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
-                                                 const int32_t* seg_rows, int tm) {
-  // largest g with n_tiles * mt_prefix[g] <= tile
-  int lo = 0, hi = ngroups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileCoord c;
-  c.g = lo;
-  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
-  const int local = tile - n_tiles * mt_prefix[lo];
-  c.nb = local / mt;
-  c.mb = local - c.nb * mt;
-  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
-  return c;
-}
-
 // CG = 1: one CTA per 128-row tile (tcgen05.mma.cta_group::1, M = 128).
 // CG = 2: a cluster of two CTAs per 256-row tile (cta_group::2, M = 256): each CTA loads its
 // 128 A rows and half of the tile's B rows (SwiGLU: CTA 0 the gate rows, CTA 1 the up rows);
@@ -152,29 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU) tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, S::kTmemCols);
-  if (warp == 2) {
-    // rows per group and an exclusive prefix of ceil(rows / TM), 32 groups per step
-    int carry = 0;
-    for (int g0 = 0; g0 < ngroups; g0 += 32) {
-      const int g = g0 + lane;
-      int rows = 0;
-      if (g < p.G) rows = p.offsets[g + 1] - p.offsets[g];
-      else if (g < ngroups) rows = p.T_extra;
-      const int mt = (rows + TM - 1) / TM;
-      int inc = mt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      if (g < ngroups) {
-        seg_rows[g] = rows;
-        mt_prefix[g] = carry + inc - mt;
-      }
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) mt_prefix[ngroups] = carry;
-  }
+  if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
   tc_fence_before();
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised before any remote use

@@ -345,5 +345,60 @@ __host__ __device__ constexpr uint32_t idesc_make(uint32_t ab_type, int M, int N
   return (1u << 4) | (ab_type << 7) | (ab_type << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- ragged tile schedule
+// The grouped GEMMs' tiles over ragged groups: groups [0, G) are the routed experts (rows
+// offsets[g + 1] - offsets[g], read on the device) and, when ngroups = G + 1, group G holds
+// t_extra rows (the shared expert, or a single problem). One warp builds, 32 groups per
+// step, seg_rows[g] and the exclusive prefix mt_prefix[0..ngroups] of the groups' m tiles
+// ceil(rows / tm).
+__device__ __forceinline__ void build_tile_prefix(const int32_t* offsets, int G, int ngroups, int t_extra, int tm,
+                                                  int lane, int32_t* seg_rows, int32_t* mt_prefix) {
+  int carry = 0;
+  for (int g0 = 0; g0 < ngroups; g0 += 32) {
+    const int g = g0 + lane;
+    int rows = 0;
+    if (g < G) rows = offsets[g + 1] - offsets[g];
+    else if (g < ngroups) rows = t_extra;
+    const int mt = (rows + tm - 1) / tm;
+    int inc = mt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += o;
+    }
+    if (g < ngroups) {
+      seg_rows[g] = rows;
+      mt_prefix[g] = carry + inc - mt;
+    }
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) mt_prefix[ngroups] = carry;
+}
+
+struct TileCoord {
+  int g, mb, nb, rows;  // group, m tile, n tile; rows: valid rows of the tile (<= tm)
+};
+
+// Tile index -> coordinates. Tiles run group-major, then n tile, then m tile, so the m
+// tiles of one (group, n tile) run side by side and share the weight tile through L2; empty
+// groups own no tiles.
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int32_t* mt_prefix, int ngroups, int n_tiles,
+                                                 const int32_t* seg_rows, int tm) {
+  int lo = 0, hi = ngroups - 1;  // largest g with n_tiles * mt_prefix[g] <= tile
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n_tiles * mt_prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileCoord c;
+  c.g = lo;
+  const int mt = mt_prefix[lo + 1] - mt_prefix[lo];
+  const int local = tile - n_tiles * mt_prefix[lo];
+  c.nb = local / mt;
+  c.mb = local - c.nb * mt;
+  c.rows = min(tm, seg_rows[lo] - c.mb * tm);
+  return c;
+}
+
 }  // namespace tc
 }  // namespace moe
