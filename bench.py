@@ -82,6 +82,18 @@ def quant_kind(w):
     return {synth.E4M3: 1, synth.MXE4M3: 2}.get(w["xfer_dtype"], 0)
 
 
+# DRAM bytes (read + write) per forward of the two grouped-GEMM launches, from one ncu
+# capture of the current kernels (profiles/tc_gemm_bf16_gateup_mixtral_bf16.md): the
+# T=2048, E=4 case moved 1.891 GB; the T=4096, E=8 layer has twice its weights and twice its
+# rows, so 3.782 GB. Other workloads: not captured at the current kernels (null).
+GEMM_TRAFFIC = {"mixtral_bf16": (3.782e9, "ncu T=2048 E=4 capture x2 (weights and rows both double)")}
+
+
+def gemm_traffic(w):
+    t = GEMM_TRAFFIC.get(w["name"])
+    return {"traffic": t[0], "traffic_source": t[1]} if t else {"traffic": None}
+
+
 def algorithmic(w):
     """Algorithmic bytes / flops per forward (each tensor read or written once)."""
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
@@ -425,7 +437,8 @@ def run_gpu(args, w):
         "roofline": {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
                      "bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
                      "peak_kind": f"{peak_kind} bf16 sustained" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
-                     "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 3), "traffic": None},
+                     "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 3),
+                     **gemm_traffic(w)},
         "hbm_roofline": {"dispatch_frac": round(alg["dispatch_bytes"] / (b2b_disp / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
                          "combine_frac": round(alg["combine_bytes"] / (b2b_comb / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
                          "peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
