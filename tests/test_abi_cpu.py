@@ -93,3 +93,41 @@ def test_null_and_misaligned_pointers_rejected_on_host(L):
     assert L.moe_forward(None, None, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_read_status(None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_status_string(moe.MOE_ERR_TIMEOUT).startswith("device")
+
+
+def test_variant_mismatches_rejected_on_host(L):
+    """Calls for a variant the config does not describe, or shapes a kernel does not take,
+    return their error before any launch."""
+    import ctypes
+    P = ctypes.c_void_p
+    mx = cfg(H=256, xfer_dtype=moe.MXE4M3)
+    bf = cfg(H=256)
+    # MXFP8 dispatch has its own entry point, and it refuses other transfer types
+    assert L.moe_dispatch(ctypes.byref(mx), P(4096), P(4096), P(4096), P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_dispatch_mx(ctypes.byref(bf), P(4096), P(4096), P(4096), P(4096), P(4096), P(4096),
+                             None) == moe.MOE_ERR_INVALID_ARG
+    # the backward takes bf16 layers with H and F multiples of 256
+    assert L.moe_combine_backward(ctypes.byref(cfg(act_dtype=moe.F32)), P(4096), P(4096), P(4096), P(4096),
+                                  P(4096), P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_mlp_backward(ctypes.byref(cfg(H=256, F=384)), P(4096), P(4096), P(4096), None, P(4096),
+                                      P(4096), None, P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_backward(ctypes.byref(cfg(H=256, xfer_dtype=moe.E4M3)), P(4096), None, P(4096), P(4096), P(4096),
+                          P(4096), None, P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    # quantisers: the MX one wants multiples of 128, the fp32-scale one 1 or 128 blocks
+    assert L.moe_quantize_mx(P(4096), 100, 128, P(4096), P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_quantize_mx(P(4096), -1, 128, P(4096), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_e4m3(P(4096), 128, 128, 64, 128, P(4096), P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T,k,E,shared", [(64, 2, 8, 0), (300, 8, 16, 1), (1, 1, 4, 0), (0, 2, 8, 1)])
+def test_mx_scale_bytes_follow_the_atom_layout(L, T, k, E, shared):
+    """Each expert's rows start a fresh 128-row atom row (at ceil((offsets[e] + 127 e) / 128)),
+    the shared expert's rows follow, and two spare atom rows close the buffer; every atom row
+    holds one 512-byte atom per 128 columns."""
+    c = cfg(T=T, k=k, E=E, H=256, xfer_dtype=moe.MXE4M3, n_shared=shared, F_shared=256 if shared else 0)
+    rows = -(-(T * k + 127 * E) // 128) + (-(-T // 128) if shared else 0) + 2
+    for K in (128, 256, 2048):
+        assert moe.moe_mx_scale_bytes(c, K) == rows * (K // 128) * 512
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_mx_scale_bytes(c, 100)
+    assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
