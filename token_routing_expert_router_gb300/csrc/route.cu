@@ -114,8 +114,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
     int gidx = INT_MAX;
     if (lane < G) {
       float m1 = -INFINITY, m2 = -INFINITY;  // the two largest scores of the group
+      // lanes start at different offsets of their groups (no bank conflicts); the two
+      // largest do not depend on the order the scores are visited in
       for (int i = 0; i < gs; ++i) {
-        const float x = sc[lane * gs + i];
+        const float x = sc[lane * gs + (i + lane) % gs];
         if (x > m1) { m2 = m1; m1 = x; }
         else if (x > m2) m2 = x;
       }
@@ -203,20 +205,41 @@ __global__ void __launch_bounds__(kScanChunk) scan_count_kernel(
 }
 
 // S2 pass 2 (one block): counts, offsets (exclusive scan over experts) and, in place of
-// each block's count, the first row that block's entries of expert e take.
-__global__ void __launch_bounds__(1024) scan_offsets_kernel(int E, int NB, int32_t* __restrict__ blockcnt,
+// each block's count, the first row that block's entries of expert e take. Each expert's
+// NB block counts are split into P contiguous shares, one per thread (P consecutive lanes),
+// so the dependent chains over the blocks are P times shorter; s_off holds the experts'
+// totals [E], their exclusive offsets [E] and the shares' sums [E * P].
+__global__ void __launch_bounds__(1024) scan_offsets_kernel(int E, int NB, int P, int32_t* __restrict__ blockcnt,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
+  extern __shared__ int32_t s_off[];
+  int32_t* tot_s = s_off;
+  int32_t* excl_s = s_off + E;
+  int32_t* part_s = s_off + 2 * E;
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (NB + P - 1) / P;  // blocks per share
+  // shares and expert totals (the loop bound is the same for every thread, so the lane
+  // groups are complete at every shuffle)
+  for (int i0 = 0; i0 < E * P; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const int e = i / P, q = i - e * P;
+    int32_t part = 0;
+    if (e < E) {
+      const int b1 = min(NB, (q + 1) * per);
+      for (int b = q * per; b < b1; ++b) part += blockcnt[(int64_t)b * E + e];
+      part_s[i] = part;
+    }
+    int32_t tot = part;
+    for (int off = 1; off < P; off <<= 1) tot += __shfl_xor_sync(kFull, tot, off);
+    if (e < E && q == 0) tot_s[e] = tot;
+  }
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
-    int32_t tot = 0;
-    if (e < E)
-      for (int b = 0; b < NB; ++b) tot += blockcnt[(int64_t)b * E + e];
+    const int32_t tot = e < E ? tot_s[e] : 0;
     int32_t inc = tot;  // inclusive warp scan
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -241,18 +264,28 @@ __global__ void __launch_bounds__(1024) scan_offsets_kernel(int E, int NB, int32
     if (e < E) {
       counts[e] = tot;
       offsets[e] = excl;
-      int32_t run = excl;
-      for (int b = 0; b < NB; ++b) {
-        const int32_t c = blockcnt[(int64_t)b * E + e];
-        blockcnt[(int64_t)b * E + e] = run;
-        run += c;
-      }
+      excl_s[e] = excl;
     }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) carry = excl + tot;
     __syncthreads();
   }
   if (threadIdx.x == 0) offsets[E] = carry;
+  // each share's blocks get their first rows: the expert's offset plus the earlier shares
+  for (int i0 = 0; i0 < E * P; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const int e = i / P, q = i - e * P;
+    if (e < E) {
+      int32_t run = excl_s[e];
+      for (int qq = 0; qq < q; ++qq) run += part_s[e * P + qq];
+      const int b1 = min(NB, (q + 1) * per);
+      for (int b = q * per; b < b1; ++b) {
+        const int32_t c = blockcnt[(int64_t)b * E + e];
+        blockcnt[(int64_t)b * E + e] = run;
+        run += c;
+      }
+    }
+  }
 }
 
 // S2 pass 3: one warp per block of kScanChunk tokens walks them in ascending order, 32 at
@@ -522,7 +555,10 @@ cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, in
   if (NB > 0) {
     scan_count_kernel<<<NB, kScanChunk, c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, blockcnt, st);
   }
-  scan_offsets_kernel<<<1, 1024, 0, s>>>(c.E, NB, blockcnt, counts, offsets);
+  int P = 1;  // threads per expert in the offsets pass: a power of two, at most 32
+  while (P < 32 && 2 * P * c.E <= 1024) P *= 2;
+  scan_offsets_kernel<<<1, 1024, (size_t)(2 + P) * c.E * sizeof(int32_t), s>>>(c.E, NB, P, blockcnt, counts,
+                                                                             offsets);
   if (NB > 0) {
     scan_assign_kernel<<<NB, 32, 2 * c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, blockcnt,
                                                                  row_token, tok_row, st);
