@@ -78,6 +78,7 @@ def _L():
             "oc_combine_backward": (None, [P, P, P, P, i32, i32, i32, i32, P, P]),
             "oc_expert_mlp_backward": (None, [P, i64, i32, i32, P, P, P, P, P, P, P, P]),
             "oc_dispatch_backward": (None, [P, P, i32, i32, i32, i32, P]),
+            "oc_router_backward": (None, [P, i32, i32, i32, P, i32, i32, f64, P, P]),
             "oc_dense_forward": (i32, [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f64, P, P, P, i32, P, P, P, P]),
         }
@@ -386,6 +387,28 @@ def dispatch_backward(dxd, tok_row, shared: bool) -> np.ndarray:
     dx = np.empty((T, H), dtype=np.float64)
     _L().oc_dispatch_backward(_p(dxd), _p(tr), T, k, H, int(shared), _p(dx))
     return dx
+
+
+def router_backward(cfg: dict, logits, topk_idx, dtopk_w) -> np.ndarray:
+    """dL/dlogits [T, E] (fp64) from dL/dtopk_w [T, k], the chosen experts held fixed: the
+    chain rule through the weight step of the routing (softmax over all experts or over the
+    chosen k, or sigmoid with or without normalisation, times the routed scale)."""
+    l = _c(logits, np.float32)
+    idx = _c(topk_idx, np.int32)
+    dw = _c(dtopk_w, np.float64)
+    T, E = l.shape
+    k = idx.shape[1]
+    dl = np.empty((T, E), dtype=np.float64)
+    _L().oc_router_backward(_p(l), T, E, k, _p(idx), cfg["score_fn"], cfg["renorm"], float(cfg["routed_scale"]),
+                            _p(dw), _p(dl))
+    return dl
+
+
+def router_linear_backward(x, w_router, dlogits):
+    """(dW_router [E, H], dx through the router [T, H]) of logits = x W_router^T: the two
+    products of the linear map's gradient, in fp64."""
+    dl = np.asarray(dlogits, dtype=np.float64)
+    return dl.T @ np.asarray(x, dtype=np.float64), dl @ np.asarray(w_router, dtype=np.float64)
 
 
 def backward(cfg: dict, inp: dict, fwd: dict, dy) -> dict:

@@ -452,6 +452,56 @@ void oc_combine(const double* yd, const int32_t* tok_row, const double* w, const
 /* steps, in fp64, in the reverse order.                                                 */
 /* ------------------------------------------------------------------------------------ */
 
+/* Router backward. The top-k choice is a piecewise-constant function of the logits and  */
+/* is held fixed; the chosen weights are w = rho * f(l) with f the weight step of          */
+/* route_one. With g[j] = rho * dw[t,j] (dw = dL/dw, the combine backward's result):        */
+/*   softmax over all experts:  p = softmax(l);  dl[e] = [e chosen] g_e p_e - p_e sum_j g_j p_j */
+/*   softmax over the chosen k: q = softmax(l over the chosen); dl[i_j] = q_j (g_j - sum g q) */
+/*   sigmoid s, normalised:     w~ = s / S;  dl[i_j] = s_j (1 - s_j) (g_j - sum g w~) / S     */
+/*   sigmoid, not normalised:   dl[i_j] = g_j s_j (1 - s_j)                                  */
+/* and dl = 0 for experts not chosen, except in the first form. Experts chosen twice do  */
+/* not occur (a token's k experts are distinct).                                          */
+void oc_router_backward(const float* logits, int T, int E, int k, const int32_t* topk_idx, int score_fn,
+                        int renorm, double routed_scale, const double* dw, double* dl) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    const int32_t* idx = topk_idx + (int64_t)t * k;
+    double* d = dl + (int64_t)t * E;
+    double* g = (double*)malloc(sizeof(double) * (size_t)k);
+    double* v = (double*)malloc(sizeof(double) * (size_t)k);
+    for (int e = 0; e < E; ++e) d[e] = 0.0;
+    for (int j = 0; j < k; ++j) g[j] = routed_scale * dw[(int64_t)t * k + j];
+    if (score_fn == 0) {
+      double m = -INFINITY;
+      for (int e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+      if (renorm) {
+        double den = 0.0, c = 0.0;
+        for (int j = 0; j < k; ++j) { v[j] = exp((double)l[idx[j]] - m); den += v[j]; }
+        for (int j = 0; j < k; ++j) { v[j] /= den; c += g[j] * v[j]; }
+        for (int j = 0; j < k; ++j) d[idx[j]] = v[j] * (g[j] - c);
+      } else {
+        double den = 0.0, c = 0.0;
+        for (int e = 0; e < E; ++e) den += exp((double)l[e] - m);
+        for (int j = 0; j < k; ++j) { v[j] = exp((double)l[idx[j]] - m) / den; c += g[j] * v[j]; }
+        for (int e = 0; e < E; ++e) d[e] = -exp((double)l[e] - m) / den * c;
+        for (int j = 0; j < k; ++j) d[idx[j]] += g[j] * v[j];
+      }
+    } else {
+      double S = 0.0, c = 0.0;
+      for (int j = 0; j < k; ++j) { v[j] = 1.0 / (1.0 + exp(-(double)l[idx[j]])); S += v[j]; }
+      if (renorm) {
+        for (int j = 0; j < k; ++j) c += g[j] * v[j] / S;
+        for (int j = 0; j < k; ++j) d[idx[j]] = v[j] * (1.0 - v[j]) * (g[j] - c) / S;
+      } else {
+        for (int j = 0; j < k; ++j) d[idx[j]] = g[j] * v[j] * (1.0 - v[j]);
+      }
+    }
+    free(g);
+    free(v);
+  }
+}
+
 /* Combine backward. From y[t] = sum_j w[t,j] * yd[r_tj] (+ yd[R+t]):                    */
 /*   dyd[r_tj] = w[t,j] * dy[t],  dyd[R+t] = dy[t]  (shared),                            */
 /*   dw[t,j]  = sum_o dy[t,o] * yd[r_tj, o].                                              */

@@ -611,6 +611,123 @@ def test_layer_backward_matches_finite_differences(name):
         assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3), (key, fd, an)
 
 
+ROUTER_BWD = {
+    "softmax_all": cfg(8, 2, score_fn=0, renorm=0),
+    "softmax_topk": cfg(8, 2, score_fn=0, renorm=1, rho=2.5),
+    "sigmoid": cfg(16, 3, score_fn=1, renorm=0, rho=1.5),
+    "sigmoid_renorm_groups": cfg(16, 4, score_fn=1, renorm=1, n_groups=4, topk_groups=2, group_score=1, rho=2.5),
+    "softmax_k_eq_e": cfg(4, 4, score_fn=0, renorm=1),
+}
+
+
+FD_EPS = 2.0 ** -16
+
+
+def _grid_logits(seed, T, E):
+    """Logits on the grid 2^-16 with |l| < 2^7, so that l +- 2^-16 * v for small integer v
+    is an exact fp32 value and the finite difference sees exactly the step it divides by."""
+    l = synth.synthetic_logits(seed, T, E).astype(np.float64)
+    assert np.abs(l).max() < 100.0
+    return (np.round(l / FD_EPS) * FD_EPS).astype(np.float32)
+
+
+@pytest.mark.parametrize("name", list(ROUTER_BWD))
+def test_router_backward_matches_finite_differences_of_the_weights(name):
+    """With the chosen experts fixed, <g, w(l + eps v) - w(l - eps v)> / (2 eps) equals
+    <dl, v> for dl = router_backward(g), up to O(eps^2)."""
+    c = ROUTER_BWD[name]
+    T, E, k = 24, c["E"], c["k"]
+    l = _grid_logits(30, T, E)
+    idx, _ = oracle.route(l, c)
+    g = synth.normal(30, 1, (T, k), 1.0, "f32").astype(np.float64)
+    dl = oracle.router_backward(c, l, idx, g)
+    eps = FD_EPS
+    v = np.round(synth.normal(30, 2, (T, E), 2.0, "f32").astype(np.float64))
+    lp, lm = (l.astype(np.float64) + eps * v).astype(np.float32), (l.astype(np.float64) - eps * v).astype(np.float32)
+    assert np.array_equal(lp.astype(np.float64) - l, eps * v) and np.array_equal(l - lm.astype(np.float64), eps * v)
+    ip, wp = oracle.route(lp, c)
+    im, wm = oracle.route(lm, c)
+    assert np.array_equal(ip, idx) and np.array_equal(im, idx), "a step this small changed a choice"
+    fd = np.sum(g * (wp - wm), axis=1) / (2 * eps)
+    an = np.sum(dl * v, axis=1)
+    assert np.allclose(fd, an, rtol=1e-6, atol=1e-8 * np.abs(an).max())
+    # experts no weight depends on get no gradient
+    chosen = np.zeros((T, E), bool)
+    np.put_along_axis(chosen, idx.astype(np.int64), True, axis=1)
+    if not (c["score_fn"] == 0 and c["renorm"] == 0):
+        assert np.all(dl[~chosen] == 0.0)
+
+
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_router_backward_softmax_is_shift_invariant(renorm):
+    """Softmax weights do not change when every logit of a token moves by the same amount,
+    so each token's logit gradient sums to zero; with k = E and renorm the weight step is
+    the plain softmax, whose Jacobian-vector product is p * (g - <g, p>)."""
+    c = cfg(8, 3, score_fn=0, renorm=renorm, rho=1.7)
+    T = 40
+    l = synth.synthetic_logits(31, T, 8)
+    idx, _ = oracle.route(l, c)
+    g = synth.normal(31, 1, (T, 3), 1.0, "f32").astype(np.float64)
+    dl = oracle.router_backward(c, l, idx, g)
+    assert np.allclose(dl.sum(axis=1), 0.0, atol=1e-14 * np.abs(dl).max())
+    ce = cfg(6, 6, score_fn=0, renorm=1)
+    le = synth.synthetic_logits(32, T, 6)
+    ie, _ = oracle.route(le, ce)
+    ge = synth.normal(32, 1, (T, 6), 1.0, "f32").astype(np.float64)
+    p = np.exp(le.astype(np.float64) - le.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    gp = np.zeros((T, 6))
+    np.put_along_axis(gp, ie.astype(np.int64), ge, axis=1)  # g in expert order
+    want = p * (gp - np.sum(gp * p, axis=1, keepdims=True))
+    assert np.allclose(oracle.router_backward(ce, le, ie, ge), want, rtol=1e-12, atol=1e-15)
+
+
+def test_router_backward_sigmoid_without_renorm_is_the_logistic_derivative():
+    """Without normalisation each weight is rho * sigma(l_i) alone: dl_i = rho g_i s_i (1 - s_i)."""
+    c = cfg(8, 2, score_fn=1, renorm=0, rho=3.0)
+    l = synth.synthetic_logits(33, 16, 8)
+    idx, _ = oracle.route(l, c)
+    g = synth.normal(33, 1, (16, 2), 1.0, "f32").astype(np.float64)
+    dl = oracle.router_backward(c, l, idx, g)
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(l.astype(np.float64), idx.astype(np.int64), axis=1)))
+    assert np.allclose(np.take_along_axis(dl, idx.astype(np.int64), axis=1), 3.0 * g * s * (1 - s), rtol=1e-13)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "dsv3"])
+def test_layer_backward_through_the_router_matches_finite_differences(name):
+    """L = <dy, y> as a function of the logits (selection fixed): the combine backward's
+    dtopk_w fed through router_backward gives dL/dlogits; the linear router's products give
+    dL/dW_router = dl^T x and x's share dl W_router, checked on the linear map's definition."""
+    w = {"mixtral": small("mixtral_bf16", T=10, H=32, E=4, F=24, renorm=1),
+         "dsv3": small("dsv3_bf16", T=8, H=32, E=8, k=2, F=16, F_shared=16, n_groups=2, topk_groups=1)}[name]
+    inp = {kk: (v.astype(np.float64) if isinstance(v, np.ndarray) else v)
+           for kk, v in synth.host_inputs(w, seed=24).items()}
+    l = _grid_logits(24, w["T"], w["E"])
+    fwd = oracle.forward(w, inp, logits=l)
+    dy = synth.normal(24, 11, (w["T"], w["H"]), 1.0, "f32").astype(np.float64)
+    g = oracle.backward(w, inp, fwd, dy)
+    dl = oracle.router_backward(w, l, fwd["topk_idx"], g["dtopk_w"])
+    eps = FD_EPS
+    v = np.round(synth.normal(24, 12, l.shape, 2.0, "f32").astype(np.float64))
+
+    def L(sign):
+        lx = (l.astype(np.float64) + sign * eps * v).astype(np.float32)
+        o = oracle.forward(w, inp, logits=lx)
+        assert np.array_equal(o["topk_idx"], fwd["topk_idx"])
+        return float(np.sum(o["y"] * dy))
+
+    fd = (L(1) - L(-1)) / (2 * eps)
+    an = float(np.sum(dl * v))
+    assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3), (fd, an)
+    # the linear router: logits = x W^T, so <dl, dlogits> = <dW, dWdir> + <dx_r, dxdir>
+    dwr, dxr = oracle.router_linear_backward(inp["x"], inp["w_router"], dl)
+    vx = synth.normal(24, 13, inp["x"].shape, 1.0, "f32").astype(np.float64)
+    vw = synth.normal(24, 14, inp["w_router"].shape, 1.0, "f32").astype(np.float64)
+    x64, w64 = inp["x"].astype(np.float64), inp["w_router"].astype(np.float64)
+    dlog = vx @ w64.T + x64 @ vw.T  # the exact first-order change of the logits
+    assert np.isclose(np.sum(dl * dlog), np.sum(dwr * vw) + np.sum(dxr * vx), rtol=1e-12)
+
+
 # ------------------------------------------------------------------ aux load-balancing loss
 def test_aux_loss_closed_forms():
     T, E, k = 64, 8, 2
