@@ -79,6 +79,7 @@ def _L():
             "oc_expert_mlp_backward": (None, [P, i64, i32, i32, P, P, P, P, P, P, P, P]),
             "oc_dispatch_backward": (None, [P, P, i32, i32, i32, i32, P]),
             "oc_router_backward": (None, [P, i32, i32, i32, P, i32, i32, f64, P, P]),
+            "oc_aux_loss_backward": (None, [P, P, i32, i32, i32, i32, f64, P]),
             "oc_dense_forward": (i32, [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f64, P, P, P, i32, P, P, P, P]),
         }
@@ -401,6 +402,16 @@ def router_backward(cfg: dict, logits, topk_idx, dtopk_w) -> np.ndarray:
     dl = np.empty((T, E), dtype=np.float64)
     _L().oc_router_backward(_p(l), T, E, k, _p(idx), cfg["score_fn"], cfg["renorm"], float(cfg["routed_scale"]),
                             _p(dw), _p(dl))
+    return dl
+
+
+def aux_loss_backward(logits, counts, k: int, score_fn: int, alpha: float = 0.01) -> np.ndarray:
+    """dL_aux/dlogits [T, E] (fp64) of aux_loss, the routed counts held fixed."""
+    l = _c(logits, np.float32)
+    cn = _c(counts, np.int32)
+    T, E = l.shape
+    dl = np.zeros((T, E), dtype=np.float64)
+    _L().oc_aux_loss_backward(_p(l), _p(cn), T, E, k, score_fn, float(alpha), _p(dl))
     return dl
 
 

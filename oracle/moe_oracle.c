@@ -452,6 +452,37 @@ void oc_combine(const double* yd, const int32_t* tok_row, const double* w, const
 /* steps, in fp64, in the reverse order.                                                 */
 /* ------------------------------------------------------------------------------------ */
 
+/* Backward of the auxiliary loss above, counts held fixed (they are integers): with      */
+/* a_e = alpha * E * c_e / (T^2 * k) = dL/dp_hat[t,e] for every token, and p_hat the      */
+/* normalised probabilities, adds to dl[t,:]                                              */
+/*   softmax:  p_hat_e (a_e - sum_j a_j p_hat_j)                                          */
+/*   sigmoid:  s_e (1 - s_e) (a_e - sum_j a_j p_hat_j) / sum_j s_j                         */
+void oc_aux_loss_backward(const float* logits, const int32_t* counts, int T, int E, int k, int score_fn,
+                          double alpha, double* dl) {
+  if (T == 0) return;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    double* d = dl + (int64_t)t * E;
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double sum = 0.0, c = 0.0;
+    if (score_fn == 0) {
+      double m = -INFINITY;
+      for (int e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+      for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - m); sum += p[e]; }
+    } else {
+      for (int e = 0; e < E; ++e) { p[e] = 1.0 / (1.0 + exp(-(double)l[e])); sum += p[e]; }
+    }
+    const double a0 = alpha * (double)E / ((double)T * (double)T * (double)k);
+    for (int e = 0; e < E; ++e) c += a0 * (double)counts[e] * p[e] / sum;
+    for (int e = 0; e < E; ++e) {
+      const double de = a0 * (double)counts[e] - c;
+      d[e] += score_fn == 0 ? p[e] / sum * de : p[e] * (1.0 - p[e]) * de / sum;
+    }
+    free(p);
+  }
+}
+
 /* Router backward. The top-k choice is a piecewise-constant function of the logits and  */
 /* is held fixed; the chosen weights are w = rho * f(l) with f the weight step of          */
 /* route_one. With g[j] = rho * dw[t,j] (dw = dL/dw, the combine backward's result):        */

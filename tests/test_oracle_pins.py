@@ -729,6 +729,30 @@ def test_layer_backward_through_the_router_matches_finite_differences(name):
 
 
 # ------------------------------------------------------------------ aux load-balancing loss
+@pytest.mark.parametrize("score_fn", [0, 1])
+def test_aux_loss_backward_matches_finite_differences(score_fn):
+    """With the counts fixed, (L(l + eps v) - L(l - eps v)) / (2 eps) = <dL/dl, v>; and for
+    softmax each token's gradient sums to zero (the loss does not see a shift of a row)."""
+    T, E, k = 32, 8, 2
+    l = _grid_logits(34, T, E)
+    counts = oracle.permute(oracle.route(l, cfg(E, k))[0], E)[0]
+    dl = oracle.aux_loss_backward(l, counts, k, score_fn, 0.01)
+    v = np.round(synth.normal(34, 2, (T, E), 2.0, "f32").astype(np.float64))
+    lp = (l.astype(np.float64) + FD_EPS * v).astype(np.float32)
+    lm = (l.astype(np.float64) - FD_EPS * v).astype(np.float32)
+    fd = (oracle.aux_loss(lp, counts, k, score_fn, 0.01)[0] - oracle.aux_loss(lm, counts, k, score_fn, 0.01)[0]) / (
+        2 * FD_EPS)
+    an = float(np.sum(dl * v))
+    assert abs(fd - an) <= 1e-6 * abs(an), (fd, an)
+    if score_fn == 0:
+        assert np.allclose(dl.sum(axis=1), 0.0, atol=1e-14 * np.abs(dl).max())
+    # uniform counts make the loss alpha * E / (T k) * (T k / E) * sum_e Pbar_e = alpha for
+    # softmax, whatever the logits: its gradient vanishes
+    flat = np.full(E, T * k // E, np.int32)
+    if score_fn == 0:
+        assert np.abs(oracle.aux_loss_backward(l, flat, k, 0, 0.01)).max() < 1e-18
+
+
 def test_aux_loss_closed_forms():
     T, E, k = 64, 8, 2
     c8 = cfg(E, k)
