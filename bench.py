@@ -461,8 +461,10 @@ def run_gpu(args, w):
 
 
 def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
-    """moe_backward after the forward whose workspace is ws, and its three staged calls
-    (combine backward, grouped MLP backward, dispatch backward), L2 flushed before each."""
+    """moe_backward after the forward whose workspace is ws (with the router's backward and
+    the auxiliary loss's gradient), the same call without the router, and the staged calls
+    (combine backward, grouped MLP backward, router backward, the fused input gradient and
+    the plain dispatch backward), L2 flushed before each."""
     import torch
     import token_routing_expert_router_gb300 as moe
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
@@ -480,14 +482,27 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
         grads.update(dws_gate=torch.empty((Fs, H), dtype=torch.float32, device=dev),
                      dws_up=torch.empty((Fs, H), dtype=torch.float32, device=dev),
                      dws_down=torch.empty((H, Fs), dtype=torch.float32, device=dev))
+    rgrads = dict(grads, dw_router=torch.empty((E, H), dtype=torch.float32, device=dev),
+                  dlogits=torch.empty((T, E), dtype=torch.float32, device=dev), aux_loss_coeff=0.01)
+    if wts.get("router_bias") is not None:
+        rgrads["d_router_bias"] = torch.empty((E,), dtype=torch.float32, device=dev)
+    rws = torch.zeros(moe.moe_router_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device=dev)
+    moe.moe_workspace_init(rws)
     dyd = torch.empty((rows, H), dtype=dt, device=dev)
     dxd = torch.empty((rows, H), dtype=dt, device=dev)
     moe.moe_forward(cfg, x, wts, torch.empty((T, H), dtype=dt, device=dev), ws)
     stages = {
-        "backward": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
+        "backward": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, rgrads, bws),
+        "backward_without_router": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
         "combine_backward": lambda: moe.moe_combine_backward(cfg, dy, b["yd"], b["tok_row"], b["w"], dyd, dtw),
         "grouped_mlp_backward": lambda: moe.moe_grouped_mlp_backward(cfg, b["xd"], x, b["offsets"], wts, dyd, dxd,
                                                                      grads, bws),
+        "router_backward": lambda: moe.moe_router_backward(cfg, b["logits"], b["idx"], dtw, x, rgrads["dlogits"],
+                                                           rgrads["dw_router"], rws,
+                                                           d_router_bias=rgrads.get("d_router_bias"),
+                                                           counts=b["counts"], aux_alpha=0.01),
+        "dispatch_router_backward": lambda: moe.moe_dispatch_router_backward(cfg, dxd, b["tok_row"], rgrads["dlogits"],
+                                                                             wts["w_router"], dx),
         "dispatch_backward": lambda: moe.moe_dispatch_backward(cfg, dxd, b["tok_row"], dx),
     }
     for f in stages.values():
@@ -503,7 +518,7 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
             e1.record(stream)
             times[n].append((e0, e1))
     torch.cuda.synchronize()
-    assert moe.moe_read_status(bws) == moe.MOE_OK
+    assert moe.moe_read_status(bws) == moe.MOE_OK and moe.moe_read_status(rws) == moe.MOE_OK
     ms = {n: statistics.median(a.elapsed_time(bb) for a, bb in v) for n, v in times.items()}
     flops = 2.0 * synth.gemm_flops(w)  # dgrad + wgrad, each the forward GEMMs' flops
     recompute = synth.gemm_flops(w) * 2.0 / 3.0  # the gate/up GEMM run again
@@ -513,8 +528,11 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
             "ms_per_step": round(ms["backward"], 4), "stages_ms": {n: round(v, 4) for n, v in ms.items() if n != "backward"},
             "grouped_gemm_tflops": round(tf, 1), "grouped_gemm_frac_of_peak": round(tf / peak, 3),
             "algorithmic_flops": flops, "recompute_flops": recompute,
-            "note": "dgrad + wgrad flops over the grouped MLP backward time (the gate/up recompute is extra work "
-                    "in that time); weight gradients fp32; L2 flushed before each call"}
+            "router_flops": 4.0 * T * H * E,
+            "note": "the step: moe_backward with the router's backward and the auxiliary loss's gradient; "
+                    "dgrad + wgrad flops over the grouped MLP backward time (the gate/up recompute is extra work "
+                    "in that time); router_flops: dW_router and dx's router share (fp32 SIMT); weight gradients "
+                    "fp32; L2 flushed before each call"}
 
 
 def launches_per_forward(w):

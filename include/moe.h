@@ -20,8 +20,10 @@
  *   moe_combine         S7  y[t] = sum_j w[t,j] * yd[tok_row[t,j]] (+ shared row)
  *   moe_forward         S0-S7 in one stream-ordered call
  *   moe_forward_host    the same with the tokens and the output in host memory
- *   moe_backward        the training step's backward of S3-S7 (bf16 layers): combine,
- *                       the experts' grouped dgrad/wgrad with recomputed SwiGLU, dispatch
+ *   moe_backward        the training step's backward of S0-S7 (bf16 layers): combine,
+ *                       the experts' grouped dgrad/wgrad with recomputed SwiGLU, dispatch,
+ *                       and (optionally) the router and the auxiliary loss
+ *   moe_router_backward the router's backward: dlogits, dW_router, d bias
  *
  * Conventions shared by every call:
  *  - Every data pointer is DEVICE memory owned by the caller; the library allocates
@@ -105,14 +107,19 @@ typedef struct {
 } moe_weights_t;
 
 /* Weight gradients written by the backward (device fp32, caller-owned; overwritten, not
- * accumulated). */
+ * accumulated). The router fields are optional: with dw_router = NULL, moe_backward leaves
+ * the router out and its dx holds the gradient through the experts only. */
 typedef struct {
-  float* dw_gate;  /* [E, F, H] */
-  float* dw_up;    /* [E, F, H] */
-  float* dw_down;  /* [E, H, F] */
-  float* dws_gate; /* shared expert [F, H], or NULL when n_shared = 0 */
-  float* dws_up;   /* [F, H] */
-  float* dws_down; /* [H, F] */
+  float* dw_gate;       /* [E, F, H] */
+  float* dw_up;         /* [E, F, H] */
+  float* dw_down;       /* [E, H, F] */
+  float* dws_gate;      /* shared expert [F, H], or NULL when n_shared = 0 */
+  float* dws_up;        /* [F, H] */
+  float* dws_down;      /* [H, F] */
+  float* dw_router;     /* [E, H], or NULL: no router backward */
+  float* d_router_bias; /* [E], or NULL: not written (the column sums of dlogits) */
+  float* dlogits;       /* [T, E], or NULL: kept in the backward workspace */
+  float aux_loss_coeff; /* alpha of moe_aux_loss, whose gradient joins dlogits; 0: none */
 } moe_weight_grads_t;
 
 /* MX scale atoms. The UE8M0 codes (code = s + 127 for the block scale 2^s) of an e4m3
@@ -272,8 +279,9 @@ moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host, const
  * Backward (a training step; bf16 layers on the tensor-core path, H % 256 == 0 and
  * F % 256 == 0, else MOE_ERR_UNSUPPORTED). The routing (map, weights, permutation) is that
  * of the forward and is held fixed: these calls return the gradient of the layer output with
- * respect to x through the experts, to the routing weights and to the expert weights. The
- * router's own backward (to its logits and weight) is not part of them. The experts' grouped
+ * respect to x through the experts, to the routing weights and to the expert weights, and
+ * (moe_router_backward, moe_dispatch_router_backward) through the router to its logits, its
+ * weight and bias and x. The experts' grouped
  * GEMMs serve the backward as in the forward (Megatron-Core summary, section 2.4), and the
  * SwiGLU activation is recomputed from the dispatched rows instead of being kept from the
  * forward (section 2.2, recomputation).
@@ -312,11 +320,53 @@ moe_status_t moe_dispatch_backward(const moe_config_t* cfg, const void* dxd, con
 /* The three calls above in one stream-ordered call after moe_forward: the routing, the
  * dispatched rows and yd are read from that call's workspace fwd_ws (so it must not have
  * been reused in between), x and w are the forward's inputs, dy [T,H] bf16. Writes
- * dx [T,H] bf16, dtopk_w [T,k] fp32 and the weight gradients. bwd_ws:
+ * dx [T,H] bf16, dtopk_w [T,k] fp32 and the weight gradients. With grads->dw_router set it
+ * also runs the router's backward below on the forward's logits, map and counts (adding the
+ * auxiliary loss's gradient when grads->aux_loss_coeff != 0) and forms dx with
+ * moe_dispatch_router_backward, so that dx holds both shares. bwd_ws:
  * moe_backward_workspace_size bytes. */
 moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                           const void* dy, const void* fwd_ws, void* dx, float* dtopk_w,
                           const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream);
+
+/* Router backward (the router scores every token against the experts, Megatron-Core
+ * summary, "O essencial"; the weights are the softmax or sigmoid of the chosen scores).
+ * The chosen experts are held fixed, so with g = routed_scale * dtopk_w[t, :]:
+ *   softmax, not renormalised (p = softmax of all E logits):
+ *       dlogits[t, e] = [e chosen as j] g_j p_e - p_e * sum_j g_j p_{i_j}
+ *   softmax renormalised over the chosen (q_j = their softmax):
+ *       dlogits[t, i_j] = q_j (g_j - sum_i g_i q_i)
+ *   sigmoid s, renormalised (S = sum of the chosen s):
+ *       dlogits[t, i_j] = s_j (1 - s_j) (g_j - sum_i g_i s_i / S) / S
+ *   sigmoid, not renormalised:  dlogits[t, i_j] = g_j s_j (1 - s_j)
+ * (zero for experts not chosen, except in the first form). With counts != NULL the
+ * gradient of moe_aux_loss's loss (coefficient aux_alpha, counts held fixed) is added:
+ *   a_e = aux_alpha * E * counts[e] / (T^2 k),  p_hat the loss's normalised probabilities,
+ *   softmax: p_hat_e (a_e - sum a p_hat);  sigmoid: s_e (1 - s_e) (a_e - sum a p_hat) / sum s.
+ * Then, for the linear router logits = x W_router^T (+ bias):
+ *   dw_router[e, h] = sum_t dlogits[t, e] x[t, h],  d_router_bias[e] = sum_t dlogits[t, e],
+ * summed in fp32 over token slices whose partial sums are added in a fixed order.
+ * logits [T,E] fp32 (moe_router_logits), topk_idx [T,k] (moe_route; an id out of range sets
+ * MOE_ERR_DEVICE_BAD_INPUT in the status word and leaves that token's row unwritten),
+ * dtopk_w [T,k] fp32 (moe_combine_backward), x [T,H] act dtype, H % 8 == 0 (else
+ * MOE_ERR_UNSUPPORTED). Outputs fp32: dlogits [T,E]; dw_router [E,H] or NULL (then x may be
+ * NULL and no weight gradient is formed); d_router_bias [E] or NULL.
+ * ws: moe_router_backward_workspace_size bytes (status head + partial sums), zeroed once
+ * with moe_workspace_init. */
+moe_status_t moe_router_backward_workspace_size(const moe_config_t* cfg, size_t* bytes);
+moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, const int32_t* topk_idx,
+                                 const float* dtopk_w, const int32_t* counts, float aux_alpha, const void* x,
+                                 float* dlogits, float* dw_router, float* d_router_bias, void* ws,
+                                 moe_stream_t stream);
+
+/* The input gradient's two shares in one pass (bf16 layers):
+ *   dx[t] = sum_e dlogits[t, e] W_router[e]  +  sum_{j<k} dxd[tok_row[t, j]]  (+ dxd[R + t])
+ * accumulated in fp32 in that order and written once in bf16. dxd = NULL leaves the
+ * dispatch share out (dx = the router's share alone; tok_row is then not read). tok_row is
+ * the forward's map, trusted as in moe_dispatch_backward. H % 8 == 0. */
+moe_status_t moe_dispatch_router_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row,
+                                          const float* dlogits, const void* w_router, void* dx,
+                                          moe_stream_t stream);
 
 /* Offline weight preparation for the E4M3 variant: quantise a bf16 [rows, cols] matrix in
  * br x bc blocks with the rule of moe_dispatch; q [rows, cols] e4m3, scale

@@ -119,6 +119,42 @@ def test_variant_mismatches_rejected_on_host(L):
     assert L.moe_quantize_e4m3(P(4096), 128, 128, 64, 128, P(4096), P(4096), None) == moe.MOE_ERR_UNSUPPORTED
 
 
+def test_router_backward_rejected_on_host(L):
+    """The router backward's argument rules: the bias gradient only with the weight's, H a
+    multiple of 8, 16-byte aligned buffers, a finite loss coefficient; the fused input
+    gradient only for bf16 layers."""
+    import ctypes
+    P = ctypes.c_void_p
+    c = cfg()
+    rb = lambda cc, **kw: L.moe_router_backward(
+        ctypes.byref(cc), kw.get("logits", P(4096)), P(4096), P(4096), kw.get("counts"),
+        ctypes.c_float(kw.get("alpha", 0.0)), kw.get("x", P(4096)), kw.get("dl", P(4096)), kw.get("dw", P(4096)),
+        kw.get("db"), P(4096), None)
+    assert rb(c, dw=None, db=P(4096)) == moe.MOE_ERR_INVALID_ARG
+    assert rb(c, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert rb(c, logits=P(4096 + 4)) == moe.MOE_ERR_INVALID_ARG
+    assert rb(c, counts=P(4096 + 8)) == moe.MOE_ERR_INVALID_ARG
+    assert rb(c, alpha=float("nan")) == moe.MOE_ERR_INVALID_ARG
+    assert rb(c, dl=None) == moe.MOE_ERR_INVALID_ARG
+    assert rb(cfg(H=100)) == moe.MOE_ERR_UNSUPPORTED
+    ir = lambda cc, **kw: L.moe_dispatch_router_backward(ctypes.byref(cc), kw.get("dxd", P(4096)),
+                                                         kw.get("tok_row", P(4096)), P(4096), P(4096), P(4096), None)
+    assert ir(cfg(act_dtype=moe.F32)) == moe.MOE_ERR_UNSUPPORTED
+    assert ir(cfg(H=100)) == moe.MOE_ERR_UNSUPPORTED
+    assert ir(c, tok_row=None) == moe.MOE_ERR_INVALID_ARG
+    assert ir(c, dxd=P(4096 + 2)) == moe.MOE_ERR_INVALID_ARG
+    # moe_backward: the router fields follow the same rules
+    bf = cfg(H=256)
+    g = moe.MoEWeightGrads.from_tensors({"dw_gate": 4096, "dw_up": 4096, "dw_down": 4096, "d_router_bias": 4096})
+    w = moe.MoEWeights.from_tensors({"w_router": 4096, "w_gate": 4096, "w_up": 4096, "w_down": 4096})
+    assert L.moe_backward(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096), P(4096),
+                          ctypes.byref(g), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    # the router backward's workspace: the status head and S slices of [E, H] + [E] partials
+    n = moe.moe_router_backward_workspace_size(c)
+    assert n % 256 == 0 and n >= 256 + c.E * c.H * 4 + c.E * 4
+    assert moe.moe_backward_workspace_size(bf) > moe.moe_router_backward_workspace_size(bf)
+
+
 @pytest.mark.parametrize("T,k,E,shared", [(64, 2, 8, 0), (300, 8, 16, 1), (1, 1, 4, 0), (0, 2, 8, 1)])
 def test_mx_scale_bytes_follow_the_atom_layout(L, T, k, E, shared):
     """Each expert's rows start a fresh 128-row atom row (at ceil((offsets[e] + 127 e) / 128)),

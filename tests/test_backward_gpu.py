@@ -91,6 +91,21 @@ def test_backward_against_oracle(w):
     b["offsets"].copy_(up(ref_fwd["offsets"]))
     b["tok_row"].copy_(up(ref_fwd["tok_row"]))
     got = run_staged_backward(w, d, b, up(dy_h, torch.bfloat16))
+    # the router's backward on the same routing: dlogits, dW_router, and dx with both shares
+    cfg = b["cfg"]
+    rws = torch.zeros(moe.moe_router_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(rws)
+    dl = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    dwr = torch.empty((E, H), dtype=torch.float32, device="cuda")
+    moe.moe_router_backward(cfg, up(logits), up(ref_fwd["topk_idx"]), got["dtopk_w"], d["x"], dl, dwr, rws)
+    dx_all = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx_all)
+    assert moe.moe_read_status(rws) == moe.MOE_OK
+    dl_ref = oracle.router_backward(w, logits, ref_fwd["topk_idx"], ref["dtopk_w"])
+    dwr_ref, dxr_ref = oracle.router_linear_backward(inp["x"], inp["w_router"], dl_ref)
+    assert oracle.rel_l2(np_of(dl).astype(np.float64), dl_ref) < TOL
+    assert oracle.rel_l2(np_of(dwr).astype(np.float64), dwr_ref) < TOL
+    assert oracle.rel_l2(np_of(dx_all.float()).astype(np.float64), ref["dx"] + dxr_ref) < TOL
     g = {key: np_of(v).astype(np.float64) for key, v in got.items()}
     assert oracle.rel_l2(g["dyd"], ref["dyd"]) < TOL
     assert oracle.rel_l2(g["dtopk_w"], ref["dtopk_w"]) < TOL
@@ -134,6 +149,14 @@ def test_backward_after_forward_equals_staged(w):
     g1 = grads_alloc(w)
     moe.moe_backward(cfg, d["x"], weights_arg(d), dy, fws, dx, dtw, g1, bws)
     assert moe.moe_read_status(bws) == moe.MOE_OK
+    # with the router (and the auxiliary loss's gradient): dx gains the router's share
+    dx_r = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    g2 = grads_alloc(w)
+    g2.update(dw_router=torch.empty((E, H), dtype=torch.float32, device="cuda"),
+              d_router_bias=torch.empty((E,), dtype=torch.float32, device="cuda"),
+              dlogits=torch.empty((T, E), dtype=torch.float32, device="cuda"))
+    moe.moe_backward(cfg, d["x"], weights_arg(d), dy, fws, dx_r, dtw, dict(g2, aux_loss_coeff=0.01), bws)
+    assert moe.moe_read_status(bws) == moe.MOE_OK
     # staged, on the same routing (the permutation rebuilt from the forward's map)
     b = alloc(w)
     moe.moe_route_from_map(b["cfg"], idx, b["counts"], b["offsets"], b["row_token"], b["tok_row"], b["ws"])
@@ -143,6 +166,25 @@ def test_backward_after_forward_equals_staged(w):
     assert torch.equal(got["dtopk_w"], dtw)
     for key in g1:
         assert torch.equal(got[key], g1[key]), key
+        assert torch.equal(got[key], g2[key]), key
+    # the router's staged calls on the forward's logits (moe_router_logits recomputes them)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(cfg, d["x"], d["w_router"], d.get("router_bias"), logits, b["ws"])
+    rws = torch.zeros(moe.moe_router_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(rws)
+    dl = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    dwr = torch.empty((E, H), dtype=torch.float32, device="cuda")
+    db = torch.empty((E,), dtype=torch.float32, device="cuda")
+    moe.moe_router_backward(cfg, logits, idx, got["dtopk_w"], d["x"], dl, dwr, rws, d_router_bias=db,
+                            counts=b["counts"], aux_alpha=0.01)
+    dx2 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx2)
+    assert moe.moe_read_status(rws) == moe.MOE_OK
+    assert torch.equal(dl, g2["dlogits"])
+    assert torch.equal(dwr, g2["dw_router"])
+    assert torch.equal(db, g2["d_router_bias"])
+    assert torch.equal(dx2, dx_r)
+    assert not torch.equal(dx_r, dx)
 
 
 def test_backward_no_tokens_gives_zero_weight_gradients():
@@ -151,6 +193,8 @@ def test_backward_no_tokens_gives_zero_weight_gradients():
     inp = synth.host_inputs(synth.scaled(CASES[1], T=4), seed=33)
     d = device_weights_from_host(synth.scaled(CASES[1], T=4), inp)
     g = grads_alloc(w)
+    g.update(dw_router=torch.empty((w["E"], w["H"]), dtype=torch.float32, device="cuda"),
+             d_router_bias=torch.empty((w["E"],), dtype=torch.float32, device="cuda"))
     for v in g.values():
         v.fill_(7.0)
     bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")

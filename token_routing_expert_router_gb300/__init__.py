@@ -64,13 +64,16 @@ class MoEWeights(ctypes.Structure):
 
 
 class MoEWeightGrads(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw_up", "dw_down", "dws_gate", "dws_up", "dws_down")]
+    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw_up", "dw_down", "dws_gate", "dws_up", "dws_down",
+                                        "dw_router", "d_router_bias", "dlogits")] + [("aux_loss_coeff", ctypes.c_float)]
 
     @classmethod
     def from_tensors(cls, d: dict) -> "MoEWeightGrads":
+        """Tensors by field name (absent: NULL); ``aux_loss_coeff`` a number (absent: 0)."""
         g = cls()
-        for name, _ in cls._fields_:
+        for name, _ in cls._fields_[:-1]:
             setattr(g, name, _ptr(d.get(name)))
+        g.aux_loss_coeff = float(d.get("aux_loss_coeff", 0.0))
         return g
 
 
@@ -110,6 +113,9 @@ def lib():
             "moe_grouped_mlp_backward": [cfg, P, P, P, wts, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_dispatch_backward": [cfg, P, P, P, P],
             "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
+            "moe_router_backward_workspace_size": [cfg, POINTER(c_size_t)],
+            "moe_router_backward": [cfg, P, P, P, P, ctypes.c_float, P, P, P, P, P, P],
+            "moe_dispatch_router_backward": [cfg, P, P, P, P, P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
             "moe_grouped_mlp_gather": [cfg, P, P, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
@@ -137,7 +143,8 @@ def exported_symbols() -> list:
             "moe_quantize_e4m3",
             "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
             "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_mlp_backward",
-            "moe_dispatch_backward", "moe_backward",
+            "moe_dispatch_backward", "moe_backward", "moe_router_backward_workspace_size",
+            "moe_router_backward", "moe_dispatch_router_backward",
             "moe_read_status", "moe_status_string", "moe_route_static_scratch",
             "moe_selftest_bounded_wait"]
 
@@ -304,6 +311,28 @@ def moe_backward(cfg, x, weights: dict, dy, fwd_ws, dx, dtopk_w, grads: dict, bw
     g = MoEWeightGrads.from_tensors(grads)
     _check(lib().moe_backward(byref(cfg), _ptr(x), byref(w), _ptr(dy), _ptr(fwd_ws), _ptr(dx), _ptr(dtopk_w),
                               byref(g), _ptr(bwd_ws), _stream(stream)), "moe_backward")
+
+
+def moe_router_backward_workspace_size(cfg: MoEConfig) -> int:
+    n = c_size_t()
+    _check(lib().moe_router_backward_workspace_size(byref(cfg), byref(n)), "moe_router_backward_workspace_size")
+    return n.value
+
+
+def moe_router_backward(cfg, logits, topk_idx, dtopk_w, x, dlogits, dw_router, ws, d_router_bias=None,
+                        counts=None, aux_alpha=0.0, stream=None):
+    """dlogits (and, given dw_router, the router weight and bias gradients) from the
+    routing-weight gradient dtopk_w; counts + aux_alpha add the auxiliary loss's gradient."""
+    _check(lib().moe_router_backward(byref(cfg), _ptr(logits), _ptr(topk_idx), _ptr(dtopk_w), _ptr(counts),
+                                     float(aux_alpha), _ptr(x), _ptr(dlogits), _ptr(dw_router), _ptr(d_router_bias),
+                                     _ptr(ws), _stream(stream)), "moe_router_backward")
+
+
+def moe_dispatch_router_backward(cfg, dxd, tok_row, dlogits, w_router, dx, stream=None):
+    """dx = dlogits W_router + the dispatch backward's sum of dxd rows (dxd None: the
+    router's share alone)."""
+    _check(lib().moe_dispatch_router_backward(byref(cfg), _ptr(dxd), _ptr(tok_row), _ptr(dlogits), _ptr(w_router),
+                                              _ptr(dx), _stream(stream)), "moe_dispatch_router_backward")
 
 
 def moe_quantize_mx(src, q, sf, stream=None):

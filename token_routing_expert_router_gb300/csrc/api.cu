@@ -109,9 +109,10 @@ FwdLayout fwd_layout(const moe_config_t& c) {
 }
 
 // Backward workspace: status head, then dyd, dxd [rows, H], gu [rows, 2F], dgu [prows, 2F],
-// h [prows, F] (prows: every expert's rows padded to a multiple of 64).
+// h [prows, F] (prows: every expert's rows padded to a multiple of 64), then the router's
+// dlogits [T, E] and its weight gradient's per-slice partial sums [S, E, H] and [S, E].
 struct BwdLayout {
-  size_t dyd, dxd, gu, dgu, h, total;
+  size_t dyd, dxd, gu, dgu, h, dl, rpart, rbpart, total;
 };
 
 BwdLayout bwd_layout(const moe_config_t& c) {
@@ -124,18 +125,41 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   };
   const size_t rows = (size_t)total_rows(c);
   const size_t prows = (size_t)tc::backward_padded_rows(c);  // dgu and h: 64-row padded segments
+  const size_t S = (size_t)router_wgrad_slices(c);
   L.dyd = take(rows * c.H * 2);
   L.dxd = take(rows * c.H * 2);
   L.gu = take(rows * 2 * c.F * 2);
   L.dgu = take(prows * 2 * c.F * 2);
   L.h = take(prows * c.F * 2);
+  L.dl = take((size_t)c.T * c.E * 4);
+  L.rpart = take(S * c.E * c.H * 4);
+  L.rbpart = take(S * c.E * 4);
   L.total = o;
   return L;
 }
 
+// moe_router_backward's own workspace: status head, then the partial sums.
+struct RouterBwdLayout {
+  size_t rpart, rbpart, total;
+};
+
+RouterBwdLayout router_bwd_layout(const moe_config_t& c) {
+  RouterBwdLayout L;
+  const size_t S = (size_t)router_wgrad_slices(c);
+  L.rpart = kWsHead;
+  L.rbpart = align_up(L.rpart + S * c.E * c.H * 4, 256);
+  L.total = align_up(L.rbpart + S * c.E * 4, 256);
+  return L;
+}
+
+bool opt_ok(const void* p) { return p == nullptr || aligned16(p); }
+
 bool grads_ok(const moe_config_t& c, const moe_weight_grads_t* g) {
   if (!g || !ptr_ok(g->dw_gate) || !ptr_ok(g->dw_up) || !ptr_ok(g->dw_down)) return false;
   if (c.n_shared && (!ptr_ok(g->dws_gate) || !ptr_ok(g->dws_up) || !ptr_ok(g->dws_down))) return false;
+  if (!opt_ok(g->dw_router) || !opt_ok(g->d_router_bias) || !opt_ok(g->dlogits)) return false;
+  if (!g->dw_router && g->d_router_bias) return false;  // the bias gradient comes with the weight's
+  if (!(g->aux_loss_coeff == g->aux_loss_coeff)) return false;  // NaN
   return true;
 }
 
@@ -511,13 +535,18 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (!tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->T == 0) return moe_grouped_mlp_backward(cfg, nullptr, nullptr, nullptr, w, nullptr, nullptr, grads,
-                                                   bwd_ws, stream);
+  if (cfg->T == 0) {
+    v = moe_grouped_mlp_backward(cfg, nullptr, nullptr, nullptr, w, nullptr, nullptr, grads, bwd_ws, stream);
+    if (v != MOE_OK || !grads->dw_router) return v;
+    return cuda_status(launch_router_wgrad(*cfg, nullptr, nullptr, grads->dw_router, grads->d_router_bias, nullptr,
+                                           nullptr, (cudaStream_t)stream));
+  }
   v = check_weights(*cfg, w, false);
   if (v != MOE_OK) return v;
   if (!ptr_ok(x) || !ptr_ok(dy) || !ptr_ok(fwd_ws) || !ptr_ok(dx) || !ptr_ok(dtopk_w) || !ptr_ok(bwd_ws) ||
       !grads_ok(*cfg, grads))
     return MOE_ERR_INVALID_ARG;
+  if (grads->dw_router && cfg->H % 8) return MOE_ERR_UNSUPPORTED;
   const moe_config_t& c = *cfg;
   cudaStream_t s = (cudaStream_t)stream;
   const FwdLayout F = fwd_layout(c);
@@ -530,8 +559,69 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (e == cudaSuccess)
     e = tc::launch_grouped_mlp_backward(c, fb + F.xd, x, (const int32_t*)(fb + F.offsets), *w, bb + B.dyd,
                                         bb + B.gu, bb + B.dgu, bb + B.h, bb + B.dxd, *grads, status_of(bwd_ws), s);
-  if (e == cudaSuccess) e = launch_combine(c, bb + B.dxd, tok_row, nullptr, dx, s);
+  if (!grads->dw_router) {
+    if (e == cudaSuccess) e = launch_combine(c, bb + B.dxd, tok_row, nullptr, dx, s);
+    return cuda_status(e);
+  }
+  float* dl = grads->dlogits ? grads->dlogits : (float*)(bb + B.dl);
+  const int32_t* counts = grads->aux_loss_coeff != 0.0f ? (const int32_t*)(fb + F.counts) : nullptr;
+  if (e == cudaSuccess)
+    e = launch_router_logit_grad(c, (const float*)(fb + F.logits), (const int32_t*)(fb + F.topk_idx), dtopk_w,
+                                 counts, grads->aux_loss_coeff, dl, status_of(bwd_ws), s);
+  if (e == cudaSuccess)
+    e = launch_router_wgrad(c, dl, x, grads->dw_router, grads->d_router_bias, (float*)(bb + B.rpart),
+                            (float*)(bb + B.rbpart), s);
+  if (e == cudaSuccess) e = launch_router_input_grad(c, dl, w->w_router, bb + B.dxd, tok_row, dx, s);
   return cuda_status(e);
+}
+
+moe_status_t moe_router_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = router_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, const int32_t* topk_idx,
+                                 const float* dtopk_w, const int32_t* counts, float aux_alpha, const void* x,
+                                 float* dlogits, float* dw_router, float* d_router_bias, void* ws,
+                                 moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->H % 8) return MOE_ERR_UNSUPPORTED;
+  if (!opt_ok(counts) || !opt_ok(dw_router) || !opt_ok(d_router_bias) || !(aux_alpha == aux_alpha) ||
+      (!dw_router && d_router_bias))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c.T == 0)
+    return dw_router ? cuda_status(launch_router_wgrad(c, nullptr, nullptr, dw_router, d_router_bias, nullptr,
+                                                       nullptr, s))
+                     : MOE_OK;
+  if (!ptr_ok(logits) || !ptr_ok(topk_idx) || !ptr_ok(dtopk_w) || !ptr_ok(dlogits) || !ptr_ok(ws) ||
+      (dw_router && !ptr_ok(x)))
+    return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_router_logit_grad(c, logits, topk_idx, dtopk_w, counts, aux_alpha, dlogits, status_of(ws), s);
+  if (e == cudaSuccess && dw_router) {
+    const RouterBwdLayout L = router_bwd_layout(c);
+    char* base = (char*)ws;
+    e = launch_router_wgrad(c, dlogits, x, dw_router, d_router_bias, (float*)(base + L.rpart),
+                            (float*)(base + L.rbpart), s);
+  }
+  return cuda_status(e);
+}
+
+moe_status_t moe_dispatch_router_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row,
+                                          const float* dlogits, const void* w_router, void* dx,
+                                          moe_stream_t stream) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (cfg->act_dtype != MOE_DTYPE_BF16 || cfg->H % 8) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ptr_ok(dlogits) || !ptr_ok(w_router) || !ptr_ok(dx) || (dxd && !ptr_ok(tok_row)) || !opt_ok(dxd))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_input_grad(*cfg, dlogits, w_router, dxd, tok_row, dx, (cudaStream_t)stream));
 }
 
 moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,

@@ -63,6 +63,17 @@ cudaError_t launch_dispatch_mx(const moe_config_t& c, const void* x, const int32
 cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
                                cudaStream_t s);
 
+// Router backward (router_bwd.cu). dl: dL/dlogits [T, E] fp32.
+int router_wgrad_slices(const moe_config_t& c);  // token slices of the weight gradient
+cudaError_t launch_router_logit_grad(const moe_config_t& c, const float* logits, const int32_t* topk_idx,
+                                     const float* dtopk_w, const int32_t* counts, float aux_alpha, float* dl,
+                                     DeviceStatus* st, cudaStream_t s);
+// part: router_wgrad_slices * E * H floats, bias_part: router_wgrad_slices * E floats
+cudaError_t launch_router_wgrad(const moe_config_t& c, const float* dl, const void* x, float* dw_router,
+                                float* d_bias, float* part, float* bias_part, cudaStream_t s);
+cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, const void* w_router, const void* dxd,
+                                     const int32_t* tok_row, void* dx, cudaStream_t s);
+
 // SIMT grouped GEMM (fp32 FFMA): C = A . B^T per group, with optional SwiGLU pair.
 // Groups: routed experts g < E over rows [offsets[g], offsets[g+1]) of A, plus an optional
 // extra group (shared expert) over rows [0, T) of A2 written at output row R + t.
