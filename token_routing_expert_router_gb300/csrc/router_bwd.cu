@@ -404,9 +404,10 @@ __global__ void __launch_bounds__(kIgThreads)
 int router_wgrad_slices(const moe_config_t& c) {
   const int bm = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
   const int64_t tiles = ceil_div(c.H, kWgBN) * ceil_div(c.E, bm);
-  // about two blocks per SM of a 152-SM part, and no slice shorter than 256 tokens
-  int64_t s = ceil_div(2 * 152, tiles);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, c.T / 256));
+  // about eight blocks per SM of a 152-SM part (enough loads in flight when the product is
+  // HBM-bound, several waves when it is ALU-bound), and no slice shorter than 128 tokens
+  int64_t s = ceil_div(8 * 152, tiles);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, c.T / 128));
   return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
 }
 
