@@ -502,7 +502,7 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
                                                            d_router_bias=rgrads.get("d_router_bias"),
                                                            counts=b["counts"], aux_alpha=0.01),
         "dispatch_router_backward": lambda: moe.moe_dispatch_router_backward(cfg, dxd, b["tok_row"], rgrads["dlogits"],
-                                                                             wts["w_router"], dx),
+                                                                             wts["w_router"], dx, rws),
         "dispatch_backward": lambda: moe.moe_dispatch_backward(cfg, dxd, b["tok_row"], dx),
     }
     for f in stages.values():
@@ -531,7 +531,8 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
             "router_flops": 4.0 * T * H * E,
             "note": "the step: moe_backward with the router's backward and the auxiliary loss's gradient; "
                     "dgrad + wgrad flops over the grouped MLP backward time (the gate/up recompute is extra work "
-                    "in that time); router_flops: dW_router and dx's router share (fp32 SIMT); weight gradients "
+                    "in that time); router_flops: dW_router and dx's router share (tensor cores when E and H are multiples of "
+                    "256, else fp32 SIMT); weight gradients "
                     "fp32; L2 flushed before each call"}
 
 

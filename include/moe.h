@@ -351,21 +351,29 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
  * dtopk_w [T,k] fp32 (moe_combine_backward), x [T,H] act dtype, H % 8 == 0 (else
  * MOE_ERR_UNSUPPORTED). Outputs fp32: dlogits [T,E]; dw_router [E,H] or NULL (then x may be
  * NULL and no weight gradient is formed); d_router_bias [E] or NULL.
- * ws: moe_router_backward_workspace_size bytes (status head + partial sums), zeroed once
- * with moe_workspace_init. */
+ * ws: moe_router_backward_workspace_size bytes (status head, partial sums, and on the
+ * tensor-core path below dlogits in bf16 and the router's share of dx), initialised with
+ * moe_workspace_init. */
 moe_status_t moe_router_backward_workspace_size(const moe_config_t* cfg, size_t* bytes);
 moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, const int32_t* topk_idx,
                                  const float* dtopk_w, const int32_t* counts, float aux_alpha, const void* x,
                                  float* dlogits, float* dw_router, float* d_router_bias, void* ws,
                                  moe_stream_t stream);
 
-/* The input gradient's two shares in one pass (bf16 layers):
+/* The input gradient's two shares (bf16 layers):
  *   dx[t] = sum_e dlogits[t, e] W_router[e]  +  sum_{j<k} dxd[tok_row[t, j]]  (+ dxd[R + t])
- * accumulated in fp32 in that order and written once in bf16. dxd = NULL leaves the
- * dispatch share out (dx = the router's share alone; tok_row is then not read). tok_row is
- * the forward's map, trusted as in moe_dispatch_backward. H % 8 == 0. */
+ * accumulated in fp32 and written once in bf16; on the tensor-core path (below) the
+ * router's share is first rounded to bf16 and added last. dxd = NULL leaves the dispatch
+ * share out (dx = the router's share alone; tok_row is then not read). tok_row is the
+ * forward's map, trusted as in moe_dispatch_backward. H % 8 == 0. ws:
+ * moe_router_backward_workspace_size bytes, initialised with moe_workspace_init.
+ *
+ * Precision of the router's products: with E % 256 == 0, H % 256 == 0 and bf16 layers
+ * (and k + shared <= 9), dw_router = dl^T x and dl W_router run on the tensor cores with
+ * dlogits rounded to bf16 and fp32 accumulation, as the expert GEMMs do; dlogits itself
+ * stays fp32. Otherwise both are fp32 FMA products. */
 moe_status_t moe_dispatch_router_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row,
-                                          const float* dlogits, const void* w_router, void* dx,
+                                          const float* dlogits, const void* w_router, void* dx, void* ws,
                                           moe_stream_t stream);
 
 /* Offline weight preparation for the E4M3 variant: quantise a bf16 [rows, cols] matrix in

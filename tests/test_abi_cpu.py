@@ -138,11 +138,13 @@ def test_router_backward_rejected_on_host(L):
     assert rb(c, dl=None) == moe.MOE_ERR_INVALID_ARG
     assert rb(cfg(H=100)) == moe.MOE_ERR_UNSUPPORTED
     ir = lambda cc, **kw: L.moe_dispatch_router_backward(ctypes.byref(cc), kw.get("dxd", P(4096)),
-                                                         kw.get("tok_row", P(4096)), P(4096), P(4096), P(4096), None)
+                                                         kw.get("tok_row", P(4096)), P(4096), P(4096), P(4096),
+                                                         kw.get("ws", P(4096)), None)
     assert ir(cfg(act_dtype=moe.F32)) == moe.MOE_ERR_UNSUPPORTED
     assert ir(cfg(H=100)) == moe.MOE_ERR_UNSUPPORTED
     assert ir(c, tok_row=None) == moe.MOE_ERR_INVALID_ARG
     assert ir(c, dxd=P(4096 + 2)) == moe.MOE_ERR_INVALID_ARG
+    assert ir(c, ws=None) == moe.MOE_ERR_INVALID_ARG
     # moe_backward: the router fields follow the same rules
     bf = cfg(H=256)
     g = moe.MoEWeightGrads.from_tensors({"dw_gate": 4096, "dw_up": 4096, "dw_down": 4096, "d_router_bias": 4096})
@@ -152,6 +154,10 @@ def test_router_backward_rejected_on_host(L):
     # the router backward's workspace: the status head and S slices of [E, H] + [E] partials
     n = moe.moe_router_backward_workspace_size(c)
     assert n % 256 == 0 and n >= 256 + c.E * c.H * 4 + c.E * 4
+    # many experts (E, H multiples of 256): dl in bf16 and the router's share of dx instead
+    big = cfg(T=1000, H=512, E=256, k=8)
+    n = moe.moe_router_backward_workspace_size(big)
+    assert n >= 256 + 1000 * 256 * 2 + 1000 * 512 * 2 and n < 256 + 1000 * 256 * 2 + 1000 * 512 * 2 + 64 * 256 * 4 + 1024
     assert moe.moe_backward_workspace_size(bf) > moe.moe_router_backward_workspace_size(bf)
 
 

@@ -27,6 +27,9 @@ CASES = [
     # 192..511 rows per expert: the recomputed gate/up GEMM on two or three m tiles per expert
     synth.scaled(W["dsv3_bf16"], T=520, H=512, E=16, F=256, F_shared=256, n_groups=4, topk_groups=2,
                  name="mid_shared"),
+    # 256 experts: the router's products on the tensor cores (most experts get a few rows)
+    synth.scaled(W["dsv3_bf16"], T=600, H=512, E=256, k=8, F=256, F_shared=256, n_groups=8, topk_groups=4,
+                 name="e256_shared"),
 ]
 TOL = 1e-2  # bf16 layers
 
@@ -99,7 +102,7 @@ def test_backward_against_oracle(w):
     dwr = torch.empty((E, H), dtype=torch.float32, device="cuda")
     moe.moe_router_backward(cfg, up(logits), up(ref_fwd["topk_idx"]), got["dtopk_w"], d["x"], dl, dwr, rws)
     dx_all = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx_all)
+    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx_all, rws)
     assert moe.moe_read_status(rws) == moe.MOE_OK
     dl_ref = oracle.router_backward(w, logits, ref_fwd["topk_idx"], ref["dtopk_w"])
     dwr_ref, dxr_ref = oracle.router_linear_backward(inp["x"], inp["w_router"], dl_ref)
@@ -126,7 +129,8 @@ def test_backward_against_oracle(w):
         assert oracle.rel_l2(g["dxd"][R:], ref["dxd"][R:]) < TOL
 
 
-@pytest.mark.parametrize("w", [CASES[1], CASES[3], CASES[4]], ids=["dsv3_small", "pair_shared", "mid_shared"])
+@pytest.mark.parametrize("w", [CASES[1], CASES[3], CASES[4], CASES[5]],
+                         ids=["dsv3_small", "pair_shared", "mid_shared", "e256_shared"])
 def test_backward_after_forward_equals_staged(w):
     """moe_backward reads the routing, xd and yd from moe_forward's workspace and runs the
     same kernels as the staged calls: identical bits."""
@@ -178,7 +182,7 @@ def test_backward_after_forward_equals_staged(w):
     moe.moe_router_backward(cfg, logits, idx, got["dtopk_w"], d["x"], dl, dwr, rws, d_router_bias=db,
                             counts=b["counts"], aux_alpha=0.01)
     dx2 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx2)
+    moe.moe_dispatch_router_backward(cfg, got["dxd"], b["tok_row"], dl, d["w_router"], dx2, rws)
     assert moe.moe_read_status(rws) == moe.MOE_OK
     assert torch.equal(dl, g2["dlogits"])
     assert torch.equal(dwr, g2["dw_router"])

@@ -115,7 +115,7 @@ def lib():
             "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_router_backward_workspace_size": [cfg, POINTER(c_size_t)],
             "moe_router_backward": [cfg, P, P, P, P, ctypes.c_float, P, P, P, P, P, P],
-            "moe_dispatch_router_backward": [cfg, P, P, P, P, P, P],
+            "moe_dispatch_router_backward": [cfg, P, P, P, P, P, P, P],
             "moe_grouped_mlp": [cfg, P, P, P, P, wts, P, P, P, P, P],
             "moe_grouped_mlp_gather": [cfg, P, P, P, P, P, wts, P, P, P, P],
             "moe_combine": [cfg, P, P, P, P, P],
@@ -328,11 +328,11 @@ def moe_router_backward(cfg, logits, topk_idx, dtopk_w, x, dlogits, dw_router, w
                                      _ptr(ws), _stream(stream)), "moe_router_backward")
 
 
-def moe_dispatch_router_backward(cfg, dxd, tok_row, dlogits, w_router, dx, stream=None):
+def moe_dispatch_router_backward(cfg, dxd, tok_row, dlogits, w_router, dx, ws, stream=None):
     """dx = dlogits W_router + the dispatch backward's sum of dxd rows (dxd None: the
-    router's share alone)."""
+    router's share alone). ws: moe_router_backward_workspace_size bytes."""
     _check(lib().moe_dispatch_router_backward(byref(cfg), _ptr(dxd), _ptr(tok_row), _ptr(dlogits), _ptr(w_router),
-                                              _ptr(dx), _stream(stream)), "moe_dispatch_router_backward")
+                                              _ptr(dx), _ptr(ws), _stream(stream)), "moe_dispatch_router_backward")
 
 
 def moe_quantize_mx(src, q, sf, stream=None):

@@ -112,7 +112,7 @@ FwdLayout fwd_layout(const moe_config_t& c) {
 // h [prows, F] (prows: every expert's rows padded to a multiple of 64), then the router's
 // dlogits [T, E] and its weight gradient's per-slice partial sums [S, E, H] and [S, E].
 struct BwdLayout {
-  size_t dyd, dxd, gu, dgu, h, dl, rpart, rbpart, total;
+  size_t dyd, dxd, gu, dgu, h, dl, rpart, rbpart, dlb, dxr, total;
 };
 
 BwdLayout bwd_layout(const moe_config_t& c) {
@@ -131,25 +131,43 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.gu = take(rows * 2 * c.F * 2);
   L.dgu = take(prows * 2 * c.F * 2);
   L.h = take(prows * c.F * 2);
+  const bool tcr = router_backward_tc(c);
   L.dl = take((size_t)c.T * c.E * 4);
-  L.rpart = take(S * c.E * c.H * 4);
+  L.rpart = take(tcr ? 0 : S * c.E * c.H * 4);
   L.rbpart = take(S * c.E * 4);
+  L.dlb = take(tcr ? (size_t)c.T * c.E * 2 : 0);
+  L.dxr = take(tcr ? (size_t)c.T * c.H * 2 : 0);
   L.total = o;
   return L;
 }
 
-// moe_router_backward's own workspace: status head, then the partial sums.
+// moe_router_backward's and moe_dispatch_router_backward's workspace: status head, then the
+// partial sums of the SIMT path, or dl in bf16 and dx_r on the tensor-core path.
 struct RouterBwdLayout {
-  size_t rpart, rbpart, total;
+  size_t rpart, rbpart, dlb, dxr, total;
 };
 
 RouterBwdLayout router_bwd_layout(const moe_config_t& c) {
   RouterBwdLayout L;
+  size_t o = kWsHead;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
   const size_t S = (size_t)router_wgrad_slices(c);
-  L.rpart = kWsHead;
-  L.rbpart = align_up(L.rpart + S * c.E * c.H * 4, 256);
-  L.total = align_up(L.rbpart + S * c.E * 4, 256);
+  const bool tcr = router_backward_tc(c);
+  L.rpart = take(tcr ? 0 : S * c.E * c.H * 4);
+  L.rbpart = take(S * c.E * 4);
+  L.dlb = take(tcr ? (size_t)c.T * c.E * 2 : 0);
+  L.dxr = take(tcr ? (size_t)c.T * c.H * 2 : 0);
+  L.total = o;
   return L;
+}
+
+RouterScratch router_scratch(char* base, size_t part, size_t bias_part, size_t dlb, size_t dxr) {
+  return RouterScratch{reinterpret_cast<float*>(base + part), reinterpret_cast<float*>(base + bias_part), base + dlb,
+                       base + dxr};
 }
 
 bool opt_ok(const void* p) { return p == nullptr || aligned16(p); }
@@ -538,8 +556,9 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   if (cfg->T == 0) {
     v = moe_grouped_mlp_backward(cfg, nullptr, nullptr, nullptr, w, nullptr, nullptr, grads, bwd_ws, stream);
     if (v != MOE_OK || !grads->dw_router) return v;
-    return cuda_status(launch_router_wgrad(*cfg, nullptr, nullptr, grads->dw_router, grads->d_router_bias, nullptr,
-                                           nullptr, (cudaStream_t)stream));
+    return cuda_status(launch_router_backward(*cfg, nullptr, nullptr, nullptr, nullptr, 0.0f, nullptr, nullptr,
+                                              grads->dw_router, grads->d_router_bias, RouterScratch{},
+                                              nullptr, (cudaStream_t)stream));
   }
   v = check_weights(*cfg, w, false);
   if (v != MOE_OK) return v;
@@ -565,13 +584,14 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
   }
   float* dl = grads->dlogits ? grads->dlogits : (float*)(bb + B.dl);
   const int32_t* counts = grads->aux_loss_coeff != 0.0f ? (const int32_t*)(fb + F.counts) : nullptr;
+  const RouterScratch sc = router_scratch(bb, B.rpart, B.rbpart, B.dlb, B.dxr);
   if (e == cudaSuccess)
-    e = launch_router_logit_grad(c, (const float*)(fb + F.logits), (const int32_t*)(fb + F.topk_idx), dtopk_w,
-                                 counts, grads->aux_loss_coeff, dl, status_of(bwd_ws), s);
+    e = launch_router_backward(c, (const float*)(fb + F.logits), (const int32_t*)(fb + F.topk_idx), dtopk_w, counts,
+                               grads->aux_loss_coeff, x, dl, grads->dw_router, grads->d_router_bias, sc,
+                               status_of(bwd_ws), s);
   if (e == cudaSuccess)
-    e = launch_router_wgrad(c, dl, x, grads->dw_router, grads->d_router_bias, (float*)(bb + B.rpart),
-                            (float*)(bb + B.rbpart), s);
-  if (e == cudaSuccess) e = launch_router_input_grad(c, dl, w->w_router, bb + B.dxd, tok_row, dx, s);
+    e = launch_router_input_grad(c, dl, router_backward_tc(c) ? sc.dl_bf16 : nullptr, w->w_router, bb + B.dxd,
+                                 tok_row, dx, sc, status_of(bwd_ws), s);
   return cuda_status(e);
 }
 
@@ -596,32 +616,31 @@ moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, c
   const moe_config_t& c = *cfg;
   cudaStream_t s = (cudaStream_t)stream;
   if (c.T == 0)
-    return dw_router ? cuda_status(launch_router_wgrad(c, nullptr, nullptr, dw_router, d_router_bias, nullptr,
-                                                       nullptr, s))
-                     : MOE_OK;
+    return cuda_status(launch_router_backward(c, nullptr, nullptr, nullptr, nullptr, 0.0f, nullptr, nullptr, dw_router,
+                                              d_router_bias, RouterScratch{}, nullptr, s));
   if (!ptr_ok(logits) || !ptr_ok(topk_idx) || !ptr_ok(dtopk_w) || !ptr_ok(dlogits) || !ptr_ok(ws) ||
       (dw_router && !ptr_ok(x)))
     return MOE_ERR_INVALID_ARG;
-  cudaError_t e = launch_router_logit_grad(c, logits, topk_idx, dtopk_w, counts, aux_alpha, dlogits, status_of(ws), s);
-  if (e == cudaSuccess && dw_router) {
-    const RouterBwdLayout L = router_bwd_layout(c);
-    char* base = (char*)ws;
-    e = launch_router_wgrad(c, dlogits, x, dw_router, d_router_bias, (float*)(base + L.rpart),
-                            (float*)(base + L.rbpart), s);
-  }
-  return cuda_status(e);
+  const RouterBwdLayout L = router_bwd_layout(c);
+  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr);
+  return cuda_status(launch_router_backward(c, logits, topk_idx, dtopk_w, counts, aux_alpha, x, dlogits, dw_router,
+                                            d_router_bias, sc, status_of(ws), s));
 }
 
 moe_status_t moe_dispatch_router_backward(const moe_config_t* cfg, const void* dxd, const int32_t* tok_row,
-                                          const float* dlogits, const void* w_router, void* dx,
+                                          const float* dlogits, const void* w_router, void* dx, void* ws,
                                           moe_stream_t stream) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (cfg->act_dtype != MOE_DTYPE_BF16 || cfg->H % 8) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
-  if (!ptr_ok(dlogits) || !ptr_ok(w_router) || !ptr_ok(dx) || (dxd && !ptr_ok(tok_row)) || !opt_ok(dxd))
+  if (!ptr_ok(dlogits) || !ptr_ok(w_router) || !ptr_ok(dx) || !ptr_ok(ws) || (dxd && !ptr_ok(tok_row)) ||
+      !opt_ok(dxd))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router_input_grad(*cfg, dlogits, w_router, dxd, tok_row, dx, (cudaStream_t)stream));
+  const RouterBwdLayout L = router_bwd_layout(*cfg);
+  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr);
+  return cuda_status(launch_router_input_grad(*cfg, dlogits, nullptr, w_router, dxd, tok_row, dx, sc, status_of(ws),
+                                              (cudaStream_t)stream));
 }
 
 moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,

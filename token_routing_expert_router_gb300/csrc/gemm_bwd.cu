@@ -12,6 +12,10 @@
 //   WGRAD_DOWN  dWd[e] = dyd_e^T . h_e    K = the expert's token rows, both operands
 //               MN-major (an activation's rows are the K index)
 //   WGRAD_GU    dWg[e], dWu[e] = dgu_e^T . xd_e
+//   DGRAD_PLAIN C = A . B                 K-major A, B read MN-major (its rows are the K
+//               index), a plain bf16 store: the router's share of the input gradient,
+//               dl . W_router, over the tokens as one group (the router's weight gradient
+//               dl^T . x is WGRAD_DOWN over that group)
 // An MN-major operand is loaded by TMA as boxes of 64 MN elements (128 bytes, 128-byte
 // swizzle) x 64 K rows; its shared-memory descriptor has LBO = the byte distance between
 // the 64-element MN blocks (8 KB here), SBO = 1024 B between 8-row K groups, and each MMA
@@ -67,7 +71,7 @@ struct BwdSmem {
       1024 + (size_t)kStages * kStageBytes + 256 + 2 * kMaxGroups * sizeof(int32_t) + kEpiWarps * 2048;
 };
 
-enum Mode { DGRAD_DOWN = 0, DGRAD_GU = 1, WGRAD_DOWN = 2, WGRAD_GU = 3 };
+enum Mode { DGRAD_DOWN = 0, DGRAD_GU = 1, WGRAD_DOWN = 2, WGRAD_GU = 3, DGRAD_PLAIN = 4 };
 
 struct BwdParams {
   const int32_t* offsets;
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ax = kb * BK;
             ay = a_row0 + c.mb * TM + (int)rank * BM;
             a_two_boxes = false;
-            if (MODE == DGRAD_DOWN) {
+            if (MODE == DGRAD_DOWN || MODE == DGRAD_PLAIN) {
               tb = extra ? &tmB0x : &tmB0;
               by = kb * BK;
             } else {  // K = 2F: 128-column blocks alternate gate / up
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t warp_row0 = (int64_t)row0 + c.mb * TM + wrow;
         const int warp_live = c.rows - wrow;
         const bool live = r < c.rows;
-        if (MODE == DGRAD_GU) {
+        if (MODE == DGRAD_GU || MODE == DGRAD_PLAIN) {
           uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN + cbase) * 2;
 #pragma unroll 1
           for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -629,6 +633,54 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   p.w0x = gr.dws_gate;
   p.w1x = gr.dws_up;
   return launch<WGRAD_GU, 2>(a, b0, b0, b0x, b0x, p, (int64_t)ngroups * p.m_tiles_out * p.n_tiles, s);
+}
+
+bool router_backward_tc_supported(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && c.E % 256 == 0 && c.H % 256 == 0;
+}
+
+cudaError_t launch_router_products(const moe_config_t& c, const void* dl_bf16, const void* x, const void* w_router,
+                                   float* dw_router, void* dx_r, DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  // the tokens are one group: the "extra" group of the kernels (no routed groups), rows [0, T)
+  BwdParams p{};
+  p.offsets = nullptr;
+  p.G = 0;
+  p.has_extra = 1;
+  p.T_extra = c.T;
+  p.a2_row_base = 0;
+  p.status = st;
+  p.timeout_ns = kTimeoutNs;
+  CUtensorMap a, b;
+  cudaError_t e = cudaSuccess;
+  if (dw_router) {
+    // dW_router = dl^T x: M_out = E, N_out = H, K = T, both operands MN-major; the maps end
+    // at row T, so the last K stage reads zeros past it
+    if (!make_bf16_box(&a, dl_bf16, c.T, c.E, 64) || !make_bf16_box(&b, x, c.T, c.H, 64)) return cudaErrorInvalidValue;
+    p.M_out = c.E;
+    p.N_out = c.H;
+    p.m_tiles_out = c.E / (2 * BM);
+    p.n_tiles = c.H / BN;
+    p.w0 = nullptr;
+    p.w0x = dw_router;
+    e = launch<WGRAD_DOWN, 2>(a, b, b, b, b, p, (int64_t)p.m_tiles_out * p.n_tiles, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (dx_r) {
+    // dx_r = dl W_router: M = T, N = H, K = E; W_router [E, H] read MN-major
+    if (!make_bf16_box(&a, dl_bf16, c.T, c.E, BM) || !make_bf16_box(&b, w_router, c.E, c.H, 64))
+      return cudaErrorInvalidValue;
+    const bool pair = c.T >= 512;
+    const int tm = pair ? 2 * BM : BM;
+    p.K = c.E;
+    p.n_tiles = c.H / BN;
+    p.b_group_rows = 0;
+    p.ldc = c.H;
+    p.out = static_cast<__nv_bfloat16*>(dx_r);
+    const int64_t tiles = ceil_div(c.T, tm) * p.n_tiles;
+    e = pair ? launch<DGRAD_PLAIN, 2>(a, b, b, b, b, p, tiles, s) : launch<DGRAD_PLAIN, 1>(a, b, b, b, b, p, tiles, s);
+  }
+  return e;
 }
 
 }  // namespace tc

@@ -64,15 +64,32 @@ cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint
                                cudaStream_t s);
 
 // Router backward (router_bwd.cu). dl: dL/dlogits [T, E] fp32.
-int router_wgrad_slices(const moe_config_t& c);  // token slices of the weight gradient
-cudaError_t launch_router_logit_grad(const moe_config_t& c, const float* logits, const int32_t* topk_idx,
-                                     const float* dtopk_w, const int32_t* counts, float aux_alpha, float* dl,
-                                     DeviceStatus* st, cudaStream_t s);
-// part: router_wgrad_slices * E * H floats, bias_part: router_wgrad_slices * E floats
-cudaError_t launch_router_wgrad(const moe_config_t& c, const float* dl, const void* x, float* dw_router,
-                                float* d_bias, float* part, float* bias_part, cudaStream_t s);
-cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, const void* w_router, const void* dxd,
-                                     const int32_t* tok_row, void* dx, cudaStream_t s);
+int router_wgrad_slices(const moe_config_t& c);  // token slices of the split reductions
+// true: the two router products run on the tensor cores (dl rounded to bf16)
+bool router_backward_tc(const moe_config_t& c);
+// Workspace buffers of the router backward: part [S, E, H] and bias_part [S, E] fp32 (S =
+// router_wgrad_slices), and on the tensor-core path dl_bf16 [T, E] and dx_r [T, H] bf16.
+struct RouterScratch {
+  float* part;
+  float* bias_part;
+  void* dl_bf16;
+  void* dx_r;
+};
+// dl from dtopk_w (+ the aux loss's gradient when counts != NULL); with dw_router, the
+// router weight gradient and (d_bias != NULL) the bias gradient.
+cudaError_t launch_router_backward(const moe_config_t& c, const float* logits, const int32_t* topk_idx,
+                                   const float* dtopk_w, const int32_t* counts, float aux_alpha, const void* x,
+                                   float* dl, float* dw_router, float* d_bias, const RouterScratch& sc,
+                                   DeviceStatus* st, cudaStream_t s);
+// dx = dl W_router (+ the dispatch backward's rows when dxd != NULL). dl_bf16: dl already
+// in bf16 (from launch_router_backward on the tensor-core path), or NULL.
+cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, const void* dl_bf16,
+                                     const void* w_router, const void* dxd, const int32_t* tok_row, void* dx,
+                                     const RouterScratch& sc, DeviceStatus* st, cudaStream_t s);
+// The combine kernel with unit weights and one more row, row t of extra [T, H] (bf16).
+bool combine_extra_supported(const moe_config_t& c);
+cudaError_t launch_combine_extra(const moe_config_t& c, const void* yd, const int32_t* tok_row, const void* extra,
+                                 void* y, cudaStream_t s);
 
 // SIMT grouped GEMM (fp32 FFMA): C = A . B^T per group, with optional SwiGLU pair.
 // Groups: routed experts g < E over rows [offsets[g], offsets[g+1]) of A, plus an optional

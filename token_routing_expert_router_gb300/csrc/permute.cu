@@ -319,12 +319,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const void* __restric
 // 16-byte vector of a chunk is loaded before any of them is summed, so one memory round
 // trip covers all NR rows. With few rows, each thread takes U chunks per pass and issues
 // all NR * U loads first, so about eight 16-byte loads are in flight per thread whatever k
-// is. The shared row enters with weight 1 (fma(1, v, acc) == acc + v).
-template <int NR, bool BF16>
+// is. The shared row enters with weight 1 (fma(1, v, acc) == acc + v). EXTRA (bf16): the
+// last of the NR rows is row t of a separate [T, H] buffer, added with weight 1 (the
+// router's share of the input gradient, after the dispatch backward's rows).
+template <int NR, bool BF16, bool EXTRA = false>
 __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __restrict__ yd_, int H, int k,
                                                               const int32_t* __restrict__ tok_row,
                                                               const float* __restrict__ topk_w, int64_t R,
-                                                              void* __restrict__ y_) {
+                                                              void* __restrict__ y_,
+                                                              const void* __restrict__ extra_ = nullptr) {
   constexpr int U = NR >= 8 ? 1 : 8 / NR;
   __shared__ int64_t rows[NR];
   __shared__ float wts[NR];
@@ -344,7 +347,9 @@ __global__ void __launch_bounds__(kThreads) combine_nr_kernel(const void* __rest
         const int c = base + u * kThreads;
         if (c < n8) {
 #pragma unroll
-          for (int j = 0; j < NR; ++j) raw[u][j] = __ldg(reinterpret_cast<const uint4*>(yd_) + rows[j] * n8 + c);
+          for (int j = 0; j < NR; ++j)
+            raw[u][j] = (EXTRA && j == NR - 1) ? __ldg(reinterpret_cast<const uint4*>(extra_) + (int64_t)t * n8 + c)
+                                               : __ldg(reinterpret_cast<const uint4*>(yd_) + rows[j] * n8 + c);
         }
       }
 #pragma unroll
@@ -523,6 +528,34 @@ cudaError_t launch_dispatch(const moe_config_t& c, const void* x, const int32_t*
                                               reinterpret_cast<uint4*>(xd));
   }
   return cudaGetLastError();
+}
+
+template <int NR>
+cudaError_t launch_combine_extra_nr(const moe_config_t& c, const void* yd, const int32_t* tok_row, const void* extra,
+                                    void* y, cudaStream_t s) {
+  combine_nr_kernel<NR, true, true><<<c.T, kThreads, 0, s>>>(yd, c.H, c.k, tok_row, nullptr, routed_rows(c), y, extra);
+  return cudaGetLastError();
+}
+
+bool combine_extra_supported(const moe_config_t& c) {
+  return c.act_dtype == MOE_DTYPE_BF16 && c.k + (c.n_shared ? 1 : 0) + 1 <= 10;
+}
+
+cudaError_t launch_combine_extra(const moe_config_t& c, const void* yd, const int32_t* tok_row, const void* extra,
+                                 void* y, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  switch (c.k + (c.n_shared ? 1 : 0) + 1) {
+    case 2: return launch_combine_extra_nr<2>(c, yd, tok_row, extra, y, s);
+    case 3: return launch_combine_extra_nr<3>(c, yd, tok_row, extra, y, s);
+    case 4: return launch_combine_extra_nr<4>(c, yd, tok_row, extra, y, s);
+    case 5: return launch_combine_extra_nr<5>(c, yd, tok_row, extra, y, s);
+    case 6: return launch_combine_extra_nr<6>(c, yd, tok_row, extra, y, s);
+    case 7: return launch_combine_extra_nr<7>(c, yd, tok_row, extra, y, s);
+    case 8: return launch_combine_extra_nr<8>(c, yd, tok_row, extra, y, s);
+    case 9: return launch_combine_extra_nr<9>(c, yd, tok_row, extra, y, s);
+    case 10: return launch_combine_extra_nr<10>(c, yd, tok_row, extra, y, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_combine(const moe_config_t& c, const void* yd, const int32_t* tok_row,

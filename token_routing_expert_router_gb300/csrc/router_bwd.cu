@@ -15,8 +15,14 @@
 //  3. input_grad_kernel: dx[t] = sum_e dl[t,e] W_router[e] + sum_j dxd[tok_row[t,j]]
 //     (+ dxd[R + t]): the router's share and the dispatch backward's gather-reduce in one
 //     pass over dx, accumulated in fp32 and rounded to bf16 once.
+// With many experts (E and H multiples of 256, bf16) the two products are dense enough for
+// the tensor cores: dl is also written in bf16, dW_router = dl^T x and dx_r = dl W_router
+// run as the expert backward's tcgen05 GEMMs over the tokens as one group, the bias
+// gradient is a column sum of dl, and dx = dx_r + the dispatch rows is the combine kernel
+// with one extra row.
 #include <algorithm>
 
+#include "gemm_tc.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -47,7 +53,8 @@ template <int EPL>
 __global__ void __launch_bounds__(kLgWarps * 32)
     logit_grad_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                       const float* __restrict__ dtopk_w, int T, int E, int k, int score_fn, int renorm, float rho,
-                      const int32_t* __restrict__ counts, float aux_a0, float* __restrict__ dl, DeviceStatus* st) {
+                      const int32_t* __restrict__ counts, float aux_a0, float* __restrict__ dl,
+                      __nv_bfloat16* __restrict__ dlb, DeviceStatus* st) {
   __shared__ float row_s[kLgWarps][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kLgWarps + warp;
@@ -155,6 +162,29 @@ __global__ void __launch_bounds__(kLgWarps * 32)
 #pragma unroll
   for (int i = 0; i < EPL; ++i)
     if (lane + 32 * i < E) out[lane + 32 * i] = row[lane + 32 * i];
+  if (dlb != nullptr) {
+    __nv_bfloat16* ob = dlb + (int64_t)t * E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) ob[lane + 32 * i] = __float2bfloat16_rn(row[lane + 32 * i]);
+  }
+}
+
+// Column sums of dl over token slice z (the bias gradient's partials), one thread per expert.
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ dl, int T, int E, int slice,
+                                                     float* __restrict__ out) {
+  const int t0 = blockIdx.x * slice, t1 = min(T, t0 + slice);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float a = 0.0f;
+    for (int t = t0; t < t1; ++t) a += dl[(int64_t)t * E + e];
+    out[(int64_t)blockIdx.x * E + e] = a;
+  }
+}
+
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ src, int64_t n,
+                                                      __nv_bfloat16* __restrict__ dst) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -411,40 +441,36 @@ int router_wgrad_slices(const moe_config_t& c) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
 }
 
-cudaError_t launch_router_logit_grad(const moe_config_t& c, const float* logits, const int32_t* topk_idx,
-                                     const float* dtopk_w, const int32_t* counts, float aux_alpha, float* dl,
-                                     DeviceStatus* st, cudaStream_t s) {
-  if (c.T == 0) return cudaSuccess;
-  const float a0 = counts ? (float)((double)aux_alpha * c.E / ((double)c.T * c.T * c.k)) : 0.0f;
-  const dim3 grid((unsigned)ceil_div(c.T, kLgWarps));
-  const int epl = (int)ceil_div(c.E, 32);
-#define MOE_LG(N)                                                                                              \
-  logit_grad_kernel<N><<<grid, kLgWarps * 32, 0, s>>>(logits, topk_idx, dtopk_w, c.T, c.E, c.k, c.score_fn,     \
-                                                       c.renorm, c.routed_scale, counts, a0, dl, st)
-  if (epl <= 1) MOE_LG(1);
-  else if (epl <= 2) MOE_LG(2);
-  else if (epl <= 4) MOE_LG(4);
-  else if (epl <= 8) MOE_LG(8);
-  else MOE_LG(16);
-#undef MOE_LG
+bool router_backward_tc(const moe_config_t& c) {
+  return tc::router_backward_tc_supported(c) && combine_extra_supported(c);
+}
+
+namespace {
+
+// token slices of the split reductions: (slice length, slices used)
+void slices_of(const moe_config_t& c, int* slice, int* used) {
+  const int S = router_wgrad_slices(c);
+  *slice = (int)(ceil_div(ceil_div(c.T, S), kWgBK) * kWgBK);
+  *used = (int)ceil_div(c.T, *slice);  // <= S
+}
+
+cudaError_t bias_grad(const moe_config_t& c, const float* dl, float* d_bias, float* bias_part, cudaStream_t s) {
+  int slice, used;
+  slices_of(c, &slice, &used);
+  colsum_kernel<<<used, 256, 0, s>>>(dl, c.T, c.E, slice, used > 1 ? bias_part : d_bias);
+  if (used > 1) sum_slices_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, d_bias);
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_wgrad(const moe_config_t& c, const float* dl, const void* x, float* dw_router,
-                                float* d_bias, float* part, float* bias_part, cudaStream_t s) {
-  if (c.T == 0) {  // no tokens: zero gradients
-    cudaError_t e = cudaMemsetAsync(dw_router, 0, (size_t)c.E * c.H * 4, s);
-    if (e == cudaSuccess && d_bias) e = cudaMemsetAsync(d_bias, 0, (size_t)c.E * 4, s);
-    return e;
-  }
-  const int S = router_wgrad_slices(c);
-  const int slice = (int)(ceil_div(ceil_div(c.T, S), kWgBK) * kWgBK);
-  const int Sused = (int)ceil_div(c.T, slice);  // <= S
-  float* out = Sused > 1 ? part : dw_router;
-  float* bout = d_bias ? (Sused > 1 ? bias_part : d_bias) : nullptr;
+cudaError_t simt_wgrad(const moe_config_t& c, const float* dl, const void* x, float* dw_router, float* d_bias,
+                       float* part, float* bias_part, cudaStream_t s) {
+  int slice, used;
+  slices_of(c, &slice, &used);
+  float* out = used > 1 ? part : dw_router;
+  float* bout = d_bias ? (used > 1 ? bias_part : d_bias) : nullptr;
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
   const int bm = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
-  const dim3 grid((unsigned)ceil_div(c.H, kWgBN), (unsigned)ceil_div(c.E, bm), (unsigned)Sused);
+  const dim3 grid((unsigned)ceil_div(c.H, kWgBN), (unsigned)ceil_div(c.E, bm), (unsigned)used);
 #define MOE_WG(BM)                                                                                     \
   if (bf) wgrad_kernel<BM, true><<<grid, kWgThreads, 0, s>>>(dl, x, c.T, c.E, c.H, slice, out, bout); \
   else wgrad_kernel<BM, false><<<grid, kWgThreads, 0, s>>>(dl, x, c.T, c.E, c.H, slice, out, bout)
@@ -454,17 +480,66 @@ cudaError_t launch_router_wgrad(const moe_config_t& c, const float* dl, const vo
   else { MOE_WG(64); }
 #undef MOE_WG
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || Sused == 1) return e;
+  if (e != cudaSuccess || used == 1) return e;
   const int64_t n = (int64_t)c.E * c.H;
   const int blocks = (int)std::min<int64_t>(ceil_div(n / 4, 256), 152 * 8);
-  sum_slices_kernel<<<blocks, 256, 0, s>>>(part, Sused, n, dw_router);
-  if (d_bias) sum_slices_kernel<<<1, 256, 0, s>>>(bias_part, Sused, c.E, d_bias);
+  sum_slices_kernel<<<blocks, 256, 0, s>>>(part, used, n, dw_router);
+  if (d_bias) sum_slices_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, d_bias);
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, const void* w_router, const void* dxd,
-                                     const int32_t* tok_row, void* dx, cudaStream_t s) {
+}  // namespace
+
+cudaError_t launch_router_backward(const moe_config_t& c, const float* logits, const int32_t* topk_idx,
+                                   const float* dtopk_w, const int32_t* counts, float aux_alpha, const void* x,
+                                   float* dl, float* dw_router, float* d_bias, const RouterScratch& sc,
+                                   DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) {  // no tokens: zero gradients
+    cudaError_t e = dw_router ? cudaMemsetAsync(dw_router, 0, (size_t)c.E * c.H * 4, s) : cudaSuccess;
+    if (e == cudaSuccess && d_bias) e = cudaMemsetAsync(d_bias, 0, (size_t)c.E * 4, s);
+    return e;
+  }
+  const bool tc_path = router_backward_tc(c);
+  const float a0 = counts ? (float)((double)aux_alpha * c.E / ((double)c.T * c.T * c.k)) : 0.0f;
+  const dim3 grid((unsigned)ceil_div(c.T, kLgWarps));
+  const int epl = (int)ceil_div(c.E, 32);
+  __nv_bfloat16* dlb = tc_path ? static_cast<__nv_bfloat16*>(sc.dl_bf16) : nullptr;
+#define MOE_LG(N)                                                                                              \
+  logit_grad_kernel<N><<<grid, kLgWarps * 32, 0, s>>>(logits, topk_idx, dtopk_w, c.T, c.E, c.k, c.score_fn,     \
+                                                       c.renorm, c.routed_scale, counts, a0, dl, dlb, st)
+  if (epl <= 1) MOE_LG(1);
+  else if (epl <= 2) MOE_LG(2);
+  else if (epl <= 4) MOE_LG(4);
+  else if (epl <= 8) MOE_LG(8);
+  else MOE_LG(16);
+#undef MOE_LG
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !dw_router) return e;
+  if (!tc_path) return simt_wgrad(c, dl, x, dw_router, d_bias, sc.part, sc.bias_part, s);
+  e = tc::launch_router_products(c, dlb, x, nullptr, dw_router, nullptr, st, s);
+  if (e == cudaSuccess && d_bias) e = bias_grad(c, dl, d_bias, sc.bias_part, s);
+  return e;
+}
+
+cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, const void* dl_bf16,
+                                     const void* w_router, const void* dxd, const int32_t* tok_row, void* dx,
+                                     const RouterScratch& sc, DeviceStatus* st, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
+  if (router_backward_tc(c)) {
+    // dx_r = dl W_router on the tensor cores, then dx = the dispatch rows + dx_r
+    cudaError_t e = cudaSuccess;
+    if (!dl_bf16) {
+      const int64_t n = (int64_t)c.T * c.E;
+      to_bf16_kernel<<<(unsigned)std::min<int64_t>(ceil_div(n, 256), 152 * 8), 256, 0, s>>>(
+          dl, n, static_cast<__nv_bfloat16*>(sc.dl_bf16));
+      e = cudaGetLastError();
+      dl_bf16 = sc.dl_bf16;
+    }
+    void* dx_r = dxd ? sc.dx_r : dx;
+    if (e == cudaSuccess) e = tc::launch_router_products(c, dl_bf16, nullptr, w_router, nullptr, dx_r, st, s);
+    if (e == cudaSuccess && dxd) e = launch_combine_extra(c, dxd, tok_row, dx_r, dx, s);
+    return e;
+  }
   const dim3 grid((unsigned)ceil_div(c.H, kIgBN), (unsigned)ceil_div(c.T, kIgBM));
   input_grad_kernel<<<grid, kIgThreads, 0, s>>>(dl, (const uint16_t*)w_router, (const uint16_t*)dxd, tok_row, c.T,
                                                 c.E, c.H, c.k, c.n_shared, routed_rows(c), (__nv_bfloat16*)dx);
