@@ -461,10 +461,12 @@ def run_gpu(args, w):
 
 
 def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
-    """moe_backward after the forward whose workspace is ws (with the router's backward and
-    the auxiliary loss's gradient), the same call without the router, and the staged calls
-    (combine backward, grouped MLP backward, router backward, the fused input gradient and
-    the plain dispatch backward), L2 flushed before each."""
+    """The training step's backward: moe_backward_kept after moe_forward_train (the gate/up
+    pre-activations kept, the router's backward and the auxiliary loss's gradient included).
+    Beside it: the training forward, moe_backward (recomputing the gate/up GEMM) with and
+    without the router, and the staged calls (combine backward, grouped MLP backward, router
+    backward, the fused input gradient and the plain dispatch backward). L2 flushed before
+    each call."""
     import torch
     import token_routing_expert_router_gb300 as moe
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
@@ -490,9 +492,13 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     moe.moe_workspace_init(rws)
     dyd = torch.empty((rows, H), dtype=dt, device=dev)
     dxd = torch.empty((rows, H), dtype=dt, device=dev)
-    moe.moe_forward(cfg, x, wts, torch.empty((T, H), dtype=dt, device=dev), ws)
+    gu = torch.empty((rows, 2 * F), dtype=dt, device=dev)
+    yt = torch.empty((T, H), dtype=dt, device=dev)
+    moe.moe_forward_train(cfg, x, wts, yt, ws, gu)
     stages = {
-        "backward": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, rgrads, bws),
+        "backward": lambda: moe.moe_backward_kept(cfg, x, wts, dy, ws, gu, dx, dtw, rgrads, bws),
+        "forward_train": lambda: moe.moe_forward_train(cfg, x, wts, yt, ws, gu),
+        "backward_recompute": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, rgrads, bws),
         "backward_without_router": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
         "combine_backward": lambda: moe.moe_combine_backward(cfg, dy, b["yd"], b["tok_row"], b["w"], dyd, dtw),
         "grouped_mlp_backward": lambda: moe.moe_grouped_mlp_backward(cfg, b["xd"], x, b["offsets"], wts, dyd, dxd,
@@ -529,9 +535,10 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
             "grouped_gemm_tflops": round(tf, 1), "grouped_gemm_frac_of_peak": round(tf / peak, 3),
             "algorithmic_flops": flops, "recompute_flops": recompute,
             "router_flops": 4.0 * T * H * E,
-            "note": "the step: moe_backward with the router's backward and the auxiliary loss's gradient; "
-                    "dgrad + wgrad flops over the grouped MLP backward time (the gate/up recompute is extra work "
-                    "in that time); router_flops: dW_router and dx's router share (tensor cores when E and H are multiples of "
+            "note": "the step: moe_backward_kept after moe_forward_train (gate/up pre-activations kept), with "
+                    "the router's backward and the auxiliary loss's gradient; backward_recompute reruns the gate/up "
+                    "GEMM instead; grouped_gemm_tflops: dgrad + wgrad flops over the grouped MLP backward time "
+                    "(which includes that recompute); router_flops: dW_router and dx's router share (tensor cores when E and H are multiples of "
                     "256, else fp32 SIMT); weight gradients "
                     "fp32; L2 flushed before each call"}
 

@@ -23,6 +23,8 @@
  *   moe_backward        the training step's backward of S0-S7 (bf16 layers): combine,
  *                       the experts' grouped dgrad/wgrad with recomputed SwiGLU, dispatch,
  *                       and (optionally) the router and the auxiliary loss
+ *   moe_forward_train   moe_forward that keeps the gate/up pre-activations, and
+ *   moe_backward_kept   the backward that reads them instead of rerunning that GEMM
  *   moe_router_backward the router's backward: dlogits, dW_router, d bias
  *
  * Conventions shared by every call:
@@ -328,6 +330,24 @@ moe_status_t moe_dispatch_backward(const moe_config_t* cfg, const void* dxd, con
 moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
                           const void* dy, const void* fwd_ws, void* dx, float* dtopk_w,
                           const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream);
+
+/* The forward of a training step: moe_forward, with GEMM1 also storing the gate/up
+ * pre-activations g = xd Wg^T and u = xd Wu^T (bf16) into gu [R(+T), 2F], row r holding
+ * F/128 blocks of 256 columns (128 of g, then 128 of u). With them kept, the backward
+ * recomputes only the activation silu(g) u and its derivative, the cheap part (Megatron-Core
+ * summary, section 2.2, granular recomputation: activation functions are recomputed rather
+ * than stored), instead of rerunning the gate/up GEMM. gu is caller-owned: R(+T) * 2F * 2
+ * bytes, 16-byte aligned. bf16 layers the backward takes (else MOE_ERR_UNSUPPORTED); y and
+ * the workspace are bit-identical to moe_forward's. */
+moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
+                               void* gu, moe_stream_t stream);
+
+/* moe_backward after moe_forward_train: reads the kept gu instead of recomputing it. The
+ * kept values are the ones the recomputation would produce, so every output is
+ * bit-identical to moe_backward's. */
+moe_status_t moe_backward_kept(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                               const void* fwd_ws, const void* gu, void* dx, float* dtopk_w,
+                               const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream);
 
 /* Router backward (the router scores every token against the experts, Megatron-Core
  * summary, "O essencial"; the weights are the softmax or sigmoid of the chosen scores).

@@ -151,6 +151,14 @@ def test_router_backward_rejected_on_host(L):
     w = moe.MoEWeights.from_tensors({"w_router": 4096, "w_gate": 4096, "w_up": 4096, "w_down": 4096})
     assert L.moe_backward(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096), P(4096),
                           ctypes.byref(g), P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    # the training forward keeps g and u only for layers the backward takes, into an aligned buffer
+    assert L.moe_forward_train(ctypes.byref(cfg(act_dtype=moe.F32)), P(4096), ctypes.byref(w), P(4096), P(4096),
+                               P(4096), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_forward_train(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096 + 8),
+                               None) == moe.MOE_ERR_INVALID_ARG
+    g0 = moe.MoEWeightGrads.from_tensors({"dw_gate": 4096, "dw_up": 4096, "dw_down": 4096})
+    assert L.moe_backward_kept(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), None, P(4096),
+                               P(4096), ctypes.byref(g0), P(4096), None) == moe.MOE_ERR_INVALID_ARG
     # the router backward's workspace: the status head and S slices of [E, H] + [E] partials
     n = moe.moe_router_backward_workspace_size(c)
     assert n % 256 == 0 and n >= 256 + c.E * c.H * 4 + c.E * 4

@@ -191,6 +191,67 @@ def test_backward_after_forward_equals_staged(w):
     assert not torch.equal(dx_r, dx)
 
 
+@pytest.mark.parametrize("w", [CASES[0], CASES[3], CASES[5]], ids=["mixtral_small", "pair_shared", "e256_shared"])
+def test_forward_train_keeps_what_the_backward_recomputes(w):
+    """moe_forward_train gives moe_forward's y and keeps g and u; moe_backward_kept on them
+    gives moe_backward's every output bit for bit (the recomputed gate/up GEMM is the same
+    GEMM), router and auxiliary loss included. g and u match the plain products xd Wg^T,
+    xd Wu^T."""
+    seed = 34
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    rows = T * k + (T if w["n_shared"] else 0)
+    inp = synth.host_inputs(w, seed=seed)
+    d = device_weights_from_host(w, inp)
+    cfg = cfg_of(w)
+    fws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(fws)
+    y0 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(cfg, d["x"], weights_arg(d), y0, fws)
+    y1 = torch.empty_like(y0)
+    gu = torch.full((rows, 2 * F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward_train(cfg, d["x"], weights_arg(d), y1, fws, gu)
+    assert moe.moe_read_status(fws) == moe.MOE_OK
+    assert torch.equal(y0, y1)
+    dy = up(synth.normal(seed, 50, (T, H), 1.0, "bf16"), torch.bfloat16)
+    outs = []
+    for kept in (False, True):
+        bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+        moe.moe_workspace_init(bws)
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        dtw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        g = grads_alloc(w)
+        g.update(dw_router=torch.empty((E, H), dtype=torch.float32, device="cuda"),
+                 dlogits=torch.empty((T, E), dtype=torch.float32, device="cuda"), aux_loss_coeff=0.01)
+        if kept:
+            moe.moe_backward_kept(cfg, d["x"], weights_arg(d), dy, fws, gu, dx, dtw, g, bws)
+        else:
+            moe.moe_backward(cfg, d["x"], weights_arg(d), dy, fws, dx, dtw, g, bws)
+        assert moe.moe_read_status(bws) == moe.MOE_OK
+        outs.append(dict(g, dx=dx, dtopk_w=dtw))
+    for key, v in outs[0].items():
+        if isinstance(v, torch.Tensor):
+            assert torch.equal(v, outs[1][key]), key
+    # g and u of a few rows against the plain products (the routing read back from the forward)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    b = alloc(w)
+    moe.moe_forward(cfg, d["x"], weights_arg(d), y0, fws, idx)
+    moe.moe_route_from_map(b["cfg"], idx, b["counts"], b["offsets"], b["row_token"], b["tok_row"], b["ws"])
+    row_token = np_of(b["row_token"])
+    offsets = np_of(b["offsets"])
+    x64 = inp["x"].astype(np.float64)
+    got = np_of(gu.float()).astype(np.float64)
+    for r in np.linspace(0, rows - 1, 12).astype(int):
+        if r < T * k:
+            e = int(np.searchsorted(offsets, r, side="right") - 1)
+            a, wg, wu = x64[row_token[r]], inp["w_gate"][e], inp["w_up"][e]
+        else:
+            a, wg, wu = x64[r - T * k], inp["ws_gate"], inp["ws_up"]
+        gref, uref = wg.astype(np.float64) @ a, wu.astype(np.float64) @ a
+        blocks = got[r].reshape(F // 128, 2, 128)
+        assert oracle.rel_l2(blocks[:, 0].ravel(), gref) < 1e-2, r
+        assert oracle.rel_l2(blocks[:, 1].ravel(), uref) < 1e-2, r
+
+
 def test_backward_no_tokens_gives_zero_weight_gradients():
     w = synth.scaled(CASES[1], T=0)
     cfg = cfg_of(w)

@@ -113,6 +113,8 @@ def lib():
             "moe_grouped_mlp_backward": [cfg, P, P, P, wts, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_dispatch_backward": [cfg, P, P, P, P],
             "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
+            "moe_forward_train": [cfg, P, wts, P, P, P, P],
+            "moe_backward_kept": [cfg, P, wts, P, P, P, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_router_backward_workspace_size": [cfg, POINTER(c_size_t)],
             "moe_router_backward": [cfg, P, P, P, P, ctypes.c_float, P, P, P, P, P, P],
             "moe_dispatch_router_backward": [cfg, P, P, P, P, P, P, P],
@@ -143,7 +145,8 @@ def exported_symbols() -> list:
             "moe_quantize_e4m3",
             "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
             "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_mlp_backward",
-            "moe_dispatch_backward", "moe_backward", "moe_router_backward_workspace_size",
+            "moe_dispatch_backward", "moe_backward", "moe_forward_train", "moe_backward_kept",
+            "moe_router_backward_workspace_size",
             "moe_router_backward", "moe_dispatch_router_backward",
             "moe_read_status", "moe_status_string", "moe_route_static_scratch",
             "moe_selftest_bounded_wait"]
@@ -311,6 +314,21 @@ def moe_backward(cfg, x, weights: dict, dy, fwd_ws, dx, dtopk_w, grads: dict, bw
     g = MoEWeightGrads.from_tensors(grads)
     _check(lib().moe_backward(byref(cfg), _ptr(x), byref(w), _ptr(dy), _ptr(fwd_ws), _ptr(dx), _ptr(dtopk_w),
                               byref(g), _ptr(bwd_ws), _stream(stream)), "moe_backward")
+
+
+def moe_forward_train(cfg, x, weights: dict, y, ws, gu, stream=None):
+    """moe_forward that also keeps the gate/up pre-activations in gu [R(+T), 2F] bf16."""
+    w = MoEWeights.from_tensors(weights)
+    _check(lib().moe_forward_train(byref(cfg), _ptr(x), byref(w), _ptr(y), _ptr(ws), _ptr(gu), _stream(stream)),
+           "moe_forward_train")
+
+
+def moe_backward_kept(cfg, x, weights: dict, dy, fwd_ws, gu, dx, dtopk_w, grads: dict, bwd_ws, stream=None):
+    """moe_backward reading the gate/up pre-activations kept by moe_forward_train."""
+    w = MoEWeights.from_tensors(weights)
+    g = MoEWeightGrads.from_tensors(grads)
+    _check(lib().moe_backward_kept(byref(cfg), _ptr(x), byref(w), _ptr(dy), _ptr(fwd_ws), _ptr(gu), _ptr(dx),
+                                   _ptr(dtopk_w), byref(g), _ptr(bwd_ws), _stream(stream)), "moe_backward_kept")
 
 
 def moe_router_backward_workspace_size(cfg: MoEConfig) -> int:

@@ -412,15 +412,18 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* yd, const int32_t*
   return cuda_status(launch_combine(*cfg, yd, tok_row, topk_w, y, (cudaStream_t)stream));
 }
 
-moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
-                         void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
-                         int32_t* counts_out, moe_stream_t stream) {
+namespace {
+// moe_forward, and with keep (moe_forward_train) GEMM1 also keeps g and u in gu_keep.
+moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
+                          int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, bool keep, void* gu_keep,
+                          moe_stream_t stream) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
+  if (keep && !tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
   v = check_weights(*cfg, w, true);
   if (v != MOE_OK) return v;
-  if (!ptr_ok(x) || !ptr_ok(y) || !ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  if (!ptr_ok(x) || !ptr_ok(y) || !ptr_ok(ws) || (keep && !ptr_ok(gu_keep))) return MOE_ERR_INVALID_ARG;
   if ((topk_idx_out && !aligned16(topk_idx_out)) || (topk_w_out && !aligned16(topk_w_out)) ||
       (counts_out && !aligned16(counts_out)))
     return MOE_ERR_INVALID_ARG;
@@ -452,7 +455,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
     e = is_mx(c) ? launch_dispatch_mx(c, x, topk_idx, tok_row, offsets, xd, xd_scale, s)
                  : launch_dispatch(c, x, tok_row, xd, static_cast<float*>(xd_scale), s);
   if (e == cudaSuccess)
-    e = grouped_mlp(c, xd, xd_scale, x, offsets, *w, h, h_scale, yd, status_of(ws), s);
+    e = keep ? tc::launch_grouped_mlp(c, xd, nullptr, x, offsets, *w, h, nullptr, yd, status_of(ws), s, nullptr,
+                                         nullptr, nullptr, gu_keep)
+                : grouped_mlp(c, xd, xd_scale, x, offsets, *w, h, h_scale, yd, status_of(ws), s);
   if (e == cudaSuccess) e = launch_combine(c, yd, tok_row, topk_w, y, s);
   const size_t Tk = (size_t)c.T * c.k;
   if (e == cudaSuccess && topk_idx_out)
@@ -462,6 +467,18 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
   if (e == cudaSuccess && counts_out)
     e = cudaMemcpyAsync(counts_out, counts, (size_t)c.E * 4, cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
+}
+}  // namespace
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weights_t* w,
+                         void* y, void* ws, int32_t* topk_idx_out, float* topk_w_out,
+                         int32_t* counts_out, moe_stream_t stream) {
+  return forward_impl(cfg, x, w, y, ws, topk_idx_out, topk_w_out, counts_out, false, nullptr, stream);
+}
+
+moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
+                               void* gu, moe_stream_t stream) {
+  return forward_impl(cfg, x, w, y, ws, nullptr, nullptr, nullptr, true, gu, stream);
 }
 
 moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host, const moe_weights_t* w,
@@ -547,9 +564,29 @@ moe_status_t moe_dispatch_backward(const moe_config_t* cfg, const void* dxd, con
   return cuda_status(launch_combine(*cfg, dxd, tok_row, nullptr, dx, (cudaStream_t)stream));
 }
 
+namespace {
+moe_status_t backward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                           const void* fwd_ws, const void* gu_kept, void* dx, float* dtopk_w,
+                           const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream);
+}  // namespace
+
 moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
                           const void* fwd_ws, void* dx, float* dtopk_w, const moe_weight_grads_t* grads, void* bwd_ws,
                           moe_stream_t stream) {
+  return backward_impl(cfg, x, w, dy, fwd_ws, nullptr, dx, dtopk_w, grads, bwd_ws, stream);
+}
+
+moe_status_t moe_backward_kept(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                               const void* fwd_ws, const void* gu, void* dx, float* dtopk_w,
+                               const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream) {
+  if (cfg && cfg->T > 0 && !ptr_ok(gu)) return MOE_ERR_INVALID_ARG;  // (T = 0 reads nothing)
+  return backward_impl(cfg, x, w, dy, fwd_ws, gu, dx, dtopk_w, grads, bwd_ws, stream);
+}
+
+namespace {
+moe_status_t backward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, const void* dy,
+                           const void* fwd_ws, const void* gu_kept, void* dx, float* dtopk_w,
+                           const moe_weight_grads_t* grads, void* bwd_ws, moe_stream_t stream) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (!tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
@@ -577,7 +614,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
                                           dtopk_w, s);
   if (e == cudaSuccess)
     e = tc::launch_grouped_mlp_backward(c, fb + F.xd, x, (const int32_t*)(fb + F.offsets), *w, bb + B.dyd,
-                                        bb + B.gu, bb + B.dgu, bb + B.h, bb + B.dxd, *grads, status_of(bwd_ws), s);
+                                        gu_kept ? const_cast<void*>(gu_kept) : (void*)(bb + B.gu), bb + B.dgu,
+                                        bb + B.h, bb + B.dxd, *grads, status_of(bwd_ws), s, gu_kept != nullptr);
   if (!grads->dw_router) {
     if (e == cudaSuccess) e = launch_combine(c, bb + B.dxd, tok_row, nullptr, dx, s);
     return cuda_status(e);
@@ -594,6 +632,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
                                  tok_row, dx, sc, status_of(bwd_ws), s);
   return cuda_status(e);
 }
+
+}  // namespace
 
 moe_status_t moe_router_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
   moe_status_t v = validate(cfg);

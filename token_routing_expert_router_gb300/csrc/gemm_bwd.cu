@@ -551,7 +551,7 @@ bool mlp_backward_supported(const moe_config_t& c) {
 cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, const void* x,
                                         const int32_t* offsets, const moe_weights_t& w, const void* dyd, void* gu,
                                         void* dgu, void* h, void* dxd, const moe_weight_grads_t& gr,
-                                        DeviceStatus* st, cudaStream_t s) {
+                                        DeviceStatus* st, cudaStream_t s, bool gu_ready) {
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
   const int64_t prows = backward_padded_rows(c);  // rows of the padded dgu and h
@@ -560,8 +560,8 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
   const bool pair = (int64_t)c.T * c.k >= 512LL * c.E;
   const int tm = pair ? 2 * BM : BM;
   const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
-  // ---- recompute g and u (the forward GEMM1 without its activation)
-  cudaError_t e = launch_gate_up_preact(c, xd, x, offsets, w, gu, st, s);
+  // ---- recompute g and u (the forward GEMM1 without its activation), unless kept
+  cudaError_t e = gu_ready ? cudaSuccess : launch_gate_up_preact(c, xd, x, offsets, w, gu, st, s);
   if (e != cudaSuccess) return e;
   BwdParams p{};
   p.offsets = offsets;

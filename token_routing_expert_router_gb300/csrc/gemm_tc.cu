@@ -29,8 +29,10 @@ constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
 // EPI_STORE_GU: the gate/up GEMM (B = gate and up rows, as for SwiGLU) storing g and u
-// themselves, for the backward's recomputation of the activation.
-enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2, EPI_STORE_GU = 3 };
+// themselves, for the backward's recomputation of the activation. EPI_SWIGLU_GU: the
+// forward's SwiGLU epilogue that also keeps g and u (out2), so that the backward recomputes
+// only the activation and not this GEMM.
+enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2, EPI_STORE_GU = 3, EPI_SWIGLU_GU = 4 };
 
 struct TcParams {
   const int32_t* offsets;   // [G+1] routed segment starts (device); may be null when G = 0
@@ -44,6 +46,8 @@ struct TcParams {
   int b_group_rows;         // rows of B per routed group
   int ldc;                  // output row length in elements
   void* out;
+  void* out2;               // EPI_SWIGLU_GU: g and u [rows, ldc2] in 128-column blocks (g, then u)
+  int ldc2;
   const float* bias;        // EPI_STORE_F32_BIAS: [N] or null
   const int32_t* row_token; // non-null: routed A rows are gathered, row r = token row_token[r]
                             //   of tmA (a one-row-box map of x); else tmA holds the rows
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU) tma_prefetch_desc(&tmB1);
+    if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU) tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, S::kTmemCols);
   if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
@@ -151,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
       const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
       const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
-      constexpr bool kGatedB = EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU;  // B = gate + up rows
+      constexpr bool kGatedB =
+          EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU;  // B = gate + up rows
       const int b_tile_rows = kGatedB ? BN / 2 : BN;  // rows of B per N tile
       int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
       if (CG == 2 && !kGatedB) b_row += (int)rank * (BN / 2);
@@ -281,9 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int warp_live = min(c.rows - (row_in_tile - lane), m64 ? 16 : 32);
       const int64_t warp_row0 = out_row - lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == EPI_SWIGLU_BF16) {
+      if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_GU) {
         // cols [0, BN/2) gate, [BN/2, BN) up -> BN/2 columns of h
         uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * (BN / 2)) * 2;
+        uint8_t* out2 = EPI == EPI_SWIGLU_GU
+                            ? reinterpret_cast<uint8_t*>(p.out2) + (warp_row0 * p.ldc2 + c.nb * BN) * 2
+                            : nullptr;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN / 2; c0 += 32) {
           uint32_t g[32], u[32];
@@ -303,6 +311,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 4; ++v)
             stage_piece(stage, lane, v, make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
           flush_rows_64B(stage, lane, out + 2 * c0, (int64_t)p.ldc * 2, warp_live);
+          if (EPI == EPI_SWIGLU_GU) {
+            // g and u as the backward reads them: the tile's block of 128 g, then 128 u
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t* src = half ? u : g;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__uint_as_float(src[2 * i]), __uint_as_float(src[2 * i + 1]));
+                packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                stage_piece(stage, lane, v,
+                            make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+              flush_rows_64B(stage, lane, out2 + 2 * (c0 + half * (BN / 2)), (int64_t)p.ldc2 * 2, warp_live);
+            }
+          }
         }
       } else if (EPI == EPI_STORE_BF16 || EPI == EPI_STORE_GU) {
         uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * BN) * 2;
@@ -517,7 +543,7 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale, const void* x,
                                const int32_t* offsets, const moe_weights_t& w, void* h, float* h_scale, void* yd,
                                DeviceStatus* st, cudaStream_t s, const int32_t* row_token, const int32_t* tok_row,
-                               const float* topk_w) {
+                               const float* topk_w, void* gu_keep) {
   if (c.xfer_dtype == MOE_DTYPE_E4M3)
     return launch_grouped_mlp_fp8(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
   const int64_t R = routed_rows(c), rows = total_rows(c);
@@ -555,8 +581,17 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   const bool pair = (int64_t)c.T * c.k >= 512LL * c.E && c.H % 256 == 0;
   const int tm = pair ? 2 * BM : BM;
   const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
-  cudaError_t e = pair ? launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
-                       : launch<256, EPI_SWIGLU_BF16, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  cudaError_t e;
+  if (gu_keep != nullptr) {  // also keep g and u for the backward
+    p.out2 = gu_keep;
+    p.ldc2 = 2 * c.F;
+    e = pair ? launch<256, EPI_SWIGLU_GU, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+             : launch<256, EPI_SWIGLU_GU, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+    p.out2 = nullptr;
+  } else {
+    e = pair ? launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+             : launch<256, EPI_SWIGLU_BF16, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+  }
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = h Wd^T (the shared expert's h rows follow the routed ones)
   const int bn2 = c.H % 256 == 0 ? 256 : 128;

@@ -16,11 +16,14 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
 // row_token non-null (bf16 only): GEMM1 gathers its routed A rows from x by token instead
 // of reading dispatched rows from xd (xd unused). topk_w non-null (with row_token and
 // tok_row): GEMM2 scales each routed row of yd by its routing weight before rounding.
+// gu_keep non-null (bf16, not with row_token): GEMM1 also stores g and u [rows, 2F] in the
+// layout the backward reads (the recomputed gate/up pre-activations, bit for bit).
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale,
                                const void* x, const int32_t* offsets, const moe_weights_t& w,
                                void* h, float* h_scale, void* yd, DeviceStatus* st,
                                cudaStream_t s, const int32_t* row_token = nullptr,
-                               const int32_t* tok_row = nullptr, const float* topk_w = nullptr);
+                               const int32_t* tok_row = nullptr, const float* topk_w = nullptr,
+                               void* gu_keep = nullptr);
 
 // Backward of the grouped expert MLP (bf16). gu [R(+T), 2F] (g and u in 128-column blocks,
 // as the gate/up GEMM's tiles hold them); dgu the same columns and h [., F] with each
@@ -31,10 +34,11 @@ bool mlp_backward_supported(const moe_config_t& c);
 int64_t backward_padded_rows(const moe_config_t& c);
 cudaError_t launch_gate_up_preact(const moe_config_t& c, const void* xd, const void* x, const int32_t* offsets,
                                   const moe_weights_t& w, void* gu, DeviceStatus* st, cudaStream_t s);
+// gu_ready: gu already holds g and u (kept by the forward), so the gate/up GEMM is not rerun.
 cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, const void* x,
                                         const int32_t* offsets, const moe_weights_t& w, const void* dyd, void* gu,
                                         void* dgu, void* h, void* dxd, const moe_weight_grads_t& gr,
-                                        DeviceStatus* st, cudaStream_t s);
+                                        DeviceStatus* st, cudaStream_t s, bool gu_ready = false);
 
 // The router's two products for its backward on the tensor cores (bf16, E and H multiples
 // of 256): dw_router = dl^T x (fp32, NULL to skip) and dx_r = dl W_router (bf16 [T, H], NULL
