@@ -498,6 +498,7 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     stages = {
         "backward": lambda: moe.moe_backward_kept(cfg, x, wts, dy, ws, gu, dx, dtw, rgrads, bws),
         "forward_train": lambda: moe.moe_forward_train(cfg, x, wts, yt, ws, gu),
+        "forward_same_timing": lambda: moe.moe_forward(cfg, x, wts, yt, ws),
         "backward_recompute": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, rgrads, bws),
         "backward_without_router": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
         "combine_backward": lambda: moe.moe_combine_backward(cfg, dy, b["yd"], b["tok_row"], b["w"], dyd, dtw),
@@ -513,6 +514,7 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     }
     for f in stages.values():
         f()
+    moe.moe_forward_train(cfg, x, wts, yt, ws, gu)  # the kept g and u match ws again
     reps = max(3, min(args.steps, 5))
     times = {n: [] for n in stages}
     for _ in range(reps):
