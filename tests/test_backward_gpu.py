@@ -191,7 +191,8 @@ def test_backward_after_forward_equals_staged(w):
     assert not torch.equal(dx_r, dx)
 
 
-@pytest.mark.parametrize("w", [CASES[0], CASES[3], CASES[5]], ids=["mixtral_small", "pair_shared", "e256_shared"])
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[3], CASES[5]],
+                         ids=["mixtral_small", "imbalanced_small", "pair_shared", "e256_shared"])
 def test_forward_train_keeps_what_the_backward_recomputes(w):
     """moe_forward_train gives moe_forward's y and keeps g and u; moe_backward_kept on them
     gives moe_backward's every output bit for bit (the recomputed gate/up GEMM is the same
