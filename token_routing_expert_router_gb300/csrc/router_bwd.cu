@@ -429,6 +429,63 @@ __global__ void __launch_bounds__(kIgThreads)
   }
 }
 
+// 3'. The same sum for few experts (E <= 16), one 128-thread block per token: each thread
+// takes 16-byte vectors of 8 columns, issues the NR dispatch rows' loads first, then adds
+// dl[t, e] W_router[e] over e (W_router stays in L1) and the rows, in the order of
+// input_grad_kernel (experts ascending, then rows j = 0..NR-1), so the bits are the same.
+// NR = 0: the router's share alone.
+template <int NR>
+__global__ void __launch_bounds__(128)
+    input_grad_small_kernel(const float* __restrict__ dl, const uint4* __restrict__ wr, const uint4* __restrict__ dxd,
+                            const int32_t* __restrict__ tok_row, int E, int H, int k, int64_t R,
+                            uint4* __restrict__ dx) {
+  __shared__ float dls[16];
+  __shared__ int64_t rows[NR > 0 ? NR : 1];
+  const int t = blockIdx.x;
+  if (threadIdx.x < E) dls[threadIdx.x] = dl[(int64_t)t * E + threadIdx.x];
+  if (NR > 0 && threadIdx.x < NR) {
+    const int j = threadIdx.x;
+    rows[j] = j < k ? (int64_t)tok_row[(int64_t)t * k + j] : R + t;
+  }
+  __syncthreads();
+  const int n8 = H / 8;
+  for (int c = threadIdx.x; c < n8; c += 128) {
+    uint4 raw[NR > 0 ? NR : 1];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) raw[j] = __ldg(dxd + rows[j] * n8 + c);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int e = 0; e < E; ++e) {
+      const float a = dls[e];
+      const uint4 w = __ldg(wr + (int64_t)e * n8 + c);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = __fmaf_rn(a, bf16_lo(w4[q]), acc[2 * q]);
+        acc[2 * q + 1] = __fmaf_rn(a, bf16_hi(w4[q]), acc[2 * q + 1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      const uint32_t v4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += bf16_lo(v4[q]);
+        acc[2 * q + 1] += bf16_hi(v4[q]);
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      op[q] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    dx[(int64_t)t * n8 + c] = o;
+  }
+}
+
 }  // namespace
 
 int router_wgrad_slices(const moe_config_t& c) {
@@ -539,6 +596,21 @@ cudaError_t launch_router_input_grad(const moe_config_t& c, const float* dl, con
     if (e == cudaSuccess) e = tc::launch_router_products(c, dl_bf16, nullptr, w_router, nullptr, dx_r, st, s);
     if (e == cudaSuccess && dxd) e = launch_combine_extra(c, dxd, tok_row, dx_r, dx, s);
     return e;
+  }
+  const int nr = dxd ? c.k + (c.n_shared ? 1 : 0) : 0;
+  if (c.E <= 16 && nr <= 9) {
+    const uint4* wr = static_cast<const uint4*>(w_router);
+    const uint4* rows = static_cast<const uint4*>(dxd);
+    uint4* out = static_cast<uint4*>(dx);
+#define MOE_IGS(N)                                                                                         \
+  case N:                                                                                                  \
+    input_grad_small_kernel<N><<<c.T, 128, 0, s>>>(dl, wr, rows, tok_row, c.E, c.H, c.k, routed_rows(c), out); \
+    return cudaGetLastError();
+    switch (nr) {
+      MOE_IGS(0) MOE_IGS(1) MOE_IGS(2) MOE_IGS(3) MOE_IGS(4) MOE_IGS(5) MOE_IGS(6) MOE_IGS(7) MOE_IGS(8) MOE_IGS(9)
+      default: break;
+    }
+#undef MOE_IGS
   }
   const dim3 grid((unsigned)ceil_div(c.H, kIgBN), (unsigned)ceil_div(c.T, kIgBM));
   input_grad_kernel<<<grid, kIgThreads, 0, s>>>(dl, (const uint16_t*)w_router, (const uint16_t*)dxd, tok_row, c.T,
