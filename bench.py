@@ -386,7 +386,10 @@ def run_gpu(args, w):
     # each with its own workspace, device staging and pinned buffers, take the steps in turn,
     # so the copies of one step run under the kernels of the other; every step still makes
     # its own host->device copy of x and device->host copy of y inside the timed region.
-    e2e_steps = max(4, min(args.steps, 10))
+    e2e_steps = max(4, min(args.steps, 20))
+    # pinned buffers on the GPU's own host node: the process runs on the CPUs local to the
+    # GPU while it allocates and uses them (best effort; restored afterwards)
+    saved_affinity, local_cpus = set_gpu_local_affinity(dev)
     lanes = []
     for _ in range(2):
         wsl = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device=dev)
@@ -413,6 +416,9 @@ def run_gpu(args, w):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     for ln in lanes:
         assert moe.moe_read_status(ln["ws"]) == moe.MOE_OK
+    del lanes
+    if saved_affinity is not None:
+        os.sched_setaffinity(0, saved_affinity)
 
     # ---- backward (training step) of the same layer: bf16 layers
     bwd = None
@@ -476,6 +482,7 @@ def run_gpu(args, w):
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size()),
                 "call": "moe_forward_host (pinned host x in, host y out), steps alternating on two streams",
+                "host_cpus": local_cpus or "not restricted",
                 "l2": "not flushed (each step's x arrives by its own host-to-device copy)"},
         "gpu_launches": args.steps * launches_per_forward(w),
         **({"backward": bwd} if bwd is not None else {}),
@@ -572,6 +579,30 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
                     "(which includes that recompute); router_flops: dW_router and dx's router share (tensor cores when E and H are multiples of "
                     "256, else fp32 SIMT); weight gradients "
                     "fp32; L2 flushed before each call"}
+
+
+def set_gpu_local_affinity(dev):
+    """Restricts this process to the CPUs local to the GPU (from sysfs, by its PCI bus id), so
+    that pinned host buffers allocated now live on the GPU's host node. Returns (previous
+    affinity, cpulist text), or (None, None) where that information is not available."""
+    import torch
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        saved = os.sched_getaffinity(0)
+        cpus &= saved
+        if not cpus or cpus == saved:
+            return None, None
+        os.sched_setaffinity(0, cpus)
+        return saved, text
+    except (AttributeError, OSError, ValueError):
+        return None, None
 
 
 def launches_per_forward(w):

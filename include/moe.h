@@ -388,7 +388,7 @@ moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, c
  * forward's map, trusted as in moe_dispatch_backward. H % 8 == 0. ws:
  * moe_router_backward_workspace_size bytes, initialised with moe_workspace_init.
  *
- * Precision of the router's products: with E % 256 == 0, H % 256 == 0 and bf16 layers
+ * Precision of the router's products: with E % 128 == 0, H % 256 == 0 and bf16 layers
  * (and k + shared <= 9), dw_router = dl^T x and dl W_router run on the tensor cores with
  * dlogits rounded to bf16 and fp32 accumulation, as the expert GEMMs do; dlogits itself
  * stays fp32. Otherwise both are fp32 FMA products. */

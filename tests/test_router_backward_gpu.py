@@ -3,8 +3,8 @@ weight rule (softmax over all experts or over the chosen, sigmoid with or withou
 normalisation, group-limited choice, a routed scale), the auxiliary loss's gradient, the
 router weight and bias gradients (token slices with a ragged last slice, ragged column
 tiles, expert counts from one warp lane to sixteen), and the input gradient (the router's
-share plus the dispatch backward's rows, shared expert included). Layers with E and H
-multiples of 256 take the tensor-core path (dl rounded to bf16 for the two products, a
+share plus the dispatch backward's rows, shared expert included). Layers with E a
+multiple of 128 and H of 256 take the tensor-core path (dl rounded to bf16 for the two products, a
 ragged last 64-token K stage and 128- or 256-row dgrad tiles); the others the fp32 one.
 Every input is seeded on the host; the oracle never sees a GPU result."""
 import numpy as np
@@ -32,7 +32,7 @@ def mcfg(c):
 
 def tc_path(c):
     """The library's rule for the router's products on the tensor cores."""
-    return (c["act_dtype"] == synth.BF16 and c["E"] % 256 == 0 and c["H"] % 256 == 0
+    return (c["act_dtype"] == synth.BF16 and c["E"] % 128 == 0 and c["H"] % 256 == 0
             and c["k"] + c["n_shared"] + 1 <= 10)
 
 
@@ -53,6 +53,8 @@ CASES = {
     # tensor-core path: 700 tokens = 10 K stages of 64 + 60; E = 512 two M tiles
     "tc_sigmoid_groups_e256": rcfg(700, 512, 256, 8, score_fn=1, renorm=1, n_groups=8, topk_groups=4, rho=2.5),
     "tc_softmax_all_e512": rcfg(300, 256, 512, 4),
+    # 128 experts: the weight gradient as single-CTA 128-row tiles
+    "tc_softmax_topk_e128": rcfg(450, 512, 128, 8, renorm=1),
 }
 
 
@@ -139,6 +141,7 @@ IG_CASES = {
     # CTA tiles (128 rows + 2)
     "tc_e256_k8_shared": rcfg(600, 512, 256, 8, shared=1),
     "tc_e256_k2_few_tokens": rcfg(130, 256, 256, 2),
+    "tc_e128_k8": rcfg(700, 512, 128, 8),
 }
 
 

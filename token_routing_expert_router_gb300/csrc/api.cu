@@ -112,8 +112,16 @@ FwdLayout fwd_layout(const moe_config_t& c) {
 // h [prows, F] (prows: every expert's rows padded to a multiple of 64), then the router's
 // dlogits [T, E] and its weight gradient's per-slice partial sums [S, E, H] and [S, E].
 struct BwdLayout {
-  size_t dyd, dxd, gu, dgu, h, dl, rpart, rbpart, dlb, dxr, total;
+  size_t dyd, dxd, gu, dgu, h, dl, rpart, rbpart, dlb, dxr, roff, total;
 };
+
+// Router backward partial sums: the SIMT path's token slices, or the tensor-core path's.
+size_t router_part_slices(const moe_config_t& c) {
+  if (!router_backward_tc(c)) return (size_t)router_wgrad_slices(c);
+  int slice, slices;
+  router_tc_slices(c, &slice, &slices);
+  return slices > 1 ? (size_t)slices : 0;
+}
 
 BwdLayout bwd_layout(const moe_config_t& c) {
   BwdLayout L;
@@ -133,10 +141,11 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.h = take(prows * c.F * 2);
   const bool tcr = router_backward_tc(c);
   L.dl = take((size_t)c.T * c.E * 4);
-  L.rpart = take(tcr ? 0 : S * c.E * c.H * 4);
-  L.rbpart = take(S * c.E * 4);
+  L.rpart = take(router_part_slices(c) * c.E * c.H * 4);
+  L.rbpart = take(std::max(S, (size_t)router_bias_slices(c)) * c.E * 4);
   L.dlb = take(tcr ? (size_t)c.T * c.E * 2 : 0);
   L.dxr = take(tcr ? (size_t)c.T * c.H * 2 : 0);
+  L.roff = take(256 * 4);
   L.total = o;
   return L;
 }
@@ -144,7 +153,7 @@ BwdLayout bwd_layout(const moe_config_t& c) {
 // moe_router_backward's and moe_dispatch_router_backward's workspace: status head, then the
 // partial sums of the SIMT path, or dl in bf16 and dx_r on the tensor-core path.
 struct RouterBwdLayout {
-  size_t rpart, rbpart, dlb, dxr, total;
+  size_t rpart, rbpart, dlb, dxr, roff, total;
 };
 
 RouterBwdLayout router_bwd_layout(const moe_config_t& c) {
@@ -157,17 +166,18 @@ RouterBwdLayout router_bwd_layout(const moe_config_t& c) {
   };
   const size_t S = (size_t)router_wgrad_slices(c);
   const bool tcr = router_backward_tc(c);
-  L.rpart = take(tcr ? 0 : S * c.E * c.H * 4);
-  L.rbpart = take(S * c.E * 4);
+  L.rpart = take(router_part_slices(c) * c.E * c.H * 4);
+  L.rbpart = take(std::max(S, (size_t)router_bias_slices(c)) * c.E * 4);
   L.dlb = take(tcr ? (size_t)c.T * c.E * 2 : 0);
   L.dxr = take(tcr ? (size_t)c.T * c.H * 2 : 0);
+  L.roff = take(256 * 4);
   L.total = o;
   return L;
 }
 
-RouterScratch router_scratch(char* base, size_t part, size_t bias_part, size_t dlb, size_t dxr) {
+RouterScratch router_scratch(char* base, size_t part, size_t bias_part, size_t dlb, size_t dxr, size_t roff) {
   return RouterScratch{reinterpret_cast<float*>(base + part), reinterpret_cast<float*>(base + bias_part), base + dlb,
-                       base + dxr};
+                       base + dxr, reinterpret_cast<int32_t*>(base + roff)};
 }
 
 bool opt_ok(const void* p) { return p == nullptr || aligned16(p); }
@@ -622,7 +632,7 @@ moe_status_t backward_impl(const moe_config_t* cfg, const void* x, const moe_wei
   }
   float* dl = grads->dlogits ? grads->dlogits : (float*)(bb + B.dl);
   const int32_t* counts = grads->aux_loss_coeff != 0.0f ? (const int32_t*)(fb + F.counts) : nullptr;
-  const RouterScratch sc = router_scratch(bb, B.rpart, B.rbpart, B.dlb, B.dxr);
+  const RouterScratch sc = router_scratch(bb, B.rpart, B.rbpart, B.dlb, B.dxr, B.roff);
   if (e == cudaSuccess)
     e = launch_router_backward(c, (const float*)(fb + F.logits), (const int32_t*)(fb + F.topk_idx), dtopk_w, counts,
                                grads->aux_loss_coeff, x, dl, grads->dw_router, grads->d_router_bias, sc,
@@ -662,7 +672,7 @@ moe_status_t moe_router_backward(const moe_config_t* cfg, const float* logits, c
       (dw_router && !ptr_ok(x)))
     return MOE_ERR_INVALID_ARG;
   const RouterBwdLayout L = router_bwd_layout(c);
-  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr);
+  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr, L.roff);
   return cuda_status(launch_router_backward(c, logits, topk_idx, dtopk_w, counts, aux_alpha, x, dlogits, dw_router,
                                             d_router_bias, sc, status_of(ws), s));
 }
@@ -678,7 +688,7 @@ moe_status_t moe_dispatch_router_backward(const moe_config_t* cfg, const void* d
       !opt_ok(dxd))
     return MOE_ERR_INVALID_ARG;
   const RouterBwdLayout L = router_bwd_layout(*cfg);
-  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr);
+  const RouterScratch sc = router_scratch((char*)ws, L.rpart, L.rbpart, L.dlb, L.dxr, L.roff);
   return cuda_status(launch_router_input_grad(*cfg, dlogits, nullptr, w_router, dxd, tok_row, dx, sc, status_of(ws),
                                               (cudaStream_t)stream));
 }

@@ -91,6 +91,8 @@ struct BwdParams {
   float* w1x;
   int M_out, N_out;
   int extra_b_row0;           // WGRAD_GU: the shared expert's first row in its B map (x)
+  int b_unpadded;             // WGRAD_DOWN: B's rows are the groups' own rows (not padded h);
+                              //   every group but the last then spans whole 64-row K stages
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ay = MODE == WGRAD_GU ? y_pad : row0 + kb * BK;
             a_two_boxes = true;
             tb = extra ? &tmB0x : &tmB0;
-            by = MODE == WGRAD_DOWN ? y_pad : (extra ? p.extra_b_row0 + kb * BK : row0 + kb * BK);
+            by = MODE == WGRAD_DOWN ? (p.b_unpadded ? row0 + kb * BK : y_pad)
+                                    : (extra ? p.extra_b_row0 + kb * BK : row0 + kb * BK);
           } else {
             // A: [rows, K] K-major, this CTA's 128 rows (dgu: padded rows); B: weight rows =
             // the K index, MN-major
@@ -636,11 +639,12 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
 }
 
 bool router_backward_tc_supported(const moe_config_t& c) {
-  return c.act_dtype == MOE_DTYPE_BF16 && c.E % 256 == 0 && c.H % 256 == 0;
+  return c.act_dtype == MOE_DTYPE_BF16 && c.E % 128 == 0 && c.H % 256 == 0;
 }
 
 cudaError_t launch_router_products(const moe_config_t& c, const void* dl_bf16, const void* x, const void* w_router,
-                                   float* dw_router, void* dx_r, DeviceStatus* st, cudaStream_t s) {
+                                   float* dw_router, void* dx_r, DeviceStatus* st, cudaStream_t s,
+                                   const int32_t* slice_offsets, int slices) {
   if (c.T == 0) return cudaSuccess;
   // the tokens are one group: the "extra" group of the kernels (no routed groups), rows [0, T)
   BwdParams p{};
@@ -657,14 +661,34 @@ cudaError_t launch_router_products(const moe_config_t& c, const void* dl_bf16, c
     // dW_router = dl^T x: M_out = E, N_out = H, K = T, both operands MN-major; the maps end
     // at row T, so the last K stage reads zeros past it
     if (!make_bf16_box(&a, dl_bf16, c.T, c.E, 64) || !make_bf16_box(&b, x, c.T, c.H, 64)) return cudaErrorInvalidValue;
+    // 256-row tiles as CTA pairs when E allows, else 128-row tiles on single CTAs. With
+    // slices > 1 the tokens are split into that many groups (K splits, slice_offsets on the
+    // device, whole 64-row stages but the last): dw_router then receives the per-slice
+    // partial sums [slices, E, H], which the caller adds in slice order.
+    const bool pair = c.E % 256 == 0;
     p.M_out = c.E;
     p.N_out = c.H;
-    p.m_tiles_out = c.E / (2 * BM);
+    p.m_tiles_out = c.E / (pair ? 2 * BM : BM);
     p.n_tiles = c.H / BN;
     p.w0 = nullptr;
     p.w0x = dw_router;
-    e = launch<WGRAD_DOWN, 2>(a, b, b, b, b, p, (int64_t)p.m_tiles_out * p.n_tiles, s);
+    if (slices > 1) {
+      p.offsets = slice_offsets;
+      p.G = slices;
+      p.has_extra = 0;
+      p.T_extra = 0;
+      p.w0 = dw_router;
+      p.w0x = nullptr;
+      p.b_unpadded = 1;
+    }
+    const int64_t tiles = (int64_t)(p.G + p.has_extra) * p.m_tiles_out * p.n_tiles;
+    e = pair ? launch<WGRAD_DOWN, 2>(a, b, b, b, b, p, tiles, s) : launch<WGRAD_DOWN, 1>(a, b, b, b, b, p, tiles, s);
     if (e != cudaSuccess) return e;
+    p.offsets = nullptr;
+    p.G = 0;
+    p.has_extra = 1;
+    p.T_extra = c.T;
+    p.b_unpadded = 0;
   }
   if (dx_r) {
     // dx_r = dl W_router: M = T, N = H, K = E; W_router [E, H] read MN-major

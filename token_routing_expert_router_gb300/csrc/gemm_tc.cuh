@@ -40,12 +40,15 @@ cudaError_t launch_grouped_mlp_backward(const moe_config_t& c, const void* xd, c
                                         void* dgu, void* h, void* dxd, const moe_weight_grads_t& gr,
                                         DeviceStatus* st, cudaStream_t s, bool gu_ready = false);
 
-// The router's two products for its backward on the tensor cores (bf16, E and H multiples
-// of 256): dw_router = dl^T x (fp32, NULL to skip) and dx_r = dl W_router (bf16 [T, H], NULL
-// to skip), dl_bf16 [T, E] the logit gradient rounded to bf16.
+// The router's two products for its backward on the tensor cores (bf16, E a multiple of
+// 128, H of 256): dw_router = dl^T x (fp32, NULL to skip) and dx_r = dl W_router (bf16 [T, H], NULL
+// to skip), dl_bf16 [T, E] the logit gradient rounded to bf16. slices > 1: the weight
+// gradient is split over token slices (slice_offsets [slices + 1] on the device, every slice
+// but the last a multiple of 64 tokens) and dw_router receives the partial sums [slices, E, H].
 bool router_backward_tc_supported(const moe_config_t& c);
 cudaError_t launch_router_products(const moe_config_t& c, const void* dl_bf16, const void* x, const void* w_router,
-                                   float* dw_router, void* dx_r, DeviceStatus* st, cudaStream_t s);
+                                   float* dw_router, void* dx_r, DeviceStatus* st, cudaStream_t s,
+                                   const int32_t* slice_offsets = nullptr, int slices = 1);
 
 // MXFP8 (e4m3, UE8M0 scale atoms) variant on the block-scaled MMA.
 bool mx_supported(const moe_config_t& c);

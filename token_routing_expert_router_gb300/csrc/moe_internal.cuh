@@ -65,15 +65,21 @@ cudaError_t launch_quantize_mx(const void* src, int64_t rows, int64_t cols, uint
 
 // Router backward (router_bwd.cu). dl: dL/dlogits [T, E] fp32.
 int router_wgrad_slices(const moe_config_t& c);  // token slices of the split reductions
+int router_bias_slices(const moe_config_t& c);   // slices of the tensor-core path's bias sum
+// token slices of the tensor-core weight gradient: (tokens per slice, slices <= 255)
+void router_tc_slices(const moe_config_t& c, int* slice, int* slices);
 // true: the two router products run on the tensor cores (dl rounded to bf16)
 bool router_backward_tc(const moe_config_t& c);
-// Workspace buffers of the router backward: part [S, E, H] and bias_part [S, E] fp32 (S =
-// router_wgrad_slices), and on the tensor-core path dl_bf16 [T, E] and dx_r [T, H] bf16.
+// Workspace buffers of the router backward: part [S, E, H] fp32 (S = router_wgrad_slices,
+// or on the tensor-core path the slices of router_tc_slices), bias_part
+// [max(S, router_bias_slices), E] fp32, and on the tensor-core path dl_bf16 [T, E], dx_r
+// [T, H] bf16 and slice_offsets [slices + 1].
 struct RouterScratch {
   float* part;
   float* bias_part;
   void* dl_bf16;
   void* dx_r;
+  int32_t* slice_offsets;
 };
 // dl from dtopk_w (+ the aux loss's gradient when counts != NULL); with dw_router, the
 // router weight gradient and (d_bias != NULL) the bias gradient.

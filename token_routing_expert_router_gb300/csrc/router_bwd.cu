@@ -15,7 +15,7 @@
 //  3. input_grad_kernel: dx[t] = sum_e dl[t,e] W_router[e] + sum_j dxd[tok_row[t,j]]
 //     (+ dxd[R + t]): the router's share and the dispatch backward's gather-reduce in one
 //     pass over dx, accumulated in fp32 and rounded to bf16 once.
-// With many experts (E and H multiples of 256, bf16) the two products are dense enough for
+// With many experts (E a multiple of 128, H of 256, bf16) the two products are dense enough for
 // the tensor cores: dl is also written in bf16, dW_router = dl^T x and dx_r = dl W_router
 // run as the expert backward's tcgen05 GEMMs over the tokens as one group, the bias
 // gradient is a column sum of dl, and dx = dx_r + the dispatch rows is the combine kernel
@@ -54,9 +54,13 @@ __global__ void __launch_bounds__(kLgWarps * 32)
     logit_grad_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                       const float* __restrict__ dtopk_w, int T, int E, int k, int score_fn, int renorm, float rho,
                       const int32_t* __restrict__ counts, float aux_a0, float* __restrict__ dl,
-                      __nv_bfloat16* __restrict__ dlb, DeviceStatus* st) {
+                      __nv_bfloat16* __restrict__ dlb, int32_t* __restrict__ slice_offsets, int slice, int slices,
+                      DeviceStatus* st) {
   __shared__ float row_s[kLgWarps][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the token slices of the tensor-core weight gradient (read by a later launch)
+  if (slice_offsets != nullptr && blockIdx.x == 0 && (int)threadIdx.x <= slices)
+    slice_offsets[threadIdx.x] = (int)min((int64_t)threadIdx.x * slice, (int64_t)T);
   const int t = blockIdx.x * kLgWarps + warp;
   if (t >= T) return;
   const float* l = logits + (int64_t)t * E;
@@ -170,14 +174,32 @@ __global__ void __launch_bounds__(kLgWarps * 32)
   }
 }
 
-// Column sums of dl over token slice z (the bias gradient's partials), one thread per expert.
-__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ dl, int T, int E, int slice,
+// Column sums of src [rows, cols] over row slice b (rows [b * slice, + slice)) -> out[b, :]:
+// the bias gradient's two levels (dl's token slices, then the slices' partials). With
+// cols <= 256 the block's threads split into 256 / cols row phases; every thread keeps four
+// independent partial sums (rows i = 0, 1, 2, 3 mod 4 of its phase) so that loads overlap,
+// and the partials and then the phases are added in a fixed order.
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ src, int rows, int cols, int slice,
                                                      float* __restrict__ out) {
-  const int t0 = blockIdx.x * slice, t1 = min(T, t0 + slice);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float a = 0.0f;
-    for (int t = t0; t < t1; ++t) a += dl[(int64_t)t * E + e];
-    out[(int64_t)blockIdx.x * E + e] = a;
+  __shared__ float red[256];
+  const int r0 = blockIdx.x * slice, r1 = min(rows, r0 + slice);
+  const int nph = cols <= 256 ? 256 / cols : 1;
+  for (int cbase = 0; cbase < cols; cbase += 256) {
+    const int c = cbase + (cols <= 256 ? (int)threadIdx.x % cols : (int)threadIdx.x);
+    const int ph = cols <= 256 ? (int)threadIdx.x / cols : 0;
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (ph < nph && c < cols) {
+      int i = 0;
+      for (int r = r0 + ph; r < r1; r += nph, ++i) a[i & 3] += src[(int64_t)r * cols + c];
+    }
+    __syncthreads();
+    red[threadIdx.x] = (a[0] + a[1]) + (a[2] + a[3]);
+    __syncthreads();
+    if (ph == 0 && c < cols) {
+      float v = red[threadIdx.x];
+      for (int q = 1; q < nph; ++q) v += red[threadIdx.x + q * cols];
+      out[(int64_t)blockIdx.x * cols + c] = v;
+    }
   }
 }
 
@@ -194,6 +216,7 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ 
 // loads issued before the current stage's products.
 // ---------------------------------------------------------------------------------------
 constexpr int kWgBN = 128, kWgBK = 32, kWgThreads = 256;
+constexpr int kBiasSlice = 128;  // tokens per slice of the tensor-core path's bias gradient
 
 template <int BM, bool BF16>
 __global__ void __launch_bounds__(kWgThreads)
@@ -488,6 +511,20 @@ __global__ void __launch_bounds__(128)
 
 }  // namespace
 
+int router_bias_slices(const moe_config_t& c) { return (int)std::max<int64_t>(1, ceil_div(c.T, kBiasSlice)); }
+
+void router_tc_slices(const moe_config_t& c, int* slice, int* slices) {
+  // SMs one token slice occupies (CTA pairs of 256 rows when E allows, else single CTAs of
+  // 128), and as many slices as fill the 152 SMs, each a whole number of 64-token K stages
+  const int64_t sms = (c.E % 256 == 0 ? 2 * (c.E / 256) : c.E / 128) * (int64_t)std::max(1, c.H / 256);
+  int64_t s = std::max<int64_t>(1, 152 / std::max<int64_t>(1, sms));
+  s = std::min<int64_t>(s, std::max<int64_t>(1, ceil_div(c.T, 64)));
+  s = std::min<int64_t>(s, 255);
+  const int64_t len = std::max<int64_t>(64, ceil_div(ceil_div(c.T, s), 64) * 64);
+  *slice = (int)len;
+  *slices = (int)std::max<int64_t>(1, ceil_div(c.T, len));
+}
+
 int router_wgrad_slices(const moe_config_t& c) {
   const int bm = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
   const int64_t tiles = ceil_div(c.H, kWgBN) * ceil_div(c.E, bm);
@@ -511,11 +548,11 @@ void slices_of(const moe_config_t& c, int* slice, int* used) {
   *used = (int)ceil_div(c.T, *slice);  // <= S
 }
 
+// d_bias = column sums of dl: slices of kBiasSlice tokens, then one block over the slices.
 cudaError_t bias_grad(const moe_config_t& c, const float* dl, float* d_bias, float* bias_part, cudaStream_t s) {
-  int slice, used;
-  slices_of(c, &slice, &used);
-  colsum_kernel<<<used, 256, 0, s>>>(dl, c.T, c.E, slice, used > 1 ? bias_part : d_bias);
-  if (used > 1) sum_slices_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, d_bias);
+  const int used = (int)ceil_div(c.T, kBiasSlice);
+  colsum_kernel<<<used, 256, 0, s>>>(dl, c.T, c.E, kBiasSlice, used > 1 ? bias_part : d_bias);
+  if (used > 1) colsum_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, used, d_bias);
   return cudaGetLastError();
 }
 
@@ -541,7 +578,7 @@ cudaError_t simt_wgrad(const moe_config_t& c, const float* dl, const void* x, fl
   const int64_t n = (int64_t)c.E * c.H;
   const int blocks = (int)std::min<int64_t>(ceil_div(n / 4, 256), 152 * 8);
   sum_slices_kernel<<<blocks, 256, 0, s>>>(part, used, n, dw_router);
-  if (d_bias) sum_slices_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, d_bias);
+  if (d_bias) colsum_kernel<<<1, 256, 0, s>>>(bias_part, used, c.E, used, d_bias);
   return cudaGetLastError();
 }
 
@@ -561,9 +598,13 @@ cudaError_t launch_router_backward(const moe_config_t& c, const float* logits, c
   const dim3 grid((unsigned)ceil_div(c.T, kLgWarps));
   const int epl = (int)ceil_div(c.E, 32);
   __nv_bfloat16* dlb = tc_path ? static_cast<__nv_bfloat16*>(sc.dl_bf16) : nullptr;
+  int tslice = 0, tslices = 1;
+  if (tc_path) router_tc_slices(c, &tslice, &tslices);
+  int32_t* soff = (tc_path && dw_router && tslices > 1) ? sc.slice_offsets : nullptr;
 #define MOE_LG(N)                                                                                              \
   logit_grad_kernel<N><<<grid, kLgWarps * 32, 0, s>>>(logits, topk_idx, dtopk_w, c.T, c.E, c.k, c.score_fn,     \
-                                                       c.renorm, c.routed_scale, counts, a0, dl, dlb, st)
+                                                       c.renorm, c.routed_scale, counts, a0, dl, dlb, soff, tslice,  \
+                                                       tslices, st)
   if (epl <= 1) MOE_LG(1);
   else if (epl <= 2) MOE_LG(2);
   else if (epl <= 4) MOE_LG(4);
@@ -573,7 +614,17 @@ cudaError_t launch_router_backward(const moe_config_t& c, const float* logits, c
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !dw_router) return e;
   if (!tc_path) return simt_wgrad(c, dl, x, dw_router, d_bias, sc.part, sc.bias_part, s);
-  e = tc::launch_router_products(c, dlb, x, nullptr, dw_router, nullptr, st, s);
+  if (tslices > 1) {  // K split over token slices, then their partial sums in slice order
+    e = tc::launch_router_products(c, dlb, x, nullptr, sc.part, nullptr, st, s, soff, tslices);
+    if (e == cudaSuccess) {
+      const int64_t n = (int64_t)c.E * c.H;
+      const int blocks = (int)std::min<int64_t>(ceil_div(n / 4, 256), 152 * 8);
+      sum_slices_kernel<<<blocks, 256, 0, s>>>(sc.part, tslices, n, dw_router);
+      e = cudaGetLastError();
+    }
+  } else {
+    e = tc::launch_router_products(c, dlb, x, nullptr, dw_router, nullptr, st, s);
+  }
   if (e == cudaSuccess && d_bias) e = bias_grad(c, dl, d_bias, sc.bias_part, s);
   return e;
 }
