@@ -245,3 +245,84 @@ def test_fullsize_combine_sampled(name):
             ref[i] += synth.rows(9, synth.YD, [R + t], H, 1.0, "bf16")[0]
     got = np_of(y[torch.from_numpy(toks).cuda()]).astype(np.float64)
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+
+
+@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_bf16"])
+def test_fullsize_training_step_sampled_tokens(name):
+    """The training step at full size, in the calls the benchmark times (moe_forward_train,
+    then moe_backward_kept with the router's backward): for sampled tokens whose routing is
+    unambiguous, dx (through the experts and through the router) and dlogits against the
+    oracle's chain rule, token by token; and dW_router against its defining identity
+    dl^T x on sampled experts (a property of the outputs at any size). dy is drawn on the
+    GPU by the generator's device twin and redrawn on the host from the same counters."""
+    L = layer(name)
+    w, cfg, d = L.w, L.cfg, L.d
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    shared = bool(w["n_shared"])
+    rows = T * k + (T if shared else 0)
+    bf, f32 = dict(dtype=torch.bfloat16, device="cuda"), dict(dtype=torch.float32, device="cuda")
+    gu = torch.empty((rows, 2 * F), **bf)
+    y = torch.empty((T, H), **bf)
+    moe.moe_forward_train(cfg, d["x"], weights_arg(d), y, L.ws, gu)
+    dy = synth.device_normal(torch.empty((T, H), **bf), 0, synth.DY, 1.0)
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(bws)
+    g = {"dw_gate": torch.empty((E, F, H), **f32), "dw_up": torch.empty((E, F, H), **f32),
+         "dw_down": torch.empty((E, H, F), **f32), "dw_router": torch.empty((E, H), **f32),
+         "dlogits": torch.empty((T, E), **f32)}
+    if shared:
+        Fs = w["F_shared"]
+        g.update(dws_gate=torch.empty((Fs, H), **f32), dws_up=torch.empty((Fs, H), **f32),
+                 dws_down=torch.empty((H, Fs), **f32))
+    dx = torch.empty((T, H), **bf)
+    dtw = torch.empty((T, k), **f32)
+    moe.moe_backward_kept(cfg, d["x"], weights_arg(d), dy, L.ws, gu, dx, dtw, g, bws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(bws) == moe.MOE_OK
+    # sampled tokens, routed by the oracle from its own logits
+    toks = sample_tokens(w, 3)
+    xs = synth.rows(0, synth.X, toks, H, 1.0, "bf16")
+    dys = synth.rows(0, synth.DY, toks, H, 1.0, "bf16")
+    assert np.array_equal(np_of(dy[torch.from_numpy(toks).cuda()].float()), dys)  # device twin == host
+    wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], "bf16")
+    bias = synth.zipf_bias(0, E) if w["zipf"] else None
+    l_ref = oracle.router_logits(xs, wr, bias)
+    idx_ref, wt_ref = oracle.route(l_ref, dict(w, T=len(toks)))
+    l_gpu = np_of(L.logits[torch.from_numpy(toks).cuda()])
+    amb = routing_ambiguity(w, l_ref, float(np.abs(l_gpu.astype(np.float64) - l_ref).max()))
+    idx_gpu = np_of(L.idx)[toks]
+    same = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
+    assert np.all(same | amb) and same.any()
+    experts = {}
+    dx_gpu = np_of(dx.float()).astype(np.float64)[toks]
+    dl_gpu = np_of(g["dlogits"]).astype(np.float64)[toks]
+    for i in np.nonzero(same)[0]:
+        a = xs[i:i + 1].astype(np.float64)
+        dyt = dys[i].astype(np.float64)
+        dx_ref = np.zeros(H)
+        dtw_ref = np.zeros(k)
+        for j in range(k):
+            e = int(idx_ref[i, j])
+            if e not in experts:
+                experts[e] = host_expert(w, e, 0)
+            wg, wu, wd = experts[e]
+            dtw_ref[j] = dyt @ oracle.expert_mlp(a, wg, wu, wd)[0]
+            dx_ref += oracle.expert_mlp_backward(a, wg, wu, wd, (wt_ref[i, j] * dyt)[None])[0][0]
+        if shared:
+            dx_ref += oracle.expert_mlp_backward(a, *host_shared(w, 0), dyt[None])[0][0]
+        dl_ref = oracle.router_backward(w, l_ref[i:i + 1], idx_ref[i:i + 1], dtw_ref[None])[0]
+        dx_ref += dl_ref @ wr.astype(np.float64)
+        assert oracle.rel_l2(dx_gpu[i], dx_ref) < 2e-2, (i, oracle.rel_l2(dx_gpu[i], dx_ref))
+        # dlogits is a difference of the routing-weight gradients (softmax: q_j (g_j - <g, q>)),
+        # each a dot product over H taken from bf16 expert outputs, so it is bounded against
+        # their scale, rho * max |dtopk_w|, not its own (which can be a small difference)
+        scale = float(w["routed_scale"]) * np.abs(dtw_ref).max()
+        assert np.abs(dl_gpu[i] - dl_ref).max() <= 2e-2 * scale, (i, dl_gpu[i], dl_ref, scale)
+    # dW_router = dl^T x on sampled experts (x redrawn on the host)
+    x_all = synth.normal(0, synth.X, (T, H), 1.0, "bf16").astype(np.float64)
+    dl_all = np_of(g["dlogits"]).astype(np.float64)
+    dwr = np_of(g["dw_router"]).astype(np.float64)
+    tc_path = E % 128 == 0 and H % 256 == 0
+    for e in (0, E // 2, E - 1):
+        ident = dl_all[:, e] @ x_all
+        assert oracle.rel_l2(dwr[e], ident) < (8e-3 if tc_path else 1e-5), e
