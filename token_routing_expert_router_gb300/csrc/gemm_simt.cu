@@ -72,18 +72,32 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(SimtGemmArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) { acc0[i][j] = 0.0f; acc1[i][j] = 0.0f; }
 
-  for (int k0 = 0; k0 < K; k0 += BK) {
-    // 64 x 16 tiles: each thread loads 4 elements of A and 4 of each B
+  // 64 x 16 tiles: each thread loads 4 elements of A and 4 of each B, the next K tile's
+  // into registers while the current one is multiplied
+  float ra[4], rb0[4], rb1[4];
+  auto load = [&](int k0) {
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       const int e = threadIdx.x + l * NT;  // 0..1023
       const int r = e / BK, kk = e % BK;
       const int gr = m0 + r, gk = k0 + kk, gn = n0 + r;
-      As[kk][r] = (gr < M && gk < K) ? ld_elem<BF16>(A, (row_in + gr) * K + gk) : 0.0f;
-      Bs[0][kk][r] = (gn < N && gk < K) ? ld_elem<BF16>(B0, (int64_t)gn * K + gk) : 0.0f;
-      if (MODE == 1) Bs[1][kk][r] = (gn < N && gk < K) ? ld_elem<BF16>(B1, (int64_t)gn * K + gk) : 0.0f;
+      ra[l] = (gr < M && gk < K) ? ld_elem<BF16>(A, (row_in + gr) * K + gk) : 0.0f;
+      rb0[l] = (gn < N && gk < K) ? ld_elem<BF16>(B0, (int64_t)gn * K + gk) : 0.0f;
+      if (MODE == 1) rb1[l] = (gn < N && gk < K) ? ld_elem<BF16>(B1, (int64_t)gn * K + gk) : 0.0f;
+    }
+  };
+  if (K > 0) load(0);
+  for (int k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int e = threadIdx.x + l * NT;
+      const int r = e / BK, kk = e % BK;
+      As[kk][r] = ra[l];
+      Bs[0][kk][r] = rb0[l];
+      if (MODE == 1) Bs[1][kk][r] = rb1[l];
     }
     __syncthreads();
+    if (k0 + BK < K) load(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float av[4], bv[4], cv[4];
