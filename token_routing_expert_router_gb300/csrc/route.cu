@@ -340,6 +340,101 @@ __global__ void __launch_bounds__(32) scan_assign_kernel(
   }
 }
 
+// S2 for small batches (T <= kScanSmallT): the three passes above in one launch of one
+// 1024-thread block. The counts come from shared-memory atomics, the offsets from one
+// block-wide scan over the experts (E <= 512), and warp 0 walks the tokens in ascending
+// order 32 at a time with the same lane-mask ranks as scan_assign_kernel, so the map is the
+// same bit for bit. Shared memory: hist [E], counter [E], mask [E].
+constexpr int kScanSmallT = 512;
+
+__global__ void __launch_bounds__(1024) scan_small_kernel(const int32_t* __restrict__ topk_idx, int T, int k, int E,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ row_token,
+                                                          int32_t* __restrict__ tok_row, DeviceStatus* st) {
+  extern __shared__ int32_t sm[];
+  int32_t* hist = sm;
+  int32_t* counter = sm + E;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(sm + 2 * E);
+  __shared__ int32_t warp_tot[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    hist[e] = 0;
+    mask[e] = 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    int e = topk_idx[i];
+    if (e < 0 || e >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, i / k); e = 0; }
+    atomicAdd(&hist[e], 1);  // a count: the order of the adds does not show
+  }
+  __syncthreads();
+  // exclusive scan over the experts (one element per thread, E <= 512 < blockDim)
+  const int e = threadIdx.x;
+  const int32_t tot = e < E ? hist[e] : 0;
+  int32_t inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t wv = warp_tot[lane];
+    int32_t wi = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(kFull, wi, off);
+      if (lane >= off) wi += o;
+    }
+    warp_tot[lane] = wi - wv;
+  }
+  __syncthreads();
+  const int32_t excl = warp_tot[warp] + inc - tot;
+  if (e < E) {
+    counts[e] = tot;
+    offsets[e] = excl;
+    counter[e] = excl;
+  }
+  if (e == E - 1) offsets[E] = excl + tot;
+  __syncthreads();
+  if (warp != 0) return;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int t0 = 0; t0 < T; t0 += 32) {
+    const int t = t0 + lane;
+    const bool valid = t < T;
+    const int32_t* ids = topk_idx + (int64_t)t * k;
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int ej = ids[j];
+        if (ej < 0 || ej >= E) ej = 0;
+        const uint32_t old = atomicOr(&mask[ej], 1u << lane);
+        if (old >> lane & 1) set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t);  // repeated id
+      }
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int ej = ids[j];
+        if (ej < 0 || ej >= E) ej = 0;
+        const int32_t r = counter[ej] + __popc(mask[ej] & below);
+        row_token[r] = t;
+        tok_row[(int64_t)t * k + j] = r;
+      }
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        int ej = ids[j];
+        if (ej < 0 || ej >= E) ej = 0;
+        const uint32_t m = mask[ej];
+        if (m && 31 - __clz(m) == lane) {  // the highest lane closes expert ej's batch
+          counter[ej] += __popc(m);
+          mask[ej] = 0;
+        }
+      }
+    __syncwarp();
+  }
+}
+
 // S0 for small expert counts (E <= EP <= 32): one 256-thread block per TB tokens; the
 // threads split the hidden dimension (16-byte chunks c = tid, tid + 256, ...), each keeping
 // TB x E partial dot products, then a warp reduction and a cross-warp sum through smem.
@@ -551,6 +646,11 @@ cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_
 cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
                               int32_t* offsets, int32_t* row_token, int32_t* tok_row,
                               int32_t* blockcnt, DeviceStatus* st, cudaStream_t s) {
+  if (c.T > 0 && c.T <= kScanSmallT) {  // small batches: one launch
+    scan_small_kernel<<<1, 1024, (size_t)3 * c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, counts, offsets,
+                                                                         row_token, tok_row, st);
+    return cudaGetLastError();
+  }
   const int NB = scan_blocks(c);
   if (NB > 0) {
     scan_count_kernel<<<NB, kScanChunk, c.E * sizeof(int32_t), s>>>(topk_idx, c.T, c.k, c.E, blockcnt, st);
