@@ -156,6 +156,9 @@ def test_router_backward_rejected_on_host(L):
                                P(4096), None) == moe.MOE_ERR_UNSUPPORTED
     assert L.moe_forward_train(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096 + 8),
                                None) == moe.MOE_ERR_INVALID_ARG
+    # no tokens: nothing to keep, no buffer is touched
+    assert L.moe_forward_train(ctypes.byref(cfg(T=0, H=256)), None, ctypes.byref(w), None, None, None,
+                               None) == moe.MOE_OK
     g0 = moe.MoEWeightGrads.from_tensors({"dw_gate": 4096, "dw_up": 4096, "dw_down": 4096})
     assert L.moe_backward_kept(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), None, P(4096),
                                P(4096), ctypes.byref(g0), P(4096), None) == moe.MOE_ERR_INVALID_ARG

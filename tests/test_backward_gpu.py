@@ -268,3 +268,9 @@ def test_backward_no_tokens_gives_zero_weight_gradients():
     torch.cuda.synchronize()
     for key, v in g.items():
         assert not v.any(), key
+    for v in g.values():
+        v.fill_(7.0)
+    moe.moe_backward_kept(cfg, None, weights_arg(d), None, None, None, None, None, g, bws)
+    torch.cuda.synchronize()
+    for key, v in g.items():
+        assert not v.any(), key
