@@ -551,6 +551,22 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     for f in stages.values():
         f()
     moe.moe_forward_train(cfg, x, wts, yt, ws, gu)  # the kept g and u match ws again
+
+    # the whole training step (training forward + training backward) as one CUDA graph
+    def train_step():
+        moe.moe_forward_train(cfg, x, wts, yt, ws, gu)
+        moe.moe_backward_kept(cfg, x, wts, dy, ws, gu, dx, dtw, rgrads, bws)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        train_step()
+    torch.cuda.current_stream().wait_stream(side)
+    tgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(tgraph):
+        train_step()
+    tgraph.replay()
+    stages["training_step_graph"] = tgraph.replay
     reps = max(3, min(args.steps, 5))
     times = {n: [] for n in stages}
     for _ in range(reps):
@@ -573,7 +589,11 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
             "grouped_gemm_tflops": round(tf, 1), "grouped_gemm_frac_of_peak": round(tf / peak, 3),
             "algorithmic_flops": flops, "recompute_flops": recompute,
             "router_flops": 4.0 * T * H * E,
+            "training_step_ms": round(ms["forward_train"] + ms["backward"], 4),
+            "training_step_graph_ms": round(ms["training_step_graph"], 4),
+            "training_step_tokens_per_s": round(T / (ms["training_step_graph"] / 1e3), 1),
             "note": "the step: moe_backward_kept after moe_forward_train (gate/up pre-activations kept), with "
+                    "training_step_graph: both replayed as one CUDA graph; "
                     "the router's backward and the auxiliary loss's gradient; backward_recompute reruns the gate/up "
                     "GEMM instead; grouped_gemm_tflops: dgrad + wgrad flops over the grouped MLP backward time "
                     "(which includes that recompute); router_flops: dW_router and dx's router share (tensor cores when E and H are multiples of "

@@ -253,6 +253,58 @@ def test_forward_train_keeps_what_the_backward_recomputes(w):
         assert oracle.rel_l2(blocks[:, 1].ravel(), uref) < 1e-2, r
 
 
+def test_training_step_replays_from_a_cuda_graph():
+    """moe_forward_train + moe_backward_kept (router and auxiliary loss included) issue no
+    host sync, so the whole training step captures into one CUDA graph; a replay gives the
+    eager call's bits."""
+    w = CASES[4]
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    rows = T * k + (T if w["n_shared"] else 0)
+    inp = synth.host_inputs(w, seed=35)
+    d = device_weights_from_host(w, inp)
+    cfg = cfg_of(w)
+    fws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(fws)
+    moe.moe_workspace_init(bws)
+    dy = up(synth.normal(35, 50, (T, H), 1.0, "bf16"), torch.bfloat16)
+
+    def buffers():
+        g = grads_alloc(w)
+        g.update(dw_router=torch.empty((E, H), dtype=torch.float32, device="cuda"),
+                 dlogits=torch.empty((T, E), dtype=torch.float32, device="cuda"), aux_loss_coeff=0.01)
+        return dict(g, y=torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
+                    gu=torch.empty((rows, 2 * F), dtype=torch.bfloat16, device="cuda"),
+                    dx=torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
+                    dtw=torch.empty((T, k), dtype=torch.float32, device="cuda"))
+
+    def step(b):
+        moe.moe_forward_train(cfg, d["x"], weights_arg(d), b["y"], fws, b["gu"])
+        moe.moe_backward_kept(cfg, d["x"], weights_arg(d), dy, fws, b["gu"], b["dx"], b["dtw"], b, bws)
+
+    eager = buffers()
+    step(eager)
+    torch.cuda.synchronize()
+    replayed = buffers()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(replayed)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    for v in replayed.values():
+        if isinstance(v, torch.Tensor):
+            v.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(replayed)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(fws) == moe.MOE_OK and moe.moe_read_status(bws) == moe.MOE_OK
+    for key, v in eager.items():
+        if isinstance(v, torch.Tensor):
+            assert torch.equal(v, replayed[key]), key
+
+
 def test_backward_no_tokens_gives_zero_weight_gradients():
     w = synth.scaled(CASES[1], T=0)
     cfg = cfg_of(w)
