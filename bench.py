@@ -530,10 +530,11 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     dxd = torch.empty((rows, H), dtype=dt, device=dev)
     gu = torch.empty((rows, 2 * F), dtype=dt, device=dev)
     yt = torch.empty((T, H), dtype=dt, device=dev)
-    moe.moe_forward_train(cfg, x, wts, yt, ws, gu)
+    aux = torch.empty((1,), dtype=torch.float32, device=dev)
+    moe.moe_forward_train(cfg, x, wts, yt, ws, gu, aux_alpha=0.01, aux_loss=aux)
     stages = {
         "backward": lambda: moe.moe_backward_kept(cfg, x, wts, dy, ws, gu, dx, dtw, rgrads, bws),
-        "forward_train": lambda: moe.moe_forward_train(cfg, x, wts, yt, ws, gu),
+        "forward_train": lambda: moe.moe_forward_train(cfg, x, wts, yt, ws, gu, aux_alpha=0.01, aux_loss=aux),
         "forward_same_timing": lambda: moe.moe_forward(cfg, x, wts, yt, ws),
         "backward_recompute": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, rgrads, bws),
         "backward_without_router": lambda: moe.moe_backward(cfg, x, wts, dy, ws, dx, dtw, grads, bws),
@@ -550,11 +551,11 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     }
     for f in stages.values():
         f()
-    moe.moe_forward_train(cfg, x, wts, yt, ws, gu)  # the kept g and u match ws again
+    moe.moe_forward_train(cfg, x, wts, yt, ws, gu, aux_alpha=0.01, aux_loss=aux)  # g and u match ws again
 
     # the whole training step (training forward + training backward) as one CUDA graph
     def train_step():
-        moe.moe_forward_train(cfg, x, wts, yt, ws, gu)
+        moe.moe_forward_train(cfg, x, wts, yt, ws, gu, aux_alpha=0.01, aux_loss=aux)
         moe.moe_backward_kept(cfg, x, wts, dy, ws, gu, dx, dtw, rgrads, bws)
 
     side = torch.cuda.Stream(device=dev)

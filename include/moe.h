@@ -338,9 +338,12 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
  * summary, section 2.2, granular recomputation: activation functions are recomputed rather
  * than stored), instead of rerunning the gate/up GEMM. gu is caller-owned: R(+T) * 2F * 2
  * bytes, 16-byte aligned. bf16 layers the backward takes (else MOE_ERR_UNSUPPORTED); y and
- * the workspace are bit-identical to moe_forward's. */
+ * the workspace are bit-identical to moe_forward's. aux_loss: NULL, or one device float
+ * that receives moe_aux_loss's loss (coefficient aux_alpha; a NaN coefficient is
+ * MOE_ERR_INVALID_ARG) on this call's logits and counts (0 when T = 0); pass the same
+ * coefficient as grads->aux_loss_coeff to moe_backward_kept for its gradient. */
 moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
-                               void* gu, moe_stream_t stream);
+                               void* gu, float aux_alpha, float* aux_loss, moe_stream_t stream);
 
 /* moe_backward after moe_forward_train: reads the kept gu instead of recomputing it. The
  * kept values are the ones the recomputation would produce, so every output is

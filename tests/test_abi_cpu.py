@@ -152,12 +152,15 @@ def test_router_backward_rejected_on_host(L):
     assert L.moe_backward(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096), P(4096),
                           ctypes.byref(g), P(4096), None) == moe.MOE_ERR_INVALID_ARG
     # the training forward keeps g and u only for layers the backward takes, into an aligned buffer
+    f0 = ctypes.c_float(0.0)
     assert L.moe_forward_train(ctypes.byref(cfg(act_dtype=moe.F32)), P(4096), ctypes.byref(w), P(4096), P(4096),
-                               P(4096), None) == moe.MOE_ERR_UNSUPPORTED
-    assert L.moe_forward_train(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096 + 8),
+                               P(4096), f0, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_forward_train(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096 + 8), f0, None,
                                None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_train(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), P(4096),
+                               ctypes.c_float(float("nan")), P(4096), None) == moe.MOE_ERR_INVALID_ARG
     # no tokens: nothing to keep, no buffer is touched
-    assert L.moe_forward_train(ctypes.byref(cfg(T=0, H=256)), None, ctypes.byref(w), None, None, None,
+    assert L.moe_forward_train(ctypes.byref(cfg(T=0, H=256)), None, ctypes.byref(w), None, None, None, f0, None,
                                None) == moe.MOE_OK
     g0 = moe.MoEWeightGrads.from_tensors({"dw_gate": 4096, "dw_up": 4096, "dw_down": 4096})
     assert L.moe_backward_kept(ctypes.byref(bf), P(4096), ctypes.byref(w), P(4096), P(4096), None, P(4096),

@@ -210,7 +210,8 @@ def test_forward_train_keeps_what_the_backward_recomputes(w):
     moe.moe_forward(cfg, d["x"], weights_arg(d), y0, fws)
     y1 = torch.empty_like(y0)
     gu = torch.full((rows, 2 * F), float("nan"), dtype=torch.bfloat16, device="cuda")
-    moe.moe_forward_train(cfg, d["x"], weights_arg(d), y1, fws, gu)
+    aux = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_forward_train(cfg, d["x"], weights_arg(d), y1, fws, gu, aux_alpha=0.01, aux_loss=aux)
     assert moe.moe_read_status(fws) == moe.MOE_OK
     assert torch.equal(y0, y1)
     dy = up(synth.normal(seed, 50, (T, H), 1.0, "bf16"), torch.bfloat16)
@@ -237,6 +238,12 @@ def test_forward_train_keeps_what_the_backward_recomputes(w):
     b = alloc(w)
     moe.moe_forward(cfg, d["x"], weights_arg(d), y0, fws, idx)
     moe.moe_route_from_map(b["cfg"], idx, b["counts"], b["offsets"], b["row_token"], b["tok_row"], b["ws"])
+    # the auxiliary loss it returned is moe_aux_loss on the same logits and counts
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(cfg, d["x"], d["w_router"], d.get("router_bias"), logits, b["ws"])
+    aux2 = torch.empty((1,), dtype=torch.float32, device="cuda")
+    moe.moe_aux_loss(cfg, logits, b["counts"], 0.01, aux2, b["ws"])
+    assert torch.equal(aux, aux2) and bool(torch.isfinite(aux).all())
     row_token = np_of(b["row_token"])
     offsets = np_of(b["offsets"])
     x64 = inp["x"].astype(np.float64)
@@ -276,10 +283,11 @@ def test_training_step_replays_from_a_cuda_graph():
         return dict(g, y=torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
                     gu=torch.empty((rows, 2 * F), dtype=torch.bfloat16, device="cuda"),
                     dx=torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
-                    dtw=torch.empty((T, k), dtype=torch.float32, device="cuda"))
+                    dtw=torch.empty((T, k), dtype=torch.float32, device="cuda"),
+                    aux=torch.empty((1,), dtype=torch.float32, device="cuda"))
 
     def step(b):
-        moe.moe_forward_train(cfg, d["x"], weights_arg(d), b["y"], fws, b["gu"])
+        moe.moe_forward_train(cfg, d["x"], weights_arg(d), b["y"], fws, b["gu"], aux_alpha=0.01, aux_loss=b["aux"])
         moe.moe_backward_kept(cfg, d["x"], weights_arg(d), dy, fws, b["gu"], b["dx"], b["dtw"], b, bws)
 
     eager = buffers()

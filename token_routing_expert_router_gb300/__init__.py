@@ -113,7 +113,7 @@ def lib():
             "moe_grouped_mlp_backward": [cfg, P, P, P, wts, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_dispatch_backward": [cfg, P, P, P, P],
             "moe_backward": [cfg, P, wts, P, P, P, P, POINTER(MoEWeightGrads), P, P],
-            "moe_forward_train": [cfg, P, wts, P, P, P, P],
+            "moe_forward_train": [cfg, P, wts, P, P, P, ctypes.c_float, P, P],
             "moe_backward_kept": [cfg, P, wts, P, P, P, P, P, POINTER(MoEWeightGrads), P, P],
             "moe_router_backward_workspace_size": [cfg, POINTER(c_size_t)],
             "moe_router_backward": [cfg, P, P, P, P, ctypes.c_float, P, P, P, P, P, P],
@@ -316,11 +316,12 @@ def moe_backward(cfg, x, weights: dict, dy, fwd_ws, dx, dtopk_w, grads: dict, bw
                               byref(g), _ptr(bwd_ws), _stream(stream)), "moe_backward")
 
 
-def moe_forward_train(cfg, x, weights: dict, y, ws, gu, stream=None):
-    """moe_forward that also keeps the gate/up pre-activations in gu [R(+T), 2F] bf16."""
+def moe_forward_train(cfg, x, weights: dict, y, ws, gu, aux_alpha=0.0, aux_loss=None, stream=None):
+    """moe_forward that also keeps the gate/up pre-activations in gu [R(+T), 2F] bf16, and
+    (aux_loss: a 1-element fp32 CUDA tensor) computes the auxiliary load-balancing loss."""
     w = MoEWeights.from_tensors(weights)
-    _check(lib().moe_forward_train(byref(cfg), _ptr(x), byref(w), _ptr(y), _ptr(ws), _ptr(gu), _stream(stream)),
-           "moe_forward_train")
+    _check(lib().moe_forward_train(byref(cfg), _ptr(x), byref(w), _ptr(y), _ptr(ws), _ptr(gu), float(aux_alpha),
+                                   _ptr(aux_loss), _stream(stream)), "moe_forward_train")
 
 
 def moe_backward_kept(cfg, x, weights: dict, dy, fwd_ws, gu, dx, dtopk_w, grads: dict, bwd_ws, stream=None):

@@ -426,11 +426,13 @@ namespace {
 // moe_forward, and with keep (moe_forward_train) GEMM1 also keeps g and u in gu_keep.
 moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
                           int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, bool keep, void* gu_keep,
-                          moe_stream_t stream) {
+                          moe_stream_t stream, float aux_alpha = 0.0f, float* aux_loss_out = nullptr) {
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (keep && !tc::mlp_backward_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->T == 0) return MOE_OK;
+  if (aux_loss_out && !(aux_alpha == aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0)
+    return aux_loss_out ? cuda_status(cudaMemsetAsync(aux_loss_out, 0, sizeof(float), (cudaStream_t)stream)) : MOE_OK;
   v = check_weights(*cfg, w, true);
   if (v != MOE_OK) return v;
   if (!ptr_ok(x) || !ptr_ok(y) || !ptr_ok(ws) || (keep && !ptr_ok(gu_keep))) return MOE_ERR_INVALID_ARG;
@@ -461,6 +463,8 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weig
   if (e == cudaSuccess)
     e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
                           status_of(ws), s);
+  if (e == cudaSuccess && aux_loss_out)  // the scan's scratch is free again: it holds the partials
+    e = launch_aux_loss(c, logits, counts, aux_alpha, aux_loss_out, reinterpret_cast<float*>(blockcnt_of(ws)), s);
   if (e == cudaSuccess)
     e = is_mx(c) ? launch_dispatch_mx(c, x, topk_idx, tok_row, offsets, xd, xd_scale, s)
                  : launch_dispatch(c, x, tok_row, xd, static_cast<float*>(xd_scale), s);
@@ -487,8 +491,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const moe_weigh
 }
 
 moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
-                               void* gu, moe_stream_t stream) {
-  return forward_impl(cfg, x, w, y, ws, nullptr, nullptr, nullptr, true, gu, stream);
+                               void* gu, float aux_alpha, float* aux_loss, moe_stream_t stream) {
+  return forward_impl(cfg, x, w, y, ws, nullptr, nullptr, nullptr, true, gu, stream, aux_alpha, aux_loss);
 }
 
 moe_status_t moe_forward_host(const moe_config_t* cfg, const void* x_host, const moe_weights_t* w,
