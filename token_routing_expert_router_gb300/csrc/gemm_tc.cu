@@ -51,6 +51,8 @@ struct TcParams {
   const float* bias;        // EPI_STORE_F32_BIAS: [N] or null
   const int32_t* row_token; // non-null: routed A rows are gathered, row r = token row_token[r]
                             //   of tmA (a one-row-box map of x); else tmA holds the rows
+  const uint8_t* a_rows;    // with row_token on single CTAs: x itself (rows copied by cp.async)
+  int64_t a_ld_bytes;       //   and its row length in bytes
   // EPI_STORE_BF16 with w_topk non-null: routed row r is scaled by its routing weight
   // w_topk[t * w_k + j] before rounding, t = w_row_token[r] and j the slot with
   // w_tok_row[t * w_k + j] == r (the routing weight applied in the down projection's epilogue)
@@ -112,9 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = blockIdx.x / CG, nunits = gridDim.x / CG;  // tile walkers (CTAs or pairs)
 
   // ---- per-block setup: barriers, TMEM, and the m-tile prefix over the groups
+  // single CTAs gather A rows with cp.async: each stage's barrier then also takes one
+  // arrival per producer lane (after its copies are complete and fenced to the async proxy)
+  const bool lsu_gather = CG == 1 && p.row_token != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], lsu_gather ? 33 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -147,10 +152,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
+    // cp.async stages whose arrival is still owed: the npend fills starting at slot pend0
+    // (consecutive), at most kPend of them, so a slot is always refilled after its arrival
+    constexpr int kPend = 2;
+    int pend0 = 0, npend = 0;
+    auto arrive_oldest = [&]() {
+      fence_proxy_async_smem();
+      mbar_arrive(&full[pend0]);
+      pend0 = pend0 + 1 == STAGES ? 0 : pend0 + 1;
+      --npend;
+    };
+    auto drain_pending = [&]() {
+      if (npend > 0) {
+        cp_async_wait<0>();
+        while (npend > 0) arrive_oldest();
+      }
+    };
     for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
       const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
       const bool extra = c.g >= p.G;
       const bool gather = p.row_token != nullptr && !extra;
+      if (lsu_gather && !gather) drain_pending();
       const CUtensorMap* ta = extra ? &tmA2 : &tmA;
       const CUtensorMap* tb0 = extra ? &tmB0x : &tmB0;
       const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
@@ -173,11 +195,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* a_dst = sA + stage * S::kABytes;
         uint8_t* b_dst = sB + stage * S::kBBytes;
         if constexpr (CG == 1) {
-          if (lane == 0) mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&full[stage], gather ? S::kBBytes : S::kStageBytes);
           if (gather) {
-            tma_gather4(ta, a_dst + lane * 4 * BK * 2, &full[stage], kb * BK, tok[0], tok[1], tok[2], tok[3]);
-          } else if (lane == 0) {
-            tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+            // this lane's 4 rows x 8 16-byte pieces, 128-byte swizzle (piece c of row r at
+            // r * 128 + 16 * (c ^ (r % 8))), the layout a TMA box load writes
+            const uint32_t a_base = smem_addr(a_dst);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 4 * lane + i;
+              const uint8_t* src = p.a_rows + (int64_t)tok[i] * p.a_ld_bytes + (int64_t)kb * BK * 2;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) cp_async16(a_base + r * 128 + 16 * (q ^ (r & 7)), src + 16 * q);
+            }
+            cp_async_commit();
+            if (npend == 0) pend0 = stage;
+            ++npend;
+            if (npend > kPend) {  // the oldest stage's copies are done: fence and arrive
+              cp_async_wait<kPend>();
+              arrive_oldest();
+            }
+          } else {
+            if (lane == 0) tma_load_2d(ta, a_dst, &full[stage], kb * BK, a_row);
+            if (lsu_gather) mbar_arrive(&full[stage]);  // the lanes' share of the count
           }
           if (lane == 0) {
             if (kGatedB) {
@@ -202,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
+    drain_pending();
     if (lane == 0) {
       // tail: every stage's last fill has been consumed (so no TMA write or MMA commit
       // is still in flight when the block exits); after an abort, only the own loads
@@ -574,6 +614,8 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.ldc = c.F;
   p.out = h;
   p.row_token = row_token;
+  p.a_rows = static_cast<const uint8_t*>(x);
+  p.a_ld_bytes = (int64_t)c.H * 2;
   p.status = st;
   p.timeout_ns = kTimeoutNs;
   // CTA pairs (256-row tiles) when experts average at least 512 rows; with fewer rows the
