@@ -184,10 +184,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (CG == 2 && !kGatedB) b_row += (int)rank * (BN / 2);
       const CUtensorMap* tb_mine = (CG == 2 && kGatedB && rank == 1) ? tb1 : tb0;
       int tok[4] = {0, 0, 0, 0};
+      // single CTAs (only GEMM1 gathers): the token of row 4 i + lane / 8, i < 32
+      constexpr bool kLsuRows = CG == 1 && EPI == EPI_SWIGLU_BF16;
+      int tokrow[kLsuRows ? 32 : 1];
       if (gather) {  // tokens of this lane's rows; rows past the segment repeat its last row
         const int seg_end = p.offsets[c.g + 1];
+        if constexpr (kLsuRows) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tok[i] = p.row_token[min(a_row + 4 * lane + i, seg_end - 1)];
+          for (int i = 0; i < 32; ++i) tokrow[i] = p.row_token[min(a_row + 4 * i + (lane >> 3), seg_end - 1)];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tok[i] = p.row_token[min(a_row + 4 * lane + i, seg_end - 1)];
+        }
       }
       for (int kb = 0; kb < kblocks; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, abort, p.timeout_ns, p.status));
@@ -196,16 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* b_dst = sB + stage * S::kBBytes;
         if constexpr (CG == 1) {
           if (lane == 0) mbar_arrive_expect_tx(&full[stage], gather ? S::kBBytes : S::kStageBytes);
-          if (gather) {
-            // this lane's 4 rows x 8 16-byte pieces, 128-byte swizzle (piece c of row r at
-            // r * 128 + 16 * (c ^ (r % 8))), the layout a TMA box load writes
+          if (kLsuRows && gather) {
+            // 128 rows x 8 16-byte pieces; 8 consecutive lanes take one row's 128 bytes, so a
+            // warp instruction moves 4 whole rows (4 lines), into the 128-byte swizzle a TMA
+            // box load writes (piece q of row r at r * 128 + 16 * (q ^ (r % 8)))
             const uint32_t a_base = smem_addr(a_dst);
+            const int q = lane & 7, rsub = lane >> 3;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = 4 * lane + i;
-              const uint8_t* src = p.a_rows + (int64_t)tok[i] * p.a_ld_bytes + (int64_t)kb * BK * 2;
-#pragma unroll
-              for (int q = 0; q < 8; ++q) cp_async16(a_base + r * 128 + 16 * (q ^ (r & 7)), src + 16 * q);
+            for (int i = 0; i < 32; ++i) {
+              const int r = 4 * i + rsub;
+              cp_async16(a_base + r * 128 + 16 * (q ^ (r & 7)),
+                         p.a_rows + (int64_t)tokrow[i] * p.a_ld_bytes + (int64_t)kb * BK * 2 + 16 * q);
             }
             cp_async_commit();
             if (npend == 0) pend0 = stage;
