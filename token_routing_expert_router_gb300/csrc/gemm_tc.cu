@@ -32,7 +32,16 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes
 // themselves, for the backward's recomputation of the activation. EPI_SWIGLU_GU: the
 // forward's SwiGLU epilogue that also keeps g and u (out2), so that the backward recomputes
 // only the activation and not this GEMM.
-enum Epi { EPI_SWIGLU_BF16 = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32_BIAS = 2, EPI_STORE_GU = 3, EPI_SWIGLU_GU = 4 };
+// EPI_SWIGLU_GATHER: EPI_SWIGLU_BF16 for single CTAs whose A rows are gathered by token with
+// cp.async (its own instantiation, so the plain GEMM1 does not carry the gather's registers).
+enum Epi {
+  EPI_SWIGLU_BF16 = 0,
+  EPI_STORE_BF16 = 1,
+  EPI_STORE_F32_BIAS = 2,
+  EPI_STORE_GU = 3,
+  EPI_SWIGLU_GU = 4,
+  EPI_SWIGLU_GATHER = 5
+};
 
 struct TcParams {
   const int32_t* offsets;   // [G+1] routed segment starts (device); may be null when G = 0
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- per-block setup: barriers, TMEM, and the m-tile prefix over the groups
   // single CTAs gather A rows with cp.async: each stage's barrier then also takes one
   // arrival per producer lane (after its copies are complete and fenced to the async proxy)
-  const bool lsu_gather = CG == 1 && p.row_token != nullptr;
+  const bool lsu_gather = CG == 1 && EPI == EPI_SWIGLU_GATHER && p.row_token != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], lsu_gather ? 33 : 1);
@@ -133,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU) tma_prefetch_desc(&tmB1);
+    if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU || EPI == EPI_SWIGLU_GATHER)
+      tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_cg<CG>(tmem_slot, S::kTmemCols);
   if (warp == 2) build_tile_prefix(p.offsets, p.G, ngroups, p.T_extra, TM, lane, seg_rows, mt_prefix);
@@ -178,14 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tb1 = extra ? &tmB1x : &tmB1;
       const int a_row = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * BM;
       constexpr bool kGatedB =
-          EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU;  // B = gate + up rows
+          EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_GU || EPI == EPI_SWIGLU_GU ||
+          EPI == EPI_SWIGLU_GATHER;  // B = gate + up rows
       const int b_tile_rows = kGatedB ? BN / 2 : BN;  // rows of B per N tile
       int b_row = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows;
       if (CG == 2 && !kGatedB) b_row += (int)rank * (BN / 2);
       const CUtensorMap* tb_mine = (CG == 2 && kGatedB && rank == 1) ? tb1 : tb0;
       int tok[4] = {0, 0, 0, 0};
       // single CTAs (only GEMM1 gathers): the token of row 4 i + lane / 8, i < 32
-      constexpr bool kLsuRows = CG == 1 && EPI == EPI_SWIGLU_BF16;
+      constexpr bool kLsuRows = CG == 1 && EPI == EPI_SWIGLU_GATHER;
       int tokrow[kLsuRows ? 32 : 1];
       if (gather) {  // tokens of this lane's rows; rows past the segment repeat its last row
         const int seg_end = p.offsets[c.g + 1];
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int warp_live = min(c.rows - (row_in_tile - lane), m64 ? 16 : 32);
       const int64_t warp_row0 = out_row - lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_GU) {
+      if (EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_GU || EPI == EPI_SWIGLU_GATHER) {
         // cols [0, BN/2) gate, [BN/2, BN) up -> BN/2 columns of h
         uint8_t* out = reinterpret_cast<uint8_t*>(p.out) + (warp_row0 * p.ldc + c.nb * (BN / 2)) * 2;
         uint8_t* out2 = EPI == EPI_SWIGLU_GU
@@ -640,8 +651,12 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
              : launch<256, EPI_SWIGLU_GU, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
     p.out2 = nullptr;
   } else {
-    e = pair ? launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
-             : launch<256, EPI_SWIGLU_BF16, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+    if (pair)
+      e = launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+    else if (row_token)  // single CTAs gather their rows with cp.async
+      e = launch<256, EPI_SWIGLU_GATHER, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
+    else
+      e = launch<256, EPI_SWIGLU_BF16, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
   }
   if (e != cudaSuccess) return e;
   // ---- GEMM2: yd = h Wd^T (the shared expert's h rows follow the routed ones)
