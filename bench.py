@@ -84,9 +84,9 @@ def quant_kind(w):
 
 # DRAM bytes (read + write) per forward of the two grouped-GEMM launches, from one ncu
 # capture of the current kernels (profiles/tc_gemm_bf16_gateup_mixtral_bf16.md): the
-# T=2048, E=4 case moved 1.958 GB; the T=4096, E=8 layer has twice its weights and twice its
-# rows, so 3.916 GB. Other workloads: not captured at the current kernels (null).
-GEMM_TRAFFIC = {"mixtral_bf16": (3.916e9, "ncu T=2048 E=4 capture x2 (weights and rows both double)")}
+# T=2048, E=4 case moved 1.973 GB; the T=4096, E=8 layer has twice its weights and twice its
+# rows, so 3.946 GB. Other workloads: not captured at the current kernels (null).
+GEMM_TRAFFIC = {"mixtral_bf16": (3.946e9, "ncu T=2048 E=4 capture x2 (weights and rows both double)")}
 
 
 def gemm_traffic(w):
