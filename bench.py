@@ -6,6 +6,12 @@ inputs and weights resident in HBM. L2 is flushed (a 512 MB write) before every 
 and each step is timed with CUDA events on the launching stream. Per-stage times come from
 a second loop over the staged entry points, timed the same way.
 
+The headline is the Mixtral-shaped layer (T=4096, H=4096, 8 experts top-2, F=14336). The
+default run then measures the other four layer shapes the same way (tiny fp32,
+DeepSeek-V3-shaped bf16, imbalanced routing, FP8 dispatch) and reports them under
+"configs", each with its throughput, its grouped-GEMM and dispatch/combine rooflines and
+its own CPU-oracle baseline (--headline-only skips them).
+
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
 Multi-GPU: independent token-sharded replicas (no collective in the data path; the path has
@@ -82,11 +88,11 @@ def quant_kind(w):
     return {synth.E4M3: 1, synth.MXE4M3: 2}.get(w["xfer_dtype"], 0)
 
 
-# DRAM bytes (read + write) per forward of the two grouped-GEMM launches, from one ncu
-# capture of the current kernels (profiles/tc_gemm_bf16_gateup_mixtral_bf16.md): the
-# T=2048, E=4 case moved 1.973 GB; the T=4096, E=8 layer has twice its weights and twice its
-# rows, so 3.946 GB. Other workloads: not captured at the current kernels (null).
-GEMM_TRAFFIC = {"mixtral_bf16": (3.946e9, "ncu T=2048 E=4 capture x2 (weights and rows both double)")}
+# DRAM bytes (read + write) per forward of the two grouped-GEMM launches, from one-pass ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum) of the current GEMM kernels on the
+# full-size workloads. A workload without an entry has no capture of the current kernels and
+# reports null.
+GEMM_TRAFFIC = {}
 
 
 def gemm_traffic(w):
@@ -164,23 +170,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def run_gpu(args, w):
+class GpuContext:
+    """The rank's device, peaks, stream and L2-flush buffer, shared by every workload."""
+
+    def __init__(self):
+        import torch
+        self.world, self.rank, local = rank_env()
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+            self.dist = dist
+        else:
+            torch.cuda.set_device(0)
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.peaks, self.peak_kind = load_peaks()
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=self.dev)
+        self.stream = torch.cuda.current_stream()
+
+    def barrier(self):
+        import torch
+        torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+        torch.cuda.synchronize()
+
+
+def build_layer(ctx, w):
+    """This rank's token shard (seed = rank) and the replicated weights (seed 0) of workload
+    w, drawn on the device; e4m3 / MX weights quantised once, outside any timing."""
     import torch
     import token_routing_expert_router_gb300 as moe
-
-    world, rank, local = rank_env()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    moe.build()
-    peaks, peak_kind = load_peaks()
-
-    # ---- inputs: this rank's token shard (seed = rank) and the replicated weights (seed 0)
+    dev = ctx.dev
     dt = torch.bfloat16 if w["act_dtype"] == synth.BF16 else torch.float32
     T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
     s = w["w_std"]
@@ -189,22 +211,24 @@ def run_gpu(args, w):
         t = torch.empty(shape, dtype=dtype, device=dev)
         return synth.device_normal(t, seed, tid, std)
 
-    x = gen((T, H), synth.X, 1.0, seed=shard_seed(rank))
+    x = gen((T, H), synth.X, 1.0, seed=shard_seed(ctx.rank))
     wts = {"w_router": gen((E, H), synth.W_ROUTER, s), "w_gate": gen((E, F, H), synth.W_GATE, s),
            "w_up": gen((E, F, H), synth.W_UP, s), "w_down": gen((E, H, F), synth.W_DOWN, s),
            "router_bias": torch.from_numpy(synth.zipf_bias(0, E)).to(dev) if w["zipf"] else None}
     if w["n_shared"]:
-        wts["ws_gate"] = gen((F, H), synth.WS_GATE, s)
-        wts["ws_up"] = gen((F, H), synth.WS_UP, s)
-        wts["ws_down"] = gen((H, F), synth.WS_DOWN, s)
-    if quant_kind(w):
+        Fs = w["F_shared"]
+        wts["ws_gate"] = gen((Fs, H), synth.WS_GATE, s)
+        wts["ws_up"] = gen((Fs, H), synth.WS_UP, s)
+        wts["ws_down"] = gen((H, Fs), synth.WS_DOWN, s)
+    qk = quant_kind(w)
+    if qk:
         pairs = [("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")]
         if w["n_shared"]:
             pairs += [("ws_gate", "ss_gate"), ("ws_up", "ss_up"), ("ws_down", "ss_down")]
         for wn, sn in pairs:
             src = wts[wn].reshape(-1, wts[wn].shape[-1])
             q = torch.empty(src.shape, dtype=torch.uint8, device=dev)
-            if quant_kind(w) == 2:
+            if qk == 2:
                 sc = torch.empty((src.shape[0] // 128) * (src.shape[1] // 128) * 512, dtype=torch.uint8, device=dev)
                 moe.moe_quantize_mx(src, q, sc)
             else:
@@ -219,45 +243,43 @@ def run_gpu(args, w):
     ws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device=dev)
     moe.moe_workspace_init(ws)
     y = torch.empty((T, H), dtype=dt, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
+    return {"w": w, "cfg": cfg, "x": x, "wts": wts, "ws": ws, "y": y, "dt": dt, "gen": gen}
 
-    def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
 
-    # ---- whole-layer steps (moe_forward issues no host sync, so one step is a CUDA graph)
-    for _ in range(args.warmup):
+def time_forward(ctx, L, steps, warmup, use_graph=True):
+    """W warm-up forwards, then K forwards (CUDA-graph replays of moe_forward), each after an
+    L2-flushing write and bracketed by CUDA events on the launching stream, with nvidia-smi
+    sampling the clocks meanwhile; then the same steps with L2 left warm (context)."""
+    import torch
+    import token_routing_expert_router_gb300 as moe
+    cfg, x, wts, y, ws = L["cfg"], L["x"], L["wts"], L["y"], L["ws"]
+    stream = ctx.stream
+    for _ in range(warmup):
         moe.moe_forward(cfg, x, wts, y, ws)
     st = moe.moe_read_status(ws)
     assert st == moe.MOE_OK, moe.moe_status_string(st)
     graph = None
-    if not args.no_graph:
+    if use_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             moe.moe_forward(cfg, x, wts, y, ws)
         graph.replay()
     step = graph.replay if graph is not None else (lambda: moe.moe_forward(cfg, x, wts, y, ws))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ctx.barrier()
     with ClockSampler(torch.cuda.current_device()) as clocks:
         t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(float(i))  # evict the previous step's lines from L2
+        for i in range(steps):
+            ctx.flush.fill_(float(i))  # evict the previous step's lines from L2
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
-        barrier()
+        ctx.barrier()
         t_wall = time.perf_counter() - t_wall
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    total_ms = max_over_ranks(sum(step_ms), ctx.dist, ctx.dev)
     assert moe.moe_read_status(ws) == moe.MOE_OK
-    ms_per_step = total_ms / args.steps
-    value = job_tokens_per_s(world, T, args.steps, total_ms)
-    # the same steps with the L2 left warm between them: context only (labelled as such)
-    n_warm = max(3, min(args.steps, 20))
+    n_warm = max(3, min(steps, 20))
     ev_w = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_warm)]
     step()
     for i in range(n_warm):
@@ -265,32 +287,49 @@ def run_gpu(args, w):
         step()
         ev_w[i][1].record(stream)
     torch.cuda.synchronize()
-    warm_step_ms = statistics.median(a.elapsed_time(bb) for a, bb in ev_w)
+    warm_ms = statistics.median(a.elapsed_time(bb) for a, bb in ev_w)
+    del graph
+    return {"total_ms": total_ms, "ms_per_step": total_ms / steps, "wall_s": t_wall, "clocks": clocks.summary(),
+            "warm_ms": warm_ms, "used_graph": use_graph}
 
-    # ---- per-stage times through the staged entry points (same kernels)
+
+def stage_buffers(ctx, L):
+    import torch
+    import token_routing_expert_router_gb300 as moe
+    w, cfg, dev, dt = L["w"], L["cfg"], ctx.dev, L["dt"]
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
     R = T * k
     rows = R + (T if w["n_shared"] else 0)
     qk = quant_kind(w)
-    fp8 = qk != 0
-    xdt = torch.uint8 if fp8 else dt
+    xdt = torch.uint8 if qk else dt
 
     def act_scales(K):
         if qk == 2:
             return torch.empty(moe.moe_mx_scale_bytes(cfg, K), dtype=torch.uint8, device=dev)
         return torch.empty((K // 128, rows), dtype=torch.float32, device=dev) if qk == 1 else None
 
-    b = {"logits": torch.empty((T, E), dtype=torch.float32, device=dev),
-         "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
-         "w": torch.empty((T, k), dtype=torch.float32, device=dev),
-         "counts": torch.empty(E, dtype=torch.int32, device=dev),
-         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
-         "row_token": torch.empty(R, dtype=torch.int32, device=dev),
-         "tok_row": torch.empty((T, k), dtype=torch.int32, device=dev),
-         "xd": torch.empty((rows, H), dtype=xdt, device=dev),
-         "xd_scale": act_scales(H),
-         "h": torch.empty((rows, F), dtype=xdt, device=dev),
-         "h_scale": act_scales(F),
-         "yd": torch.empty((rows, H), dtype=dt, device=dev)}
+    return {"logits": torch.empty((T, E), dtype=torch.float32, device=dev),
+            "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+            "w": torch.empty((T, k), dtype=torch.float32, device=dev),
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "row_token": torch.empty(R, dtype=torch.int32, device=dev),
+            "tok_row": torch.empty((T, k), dtype=torch.int32, device=dev),
+            "xd": torch.empty((rows, H), dtype=xdt, device=dev),
+            "xd_scale": act_scales(H),
+            "h": torch.empty((rows, F), dtype=xdt, device=dev),
+            "h_scale": act_scales(F),
+            "yd": torch.empty((rows, H), dtype=dt, device=dev)}
+
+
+def time_stages(ctx, L, b, reps, gather=True):
+    """Each staged entry point (the same kernels moe_forward launches) as one call after an
+    L2 flush, median of ``reps``; dispatch and combine again with L2 warm (context)."""
+    import torch
+    import token_routing_expert_router_gb300 as moe
+    w, cfg, x, wts, ws, y = L["w"], L["cfg"], L["x"], L["wts"], L["ws"], L["y"]
+    qk = quant_kind(w)
+    stream = ctx.stream
     stages = {
         "router_logits": lambda: moe.moe_router_logits(cfg, x, wts["w_router"], wts["router_bias"], b["logits"], ws),
         "route": lambda: moe.moe_route(cfg, b["logits"], b["idx"], b["w"], b["counts"], b["offsets"],
@@ -302,7 +341,7 @@ def run_gpu(args, w):
                                                    b["h_scale"], b["yd"], ws),
         "combine": lambda: moe.moe_combine(cfg, b["yd"], b["tok_row"], b["w"], y),
     }
-    if w["act_dtype"] == synth.BF16 and not fp8:  # the fused-permutation alternative
+    if gather and w["act_dtype"] == synth.BF16 and not qk:  # the fused-permutation alternative
         # rows gathered by token in GEMM1, routing weights applied in GEMM2's epilogue
         stages["grouped_mlp_gather"] = lambda: moe.moe_grouped_mlp_gather(cfg, x, b["row_token"], b["offsets"],
                                                                           wts, b["h"], b["yd"], ws,
@@ -310,20 +349,19 @@ def run_gpu(args, w):
     for _ in range(2):
         for f in stages.values():
             f()
-    reps = max(3, min(args.steps, 10))
     times = {n: [] for n in stages}
     for _ in range(reps):
         for n, f in stages.items():
-            flush.fill_(1.0)
+            ctx.flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             f()
             e1.record(stream)
             times[n].append((e0, e1))
     torch.cuda.synchronize()
+    assert moe.moe_read_status(ws) == moe.MOE_OK
     stage_ms = {n: statistics.median(a.elapsed_time(bb) for a, bb in v) for n, v in times.items()}
-    alg = algorithmic(w)
-    warm_stage = {}
+    warm = {}
     for n in ("dispatch", "combine"):  # again without the flush: the call's own inputs warm in L2
         f = stages[n]
         f()
@@ -335,35 +373,45 @@ def run_gpu(args, w):
             e1.record(stream)
             pairs.append((e0, e1))
         torch.cuda.synchronize()
-        warm_stage[n] = statistics.median(a.elapsed_time(bb) for a, bb in pairs)
+        warm[n] = statistics.median(a.elapsed_time(bb) for a, bb in pairs)
+    return stage_ms, warm
 
-    # ---- dispatch and combine back to back: one event pair around K launches, each on its
-    # own copy of the inputs and outputs (together well beyond L2, flushed first), so the
-    # per-launch time leaves out the launch and completion overhead that a single timed
-    # ~15 us launch carries, without any launch finding the previous one's data in L2
-    def back_to_back(make_buffers, call, nbytes):
-        K = max(3, min(8, -(-600_000_000 // max(1, nbytes))))
-        bufs = [make_buffers() for _ in range(K)]
-        for bb in bufs:  # warm
+
+def back_to_back(ctx, make_buffers, call, nbytes):
+    """Per-launch time of K launches replayed back to back from one CUDA graph, each on its
+    own copy of the inputs and outputs (together well beyond L2, flushed first), so the
+    per-launch time leaves out the launch and completion overhead that a single timed
+    ~15 us launch carries, without any launch finding the previous one's data in L2."""
+    import torch
+    K = max(3, min(8, -(-600_000_000 // max(1, nbytes))))
+    bufs = [make_buffers() for _ in range(K)]
+    for bb in bufs:  # warm
+        call(bb)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()  # the K launches replay from one graph: no host pacing
+    with torch.cuda.graph(g):
+        for bb in bufs:
             call(bb)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(3):
+        ctx.flush.fill_(3.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        g.replay()
+        e1.record(ctx.stream)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()  # the K launches replay from one graph: no host pacing
-        with torch.cuda.graph(g):
-            for bb in bufs:
-                call(bb)
-        torch.cuda.synchronize()
-        ms = []
-        for _ in range(3):
-            flush.fill_(3.0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ms.append(e0.elapsed_time(e1) / K)
-        del g, bufs
-        torch.cuda.empty_cache()
-        return statistics.median(ms), K
+        ms.append(e0.elapsed_time(e1) / K)
+    del g, bufs
+    torch.cuda.empty_cache()
+    return statistics.median(ms), K
+
+
+def time_dispatch_combine(ctx, L, b, alg):
+    import torch
+    import token_routing_expert_router_gb300 as moe
+    cfg, x, y = L["cfg"], L["x"], L["y"]
+    qk = quant_kind(L["w"])
 
     def dispatch_bufs():
         return {"x": x.clone(), "xd": torch.empty_like(b["xd"]),
@@ -378,9 +426,114 @@ def run_gpu(args, w):
     def combine_bufs():
         return {"yd": b["yd"].clone(), "y": torch.empty_like(y)}
 
-    b2b_disp, k_disp = back_to_back(dispatch_bufs, dispatch_call, alg["dispatch_bytes"])
-    b2b_comb, k_comb = back_to_back(combine_bufs, lambda bb: moe.moe_combine(cfg, bb["yd"], b["tok_row"], b["w"],
-                                                                             bb["y"]), alg["combine_bytes"])
+    disp, k_disp = back_to_back(ctx, dispatch_bufs, dispatch_call, alg["dispatch_bytes"])
+    comb, k_comb = back_to_back(ctx, combine_bufs, lambda bb: moe.moe_combine(cfg, bb["yd"], b["tok_row"], b["w"],
+                                                                              bb["y"]), alg["combine_bytes"])
+    return disp, k_disp, comb, k_comb
+
+
+def tensor_peak(ctx, w, kind="bf16_tflops"):
+    """The measured bf16 peak of the given kind (burst for calls timed alone), times the
+    part's nominal fp8:bf16 dense ratio of 2 for the e4m3 GEMMs."""
+    p = ctx.peaks.get(kind, ctx.peaks["bf16_tflops"])
+    return p * (2.0 if quant_kind(w) else 1.0)
+
+
+def gemm_roofline(ctx, w, gemm_ms, alg):
+    achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+    peak = tensor_peak(ctx, w)
+    sus = tensor_peak(ctx, w, "bf16_tflops_sustained")
+    return {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "peak_kind": f"{ctx.peak_kind} bf16 burst" + (" x2 (nominal fp8:bf16 dense ratio)" if quant_kind(w) else "")
+                         + ": the GEMM pair is timed as single calls after an L2 flush",
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+            "frac_of_sustained": round(achieved / sus, 3),
+            "timing": "CUDA events around moe_grouped_mlp on the launching stream, median of the stage loop",
+            **gemm_traffic(w)}
+
+
+def hbm_roofline(ctx, alg, disp_ms, comb_ms):
+    d = alg["dispatch_bytes"] / (disp_ms / 1e3) / 1e9
+    c = alg["combine_bytes"] / (comb_ms / 1e3) / 1e9
+    return {"dispatch_gbs": round(d, 1), "combine_gbs": round(c, 1),
+            "dispatch_frac": round(d / ctx.peaks["hbm_gbs"], 3), "combine_frac": round(c / ctx.peaks["hbm_gbs"], 3),
+            "peak_gbs": ctx.peaks["hbm_gbs"], "peak_kind": ctx.peak_kind + " copy (read + write)"}
+
+
+def config_of(w, world):
+    """The workload's config object, the same for both arms."""
+    return {"workload": describe(w), "tokens_per_gpu": w["T"], "parallelism": f"replicas x{world} (token-sharded)",
+            "weights_bytes": algorithmic(w)["weight_bytes"]}
+
+
+def dtype_name(w):
+    return {1: "e4m3+bf16", 2: "mxfp8(e4m3,ue8m0)+bf16"}.get(quant_kind(w), "bf16" if w["act_dtype"] == synth.BF16 else "f32")
+
+
+# Oracle tokens per workload for the CPU baseline: about 2-20 s of fp64 work each on a
+# 16-core host (the DeepSeek-V3 shapes touch most of their experts' weights even for a few
+# tokens, and drawing those weights on the host is not timed but takes time).
+CPU_TOKENS = {"tiny_fp32": 256, "mixtral_bf16": 64, "dsv3_bf16": 8, "imbalanced_bf16": 64, "dsv3_fp8": 8,
+              "dsv3_mxfp8": 8}
+OTHER_CONFIGS = ["tiny_fp32", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8"]
+
+
+def measure_config(ctx, args, w):
+    """One workload's forward, stages, GEMM roofline and dispatch/combine rooflines (the
+    entries of the "configs" object)."""
+    import torch
+    L = build_layer(ctx, w)
+    steps = max(3, min(args.steps, 20))
+    fw = time_forward(ctx, L, steps, args.warmup, use_graph=not args.no_graph)
+    b = stage_buffers(ctx, L)
+    stage_ms, warm = time_stages(ctx, L, b, reps=max(3, min(args.steps, 10)), gather=False)
+    alg = algorithmic(w)
+    disp, _, comb, _ = time_dispatch_combine(ctx, L, b, alg)
+    counts = b["counts"].cpu().numpy()
+    T = w["T"]
+    out = {"workload": describe(w), "dtype": dtype_name(w),
+           "value": round(job_tokens_per_s(ctx.world, T, steps, fw["total_ms"]), 1), "unit": "tokens/s",
+           "ms_per_step": round(fw["ms_per_step"], 4), "steps": steps,
+           "stages_ms": {n: round(v, 4) for n, v in stage_ms.items()},
+           "grouped_gemm": gemm_roofline(ctx, w, stage_ms["grouped_mlp"], alg),
+           "dispatch_combine": dict(hbm_roofline(ctx, alg, disp, comb), dispatch_ms=round(disp, 4),
+                                    combine_ms=round(comb, 4)),
+           "expert_rows": {"min": int(counts.min()), "max": int(counts.max()), "empty": int((counts == 0).sum())},
+           "clocks": fw["clocks"]}
+    if w["T"] <= 512:
+        out["note"] = "launch-latency-bound layer: the roofline fractions carry little meaning"
+    del L, b
+    torch.cuda.empty_cache()
+    if ctx.rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, min(CPU_TOKENS.get(w["name"], args.cpu_tokens), T))
+    return out
+
+
+def run_gpu(args, w):
+    import torch
+    import token_routing_expert_router_gb300 as moe
+
+    ctx = GpuContext()
+    moe.build()
+    L = build_layer(ctx, w)
+    cfg, x, wts, ws, y, dt, gen = L["cfg"], L["x"], L["wts"], L["ws"], L["y"], L["dt"], L["gen"]
+    dev, stream, flush, dist = ctx.dev, ctx.stream, ctx.flush, ctx.dist
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    world, rank = ctx.world, ctx.rank
+
+    # ---- whole-layer steps (moe_forward issues no host sync, so one step is a CUDA graph)
+    fw = time_forward(ctx, L, args.steps, args.warmup, use_graph=not args.no_graph)
+    ms_per_step = fw["ms_per_step"]
+    value = job_tokens_per_s(world, T, args.steps, fw["total_ms"])
+
+    # ---- per-stage times through the staged entry points (same kernels)
+    qk = quant_kind(w)
+    fp8 = qk != 0
+    b = stage_buffers(ctx, L)
+    stage_ms, warm_stage = time_stages(ctx, L, b, reps=max(3, min(args.steps, 10)))
+    alg = algorithmic(w)
+    b2b_disp, k_disp, b2b_comb, k_comb = time_dispatch_combine(ctx, L, b, alg)
 
     # ---- end to end: pinned host x in, host y out, through moe_forward_host. Two streams,
     # each with its own workspace, device staging and pinned buffers, take the steps in turn,
@@ -401,7 +554,7 @@ def run_gpu(args, w):
     for ln in lanes:  # warm both lanes
         moe.moe_forward_host(cfg, ln["xh"], wts, ln["yh"], ln["xdev"], ln["ydev"], ln["ws"], stream=ln["s"])
     torch.cuda.synchronize()
-    barrier()
+    ctx.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for ln in lanes:
@@ -412,11 +565,10 @@ def run_gpu(args, w):
     for ln in lanes:
         stream.wait_stream(ln["s"])
     e1.record(stream)
-    barrier()
+    ctx.barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     for ln in lanes:
         assert moe.moe_read_status(ln["ws"]) == moe.MOE_OK
-    del lanes
     if saved_affinity is not None:
         os.sched_setaffinity(0, saved_affinity)
 
@@ -424,16 +576,23 @@ def run_gpu(args, w):
     bwd = None
     if not args.no_backward and w["act_dtype"] == synth.BF16 and not fp8:
         bwd = time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt)
+    counts = b["counts"].cpu().numpy()
+    h2d_bytes, d2h_bytes = int(x.numel() * x.element_size()), int(y.numel() * y.element_size())
+    del L, b, x, y, wts, ws, lanes
+    torch.cuda.empty_cache()
+
+    # ---- the other layer shapes, each measured the same way (forward only)
+    others = {}
+    if not args.headline_only and not (args.tokens or args.experts):
+        for name in OTHER_CONFIGS:
+            if name != w["name"]:
+                others[name] = measure_config(ctx, args, synth.WORKLOADS[name])
 
     if rank != 0:
         dist.destroy_process_group()
         return None
-    gemm_ms = stage_ms["grouped_mlp"]
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    if fp8:
-        tensor_peak *= 2.0  # nominal fp8:bf16 dense ratio of the part
-    achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
-    counts = b["counts"].cpu().numpy()
+    roof = gemm_roofline(ctx, w, stage_ms["grouped_mlp"], alg)
+    hbm = hbm_roofline(ctx, alg, b2b_disp, b2b_comb)
     line = {
         "metric": "MoE-layer fwd tokens/s",
         "value": round(value, 1),
@@ -445,21 +604,20 @@ def run_gpu(args, w):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {1: "e4m3+bf16", 2: "mxfp8(e4m3,ue8m0)+bf16"}.get(qk, "bf16" if w["act_dtype"] == synth.BF16 else "f32"),
+        "dtype": dtype_name(w),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset or trained weights)",
-        "config": {"workload": describe(w), "tokens_per_gpu": T, "parallelism": f"replicas x{world} (token-sharded)",
-                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
-                   "launch": "CUDA graph replay of moe_forward" if graph is not None else "moe_forward calls",
-                   "weights_bytes": alg["weight_bytes"]},
+        "config": config_of(w, world),
+        "timing": {"l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "launch": "CUDA graph replay of moe_forward" if fw["used_graph"] else "moe_forward calls"},
         "stages_ms": {n: round(v, 4) for n, v in stage_ms.items()},
         "warm_l2": {"note": "context only: L2 not flushed between calls, so inputs and weights may be served "
                             "from L2; the flushed numbers are the results",
-                    "ms_per_step": round(warm_step_ms, 4), "tokens_per_s": round(T * world / (warm_step_ms / 1e3), 1),
+                    "ms_per_step": round(fw["warm_ms"], 4), "tokens_per_s": round(T * world / (fw["warm_ms"] / 1e3), 1),
                     "dispatch_ms": round(warm_stage["dispatch"], 4), "combine_ms": round(warm_stage["combine"], 4),
                     "dispatch_gbs": round(alg["dispatch_bytes"] / (warm_stage["dispatch"] / 1e3) / 1e9, 1),
                     "combine_gbs": round(alg["combine_bytes"] / (warm_stage["combine"] / 1e3) / 1e9, 1)},
-        "dispatch_gbs": round(alg["dispatch_bytes"] / (b2b_disp / 1e3) / 1e9, 1),
-        "combine_gbs": round(alg["combine_bytes"] / (b2b_comb / 1e3) / 1e9, 1),
+        "dispatch_gbs": hbm["dispatch_gbs"],
+        "combine_gbs": hbm["combine_gbs"],
         "dispatch_combine_timing": {
             "method": "per launch, from K launches replayed back to back from one CUDA graph, each "
                       "on its own copy of its buffers (L2 flushed first, K copies well beyond L2)",
@@ -467,30 +625,26 @@ def run_gpu(args, w):
             "combine_ms": round(b2b_comb, 4), "combine_K": k_comb,
             "dispatch_gbs_single_launch": round(alg["dispatch_bytes"] / (stage_ms["dispatch"] / 1e3) / 1e9, 1),
             "combine_gbs_single_launch": round(alg["combine_bytes"] / (stage_ms["combine"] / 1e3) / 1e9, 1)},
-        "grouped_gemm_tflops": round(achieved, 1),
-        "grouped_gemm_frac_of_peak": round(achieved / tensor_peak, 3),
-        "roofline": {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
-                     "bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
-                     "peak_kind": f"{peak_kind} bf16 sustained" + (" x2 (fp8 nominal ratio)" if fp8 else ""),
-                     "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 3),
-                     **gemm_traffic(w)},
-        "hbm_roofline": {"dispatch_frac": round(alg["dispatch_bytes"] / (b2b_disp / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
-                         "combine_frac": round(alg["combine_bytes"] / (b2b_comb / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
-                         "peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
+        "grouped_gemm_tflops": roof["achieved"],
+        "grouped_gemm_frac_of_peak": roof["frac"],
+        "roofline": roof,
+        "hbm_roofline": hbm,
         "expert_rows": {"min": int(counts.min()), "max": int(counts.max()), "empty": int((counts == 0).sum())},
         "e2e": {"value": round(job_tokens_per_s(world, T, 1, e2e_ms), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
-                "d2h_bytes_per_step": int(y.numel() * y.element_size()),
+                "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes,
                 "call": "moe_forward_host (pinned host x in, host y out), steps alternating on two streams",
                 "host_cpus": local_cpus or "not restricted",
                 "l2": "not flushed (each step's x arrives by its own host-to-device copy)"},
         "gpu_launches": args.steps * launches_per_forward(w),
         **({"backward": bwd} if bwd is not None else {}),
-        "clocks": clocks.summary(),
-        "wall_s_timed_region": round(t_wall, 3),
+        "clocks": fw["clocks"],
+        "wall_s_timed_region": round(fw["wall_s"], 3),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens)
+    if others:
+        line["configs"] = others
     if dist is not None:
         dist.destroy_process_group()
     return line
@@ -583,7 +737,7 @@ def time_backward(args, w, cfg, x, wts, ws, b, flush, stream, gen, dev, dt):
     ms = {n: statistics.median(a.elapsed_time(bb) for a, bb in v) for n, v in times.items()}
     flops = 2.0 * synth.gemm_flops(w)  # dgrad + wgrad, each the forward GEMMs' flops
     recompute = synth.gemm_flops(w) * 2.0 / 3.0  # the gate/up GEMM run again
-    peak = load_peaks()[0].get("bf16_tflops_sustained", load_peaks()[0]["bf16_tflops"])
+    peak = load_peaks()[0]["bf16_tflops"]  # measured burst: each call is timed alone
     tf = flops / (ms["grouped_mlp_backward"] / 1e3) / 1e12
     return {"metric": "MoE-layer bwd tokens/s", "value": round(T / (ms["backward"] / 1e3), 1), "unit": "tokens/s",
             "ms_per_step": round(ms["backward"], 4), "stages_ms": {n: round(v, 4) for n, v in ms.items() if n != "backward"},
@@ -711,7 +865,7 @@ def run_reference(args, w):
             "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_all / args.steps, 1), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(w)}, "cpu_baseline": cb,
+            "config": config_of(w, world), "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -726,6 +880,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct moe_forward calls")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (bf16 layers)")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other layer shapes' entries")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     args = ap.parse_args()

@@ -236,12 +236,14 @@ moe_status_t moe_grouped_mlp(const moe_config_t* cfg, const void* xd, const void
 /* S3 + S4 + S5 fused — the grouped expert MLP with the dispatch folded into GEMM1's operand
  * loads: the memory-efficient permutation of the Megatron-Core summary (section 2.2: the
  * computation is reorganised so that no redundant intermediate tensor is materialised).
- * Routed A rows are gathered from x by token (row r reads x[row_token[r]]) four rows per
- * TMA instruction, so no dispatched copy xd exists; the shared expert reads x directly.
- * Same outputs as moe_dispatch + moe_grouped_mlp (bit-identical). bf16 layers on the
- * tensor-core path only (else MOE_ERR_UNSUPPORTED). x [T,H], row_token [T*k], offsets
- * [E+1], h [R(+T), F], yd [R(+T), H]. moe_forward keeps the separate dispatch: the four-row
- * gathers are slower on GB300 than the dispatch pass they replace.
+ * Routed A rows are gathered from x by token (row r reads x[row_token[r]]), so no
+ * dispatched copy xd exists; the shared expert reads x directly. 256-row CTA-pair tiles
+ * gather four rows per TMA instruction; 128-row single-CTA tiles copy their rows with
+ * cp.async, eight lanes per row. Same outputs as moe_dispatch + moe_grouped_mlp
+ * (bit-identical). bf16 layers on the tensor-core path only (else MOE_ERR_UNSUPPORTED).
+ * x [T,H], row_token [T*k], offsets [E+1], h [R(+T), F], yd [R(+T), H]. moe_forward keeps
+ * the separate dispatch: the gathers are slower on GB300 than the dispatch pass they
+ * replace.
  * The other half of the fused permutation is optional: with tok_row [T,k] and topk_w [T,k]
  * (both given, or both NULL; else MOE_ERR_INVALID_ARG) the down projection's epilogue
  * scales each routed row by its routing weight before rounding,
@@ -417,12 +419,15 @@ moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, u
  * this is a library convenience. It computes exactly what moe_route computes (same kernels,
  * same bits) but takes no workspace: the routing scan's scratch lives in a fixed array
  * inside the library (1 MiB of device memory per GPU that loads the library, held until
- * the process exits), so callers that are handed only their inputs and outputs, or that
- * must not allocate while a CUDA graph is being captured, can still route.
+ * the process exits). It is meant for callers that are handed only their inputs and
+ * outputs (a plugin inside a host framework), that run on a fixed memory budget reserved
+ * up front, or that run where allocating is not allowed (an allocator's own callback).
  *  - Limit: ceil(T / 128) * E <= 262144 (e.g. T = 131072 tokens with E = 256); larger
  *    problems return MOE_ERR_UNSUPPORTED before anything is launched.
- *  - The first call on each device looks up the array's device address (no allocation);
- *    make that first call before any stream capture.
+ *  - A call looks up the array's device address (no allocation) when the device's current
+ *    context is not the one it last looked it up in: the first call on each device, and the
+ *    first call after the device was reset. Make such a first call before any stream
+ *    capture.
  *  - Every call on a device shares the one array: calls whose kernels overlap on the GPU
  *    (two streams, two host threads) race, and the caller must serialise them.
  *  - device_status: optional caller-owned device int32[2] (code, detail) that receives

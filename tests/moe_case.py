@@ -215,30 +215,45 @@ def np_of(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
-def routing_ambiguity(w: dict, l_oracle: np.ndarray, delta: float) -> np.ndarray:
-    """Tokens whose top-k selection is not decided by fp32 logits known only to within
-    ``delta`` (the measured |GPU - oracle| logit difference bound): the k-th and (k+1)-th
-    allowed keys are within 2*delta, or (group-limited) the topk_groups-th and next group
-    scores are within delta/2 (sigmoid slope <= 1/4, two scores per group) + 1e-6."""
-    import oracle
-    T, E, k = l_oracle.shape[0], w["E"], w["k"]
-    amb = np.zeros(T, dtype=bool)
-    grouped = w["n_groups"] > 1 and w["topk_groups"] < w["n_groups"]
-    gs = E // w["n_groups"]
-    for t in range(T):
-        row = l_oracle[t]
-        allowed = np.ones(E, dtype=bool)
-        if grouped:
-            sc = oracle.group_scores(row, w["n_groups"], w["group_score"]).astype(np.float64)
-            order = np.argsort(-sc, kind="stable")
-            g = w["topk_groups"]
-            if sc[order[g - 1]] - sc[order[g]] <= delta / 2 + 1e-6:
-                amb[t] = True
-                continue
-            allowed[:] = False
-            for q in order[:g]:
-                allowed[q * gs:(q + 1) * gs] = True
-        keys = np.sort(row[allowed].astype(np.float64))[::-1]
-        if len(keys) > k and keys[k - 1] - keys[k] <= 2 * delta:
-            amb[t] = True
-    return amb
+# ---------------------------------------------------------------- exact router inputs
+# The router GEMM sums H products in an order each kernel chooses. With x on a 1/16 grid
+# and the router weight on a 2^-10 grid, every product is a multiple of 2^-14; if in
+# addition sum_h |x_h| |w_eh| <= 2^10 for a token and expert, every partial sum, in any
+# order or grouping, is a multiple of 2^-14 below 2^10 in magnitude, which fp32's 24-bit
+# significand holds exactly. The logit is then exact before the bias, the bias is added
+# once with one rounding on both sides, and the GPU's fp32 logits equal the oracle's
+# (fp64, rounded once) bit for bit: the routing of both sides is decided by identical
+# scores, and no GPU result is handed to the oracle.
+X_GRID, W_GRID, SUM_BOUND = 16.0, 1024.0, 1024.0
+
+
+def grid_x(x: np.ndarray) -> np.ndarray:
+    return (np.round(np.asarray(x, dtype=np.float32) * np.float32(X_GRID)) / np.float32(X_GRID)).astype(np.float32)
+
+
+def grid_w_router(wr: np.ndarray) -> np.ndarray:
+    return (np.round(np.asarray(wr, dtype=np.float32) * np.float32(W_GRID)) / np.float32(W_GRID)).astype(np.float32)
+
+
+def assert_exact_router_sums(x: np.ndarray, wr: np.ndarray) -> None:
+    """The precondition above, on the host, for the given tokens."""
+    b = np.abs(np.asarray(x, dtype=np.float64)) @ np.abs(np.asarray(wr, dtype=np.float64)).T
+    assert b.max() <= SUM_BOUND, b.max()
+
+
+def exact_router_inputs(inp: dict) -> dict:
+    """A copy of a layer's host inputs with x and the router weight on the grids above (x
+    keeps its N(0,1) shape, rounded to multiples of 1/16; the weight its N(0, 0.02^2) shape,
+    rounded to multiples of 2^-10; both stay exact in bf16)."""
+    out = dict(inp)
+    out["x"] = grid_x(inp["x"])
+    out["w_router"] = grid_w_router(inp["w_router"])
+    assert_exact_router_sums(out["x"], out["w_router"])
+    return out
+
+
+def grid_device_(t: torch.Tensor, grid: float) -> torch.Tensor:
+    """The same rounding on a device tensor, in place (scaling by a power of two is exact,
+    and both numpy and torch round half to even)."""
+    return t.mul_(grid).round_().div_(grid)
+

@@ -4,7 +4,9 @@ one by one: sampled router-logit rows, sampled dispatched rows, sampled rows of 
 experts' MLP outputs, sampled combined tokens, and the whole-layer output of sampled
 tokens. Large weights are drawn on the GPU by the device twin of the generator; every
 oracle input is redrawn on the host from the same counters (never read back from a GPU
-result)."""
+result). x and the router weight are rounded, on both sides, to grids on which the router
+GEMM is exact in fp32 (moe_case.exact_router_inputs), so the GPU's logits equal the
+oracle's bit for bit, the routing is unique, and every sampled token is compared."""
 import numpy as np
 import pytest
 import torch
@@ -12,8 +14,8 @@ import torch
 import oracle
 import synth
 import token_routing_expert_router_gb300 as moe
-from moe_case import (cfg_of, device_weights_generated, mx_atom_offsets, mx_grouped_rows, np_of, routing_ambiguity,
-                      up, weights_arg)
+from moe_case import (W_GRID, X_GRID, assert_exact_router_sums, cfg_of, device_weights_generated, grid_device_,
+                      grid_w_router, grid_x, mx_atom_offsets, mx_grouped_rows, np_of, up, weights_arg)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +55,8 @@ class Layer:
         for key in list(self.d):
             if key.endswith("_bf16"):
                 del self.d[key]  # keep only what the layer reads
+        grid_device_(self.d["x"], X_GRID)  # the exact-router grids, also applied by x_rows
+        grid_device_(self.d["w_router"], W_GRID)
         cfg = cfg_of(w)
         self.cfg = cfg
         T, k, E, H = w["T"], w["k"], w["E"], w["H"]
@@ -96,6 +100,15 @@ def sample_tokens(w, n, seed=5):
     return np.unique(np.concatenate([[0, T - 1], rng.astype(np.int64)]))
 
 
+def x_rows(w, toks, dt=None):
+    """Host rows of the layer's x: the generator's rows on the exact-router grid."""
+    return grid_x(synth.rows(0, synth.X, toks, w["H"], 1.0, dt or synth.act_name(w)))
+
+
+def w_router_host(w):
+    return grid_w_router(synth.normal(0, synth.W_ROUTER, (w["E"], w["H"]), w["w_std"], synth.act_name(w)))
+
+
 def host_expert(w, e, mode):
     return tuple(quant_weight(m, mode) for m in synth.expert_weights(w, 0, e))
 
@@ -112,13 +125,15 @@ def test_fullsize_generator_twin_and_router_logits(name):
     L = layer(name)
     w = L.w
     toks = sample_tokens(w, 16)
-    xs = synth.rows(0, synth.X, toks, w["H"], 1.0, synth.act_name(w))
+    xs = x_rows(w, toks)
     assert np.array_equal(np_of(L.d["x"][torch.from_numpy(toks).cuda()]), xs)  # device twin == host
-    wr = synth.normal(0, synth.W_ROUTER, (w["E"], w["H"]), w["w_std"], synth.act_name(w))
+    wr = w_router_host(w)
+    assert np.array_equal(np_of(L.d["w_router"]), wr)
+    assert_exact_router_sums(xs, wr)
     bias = synth.zipf_bias(0, w["E"]) if w["zipf"] else None
     ref = oracle.router_logits(xs, wr, bias)
     got = np_of(L.logits[torch.from_numpy(toks).cuda()])
-    assert oracle.rel_l2(got, ref) < 1e-4
+    assert np.array_equal(got, ref)
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -130,22 +145,19 @@ def test_fullsize_layer_sampled_tokens(name):
     toks = sample_tokens(w, SAMPLE_TOKENS[name])
     counts = np_of(L.cnt)
     assert counts.sum() == T * k
-    xs = synth.rows(0, synth.X, toks, H, 1.0, synth.act_name(w))
-    wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], synth.act_name(w))
+    xs = x_rows(w, toks)
+    wr = w_router_host(w)
+    assert_exact_router_sums(xs, wr)
     bias = synth.zipf_bias(0, E) if w["zipf"] else None
     l_ref = oracle.router_logits(xs, wr, bias)
     idx_ref, wt_ref = oracle.route(l_ref, dict(w, T=len(toks)))
-    l_gpu = np_of(L.logits[torch.from_numpy(toks).cuda()])
-    delta = float(np.abs(l_gpu.astype(np.float64) - l_ref).max())
-    amb = routing_ambiguity(w, l_ref, delta)
-    idx_gpu = np_of(L.idx)[toks]
-    same = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
-    assert np.all(same | amb)
+    assert np.array_equal(np_of(L.logits[torch.from_numpy(toks).cuda()]), l_ref)
+    assert np.array_equal(np_of(L.idx)[toks], idx_ref)
     a = quant_act(xs, mode)
     y_ref = np.zeros((len(toks), H))
-    for e in sorted(set(idx_ref[same].ravel().tolist())):
+    for e in sorted(set(idx_ref.ravel().tolist())):
         mats = host_expert(w, e, mode)
-        for i in np.nonzero(same)[0]:
+        for i in range(len(toks)):
             for j in range(k):
                 if idx_ref[i, j] == e:
                     y_ref[i] += wt_ref[i, j] * oracle.expert_mlp(a[i:i + 1], *mats, quant_h=mode)[0]
@@ -153,7 +165,7 @@ def test_fullsize_layer_sampled_tokens(name):
         y_ref += oracle.expert_mlp(a, *host_shared(w, mode), quant_h=mode)
     got = np_of(L.y)[toks].astype(np.float64)
     tol = 3e-2 if mode else 1e-2
-    err = oracle.rel_l2(got[same], y_ref[same])
+    err = oracle.rel_l2(got, y_ref)
     assert err < tol, err
 
 
@@ -188,7 +200,7 @@ def test_fullsize_dispatch_and_expert_rows(name):
     assert moe.moe_read_status(L.ws) == moe.MOE_OK
     # sampled dispatched rows are bit-exact copies (or quantisations) of host-drawn tokens
     pick = np.unique(np.concatenate([[0, R - 1], (synth.bits_at(8, 91, np.arange(24, dtype=np.uint64)) % np.uint64(R)).astype(np.int64)]))
-    xt = synth.rows(0, synth.X, row_token[pick], H, 1.0, "bf16")
+    xt = x_rows(w, row_token[pick], "bf16")
     if fp8:
         q, s = oracle.quant_blocks(xt, 1, 128)
         assert np.array_equal(np_of(xd[torch.from_numpy(pick).cuda()]), q)
@@ -209,11 +221,11 @@ def test_fullsize_dispatch_and_expert_rows(name):
     for e in experts:
         r0, r1 = offsets[e], offsets[e + 1]
         rr = np.unique(np.array([r0, (r0 + r1) // 2, r1 - 1]))
-        xa = quant_act(synth.rows(0, synth.X, row_token[rr], H, 1.0, "bf16"), mode)
+        xa = quant_act(x_rows(w, row_token[rr], "bf16"), mode)
         ref_all.append(oracle.expert_mlp(xa, *host_expert(w, e, mode), quant_h=mode))
         got_all.append(np_of(yd[torch.from_numpy(rr).cuda()]))
     ts = np.array([0, T // 2, T - 1])
-    xa = quant_act(synth.rows(0, synth.X, ts, H, 1.0, "bf16"), mode)
+    xa = quant_act(x_rows(w, ts, "bf16"), mode)
     ref_all.append(oracle.expert_mlp(xa, *host_shared(w, mode), quant_h=mode))
     got_all.append(np_of(yd[torch.from_numpy(R + ts).cuda()]))
     got = np.concatenate(got_all).astype(np.float64)
@@ -250,9 +262,9 @@ def test_fullsize_combine_sampled(name):
 @pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_bf16"])
 def test_fullsize_training_step_sampled_tokens(name):
     """The training step at full size, in the calls the benchmark times (moe_forward_train,
-    then moe_backward_kept with the router's backward): for sampled tokens whose routing is
-    unambiguous, dx (through the experts and through the router) and dlogits against the
-    oracle's chain rule, token by token; and dW_router against its defining identity
+    then moe_backward_kept with the router's backward): for sampled tokens, routed by the
+    oracle from the layer's own fp32 scores, dx (through the experts and through the router)
+    and dlogits against the oracle's chain rule, token by token; and dW_router against its defining identity
     dl^T x on sampled experts (a property of the outputs at any size). dy is drawn on the
     GPU by the generator's device twin and redrawn on the host from the same counters."""
     L = layer(name)
@@ -279,24 +291,22 @@ def test_fullsize_training_step_sampled_tokens(name):
     moe.moe_backward_kept(cfg, d["x"], weights_arg(d), dy, L.ws, gu, dx, dtw, g, bws)
     torch.cuda.synchronize()
     assert moe.moe_read_status(bws) == moe.MOE_OK
-    # sampled tokens, routed by the oracle from its own logits
+    # sampled tokens, routed by the oracle from its own logits (equal to the layer's)
     toks = sample_tokens(w, 3)
-    xs = synth.rows(0, synth.X, toks, H, 1.0, "bf16")
+    xs = x_rows(w, toks, "bf16")
     dys = synth.rows(0, synth.DY, toks, H, 1.0, "bf16")
     assert np.array_equal(np_of(dy[torch.from_numpy(toks).cuda()].float()), dys)  # device twin == host
-    wr = synth.normal(0, synth.W_ROUTER, (E, H), w["w_std"], "bf16")
+    wr = w_router_host(w)
+    assert_exact_router_sums(xs, wr)
     bias = synth.zipf_bias(0, E) if w["zipf"] else None
     l_ref = oracle.router_logits(xs, wr, bias)
+    assert np.array_equal(np_of(L.logits[torch.from_numpy(toks).cuda()]), l_ref)
     idx_ref, wt_ref = oracle.route(l_ref, dict(w, T=len(toks)))
-    l_gpu = np_of(L.logits[torch.from_numpy(toks).cuda()])
-    amb = routing_ambiguity(w, l_ref, float(np.abs(l_gpu.astype(np.float64) - l_ref).max()))
-    idx_gpu = np_of(L.idx)[toks]
-    same = np.all(np.sort(idx_gpu, 1) == np.sort(idx_ref, 1), axis=1)
-    assert np.all(same | amb) and same.any()
+    assert np.array_equal(np_of(L.idx)[toks], idx_ref)
     experts = {}
     dx_gpu = np_of(dx.float()).astype(np.float64)[toks]
     dl_gpu = np_of(g["dlogits"]).astype(np.float64)[toks]
-    for i in np.nonzero(same)[0]:
+    for i in range(len(toks)):
         a = xs[i:i + 1].astype(np.float64)
         dyt = dys[i].astype(np.float64)
         dx_ref = np.zeros(H)
@@ -319,7 +329,7 @@ def test_fullsize_training_step_sampled_tokens(name):
         scale = float(w["routed_scale"]) * np.abs(dtw_ref).max()
         assert np.abs(dl_gpu[i] - dl_ref).max() <= 2e-2 * scale, (i, dl_gpu[i], dl_ref, scale)
     # dW_router = dl^T x on sampled experts (x redrawn on the host)
-    x_all = synth.normal(0, synth.X, (T, H), 1.0, "bf16").astype(np.float64)
+    x_all = grid_x(synth.normal(0, synth.X, (T, H), 1.0, "bf16")).astype(np.float64)
     dl_all = np_of(g["dlogits"]).astype(np.float64)
     dwr = np_of(g["dw_router"]).astype(np.float64)
     tc_path = E % 128 == 0 and H % 256 == 0

@@ -543,6 +543,67 @@ def test_mxfp8_layer_with_representable_inputs_is_exact_before_h():
     assert np.array_equal(y, q["yd"])
 
 
+def _e4m3_blocks(rng, rows, cols, br, bc, exps):
+    """Values that are e4m3 values times one power of two 2^j per br x bc block, each block
+    holding +-448 * 2^j exactly once and no other magnitude of 448, so a block quantiser of
+    that shape reproduces them exactly (scale = amax / 448 = 2^j). Returns (values, codes,
+    per-block j)."""
+    vals = oracle.e4m3_decode_all()
+    fin = np.array([c for c in range(256) if np.isfinite(vals[c]) and abs(vals[c]) < 448])
+    codes = rng.choice(fin, size=(rows, cols)).astype(np.uint8)
+    nbr, nbc = -(-rows // br), -(-cols // bc)
+    j = rng.choice(exps, size=(nbr, nbc))
+    for bi in range(nbr):
+        for bj in range(nbc):
+            r = bi * br + rng.integers(min(br, rows - bi * br))
+            c = bj * bc + rng.integers(min(bc, cols - bj * bc))
+            codes[r, c] = rng.choice([0x7E, 0xFE])  # +448, -448
+    scale = np.exp2(np.repeat(np.repeat(j, br, 0), bc, 1)[:rows, :cols].astype(np.float64))
+    return (vals[codes] * scale).astype(np.float32), codes, j
+
+
+def test_fp8_layer_with_representable_inputs_is_exact_before_h():
+    """The FP8 layer's composition step by step: x quantised per 1x128 block of a token's
+    row, each expert weight per 128x128 block, and h requantised per 1x128 block before the
+    down projection. With x and the weights built from e4m3 codes times a power-of-two scale
+    per block of those shapes, the first two quantisations are exact, so the layer must equal
+    the per-expert MLP with the 1x128 h requantisation alone, on those values, bit for bit.
+    Blocks of any other shape (x in 128x1 columns, weights in 1x128 rows) are lossy on the
+    same values, which the last asserts show."""
+    w = small("dsv3_fp8", T=16, H=256, E=4, k=2, F=128, F_shared=128, n_groups=1, topk_groups=1)
+    T, H, E, F = w["T"], w["H"], w["E"], w["F"]
+    rng = np.random.default_rng(31)
+    inp = synth.host_inputs(w, seed=7)
+    x, x_codes, x_j = _e4m3_blocks(rng, T, H, 1, 128, np.arange(-9, -3))
+    inp["x"] = x
+    wexp = np.arange(-14, -8)
+    for key, shape in (("w_gate", (E, F, H)), ("w_up", (E, F, H)), ("w_down", (E, H, F))):
+        inp[key] = np.stack([_e4m3_blocks(rng, shape[1], shape[2], 128, 128, wexp)[0] for _ in range(E)])
+    for key, shape in (("ws_gate", (F, H)), ("ws_up", (F, H)), ("ws_down", (H, F))):
+        inp[key] = _e4m3_blocks(rng, shape[0], shape[1], 128, 128, wexp)[0]
+    q = oracle.forward(w, inp)
+    # x: one fp32 scale per (token, 128 columns), equal to the block's 2^j; codes unchanged
+    assert q["x_scale"].shape == (T, H // 128)
+    assert np.array_equal(q["x_scale"], np.exp2(x_j).astype(np.float32))
+    assert np.array_equal(q["x_q"], x_codes)
+    # the experts, the shared expert and combine on the exact values
+    x64 = x.astype(np.float64)
+    yd = np.zeros_like(q["yd"])
+    for e in range(E):
+        r0, r1 = q["offsets"][e], q["offsets"][e + 1]
+        yd[r0:r1] = oracle.expert_mlp(x64[q["row_token"][r0:r1]], inp["w_gate"][e], inp["w_up"][e],
+                                      inp["w_down"][e], quant_h=1)
+    assert np.array_equal(yd, q["yd"])
+    ys = oracle.expert_mlp(x64, inp["ws_gate"], inp["ws_up"], inp["ws_down"], quant_h=1)
+    assert np.array_equal(ys, q["ys"])
+    assert np.array_equal(oracle.combine(yd, q["tok_row"], q["topk_w"], ys), q["y"])
+    # the same values through blocks of the other orientation are not reproduced
+    assert not np.array_equal(oracle.dequant_blocks(*oracle.quant_blocks(x, 128, 1), 128, 1), x64)
+    wg0 = inp["w_gate"][0]
+    assert not np.array_equal(oracle.dequant_blocks(*oracle.quant_blocks(wg0, 1, 128), 1, 128),
+                              wg0.astype(np.float64))
+
+
 # ------------------------------------------------------------------ backward
 def test_expert_mlp_backward_matches_torch_autograd():
     n, H, F = 13, 48, 40

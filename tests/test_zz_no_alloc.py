@@ -1,16 +1,15 @@
 """moe_route_static_scratch: routing for callers that cannot allocate device memory (a
-plugin handed only its input and output buffers, code running while a CUDA graph is
-captured, a runtime with a fixed memory budget). It must give exactly what moe_route gives
-(same kernels, same bits) while its scan scratch lives in the library's fixed array, call
-after call. This file is collected last so that a failure here comes after every other test
-has run."""
+plugin handed only its input and output buffers, a runtime with a fixed memory budget
+reserved up front). It must give exactly what moe_route gives (same kernels, same bits)
+while its scan scratch lives in the library's fixed array, call after call. This file is
+collected last so that a failure here comes after every other test has run."""
 import numpy as np
 import pytest
 import torch
 
 import synth
 import token_routing_expert_router_gb300 as moe
-from moe_case import alloc, cfg_of, np_of, up
+from moe_case import alloc, cfg_of, up
 
 pytestmark = pytest.mark.gpu
 
@@ -51,11 +50,8 @@ def test_static_scratch_matches_moe_route(w):
         moe.moe_route_static_scratch(b["cfg"], lg, o["topk_idx"], o["topk_w"], o["counts"],
                                      o["offsets"], o["row_token"], o["tok_row"], status)
         torch.cuda.synchronize()
-        for key in KEYS:
-            if key == "topk_w":
-                assert np.allclose(np_of(o[key]), np_of(b[key]), rtol=4e-6, atol=1e-7), (call, key)
-            else:
-                assert torch.equal(o[key], b[key]), (call, key)
+        for key in KEYS:  # same kernels on the same scores: every output bit for bit
+            assert torch.equal(o[key], b[key]), (call, key)
         assert int(status[0]) == 0
 
 

@@ -644,6 +644,9 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   const int tm = pair ? 2 * BM : BM;
   const int64_t mt_bound = ceil_div(R, tm) + c.E + (shared ? ceil_div(c.T, tm) : 0);
   cudaError_t e;
+  // The keep epilogue reads A by TMA boxes: gathered rows reach it only as CTA pairs, whose
+  // producers gather with TMA; single CTAs gather with cp.async in their own epilogue mode.
+  if (gu_keep != nullptr && row_token != nullptr && !pair) return cudaErrorInvalidValue;
   if (gu_keep != nullptr) {  // also keep g and u for the backward
     p.out2 = gu_keep;
     p.ldc2 = 2 * c.F;

@@ -1,19 +1,22 @@
 // moe_route_static_scratch: moe_route without a caller-provided workspace.
 //
-// Some callers cannot allocate device memory at the point where they route: code running
-// inside a CUDA graph capture or a custom allocator's callback, a plugin handed only its
-// input and output buffers by a host framework, or a runtime with a fixed memory budget
-// reserved up front. For them this entry point keeps the routing scan's scratch (the
-// per-block expert counts) in a fixed array that lives in the library's own device memory.
+// Some callers cannot allocate device memory at the point where they route: a plugin that a
+// host framework hands only its input and output buffers, a runtime whose device memory is
+// a fixed budget reserved up front, or code that runs inside an allocator's own callback.
+// For them this entry point keeps the routing scan's scratch (the per-block expert counts)
+// in a fixed array that lives in the library's own device memory.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the library holds
 // kStaticScratchInts int32 (1 MiB) of it until the process exits. Host code cannot use the
-// variable's name as a device address, so the first call on each device looks the address
-// up with cudaGetSymbolAddress (with that device current) and caches it; that first call
-// should therefore come before any stream capture. Every call on a device shares the one
-// array, so calls whose kernels overlap on the GPU (other streams, other threads) race and
-// must be serialised by the caller. Nothing in the array has to start at zero: the
-// counting pass writes every entry it later reads.
+// variable's name as a device address, so a call looks the address up with
+// cudaGetSymbolAddress (with the device current) whenever the current context differs from
+// the one the cached address belongs to: the first call on each device, and the first call
+// after that device's context was destroyed and recreated (cudaDeviceReset), when the module
+// may be loaded at another address. Such a first call should come before any stream
+// capture. Every call on a device shares the one array, so calls whose kernels overlap on
+// the GPU (other streams, other threads) race and must be serialised by the caller. Nothing
+// in the array has to start at zero: the counting pass writes every entry it later reads.
+#include <cuda.h>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -32,25 +35,54 @@ struct StaticScratch {
   DeviceStatus* sink;
 };
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link against libcuda).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    tried = true;
+  }
+  return fn;
+}
+
 std::mutex g_mu;
 StaticScratch g_addr[kMaxDevices];
-bool g_ready[kMaxDevices];
+CUcontext g_ctx[kMaxDevices];  // context the cached addresses belong to (null: none yet)
 
-// Device addresses of the two arrays on the current device (looked up once per device).
+cudaError_t current_ctx(CUcontext* out) {
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return cudaErrorNotSupported;
+  return get(out) == CUDA_SUCCESS ? cudaSuccess : cudaErrorContextIsDestroyed;
+}
+
+// Device addresses of the two arrays in the current context (looked up again whenever the
+// context is not the one they were looked up in).
 cudaError_t static_scratch(StaticScratch* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ready[dev]) {
+  CUcontext ctx = nullptr;
+  e = current_ctx(&ctx);
+  if (e != cudaSuccess) return e;
+  if (ctx == nullptr || ctx != g_ctx[dev]) {
     StaticScratch a{};
-    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&a.scratch), g_scan_scratch);
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&a.scratch), g_scan_scratch);  // makes the context current
     if (e != cudaSuccess) return e;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&a.sink), g_status_sink);
     if (e != cudaSuccess) return e;
+    e = current_ctx(&ctx);
+    if (e != cudaSuccess) return e;
     g_addr[dev] = a;
-    g_ready[dev] = true;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return cudaSuccess;
