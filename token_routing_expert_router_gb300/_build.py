@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_fp8.cu", "gemm_mx.cu", "gemm_bwd.cu", "router_bwd.cu", "route_noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_swap.cu", "gemm_fp8.cu", "gemm_mx.cu", "gemm_bwd.cu", "router_bwd.cu", "route_noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -606,6 +606,11 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                const float* topk_w, void* gu_keep) {
   if (c.xfer_dtype == MOE_DTYPE_E4M3)
     return launch_grouped_mlp_fp8(c, xd, xd_scale, offsets, w, h, h_scale, yd, st, s);
+  // experts averaging fewer than 512 rows: the tokens go on the MMA's N axis, so an expert's
+  // last tile is padded to a multiple of 32 tokens instead of 128 rows
+  if (row_token == nullptr && topk_w == nullptr && gu_keep == nullptr && swap_supported(c) &&
+      (int64_t)c.T * c.k < 512LL * c.E)
+    return launch_grouped_mlp_swap(c, xd, x, offsets, w, h, yd, st, s);
   const int64_t R = routed_rows(c), rows = total_rows(c);
   const bool shared = c.n_shared != 0;
   // ---- GEMM1: h = silu(A Wg^T) * (A Wu^T), tiles of 128 h columns (256 B rows). A is the

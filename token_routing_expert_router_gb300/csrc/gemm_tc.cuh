@@ -25,6 +25,12 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
                                const int32_t* tok_row = nullptr, const float* topk_w = nullptr,
                                void* gu_keep = nullptr);
 
+// The bf16 grouped MLP with the tokens on the MMA's N axis (CTA pairs of 256 weight rows,
+// token tiles in multiples of 32): the form for experts with few rows each.
+bool swap_supported(const moe_config_t& c);
+cudaError_t launch_grouped_mlp_swap(const moe_config_t& c, const void* xd, const void* x, const int32_t* offsets,
+                                    const moe_weights_t& w, void* h, void* yd, DeviceStatus* st, cudaStream_t s);
+
 // Backward of the grouped expert MLP (bf16). gu [R(+T), 2F] (g and u in 128-column blocks,
 // as the gate/up GEMM's tiles hold them); dgu the same columns and h [., F] with each
 // expert's rows padded to a multiple of 64 (backward_padded_rows rows): workspace.
