@@ -8,7 +8,8 @@ import torch
 import oracle
 import synth
 import token_routing_expert_router_gb300 as moe
-from moe_case import alloc, np_of, tdtype, up, weights_arg, device_weights_from_host
+from moe_case import (alloc, assert_exact_router_sums, device_weights_from_host, grid_w_router, grid_x, np_of, tdtype, up,
+                      weights_arg)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,6 +108,22 @@ def test_router_logits_real_widths(name, T, H, E):
     moe.moe_router_logits(b["cfg"], d["x"], d["w_router"], None, b["logits"], b["ws"])
     ref = oracle.router_logits(inp["x"], inp["w_router"], None)
     assert oracle.rel_l2(np_of(b["logits"]), ref) < 1e-4
+
+
+@pytest.mark.parametrize("T,H,E", [(701, 2048, 5), (4096, 4096, 8), (333, 2048, 12), (130, 2048, 16),
+                                   (1, 4096, 8), (3, 2048, 16)])
+def test_router_logits_small_e_streamed_shapes(T, H, E):
+    """The small-expert router's streamed form (bf16, E <= 8 with H of 2048 or 4096, E <= 16
+    with H = 2048): ragged last token groups, E below the kernel's width, a bias. On the
+    exact-sum grids every logit equals the oracle's bit for bit, whatever the summation order."""
+    w = synth.workload("stream_router", T, H, E, 2, 128)
+    inp = synth.host_inputs(w, seed=9, with_weights=False)
+    x, wr = grid_x(inp["x"]), grid_w_router(inp["w_router"])
+    assert_exact_router_sums(x, wr)
+    bias = synth.zipf_bias(9, E)
+    b = alloc(w)
+    moe.moe_router_logits(b["cfg"], up(x, torch.bfloat16), up(wr, torch.bfloat16), up(bias), b["logits"], b["ws"])
+    assert np.array_equal(np_of(b["logits"]), oracle.router_logits(x, wr, bias))
 
 
 BF16_CASES = [c for c in CASES if c["act_dtype"] == synth.BF16 and c["xfer_dtype"] == synth.BF16]

@@ -510,6 +510,89 @@ __global__ void __launch_bounds__(256) router_small_kernel(const void* __restric
   }
 }
 
+// S0 for bf16 layers with E <= EP <= 16 experts and H = 2048 * CPT: x streamed once with
+// many loads in flight, the router weights held in registers. Thread i of a block owns the
+// 16-byte chunks c = i + 256 j (j < CPT) of every row, and keeps W[e][c] for all e. The
+// block walks groups of TB = 32 / EP tokens (groups b, b + gridDim.x, ...; the next group's
+// rows are loaded while the current one is reduced); each thread forms the group's TB x EP
+// partial dot products, a warp reduce-scatter (31 shuffles) leaves lane l with the warp's
+// sum of product l, and 32 threads add the 8 warps' sums in order. fp32 accumulation.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(u[q] << 16);
+    f[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
+  }
+}
+
+template <int EP, int CPT>
+__global__ void __launch_bounds__(256) router_stream_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
+                                                            const float* __restrict__ bias, int T, int E,
+                                                            float* __restrict__ logits) {
+  constexpr int TB = 32 / EP;
+  constexpr int NCH = 256 * CPT;  // 16-byte chunks of a row
+  __shared__ float red[8][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float wf[EP][CPT][8];
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const uint4 v = e < E ? __ldg(w + (int64_t)e * NCH + tid + 256 * j) : make_uint4(0, 0, 0, 0);
+      bf16x8_to_f32(v, wf[e][j]);
+    }
+  const int ngroups = (T + TB - 1) / TB;
+  uint4 xv[TB][CPT];
+  auto load = [&](int g) {
+#pragma unroll
+    for (int i = 0; i < TB; ++i) {
+      const int t = min(g * TB + i, T - 1);  // a short last group repeats a row; not stored
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) xv[i][j] = __ldg(x + (int64_t)t * NCH + tid + 256 * j);
+    }
+  };
+  if (blockIdx.x < ngroups) load(blockIdx.x);
+  for (int g = blockIdx.x; g < ngroups; g += gridDim.x) {
+    float acc[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < TB; ++i)
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        float xf[8];
+        bf16x8_to_f32(xv[i][j], xf);
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[i * EP + e] = __fmaf_rn(xf[q], wf[e][j][q], acc[i * EP + e]);
+      }
+    if (g + (int)gridDim.x < ngroups) load(g + gridDim.x);  // in flight during the reduction
+    // reduce-scatter: at each step a lane keeps the half of its window its lane bit selects
+#pragma unroll
+    for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int q = 0; q < n / 2; ++q) {
+        const float send = upper ? acc[q] : acc[q + n / 2];
+        const float keep = upper ? acc[q + n / 2] : acc[q];
+        acc[q] = keep + __shfl_xor_sync(kFull, send, off);
+      }
+    }
+    red[warp][lane] = acc[0];  // the warp's sum of product `lane` (token lane / EP, expert lane % EP)
+    __syncthreads();
+    if (tid < 32) {
+      float v = 0.0f;
+#pragma unroll
+      for (int wp = 0; wp < 8; ++wp) v += red[wp][tid];
+      const int t = g * TB + tid / EP, e = tid % EP;
+      if (t < T && e < E) logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
+    }
+    __syncthreads();
+  }
+}
+
 // Auxiliary load-balancing loss, pass 1: per block of 128 tokens (8 warps x 16 tokens), the
 // sum over its tokens of each expert's probability (softmax over all experts, or sigmoid
 // scores divided by their sum). Every sum runs in a fixed order: no float atomics.
@@ -603,7 +686,21 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
-  (void)sms;
+  // streamed form, one block per SM, for the shapes whose weight slice fits in registers
+  // without spilling (E <= 8 with H of 2048 or 4096; E <= 16 with H of 2048)
+  if (bf && ((c.E <= 8 && (c.H == 2048 || c.H == 4096)) || (c.E <= 16 && c.H == 2048))) {
+    const int tb = c.E <= 8 ? 4 : 2;
+    const unsigned blocks = (unsigned)std::min<int64_t>(sms, ceil_div(c.T, tb));
+    const uint4* xv = static_cast<const uint4*>(x);
+    const uint4* wv = static_cast<const uint4*>(w);
+#define MOE_RST(EP, CPT) \
+  if (c.E <= EP && c.H == 2048 * CPT) { \
+    router_stream_kernel<EP, CPT><<<blocks, 256, 0, s>>>(xv, wv, bias, c.T, c.E, logits); \
+    return cudaGetLastError(); \
+  }
+    MOE_RST(8, 1) MOE_RST(8, 2) MOE_RST(16, 1)
+#undef MOE_RST
+  }
 #define MOE_RS(EP, TB)                                                                                \
   if (c.E <= EP) {                                                                                  \
     const unsigned blocks = (unsigned)ceil_div(c.T, TB);                                            \
