@@ -8,9 +8,9 @@ a second loop over the staged entry points, timed the same way.
 
 The headline is the Mixtral-shaped layer (T=4096, H=4096, 8 experts top-2, F=14336). The
 default run then measures the other four layer shapes the same way (tiny fp32,
-DeepSeek-V3-shaped bf16, imbalanced routing, FP8 dispatch) and reports them under
-"configs", each with its throughput, its grouped-GEMM and dispatch/combine rooflines and
-its own CPU-oracle baseline (--headline-only skips them).
+DeepSeek-V3-shaped bf16, imbalanced routing, FP8 dispatch), and the FP8 shape with MXFP8
+block scales, and reports them under "configs", each with its throughput, its grouped-GEMM
+and dispatch/combine rooflines and its own CPU-oracle baseline (--headline-only skips them).
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -483,7 +483,7 @@ def dtype_name(w):
 # tokens, and drawing those weights on the host is not timed but takes time).
 CPU_TOKENS = {"tiny_fp32": 256, "mixtral_bf16": 64, "dsv3_bf16": 8, "imbalanced_bf16": 64, "dsv3_fp8": 8,
               "dsv3_mxfp8": 8}
-OTHER_CONFIGS = ["tiny_fp32", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8"]
+OTHER_CONFIGS = ["tiny_fp32", "dsv3_bf16", "imbalanced_bf16", "dsv3_fp8", "dsv3_mxfp8"]
 
 
 def measure_config(ctx, args, w):
