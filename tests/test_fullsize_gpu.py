@@ -233,6 +233,33 @@ def test_fullsize_dispatch_and_expert_rows(name):
     assert oracle.rel_l2(got, ref) < (3e-2 if mode else 1e-2)
 
 
+@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_bf16"])
+def test_fullsize_gathered_rows_equal_dispatched_rows(name):
+    """The fused permutation at full size (CTA-pair TMA row gathers on the Mixtral shape,
+    single-CTA cp.async gathers with routed/shared tile switches on the DeepSeek-V3 shape):
+    GEMM1 gathering its rows from x by token gives h and yd bit-identical to dispatch +
+    grouped MLP on the dispatched copy."""
+    L = layer(name)
+    w = L.w
+    T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
+    R = T * k
+    rows = R + (T if w["n_shared"] else 0)
+    idx, _ = oracle.route(synth.synthetic_logits(11, T, E), w)
+    counts, offsets, row_token, tok_row = oracle.permute(idx, E)
+    xd = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(L.cfg, L.d["x"], up(tok_row), xd, None)
+    h1 = torch.empty((rows, F), dtype=torch.bfloat16, device="cuda")
+    yd1 = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_mlp(L.cfg, xd, None, L.d["x"], up(offsets), weights_arg(L.d), h1, None, yd1, L.ws)
+    del xd
+    h2, yd2 = torch.empty_like(h1), torch.empty_like(yd1)
+    moe.moe_grouped_mlp_gather(L.cfg, L.d["x"], up(row_token), up(offsets), weights_arg(L.d), h2, yd2, L.ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(L.ws) == moe.MOE_OK
+    assert torch.equal(h2, h1)
+    assert torch.equal(yd2, yd1)
+
+
 @pytest.mark.parametrize("name", ["dsv3_bf16", "imbalanced_bf16"])
 def test_fullsize_combine_sampled(name):
     L = layer(name)
