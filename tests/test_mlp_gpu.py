@@ -88,6 +88,52 @@ def test_grouped_mlp_against_oracle(w):
     assert moe.moe_read_status(b["ws"]) == moe.MOE_OK
 
 
+# CTA-pair shapes (at least 512 rows per expert on average) with explicit segment sizes:
+# tails of 1-64 rows (run with their tokens on the MMA's N axis), a whole expert of 64 rows,
+# an empty expert, tails of 76 and more rows (ordinary tiles), and a shared expert whose
+# 1060 rows end in a 36-row tail
+TAIL_CASES = [
+    (synth.scaled(W["dsv3_bf16"], T=1060, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2, topk_groups=1,
+                  name="tails_shared"), [64, 300, 1035, 721]),
+    (synth.scaled(W["mixtral_bf16"], T=1100, H=512, E=4, F=384, name="tails_empty_expert"), [0, 34, 1100, 1066]),
+    (synth.scaled(W["mixtral_bf16"], T=1100, H=512, E=4, F=384, name="tails_tiny"), [1, 2, 17, 2180]),
+]
+
+
+@pytest.mark.parametrize("w,counts", TAIL_CASES, ids=[c[0]["name"] for c in TAIL_CASES])
+def test_pair_segment_tails_against_oracle(w, counts):
+    """Every expert segment, and separately the rows of its last (partial) 256-row tile,
+    against the oracle's per-expert MLP, for segment sizes chosen to hit each tail form."""
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    R = T * k
+    assert sum(counts) == R and R >= 512 * E
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    seed = 12
+    inp = synth.host_inputs(w, seed=seed)
+    xd = synth.normal(seed + 1, synth.X, (R, H), 1.0, synth.act_name(w))
+    d = device_weights_from_host(w, inp)
+    b = alloc(w)
+    b["xd"][:R].copy_(up(xd, tdtype(w)))
+    moe.moe_grouped_mlp(b["cfg"], b["xd"], None, d["x"], up(offsets), weights_arg(d), b["h"], None, b["yd"],
+                        b["ws"])
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(b["ws"]) == moe.MOE_OK
+    got = np_of(b["yd"]).astype(np.float64)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        ref = oracle.expert_mlp(xd[r0:r1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+        assert oracle.rel_l2(got[r0:r1], ref) < 1e-2, e
+        tail = (r1 - r0) % 256 or 256
+        assert oracle.rel_l2(got[r1 - tail:r1], ref[-tail:]) < 1e-2, (e, tail)
+    if w["n_shared"]:
+        ref = oracle.expert_mlp(inp["x"], inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+        assert oracle.rel_l2(got[R:], ref) < 1e-2
+        tail = T % 256
+        assert oracle.rel_l2(got[R + T - tail:], ref[-tail:]) < 1e-2
+
+
 @pytest.mark.parametrize("w", CASES[:4], ids=[c["name"] for c in CASES[:4]])
 def test_router_logits_against_oracle(w):
     inp = synth.host_inputs(w, seed=6, with_weights=False)

@@ -13,6 +13,11 @@
 // group's many M tiles spread over every SM. Ragged segment tails are handled by loading
 // the full 128-row box (rows past the segment belong to the next group or are zero-filled
 // past the end of the tensor) and storing only the segment's rows.
+// CTA pairs of the plain forward GEMMs run a tile holding at most 64 of a segment's rows
+// (its tail) with the operands swapped: the MMA's M side is the tile's 256 weight rows and
+// its N side the tail's tokens rounded up to 32, so the tile costs the tensor core N / 256
+// of a full one. It follows the segment's full tiles of the same weight block, which read
+// that block from HBM at about the same time, so its weight loads mostly hit L2.
 #include <cudaTypedefs.h>
 
 #include "gemm_tc.cuh"
@@ -69,9 +74,21 @@ struct TcParams {
   const int32_t* w_tok_row;
   const float* w_topk;
   int w_k;
+  int swap_rows;            // CTA pairs, plain GEMM1 / GEMM2: tiles of at most this many rows
+                            //   run with tokens on the MMA's N axis (0: never)
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
+
+// The tokens-on-N tail tiles' own boxes: A rows 16 at a time (routed and extra group) and,
+// for GEMM1, 64-row boxes of the gate and up weights, so that each CTA holds the gate and
+// up rows of the same 64 features.
+struct SwapMaps {
+  CUtensorMap t16, t16x, g64, u64, g64x, u64x;
+};
+
+// Named barrier 2 over the four epilogue warps (the tail tiles' gate/up exchange).
+__device__ __forceinline__ void swap_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // Shared memory of one CTA. CG = 2 (a CTA pair) halves the B rows each CTA holds, so a
 // stage is 32 KB instead of 48 KB and six stages fit instead of four.
@@ -97,10 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmB1x,
-                        const TcParams p) {
+                        const __grid_constant__ SwapMaps sw, const TcParams p) {
   using S = Smem<BN, CG>;
   constexpr int STAGES = S::kStages;
   constexpr int TM = BM * CG;  // rows of an m tile
+  constexpr bool kSwapTail = CG == 2 && BN == 256 && (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_BF16);
+  // a tail tile: its tokens (rounded up to 32) on the MMA's N axis
+  auto swap_tile = [&](int rows) { return kSwapTail && rows <= p.swap_rows; };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -246,6 +266,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(tb0, b_dst, &full[stage], kb * BK, b_row);
             }
           }
+        } else if (swap_tile(c.rows)) {
+          // tail tile: this CTA's 128 weight rows into the A slot (GEMM1: 64 gate + 64 up rows
+          // of features [128 nb + 64 rank, +64); GEMM2: its usual 128 rows) and its half of
+          // the tokens (16 or 32 rows) into the B slot
+          const int nhalf = ((c.rows + 31) & ~31) / 2;
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(S::kABytes + nhalf * BK * 2));
+            const uint32_t bar = mapa_shared(smem_addr(&full[stage]), 0);
+            if (kGatedB) {
+              const int wrow = (extra ? 0 : c.g * p.b_group_rows) + c.nb * b_tile_rows + (int)rank * 64;
+              tma_load_2d_pair(extra ? &sw.g64x : &sw.g64, a_dst, bar, kb * BK, wrow);
+              tma_load_2d_pair(extra ? &sw.u64x : &sw.u64, a_dst + 64 * BK * 2, bar, kb * BK, wrow);
+            } else {
+              tma_load_2d_pair(tb0, a_dst, bar, kb * BK, b_row);
+            }
+            const int trow = (extra ? p.a2_row_base : p.offsets[c.g]) + c.mb * TM + (int)rank * nhalf;
+            for (int j = 0; j < nhalf; j += 16)
+              tma_load_2d_pair(extra ? &sw.t16x : &sw.t16, b_dst + j * BK * 2, bar, kb * BK, trow + j);
+          }
         } else {
           // both CTAs' loads complete on the leader's barrier, which expects both
           if (lane == 0 && leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
@@ -288,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = unit; tile < total_tiles && ok; tile += nunits) {
         const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
-        const uint32_t id = (CG == 1 && c.rows <= 64) ? idesc64 : idesc;
+        // tail tiles: A = the weight rows, B = the tokens (N = rows rounded up to 32)
+        const uint32_t id = swap_tile(c.rows) ? idesc_make(1u, TM, (c.rows + 31) & ~31)
+                                              : (CG == 1 && c.rows <= 64) ? idesc64 : idesc;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort, p.timeout_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -302,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (CG == 1)
               mma_bf16(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), id, (kb | k) != 0);
             else
-              mma_bf16_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), idesc,
+              mma_bf16_pair(d_tmem, desc_k_sw128(a_addr + k * 32), desc_k_sw128(b_addr + k * 32), id,
                             (kb | k) != 0);
           }
           // frees the stage (in both CTAs) once these MMAs have read it
@@ -330,13 +371,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_addr(&tempty[0]), 0) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    bool dead = false;  // a wait gave up: the warp walks the rest of its tiles without work
     for (int tile = unit; tile < total_tiles; tile += nunits) {
       const TileCoord c = decode_tile(tile, mt_prefix, ngroups, p.n_tiles, seg_rows, TM);
-      bool ok = mbar_wait(&tfull[acc], acc_phase, abort, p.timeout_ns, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
+      if (!dead) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, p.timeout_ns, p.status));
+        if (ok) tc_fence_after();
+        else dead = true;
+      }
+      if (dead) {
+        // every epilogue warp still meets each named barrier of the tail tiles' SwiGLU
+        if (EPI == EPI_SWIGLU_BF16 && swap_tile(c.rows)) {
+          for (int t0 = 0; t0 < c.rows; t0 += 32) {
+            swap_bar();
+            swap_bar();
+          }
+          swap_bar();
+        }
+        continue;
+      }
       const bool extra = c.g >= p.G;
+      if constexpr (kSwapTail) {
+        if (swap_tile(c.rows)) {
+          // TMEM lane = weight row, column = token. Token t is output row row0 + t.
+          const int n = c.rows;
+          const int64_t row0 = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + (int64_t)c.mb * TM;
+          const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+          if (EPI == EPI_SWIGLU_BF16) {
+            // lanes 0-63 gate, 64-127 up of features f = 128 nb + 64 rank + fl; the up warps
+            // hand their values to the gate warps through the four warps' staging areas, as
+            // U[32 tokens][64 fl]. A barrier before each fill (no warp still uses its staging
+            // for an earlier tile or chunk) and one after the tile (the next tile's stores).
+            float* U = reinterpret_cast<float*>(seg_rows + kMaxGroups);
+            const int fl = (quarter & 1) * 32 + lane;
+            __nv_bfloat16* col = out + row0 * p.ldc + c.nb * (BN / 2) + (int)rank * 64 + fl;
+            for (int t0 = 0; t0 < n; t0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(t_row + t0, v);
+              tmem_ld_wait();
+              swap_bar();
+              if (quarter >= 2) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) U[i * 64 + fl] = __uint_as_float(v[i]);
+              }
+              swap_bar();
+              if (quarter < 2) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float g = __uint_as_float(v[i]);
+                  const float h = g / (1.0f + __expf(-g)) * U[i * 64 + fl];
+                  if (t0 + i < n) col[(int64_t)(t0 + i) * p.ldc] = __float2bfloat16_rn(h);
+                }
+              }
+            }
+            swap_bar();
+          } else {
+            // lane = output feature 256 nb + 128 rank + 32 quarter + lane
+            __nv_bfloat16* col = out + row0 * p.ldc + c.nb * BN + (int)rank * 128 + quarter * 32 + lane;
+            for (int t0 = 0; t0 < n; t0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(t_row + t0, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (t0 + i < n) col[(int64_t)(t0 + i) * p.ldc] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            }
+          }
+          tc_fence_before();
+          if (!leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+          else mbar_arrive_relaxed(&tempty[acc]);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+          continue;
+        }
+      }
       const bool m64 = CG == 1 && c.rows <= 64;  // M = 64 tile: 16 rows per lane quarter
       const int row_in_tile = m64 ? quarter * 16 + lane : (int)rank * BM + quarter * 32 + lane;
       const int64_t out_row = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + c.mb * TM + row_in_tile;
@@ -523,8 +631,12 @@ namespace {
 template <int BN, int EPI, int CG = 1>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b0, const CUtensorMap& b1,
                    const CUtensorMap& b0x, const CUtensorMap& b1x, const TcParams& p, int64_t max_tiles,
-                   cudaStream_t s) {
+                   cudaStream_t s, const SwapMaps* swp = nullptr) {
   if (max_tiles <= 0) return cudaSuccess;
+  if (p.swap_rows > 0 && swp == nullptr) return cudaErrorInvalidValue;
+  SwapMaps unused;  // no tail tiles: never read
+  unused.t16 = unused.t16x = unused.g64 = unused.u64 = unused.g64x = unused.u64x = a;
+  const SwapMaps& sw = swp ? *swp : unused;
   auto kern = tc_gemm_bf16_kernel<BN, EPI, CG>;
   const size_t smem = Smem<BN, CG>::kBytes;
   static bool attr_set = false;  // per instantiation
@@ -535,7 +647,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMa
   }
   if constexpr (CG == 1) {
     const int grid = (int)std::min<int64_t>(num_sms(), max_tiles);
-    kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, p);
+    kern<<<grid, kThreads, smem, s>>>(a, a2, b0, b1, b0x, b1x, sw, p);
   } else {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * (num_sms() / 2));
@@ -557,7 +669,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMa
     }
     const int pairs = (int)std::min<int64_t>(std::min(max_pairs, num_sms() / 2), max_tiles);
     cfg.gridDim = dim3(2 * pairs);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, a2, b0, b1, b0x, b1x, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, a2, b0, b1, b0x, b1x, sw, p);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -659,7 +771,22 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
              : launch<256, EPI_SWIGLU_GU, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
     p.out2 = nullptr;
   } else {
-    if (pair)
+    if (pair && row_token == nullptr) {
+      // segment tails of at most 64 rows run with their tokens on the MMA's N axis
+      SwapMaps sw;
+      ok = make_bf16(&sw.t16, xd, rows, c.H, 16) && make_bf16(&sw.g64, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
+           make_bf16(&sw.u64, w.w_up, (uint64_t)c.E * c.F, c.H, 64);
+      if (shared) {
+        ok = ok && make_bf16(&sw.t16x, x, c.T, c.H, 16) && make_bf16(&sw.g64x, w.ws_gate, c.F, c.H, 64) &&
+             make_bf16(&sw.u64x, w.ws_up, c.F, c.H, 64);
+      } else {
+        sw.t16x = sw.t16; sw.g64x = sw.g64; sw.u64x = sw.u64;
+      }
+      if (!ok) return cudaErrorInvalidValue;
+      p.swap_rows = 64;
+      e = launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s, &sw);
+      p.swap_rows = 0;
+    } else if (pair)
       e = launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
     else if (row_token)  // single CTAs gather their rows with cp.async
       e = launch<256, EPI_SWIGLU_GATHER, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
@@ -688,6 +815,16 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.b_group_rows = c.H;
   p.ldc = c.H;
   p.out = yd;
+  if (pair && topk_w == nullptr) {
+    // segment tails of at most 64 rows run with their tokens on the MMA's N axis (the
+    // routed and the shared expert's h rows come from the same map)
+    SwapMaps sw;
+    if (!make_bf16(&sw.t16, h, rows, c.F, 16)) return cudaErrorInvalidValue;
+    sw.t16x = sw.t16;
+    sw.g64 = sw.u64 = sw.g64x = sw.u64x = bd;  // GEMM2's tail tiles load their weights through bd / bdx
+    p.swap_rows = 64;
+    return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s, &sw);
+  }
   if (pair) return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
   if (bn2 == 256) return launch<256, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
   return launch<128, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
