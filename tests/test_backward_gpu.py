@@ -30,6 +30,10 @@ CASES = [
     # 256 experts: the router's products on the tensor cores (most experts get a few rows)
     synth.scaled(W["dsv3_bf16"], T=600, H=512, E=256, k=8, F=256, F_shared=256, n_groups=8, topk_groups=4,
                  name="e256_shared"),
+    # CTA pairs whose segments (~530 rows) and shared expert (1060 rows) end in tails of at
+    # most 64 rows: the forward's tokens-on-N tail tiles, with g and u kept for the backward
+    synth.scaled(W["dsv3_bf16"], T=1060, H=512, E=4, k=2, F=256, F_shared=256, n_groups=2, topk_groups=1,
+                 name="pair_tails"),
 ]
 TOL = 1e-2  # bf16 layers
 
@@ -191,8 +195,8 @@ def test_backward_after_forward_equals_staged(w):
     assert not torch.equal(dx_r, dx)
 
 
-@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[3], CASES[5]],
-                         ids=["mixtral_small", "imbalanced_small", "pair_shared", "e256_shared"])
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[3], CASES[5], CASES[6]],
+                         ids=["mixtral_small", "imbalanced_small", "pair_shared", "e256_shared", "pair_tails"])
 def test_forward_train_keeps_what_the_backward_recomputes(w):
     """moe_forward_train gives moe_forward's y and keeps g and u; moe_backward_kept on them
     gives moe_backward's every output bit for bit (the recomputed gate/up GEMM is the same

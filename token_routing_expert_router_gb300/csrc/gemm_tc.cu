@@ -13,7 +13,7 @@
 // group's many M tiles spread over every SM. Ragged segment tails are handled by loading
 // the full 128-row box (rows past the segment belong to the next group or are zero-filled
 // past the end of the tensor) and storing only the segment's rows.
-// CTA pairs of the plain forward GEMMs run a tile holding at most 64 of a segment's rows
+// CTA pairs of the forward GEMMs run a tile holding at most 64 of a segment's rows
 // (its tail) with the operands swapped: the MMA's M side is the tile's 256 weight rows and
 // its N side the tail's tokens rounded up to 32, so the tile costs the tensor core N / 256
 // of a full one. It follows the segment's full tiles of the same weight block, which read
@@ -32,6 +32,7 @@ constexpr int BK = 64;             // bf16 K per stage: one 128-byte swizzle row
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 514;    // routed experts (<= 512) + one extra group + 1
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+constexpr int kSwapRows = 64;      // CTA pairs: tails of at most this many rows go tokens-on-N
 
 // EPI_STORE_GU: the gate/up GEMM (B = gate and up rows, as for SwiGLU) storing g and u
 // themselves, for the backward's recomputation of the activation. EPI_SWIGLU_GU: the
@@ -118,7 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = Smem<BN, CG>;
   constexpr int STAGES = S::kStages;
   constexpr int TM = BM * CG;  // rows of an m tile
-  constexpr bool kSwapTail = CG == 2 && BN == 256 && (EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_BF16);
+  constexpr bool kSwiGLU = EPI == EPI_SWIGLU_BF16 || EPI == EPI_SWIGLU_GU;
+  constexpr bool kSwapTail = CG == 2 && BN == 256 && (kSwiGLU || EPI == EPI_STORE_BF16);
   // a tail tile: its tokens (rounded up to 32) on the MMA's N axis
   auto swap_tile = [&](int rows) { return kSwapTail && rows <= p.swap_rows; };
   extern __shared__ uint8_t smem_raw[];
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dead) {
         // every epilogue warp still meets each named barrier of the tail tiles' SwiGLU
-        if (EPI == EPI_SWIGLU_BF16 && swap_tile(c.rows)) {
+        if (kSwiGLU && swap_tile(c.rows)) {
           for (int t0 = 0; t0 < c.rows; t0 += 32) {
             swap_bar();
             swap_bar();
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t row0 = (extra ? p.out_extra_base : (int64_t)p.offsets[c.g]) + (int64_t)c.mb * TM;
           const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-          if (EPI == EPI_SWIGLU_BF16) {
+          if (kSwiGLU) {
             // lanes 0-63 gate, 64-127 up of features f = 128 nb + 64 rank + fl; the up warps
             // hand their values to the gate warps through the four warps' staging areas, as
             // U[32 tokens][64 fl]. A barrier before each fill (no warp still uses its staging
@@ -406,6 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* U = reinterpret_cast<float*>(seg_rows + kMaxGroups);
             const int fl = (quarter & 1) * 32 + lane;
             __nv_bfloat16* col = out + row0 * p.ldc + c.nb * (BN / 2) + (int)rank * 64 + fl;
+            // EPI_SWIGLU_GU also keeps g and u: the tile's block of 128 g, then 128 u, of out2
+            __nv_bfloat16* gcol = EPI == EPI_SWIGLU_GU ? static_cast<__nv_bfloat16*>(p.out2) + row0 * p.ldc2 +
+                                                             c.nb * BN + (int)rank * 64 + fl
+                                                       : nullptr;
             for (int t0 = 0; t0 < n; t0 += 32) {
               uint32_t v[32];
               tmem_ld32(t_row + t0, v);
@@ -419,9 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (quarter < 2) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                  const float g = __uint_as_float(v[i]);
-                  const float h = g / (1.0f + __expf(-g)) * U[i * 64 + fl];
-                  if (t0 + i < n) col[(int64_t)(t0 + i) * p.ldc] = __float2bfloat16_rn(h);
+                  const float g = __uint_as_float(v[i]), u = U[i * 64 + fl];
+                  const float h = g / (1.0f + __expf(-g)) * u;
+                  if (t0 + i < n) {
+                    col[(int64_t)(t0 + i) * p.ldc] = __float2bfloat16_rn(h);
+                    if (EPI == EPI_SWIGLU_GU) {
+                      gcol[(int64_t)(t0 + i) * p.ldc2] = __float2bfloat16_rn(g);
+                      gcol[(int64_t)(t0 + i) * p.ldc2 + BN / 2] = __float2bfloat16_rn(u);
+                    }
+                  }
                 }
               }
             }
@@ -764,26 +776,32 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   // The keep epilogue reads A by TMA boxes: gathered rows reach it only as CTA pairs, whose
   // producers gather with TMA; single CTAs gather with cp.async in their own epilogue mode.
   if (gu_keep != nullptr && row_token != nullptr && !pair) return cudaErrorInvalidValue;
+  // CTA pairs without row gathers: segment tails of at most kSwapRows rows run with their
+  // tokens on the MMA's N axis
+  SwapMaps sw;
+  const bool tails = pair && row_token == nullptr;
+  if (tails) {
+    ok = make_bf16(&sw.t16, xd, rows, c.H, 16) && make_bf16(&sw.g64, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
+         make_bf16(&sw.u64, w.w_up, (uint64_t)c.E * c.F, c.H, 64);
+    if (shared) {
+      ok = ok && make_bf16(&sw.t16x, x, c.T, c.H, 16) && make_bf16(&sw.g64x, w.ws_gate, c.F, c.H, 64) &&
+           make_bf16(&sw.u64x, w.ws_up, c.F, c.H, 64);
+    } else {
+      sw.t16x = sw.t16; sw.g64x = sw.g64; sw.u64x = sw.u64;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+  }
   if (gu_keep != nullptr) {  // also keep g and u for the backward
     p.out2 = gu_keep;
     p.ldc2 = 2 * c.F;
-    e = pair ? launch<256, EPI_SWIGLU_GU, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s)
+    p.swap_rows = tails ? kSwapRows : 0;
+    e = pair ? launch<256, EPI_SWIGLU_GU, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s, tails ? &sw : nullptr)
              : launch<256, EPI_SWIGLU_GU, 1>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s);
     p.out2 = nullptr;
+    p.swap_rows = 0;
   } else {
-    if (pair && row_token == nullptr) {
-      // segment tails of at most 64 rows run with their tokens on the MMA's N axis
-      SwapMaps sw;
-      ok = make_bf16(&sw.t16, xd, rows, c.H, 16) && make_bf16(&sw.g64, w.w_gate, (uint64_t)c.E * c.F, c.H, 64) &&
-           make_bf16(&sw.u64, w.w_up, (uint64_t)c.E * c.F, c.H, 64);
-      if (shared) {
-        ok = ok && make_bf16(&sw.t16x, x, c.T, c.H, 16) && make_bf16(&sw.g64x, w.ws_gate, c.F, c.H, 64) &&
-             make_bf16(&sw.u64x, w.ws_up, c.F, c.H, 64);
-      } else {
-        sw.t16x = sw.t16; sw.g64x = sw.g64; sw.u64x = sw.u64;
-      }
-      if (!ok) return cudaErrorInvalidValue;
-      p.swap_rows = 64;
+    if (tails) {
+      p.swap_rows = kSwapRows;
       e = launch<256, EPI_SWIGLU_BF16, 2>(a1, a1x, bg, bu, bgx, bux, p, mt_bound * p.n_tiles, s, &sw);
       p.swap_rows = 0;
     } else if (pair)
@@ -816,14 +834,14 @@ cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const floa
   p.ldc = c.H;
   p.out = yd;
   if (pair && topk_w == nullptr) {
-    // segment tails of at most 64 rows run with their tokens on the MMA's N axis (the
+    // segment tails of at most kSwapRows rows run with their tokens on the MMA's N axis (the
     // routed and the shared expert's h rows come from the same map)
-    SwapMaps sw;
-    if (!make_bf16(&sw.t16, h, rows, c.F, 16)) return cudaErrorInvalidValue;
-    sw.t16x = sw.t16;
-    sw.g64 = sw.u64 = sw.g64x = sw.u64x = bd;  // GEMM2's tail tiles load their weights through bd / bdx
-    p.swap_rows = 64;
-    return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s, &sw);
+    SwapMaps sw2;
+    if (!make_bf16(&sw2.t16, h, rows, c.F, 16)) return cudaErrorInvalidValue;
+    sw2.t16x = sw2.t16;
+    sw2.g64 = sw2.u64 = sw2.g64x = sw2.u64x = bd;  // GEMM2's tail tiles load their weights through bd / bdx
+    p.swap_rows = kSwapRows;
+    return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s, &sw2);
   }
   if (pair) return launch<256, EPI_STORE_BF16, 2>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
   if (bn2 == 256) return launch<256, EPI_STORE_BF16, 1>(a2, a2, bd, bd, bdx, bdx, p, mt_bound * p.n_tiles, s);
