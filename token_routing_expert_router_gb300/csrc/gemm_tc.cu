@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128 * CG);
+      mbar_init(&tempty[a], 4 * CG);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -451,8 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_fence_before();
-          if (!leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
-          else mbar_arrive_relaxed(&tempty[acc]);
+          __syncwarp();  // every lane's TMEM loads are complete: one arrival per warp
+          if (lane == 0) {
+            if (!leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+            else mbar_arrive_relaxed(&tempty[acc]);
+          }
           if (++acc == 2) { acc = 0; acc_phase ^= 1; }
           continue;
         }
@@ -558,8 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
-      else mbar_arrive_relaxed(&tempty[acc]);
+      __syncwarp();  // every lane's TMEM loads are complete: one arrival per warp
+      if (lane == 0) {
+        if (CG == 2 && !leader) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+        else mbar_arrive_relaxed(&tempty[acc]);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
