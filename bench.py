@@ -446,8 +446,24 @@ def tensor_peak(ctx, w, kind="bf16_tflops"):
     return p * (2.0 if quant_kind(w) else 1.0)
 
 
+def fp32_alu_peak(ctx):
+    """fp32 FMA peak derived from unit counts and clocks: SMs x 128 FMA lanes per clock x 2
+    flops x the maximum SM clock (the fp32 grouped GEMM runs on the SIMT pipes)."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = ctx.peaks.get("sm_max_mhz", 2070.0)
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 fp32 FMA/clk x 2 flops x {mhz:.0f} MHz"
+
+
 def gemm_roofline(ctx, w, gemm_ms, alg):
     achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+    if w["act_dtype"] == synth.F32:
+        peak, kind = fp32_alu_peak(ctx)
+        return {"kernel": "SIMT fp32 grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
+                "bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1), "peak_kind": kind,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "timing": "CUDA events around moe_grouped_mlp on the launching stream, median of the stage loop",
+                **gemm_traffic(w)}
     peak = tensor_peak(ctx, w)
     sus = tensor_peak(ctx, w, "bf16_tflops_sustained")
     return {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
