@@ -804,9 +804,13 @@ def set_gpu_local_affinity(dev):
 
 
 def launches_per_forward(w):
-    # router logits, top-k, the scan (one launch up to 512 tokens, else three passes),
-    # dispatch, 2 grouped GEMMs, combine
-    return 7 if w["T"] <= 512 else 9
+    # router logits, the routing (the library reports its launch count: one cooperative
+    # launch, or the top-k launch and the scan), dispatch, 2 grouped GEMMs, combine
+    import token_routing_expert_router_gb300 as moe
+    cfg = moe.MoEConfig.make(**{kk: w[kk] for kk in (
+        "T", "H", "E", "k", "F", "n_shared", "F_shared", "score_fn", "renorm", "n_groups",
+        "topk_groups", "group_score", "routed_scale", "act_dtype", "xfer_dtype")})
+    return 1 + moe.moe_route_launch_count(cfg) + 1 + 2 + 1
 
 
 def cpu_baseline(w, n_tokens, seed=0):

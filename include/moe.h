@@ -146,7 +146,8 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
  * intermediate of the layer (logits, routing map, permutation, dispatched rows, h, yd). */
 moe_status_t moe_forward_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
-/* Clears the status word of a workspace (stream-ordered). Call once after allocating. */
+/* Clears the head of a workspace (its status word and the routing kernel's grid barrier;
+ * stream-ordered). Call once after allocating, and again after a failed call. */
 moe_status_t moe_workspace_init(void* ws, moe_stream_t stream);
 
 /* S0 — router logits (Megatron-Core summary, "O essencial": the router scores each token
@@ -168,10 +169,21 @@ moe_status_t moe_router_logits(const moe_config_t* cfg, const void* x, const voi
  *            [offsets[e], offsets[e+1]) in ascending token id;
  *   tok_row [T,k]: the row holding token t's j-th choice.
  * Bit-exact and deterministic (no atomics whose order shows in the result).
- * A non-finite logit sets MOE_ERR_DEVICE_BAD_INPUT in the status word. */
+ * A non-finite logit sets MOE_ERR_DEVICE_BAD_INPUT in the status word.
+ * One cooperative launch (every block resident at once) routes contiguous token chunks,
+ * publishes their per-expert counts in the workspace and, after a grid barrier kept in the
+ * workspace head, writes the map. The barrier's wait is bounded: if it gives up,
+ * MOE_ERR_TIMEOUT is set and the map is left empty (counts and offsets zero, tok_row 0). */
 moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* topk_idx,
                        float* topk_w, int32_t* counts, int32_t* offsets, int32_t* row_token,
                        int32_t* tok_row, void* ws, moe_stream_t stream);
+
+/* The number of kernel launches moe_route makes for this configuration (0 when T = 0): 1
+ * for the cooperative launch, else the top-k launch and the scan (one launch up to 512
+ * tokens, else three). The cooperative launch is taken where a block's token chunk times
+ * ceil(E / 32) is at most 256, which depends on the device's occupancy for the kernel
+ * (queried here on first use of a shape). Launches nothing. */
+moe_status_t moe_route_launch_count(const moe_config_t* cfg, int32_t* launches);
 
 /* S2 only, from a given routing map (router replay, Megatron-Core summary section 2.5).
  * An id outside [0,E) sets MOE_ERR_DEVICE_BAD_INPUT; that entry is then counted for
@@ -416,8 +428,9 @@ moe_status_t moe_quantize_mx(const void* src_bf16, int64_t rows, int64_t cols, u
                              uint8_t* sf, moe_stream_t stream);
 
 /* moe_route for callers that cannot allocate device memory. The paper has no counterpart:
- * this is a library convenience. It computes exactly what moe_route computes (same kernels,
- * same bits) but takes no workspace: the routing scan's scratch lives in a fixed array
+ * this is a library convenience. It computes exactly what moe_route computes (the same
+ * per-token routing code and the same map, bit for bit; here a top-k launch and the scan
+ * passes instead of moe_route's single cooperative launch) but takes no workspace: the routing scan's scratch lives in a fixed array
  * inside the library (1 MiB of device memory per GPU that loads the library, held until
  * the process exits). It is meant for callers that are handed only their inputs and
  * outputs (a plugin inside a host framework), that run on a fixed memory budget reserved

@@ -159,3 +159,15 @@ def test_aux_loss_against_oracle(w):
     loss2 = torch.zeros(1, dtype=torch.float32, device="cuda")
     moe.moe_aux_loss(b["cfg"], up(l), up(counts), 0.01, loss2, b["ws"])
     assert torch.equal(loss, loss2)  # deterministic
+
+
+def test_both_routing_paths_are_exercised():
+    """moe_route takes one cooperative launch where a block's token chunk times ceil(E / 32)
+    stays within 256, else the top-k launch and the scan passes. The bit-exact cases above
+    cover both: the Mixtral-sized routing takes the single launch, the DeepSeek-V3-sized one
+    (256 grouped experts) the top-k launch and the three scan passes."""
+    n = {w["name"]: moe.moe_route_launch_count(cfg_of(w)) for w in CASES}
+    assert n["mixtral"] == 1 and n["tiny"] == 1
+    assert n["dsv3"] == 4 and n["dsv3_fp8_tokens"] == 4
+    assert set(n.values()) <= {1, 2, 4}
+    assert moe.moe_route_launch_count(cfg_of(synth.scaled(CASES[0], T=0))) == 0

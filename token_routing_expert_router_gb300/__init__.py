@@ -103,6 +103,7 @@ def lib():
             "moe_router_logits": [cfg, P, P, P, P, P, P],
             "moe_route": [cfg, P, P, P, P, P, P, P, P, P],
             "moe_route_from_map": [cfg, P, P, P, P, P, P, P],
+            "moe_route_launch_count": [cfg, POINTER(c_int32)],
             "moe_aux_loss": [cfg, P, P, ctypes.c_float, P, P, P],
             "moe_dispatch": [cfg, P, P, P, P, P],
             "moe_dispatch_mx": [cfg, P, P, P, P, P, P, P],
@@ -140,7 +141,8 @@ def lib():
 
 def exported_symbols() -> list:
     return ["moe_workspace_size", "moe_forward_workspace_size", "moe_workspace_init",
-            "moe_router_logits", "moe_route", "moe_route_from_map", "moe_aux_loss", "moe_dispatch",
+            "moe_router_logits", "moe_route", "moe_route_launch_count", "moe_route_from_map", "moe_aux_loss",
+            "moe_dispatch",
             "moe_grouped_mlp", "moe_grouped_mlp_gather", "moe_combine", "moe_forward", "moe_forward_host",
             "moe_quantize_e4m3",
             "moe_dispatch_mx", "moe_mx_scale_bytes", "moe_quantize_mx",
@@ -193,6 +195,12 @@ def moe_status_string(code: int) -> str:
 def moe_workspace_size(cfg: MoEConfig) -> int:
     n = c_size_t()
     _check(lib().moe_workspace_size(byref(cfg), byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_route_launch_count(cfg: MoEConfig) -> int:
+    n = c_int32()
+    _check(lib().moe_route_launch_count(byref(cfg), byref(n)), "moe_route_launch_count")
     return n.value
 
 

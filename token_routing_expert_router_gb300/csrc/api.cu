@@ -51,11 +51,28 @@ moe_status_t empty_routing(const moe_config_t& c, int32_t* counts, int32_t* offs
   return cuda_status(e);
 }
 
+// Workspace head: the status word at byte 0, the fused routing kernel's grid barrier
+// (counter, flag) at byte 16; then the routing scratch (per-block expert counts).
 DeviceStatus* status_of(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); }
+uint32_t* barrier_of(void* ws) { return reinterpret_cast<uint32_t*>((char*)ws + 16); }
 int32_t* blockcnt_of(void* ws) { return reinterpret_cast<int32_t*>((char*)ws + kWsHead); }
 
 size_t route_ws_bytes(const moe_config_t& c) {
-  return kWsHead + align_up((size_t)scan_blocks(c) * c.E * sizeof(int32_t), 256);
+  const size_t blocks = std::max<size_t>((size_t)scan_blocks(c), (size_t)kFusedMaxRouteBlocks);
+  return kWsHead + align_up(blocks * c.E * sizeof(int32_t), 256);
+}
+
+// S1 + S2: one cooperative launch where it applies, else the top-k and scan passes.
+cudaError_t route_and_permute(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
+                              int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* tok_row, void* ws,
+                              cudaStream_t s) {
+  if (route_fused_supported(c))
+    return launch_route_fused(c, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, blockcnt_of(ws),
+                              barrier_of(ws), status_of(ws), s);
+  cudaError_t e = launch_route_topk(c, logits, topk_idx, topk_w, status_of(ws), s);
+  if (e == cudaSuccess)
+    e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws), status_of(ws), s);
+  return e;
 }
 
 size_t act_size(const moe_config_t& c) { return c.act_dtype == MOE_DTYPE_BF16 ? 2 : 4; }
@@ -291,7 +308,7 @@ moe_status_t moe_forward_workspace_size(const moe_config_t* cfg, size_t* bytes) 
 
 moe_status_t moe_workspace_init(void* ws, moe_stream_t stream) {
   if (!ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws, 0, kWsHead, (cudaStream_t)stream));
 }
 
 moe_status_t moe_router_logits(const moe_config_t* cfg, const void* x, const void* w_router,
@@ -315,12 +332,17 @@ moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* to
   if (!ptr_ok(logits) || !ptr_ok(topk_idx) || !ptr_ok(topk_w) || !ptr_ok(counts) ||
       !ptr_ok(offsets) || !ptr_ok(row_token) || !ptr_ok(tok_row) || !ptr_ok(ws))
     return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_route_topk(*cfg, logits, topk_idx, topk_w, status_of(ws), s);
-  if (e == cudaSuccess)
-    e = launch_route_scan(*cfg, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
-                          status_of(ws), s);
-  return cuda_status(e);
+  return cuda_status(route_and_permute(*cfg, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, ws,
+                                       (cudaStream_t)stream));
+}
+
+moe_status_t moe_route_launch_count(const moe_config_t* cfg, int32_t* launches) {
+  moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!launches) return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = *cfg;
+  *launches = c.T == 0 ? 0 : route_fused_supported(c) ? 1 : (c.T <= 512 ? 2 : 4);
+  return MOE_OK;
 }
 
 moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx,
@@ -459,10 +481,7 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weig
   void* yd = base + L.yd;
 
   cudaError_t e = router_logits(c, x, w->w_router, w->router_bias, logits, status_of(ws), s);
-  if (e == cudaSuccess) e = launch_route_topk(c, logits, topk_idx, topk_w, status_of(ws), s);
-  if (e == cudaSuccess)
-    e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws),
-                          status_of(ws), s);
+  if (e == cudaSuccess) e = route_and_permute(c, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, ws, s);
   if (e == cudaSuccess && aux_loss_out)  // the scan's scratch is free again: it holds the partials
     e = launch_aux_loss(c, logits, counts, aux_alpha, aux_loss_out, reinterpret_cast<float*>(blockcnt_of(ws)), s);
   if (e == cudaSuccess)

@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
@@ -74,16 +75,15 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// One warp per token. Lane l holds experts l, l+32, l+64, ... (NSLOT slots).
+// S1 for one token t, by one warp: lane l holds experts l, l+32, l+64, ... (NSLOT slots).
+// Writes the token's k expert ids and weights and returns, in lane j < k, the token's j-th
+// expert. sc: this warp's E floats of shared memory (group-limited routing only).
 template <int NSLOT>
-__global__ void __launch_bounds__(256) route_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G,
-    int g_keep, int group_score, float rho, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, DeviceStatus* st) {
-  extern __shared__ float s_score[];  // [warps][E] sigmoid scores (group-limited only)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
+__device__ __forceinline__ int route_token(const float* __restrict__ logits, int t, int E, int k, int score_fn,
+                                           int renorm, int G, int g_keep, int group_score, float rho,
+                                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* sc,
+                                           DeviceStatus* st) {
+  const int lane = threadIdx.x & 31;
   const float* row = logits + (int64_t)t * E;
 
   float v[NSLOT];
@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
 
   uint32_t allowed = ok;
   if (G > 1 && g_keep < G) {
-    float* sc = s_score + (size_t)warp * E;
 #pragma unroll
     for (int s = 0; s < NSLOT; ++s)
       if (ok >> s & 1) sc[s * 32 + lane] = det_sigmoid(v[s]);
@@ -124,6 +123,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
       gkey = (group_score == MOE_GROUP_SCORE_TOP2_SUM && gs >= 2) ? __fadd_rn(m1, m2) : m1;
       gidx = lane;
     }
+    __syncwarp();  // the scores are read before the warp's next token overwrites them
     uint32_t keep = 0;
     for (int r = 0; r < g_keep; ++r) {
       float bk = gkey;
@@ -181,6 +181,21 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
     topk_idx[(int64_t)t * k + lane] = my_idx;
     topk_w[(int64_t)t * k + lane] = w * rho;
   }
+  return my_idx;
+}
+
+// One warp per token.
+template <int NSLOT>
+__global__ void __launch_bounds__(256) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G,
+    int g_keep, int group_score, float rho, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, DeviceStatus* st) {
+  extern __shared__ float s_score[];  // [warps][E] sigmoid scores (group-limited only)
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  route_token<NSLOT>(logits, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx, topk_w,
+                     s_score + (size_t)warp * E, st);
 }
 
 // S2 pass 1: per block of kScanChunk tokens, the count of entries per expert.
@@ -428,6 +443,192 @@ __global__ void __launch_bounds__(1024) scan_small_kernel(const int32_t* __restr
         const uint32_t m = mask[ej];
         if (m && 31 - __clz(m) == lane) {  // the highest lane closes expert ej's batch
           counter[ej] += __popc(m);
+          mask[ej] = 0;
+        }
+      }
+    __syncwarp();
+  }
+}
+
+// S1 + S2 in one cooperative launch (every block resident at once):
+//   1. block b routes the contiguous chunk of tokens [b C, (b + 1) C) (C = ceil(T / grid)),
+//      warp w the tokens w, w + 16, ... of it, with route_token (the same ids and weights,
+//      bit for bit, as route_topk_kernel), and counts its chunk's entries per expert;
+//   2. a grid barrier after the counts are published ([grid][E] in the workspace);
+//   3. every block reads all blocks' counts: the totals give counts and offsets (block 0
+//      writes them), the blocks before it give its chunk's first row per expert, and warp 0
+//      walks the chunk's tokens in ascending order 32 at a time with the lane-mask ranks of
+//      scan_assign_kernel. The map is the stable order by expert, then token, as before.
+// The barrier is a sense-reversing one in the workspace head (counter, flag); its waits are
+// bounded, and a block that gives up sets MOE_ERR_TIMEOUT and writes no map entries.
+constexpr int kFusedWarps = 16;
+constexpr int kFusedMaxBlocks = kFusedMaxRouteBlocks;
+
+__device__ __forceinline__ bool fused_grid_barrier(uint32_t* bar, uint32_t nblocks, uint64_t timeout_ns,
+                                                   DeviceStatus* st) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile uint32_t* flag = bar + 1;
+    const uint32_t f0 = *flag;  // read before arriving: the last arrival flips it
+    __threadfence();            // this block's counts are visible before its arrival
+    const uint32_t arrived = atomicAdd(&bar[0], 1u);
+    int ok = 1;
+    if (arrived == nblocks - 1) {
+      atomicExch(&bar[0], 0u);  // ready for the next launch
+      __threadfence();
+      atomicExch(&bar[1], f0 ^ 1u);
+    } else {
+      const uint64_t t0 = tc::globaltimer_ns();
+      while (*flag == f0) {
+        if (tc::globaltimer_ns() - t0 > timeout_ns) {
+          set_status(st, MOE_ERR_TIMEOUT, -1);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+template <int NSLOT>
+__global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G, int g_keep,
+    int group_score, float rho, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+    int32_t* __restrict__ tok_row, int32_t* __restrict__ blockcnt, uint32_t* bar, uint64_t timeout_ns,
+    DeviceStatus* st) {
+  extern __shared__ int32_t fsm[];
+  int32_t* hist = fsm;                                         // [E] this chunk's entries
+  int32_t* base = fsm + E;                                     // [E] the chunk's next row
+  uint32_t* mask = reinterpret_cast<uint32_t*>(fsm + 2 * E);   // [E]
+  float* s_score = reinterpret_cast<float*>(fsm + 3 * E);      // [warps][E] (group-limited)
+  __shared__ int32_t warp_tot[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = (T + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int t0 = (int)blockIdx.x * C, t1 = min(T, t0 + C);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    hist[e] = 0;
+    mask[e] = 0;
+  }
+  __syncthreads();
+  // ---- 1. route the chunk; count its entries per expert
+  for (int t = t0 + warp; t < t1; t += kFusedWarps) {
+    int my = route_token<NSLOT>(logits, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx,
+                                topk_w, s_score + (size_t)warp * E, st);
+    if (lane < k) {
+      if (my < 0 || my >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); my = 0; }  // as the scan passes
+      atomicAdd(&hist[my], 1);  // a count: the order of the adds does not show
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
+  // ---- 2. every block's counts are published
+  if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
+    // the map stays in bounds for the launches that read it: no routed rows, and this
+    // chunk's entries pointing at row 0 (the status word reports the failure)
+    for (int i = t0 * k + (int)threadIdx.x; i < t1 * k; i += blockDim.x) tok_row[i] = 0;
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+        offsets[i] = 0;
+        if (i < E) counts[i] = 0;
+      }
+    return;
+  }
+  // ---- 3. totals, offsets and this chunk's first row per expert (E <= blockDim). P
+  // consecutive threads per expert (a power of two) each add every P-th block's count.
+  {
+    int P = 1;
+    while (P < 32 && 2 * P * E <= (int)blockDim.x) P *= 2;
+    const int ex = threadIdx.x / P, q = threadIdx.x % P;
+    int32_t tot = 0, before = 0;
+    if (ex < E) {
+#pragma unroll 4
+      for (int b = q; b < (int)gridDim.x; b += P) {
+        const int32_t c = __ldcg(blockcnt + (int64_t)b * E + ex);
+        tot += c;
+        if (b < (int)blockIdx.x) before += c;
+      }
+    }
+    for (int off = 1; off < P; off <<= 1) {  // within aligned groups of P lanes
+      tot += __shfl_xor_sync(kFull, tot, off);
+      before += __shfl_xor_sync(kFull, before, off);
+    }
+    __syncthreads();  // hist and base are free: the counts were published, nothing read them since
+    if (ex < E && q == 0) {
+      hist[ex] = tot;
+      base[ex] = before;
+    }
+    __syncthreads();
+  }
+  const int e = threadIdx.x;
+  const int32_t tot = e < E ? hist[e] : 0, before = e < E ? base[e] : 0;
+  int32_t inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t wv = lane < kFusedWarps ? warp_tot[lane] : 0;
+    int32_t wi = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(kFull, wi, off);
+      if (lane >= off) wi += o;
+    }
+    if (lane < kFusedWarps) warp_tot[lane] = wi - wv;
+  }
+  __syncthreads();
+  const int32_t excl = warp_tot[warp] + inc - tot;
+  if (e < E) {
+    base[e] = excl + before;
+    if (blockIdx.x == 0) {
+      counts[e] = tot;
+      offsets[e] = excl;
+      if (e == E - 1) offsets[E] = excl + tot;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // ---- the chunk's rows, tokens in ascending order (the ids were written by this block)
+  const int64_t R = (int64_t)T * k;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int tb = t0; tb < t1; tb += 32) {
+    const int t = tb + lane;
+    const bool valid = t < t1;
+    const int32_t* ids = topk_idx + (int64_t)t * k;
+    auto id_of = [&](int j) {
+      const int ej = ids[j];
+      return (ej < 0 || ej >= E) ? 0 : ej;  // counted for expert 0 above (status set)
+    };
+    if (valid)
+      for (int j = 0; j < k; ++j) atomicOr(&mask[id_of(j)], 1u << lane);
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        const int ej = id_of(j);
+        const int64_t r = base[ej] + __popc(mask[ej] & below);
+        if (r >= 0 && r < R) {
+          row_token[r] = t;
+          tok_row[(int64_t)t * k + j] = (int32_t)r;
+        } else {
+          set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t);
+        }
+      }
+    __syncwarp();
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        const int ej = id_of(j);
+        const uint32_t m = mask[ej];
+        if (m && 31 - __clz(m) == lane) {  // the highest lane closes expert ej's batch
+          base[ej] += __popc(m);
           mask[ej] = 0;
         }
       }
@@ -738,6 +939,96 @@ cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_
   MOE_ROUTE_CASE(16)
 #undef MOE_ROUTE_CASE
   return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// The fused kernel's instance, its shared memory and its grid for a configuration.
+struct FusedPlan {
+  const void* kern = nullptr;
+  size_t smem = 0;
+  int64_t grid = 0;
+};
+
+template <int NS>
+const void* fused_kernel_ptr() { return reinterpret_cast<const void*>(&route_fused_kernel<NS>); }
+
+FusedPlan fused_plan(const moe_config_t& c) {
+  FusedPlan f;
+  const int nslot = (int)ceil_div(c.E, 32);
+  f.kern = nslot <= 1 ? fused_kernel_ptr<1>() : nslot <= 2 ? fused_kernel_ptr<2>() : nslot <= 4 ? fused_kernel_ptr<4>()
+         : nslot <= 8 ? fused_kernel_ptr<8>() : nslot <= 16 ? fused_kernel_ptr<16>() : nullptr;
+  if (!f.kern) return f;
+  const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
+  f.smem = (size_t)3 * c.E * sizeof(int32_t) + (grouped ? (size_t)kFusedWarps * c.E * sizeof(float) : 0);
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  static const void* last_kern = nullptr;  // occupancy of the last (instance, shared memory) asked
+  static size_t last_smem = 0;
+  static int last_per_sm = 0;
+  if (f.kern != last_kern || f.smem != last_smem) {
+    if (f.smem > 48 * 1024 &&
+        cudaFuncSetAttribute(f.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f.smem) != cudaSuccess)
+      return f;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f.kern, 32 * kFusedWarps, f.smem) != cudaSuccess)
+      return f;
+    last_kern = f.kern;
+    last_smem = f.smem;
+    last_per_sm = per_sm;
+  }
+  if (last_per_sm <= 0) return f;
+  // every block resident at once (the grid barrier), at most one block per 16 tokens, and
+  // grid * E <= 32768: after the barrier each block reads all blocks' counts
+  f.grid = std::max<int64_t>(
+      1, std::min<int64_t>(std::min<int64_t>(std::min<int64_t>((int64_t)last_per_sm * sms, kFusedMaxBlocks),
+                                             ceil_div(c.T, kFusedWarps)),
+                           32768 / c.E));
+  return f;
+}
+
+}  // namespace
+
+// The fused launch where its top-k phase stays short: a warp routes its block's chunk of
+// tokens one after another, at a cost per token that grows with E / 32 (the slots a lane
+// holds), so the chunk times the slots is kept to at most 256. Longer chunks (e.g. the
+// DeepSeek-V3 shape's 256 grouped experts) keep the top-k and scan passes.
+bool route_fused_supported(const moe_config_t& c) {
+  if (c.T <= 0 || c.E > 32 * kFusedWarps || c.k > 32) return false;
+  const FusedPlan f = fused_plan(c);
+  if (f.grid <= 0) return false;
+  return ceil_div(c.T, f.grid) * ceil_div(c.E, 32) <= 256;
+}
+
+cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* tok_row,
+                               int32_t* blockcnt, uint32_t* barrier, DeviceStatus* st, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const FusedPlan f = fused_plan(c);
+  if (f.grid <= 0) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)f.grid);
+  cfg.blockDim = dim3(32 * kFusedWarps);
+  cfg.dynamicSmemBytes = f.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint64_t timeout = 2000000000ull;
+  void* args[] = {(void*)&logits,  (void*)&c.T,           (void*)&c.E,          (void*)&c.k,
+                  (void*)&c.score_fn, (void*)&c.renorm,   (void*)&c.n_groups,   (void*)&c.topk_groups,
+                  (void*)&c.group_score, (void*)&c.routed_scale, (void*)&topk_idx, (void*)&topk_w,
+                  (void*)&counts,  (void*)&offsets,       (void*)&row_token,    (void*)&tok_row,
+                  (void*)&blockcnt, (void*)&barrier,      (void*)&timeout,      (void*)&st};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, f.kern, args);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
