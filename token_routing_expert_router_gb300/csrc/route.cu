@@ -727,6 +727,83 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   }
 }
 
+// S0 on the tensor cores for bf16 x with E <= 32 experts (HBM-bound: x is read once):
+// mma.sync m16n8k16 (bf16 x bf16 -> fp32). A block takes 16 tokens; its 8 warps split H, warp
+// w taking [w H / 8, (w + 1) H / 8) in steps of 32. In a step, thread (g = lane / 4,
+// q = lane % 4) loads 16 contiguous bytes (8 bf16 at k0 + 8 q) of token rows g and g + 8
+// and of expert row nt * 8 + g for each of the NT 8-expert tiles. The step's two MMAs take
+// those as a fixed permutation of the 32 K positions (the same for x and W, so each product
+// x[t, k] W[e, k] is formed once): the first MMA's K slots 2q, 2q + 1 hold k0 + 8q + {0, 1}
+// and slots 2q + 8, 2q + 9 hold k0 + 8q + {2, 3}; the second MMA the same with + 4. The 8
+// warps' fp32 partial logits are added in warp order through shared memory, then the bias.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256) router_hmma_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
+                                                          const float* __restrict__ bias, int T, int H, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ float red[8][16][8 * NT];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int t0 = blockIdx.x * 16;
+  const int row_chunks = H / 8;  // 16-byte chunks of a row
+  const int ta = min(t0 + g, T - 1), tb = min(t0 + g + 8, T - 1);  // past T: a repeated row, not stored
+  const uint4* xa = x + (int64_t)ta * row_chunks + q;
+  const uint4* xb = x + (int64_t)tb * row_chunks + q;
+  const uint4* wr[NT];
+  bool wok[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int e = nt * 8 + g;
+    wok[nt] = e < E;
+    wr[nt] = w + (int64_t)(wok[nt] ? e : 0) * row_chunks + q;
+  }
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+  const int steps = H / 256;  // 32-wide K steps of this warp
+  const int c0 = warp * steps * 4;  // this warp's first chunk (4 chunks a step)
+#pragma unroll 4
+  for (int st = 0; st < steps; ++st) {
+    const int c = c0 + st * 4;
+    const uint4 va = __ldg(xa + c), vb = __ldg(xb + c);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 vw = wok[nt] ? __ldg(wr[nt] + c) : make_uint4(0, 0, 0, 0);
+      mma_bf16_16816(acc[nt], va.x, vb.x, va.y, vb.y, vw.x, vw.y);
+      mma_bf16_16816(acc[nt], va.z, vb.z, va.w, vb.w, vw.z, vw.w);
+    }
+  }
+  // D fragment: (token g, expert nt * 8 + 2q + {0, 1}) and (token g + 8, the same experts)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][g][nt * 8 + 2 * q] = acc[nt][0];
+    red[warp][g][nt * 8 + 2 * q + 1] = acc[nt][1];
+    red[warp][g + 8][nt * 8 + 2 * q] = acc[nt][2];
+    red[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 16 * 8 * NT; i += blockDim.x) {
+    const int tl = i / (8 * NT), e = i % (8 * NT);
+    const int t = t0 + tl;
+    if (t < T && e < E) {
+      float v = 0.0f;
+#pragma unroll
+      for (int wp = 0; wp < 8; ++wp) v += red[wp][tl][e];
+      logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
+    }
+  }
+}
+
 template <int EP, int CPT>
 __global__ void __launch_bounds__(256) router_stream_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
                                                             const float* __restrict__ bias, int T, int E,
@@ -887,6 +964,19 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
+  // bf16 rows of a multiple of 256: the tensor-core form, 16 tokens a block
+  if (bf && c.H % 256 == 0) {
+    const unsigned blocks = (unsigned)ceil_div(c.T, 16);
+    const uint4* xv = static_cast<const uint4*>(x);
+    const uint4* wv = static_cast<const uint4*>(w);
+#define MOE_RH(NT) \
+  if (c.E <= 8 * NT) { \
+    router_hmma_kernel<NT><<<blocks, 256, 0, s>>>(xv, wv, bias, c.T, c.H, c.E, logits); \
+    return cudaGetLastError(); \
+  }
+    MOE_RH(1) MOE_RH(2) MOE_RH(3) MOE_RH(4)
+#undef MOE_RH
+  }
   // streamed form, one block per SM, for the shapes whose weight slice fits in registers
   // without spilling (E <= 8 with H of 2048 or 4096; E <= 16 with H of 2048)
   if (bf && ((c.E <= 8 && (c.H == 2048 || c.H == 4096)) || (c.E <= 16 && c.H == 2048))) {
