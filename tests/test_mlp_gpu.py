@@ -16,6 +16,10 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS
 CASES = [
     synth.scaled(W["tiny_fp32"], name="tiny_fp32"),
+    # fp32 layers through the SIMT GEMMs: with a shared expert, and with F = 600 (a ragged last
+    # N tile of the gate/up GEMM and a ragged last K step of the down projection)
+    synth.scaled(W["tiny_fp32"], T=130, H=64, E=4, F=128, n_shared=1, F_shared=128, name="tiny_fp32_shared"),
+    synth.scaled(W["tiny_fp32"], T=200, H=128, F=600, name="tiny_fp32_ragged_f"),
     synth.scaled(W["mixtral_bf16"], T=600, H=512, F=384, name="mixtral_small"),
     synth.scaled(W["dsv3_bf16"], T=260, H=512, E=32, F=256, F_shared=256, name="dsv3_small"),
     synth.scaled(W["imbalanced_bf16"], T=700, H=256, E=32, k=4, F=384, name="imbalanced_small"),
@@ -134,7 +138,10 @@ def test_pair_segment_tails_against_oracle(w, counts):
         assert oracle.rel_l2(got[R + T - tail:], ref[-tail:]) < 1e-2
 
 
-@pytest.mark.parametrize("w", CASES[:4], ids=[c["name"] for c in CASES[:4]])
+ROUTER_CASES = [c for c in CASES if c["name"] in ("tiny_fp32", "mixtral_small", "dsv3_small", "imbalanced_small")]
+
+
+@pytest.mark.parametrize("w", ROUTER_CASES, ids=[c["name"] for c in ROUTER_CASES])
 def test_router_logits_against_oracle(w):
     inp = synth.host_inputs(w, seed=6, with_weights=False)
     d = device_weights_from_host(w, inp)
