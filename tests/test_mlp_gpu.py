@@ -152,7 +152,9 @@ def test_router_logits_against_oracle(w):
 
 
 @pytest.mark.parametrize("name,T,H,E", [("dsv3_router", 1000, 7168, 256), ("imb_router", 2000, 2048, 128),
-                                        ("mixtral_router", 700, 4096, 8)])
+                                        ("mixtral_router", 700, 4096, 8),
+                                        # >= one 128-token tile per SM: 256-wide N tiles, ragged last tile
+                                        ("dsv3_router_wide", 20000, 2048, 256)])
 def test_router_logits_real_widths(name, T, H, E):
     w = synth.workload(name, T, H, E, 2, 128)
     inp = synth.host_inputs(w, seed=7, with_weights=False)

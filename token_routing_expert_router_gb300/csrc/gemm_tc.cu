@@ -709,9 +709,13 @@ bool mlp_supported(const moe_config_t& c) {
 
 cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_router, const float* bias,
                           float* logits, DeviceStatus* st, cudaStream_t s) {
-  // 128-wide N tiles: E / 128 tiles per 128 tokens, so small T still spreads over the SMs
+  // 128-wide N tiles (E / 128 tiles per 128 tokens) so that small T still spreads over the
+  // SMs; with 256 experts and at least one 128-token tile per SM, one 256-wide N tile per
+  // 128 tokens instead, which reads each token row once and halves the loads per flop
+  const bool wide = c.E == 256 && ceil_div(c.T, BM) >= num_sms();
+  const int bn = wide ? 256 : 128;
   CUtensorMap ta, tb;
-  if (!make_bf16(&ta, x, c.T, c.H, BM) || !make_bf16(&tb, w_router, c.E, c.H, 128)) return cudaErrorInvalidValue;
+  if (!make_bf16(&ta, x, c.T, c.H, BM) || !make_bf16(&tb, w_router, c.E, c.H, bn)) return cudaErrorInvalidValue;
   TcParams p{};
   p.G = 0;
   p.has_extra = 1;
@@ -719,7 +723,7 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
   p.a2_row_base = 0;
   p.out_extra_base = 0;
   p.K = c.H;
-  p.n_tiles = c.E / 128;
+  p.n_tiles = c.E / bn;
   p.b_group_rows = 0;
   p.ldc = c.E;
   p.out = logits;
@@ -727,7 +731,8 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* w_ro
   p.timeout_ns = kTimeoutNs;
   p.status = st;
   const int64_t tiles = ceil_div(c.T, BM) * p.n_tiles;
-  return launch<128, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
+  return wide ? launch<256, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s)
+              : launch<128, EPI_STORE_F32_BIAS>(ta, ta, tb, tb, tb, tb, p, tiles, s);
 }
 
 cudaError_t launch_grouped_mlp(const moe_config_t& c, const void* xd, const float* xd_scale, const void* x,
