@@ -20,6 +20,8 @@ CASES = [
     # N tile of the gate/up GEMM and a ragged last K step of the down projection)
     synth.scaled(W["tiny_fp32"], T=130, H=64, E=4, F=128, n_shared=1, F_shared=128, name="tiny_fp32_shared"),
     synth.scaled(W["tiny_fp32"], T=200, H=128, F=600, name="tiny_fp32_ragged_f"),
+    # the narrowest rows the layer takes (H = 8: K = 8 in GEMM1, 8 output columns in GEMM2)
+    synth.scaled(W["tiny_fp32"], T=70, H=8, E=4, F=24, name="tiny_fp32_narrow"),
     synth.scaled(W["mixtral_bf16"], T=600, H=512, F=384, name="mixtral_small"),
     synth.scaled(W["dsv3_bf16"], T=260, H=512, E=32, F=256, F_shared=256, name="dsv3_small"),
     synth.scaled(W["imbalanced_bf16"], T=700, H=256, E=32, k=4, F=384, name="imbalanced_small"),
@@ -178,6 +180,22 @@ def test_router_logits_small_e_streamed_shapes(T, H, E):
     bias = synth.zipf_bias(9, E)
     b = alloc(w)
     moe.moe_router_logits(b["cfg"], up(x, torch.bfloat16), up(wr, torch.bfloat16), up(bias), b["logits"], b["ws"])
+    assert np.array_equal(np_of(b["logits"]), oracle.router_logits(x, wr, bias))
+
+
+@pytest.mark.parametrize("T,H,E", [(100, 128, 48), (37, 8, 40), (300, 256, 64), (200, 248, 33), (90, 264, 48)])
+def test_router_logits_fp32_simt_exact(T, H, E):
+    """The fp32 router for more than 32 experts (SIMT): the small-problem form, which holds
+    a tile's whole K in shared memory (K a multiple of 4 up to 256; here 8, 128, 248 and 256),
+    and the 64 x 64 form (K = 264); ragged token tiles and expert columns, a bias. On the
+    exact-sum grids every logit equals the oracle's bit for bit."""
+    w = synth.workload("simt_router", T, H, E, 2, 128, act=synth.F32)
+    inp = synth.host_inputs(w, seed=10, with_weights=False)
+    x, wr = grid_x(inp["x"]), grid_w_router(inp["w_router"])
+    assert_exact_router_sums(x, wr)
+    bias = synth.zipf_bias(10, E)
+    b = alloc(w)
+    moe.moe_router_logits(b["cfg"], up(x), up(wr), up(bias), b["logits"], b["ws"])
     assert np.array_equal(np_of(b["logits"]), oracle.router_logits(x, wr, bias))
 
 
