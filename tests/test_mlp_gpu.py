@@ -168,12 +168,15 @@ def test_router_logits_real_widths(name, T, H, E):
 
 
 @pytest.mark.parametrize("T,H,E", [(701, 2048, 5), (4096, 4096, 8), (333, 2048, 12), (130, 2048, 16),
-                                   (1, 4096, 8), (3, 2048, 16)])
-def test_router_logits_small_e_streamed_shapes(T, H, E):
-    """The small-expert router's streamed form (bf16, E <= 8 with H of 2048 or 4096, E <= 16
-    with H = 2048): ragged last token groups, E below the kernel's width, a bias. On the
-    exact-sum grids every logit equals the oracle's bit for bit, whatever the summation order."""
-    w = synth.workload("stream_router", T, H, E, 2, 128)
+                                   (1, 4096, 8), (3, 2048, 16), (257, 768, 24), (64, 1280, 32),
+                                   (100, 7168, 8)])
+def test_router_logits_small_e_tensor_core_shapes(T, H, E):
+    """The small-expert router on the tensor cores (bf16, E <= 32, H a multiple of 256):
+    ragged last 16-token tiles, E below each 8-expert tile's width (1 to 4 tiles), a bias,
+    and H whose 32-wide K steps do not split evenly over the 16 warps (768, 1280: some warps
+    get no steps) or do (7168). On the exact-sum grids every logit equals the oracle's bit for
+    bit, whatever the summation order."""
+    w = synth.workload("tc_router", T, H, E, 2, 128)
     inp = synth.host_inputs(w, seed=9, with_weights=False)
     x, wr = grid_x(inp["x"]), grid_w_router(inp["w_router"])
     assert_exact_router_sums(x, wr)

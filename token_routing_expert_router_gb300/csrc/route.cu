@@ -711,31 +711,18 @@ __global__ void __launch_bounds__(256) router_small_kernel(const void* __restric
   }
 }
 
-// S0 for bf16 layers with E <= EP <= 16 experts and H = 2048 * CPT: x streamed once with
-// many loads in flight, the router weights held in registers. Thread i of a block owns the
-// 16-byte chunks c = i + 256 j (j < CPT) of every row, and keeps W[e][c] for all e. The
-// block walks groups of TB = 32 / EP tokens (groups b, b + gridDim.x, ...; the next group's
-// rows are loaded while the current one is reduced); each thread forms the group's TB x EP
-// partial dot products, a warp reduce-scatter (31 shuffles) leaves lane l with the warp's
-// sum of product l, and 32 threads add the 8 warps' sums in order. fp32 accumulation.
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    f[2 * q] = __uint_as_float(u[q] << 16);
-    f[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
-  }
-}
-
 // S0 on the tensor cores for bf16 x with E <= 32 experts (HBM-bound: x is read once):
-// mma.sync m16n8k16 (bf16 x bf16 -> fp32). A block takes 16 tokens; its 8 warps split H, warp
-// w taking [w H / 8, (w + 1) H / 8) in steps of 32. In a step, thread (g = lane / 4,
+// mma.sync m16n8k16 (bf16 x bf16 -> fp32). A block takes 16 tokens; its NW warps split the
+// row's 32-wide K steps into NW contiguous ranges. In a step, thread (g = lane / 4,
 // q = lane % 4) loads 16 contiguous bytes (8 bf16 at k0 + 8 q) of token rows g and g + 8
 // and of expert row nt * 8 + g for each of the NT 8-expert tiles. The step's two MMAs take
 // those as a fixed permutation of the 32 K positions (the same for x and W, so each product
 // x[t, k] W[e, k] is formed once): the first MMA's K slots 2q, 2q + 1 hold k0 + 8q + {0, 1}
-// and slots 2q + 8, 2q + 9 hold k0 + 8q + {2, 3}; the second MMA the same with + 4. The 8
-// warps' fp32 partial logits are added in warp order through shared memory, then the bias.
+// and slots 2q + 8, 2q + 9 hold k0 + 8q + {2, 3}; the second MMA the same with + 4. A warp
+// loads U steps into registers before it issues their MMAs, so that U steps of loads are in
+// flight per warp: the kernel is bound by how many bytes of x are in flight, not by the MMAs.
+// The warps' fp32 partial logits are added in warp order through shared memory, then the
+// bias.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -745,11 +732,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT>
-__global__ void __launch_bounds__(256) router_hmma_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
-                                                          const float* __restrict__ bias, int T, int H, int E,
-                                                          float* __restrict__ logits) {
-  __shared__ float red[8][16][8 * NT];
+// NW warps a block: 8 for one 8-expert tile, so that two 256-thread blocks fit an SM's
+// registers and the whole grid is resident at once; 16 for wider E, whose fewer steps in
+// flight per warp are made up by more warps.
+template <int NT, int NW>
+__global__ void __launch_bounds__(32 * NW) router_hmma_kernel(const uint4* __restrict__ x,
+                                                                         const uint4* __restrict__ w,
+                                                                         const float* __restrict__ bias, int T, int H,
+                                                                         int E, float* __restrict__ logits) {
+  constexpr int U = NT == 1 ? 8 : NT == 2 ? 4 : 2;  // steps in flight per warp (registers: U (2 + NT) uint4)
+  __shared__ float red[NW][16][8 * NT];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int t0 = blockIdx.x * 16;
@@ -770,17 +762,30 @@ __global__ void __launch_bounds__(256) router_hmma_kernel(const uint4* __restric
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-  const int steps = H / 256;  // 32-wide K steps of this warp
-  const int c0 = warp * steps * 4;  // this warp's first chunk (4 chunks a step)
-#pragma unroll 4
-  for (int st = 0; st < steps; ++st) {
-    const int c = c0 + st * 4;
-    const uint4 va = __ldg(xa + c), vb = __ldg(xb + c);
+  const int S = H / 32;                                    // 32-wide K steps of a row
+  const int per = (S + NW - 1) / NW;                      // steps of a warp
+  const int s_end = min(S, (warp + 1) * per);
+  for (int sb = warp * per; sb < s_end; sb += U) {
+    uint4 va[U], vb[U], vw[U][NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint4 vw = wok[nt] ? __ldg(wr[nt] + c) : make_uint4(0, 0, 0, 0);
-      mma_bf16_16816(acc[nt], va.x, vb.x, va.y, vb.y, vw.x, vw.y);
-      mma_bf16_16816(acc[nt], va.z, vb.z, va.w, vb.w, vw.z, vw.w);
+    for (int u = 0; u < U; ++u) {
+      if (sb + u < s_end) {
+        const int c = (sb + u) * 4;  // 4 chunks a step
+        va[u] = __ldg(xa + c);
+        vb[u] = __ldg(xb + c);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) vw[u][nt] = wok[nt] ? __ldg(wr[nt] + c) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (sb + u < s_end) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16_16816(acc[nt], va[u].x, vb[u].x, va[u].y, vb[u].y, vw[u][nt].x, vw[u][nt].y);
+          mma_bf16_16816(acc[nt], va[u].z, vb[u].z, va[u].w, vb[u].w, vw[u][nt].z, vw[u][nt].w);
+        }
+      }
     }
   }
   // D fragment: (token g, expert nt * 8 + 2q + {0, 1}) and (token g + 8, the same experts)
@@ -798,76 +803,9 @@ __global__ void __launch_bounds__(256) router_hmma_kernel(const uint4* __restric
     if (t < T && e < E) {
       float v = 0.0f;
 #pragma unroll
-      for (int wp = 0; wp < 8; ++wp) v += red[wp][tl][e];
+      for (int wp = 0; wp < NW; ++wp) v += red[wp][tl][e];
       logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
     }
-  }
-}
-
-template <int EP, int CPT>
-__global__ void __launch_bounds__(256) router_stream_kernel(const uint4* __restrict__ x, const uint4* __restrict__ w,
-                                                            const float* __restrict__ bias, int T, int E,
-                                                            float* __restrict__ logits) {
-  constexpr int TB = 32 / EP;
-  constexpr int NCH = 256 * CPT;  // 16-byte chunks of a row
-  __shared__ float red[8][32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float wf[EP][CPT][8];
-#pragma unroll
-  for (int e = 0; e < EP; ++e)
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const uint4 v = e < E ? __ldg(w + (int64_t)e * NCH + tid + 256 * j) : make_uint4(0, 0, 0, 0);
-      bf16x8_to_f32(v, wf[e][j]);
-    }
-  const int ngroups = (T + TB - 1) / TB;
-  uint4 xv[TB][CPT];
-  auto load = [&](int g) {
-#pragma unroll
-    for (int i = 0; i < TB; ++i) {
-      const int t = min(g * TB + i, T - 1);  // a short last group repeats a row; not stored
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) xv[i][j] = __ldg(x + (int64_t)t * NCH + tid + 256 * j);
-    }
-  };
-  if (blockIdx.x < ngroups) load(blockIdx.x);
-  for (int g = blockIdx.x; g < ngroups; g += gridDim.x) {
-    float acc[32];
-#pragma unroll
-    for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < TB; ++i)
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        float xf[8];
-        bf16x8_to_f32(xv[i][j], xf);
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[i * EP + e] = __fmaf_rn(xf[q], wf[e][j][q], acc[i * EP + e]);
-      }
-    if (g + (int)gridDim.x < ngroups) load(g + gridDim.x);  // in flight during the reduction
-    // reduce-scatter: at each step a lane keeps the half of its window its lane bit selects
-#pragma unroll
-    for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int q = 0; q < n / 2; ++q) {
-        const float send = upper ? acc[q] : acc[q + n / 2];
-        const float keep = upper ? acc[q + n / 2] : acc[q];
-        acc[q] = keep + __shfl_xor_sync(kFull, send, off);
-      }
-    }
-    red[warp][lane] = acc[0];  // the warp's sum of product `lane` (token lane / EP, expert lane % EP)
-    __syncthreads();
-    if (tid < 32) {
-      float v = 0.0f;
-#pragma unroll
-      for (int wp = 0; wp < 8; ++wp) v += red[wp][tid];
-      const int t = g * TB + tid / EP, e = tid % EP;
-      if (t < T && e < E) logits[(int64_t)t * E + e] = bias ? v + bias[e] : v;
-    }
-    __syncthreads();
   }
 }
 
@@ -960,9 +898,6 @@ bool router_small_supported(const moe_config_t& c) { return c.E <= 32; }
 cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void* w, const float* bias,
                                 float* logits, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool bf = c.act_dtype == MOE_DTYPE_BF16;
   // bf16 rows of a multiple of 256: the tensor-core form, 16 tokens a block
   if (bf && c.H % 256 == 0) {
@@ -971,26 +906,12 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
     const uint4* wv = static_cast<const uint4*>(w);
 #define MOE_RH(NT) \
   if (c.E <= 8 * NT) { \
-    router_hmma_kernel<NT><<<blocks, 256, 0, s>>>(xv, wv, bias, c.T, c.H, c.E, logits); \
+    constexpr int NW = NT == 1 ? 8 : 16; \
+    router_hmma_kernel<NT, NW><<<blocks, 32 * NW, 0, s>>>(xv, wv, bias, c.T, c.H, c.E, logits); \
     return cudaGetLastError(); \
   }
     MOE_RH(1) MOE_RH(2) MOE_RH(3) MOE_RH(4)
 #undef MOE_RH
-  }
-  // streamed form, one block per SM, for the shapes whose weight slice fits in registers
-  // without spilling (E <= 8 with H of 2048 or 4096; E <= 16 with H of 2048)
-  if (bf && ((c.E <= 8 && (c.H == 2048 || c.H == 4096)) || (c.E <= 16 && c.H == 2048))) {
-    const int tb = c.E <= 8 ? 4 : 2;
-    const unsigned blocks = (unsigned)std::min<int64_t>(sms, ceil_div(c.T, tb));
-    const uint4* xv = static_cast<const uint4*>(x);
-    const uint4* wv = static_cast<const uint4*>(w);
-#define MOE_RST(EP, CPT) \
-  if (c.E <= EP && c.H == 2048 * CPT) { \
-    router_stream_kernel<EP, CPT><<<blocks, 256, 0, s>>>(xv, wv, bias, c.T, c.E, logits); \
-    return cudaGetLastError(); \
-  }
-    MOE_RST(8, 1) MOE_RST(8, 2) MOE_RST(16, 1)
-#undef MOE_RST
   }
 #define MOE_RS(EP, TB)                                                                                \
   if (c.E <= EP) {                                                                                  \
