@@ -169,13 +169,13 @@ def test_router_logits_real_widths(name, T, H, E):
 
 @pytest.mark.parametrize("T,H,E", [(701, 2048, 5), (4096, 4096, 8), (333, 2048, 12), (130, 2048, 16),
                                    (1, 4096, 8), (3, 2048, 16), (257, 768, 24), (64, 1280, 32),
-                                   (100, 7168, 8)])
+                                   (100, 7168, 8), (50, 768, 8), (333, 1280, 6), (2100, 512, 7)])
 def test_router_logits_small_e_tensor_core_shapes(T, H, E):
     """The small-expert router on the tensor cores (bf16, E <= 32, H a multiple of 256):
     ragged last 16-token tiles, E below each 8-expert tile's width (1 to 4 tiles), a bias,
-    and H whose 32-wide K steps do not split evenly over the 16 warps (768, 1280: some warps
-    get no steps) or do (7168). On the exact-sum grids every logit equals the oracle's bit for
-    bit, whatever the summation order."""
+    and H whose 32-wide K steps split evenly over the warps (512 to 7168) or not (768, 1280:
+    some warps get none). On the exact-sum grids every logit equals the oracle's bit for bit,
+    whatever the summation order."""
     w = synth.workload("tc_router", T, H, E, 2, 128)
     inp = synth.host_inputs(w, seed=9, with_weights=False)
     x, wr = grid_x(inp["x"]), grid_w_router(inp["w_router"])
