@@ -139,7 +139,8 @@ typedef struct {
  *    and never read into a result. */
 
 /* Bytes of device workspace needed by every call below except moe_forward (the status
- * word plus the routing scan's per-block counts). Zero it once with moe_workspace_init. */
+ * word, the routing scan's per-block counts and the auxiliary loss's per-block sums). Zero
+ * it once with moe_workspace_init. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
 /* Bytes of device workspace for moe_forward: the part above followed by every
@@ -197,9 +198,13 @@ moe_status_t moe_route_from_map(const moe_config_t* cfg, const int32_t* topk_idx
  * formula, so the switch-style form is taken):
  *   loss = alpha * E / (T*k) * sum_e counts[e] * Pbar_e,
  * Pbar_e = the mean over tokens of expert e's probability: the softmax of the token's logits
- * over all experts, or its sigmoid scores divided by their sum (score_fn). logits [T,E]
- * fp32, counts [E] from moe_route; *loss is one device float. Uses the workspace's scan
- * scratch (stream-ordered after moe_route on the same workspace is fine). Deterministic. */
+ * over all experts, or its sigmoid scores divided by their sum (score_fn). A non-finite
+ * logit counts as -FLT_MAX, as in routing. Each token's probability is rounded to a multiple
+ * of 2^-32 and the sums over tokens, and sum_e counts[e] * (that sum), are exact integers
+ * (64 and 128 bits), so the value does not depend on how the work is split: moe_forward_train
+ * gives the same bits from inside its routing. logits [T,E] fp32, counts [E] from moe_route;
+ * *loss is one device float. Uses the workspace's scratch (stream-ordered after moe_route on
+ * the same workspace is fine). Deterministic. */
 moe_status_t moe_aux_loss(const moe_config_t* cfg, const float* logits, const int32_t* counts,
                           float alpha, float* loss, void* ws, moe_stream_t stream);
 
@@ -355,7 +360,9 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x, const moe_weig
  * the workspace are bit-identical to moe_forward's. aux_loss: NULL, or one device float
  * that receives moe_aux_loss's loss (coefficient aux_alpha; a NaN coefficient is
  * MOE_ERR_INVALID_ARG) on this call's logits and counts (0 when T = 0); pass the same
- * coefficient as grads->aux_loss_coeff to moe_backward_kept for its gradient. */
+ * coefficient as grads->aux_loss_coeff to moe_backward_kept for its gradient. Where routing
+ * is one launch (moe_route_launch_count reports 1) that launch also forms the loss, reading
+ * the logits once; otherwise two more launches after the routing do. */
 moe_status_t moe_forward_train(const moe_config_t* cfg, const void* x, const moe_weights_t* w, void* y, void* ws,
                                void* gu, float aux_alpha, float* aux_loss, moe_stream_t stream);
 

@@ -161,6 +161,24 @@ def test_aux_loss_against_oracle(w):
     assert torch.equal(loss, loss2)  # deterministic
 
 
+@pytest.mark.parametrize("score_fn", [synth.SOFTMAX, synth.SIGMOID], ids=["softmax", "sigmoid"])
+@pytest.mark.parametrize("T,E,k", [(700, 4, 2), (300, 256, 8), (5000, 8, 2)])
+def test_aux_loss_of_equal_scores_is_alpha(T, E, k, score_fn):
+    """Equal logits: each probability is 1/E (softmax, or sigmoid scores of 1/2 over their
+    sum; exact, E a power of two), so Pbar_e = 1/E and the loss is
+    alpha * E / (T k) * sum_e counts[e] / E = alpha for any counts summing to T k. The
+    fixed-point sums are exact, so the result is alpha to the last bit."""
+    w = rcase("equal", T, E, k, score_fn=score_fn)
+    b = alloc(w)
+    counts = np.full(E, T * k // E, dtype=np.int32)
+    counts[: T * k % E] += 1
+    assert counts.sum() == T * k
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_aux_loss(b["cfg"], torch.zeros((T, E), dtype=torch.float32, device="cuda"), up(counts), 0.01, loss,
+                     b["ws"])
+    assert float(loss.item()) == np.float32(0.01)
+
+
 def test_both_routing_paths_are_exercised():
     """moe_route takes one cooperative launch where a block's token chunk times ceil(E / 32)
     stays within 256, else the top-k launch and the scan passes. The bit-exact cases above

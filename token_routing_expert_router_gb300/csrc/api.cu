@@ -57,21 +57,33 @@ DeviceStatus* status_of(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); 
 uint32_t* barrier_of(void* ws) { return reinterpret_cast<uint32_t*>((char*)ws + 16); }
 int32_t* blockcnt_of(void* ws) { return reinterpret_cast<int32_t*>((char*)ws + kWsHead); }
 
+// The routing workspace: the head, the scan's (or the single launch's) per-block counts, and
+// the auxiliary loss's per-block 64-bit partial sums.
+size_t route_blocks(const moe_config_t& c) {
+  return std::max<size_t>((size_t)scan_blocks(c), (size_t)kFusedMaxRouteBlocks);
+}
+uint64_t* auxp_of(void* ws, const moe_config_t& c) {
+  return reinterpret_cast<uint64_t*>((char*)ws + kWsHead + align_up(route_blocks(c) * c.E * sizeof(int32_t), 256));
+}
 size_t route_ws_bytes(const moe_config_t& c) {
-  const size_t blocks = std::max<size_t>((size_t)scan_blocks(c), (size_t)kFusedMaxRouteBlocks);
-  return kWsHead + align_up(blocks * c.E * sizeof(int32_t), 256);
+  return kWsHead + align_up(route_blocks(c) * c.E * sizeof(int32_t), 256) +
+         align_up(route_blocks(c) * c.E * sizeof(uint64_t), 256);
 }
 
 // S1 + S2: one cooperative launch where it applies, else the top-k and scan passes.
+// S1 + S2, and with aux_loss the auxiliary loss: inside the single routing launch where there
+// is one, else by its own two launches after the scan.
 cudaError_t route_and_permute(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
                               int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* tok_row, void* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, float aux_alpha = 0.0f, float* aux_loss = nullptr) {
   if (route_fused_supported(c))
     return launch_route_fused(c, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, blockcnt_of(ws),
-                              barrier_of(ws), status_of(ws), s);
+                              barrier_of(ws), status_of(ws), s, aux_loss ? auxp_of(ws, c) : nullptr, aux_alpha,
+                              aux_loss);
   cudaError_t e = launch_route_topk(c, logits, topk_idx, topk_w, status_of(ws), s);
   if (e == cudaSuccess)
     e = launch_route_scan(c, topk_idx, counts, offsets, row_token, tok_row, blockcnt_of(ws), status_of(ws), s);
+  if (e == cudaSuccess && aux_loss) e = launch_aux_loss(c, logits, counts, aux_alpha, aux_loss, auxp_of(ws, c), s);
   return e;
 }
 
@@ -363,8 +375,7 @@ moe_status_t moe_aux_loss(const moe_config_t* cfg, const float* logits, const in
   moe_status_t v = validate(cfg);
   if (v != MOE_OK) return v;
   if (!ptr_ok(counts) || !loss || !ptr_ok(ws) || (cfg->T > 0 && !ptr_ok(logits))) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_aux_loss(*cfg, logits, counts, alpha, loss, reinterpret_cast<float*>(blockcnt_of(ws)),
-                                     (cudaStream_t)stream));
+  return cuda_status(launch_aux_loss(*cfg, logits, counts, alpha, loss, auxp_of(ws, *cfg), (cudaStream_t)stream));
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* tok_row,
@@ -481,9 +492,9 @@ moe_status_t forward_impl(const moe_config_t* cfg, const void* x, const moe_weig
   void* yd = base + L.yd;
 
   cudaError_t e = router_logits(c, x, w->w_router, w->router_bias, logits, status_of(ws), s);
-  if (e == cudaSuccess) e = route_and_permute(c, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, ws, s);
-  if (e == cudaSuccess && aux_loss_out)  // the scan's scratch is free again: it holds the partials
-    e = launch_aux_loss(c, logits, counts, aux_alpha, aux_loss_out, reinterpret_cast<float*>(blockcnt_of(ws)), s);
+  if (e == cudaSuccess)
+    e = route_and_permute(c, logits, topk_idx, topk_w, counts, offsets, row_token, tok_row, ws, s, aux_alpha,
+                          aux_loss_out);
   if (e == cudaSuccess)
     e = is_mx(c) ? launch_dispatch_mx(c, x, topk_idx, tok_row, offsets, xd, xd_scale, s)
                  : launch_dispatch(c, x, tok_row, xd, static_cast<float*>(xd_scale), s);

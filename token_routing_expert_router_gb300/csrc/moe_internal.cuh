@@ -41,15 +41,19 @@ cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_
 bool router_small_supported(const moe_config_t& c);
 cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void* w, const float* bias,
                                 float* logits, cudaStream_t s);
+// The auxiliary loss in two launches (part: [ceil(T / 128)][E] 64-bit scratch).
 cudaError_t launch_aux_loss(const moe_config_t& c, const float* logits, const int32_t* counts, float alpha,
-                            float* loss, float* part, cudaStream_t s);
+                            float* loss, uint64_t* part, cudaStream_t s);
 // S1 + S2 in one cooperative launch (at most kFusedMaxRouteBlocks blocks): blockcnt holds
 // [blocks][E] counts, barrier two words of the workspace head (zero when initialised).
+// With auxp ([blocks][E] 64-bit scratch) the same launch writes the auxiliary loss (the value
+// launch_aux_loss gives) to *aux_loss.
 constexpr int kFusedMaxRouteBlocks = 512;
 bool route_fused_supported(const moe_config_t& c);
 cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* tok_row,
-                               int32_t* blockcnt, uint32_t* barrier, DeviceStatus* st, cudaStream_t s);
+                               int32_t* blockcnt, uint32_t* barrier, DeviceStatus* st, cudaStream_t s,
+                               uint64_t* auxp = nullptr, float aux_alpha = 0.0f, float* aux_loss = nullptr);
 cudaError_t launch_route_scan(const moe_config_t& c, const int32_t* topk_idx, int32_t* counts,
                               int32_t* offsets, int32_t* row_token, int32_t* tok_row,
                               int32_t* blockcnt, DeviceStatus* st, cudaStream_t s);

@@ -184,6 +184,84 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
   return my_idx;
 }
 
+// ---- auxiliary load-balancing loss, summed exactly
+// Each token's probabilities (the softmax of its logits over all experts, or its sigmoid
+// scores divided by their sum; a non-finite logit counts as -FLT_MAX, as in routing) are
+// rounded to multiples of 2^-32 and added as 64-bit integers, so a sum does not depend on
+// how the tokens are split between warps, blocks or launches: the single-launch routing and
+// moe_aux_loss's own pass give the same bits. kAuxOne = 2^32 stands for probability 1.
+constexpr float kAuxOne = 4294967296.0f;
+
+// One token by one warp: lane l adds the fixed-point probability of experts l, l + 32, ...
+template <int NSLOT>
+__device__ __forceinline__ void aux_token_fixed(const float* __restrict__ row, int E, int score_fn,
+                                                uint64_t (&acc)[NSLOT]) {
+  const int lane = threadIdx.x & 31;
+  float v[NSLOT];
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) {
+    const int e = s * 32 + lane;
+    float x = -FLT_MAX;
+    if (e < E) {
+      x = row[e];
+      if (!isfinite(x)) x = -FLT_MAX;
+    }
+    v[s] = x;
+    m = fmaxf(m, x);
+  }
+  float sum = 0.0f;
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    m = warp_max(m);
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      v[s] = s * 32 + lane < E ? expf(v[s] - m) : 0.0f;
+      sum += v[s];
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) {
+      v[s] = s * 32 + lane < E ? det_sigmoid(v[s]) : 0.0f;
+      sum += v[s];
+    }
+  }
+  sum = warp_sum(sum);
+  if (!(sum > 0.0f)) return;  // every score zero: the token adds nothing
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) acc[s] += __float2ull_rn(v[s] / sum * kAuxOne);
+}
+
+// loss = alpha * E / (T k) * sum_e counts[e] * Pbar_e, Pbar_e = S_e / (2^32 T), from the exact
+// V = sum_e counts[e] * S_e (at most 2^31 * 2^63 * 512 < 2^103).
+__device__ __forceinline__ float aux_loss_from(unsigned __int128 V, float alpha, int E, int T, int k) {
+  const double v = (double)(uint64_t)(V >> 64) * 18446744073709551616.0 + (double)(uint64_t)V;
+  return (float)((double)alpha * (double)E * v / (4294967296.0 * (double)T * (double)T * (double)k));
+}
+
+// Sum of a 128-bit value over the warp.
+__device__ __forceinline__ unsigned __int128 warp_sum_u128(unsigned __int128 v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const uint64_t lo = __shfl_xor_sync(kFull, (unsigned long long)(uint64_t)v, off);
+    const uint64_t hi = __shfl_xor_sync(kFull, (unsigned long long)(uint64_t)(v >> 64), off);
+    v += ((unsigned __int128)hi << 64) | lo;
+  }
+  return v;
+}
+
+// The block's V (every thread passes its share; blockDim a multiple of 32, at most 1024),
+// returned to thread 0. red: 32 shared 128-bit slots.
+__device__ __forceinline__ unsigned __int128 block_sum_u128(unsigned __int128 v, unsigned __int128* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_u128(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  unsigned __int128 t = 0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
 // One warp per token.
 template <int NSLOT>
 __global__ void __launch_bounds__(256) route_topk_kernel(
@@ -501,22 +579,31 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     int group_score, float rho, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
     int32_t* __restrict__ tok_row, int32_t* __restrict__ blockcnt, uint32_t* bar, uint64_t timeout_ns,
-    DeviceStatus* st) {
+    DeviceStatus* st, uint64_t* __restrict__ auxp, float aux_alpha, float* __restrict__ aux_loss) {
   extern __shared__ int32_t fsm[];
+  const bool grouped = G > 1 && g_keep < G;
   int32_t* hist = fsm;                                         // [E] this chunk's entries
   int32_t* base = fsm + E;                                     // [E] the chunk's next row
   uint32_t* mask = reinterpret_cast<uint32_t*>(fsm + 2 * E);   // [E]
   float* s_score = reinterpret_cast<float*>(fsm + 3 * E);      // [warps][E] (group-limited)
+  unsigned long long* asum = reinterpret_cast<unsigned long long*>(  // [E] the chunk's aux sums
+      fsm + ((3 * E + (grouped ? kFusedWarps * E : 0) + 1) & ~1));
   __shared__ int32_t warp_tot[32];
+  __shared__ unsigned __int128 red128[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = (T + (int)gridDim.x - 1) / (int)gridDim.x;
   const int t0 = (int)blockIdx.x * C, t1 = min(T, t0 + C);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     hist[e] = 0;
     mask[e] = 0;
+    asum[e] = 0;
   }
   __syncthreads();
-  // ---- 1. route the chunk; count its entries per expert
+  // ---- 1. route the chunk; count its entries per expert (and, with auxp, add up its tokens'
+  // fixed-point probabilities for the auxiliary loss)
+  uint64_t aacc[NSLOT];
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) aacc[s] = 0;
   for (int t = t0 + warp; t < t1; t += kFusedWarps) {
     int my = route_token<NSLOT>(logits, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx,
                                 topk_w, s_score + (size_t)warp * E, st);
@@ -524,9 +611,18 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
       if (my < 0 || my >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); my = 0; }  // as the scan passes
       atomicAdd(&hist[my], 1);  // a count: the order of the adds does not show
     }
+    if (auxp) aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, aacc);
+  }
+  if (auxp) {
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s)
+      if (aacc[s]) atomicAdd(&asum[s * 32 + lane], (unsigned long long)aacc[s]);  // integers: any order
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
+    if (auxp) auxp[(int64_t)blockIdx.x * E + e] = asum[e];
+  }
   // ---- 2. every block's counts are published
   if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
     // the map stays in bounds for the launches that read it: no routed rows, and this
@@ -545,18 +641,27 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     int P = 1;
     while (P < 32 && 2 * P * E <= (int)blockDim.x) P *= 2;
     const int ex = threadIdx.x / P, q = threadIdx.x % P;
+    const bool aux_here = auxp != nullptr && blockIdx.x == 0;  // block 0 also forms the aux loss
     int32_t tot = 0, before = 0;
+    unsigned long long S = 0;
     if (ex < E) {
 #pragma unroll 4
       for (int b = q; b < (int)gridDim.x; b += P) {
         const int32_t c = __ldcg(blockcnt + (int64_t)b * E + ex);
         tot += c;
         if (b < (int)blockIdx.x) before += c;
+        if (aux_here) S += __ldcg(reinterpret_cast<const unsigned long long*>(auxp) + (int64_t)b * E + ex);
       }
     }
     for (int off = 1; off < P; off <<= 1) {  // within aligned groups of P lanes
       tot += __shfl_xor_sync(kFull, tot, off);
       before += __shfl_xor_sync(kFull, before, off);
+      if (aux_here) S += __shfl_xor_sync(kFull, S, off);
+    }
+    if (aux_here) {
+      const unsigned __int128 v = block_sum_u128(
+          (ex < E && q == 0) ? (unsigned __int128)(uint32_t)tot * (uint64_t)S : (unsigned __int128)0, red128);
+      if (threadIdx.x == 0) *aux_loss = aux_loss_from(v, aux_alpha, E, T, k);
     }
     __syncthreads();  // hist and base are free: the counts were published, nothing read them since
     if (ex < E && q == 0) {
@@ -810,77 +915,49 @@ __global__ void __launch_bounds__(32 * NW) router_hmma_kernel(const uint4* __res
 }
 
 // Auxiliary load-balancing loss, pass 1: per block of 128 tokens (8 warps x 16 tokens), the
-// sum over its tokens of each expert's probability (softmax over all experts, or sigmoid
-// scores divided by their sum). Every sum runs in a fixed order: no float atomics.
+// sum over its tokens of each expert's fixed-point probability (aux_token_fixed).
 template <int NSLOT>
 __global__ void __launch_bounds__(256) aux_pbar_kernel(const float* __restrict__ logits, int T, int E,
-                                                       int score_fn, float* __restrict__ part) {
-  __shared__ float wsum[8][NSLOT * 32];
+                                                       int score_fn, uint64_t* __restrict__ part) {
+  __shared__ unsigned long long wsum[NSLOT * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float acc[NSLOT];
+  for (int e = threadIdx.x; e < NSLOT * 32; e += blockDim.x) wsum[e] = 0;
+  __syncthreads();
+  uint64_t acc[NSLOT];
 #pragma unroll
-  for (int s = 0; s < NSLOT; ++s) acc[s] = 0.0f;
+  for (int s = 0; s < NSLOT; ++s) acc[s] = 0;
   for (int i = 0; i < 16; ++i) {
     const int t = blockIdx.x * 128 + warp * 16 + i;
     if (t >= T) break;
-    const float* row = logits + (int64_t)t * E;
-    float v[NSLOT];
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int s = 0; s < NSLOT; ++s) {
-      const int e = s * 32 + lane;
-      v[s] = e < E ? row[e] : -FLT_MAX;
-      if (e < E) m = fmaxf(m, v[s]);
-    }
-    m = warp_max(m);
-    float sum = 0.0f;
-#pragma unroll
-    for (int s = 0; s < NSLOT; ++s) {
-      const int e = s * 32 + lane;
-      v[s] = e < E ? (score_fn == MOE_SCORE_SOFTMAX ? expf(v[s] - m) : det_sigmoid(v[s])) : 0.0f;
-      sum += v[s];
-    }
-    sum = warp_sum(sum);
-#pragma unroll
-    for (int s = 0; s < NSLOT; ++s) acc[s] += v[s] / sum;
+    aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, acc);
   }
 #pragma unroll
-  for (int s = 0; s < NSLOT; ++s) wsum[warp][s * 32 + lane] = acc[s];
+  for (int s = 0; s < NSLOT; ++s)
+    if (acc[s]) atomicAdd(&wsum[s * 32 + lane], (unsigned long long)acc[s]);  // integers: any order
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float v = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += wsum[w][e];
-    part[(int64_t)blockIdx.x * E + e] = v;
-  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) part[(int64_t)blockIdx.x * E + e] = wsum[e];
 }
 
-// Pass 2 (one block): Pbar_e = sum over blocks / T, then
-// loss = alpha * E / (T * k) * sum_e counts[e] * Pbar_e, reduced as a fixed tree.
-__global__ void __launch_bounds__(1024) aux_loss_kernel(const float* __restrict__ part, int NB, int E,
+// Pass 2 (one block): S_e = the sum over blocks, then the loss from the exact
+// V = sum_e counts[e] * S_e.
+__global__ void __launch_bounds__(1024) aux_loss_kernel(const uint64_t* __restrict__ part, int NB, int E,
                                                         const int32_t* __restrict__ counts, int T, int k,
                                                         float alpha, float* __restrict__ loss) {
-  __shared__ float red[32];
-  float v = 0.0f;
+  __shared__ unsigned __int128 red[32];
+  unsigned __int128 v = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float pb = 0.0f;
-    for (int b = 0; b < NB; ++b) pb += part[(int64_t)b * E + e];
-    v += (float)counts[e] * (pb / (float)T);
+    uint64_t se = 0;
+    for (int b = 0; b < NB; ++b) se += part[(int64_t)b * E + e];
+    v += (unsigned __int128)(uint32_t)max(counts[e], 0) * se;
   }
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-    v = warp_sum(v);
-    if (threadIdx.x == 0) *loss = alpha * (float)E / ((float)T * (float)k) * v;
-  }
+  v = block_sum_u128(v, red);
+  if (threadIdx.x == 0) *loss = aux_loss_from(v, alpha, E, T, k);
 }
 
 }  // namespace
 
 cudaError_t launch_aux_loss(const moe_config_t& c, const float* logits, const int32_t* counts, float alpha,
-                            float* loss, float* part, cudaStream_t s) {
+                            float* loss, uint64_t* part, cudaStream_t s) {
   const int NB = scan_blocks(c);
   const int nslot = (int)ceil_div(c.E, 32);
   if (NB > 0) {
@@ -971,7 +1048,10 @@ FusedPlan fused_plan(const moe_config_t& c) {
          : nslot <= 8 ? fused_kernel_ptr<8>() : nslot <= 16 ? fused_kernel_ptr<16>() : nullptr;
   if (!f.kern) return f;
   const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
-  f.smem = (size_t)3 * c.E * sizeof(int32_t) + (grouped ? (size_t)kFusedWarps * c.E * sizeof(float) : 0);
+  // hist, base, mask [E] ints, the group scores [warps][E] floats, then the aux sums [E]
+  // 64-bit integers at an 8-byte boundary
+  f.smem = (size_t)((3 * c.E + (grouped ? kFusedWarps * c.E : 0) + 1) & ~1) * sizeof(int32_t) +
+           (size_t)c.E * sizeof(uint64_t);
   static int sms = 0;
   if (!sms) {
     int dev = 0;
@@ -1018,7 +1098,8 @@ bool route_fused_supported(const moe_config_t& c) {
 
 cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* tok_row,
-                               int32_t* blockcnt, uint32_t* barrier, DeviceStatus* st, cudaStream_t s) {
+                               int32_t* blockcnt, uint32_t* barrier, DeviceStatus* st, cudaStream_t s,
+                               uint64_t* auxp, float aux_alpha, float* aux_loss) {
   if (c.T == 0) return cudaSuccess;
   const FusedPlan f = fused_plan(c);
   if (f.grid <= 0) return cudaErrorInvalidConfiguration;
@@ -1037,7 +1118,8 @@ cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32
                   (void*)&c.score_fn, (void*)&c.renorm,   (void*)&c.n_groups,   (void*)&c.topk_groups,
                   (void*)&c.group_score, (void*)&c.routed_scale, (void*)&topk_idx, (void*)&topk_w,
                   (void*)&counts,  (void*)&offsets,       (void*)&row_token,    (void*)&tok_row,
-                  (void*)&blockcnt, (void*)&barrier,      (void*)&timeout,      (void*)&st};
+                  (void*)&blockcnt, (void*)&barrier,      (void*)&timeout,      (void*)&st,
+                  (void*)&auxp,    (void*)&aux_alpha,     (void*)&aux_loss};
   cudaError_t e = cudaLaunchKernelExC(&cfg, f.kern, args);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
