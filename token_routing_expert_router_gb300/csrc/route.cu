@@ -573,7 +573,7 @@ __device__ __forceinline__ bool fused_grid_barrier(uint32_t* bar, uint32_t nbloc
   return s_ok != 0;
 }
 
-template <int NSLOT>
+template <int NSLOT, bool AUX>
 __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G, int g_keep,
     int group_score, float rho, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
@@ -586,17 +586,16 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
   int32_t* base = fsm + E;                                     // [E] the chunk's next row
   uint32_t* mask = reinterpret_cast<uint32_t*>(fsm + 2 * E);   // [E]
   float* s_score = reinterpret_cast<float*>(fsm + 3 * E);      // [warps][E] (group-limited)
-  unsigned long long* asum = reinterpret_cast<unsigned long long*>(  // [E] the chunk's aux sums
+  unsigned long long* asum = reinterpret_cast<unsigned long long*>(  // [E] the chunk's aux sums (AUX)
       fsm + ((3 * E + (grouped ? kFusedWarps * E : 0) + 1) & ~1));
   __shared__ int32_t warp_tot[32];
-  __shared__ unsigned __int128 red128[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = (T + (int)gridDim.x - 1) / (int)gridDim.x;
   const int t0 = (int)blockIdx.x * C, t1 = min(T, t0 + C);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     hist[e] = 0;
     mask[e] = 0;
-    asum[e] = 0;
+    if constexpr (AUX) asum[e] = 0;
   }
   __syncthreads();
   // ---- 1. route the chunk; count its entries per expert (and, with auxp, add up its tokens'
@@ -611,9 +610,9 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
       if (my < 0 || my >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); my = 0; }  // as the scan passes
       atomicAdd(&hist[my], 1);  // a count: the order of the adds does not show
     }
-    if (auxp) aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, aacc);
+    if constexpr (AUX) aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, aacc);
   }
-  if (auxp) {
+  if constexpr (AUX) {
 #pragma unroll
     for (int s = 0; s < NSLOT; ++s)
       if (aacc[s]) atomicAdd(&asum[s * 32 + lane], (unsigned long long)aacc[s]);  // integers: any order
@@ -621,7 +620,7 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
-    if (auxp) auxp[(int64_t)blockIdx.x * E + e] = asum[e];
+    if constexpr (AUX) auxp[(int64_t)blockIdx.x * E + e] = asum[e];
   }
   // ---- 2. every block's counts are published
   if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
@@ -641,7 +640,7 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     int P = 1;
     while (P < 32 && 2 * P * E <= (int)blockDim.x) P *= 2;
     const int ex = threadIdx.x / P, q = threadIdx.x % P;
-    const bool aux_here = auxp != nullptr && blockIdx.x == 0;  // block 0 also forms the aux loss
+    const bool aux_here = AUX && blockIdx.x == 0;  // block 0 also forms the aux loss
     int32_t tot = 0, before = 0;
     unsigned long long S = 0;
     if (ex < E) {
@@ -658,10 +657,13 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
       before += __shfl_xor_sync(kFull, before, off);
       if (aux_here) S += __shfl_xor_sync(kFull, S, off);
     }
-    if (aux_here) {
+    if constexpr (AUX) {
+      __shared__ unsigned __int128 red128[32];
+      if (aux_here) {
       const unsigned __int128 v = block_sum_u128(
           (ex < E && q == 0) ? (unsigned __int128)(uint32_t)tot * (uint64_t)S : (unsigned __int128)0, red128);
       if (threadIdx.x == 0) *aux_loss = aux_loss_from(v, aux_alpha, E, T, k);
+      }
     }
     __syncthreads();  // hist and base are free: the counts were published, nothing read them since
     if (ex < E && q == 0) {
@@ -1033,25 +1035,53 @@ namespace {
 
 // The fused kernel's instance, its shared memory and its grid for a configuration.
 struct FusedPlan {
-  const void* kern = nullptr;
-  size_t smem = 0;
+  const void* kern = nullptr;      // plain routing
+  const void* kern_aux = nullptr;  // routing + auxiliary loss
+  size_t smem = 0, smem_aux = 0;
   int64_t grid = 0;
 };
 
-template <int NS>
-const void* fused_kernel_ptr() { return reinterpret_cast<const void*>(&route_fused_kernel<NS>); }
+template <int NS, bool AUX>
+const void* fused_kernel_ptr() { return reinterpret_cast<const void*>(&route_fused_kernel<NS, AUX>); }
 
+template <bool AUX>
+const void* fused_kernel_for(int nslot) {
+  return nslot <= 1 ? fused_kernel_ptr<1, AUX>() : nslot <= 2 ? fused_kernel_ptr<2, AUX>()
+       : nslot <= 4 ? fused_kernel_ptr<4, AUX>() : nslot <= 8 ? fused_kernel_ptr<8, AUX>()
+       : nslot <= 16 ? fused_kernel_ptr<16, AUX>() : nullptr;
+}
+
+// Blocks per SM of one fused instance with `smem` bytes of dynamic shared memory (cached per
+// instance and size); 0 on failure.
+int fused_per_sm(const void* kern, size_t smem) {
+  struct Entry { const void* kern; size_t smem; int per_sm; };
+  static Entry cache[4] = {};
+  static int next = 0;
+  for (const Entry& e : cache)
+    if (e.kern == kern && e.smem == smem) return e.per_sm;
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kFusedWarps, smem) != cudaSuccess) return 0;
+  cache[next] = Entry{kern, smem, per_sm};
+  next = (next + 1) % 4;
+  return per_sm;
+}
+
+// The plain instance routes (moe_route); the AUX one also forms the auxiliary loss
+// (moe_forward_train). Both take the same grid, sized so that either is resident at once.
 FusedPlan fused_plan(const moe_config_t& c) {
   FusedPlan f;
   const int nslot = (int)ceil_div(c.E, 32);
-  f.kern = nslot <= 1 ? fused_kernel_ptr<1>() : nslot <= 2 ? fused_kernel_ptr<2>() : nslot <= 4 ? fused_kernel_ptr<4>()
-         : nslot <= 8 ? fused_kernel_ptr<8>() : nslot <= 16 ? fused_kernel_ptr<16>() : nullptr;
-  if (!f.kern) return f;
+  f.kern = fused_kernel_for<false>(nslot);
+  f.kern_aux = fused_kernel_for<true>(nslot);
+  if (!f.kern || !f.kern_aux) return f;
   const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
-  // hist, base, mask [E] ints, the group scores [warps][E] floats, then the aux sums [E]
-  // 64-bit integers at an 8-byte boundary
-  f.smem = (size_t)((3 * c.E + (grouped ? kFusedWarps * c.E : 0) + 1) & ~1) * sizeof(int32_t) +
-           (size_t)c.E * sizeof(uint64_t);
+  // hist, base, mask [E] ints and the group scores [warps][E] floats; the AUX instance adds
+  // the aux sums [E] 64-bit integers at an 8-byte boundary
+  const size_t ints = (size_t)((3 * c.E + (grouped ? kFusedWarps * c.E : 0) + 1) & ~1);
+  f.smem = ints * sizeof(int32_t);
+  f.smem_aux = f.smem + (size_t)c.E * sizeof(uint64_t);
   static int sms = 0;
   if (!sms) {
     int dev = 0;
@@ -1059,25 +1089,12 @@ FusedPlan fused_plan(const moe_config_t& c) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
   }
-  static const void* last_kern = nullptr;  // occupancy of the last (instance, shared memory) asked
-  static size_t last_smem = 0;
-  static int last_per_sm = 0;
-  if (f.kern != last_kern || f.smem != last_smem) {
-    if (f.smem > 48 * 1024 &&
-        cudaFuncSetAttribute(f.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f.smem) != cudaSuccess)
-      return f;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f.kern, 32 * kFusedWarps, f.smem) != cudaSuccess)
-      return f;
-    last_kern = f.kern;
-    last_smem = f.smem;
-    last_per_sm = per_sm;
-  }
-  if (last_per_sm <= 0) return f;
+  const int per_sm = std::min(fused_per_sm(f.kern, f.smem), fused_per_sm(f.kern_aux, f.smem_aux));
+  if (per_sm <= 0) return f;
   // every block resident at once (the grid barrier), at most one block per 16 tokens, and
   // grid * E <= 32768: after the barrier each block reads all blocks' counts
   f.grid = std::max<int64_t>(
-      1, std::min<int64_t>(std::min<int64_t>(std::min<int64_t>((int64_t)last_per_sm * sms, kFusedMaxBlocks),
+      1, std::min<int64_t>(std::min<int64_t>(std::min<int64_t>((int64_t)per_sm * sms, kFusedMaxBlocks),
                                              ceil_div(c.T, kFusedWarps)),
                            32768 / c.E));
   return f;
@@ -1106,7 +1123,7 @@ cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)f.grid);
   cfg.blockDim = dim3(32 * kFusedWarps);
-  cfg.dynamicSmemBytes = f.smem;
+  cfg.dynamicSmemBytes = auxp ? f.smem_aux : f.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -1120,7 +1137,7 @@ cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32
                   (void*)&counts,  (void*)&offsets,       (void*)&row_token,    (void*)&tok_row,
                   (void*)&blockcnt, (void*)&barrier,      (void*)&timeout,      (void*)&st,
                   (void*)&auxp,    (void*)&aux_alpha,     (void*)&aux_loss};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, f.kern, args);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, auxp ? f.kern_aux : f.kern, args);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
