@@ -466,14 +466,22 @@ def gemm_roofline(ctx, w, gemm_ms, alg):
                 **gemm_traffic(w)}
     peak = tensor_peak(ctx, w)
     sus = tensor_peak(ctx, w, "bf16_tflops_sustained")
-    return {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
-            "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
-            "peak_kind": f"{ctx.peak_kind} bf16 burst" + (" x2 (nominal fp8:bf16 dense ratio)" if quant_kind(w) else "")
-                         + ": the GEMM pair is timed as single calls after an L2 flush",
-            "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
-            "frac_of_sustained": round(achieved / sus, 3),
-            "timing": "CUDA events around moe_grouped_mlp on the launching stream, median of the stage loop",
-            **gemm_traffic(w)}
+    out = {"kernel": "tc grouped GEMM (gate/up + SwiGLU, down): 2 launches per forward",
+           "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+           "peak_kind": f"{ctx.peak_kind} bf16 burst" + (" x2 (nominal fp8:bf16 dense ratio)" if quant_kind(w) else "")
+                        + ": the GEMM pair is timed as single calls after an L2 flush",
+           "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+           "frac_of_sustained": round(achieved / sus, 3),
+           "timing": "CUDA events around moe_grouped_mlp on the launching stream, median of the stage loop",
+           **gemm_traffic(w)}
+    # the other roof: the recorded DRAM traffic over the same time, against the measured copy rate
+    # (the DeepSeek-V3 shapes stream their weights once, so this one binds as much as the tensor's)
+    if out.get("traffic"):
+        gbs = out["traffic"] / (gemm_ms / 1e3) / 1e9
+        out["dram_gbs"] = round(gbs, 1)
+        out["dram_frac"] = round(gbs / ctx.peaks["hbm_gbs"], 3)
+        out["weight_bound_ms"] = round(alg["weight_bytes"] / (ctx.peaks["hbm_gbs"] * 1e9) * 1e3, 3)
+    return out
 
 
 def hbm_roofline(ctx, alg, disp_ms, comb_ms):
