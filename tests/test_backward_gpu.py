@@ -338,3 +338,41 @@ def test_backward_no_tokens_gives_zero_weight_gradients():
     torch.cuda.synchronize()
     for key, v in g.items():
         assert not v.any(), key
+
+
+@pytest.mark.parametrize("w", [
+    synth.scaled(W["dsv3_bf16"], T=8192, H=256, E=256, F=256, F_shared=256, name="e256_t8192"),
+    synth.scaled(W["imbalanced_bf16"], T=16384, H=256, E=128, F=256, name="imbalanced_t16384"),
+], ids=["e256_t8192", "imbalanced_t16384"])
+def test_forward_train_aux_loss_with_two_level_counts(w):
+    """At these sizes the single routing launch has more than 8192 per-block counts, so it
+    sums them in two levels (a scan down each expert's column, then a second grid barrier),
+    and adds up the auxiliary loss's per-block sums in the same pass. The training forward's
+    loss equals moe_aux_loss on the same logits and counts bit for bit, and its routing and
+    output equal moe_forward's."""
+    T, H, E, k = w["T"], w["H"], w["E"], w["k"]
+    inp = synth.host_inputs(w, seed=41)
+    d = device_weights_from_host(w, inp)
+    cfg = cfg_of(w)
+    assert moe.moe_route_launch_count(cfg) == 1
+    fws = torch.zeros(moe.moe_forward_workspace_size(cfg) // 4 + 64, dtype=torch.int32, device="cuda")
+    moe.moe_workspace_init(fws)
+    y0 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    idx0 = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    moe.moe_forward(cfg, d["x"], weights_arg(d), y0, fws, idx0)
+    y1 = torch.empty_like(y0)
+    gu = torch.empty((T * k + (T if w["n_shared"] else 0), 2 * w["F"]), dtype=torch.bfloat16, device="cuda")
+    aux = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_forward_train(cfg, d["x"], weights_arg(d), y1, fws, gu, aux_alpha=0.01, aux_loss=aux)
+    assert moe.moe_read_status(fws) == moe.MOE_OK
+    assert torch.equal(y0, y1)
+    b = alloc(w)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(cfg, d["x"], d["w_router"], d.get("router_bias"), logits, b["ws"])
+    moe.moe_route(cfg, logits, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["row_token"],
+                  b["tok_row"], b["ws"])
+    assert torch.equal(b["topk_idx"], idx0)
+    aux2 = torch.empty((1,), dtype=torch.float32, device="cuda")
+    moe.moe_aux_loss(cfg, logits, b["counts"], 0.01, aux2, b["ws"])
+    assert torch.equal(aux, aux2) and bool(torch.isfinite(aux).all())
+    assert moe.moe_read_status(b["ws"]) == moe.MOE_OK

@@ -37,6 +37,7 @@ CASES = [
     rcase("e512_k32", 700, 512, 32, G, 1, 16, 12),
     rcase("e33_ragged", 333, 33, 5),
     rcase("one_token", 1, 64, 8, G, 1, 8, 4),
+    rcase("e512_long", 20000, 512, 8, G, 1, 16, 8),
 ]
 
 
@@ -181,11 +182,12 @@ def test_aux_loss_of_equal_scores_is_alpha(T, E, k, score_fn):
 
 def test_both_routing_paths_are_exercised():
     """moe_route takes one cooperative launch where a block's token chunk times ceil(E / 32)
-    stays within 256, else the top-k launch and the scan passes. The bit-exact cases above
-    cover both: the Mixtral-sized routing takes the single launch, the DeepSeek-V3-sized one
-    (256 grouped experts) the top-k launch and the three scan passes."""
+    stays within 1024, else the top-k launch and the scan passes. The bit-exact cases above
+    cover both: every workload-sized routing takes the single launch, the 20000-token one
+    over 512 grouped experts the top-k launch and the three scan passes."""
     n = {w["name"]: moe.moe_route_launch_count(cfg_of(w)) for w in CASES}
-    assert n["mixtral"] == 1 and n["tiny"] == 1
-    assert n["dsv3"] == 4 and n["dsv3_fp8_tokens"] == 4
+    assert n["mixtral"] == 1 and n["tiny"] == 1 and n["dsv3"] == 1 and n["imbalanced"] == 1
+    assert n["dsv3_fp8_tokens"] == 1
+    assert n["e512_long"] == 4
     assert set(n.values()) <= {1, 2, 4}
     assert moe.moe_route_launch_count(cfg_of(synth.scaled(CASES[0], T=0))) == 0

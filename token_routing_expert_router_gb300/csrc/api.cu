@@ -54,7 +54,7 @@ moe_status_t empty_routing(const moe_config_t& c, int32_t* counts, int32_t* offs
 // Workspace head: the status word at byte 0, the fused routing kernel's grid barrier
 // (counter, flag) at byte 16; then the routing scratch (per-block expert counts).
 DeviceStatus* status_of(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); }
-uint32_t* barrier_of(void* ws) { return reinterpret_cast<uint32_t*>((char*)ws + 16); }
+uint32_t* barrier_of(void* ws) { return reinterpret_cast<uint32_t*>((char*)ws + 128); }
 int32_t* blockcnt_of(void* ws) { return reinterpret_cast<int32_t*>((char*)ws + kWsHead); }
 
 // The routing workspace: the head, the scan's (or the single launch's) per-block counts, and

@@ -11,10 +11,11 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------------------
-// Workspace layout. The head (256 B) holds the device status word; the routing scan's
-// per-block expert counts follow. moe_forward's intermediates come after that.
+// Workspace layout. The head (4 KB) holds the device status word and, from byte 128, the
+// single-launch routing's grid barrier; the routing scan's per-block expert counts follow.
+// moe_forward's intermediates come after that.
 // ---------------------------------------------------------------------------------------
-constexpr size_t kWsHead = 256;
+constexpr size_t kWsHead = 4096;
 constexpr int kScanChunk = 128;  // tokens per block of the counting pass
 
 struct DeviceStatus {

@@ -54,6 +54,17 @@ __device__ __forceinline__ bool better(float k1, int i1, float k2, int i2) {
   return k1 > k2 || (k1 == k2 && i1 < i2);
 }
 
+// Order-preserving integer image of a finite float (larger float, larger key; -0 and +0
+// both map to +0's key). Every image is nonzero, so 0 can mark an empty slot.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t b = __float_as_uint(x == 0.0f ? 0.0f : x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 __device__ __forceinline__ void warp_argmax(float& key, int& idx) {
 #pragma unroll
   for (int off = 16; off; off >>= 1) {
@@ -75,28 +86,41 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// S1 for one token t, by one warp: lane l holds experts l, l+32, l+64, ... (NSLOT slots).
-// Writes the token's k expert ids and weights and returns, in lane j < k, the token's j-th
-// expert. sc: this warp's E floats of shared memory (group-limited routing only).
+// Token t's logits into the warp's registers: lane l gets experts l, l+32, ... (NSLOT slots;
+// slots past E hold -FLT_MAX). Issued apart from route_token so that a warp can load its
+// next token while it routes this one.
 template <int NSLOT>
-__device__ __forceinline__ int route_token(const float* __restrict__ logits, int t, int E, int k, int score_fn,
+__device__ __forceinline__ void load_logits(const float* __restrict__ logits, int t, int E, float (&x)[NSLOT]) {
+  const int lane = threadIdx.x & 31;
+  const float* row = logits + (int64_t)t * E;
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) {
+    const int e = s * 32 + lane;
+    x[s] = e < E ? row[e] : -FLT_MAX;
+  }
+}
+
+// S1 for one token t, by one warp, from its logits x (load_logits): lane l holds experts l,
+// l+32, l+64, ... (NSLOT slots). Writes the token's k expert ids and weights and returns, in
+// lane j < k, the token's j-th expert. sc: this warp's E floats of shared memory (group-limited
+// routing whose groups are not single slots).
+template <int NSLOT>
+__device__ __forceinline__ int route_token(const float (&x)[NSLOT], int t, int E, int k, int score_fn,
                                            int renorm, int G, int g_keep, int group_score, float rho,
                                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* sc,
                                            DeviceStatus* st) {
   const int lane = threadIdx.x & 31;
-  const float* row = logits + (int64_t)t * E;
 
   float v[NSLOT];
   uint32_t ok = 0;
   bool bad = false;
 #pragma unroll
   for (int s = 0; s < NSLOT; ++s) {
-    const int e = s * 32 + lane;
     v[s] = -FLT_MAX;
-    if (e < E) {
-      float x = row[e];
-      if (!isfinite(x)) { bad = true; x = -FLT_MAX; }
-      v[s] = x;
+    if (s * 32 + lane < E) {
+      float xv = x[s];
+      if (!isfinite(xv)) { bad = true; xv = -FLT_MAX; }
+      v[s] = xv;
       ok |= 1u << s;
     }
   }
@@ -104,64 +128,113 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
 
   uint32_t allowed = ok;
   if (G > 1 && g_keep < G) {
-#pragma unroll
-    for (int s = 0; s < NSLOT; ++s)
-      if (ok >> s & 1) sc[s * 32 + lane] = det_sigmoid(v[s]);
-    __syncwarp();
-    const int gs = E / G;
-    float gkey = -INFINITY;
-    int gidx = INT_MAX;
-    if (lane < G) {
-      float m1 = -INFINITY, m2 = -INFINITY;  // the two largest scores of the group
-      // lanes start at different offsets of their groups (no bank conflicts); the two
-      // largest do not depend on the order the scores are visited in
-      for (int i = 0; i < gs; ++i) {
-        const float x = sc[lane * gs + (i + lane) % gs];
-        if (x > m1) { m2 = m1; m1 = x; }
-        else if (x > m2) m2 = x;
-      }
-      gkey = (group_score == MOE_GROUP_SCORE_TOP2_SUM && gs >= 2) ? __fadd_rn(m1, m2) : m1;
-      gidx = lane;
-    }
-    __syncwarp();  // the scores are read before the warp's next token overwrites them
     uint32_t keep = 0;
-    for (int r = 0; r < g_keep; ++r) {
-      float bk = gkey;
-      int bi = gidx;
-      warp_argmax(bk, bi);
-      keep |= 1u << bi;
-      if (lane == bi) { gkey = -INFINITY; gidx = INT_MAX; }
-    }
-    allowed = 0;
+    if (E == 32 * G) {
+      // One group per slot (group g = experts 32g .. 32g + 31 = slot g): each group's key
+      // comes from warp reductions of its 32 scores. Scores are >= +0 (a sigmoid), so their
+      // bit patterns order as unsigned integers; the second largest equals the largest when
+      // two lanes hold it.
+      float gk[NSLOT];
 #pragma unroll
-    for (int s = 0; s < NSLOT; ++s) {
-      const int e = s * 32 + lane;
-      if ((ok >> s & 1) && (keep >> (e / gs) & 1)) allowed |= 1u << s;
+      for (int s = 0; s < NSLOT; ++s) {
+        gk[s] = -INFINITY;
+        if (s < G) {
+          const uint32_t b = __float_as_uint(det_sigmoid(v[s]));
+          const uint32_t m1 = __reduce_max_sync(kFull, b);
+          float g = __uint_as_float(m1);
+          if (group_score == MOE_GROUP_SCORE_TOP2_SUM) {
+            uint32_t m2 = m1;
+            if (__popc(__ballot_sync(kFull, b == m1)) < 2) m2 = __reduce_max_sync(kFull, b == m1 ? 0u : b);
+            g = __fadd_rn(g, __uint_as_float(m2));
+          }
+          gk[s] = g;
+        }
+      }
+      // the g_keep best groups in (key, index) order: those with fewer than g_keep better ones
+#pragma unroll
+      for (int g = 0; g < NSLOT; ++g) {
+        int rank = 0;
+#pragma unroll
+        for (int h = 0; h < NSLOT; ++h)
+          rank += (h < G && better(gk[h], h, gk[g], g)) ? 1 : 0;
+        if (g < G && rank < g_keep) keep |= 1u << g;
+      }
+      allowed = ok & keep;
+    } else {
+#pragma unroll
+      for (int s = 0; s < NSLOT; ++s)
+        if (ok >> s & 1) sc[s * 32 + lane] = det_sigmoid(v[s]);
+      __syncwarp();
+      const int gs = E / G;
+      float gkey = -INFINITY;
+      int gidx = INT_MAX;
+      if (lane < G) {
+        float m1 = -INFINITY, m2 = -INFINITY;  // the two largest scores of the group
+        // lanes start at different offsets of their groups (no bank conflicts); the two
+        // largest do not depend on the order the scores are visited in
+        for (int i = 0; i < gs; ++i) {
+          const float x = sc[lane * gs + (i + lane) % gs];
+          if (x > m1) { m2 = m1; m1 = x; }
+          else if (x > m2) m2 = x;
+        }
+        gkey = (group_score == MOE_GROUP_SCORE_TOP2_SUM && gs >= 2) ? __fadd_rn(m1, m2) : m1;
+        gidx = lane;
+      }
+      __syncwarp();  // the scores are read before the warp's next token overwrites them
+      for (int r = 0; r < g_keep; ++r) {
+        float bk = gkey;
+        int bi = gidx;
+        warp_argmax(bk, bi);
+        keep |= 1u << bi;
+        if (lane == bi) { gkey = -INFINITY; gidx = INT_MAX; }
+      }
+      allowed = 0;
+#pragma unroll
+      for (int s = 0; s < NSLOT; ++s) {
+        const int e = s * 32 + lane;
+        if ((ok >> s & 1) && (keep >> (e / gs) & 1)) allowed |= 1u << s;
+      }
     }
   }
 
-  int my_idx = 0;
-  float my_key = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    float bk = -INFINITY;
-    int bi = INT_MAX;
+  // Top-k by (logit, index): each round takes the warp's largest key (one reduction), then
+  // the lowest expert index holding it (a second one); only the lane that held the winner
+  // moves on to its next best slot. Keys are the logits' order-preserving integer images,
+  // with -0 taken as +0 so that equal logits tie; 0 marks a slot that is out of the race.
+  uint32_t key[NSLOT];
 #pragma unroll
-    for (int s = 0; s < NSLOT; ++s) {
-      const int e = s * 32 + lane;
-      if ((allowed >> s & 1) && better(v[s], e, bk, bi)) { bk = v[s]; bi = e; }
+  for (int s = 0; s < NSLOT; ++s) key[s] = order_key(v[s]);
+  uint32_t live = allowed;  // the lane's slots still in the race
+  uint32_t bk = 0u;
+  int bs = 0;
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s)
+    if ((live >> s & 1) && key[s] > bk) { bk = key[s]; bs = s; }
+  int my_idx = 0;
+  uint32_t my_k = 0u;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t m = __reduce_max_sync(kFull, bk);
+    const uint32_t cand = (bk == m && bk != 0u) ? (uint32_t)(bs * 32 + lane) : 0xffffffffu;
+    const uint32_t bi = __reduce_min_sync(kFull, cand);
+    if (lane == j) { my_idx = (int)bi; my_k = m; }
+    if (cand == bi) {  // this lane's best was taken
+      live &= ~(1u << bs);
+      bk = 0u;
+      bs = 0;
+#pragma unroll
+      for (int s = 0; s < NSLOT; ++s)
+        if ((live >> s & 1) && key[s] > bk) { bk = key[s]; bs = s; }
     }
-    warp_argmax(bk, bi);
-    if (lane == j) { my_idx = bi; my_key = bk; }
-    if ((bi & 31) == lane) allowed &= ~(1u << (bi >> 5));
   }
+  const float my_key = key_value(my_k);
 
   float w;
   if (score_fn == MOE_SCORE_SOFTMAX) {
-    float m = -FLT_MAX;
+    uint32_t mk = 0u;
 #pragma unroll
     for (int s = 0; s < NSLOT; ++s)
-      if (ok >> s & 1) m = fmaxf(m, v[s]);
-    m = warp_max(m);
+      if (ok >> s & 1) mk = max(mk, order_key(v[s]));
+    const float m = key_value(__reduce_max_sync(kFull, mk));
     const float ej = (lane < k) ? expf(my_key - m) : 0.0f;
     float part = 0.0f;
     if (renorm) {
@@ -192,9 +265,10 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
 // moe_aux_loss's own pass give the same bits. kAuxOne = 2^32 stands for probability 1.
 constexpr float kAuxOne = 4294967296.0f;
 
-// One token by one warp: lane l adds the fixed-point probability of experts l, l + 32, ...
+// One token by one warp, from its logits x (load_logits): lane l adds the fixed-point
+// probability of experts l, l + 32, ...
 template <int NSLOT>
-__device__ __forceinline__ void aux_token_fixed(const float* __restrict__ row, int E, int score_fn,
+__device__ __forceinline__ void aux_token_fixed(const float (&x)[NSLOT], int E, int score_fn,
                                                 uint64_t (&acc)[NSLOT]) {
   const int lane = threadIdx.x & 31;
   float v[NSLOT];
@@ -202,13 +276,13 @@ __device__ __forceinline__ void aux_token_fixed(const float* __restrict__ row, i
 #pragma unroll
   for (int s = 0; s < NSLOT; ++s) {
     const int e = s * 32 + lane;
-    float x = -FLT_MAX;
+    float xv = -FLT_MAX;
     if (e < E) {
-      x = row[e];
-      if (!isfinite(x)) x = -FLT_MAX;
+      xv = x[s];
+      if (!isfinite(xv)) xv = -FLT_MAX;
     }
-    v[s] = x;
-    m = fmaxf(m, x);
+    v[s] = xv;
+    m = fmaxf(m, xv);
   }
   float sum = 0.0f;
   if (score_fn == MOE_SCORE_SOFTMAX) {
@@ -272,7 +346,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
-  route_token<NSLOT>(logits, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx, topk_w,
+  float x[NSLOT];
+  load_logits<NSLOT>(logits, t, E, x);
+  route_token<NSLOT>(x, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx, topk_w,
                      s_score + (size_t)warp * E, st);
 }
 
@@ -529,34 +605,56 @@ __global__ void __launch_bounds__(1024) scan_small_kernel(const int32_t* __restr
 }
 
 // S1 + S2 in one cooperative launch (every block resident at once):
-//   1. block b routes the contiguous chunk of tokens [b C, (b + 1) C) (C = ceil(T / grid)),
-//      warp w the tokens w, w + 16, ... of it, with route_token (the same ids and weights,
-//      bit for bit, as route_topk_kernel), and counts its chunk's entries per expert;
-//   2. a grid barrier after the counts are published ([grid][E] in the workspace);
+//   1. block b takes the contiguous chunk of tokens [b C, (b + 1) C) (C = ceil(T / grid)),
+//      and warp w the contiguous part [bC + w W, bC + (w + 1) W) of it (W = ceil(C / warps)).
+//      Each token is routed by route_token (the same ids and weights, bit for bit, as
+//      route_topk_kernel), and each warp counts its part's entries per expert;
+//   2. the block's counts (the sum over its warps) are published ([grid][E] in the
+//      workspace), then a grid barrier;
 //   3. every block reads all blocks' counts: the totals give counts and offsets (block 0
-//      writes them), the blocks before it give its chunk's first row per expert, and warp 0
-//      walks the chunk's tokens in ascending order 32 at a time with the lane-mask ranks of
+//      writes them), the blocks before it give its chunk's first row per expert, and a
+//      prefix over its warps gives each warp's first row per expert. Every warp then walks
+//      its own tokens in ascending order, 32 at a time, with the lane-mask ranks of
 //      scan_assign_kernel. The map is the stable order by expert, then token, as before.
 // The barrier is a sense-reversing one in the workspace head (counter, flag); its waits are
 // bounded, and a block that gives up sets MOE_ERR_TIMEOUT and writes no map entries.
 constexpr int kFusedWarps = 16;
 constexpr int kFusedMaxBlocks = kFusedMaxRouteBlocks;
+// Above this many counts ([grid][E]) the totals take the two-level form in phase 3.
+constexpr int64_t kFusedOneLevelMax = 8192;
+
+// The barrier's words, each on its own 128-byte line: kBarGroups group counters, the top
+// counter, then the flag. Block b arrives on group b % kBarGroups; the last arrival of a group
+// arrives on the top counter, and the last of those flips the flag. Spreading the arrivals
+// keeps them from queueing on one address behind the others and the flag's readers.
+constexpr int kBarLine = 32, kBarGroups = 16;
+static_assert((kBarGroups + 2) * kBarLine * 4 + 128 <= kWsHead, "barrier words fit the workspace head");
 
 __device__ __forceinline__ bool fused_grid_barrier(uint32_t* bar, uint32_t nblocks, uint64_t timeout_ns,
                                                    DeviceStatus* st) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile uint32_t* flag = bar + 1;
+    uint32_t* top = bar + kBarGroups * kBarLine;
+    volatile uint32_t* flag = bar + (kBarGroups + 1) * kBarLine;
     const uint32_t f0 = *flag;  // read before arriving: the last arrival flips it
-    __threadfence();            // this block's counts are visible before its arrival
-    const uint32_t arrived = atomicAdd(&bar[0], 1u);
+    __threadfence();            // this block's results are visible before its arrival
+    const uint32_t g = blockIdx.x % kBarGroups;
+    const uint32_t members = (nblocks - g + kBarGroups - 1) / kBarGroups;  // blocks of group g
+    const uint32_t groups = min(nblocks, (uint32_t)kBarGroups);
     int ok = 1;
-    if (arrived == nblocks - 1) {
-      atomicExch(&bar[0], 0u);  // ready for the next launch
+    bool last = false;
+    if (atomicAdd(&bar[g * kBarLine], 1u) == members - 1) {
+      atomicExch(&bar[g * kBarLine], 0u);  // ready for the next barrier
       __threadfence();
-      atomicExch(&bar[1], f0 ^ 1u);
-    } else {
+      if (atomicAdd(top, 1u) == groups - 1) {
+        atomicExch(top, 0u);
+        __threadfence();
+        atomicExch(const_cast<uint32_t*>(flag), f0 ^ 1u);
+        last = true;
+      }
+    }
+    if (!last) {
       const uint64_t t0 = tc::globaltimer_ns();
       while (*flag == f0) {
         if (tc::globaltimer_ns() - t0 > timeout_ns) {
@@ -574,43 +672,55 @@ __device__ __forceinline__ bool fused_grid_barrier(uint32_t* bar, uint32_t nbloc
 }
 
 template <int NSLOT, bool AUX>
-__global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
+__global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_fused_kernel(
     const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G, int g_keep,
     int group_score, float rho, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
     int32_t* __restrict__ tok_row, int32_t* __restrict__ blockcnt, uint32_t* bar, uint64_t timeout_ns,
     DeviceStatus* st, uint64_t* __restrict__ auxp, float aux_alpha, float* __restrict__ aux_loss) {
   extern __shared__ int32_t fsm[];
-  const bool grouped = G > 1 && g_keep < G;
-  int32_t* hist = fsm;                                         // [E] this chunk's entries
-  int32_t* base = fsm + E;                                     // [E] the chunk's next row
-  uint32_t* mask = reinterpret_cast<uint32_t*>(fsm + 2 * E);   // [E]
-  float* s_score = reinterpret_cast<float*>(fsm + 3 * E);      // [warps][E] (group-limited)
-  unsigned long long* asum = reinterpret_cast<unsigned long long*>(  // [E] the chunk's aux sums (AUX)
-      fsm + ((3 * E + (grouped ? kFusedWarps * E : 0) + 1) & ~1));
+  // shared memory (fused_smem_ints on the host gives the same size):
+  int32_t* wcnt = fsm;                                                  // [warps][E] counts, then rows
+  uint32_t* mask = reinterpret_cast<uint32_t*>(fsm + kFusedWarps * E);  // [warps][E] lane masks
+  int32_t* tot_s = fsm + 2 * kFusedWarps * E;                           // [E] totals
+  int32_t* base = tot_s + E;                                            // [E] the chunk's first rows
+  float* s_score = reinterpret_cast<float*>(base + E);                  // [warps][E] (group scores)
+  const bool group_smem = G > 1 && g_keep < G && E != 32 * G;           // route_token's smem path
+  unsigned long long* asum = reinterpret_cast<unsigned long long*>(     // [E] the chunk's aux sums
+      fsm + ((2 * kFusedWarps * E + 2 * E + (group_smem ? kFusedWarps * E : 0) + 1) & ~1));
   __shared__ int32_t warp_tot[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = (T + (int)gridDim.x - 1) / (int)gridDim.x;
   const int t0 = (int)blockIdx.x * C, t1 = min(T, t0 + C);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    hist[e] = 0;
-    mask[e] = 0;
-    if constexpr (AUX) asum[e] = 0;
+  const int W = (C + kFusedWarps - 1) / kFusedWarps;
+  const int w0 = min(t1, t0 + warp * W), w1 = min(t1, w0 + W);
+  for (int i = threadIdx.x; i < kFusedWarps * E; i += blockDim.x) {
+    wcnt[i] = 0;
+    mask[i] = 0;
   }
+  if constexpr (AUX)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) asum[e] = 0;
   __syncthreads();
-  // ---- 1. route the chunk; count its entries per expert (and, with auxp, add up its tokens'
-  // fixed-point probabilities for the auxiliary loss)
+  // ---- 1. route the warp's tokens; count their entries per expert (and, with auxp, add up
+  // their fixed-point probabilities for the auxiliary loss)
+  int32_t* my_cnt = wcnt + warp * E;
   uint64_t aacc[NSLOT];
 #pragma unroll
   for (int s = 0; s < NSLOT; ++s) aacc[s] = 0;
-  for (int t = t0 + warp; t < t1; t += kFusedWarps) {
-    int my = route_token<NSLOT>(logits, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx,
-                                topk_w, s_score + (size_t)warp * E, st);
+  float xn[NSLOT];  // the next token's logits, loaded while this one is routed
+  if (w0 < w1) load_logits<NSLOT>(logits, w0, E, xn);
+  for (int t = w0; t < w1; ++t) {
+    float x[NSLOT];
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s) x[s] = xn[s];
+    if (t + 1 < w1) load_logits<NSLOT>(logits, t + 1, E, xn);
+    int my = route_token<NSLOT>(x, t, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx, topk_w,
+                                s_score + (size_t)warp * E, st);
     if (lane < k) {
       if (my < 0 || my >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); my = 0; }  // as the scan passes
-      atomicAdd(&hist[my], 1);  // a count: the order of the adds does not show
+      atomicAdd(&my_cnt[my], 1);
     }
-    if constexpr (AUX) aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, aacc);
+    if constexpr (AUX) aux_token_fixed<NSLOT>(x, E, score_fn, aacc);
   }
   if constexpr (AUX) {
 #pragma unroll
@@ -618,62 +728,173 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
       if (aacc[s]) atomicAdd(&asum[s * 32 + lane], (unsigned long long)aacc[s]);  // integers: any order
   }
   __syncthreads();
+  // the counts as [grid][E] (one level), or as [E][grid] (two levels: each expert's column
+  // contiguous for the warp that scans it); the aux sums likewise
+  const int nb = (int)gridDim.x, me = (int)blockIdx.x;
+  const bool two_level = (int64_t)nb * E > kFusedOneLevelMax;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    blockcnt[(int64_t)blockIdx.x * E + e] = hist[e];
-    if constexpr (AUX) auxp[(int64_t)blockIdx.x * E + e] = asum[e];
+    int32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kFusedWarps; ++w) c += wcnt[w * E + e];
+    const int64_t at = two_level ? (int64_t)e * nb + me : (int64_t)me * E + e;
+    blockcnt[at] = c;
+    if constexpr (AUX) auxp[at] = asum[e];
   }
-  // ---- 2. every block's counts are published
-  if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
-    // the map stays in bounds for the launches that read it: no routed rows, and this
-    // chunk's entries pointing at row 0 (the status word reports the failure)
+  // A block whose barrier wait ran out leaves the map in bounds for the launches that read
+  // it: no routed rows, and its chunk's entries pointing at row 0 (the status word reports
+  // the failure).
+  auto give_up = [&]() {
     for (int i = t0 * k + (int)threadIdx.x; i < t1 * k; i += blockDim.x) tok_row[i] = 0;
     if (blockIdx.x == 0)
       for (int i = threadIdx.x; i <= E; i += blockDim.x) {
         offsets[i] = 0;
         if (i < E) counts[i] = 0;
       }
+  };
+  // ---- 2. every block's counts are published
+  if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
+    give_up();
     return;
   }
-  // ---- 3. totals, offsets and this chunk's first row per expert (E <= blockDim). P
-  // consecutive threads per expert (a power of two) each add every P-th block's count.
-  {
-    int P = 1;
-    while (P < 32 && 2 * P * E <= (int)blockDim.x) P *= 2;
-    const int ex = threadIdx.x / P, q = threadIdx.x % P;
-    const bool aux_here = AUX && blockIdx.x == 0;  // block 0 also forms the aux loss
-    int32_t tot = 0, before = 0;
-    unsigned long long S = 0;
-    if (ex < E) {
-#pragma unroll 4
-      for (int b = q; b < (int)gridDim.x; b += P) {
-        const int32_t c = __ldcg(blockcnt + (int64_t)b * E + ex);
-        tot += c;
-        if (b < (int)blockIdx.x) before += c;
-        if (aux_here) S += __ldcg(reinterpret_cast<const unsigned long long*>(auxp) + (int64_t)b * E + ex);
+  // ---- 3. totals and this chunk's first row per expert: the sum over all blocks' counts,
+  // and over the blocks before this one (block 0 also adds up the aux sums).
+  if (two_level) {
+    // Two levels, so that the counts are read about once rather than once per block:
+    // (a) a warp per expert column (block c % grid, warp c / grid) turns it, in place, into
+    // the exclusive prefix over the blocks, and writes the column's total to counts (and its
+    // aux sum to the column's first slot); (b) after a second barrier each block reads its
+    // own prefixes and the totals.
+    for (int ex = warp * nb + me; ex < E; ex += nb * kFusedWarps) {
+      int32_t* col = blockcnt + (int64_t)ex * nb;
+      int32_t cv[kFusedMaxBlocks / 32];
+      int32_t sum = 0;  // over the blocks of the passes before
+      unsigned long long sa = 0;
+#pragma unroll
+      for (int i = 0; i < kFusedMaxBlocks / 32; ++i) {  // block i * 32 + lane: coalesced
+        const int bb = i * 32 + lane;
+        cv[i] = bb < nb ? __ldcg(col + bb) : 0;
+        if constexpr (AUX)
+          if (bb < nb) sa += __ldcg(reinterpret_cast<const unsigned long long*>(auxp) + (int64_t)ex * nb + bb);
+      }
+#pragma unroll
+      for (int i = 0; i < kFusedMaxBlocks / 32; ++i) {
+        if (i * 32 >= nb) break;
+        int32_t inc = cv[i];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int32_t o = __shfl_up_sync(kFull, inc, off);
+          if (lane >= off) inc += o;
+        }
+        const int bb = i * 32 + lane;
+        if (bb < nb) col[bb] = sum + inc - cv[i];
+        sum += __shfl_sync(kFull, inc, 31);
+      }
+      if (lane == 0) counts[ex] = sum;
+      if constexpr (AUX) {
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sa += __shfl_xor_sync(kFull, sa, off);
+        if (lane == 0) auxp[(int64_t)ex * nb] = sa;
       }
     }
-    for (int off = 1; off < P; off <<= 1) {  // within aligned groups of P lanes
-      tot += __shfl_xor_sync(kFull, tot, off);
-      before += __shfl_xor_sync(kFull, before, off);
-      if (aux_here) S += __shfl_xor_sync(kFull, S, off);
+    if (!fused_grid_barrier(bar, gridDim.x, timeout_ns, st)) {
+      give_up();
+      return;
+    }
+    unsigned __int128 v128 = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int32_t c = __ldcg(counts + e);
+      tot_s[e] = c;
+      base[e] = __ldcg(blockcnt + (int64_t)e * nb + me);
+      if (AUX && me == 0) v128 += (unsigned __int128)(uint32_t)c * (uint64_t)__ldcg(auxp + (int64_t)e * nb);
+    }
+    if constexpr (AUX) {
+      __shared__ unsigned __int128 red2[32];
+      if (me == 0) {
+        const unsigned __int128 v = block_sum_u128(v128, red2);
+        if (threadIdx.x == 0) *aux_loss = aux_loss_from(v, aux_alpha, E, T, k);
+      }
+    }
+    __syncthreads();
+  } else {
+    const bool aux_here = AUX && blockIdx.x == 0;
+    unsigned __int128 v128 = 0;
+    if ((E & 3) == 0) {
+      // P consecutive threads (a power of two) per 4 experts, 16-byte loads of every P-th
+      // block's counts, then a sum over the P lanes
+      const int NQ = E >> 2;
+      int P = 1;
+      while (P < 32 && 2 * P * NQ <= (int)blockDim.x) P *= 2;
+      const int q = threadIdx.x / P, ph = threadIdx.x % P;
+      int32_t tt[4] = {0, 0, 0, 0}, bf[4] = {0, 0, 0, 0};
+      unsigned long long S[4] = {0, 0, 0, 0};
+      if (q < NQ) {
+#pragma unroll 8
+        for (int bb = ph; bb < nb; bb += P) {
+          const int4 c = __ldcg(reinterpret_cast<const int4*>(blockcnt + (int64_t)bb * E) + q);
+          tt[0] += c.x; tt[1] += c.y; tt[2] += c.z; tt[3] += c.w;
+          if (bb < me) { bf[0] += c.x; bf[1] += c.y; bf[2] += c.z; bf[3] += c.w; }
+          if (aux_here) {
+            const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(auxp + (int64_t)bb * E + 4 * q);
+            const ulonglong2 u0 = __ldcg(a2), u1 = __ldcg(a2 + 1);
+            S[0] += u0.x; S[1] += u0.y; S[2] += u1.x; S[3] += u1.y;
+          }
+        }
+      }
+      for (int off = 1; off < P; off <<= 1) {  // within aligned groups of P lanes
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tt[i] += __shfl_xor_sync(kFull, tt[i], off);
+          bf[i] += __shfl_xor_sync(kFull, bf[i], off);
+          if (aux_here) S[i] += __shfl_xor_sync(kFull, S[i], off);
+        }
+      }
+      if (q < NQ && ph == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tot_s[4 * q + i] = tt[i];
+          base[4 * q + i] = bf[i];
+          if (aux_here) v128 += (unsigned __int128)(uint32_t)tt[i] * (uint64_t)S[i];
+        }
+      }
+    } else {
+      // P consecutive threads (a power of two) per expert, each adding every P-th block's count
+      int P = 1;
+      while (P < 32 && 2 * P * E <= (int)blockDim.x) P *= 2;
+      const int ex = threadIdx.x / P, q = threadIdx.x % P;
+      int32_t tot = 0, before = 0;
+      unsigned long long S = 0;
+      if (ex < E) {
+#pragma unroll 4
+        for (int bb = q; bb < nb; bb += P) {
+          const int32_t c = __ldcg(blockcnt + (int64_t)bb * E + ex);
+          tot += c;
+          if (bb < me) before += c;
+          if (aux_here) S += __ldcg(reinterpret_cast<const unsigned long long*>(auxp) + (int64_t)bb * E + ex);
+        }
+      }
+      for (int off = 1; off < P; off <<= 1) {
+        tot += __shfl_xor_sync(kFull, tot, off);
+        before += __shfl_xor_sync(kFull, before, off);
+        if (aux_here) S += __shfl_xor_sync(kFull, S, off);
+      }
+      if (ex < E && q == 0) {
+        tot_s[ex] = tot;
+        base[ex] = before;
+        if (aux_here) v128 = (unsigned __int128)(uint32_t)tot * (uint64_t)S;
+      }
     }
     if constexpr (AUX) {
       __shared__ unsigned __int128 red128[32];
       if (aux_here) {
-      const unsigned __int128 v = block_sum_u128(
-          (ex < E && q == 0) ? (unsigned __int128)(uint32_t)tot * (uint64_t)S : (unsigned __int128)0, red128);
-      if (threadIdx.x == 0) *aux_loss = aux_loss_from(v, aux_alpha, E, T, k);
+        const unsigned __int128 v = block_sum_u128(v128, red128);
+        if (threadIdx.x == 0) *aux_loss = aux_loss_from(v, aux_alpha, E, T, k);
       }
-    }
-    __syncthreads();  // hist and base are free: the counts were published, nothing read them since
-    if (ex < E && q == 0) {
-      hist[ex] = tot;
-      base[ex] = before;
     }
     __syncthreads();
   }
+  // offsets: an exclusive scan of the totals over the experts (E <= blockDim)
   const int e = threadIdx.x;
-  const int32_t tot = e < E ? hist[e] : 0, before = e < E ? base[e] : 0;
+  const int32_t tot = e < E ? tot_s[e] : 0;
   int32_t inc = tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -695,7 +916,13 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
   __syncthreads();
   const int32_t excl = warp_tot[warp] + inc - tot;
   if (e < E) {
-    base[e] = excl + before;
+    int32_t run = excl + base[e];  // the chunk's first row for expert e, then each warp's
+#pragma unroll
+    for (int w = 0; w < kFusedWarps; ++w) {
+      const int32_t c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
     if (blockIdx.x == 0) {
       counts[e] = tot;
       offsets[e] = excl;
@@ -703,25 +930,26 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     }
   }
   __syncthreads();
-  if (warp != 0) return;
-  // ---- the chunk's rows, tokens in ascending order (the ids were written by this block)
+  // ---- the warp's rows, its tokens in ascending order (their ids were written by this warp)
+  int32_t* wrow = wcnt + warp * E;
+  uint32_t* wmask = mask + warp * E;
   const int64_t R = (int64_t)T * k;
   const uint32_t below = (1u << lane) - 1u;
-  for (int tb = t0; tb < t1; tb += 32) {
+  for (int tb = w0; tb < w1; tb += 32) {
     const int t = tb + lane;
-    const bool valid = t < t1;
+    const bool valid = t < w1;
     const int32_t* ids = topk_idx + (int64_t)t * k;
     auto id_of = [&](int j) {
       const int ej = ids[j];
       return (ej < 0 || ej >= E) ? 0 : ej;  // counted for expert 0 above (status set)
     };
     if (valid)
-      for (int j = 0; j < k; ++j) atomicOr(&mask[id_of(j)], 1u << lane);
+      for (int j = 0; j < k; ++j) atomicOr(&wmask[id_of(j)], 1u << lane);
     __syncwarp();
     if (valid)
       for (int j = 0; j < k; ++j) {
         const int ej = id_of(j);
-        const int64_t r = base[ej] + __popc(mask[ej] & below);
+        const int64_t r = wrow[ej] + __popc(wmask[ej] & below);
         if (r >= 0 && r < R) {
           row_token[r] = t;
           tok_row[(int64_t)t * k + j] = (int32_t)r;
@@ -733,10 +961,10 @@ __global__ void __launch_bounds__(32 * kFusedWarps) route_fused_kernel(
     if (valid)
       for (int j = 0; j < k; ++j) {
         const int ej = id_of(j);
-        const uint32_t m = mask[ej];
+        const uint32_t m = wmask[ej];
         if (m && 31 - __clz(m) == lane) {  // the highest lane closes expert ej's batch
-          base[ej] += __popc(m);
-          mask[ej] = 0;
+          wrow[ej] += __popc(m);
+          wmask[ej] = 0;
         }
       }
     __syncwarp();
@@ -931,7 +1159,9 @@ __global__ void __launch_bounds__(256) aux_pbar_kernel(const float* __restrict__
   for (int i = 0; i < 16; ++i) {
     const int t = blockIdx.x * 128 + warp * 16 + i;
     if (t >= T) break;
-    aux_token_fixed<NSLOT>(logits + (int64_t)t * E, E, score_fn, acc);
+    float x[NSLOT];
+    load_logits<NSLOT>(logits, t, E, x);
+    aux_token_fixed<NSLOT>(x, E, score_fn, acc);
   }
 #pragma unroll
   for (int s = 0; s < NSLOT; ++s)
@@ -1076,10 +1306,12 @@ FusedPlan fused_plan(const moe_config_t& c) {
   f.kern = fused_kernel_for<false>(nslot);
   f.kern_aux = fused_kernel_for<true>(nslot);
   if (!f.kern || !f.kern_aux) return f;
-  const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
-  // hist, base, mask [E] ints and the group scores [warps][E] floats; the AUX instance adds
-  // the aux sums [E] 64-bit integers at an 8-byte boundary
-  const size_t ints = (size_t)((3 * c.E + (grouped ? kFusedWarps * c.E : 0) + 1) & ~1);
+  const bool group_smem = c.n_groups > 1 && c.topk_groups < c.n_groups && c.E != 32 * c.n_groups;
+  // per-warp counts and lane masks [warps][E], totals and first rows [E] ints, and the group
+  // scores [warps][E] floats where route_token stages them; the AUX instance adds the aux
+  // sums [E] 64-bit integers at an 8-byte boundary
+  const size_t ints =
+      (size_t)((2 * kFusedWarps * c.E + 2 * c.E + (group_smem ? kFusedWarps * c.E : 0) + 1) & ~1);
   f.smem = ints * sizeof(int32_t);
   f.smem_aux = f.smem + (size_t)c.E * sizeof(uint64_t);
   static int sms = 0;
@@ -1091,26 +1323,24 @@ FusedPlan fused_plan(const moe_config_t& c) {
   }
   const int per_sm = std::min(fused_per_sm(f.kern, f.smem), fused_per_sm(f.kern_aux, f.smem_aux));
   if (per_sm <= 0) return f;
-  // every block resident at once (the grid barrier), at most one block per 16 tokens, and
-  // grid * E <= 32768: after the barrier each block reads all blocks' counts
+  // every block resident at once (the grid barrier), and at most one block per 16 tokens
   f.grid = std::max<int64_t>(
-      1, std::min<int64_t>(std::min<int64_t>(std::min<int64_t>((int64_t)per_sm * sms, kFusedMaxBlocks),
-                                             ceil_div(c.T, kFusedWarps)),
-                           32768 / c.E));
+      1, std::min<int64_t>(std::min<int64_t>((int64_t)per_sm * sms, kFusedMaxBlocks), ceil_div(c.T, kFusedWarps)));
   return f;
 }
 
 }  // namespace
 
-// The fused launch where its top-k phase stays short: a warp routes its block's chunk of
-// tokens one after another, at a cost per token that grows with E / 32 (the slots a lane
-// holds), so the chunk times the slots is kept to at most 256. Longer chunks (e.g. the
-// DeepSeek-V3 shape's 256 grouped experts) keep the top-k and scan passes.
+// The fused launch where its top-k phase stays short: a warp routes its part of the block's
+// chunk one token after another, at a cost per token that grows with E / 32 (the slots a
+// lane holds), so the chunk times the slots is kept to at most 1024 (e.g. 108 tokens a block
+// of 256 grouped experts at T = 32768). Longer chunks keep the top-k launch, one warp per
+// token, and the scan passes.
 bool route_fused_supported(const moe_config_t& c) {
   if (c.T <= 0 || c.E > 32 * kFusedWarps || c.k > 32) return false;
   const FusedPlan f = fused_plan(c);
   if (f.grid <= 0) return false;
-  return ceil_div(c.T, f.grid) * ceil_div(c.E, 32) <= 256;
+  return ceil_div(c.T, f.grid) * ceil_div(c.E, 32) <= 1024;
 }
 
 cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32_t* topk_idx, float* topk_w,
