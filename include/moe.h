@@ -173,7 +173,8 @@ moe_status_t moe_router_logits(const moe_config_t* cfg, const void* x, const voi
  * A non-finite logit sets MOE_ERR_DEVICE_BAD_INPUT in the status word.
  * One cooperative launch (every block resident at once) routes contiguous token chunks,
  * publishes their per-expert counts in the workspace and, after a grid barrier kept in the
- * workspace head, writes the map. The barrier's wait is bounded: if it gives up,
+ * workspace head (and, with more than 8192 per-block counts, a scan of each expert's counts
+ * and a second barrier), writes the map. A barrier's wait is bounded: if it gives up,
  * MOE_ERR_TIMEOUT is set and the map is left empty (counts and offsets zero, tok_row 0). */
 moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* topk_idx,
                        float* topk_w, int32_t* counts, int32_t* offsets, int32_t* row_token,
@@ -182,7 +183,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* to
 /* The number of kernel launches moe_route makes for this configuration (0 when T = 0): 1
  * for the cooperative launch, else the top-k launch and the scan (one launch up to 512
  * tokens, else three). The cooperative launch is taken where a block's token chunk times
- * ceil(E / 32) is at most 256, which depends on the device's occupancy for the kernel
+ * ceil(E / 32) is at most 1024, which depends on the device's occupancy for the kernel
  * (queried here on first use of a shape). Launches nothing. */
 moe_status_t moe_route_launch_count(const moe_config_t* cfg, int32_t* launches);
 

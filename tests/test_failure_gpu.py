@@ -40,9 +40,10 @@ def test_bounded_wait_rejects_bad_limits():
 
 
 def test_routing_barrier_wait_gives_up_with_a_safe_map():
-    """The single-launch routing's grid barrier lives in the workspace head (counter at word 4,
-    flag at word 5). A counter left at a value no arrival can complete (here 7, for a grid of
-    one block) makes the barrier's wait run out after its 2 s limit: the call reports
+    """The single-launch routing's grid barrier lives in the workspace head (its counter at
+    byte 128, word 32; its flag 128 bytes later). A counter left at a value no arrival can
+    complete (here 7, for a grid of one block) makes the barrier's wait run out after its
+    2 s limit: the call reports
     MOE_ERR_TIMEOUT and leaves a map every later launch can read in bounds (no routed rows,
     tok_row all 0). A fresh moe_workspace_init clears the head and routing works again."""
     import oracle
@@ -51,7 +52,7 @@ def test_routing_barrier_wait_gives_up_with_a_safe_map():
     assert moe.moe_route_launch_count(b["cfg"]) == 1
     l = synth.synthetic_logits(3, 16, 8)
     moe.moe_workspace_init(b["ws"])
-    b["ws"][4] = 7
+    b["ws"][32] = 7
     b["counts"].fill_(-1)
     b["offsets"].fill_(-1)
     b["tok_row"].fill_(-1)

@@ -12,7 +12,8 @@ namespace moe {
 
 // ---------------------------------------------------------------------------------------
 // Workspace layout. The head (4 KB) holds the device status word and, from byte 128, the
-// single-launch routing's grid barrier; the routing scan's per-block expert counts follow.
+// single-launch routing's grid barrier (counter and flag on separate 128-byte lines); the
+// routing scan's per-block expert counts follow.
 // moe_forward's intermediates come after that.
 // ---------------------------------------------------------------------------------------
 constexpr size_t kWsHead = 4096;

@@ -623,38 +623,26 @@ constexpr int kFusedMaxBlocks = kFusedMaxRouteBlocks;
 // Above this many counts ([grid][E]) the totals take the two-level form in phase 3.
 constexpr int64_t kFusedOneLevelMax = 8192;
 
-// The barrier's words, each on its own 128-byte line: kBarGroups group counters, the top
-// counter, then the flag. Block b arrives on group b % kBarGroups; the last arrival of a group
-// arrives on the top counter, and the last of those flips the flag. Spreading the arrivals
-// keeps them from queueing on one address behind the others and the flag's readers.
-constexpr int kBarLine = 32, kBarGroups = 16;
-static_assert((kBarGroups + 2) * kBarLine * 4 + 128 <= kWsHead, "barrier words fit the workspace head");
+// The barrier's two words, each on its own 128-byte line: the arrival counter, then the flag
+// the last arrival flips.
+constexpr int kBarLine = 32;
+static_assert(2 * kBarLine * 4 + 128 <= kWsHead, "barrier words fit the workspace head");
 
 __device__ __forceinline__ bool fused_grid_barrier(uint32_t* bar, uint32_t nblocks, uint64_t timeout_ns,
                                                    DeviceStatus* st) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t* top = bar + kBarGroups * kBarLine;
-    volatile uint32_t* flag = bar + (kBarGroups + 1) * kBarLine;
+    volatile uint32_t* flag = bar + kBarLine;
     const uint32_t f0 = *flag;  // read before arriving: the last arrival flips it
     __threadfence();            // this block's results are visible before its arrival
-    const uint32_t g = blockIdx.x % kBarGroups;
-    const uint32_t members = (nblocks - g + kBarGroups - 1) / kBarGroups;  // blocks of group g
-    const uint32_t groups = min(nblocks, (uint32_t)kBarGroups);
+    const uint32_t arrived = atomicAdd(&bar[0], 1u);
     int ok = 1;
-    bool last = false;
-    if (atomicAdd(&bar[g * kBarLine], 1u) == members - 1) {
-      atomicExch(&bar[g * kBarLine], 0u);  // ready for the next barrier
+    if (arrived == nblocks - 1) {
+      atomicExch(&bar[0], 0u);  // ready for the next barrier
       __threadfence();
-      if (atomicAdd(top, 1u) == groups - 1) {
-        atomicExch(top, 0u);
-        __threadfence();
-        atomicExch(const_cast<uint32_t*>(flag), f0 ^ 1u);
-        last = true;
-      }
-    }
-    if (!last) {
+      atomicExch(const_cast<uint32_t*>(flag), f0 ^ 1u);
+    } else {
       const uint64_t t0 = tc::globaltimer_ns();
       while (*flag == f0) {
         if (tc::globaltimer_ns() - t0 > timeout_ns) {
