@@ -98,6 +98,7 @@ GEMM_TRAFFIC = {
     "dsv3_bf16": (17.67e9 + 0.29932e9 + 7.89e9 + 1.02e9, _SRC),
     "imbalanced_bf16": (1.45e9 + 0.19702e9 + 0.57717e9 + 0.51493e9, _SRC),
     "dsv3_fp8": (13.39e9 + 0.66015e9 + 4.96e9 + 4.20e9, _SRC),
+    "dsv3_mxfp8": (13.618e9 + 0.62394e9 + 5.149e9 + 4.2014e9, _SRC),
     "tiny_fp32": (2.379e6 + 1.584e6, _SRC),
 }
 

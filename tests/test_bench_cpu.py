@@ -34,7 +34,7 @@ def test_tensor_fraction_and_dram_rate_of_the_deepseek_shape():
 
 
 def test_no_dram_rate_without_recorded_traffic():
-    w = synth.WORKLOADS["dsv3_mxfp8"]  # no ncu traffic on record for this layer
+    w = synth.scaled(synth.WORKLOADS["dsv3_mxfp8"], T=4096)  # no ncu traffic on record for it
     r = bench.gemm_roofline(Ctx(), w, 10.0, bench.algorithmic(w))
     assert r["traffic"] is None and "dram_gbs" not in r
 
