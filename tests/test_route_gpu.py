@@ -38,6 +38,8 @@ CASES = [
     rcase("e33_ragged", 333, 33, 5),
     rcase("one_token", 1, 64, 8, G, 1, 8, 4),
     rcase("e512_long", 20000, 512, 8, G, 1, 16, 8),
+    # more than 8192 per-block counts with E not a multiple of 4: the two-level count scan
+    rcase("e33_long", 30000, 33, 5),
 ]
 
 
