@@ -257,6 +257,145 @@ __device__ __forceinline__ int route_token(const float (&x)[NSLOT], int t, int E
   return my_idx;
 }
 
+// ---- S1 for four tokens a warp (E of 64, 128 or 256, k <= 8, no group limit or 8 groups)
+// Lane j of 8-lane segment g holds experts [j M, (j + 1) M) of token t + g (M = E / 8; with 8
+// groups, group j). One pass over its experts keeps the lane's best 8 in (logit, index)
+// order, packed as (order_key << 32 | ~index) so that a larger value is a better expert,
+// and with group-limited routing the two largest sigmoid scores of its group. Three
+// butterfly steps over the segment then merge the lanes' lists (a bitonic merge of two
+// descending lists of 8 keeps their best 8), after which every lane of the segment holds
+// the token's best 8 and lane j takes the j-th. No reduction across the 32 lanes per
+// selected expert, and four tokens share each instruction: the warp-per-token form spends
+// most of its instruction slots on those reductions.
+__host__ __device__ inline bool route_sub8(int E, int k, int G, int g_keep) {
+  return (E == 64 || E == 128 || E == 256) && k <= 8 && (!(G > 1 && g_keep < G) || G == 8);
+}
+
+// A bitonic sequence of 8 sorted descending (half-cleaners of width 4, 2, 1).
+__device__ __forceinline__ void bitonic8_desc(uint64_t (&c)[8]) {
+#pragma unroll
+  for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & d) == 0 && c[i + d] > c[i]) {
+        const uint64_t tmp = c[i];
+        c[i] = c[i + d];
+        c[i + d] = tmp;
+      }
+}
+
+// Sum over the lane's 8-lane segment (a butterfly: every lane gets the same bits).
+__device__ __forceinline__ float seg8_sum(float v) {
+  v += __shfl_xor_sync(kFull, v, 1);
+  v += __shfl_xor_sync(kFull, v, 2);
+  v += __shfl_xor_sync(kFull, v, 4);
+  return v;
+}
+
+// Routes token t (its segment's; `active` false past the warp's tokens) and returns, in
+// lane j < k of the segment, the token's j-th expert. logits 16-byte aligned.
+template <int M>
+__device__ __forceinline__ int route_tokens8(const float* __restrict__ logits, int t, bool active, int E, int k,
+                                             int score_fn, int renorm, int G, int g_keep, int group_score, float rho,
+                                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                             DeviceStatus* st) {
+  const int lane = threadIdx.x & 31, j = lane & 7;
+  const bool grouped = G > 1 && g_keep < G;
+  const float4* row = reinterpret_cast<const float4*>(logits + (int64_t)t * E + j * M);
+  uint64_t top[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) top[i] = 0ull;
+  uint32_t all_max = 0u;      // the largest key of the lane's experts (the softmax's max)
+  uint32_t s1 = 0u, s2 = 0u;  // the two largest sigmoid scores of the lane's group, as bits
+  bool bad = false;
+  if (active) {
+#pragma unroll
+    for (int c = 0; c < M / 4; ++c) {
+      const float4 q = row[c];
+      const float xs[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float x = xs[u];
+        if (!isfinite(x)) { bad = true; x = -FLT_MAX; }
+        const uint32_t key = order_key(x);
+        all_max = max(all_max, key);
+        if (grouped) {  // the multiset's two largest: a tie with the largest is the second
+          const uint32_t b = __float_as_uint(det_sigmoid(x));
+          s2 = max(s2, min(s1, b));
+          s1 = max(s1, b);
+        }
+        const uint64_t pk = (uint64_t)key << 32 | (0xffffffffu - (uint32_t)(j * M + 4 * c + u));
+        if (pk > top[7]) {  // insert, keeping the list descending
+          top[7] = pk;
+#pragma unroll
+          for (int i = 7; i > 0; --i)
+            if (top[i] > top[i - 1]) {
+              const uint64_t tmp = top[i];
+              top[i] = top[i - 1];
+              top[i - 1] = tmp;
+            }
+        }
+      }
+    }
+  }
+  if (bad) set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t);
+  if (grouped) {  // 8 groups: the g_keep best in (key, index) order keep their candidates
+    const float gk = group_score == MOE_GROUP_SCORE_TOP2_SUM ? __fadd_rn(__uint_as_float(s1), __uint_as_float(s2))
+                                                             : __uint_as_float(s1);
+    int rank = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rank += better(__shfl_sync(kFull, gk, (lane & ~7) | i), i, gk, j) ? 1 : 0;
+    if (rank >= g_keep)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) top[i] = 0ull;
+  }
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) {
+    uint64_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(kFull, (unsigned long long)top[i], off);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) top[i] = max(top[i], o[7 - i]);
+    bitonic8_desc(top);
+  }
+  uint64_t pj = 0ull;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i == j) pj = top[i];
+  const int my_idx = (int)(0xffffffffu - (uint32_t)pj);  // -1 where no candidate is left
+  const float my_key = key_value((uint32_t)(pj >> 32));
+  float w;
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    uint32_t mk = all_max;
+    mk = max(mk, __shfl_xor_sync(kFull, mk, 1));
+    mk = max(mk, __shfl_xor_sync(kFull, mk, 2));
+    mk = max(mk, __shfl_xor_sync(kFull, mk, 4));
+    const float m = key_value(mk);
+    const float ej = (j < k) ? expf(my_key - m) : 0.0f;
+    float part = 0.0f;
+    if (renorm) {
+      part = ej;
+    } else if (active) {
+#pragma unroll
+      for (int c = 0; c < M / 4; ++c) {
+        const float4 q = row[c];
+        const float xs[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) part += expf((isfinite(xs[u]) ? xs[u] : -FLT_MAX) - m);
+      }
+    }
+    w = ej / seg8_sum(part);
+  } else {
+    const float sj = (j < k) ? det_sigmoid(my_key) : 0.0f;
+    w = sj / (renorm ? seg8_sum(sj) : 1.0f);
+  }
+  if (active && j < k) {
+    topk_idx[(int64_t)t * k + j] = my_idx;
+    topk_w[(int64_t)t * k + j] = w * rho;
+  }
+  return my_idx;
+}
+
 // ---- auxiliary load-balancing loss, summed exactly
 // Each token's probabilities (the softmax of its logits over all experts, or its sigmoid
 // scores divided by their sum; a non-finite logit counts as -FLT_MAX, as in routing) are
@@ -341,9 +480,19 @@ template <int NSLOT>
 __global__ void __launch_bounds__(256) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int score_fn, int renorm, int G,
     int g_keep, int group_score, float rho, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, DeviceStatus* st) {
+    float* __restrict__ topk_w, DeviceStatus* st, int sub8) {
   extern __shared__ float s_score[];  // [warps][E] sigmoid scores (group-limited only)
   const int warp = threadIdx.x >> 5;
+  if constexpr (NSLOT == 2 || NSLOT == 4 || NSLOT == 8) {
+    if (sub8) {  // four tokens a warp, E = 32 NSLOT
+      const int tb = (blockIdx.x * (blockDim.x >> 5) + warp) * 4;
+      if (tb >= T) return;
+      const int t = tb + ((threadIdx.x & 31) >> 3);
+      route_tokens8<4 * NSLOT>(logits, t, t < T, E, k, score_fn, renorm, G, g_keep, group_score, rho, topk_idx,
+                               topk_w, st);
+      return;
+    }
+  }
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
   float x[NSLOT];
@@ -665,7 +814,7 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
     int group_score, float rho, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
     int32_t* __restrict__ tok_row, int32_t* __restrict__ blockcnt, uint32_t* bar, uint64_t timeout_ns,
-    DeviceStatus* st, uint64_t* __restrict__ auxp, float aux_alpha, float* __restrict__ aux_loss) {
+    DeviceStatus* st, uint64_t* __restrict__ auxp, float aux_alpha, float* __restrict__ aux_loss, int sub8) {
   extern __shared__ int32_t fsm[];
   // shared memory (fused_smem_ints on the host gives the same size):
   int32_t* wcnt = fsm;                                                  // [warps][E] counts, then rows
@@ -680,7 +829,8 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = (T + (int)gridDim.x - 1) / (int)gridDim.x;
   const int t0 = (int)blockIdx.x * C, t1 = min(T, t0 + C);
-  const int W = (C + kFusedWarps - 1) / kFusedWarps;
+  // a warp's part: with four tokens a warp, a multiple of 4 tokens
+  const int W = sub8 ? 4 * ((C + 4 * kFusedWarps - 1) / (4 * kFusedWarps)) : (C + kFusedWarps - 1) / kFusedWarps;
   const int w0 = min(t1, t0 + warp * W), w1 = min(t1, w0 + W);
   for (int i = threadIdx.x; i < kFusedWarps * E; i += blockDim.x) {
     wcnt[i] = 0;
@@ -695,9 +845,32 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
   uint64_t aacc[NSLOT];
 #pragma unroll
   for (int s = 0; s < NSLOT; ++s) aacc[s] = 0;
+  bool routed = false;
+  if constexpr (NSLOT == 2 || NSLOT == 4 || NSLOT == 8) {
+    if (sub8) {  // four tokens a warp, E = 32 NSLOT
+      routed = true;
+      for (int tb = w0; tb < w1; tb += 4) {
+        const int t = tb + (lane >> 3);
+        const bool active = t < w1;
+        int my = route_tokens8<4 * NSLOT>(logits, t, active, E, k, score_fn, renorm, G, g_keep, group_score, rho,
+                                          topk_idx, topk_w, st);
+        if (active && (lane & 7) < k) {
+          if (my < 0 || my >= E) { set_status(st, MOE_ERR_DEVICE_BAD_INPUT, t); my = 0; }  // as the scan passes
+          atomicAdd(&my_cnt[my], 1);
+        }
+        if constexpr (AUX) {
+          for (int u = 0; u < 4 && tb + u < w1; ++u) {
+            float x[NSLOT];
+            load_logits<NSLOT>(logits, tb + u, E, x);
+            aux_token_fixed<NSLOT>(x, E, score_fn, aacc);
+          }
+        }
+      }
+    }
+  }
   float xn[NSLOT];  // the next token's logits, loaded while this one is routed
-  if (w0 < w1) load_logits<NSLOT>(logits, w0, E, xn);
-  for (int t = w0; t < w1; ++t) {
+  if (!routed && w0 < w1) load_logits<NSLOT>(logits, w0, E, xn);
+  for (int t = w0; t < w1 && !routed; ++t) {
     float x[NSLOT];
 #pragma unroll
     for (int s = 0; s < NSLOT; ++s) x[s] = xn[s];
@@ -1224,20 +1397,31 @@ cudaError_t launch_router_small(const moe_config_t& c, const void* x, const void
   return cudaErrorInvalidValue;
 }
 
+namespace {
+// Four tokens a warp where the shape allows it and the logits rows are 16-byte aligned
+// (the routine reads them as float4); every launch that routes a configuration makes the
+// same choice, so the routing kernels give the same bits.
+int route_sub8_for(const moe_config_t& c, const float* logits) {
+  return route_sub8(c.E, c.k, c.n_groups, c.topk_groups) && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+}
+
+}  // namespace
+
 cudaError_t launch_route_topk(const moe_config_t& c, const float* logits, int32_t* topk_idx,
                               float* topk_w, DeviceStatus* st, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const int warps = 8;
-  const dim3 grid((unsigned)ceil_div(c.T, warps)), block(warps * 32);
+  const int sub8 = route_sub8_for(c, logits);  // four tokens a warp
+  const dim3 grid((unsigned)ceil_div(c.T, sub8 ? 4 * warps : warps)), block(warps * 32);
   const bool grouped = c.n_groups > 1 && c.topk_groups < c.n_groups;
-  const size_t smem = grouped ? (size_t)warps * c.E * sizeof(float) : 0;
+  const size_t smem = grouped && !sub8 ? (size_t)warps * c.E * sizeof(float) : 0;
   const int nslot = (int)ceil_div(c.E, 32);
 #define MOE_ROUTE_CASE(NS)                                                                  \
   if (nslot <= NS) {                                                                        \
     route_topk_kernel<NS><<<grid, block, smem, s>>>(logits, c.T, c.E, c.k, c.score_fn,      \
                                                     c.renorm, c.n_groups, c.topk_groups,    \
                                                     c.group_score, c.routed_scale, topk_idx, \
-                                                    topk_w, st);                            \
+                                                    topk_w, st, sub8);                      \
     return cudaGetLastError();                                                              \
   }
   MOE_ROUTE_CASE(1)
@@ -1339,6 +1523,7 @@ cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32
   const FusedPlan f = fused_plan(c);
   if (f.grid <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg{};
+  const int sub8 = route_sub8_for(c, logits);
   cfg.gridDim = dim3((unsigned)f.grid);
   cfg.blockDim = dim3(32 * kFusedWarps);
   cfg.dynamicSmemBytes = auxp ? f.smem_aux : f.smem;
@@ -1354,7 +1539,7 @@ cudaError_t launch_route_fused(const moe_config_t& c, const float* logits, int32
                   (void*)&c.group_score, (void*)&c.routed_scale, (void*)&topk_idx, (void*)&topk_w,
                   (void*)&counts,  (void*)&offsets,       (void*)&row_token,    (void*)&tok_row,
                   (void*)&blockcnt, (void*)&barrier,      (void*)&timeout,      (void*)&st,
-                  (void*)&auxp,    (void*)&aux_alpha,     (void*)&aux_loss};
+                  (void*)&auxp,    (void*)&aux_alpha,     (void*)&aux_loss, (void*)&sub8};
   cudaError_t e = cudaLaunchKernelExC(&cfg, auxp ? f.kern_aux : f.kern, args);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
