@@ -445,10 +445,13 @@ __device__ __forceinline__ void aux_token_fixed(const float (&x)[NSLOT], int E, 
 }
 
 // loss = alpha * E / (T k) * sum_e counts[e] * Pbar_e, Pbar_e = S_e / (2^32 T), from the exact
-// V = sum_e counts[e] * S_e (at most 2^31 * 2^63 * 512 < 2^103).
+// V = sum_e counts[e] * S_e (at most 2^31 * 2^63 * 512 < 2^103), in fp32: V over
+// T^2 k 2^32 / E, then times alpha (a few roundings, each 2^-24 relative; fp64 arithmetic is
+// slow on this part, and the loss is a float). Every path that forms the loss calls this.
 __device__ __forceinline__ float aux_loss_from(unsigned __int128 V, float alpha, int E, int T, int k) {
-  const double v = (double)(uint64_t)(V >> 64) * 18446744073709551616.0 + (double)(uint64_t)V;
-  return (float)((double)alpha * (double)E * v / (4294967296.0 * (double)T * (double)T * (double)k));
+  const float v = __fadd_rn(__fmul_rn((float)(uint64_t)(V >> 64), 18446744073709551616.0f), (float)(uint64_t)V);
+  const float d = __fmul_rn(__fmul_rn((float)T, (float)T), __fdiv_rn(__fmul_rn((float)k, 4294967296.0f), (float)E));
+  return __fmul_rn(__fdiv_rn(v, d), alpha);
 }
 
 // Sum of a 128-bit value over the warp.
@@ -979,26 +982,21 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
   } else {
     const bool aux_here = AUX && blockIdx.x == 0;
     unsigned __int128 v128 = 0;
-    if ((E & 3) == 0) {
+    if ((E & 3) == 0 && !aux_here) {
       // P consecutive threads (a power of two) per 4 experts, 16-byte loads of every P-th
-      // block's counts, then a sum over the P lanes
+      // block's counts, then a sum over the P lanes (block 0 of the aux instance, which also
+      // adds up the aux sums, takes the per-expert loop below: measured faster for it)
       const int NQ = E >> 2;
       int P = 1;
       while (P < 32 && 2 * P * NQ <= (int)blockDim.x) P *= 2;
       const int q = threadIdx.x / P, ph = threadIdx.x % P;
       int32_t tt[4] = {0, 0, 0, 0}, bf[4] = {0, 0, 0, 0};
-      unsigned long long S[4] = {0, 0, 0, 0};
       if (q < NQ) {
 #pragma unroll 8
         for (int bb = ph; bb < nb; bb += P) {
           const int4 c = __ldcg(reinterpret_cast<const int4*>(blockcnt + (int64_t)bb * E) + q);
           tt[0] += c.x; tt[1] += c.y; tt[2] += c.z; tt[3] += c.w;
           if (bb < me) { bf[0] += c.x; bf[1] += c.y; bf[2] += c.z; bf[3] += c.w; }
-          if (aux_here) {
-            const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(auxp + (int64_t)bb * E + 4 * q);
-            const ulonglong2 u0 = __ldcg(a2), u1 = __ldcg(a2 + 1);
-            S[0] += u0.x; S[1] += u0.y; S[2] += u1.x; S[3] += u1.y;
-          }
         }
       }
       for (int off = 1; off < P; off <<= 1) {  // within aligned groups of P lanes
@@ -1006,7 +1004,6 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
         for (int i = 0; i < 4; ++i) {
           tt[i] += __shfl_xor_sync(kFull, tt[i], off);
           bf[i] += __shfl_xor_sync(kFull, bf[i], off);
-          if (aux_here) S[i] += __shfl_xor_sync(kFull, S[i], off);
         }
       }
       if (q < NQ && ph == 0) {
@@ -1014,7 +1011,6 @@ __global__ void __launch_bounds__(32 * kFusedWarps, NSLOT >= 16 ? 1 : 2) route_f
         for (int i = 0; i < 4; ++i) {
           tot_s[4 * q + i] = tt[i];
           base[4 * q + i] = bf[i];
-          if (aux_here) v128 += (unsigned __int128)(uint32_t)tt[i] * (uint64_t)S[i];
         }
       }
     } else {
